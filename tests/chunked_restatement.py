@@ -1,0 +1,127 @@
+"""Chunked form of KDA restated in fp64 numpy — test-only, not part of the oracle.
+
+It spells out, step by step, the algebra the CUDA prefill path implements, so that the
+algebra itself (decay factorisation about a mid-chunk reference, zero padding of the last
+chunk, the unit-lower-triangular inverse, the state pass, and segment composition) is proven
+equal to the token loop before any kernel runs.  Steps, per (sequence, head) unit, chunk of C
+tokens, d_k x d_v state S (all fp64):
+
+  G      = inclusive cumulative sum of g within the chunk          [C, d_k]
+  r      = G_C / 2  (per key channel; the mid-chunk reference)
+  Q_r    = q * exp(G - r);  K_p = k * exp(G - r);  K_m = k * exp(r - G)
+  K_bar  = k * exp(G_C - G)
+  A      = strict_lower(diag(beta) K_p K_m^T);   P = lower_incl(Q_r K_m^T)
+  T      = (I + A)^{-1}   (16x16 diagonal blocks by the doubling product
+                           (I-N)(I+N^2)(I+N^4)(I+N^8), off-diagonal blocks by block
+                           forward substitution)
+  W      = T diag(beta) K_p;   U_bar = T diag(beta) V
+  S'     = diag(exp(r)) S
+  U      = U_bar - W S';   O = Q_r S' + P U
+  S      = diag(exp(G_C)) S + K_bar^T U
+
+The pages fix the chunkwise idea ("How Kimi K3 Engineered Its Way to the Frontier", section
+"FlashKDA steps the state once per 16 tokens": chunk-local dense matmuls, one state step per
+chunk, result equal to the token loop; reciprocal cumulative decay; the 16x16 Neumann-series
+inverse exact after three doubling rounds).  The segment composition S_out = M S_in + S~ is
+the KCP decomposition ("k3_training_and_infra_notes", section 4.1).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def block_inverse_unit_lower(A: np.ndarray, block: int = 16) -> np.ndarray:
+    """(I + A)^{-1} for strictly lower-triangular A, by 16x16 doubling + block substitution."""
+    C = A.shape[0]
+    assert C % block == 0
+    nb = C // block
+    T = np.zeros_like(A)
+    eye = np.eye(block)
+    for b in range(nb):
+        s = slice(b * block, (b + 1) * block)
+        N = A[s, s]
+        N2 = N @ N
+        N4 = N2 @ N2
+        N8 = N4 @ N4
+        T[s, s] = (eye - N) @ (eye + N2) @ (eye + N4) @ (eye + N8)
+    for I in range(1, nb):
+        si = slice(I * block, (I + 1) * block)
+        for J in range(I):
+            sj = slice(J * block, (J + 1) * block)
+            acc = np.zeros((block, block))
+            for K in range(J, I):
+                sk = slice(K * block, (K + 1) * block)
+                acc += A[si, sk] @ T[sk, sj]
+            T[si, sj] = -T[si, si] @ acc
+    return T
+
+
+def chunk_step(S, q, k, v, g, beta):
+    """One chunk (rows beyond the sequence already zero-padded).  Returns (O, S_new)."""
+    C = q.shape[0]
+    G = np.cumsum(g, axis=0)
+    GC = G[-1]
+    r = GC / 2.0
+    Q_r = q * np.exp(G - r)
+    K_p = k * np.exp(G - r)
+    K_m = k * np.exp(r - G)
+    K_bar = k * np.exp(GC - G)
+    A = np.tril(beta[:, None] * (K_p @ K_m.T), -1)
+    P = np.tril(Q_r @ K_m.T, 0)
+    T = block_inverse_unit_lower(A)
+    W = T @ (beta[:, None] * K_p)
+    U_bar = T @ (beta[:, None] * v)
+    S_r = np.exp(r)[:, None] * S
+    U = U_bar - W @ S_r
+    O = Q_r @ S_r + P @ U
+    S_new = np.exp(GC)[:, None] * S + K_bar.T @ U
+    return O, S_new
+
+
+def _chunks(L, C):
+    return [(c0, min(L, c0 + C)) for c0 in range(0, L, C)]
+
+
+def _padded(x, c0, c1, C):
+    out = np.zeros((C,) + x.shape[1:])
+    out[: c1 - c0] = x[c0:c1]
+    return out
+
+
+def unit_forward(q, k, v, g, beta, S0, C=64):
+    """Chunked forward of one unit: q,k,g [L,d_k], v [L,d_v], beta [L]."""
+    L = q.shape[0]
+    S = S0.copy()
+    O = np.zeros((L, v.shape[1]))
+    for c0, c1 in _chunks(L, C):
+        Oc, S = chunk_step(S, *(_padded(x, c0, c1, C) for x in (q, k, v, g, beta)))
+        O[c0:c1] = Oc[: c1 - c0]
+    return O, S
+
+
+def segment_transition(k, v, g, beta, C=64):
+    """Pass A of segment parallelism: from a zero incoming state, carry the augmented state
+    [S~ | M] (M starts at I, its 'values' are zero) through the segment.  Returns (M, S~)."""
+    L, dk = k.shape
+    dv = v.shape[1]
+    X = np.concatenate([np.zeros((dk, dv)), np.eye(dk)], axis=1)
+    for c0, c1 in _chunks(L, C):
+        kk, vv, gg, bb = (_padded(x, c0, c1, C) for x in (k, v, g, beta))
+        v_aug = np.concatenate([vv, np.zeros((C, dk))], axis=1)
+        _, X = chunk_step(X, np.zeros_like(kk), kk, v_aug, gg, bb)
+    return X[:, dv:], X[:, :dv]
+
+
+def unit_forward_segmented(q, k, v, g, beta, S0, seg_len, C=64):
+    """Pass A per segment, sequential combine S_in(s+1) = M_s S_in(s) + S~_s, then pass B."""
+    L = q.shape[0]
+    bounds = [(a, min(L, a + seg_len)) for a in range(0, L, seg_len)] or [(0, 0)]
+    trans = [segment_transition(k[a:b], v[a:b], g[a:b], beta[a:b], C) for a, b in bounds]
+    s_in = [S0]
+    for M, St in trans[:-1]:
+        s_in.append(M @ s_in[-1] + St)
+    O = np.zeros((L, v.shape[1]))
+    S = S0
+    for (a, b), Si in zip(bounds, s_in):
+        O[a:b], S = unit_forward(q[a:b], k[a:b], v[a:b], g[a:b], beta[a:b], Si, C)
+    return O, S
