@@ -1,0 +1,365 @@
+"""Benchmark of the KDA forward hot path on GB300.
+
+One step = one chunked prefill call over the prefill_4x8k workload (4 sequences x 8192
+tokens, 32 heads, d = 128, bf16 inputs, fp32 state) with every input resident in HBM.  The
+decode step on the decode_512x96 workload (512 sequences x 96 heads, fp32 state updated in
+place) is timed in the same run and reported under "decode".
+
+Prints ONE JSON line (rank 0).  With --impl reference the fp64 CPU oracle is timed instead,
+on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill Mtokens/s (% bf16 TC roofline); decode state-update GB/s on 1 GB300"
+D = 128
+CHUNK = 64
+BYTES_PER_TOKEN_HEAD = 4 * D * 2 + 2 + D * 2        # q, k, v, log_alpha in; beta; o out
+FLOPS_PER_TOKEN_HEAD = 8 * CHUNK * D + 6 * D * D + 2 * CHUNK * D   # dense chunk tiles
+STATE_BYTES = D * D * 4
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        p = json.load(open(path))
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kimi_delta_attention_03_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path)).get(name)
+    except Exception:
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.result = None
+        if self.proc is None:
+            return False
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                mx.append(float(row[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, row[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(nm)
+        if sm:
+            self.result = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                           "reasons": sorted(reasons), "samples": len(sm)}
+        return False
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(x, tokens: int, threads: int):
+    """Time the fp64 oracle on the first ``tokens`` tokens of sequence 0, all heads."""
+    import oracle
+    sl = lambda t: t[:tokens].cpu()
+    s0 = x["init_state"][:1].cpu() if x["init_state"] is not None else None
+    t0 = time.perf_counter()
+    oracle.recurrence(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["log_alpha"]), sl(x["beta"]),
+                      [0, tokens], state_in=s0, threads=threads)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: bounded samples of the same workload."""
+    if rank != 0:
+        return
+    from kimi_delta_attention_03_gb300 import synth
+    w = synth.workloads()["prefill_4x8k"]
+    x = synth.make_workload(w, device="cpu", lengths=[args.ref_tokens])
+    threads = cpu_cores()
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_sample(x, min(256, args.ref_tokens), threads)
+    times = [oracle_sample(x, args.ref_tokens, threads) for _ in range(args.steps)]
+    sec = sum(times) / len(times)
+    value = args.ref_tokens / sec / 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "Mtokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample_tokens": args.ref_tokens, "heads": w.heads,
+                   "d": D},
+        "cpu_baseline": {"value": value, "unit": "Mtokens/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"first {args.ref_tokens} tokens of one 8192-token "
+                                   f"sequence, all {w.heads} heads, fp64 token loop"},
+        "e2e": {"value": value, "unit": "Mtokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_device(fn, steps, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop) / steps  # ms per step
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--cpu-baseline-tokens", type=int, default=2048)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
+
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        barrier(world)
+        return
+
+    import kimi_delta_attention_03_gb300 as kda
+    from kimi_delta_attention_03_gb300 import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    hbm_peak, tc_peak, peak_kind = peaks()
+
+    # ---------------- prefill (headline) ----------------
+    w = synth.workloads()["prefill_4x8k"]
+    x = synth.make_workload(w, device=dev)
+    T, H = x["q"].shape[0], w.heads
+    out = torch.empty_like(x["q"])
+    fin = torch.empty((len(w.lengths), H, D, D), dtype=torch.float32, device=dev)
+
+    def step():
+        kda.fwd_chunked(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                        x["seqlens"], init_state=x["init_state"], out=out, final_state=fin)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    launches0 = kda.launch_count()
+    with ClockSampler(local) as clk:
+        ms = time_device(step, args.steps, stream)
+    launches = kda.launch_count() - launches0
+    barrier(world)
+    ms_max = max_over_ranks(ms, world)
+    tokens_all = T * world
+    value = tokens_all / (ms_max * 1e-3) / 1e6
+    units = len(w.lengths) * H
+    alg_bytes = T * H * BYTES_PER_TOKEN_HEAD + units * 2 * STATE_BYTES
+    alg_flops = T * H * FLOPS_PER_TOKEN_HEAD
+    achieved_gbs = alg_bytes / (ms * 1e-3) / 1e9
+    achieved_tf = alg_flops / (ms * 1e-3) / 1e12
+    t_hbm = alg_bytes / (hbm_peak * 1e9)
+    t_tc = alg_flops / (tc_peak * 1e12)
+    roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved_gbs / hbm_peak, "peak_kind": peak_kind,
+                "traffic": recorded_traffic("kda_prefill"),
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "tensor_achieved_tflops": achieved_tf, "tensor_peak_tflops": tc_peak,
+                "tensor_frac": achieved_tf / tc_peak,
+                "frac_of_roofline_time": max(t_hbm, t_tc) / (ms * 1e-3)}
+
+    # ---------------- decode ----------------
+    decode = None
+    if not args.no_decode:
+        wd = synth.workloads()["decode_512x96"]
+        dd = synth.make_decode_inputs(512, 96, torch.bfloat16, seed=wd.seed,
+                                      state_std=wd.s0_std, device=dev)
+        dout = torch.empty_like(dd["q"])
+
+        def dstep():
+            kda.decode_step(dd["q"], dd["k"], dd["v"], dd["log_alpha"], dd["beta"],
+                            dd["state"], out=dout)
+
+        for _ in range(args.warmup):
+            dstep()
+        barrier(world)
+        dms = time_device(dstep, args.steps, stream)
+        dms = max_over_ranks(dms, world)
+        dunits = 512 * 96
+        dbytes = dunits * (2 * STATE_BYTES + BYTES_PER_TOKEN_HEAD)
+        dgbs = dbytes / (dms * 1e-3) / 1e9
+        decode = {"metric": "decode state-update GB/s", "value": dgbs * world, "unit": "GB/s",
+                  "ms_per_step": dms, "workload": wd.name,
+                  "roofline": {"bound": "hbm", "achieved": dgbs, "peak": hbm_peak,
+                               "unit": "GB/s", "frac": dgbs / hbm_peak,
+                               "peak_kind": peak_kind,
+                               "traffic": recorded_traffic("kda_decode"),
+                               "algorithmic_bytes_per_launch": dbytes}}
+        del dd, dout
+
+    # ---------------- end to end (host buffers, copies inside the timed region) ------------
+    e2e = None
+    if not args.no_e2e:
+        names = ("q", "k", "v", "log_alpha", "beta")
+        host = {nm: x[nm].cpu().pin_memory() for nm in names}
+        host["init_state"] = x["init_state"].cpu().pin_memory()
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        host_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+        dev_in = {nm: torch.empty_like(x[nm]) for nm in names}
+        dev_in["init_state"] = torch.empty_like(x["init_state"])
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = host_out.numel() * host_out.element_size() + host_fin.numel() * 4
+
+        def estep():
+            for nm, t in host.items():
+                dev_in[nm].copy_(t, non_blocking=True)
+            kda.fwd_chunked(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["log_alpha"],
+                            dev_in["beta"], x["cu_seqlens"], x["seqlens"],
+                            init_state=dev_in["init_state"], out=out, final_state=fin)
+            host_out.copy_(out, non_blocking=True)
+            host_fin.copy_(fin, non_blocking=True)
+
+        for _ in range(2):
+            estep()
+        barrier(world)
+        esteps = max(3, min(args.steps, 5))
+        ems = max_over_ranks(time_device(estep, esteps, stream), world)
+        e2e = {"value": tokens_all / (ems * 1e-3) / 1e6, "unit": "Mtokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
+               "steps": esteps}
+
+    # ---------------- CPU baseline (oracle, rank 0 only, N = 1 only) ----------------
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = cpu_cores()
+        xs = synth.make_workload(w, device="cpu", lengths=[args.cpu_baseline_tokens])
+        sec = oracle_sample(xs, args.cpu_baseline_tokens, threads)
+        cpu_base = {"value": args.cpu_baseline_tokens / sec / 1e6, "unit": "Mtokens/s",
+                    "cores": threads, "kind": "oracle", "seconds": sec,
+                    "sample": f"first {args.cpu_baseline_tokens} tokens of one 8192-token "
+                              f"sequence, all {H} heads, fp64 token loop"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "Mtokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "global_batch": len(w.lengths) * world,
+                       "seq_len": w.lengths[0], "heads": H, "d_k": D, "d_v": D,
+                       "chunk": CHUNK, "state": "fp32",
+                       "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (%.2f GB read per step)" % (alg_bytes / 1e9)},
+            "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
+            "clocks": getattr(clk, "result", None), "gpu_launches": launches,
+            "decode": decode,
+        }
+        print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+if __name__ == "__main__":
+    main()

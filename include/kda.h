@@ -1,0 +1,163 @@
+/*
+ * kda.h — C ABI of the GB300 (sm_103a) Kimi Delta Attention forward library.
+ *
+ * The operation.  Each (sequence n, head h) unit keeps a d_k x d_v fp32 state S (rows are key
+ * channels) and, token by token,
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,   o_t = S_t^T q_t,
+ *
+ * with alpha_t = exp(log_alpha_t) one retention factor per key channel and beta_t a scalar
+ * write strength.  Source: "How Kimi K3 Engineered Its Way to the Frontier"
+ * (codepointer.substack.com), section "How KDA updates its state" (the report's formula and
+ * the three-line token loop of flash-linear-attention's naive.py); restated in "Kimi K3"
+ * (ai.thesatyajit.com), section "Kimi Delta Attention: constant-size memory over a million
+ * tokens".  The interface mirrors FlashKDA's forward as described there (section "FlashKDA:
+ * the equation, shipped as a kernel"): q, k, v, gate, beta, optional state in and out,
+ * variable-length batching through cumulative sequence lengths, d = 128.
+ *
+ * Conventions shared by every entry point
+ *   - Layouts are row-major and contiguous, batch folded into tokens:
+ *       q, k, log_alpha : [T_tot, H, d_k]     v, out : [T_tot, H, d_v]     beta : [T_tot, H]
+ *       states          : fp32 [N, H, d_k, d_v], row = key channel
+ *   - Element type of q, k, v, log_alpha, beta and out: bf16 (KDA_BF16) or fp32 (KDA_FP32).
+ *     log_alpha is the natural-log gate (alpha = exp(log_alpha), expected <= 0); beta is the
+ *     write strength itself (already passed through a sigmoid).  No scale is applied to q.
+ *   - Only d_k = d_v = 128 is supported.
+ *   - Ownership: the caller owns and allocates every buffer (device memory unless marked
+ *     host).  The library never allocates or frees memory and keeps no per-call state; the
+ *     only global is the sticky device status word read by kda_read_device_status().
+ *   - Every compute entry point is asynchronous on `stream` (NULL = legacy default stream).
+ *     Host-side argument checks are synchronous and return before anything is launched.
+ *   - Errors: KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED / KDA_ERR_WORKSPACE from the host
+ *     checks, KDA_ERR_CUDA when a launch fails.  Conditions found on the device (a chunk's
+ *     cumulative log-decay outside the supported range) set the sticky device status word;
+ *     the kernels never trap or abort.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without CUDA headers. */
+typedef struct CUstream_st* kda_stream_t;
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,  /* null pointer, bad size, lengths not summing to T_tot     */
+    KDA_ERR_UNSUPPORTED = -2,  /* d_k or d_v other than 128, unknown dtype                  */
+    KDA_ERR_WORKSPACE = -3,    /* workspace missing or smaller than kda_fwd_workspace_bytes */
+    KDA_ERR_CUDA = -4,         /* a CUDA launch or query failed                             */
+    KDA_ERR_TIMEOUT = -5,      /* a bounded device-side wait gave up (device status word)   */
+    KDA_ERR_DECAY_RANGE = -6   /* a chunk's cumulative log-decay left the supported range   */
+} kda_status;
+
+typedef enum kda_dtype { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
+
+/* Problem description.  host_seqlens is a HOST array of num_seqs lengths; it must equal the
+ * differences of the device cu_seqlens array.  It lets the library size grids and workspace
+ * without reading device memory. */
+typedef struct kda_desc {
+    int32_t num_seqs;            /* N >= 1                                            */
+    int32_t num_heads;           /* H >= 1                                            */
+    int64_t total_tokens;        /* T_tot = sum of host_seqlens                       */
+    int32_t d_k;                 /* must be 128                                       */
+    int32_t d_v;                 /* must be 128                                       */
+    int32_t in_dtype;            /* kda_dtype of q, k, v, log_alpha, beta and out     */
+    int32_t reserved;            /* must be 0                                         */
+    const int32_t* host_seqlens; /* host, [num_seqs], each >= 0                       */
+} kda_desc;
+
+/* How a prefill call is split into work items (host-side plan, no device access). */
+typedef struct kda_plan_info {
+    int64_t chunks;           /* 64-token chunks summed over sequences (one head)          */
+    int64_t work_items;       /* (sequence, segment) items per head                        */
+    int32_t split_sequences;  /* sequences processed as more than one segment              */
+    int32_t chunk_size;       /* tokens per chunk (64)                                     */
+    int32_t segment_chunks;   /* chunks per segment of a split sequence                    */
+    int32_t reserved;
+    size_t workspace_bytes;   /* what kda_fwd_chunked needs for this description           */
+} kda_plan_info;
+
+/*
+ * kda_fwd_plan — fill *info with the work split of a prefill call.  Host only, no CUDA call.
+ * Returns KDA_OK, KDA_ERR_INVALID_ARG or KDA_ERR_UNSUPPORTED.
+ */
+kda_status kda_fwd_plan(const kda_desc* desc, kda_plan_info* info);
+
+/*
+ * kda_fwd_workspace_bytes — bytes of device workspace kda_fwd_chunked needs for `desc`
+ * (0 when no sequence is split into segments).  Host only.  Returns 0 for an invalid desc.
+ */
+size_t kda_fwd_workspace_bytes(const kda_desc* desc);
+
+/*
+ * kda_fwd_chunked — chunked prefill over packed variable-length sequences.
+ *
+ * Computes every o_t and, optionally, the final state of every (sequence, head) unit, exactly
+ * as the token loop would, by the chunkwise form (64-token chunks aligned to each sequence's
+ * own start; intra-chunk work as dense tensor-core tiles; one serial state step per chunk)
+ * described in "How Kimi K3 Engineered Its Way to the Frontier", section "FlashKDA steps the
+ * state once per 16 tokens".  Long sequences are split into segments whose transitions are
+ * evaluated independently of their incoming state and composed exactly afterwards
+ * ("k3_training_and_infra_notes", section 4.1, intra-device context parallelism).
+ *
+ *   desc          problem description (host)
+ *   q, k, v, log_alpha, beta   device inputs, layouts above, element type desc->in_dtype
+ *   init_state    device fp32 [N, H, 128, 128], or NULL for zeros.  May alias final_state.
+ *   cu_seqlens    device int32 [N + 1], cu_seqlens[0] = 0, differences = host_seqlens
+ *   out           device [T_tot, H, 128] of desc->in_dtype; must not alias any input
+ *   final_state   device fp32 [N, H, 128, 128], or NULL to skip.  A zero-length sequence's
+ *                 final state is its initial state.
+ *   workspace     device scratch of at least kda_fwd_workspace_bytes(desc) bytes, 256-byte
+ *                 aligned (NULL allowed when that size is 0).  Contents on entry are ignored.
+ *   stream        CUDA stream the kernels are launched on.
+ *
+ * Bit-exactness: a sequence's results depend only on its own inputs and length, never on
+ * the other sequences packed with it.
+ */
+kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, const void* v,
+                           const void* log_alpha, const void* beta, const float* init_state,
+                           const int32_t* cu_seqlens, void* out, float* final_state,
+                           void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_decode_step — one decode token per (sequence, head), state updated in place.
+ *
+ * For every unit: S <- Diag(exp(g)) S;  u = beta (v - S^T k);  S <- S + k u^T;  o = S^T q.
+ * The state is read once and written once ("k3_training_and_infra_notes", section 4.5, KDA
+ * decoding: the recurrent state is updated in place at every decoding step).
+ *
+ *   desc          num_seqs = N, total_tokens = N; host_seqlens may be NULL (all lengths 1)
+ *   q, k, log_alpha  device [N, H, 128];  v: [N, H, 128];  beta: [N, H]  (desc->in_dtype)
+ *   state         device fp32 [N, H, 128, 128], read and overwritten in place
+ *   out           device [N, H, 128] of desc->in_dtype; must not alias any input
+ */
+kda_status kda_decode_step(const kda_desc* desc, const void* q, const void* k, const void* v,
+                           const void* log_alpha, const void* beta, float* state, void* out,
+                           kda_stream_t stream);
+
+/*
+ * kda_read_device_status — synchronise `stream`, then return and clear the sticky device
+ * status word of the current device (KDA_OK when no kernel reported a problem).
+ */
+kda_status kda_read_device_status(kda_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* kda_status_string(kda_status status);
+
+/* Number of kernels this library has launched in this process (all devices, all streams). */
+uint64_t kda_launch_count(void);
+
+/* Library ABI version (increments on any signature change). */
+int32_t kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

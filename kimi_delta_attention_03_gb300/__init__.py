@@ -1,0 +1,22 @@
+"""GB300-native Kimi Delta Attention (KDA) forward: chunked varlen prefill and decode.
+
+The compute lives in a C-ABI shared library of hand-written sm_103a CUDA kernels
+(``csrc/``, declared in ``include/kda.h``).  This package is the thin Python binding over it:
+argument marshalling only, every step of the operator runs in the library's kernels.
+The library is loaded lazily on first use and its absence is an error, never a fallback.
+"""
+from .binding import (  # noqa: F401
+    KdaError,
+    decode_step,
+    fwd_chunked,
+    fwd_workspace_bytes,
+    launch_count,
+    library_path,
+    load_library,
+    read_device_status,
+)
+
+__all__ = [
+    "KdaError", "decode_step", "fwd_chunked", "fwd_workspace_bytes", "launch_count",
+    "library_path", "load_library", "read_device_status",
+]

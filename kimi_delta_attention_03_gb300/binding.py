@@ -1,0 +1,196 @@
+"""ctypes binding of the KDA C ABI (``include/kda.h``).
+
+Argument marshalling only: shapes and dtypes are checked, missing output buffers are
+allocated with torch (PyTorch is the plumbing for device memory and streams), and the call
+goes straight to the library.  Every step of the operator runs in the library's kernels.
+If the library is missing the calls raise; there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libkda_gb300.so")
+_lock = threading.Lock()
+_lib = None
+
+KDA_OK = 0
+_DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+_STATUS = {0: "KDA_OK", -1: "KDA_ERR_INVALID_ARG", -2: "KDA_ERR_UNSUPPORTED",
+           -3: "KDA_ERR_WORKSPACE", -4: "KDA_ERR_CUDA", -5: "KDA_ERR_TIMEOUT",
+           -6: "KDA_ERR_DECAY_RANGE"}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {_STATUS.get(int(status), status)}")
+
+
+class KdaDesc(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("total_tokens", ctypes.c_int64), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("host_seqlens", ctypes.POINTER(ctypes.c_int32))]
+
+
+class KdaPlanInfo(ctypes.Structure):
+    _fields_ = [("chunks", ctypes.c_int64), ("work_items", ctypes.c_int64),
+                ("split_sequences", ctypes.c_int32), ("chunk_size", ctypes.c_int32),
+                ("segment_chunks", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+# exported symbol -> (restype, argtypes)
+_P = ctypes.c_void_p
+SIGNATURES = {
+    "kda_fwd_plan": (ctypes.c_int, [ctypes.POINTER(KdaDesc), ctypes.POINTER(KdaPlanInfo)]),
+    "kda_fwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(KdaDesc)]),
+    "kda_fwd_chunked": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P,
+                                       _P, _P, ctypes.c_size_t, _P]),
+    "kda_decode_step": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kda_read_device_status": (ctypes.c_int, [_P]),
+    "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "kda_launch_count": (ctypes.c_uint64, []),
+    "kda_version": (ctypes.c_int32, []),
+}
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load ``libkda_gb300.so`` (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"KDA CUDA library not built ({_LIB_PATH} missing); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_desc(seqlens, num_heads: int, dtype: torch.dtype, d: int = 128):
+    lens = (ctypes.c_int32 * len(seqlens))(*[int(x) for x in seqlens])
+    desc = KdaDesc(len(seqlens), int(num_heads), int(sum(int(x) for x in seqlens)), d, d,
+                   _DTYPES.get(dtype, 99), 0, lens)
+    desc._lens = lens  # keep the host array alive with the struct
+    return desc
+
+
+def fwd_plan(seqlens, num_heads: int, dtype: torch.dtype = torch.bfloat16) -> dict:
+    lib = load_library()
+    info = KdaPlanInfo()
+    st = lib.kda_fwd_plan(ctypes.byref(make_desc(seqlens, num_heads, dtype)), ctypes.byref(info))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fwd_plan")
+    return {f: getattr(info, f) for f, _ in KdaPlanInfo._fields_ if f != "reserved"}
+
+
+def fwd_workspace_bytes(seqlens, num_heads: int, dtype: torch.dtype = torch.bfloat16) -> int:
+    lib = load_library()
+    return int(lib.kda_fwd_workspace_bytes(ctypes.byref(make_desc(seqlens, num_heads, dtype))))
+
+
+def _check_io(name, t, shape, dtype, device):
+    if t.device != device or t.dtype != dtype or tuple(t.shape) != tuple(shape) \
+            or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)} on {device}, got "
+                         f"{t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+def fwd_chunked(q, k, v, log_alpha, beta, cu_seqlens, seqlens, init_state=None, out=None,
+                final_state=None, want_final_state: bool = True, workspace=None, stream=None):
+    """Chunked KDA prefill.  q, k, log_alpha, v: [T, H, 128]; beta: [T, H]; cu_seqlens: int32
+    [N+1] on the device; seqlens: the same lengths on the host.  Returns (out, final_state)."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("fwd_chunked needs CUDA tensors")
+    T, H, d = q.shape
+    N = len(seqlens)
+    dt = q.dtype
+    for name, t, shp in (("k", k, (T, H, d)), ("v", v, (T, H, d)),
+                         ("log_alpha", log_alpha, (T, H, d)), ("beta", beta, (T, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    if init_state is not None:
+        _check_io("init_state", init_state, (N, H, d, d), torch.float32, dev)
+    if out is None:
+        out = torch.empty((T, H, d), dtype=dt, device=dev)
+    _check_io("out", out, (T, H, d), dt, dev)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _check_io("final_state", final_state, (N, H, d, d), torch.float32, dev)
+    desc = make_desc(seqlens, H, dt, d)
+    need = int(lib.kda_fwd_workspace_bytes(ctypes.byref(desc)))
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kda_fwd_chunked(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                             _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), _ptr(out),
+                             _ptr(final_state), _ptr(workspace), ws_bytes,
+                             _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fwd_chunked")
+    return out, final_state
+
+
+def decode_step(q, k, v, log_alpha, beta, state, out=None, stream=None):
+    """One decode token per (sequence, head); ``state`` [N, H, 128, 128] fp32 is updated in
+    place.  q, k, log_alpha, v: [N, H, 128]; beta: [N, H].  Returns out [N, H, 128]."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("decode_step needs CUDA tensors")
+    N, H, d = q.shape
+    dt = q.dtype
+    for name, t, shp in (("k", k, (N, H, d)), ("v", v, (N, H, d)),
+                         ("log_alpha", log_alpha, (N, H, d)), ("beta", beta, (N, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("state", state, (N, H, d, d), torch.float32, dev)
+    if out is None:
+        out = torch.empty((N, H, d), dtype=dt, device=dev)
+    _check_io("out", out, (N, H, d), dt, dev)
+    desc = KdaDesc(N, H, N, d, d, _DTYPES.get(dt, 99), 0, None)
+    st = lib.kda_decode_step(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                             _ptr(beta), _ptr(state), _ptr(out), _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_step")
+    return out
+
+
+def read_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the sticky device status code."""
+    lib = load_library()
+    s = None if stream is None else ctypes.c_void_p(stream.cuda_stream)
+    if s is None and torch.cuda.is_available():
+        s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return int(lib.kda_read_device_status(s))
+
+
+def launch_count() -> int:
+    return int(load_library().kda_launch_count())

@@ -1,0 +1,165 @@
+// kda_api.cu — the C ABI declared in include/kda.h: host-side checks, the work plan, the
+// sticky device status word, and the kernel launches.  No allocation happens here.
+#include <atomic>
+#include <mutex>
+
+#include "kda_common.cuh"
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+// One sticky status word per device; kernels write it with atomicCAS(0 -> code).
+__device__ int g_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+int* status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+// Vector loads and stores need 16-byte aligned tensors (torch allocations are 256-aligned).
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kda_status check_desc(const kda_desc* d, bool need_lengths) {
+    if (!d) return KDA_ERR_INVALID_ARG;
+    if (d->d_k != 128 || d->d_v != 128) return KDA_ERR_UNSUPPORTED;
+    if (d->in_dtype != KDA_BF16 && d->in_dtype != KDA_FP32) return KDA_ERR_UNSUPPORTED;
+    if (d->num_seqs < 1 || d->num_heads < 1 || d->total_tokens < 0 || d->reserved != 0)
+        return KDA_ERR_INVALID_ARG;
+    if (need_lengths) {
+        if (!d->host_seqlens) return KDA_ERR_INVALID_ARG;
+        int64_t sum = 0;
+        for (int32_t n = 0; n < d->num_seqs; ++n) {
+            if (d->host_seqlens[n] < 0) return KDA_ERR_INVALID_ARG;
+            sum += d->host_seqlens[n];
+        }
+        if (sum != d->total_tokens) return KDA_ERR_INVALID_ARG;
+        // token offsets are formed as int32 cu_seqlens
+        if (d->total_tokens > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    }
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_fwd_plan(const kda_desc* desc, kda_plan_info* info) {
+    if (!info) return KDA_ERR_INVALID_ARG;
+    kda_status st = check_desc(desc, true);
+    if (st != KDA_OK) return st;
+    kda_plan_info p = {};
+    p.chunk_size = kda::kChunk;
+    p.segment_chunks = 0;
+    for (int32_t n = 0; n < desc->num_seqs; ++n) {
+        const int64_t L = desc->host_seqlens[n];
+        p.chunks += (L + kda::kChunk - 1) / kda::kChunk;
+        p.work_items += 1;
+    }
+    p.workspace_bytes = 0;
+    *info = p;
+    return KDA_OK;
+}
+
+size_t kda_fwd_workspace_bytes(const kda_desc* desc) {
+    kda_plan_info p;
+    if (kda_fwd_plan(desc, &p) != KDA_OK) return 0;
+    return p.workspace_bytes;
+}
+
+kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, const void* v,
+                           const void* log_alpha, const void* beta, const float* init_state,
+                           const int32_t* cu_seqlens, void* out, float* final_state,
+                           void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    kda_plan_info plan;
+    kda_status st = kda_fwd_plan(desc, &plan);
+    if (st != KDA_OK) return st;
+    if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (desc->total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !out))
+        return KDA_ERR_INVALID_ARG;
+    if (out && (out == q || out == k || out == v || out == log_alpha || out == beta))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+        !aligned16(out) || !aligned16(init_state) || !aligned16(final_state))
+        return KDA_ERR_INVALID_ARG;
+    if (plan.workspace_bytes > 0 && (!workspace || workspace_bytes < plan.workspace_bytes))
+        return KDA_ERR_WORKSPACE;
+    int* status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    uint64_t launches = 0;
+    cudaError_t e = kda::launch_prefill(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v,
+                                        log_alpha, beta, init_state, cu_seqlens, out,
+                                        final_state, status, (cudaStream_t)stream, &launches);
+    g_launches += launches;
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_decode_step(const kda_desc* desc, const void* q, const void* k, const void* v,
+                           const void* log_alpha, const void* beta, float* state, void* out,
+                           kda_stream_t stream) {
+    kda_status st = check_desc(desc, false);
+    if (st != KDA_OK) return st;
+    if (desc->total_tokens != desc->num_seqs) return KDA_ERR_INVALID_ARG;
+    if (desc->host_seqlens) {
+        for (int32_t n = 0; n < desc->num_seqs; ++n)
+            if (desc->host_seqlens[n] != 1) return KDA_ERR_INVALID_ARG;
+    }
+    if (!q || !k || !v || !log_alpha || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+    if (out == q || out == k || out == v || out == log_alpha || out == beta ||
+        out == (const void*)state)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state)) return KDA_ERR_INVALID_ARG;
+    int* status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    const int64_t units = (int64_t)desc->num_seqs * desc->num_heads;
+    cudaError_t e = kda::launch_decode(desc->in_dtype, units, desc->num_heads, q, k, v,
+                                       log_alpha, beta, state, out, status,
+                                       (cudaStream_t)stream);
+    g_launches += 1;
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_read_device_status(kda_stream_t stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KDA_ERR_CUDA;
+    int* p = status_word();
+    if (!p) return KDA_ERR_CUDA;
+    int value = 0;
+    if (cudaMemcpy(&value, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (value != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    return (kda_status)value;
+}
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        case KDA_ERR_DECAY_RANGE: return "KDA_ERR_DECAY_RANGE";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+uint64_t kda_launch_count(void) { return g_launches.load(); }
+
+int32_t kda_version(void) { return 1; }
+
+}  // extern "C"

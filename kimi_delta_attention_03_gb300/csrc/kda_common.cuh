@@ -1,0 +1,58 @@
+// kda_common.cuh — small device helpers shared by the KDA kernels of this library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int kDim = 128;     // d_k = d_v
+constexpr int kChunk = 64;    // tokens per chunk of the prefill path
+
+// Device status codes written into the sticky status word (same values as kda_status).
+constexpr int kStatusDecayRange = KDA_ERR_DECAY_RANGE;
+constexpr int kStatusTimeout = KDA_ERR_TIMEOUT;
+
+// Record a device-side condition; the first one written stays until the host clears it.
+__device__ __forceinline__ void report_status(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+template <typename T> struct io;
+
+template <> struct io<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+template <> struct io<float> {
+    static __device__ __forceinline__ float to_f(float x) { return x; }
+    static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&p);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+}  // namespace kda
+
+// Launchers implemented in the kernel translation units (called by kda_api.cu).
+namespace kda {
+cudaError_t launch_decode(int dtype, int64_t units, int heads, const void* q, const void* k,
+                          const void* v, const void* g, const void* beta, float* state,
+                          void* out, int* status, cudaStream_t stream);
+
+cudaError_t launch_prefill(int dtype, int num_seqs, int heads, const void* q, const void* k,
+                           const void* v, const void* g, const void* beta,
+                           const float* init_state, const int32_t* cu_seqlens, void* out,
+                           float* final_state, int* status, cudaStream_t stream,
+                           uint64_t* launches);
+}  // namespace kda

@@ -1,0 +1,128 @@
+// kda_decode.cu — single-token KDA decode: in-place state update, one pass over HBM.
+//
+// For one (sequence, head) unit with state S (128 x 128 fp32, row = key channel) and one
+// token (q, k, v, g = log alpha, beta):
+//     S <- Diag(exp(g)) S;   u = beta (v - S^T k);   S <- S + k u^T;   o = S^T q
+// ("How Kimi K3 Engineered Its Way to the Frontier", section "How KDA updates its state";
+// in-place update at every decoding step: "k3_training_and_infra_notes", section 4.5).
+//
+// The step is bound by HBM: 64 KiB of state read and 64 KiB written per unit against about
+// 1.3 KFLOP per KiB.  Each CTA (256 threads) owns one unit and keeps the whole decayed state
+// in registers between the read and the write, so S crosses HBM exactly twice:
+//   thread (warp w, lane l) holds rows {w + 8 r : r < 16}, columns 4l .. 4l+3 (one float4
+//   per row; a warp touches one full 512-byte row per access, fully coalesced).
+// The two column reductions x = (D S)^T k and y = (D S)^T q are per-thread partial sums over
+// its 16 rows, then a cross-warp sum through shared memory.  The output uses the identity
+//     o = S_new^T q = y + (k . q) u,
+// so the updated state never has to be re-read.  Loads and stores are streaming (evict-first)
+// because every byte is touched once.
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kDecodeThreads = 256;
+
+template <typename TIn>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
+                  const TIn* __restrict__ v, const TIn* __restrict__ g,
+                  const TIn* __restrict__ beta, float* __restrict__ state,
+                  TIn* __restrict__ out, int64_t units) {
+    __shared__ float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_u[kDim];
+    __shared__ __align__(16) float s_rx[8][kDim];
+    __shared__ __align__(16) float s_ry[8][kDim];
+    __shared__ float s_kq;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+
+    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        float* S = state + unit * (int64_t)(kDim * kDim);
+        float4 s[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
+
+        if (tid < kDim) {
+            const int64_t e = unit * kDim + tid;
+            s_k[tid] = io<TIn>::to_f(k[e]);
+            s_q[tid] = io<TIn>::to_f(q[e]);
+            s_a[tid] = expf(io<TIn>::to_f(g[e]));
+            s_v[tid] = io<TIn>::to_f(v[e]);
+        }
+        const float b = io<TIn>::to_f(beta[unit]);
+        __syncthreads();
+
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+        float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const int i = warp + 8 * r;
+            const float a = s_a[i], kk = s_k[i], qq = s_q[i];
+            s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
+            x0 = fmaf(kk, s[r].x, x0); x1 = fmaf(kk, s[r].y, x1);
+            x2 = fmaf(kk, s[r].z, x2); x3 = fmaf(kk, s[r].w, x3);
+            y0 = fmaf(qq, s[r].x, y0); y1 = fmaf(qq, s[r].y, y1);
+            y2 = fmaf(qq, s[r].z, y2); y3 = fmaf(qq, s[r].w, y3);
+        }
+        reinterpret_cast<float4*>(s_rx[warp])[lane] = make_float4(x0, x1, x2, x3);
+        reinterpret_cast<float4*>(s_ry[warp])[lane] = make_float4(y0, y1, y2, y3);
+        if (warp == 0) {
+            float p = 0.f;
+#pragma unroll
+            for (int m = 0; m < kDim / 32; ++m) p = fmaf(s_k[lane + 32 * m], s_q[lane + 32 * m], p);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+            if (lane == 0) s_kq = p;
+        }
+        __syncthreads();
+
+        if (tid < kDim) {
+            float x = 0.f, y = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) { x += s_rx[w][tid]; y += s_ry[w][tid]; }
+            const float u = b * (s_v[tid] - x);
+            s_u[tid] = u;
+            out[unit * kDim + tid] = io<TIn>::from_f(fmaf(s_kq, u, y));
+        }
+        __syncthreads();
+
+        const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float kk = s_k[warp + 8 * r];
+            float4 o;
+            o.x = fmaf(kk, u4.x, s[r].x); o.y = fmaf(kk, u4.y, s[r].y);
+            o.z = fmaf(kk, u4.z, s[r].z); o.w = fmaf(kk, u4.w, s[r].w);
+            __stcs(reinterpret_cast<float4*>(S + (warp + 8 * r) * kDim) + lane, o);
+        }
+        __syncthreads();  // shared vectors are rewritten by the next unit of this CTA
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(int dtype, int64_t units, int heads, const void* q, const void* k,
+                          const void* v, const void* g, const void* beta, float* state,
+                          void* out, int* status, cudaStream_t stream) {
+    (void)heads;
+    (void)status;
+    if (units <= 0) return cudaSuccess;
+    const int64_t max_grid = 1LL << 30;
+    const unsigned grid = (unsigned)(units < max_grid ? units : max_grid);
+    if (dtype == KDA_BF16) {
+        using T = __nv_bfloat16;
+        kda_decode_kernel<T><<<grid, kDecodeThreads, 0, stream>>>(
+            (const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta, state, (T*)out,
+            units);
+    } else {
+        kda_decode_kernel<float><<<grid, kDecodeThreads, 0, stream>>>(
+            (const float*)q, (const float*)k, (const float*)v, (const float*)g,
+            (const float*)beta, state, (float*)out, units);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,95 @@
+"""The C-ABI library loads, exports every symbol include/kda.h declares, and its host-side
+logic (argument checks, work plan) behaves as documented.  No GPU needed: nothing here
+launches a kernel — every call below is rejected or answered on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kimi_delta_attention_03_gb300 import build, binding
+    build.build()
+    return binding.load_library()
+
+
+def _declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(kda_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from kimi_delta_attention_03_gb300 import binding
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+        assert name in binding.SIGNATURES, f"{name} has no binding signature"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.kda_version() >= 1
+    assert lib.kda_status_string(0) == b"KDA_OK"
+    assert lib.kda_status_string(-6) == b"KDA_ERR_DECAY_RANGE"
+    assert lib.kda_status_string(12345) == b"KDA_ERR_UNKNOWN"
+
+
+def _desc(lens, H=4, dtype=torch.bfloat16, d=128):
+    from kimi_delta_attention_03_gb300 import binding
+    return binding.make_desc(lens, H, dtype, d)
+
+
+def test_plan_counts_chunks_per_sequence(lib):
+    from kimi_delta_attention_03_gb300 import binding
+    lens = [0, 1, 63, 64, 65, 8192, 130]
+    info = binding.fwd_plan(lens, 4)
+    assert info["chunk_size"] == 64
+    assert info["chunks"] == sum((L + 63) // 64 for L in lens)
+    assert info["work_items"] >= len(lens)
+
+
+def test_host_argument_checks(lib):
+    from kimi_delta_attention_03_gb300 import binding
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    st = lambda d, **kw: lib.kda_fwd_chunked(
+        ctypes.byref(d), kw.get("q", fake), fake, fake, fake, fake, None, fake,
+        kw.get("out", P(0x2000)), None, None, 0, None)
+    assert st(_desc([4, 5], d=64)) == -2                    # unsupported head dim
+    assert st(_desc([4, 5], dtype=torch.float16)) == -2     # unsupported dtype
+    d = _desc([4, 5])
+    d.total_tokens = 10
+    assert st(d) == -1                                      # lengths do not sum to T_tot
+    assert st(_desc([4, -1])) == -1                         # negative length
+    assert st(_desc([4, 5]), q=None) == -1                  # null input
+    assert st(_desc([4, 5]), out=fake) == -1                # out aliases an input
+    assert lib.kda_fwd_plan(None, None) == -1
+    assert lib.kda_fwd_workspace_bytes(None) == 0
+    # decode: total_tokens must equal num_seqs, every host length must be 1
+    dd = _desc([1, 1, 1])
+    dd.total_tokens = 4
+    assert lib.kda_decode_step(ctypes.byref(dd), fake, fake, fake, fake, fake, P(0x3000),
+                               P(0x2000), None) == -1
+    dd = _desc([1, 2])
+    dd.total_tokens = 2
+    assert lib.kda_decode_step(ctypes.byref(dd), fake, fake, fake, fake, fake, P(0x3000),
+                               P(0x2000), None) == -1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import kimi_delta_attention_03_gb300 as kda
+    x = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kda.fwd_chunked(x, x, x, x, torch.zeros(4, 2, dtype=torch.bfloat16),
+                        torch.tensor([0, 4], dtype=torch.int32), [4])

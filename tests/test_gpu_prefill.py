@@ -1,0 +1,223 @@
+"""GPU parity of the chunked prefill (through the C ABI) against the fp64 oracle.
+
+Small cases span several chunks and a ragged tail; the full-size workloads run in the same
+launch configuration the benchmark times, compared on output windows the oracle records
+plus every final state.  Packing is checked bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kimi_delta_attention_03_gb300 import synth
+from tests.parity import assert_close, errors, oracle_threads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def kda():
+    import kimi_delta_attention_03_gb300 as m
+    return m
+
+
+def run_gpu(x, init=True, **kw):
+    out, fin = kda().fwd_chunked(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                 x["cu_seqlens"], x["seqlens"],
+                                 init_state=x["init_state"] if init else None, **kw)
+    torch.cuda.synchronize()
+    return out, fin
+
+
+def run_oracle(x, init=True, windows=None, want_out=True):
+    s0 = x["init_state"].cpu() if (init and x["init_state"] is not None) else None
+    return oracle.recurrence(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), x["log_alpha"].cpu(),
+                             x["beta"].cpu(), x["cu_seqlens"].cpu(), state_in=s0,
+                             windows=windows, want_out=want_out, threads=oracle_threads())
+
+
+def rows_of(t, windows):
+    return torch.cat([t[lo:hi] for lo, hi in windows]) if windows else t
+
+
+def check_status():
+    assert kda().read_device_status() == 0
+
+
+def test_tiny_fp32_workload():
+    w = synth.workloads()["tiny_fp32"]
+    x = synth.make_workload(w, device=DEV)
+    out, fin = run_gpu(x)
+    o_ref, s_ref = run_oracle(x)
+    assert out.dtype == torch.float32
+    assert_close("out", out.cpu().numpy(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+    check_status()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_ragged_lengths(dtype):
+    lens = [1, 15, 16, 17, 63, 64, 65, 130, 0, 200, 127, 128, 129]
+    x = synth.make_inputs(lens, 3, dtype, seed=5, device=DEV)
+    out, fin = run_gpu(x)
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+    # the zero-length sequence's final state is its initial state, bit for bit
+    assert torch.equal(fin[8], x["init_state"][8])
+    check_status()
+
+
+def test_no_initial_state():
+    x = synth.make_inputs([100, 33], 2, torch.bfloat16, seed=6, device=DEV)
+    out, fin = run_gpu(x, init=False)
+    o_ref, s_ref = run_oracle(x, init=False)
+    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+
+
+def test_packing_is_bit_exact_and_does_not_leak():
+    lens = [70, 0, 129, 64, 1, 200]
+    x = synth.make_inputs(lens, 4, torch.bfloat16, seed=8, device=DEV)
+    out, fin = run_gpu(x)
+    cu = x["cu_seqlens"].cpu().tolist()
+    for n, L in enumerate(lens):
+        lo, hi = cu[n], cu[n + 1]
+        xs = {key: x[key][lo:hi].contiguous() for key in ("q", "k", "v", "log_alpha", "beta")}
+        xs["init_state"] = x["init_state"][n:n + 1].contiguous()
+        xs["cu_seqlens"] = torch.tensor([0, L], dtype=torch.int32, device=DEV)
+        xs["seqlens"] = [L]
+        o1, f1 = run_gpu(xs)
+        assert torch.equal(o1, out[lo:hi]), f"sequence {n}: packed output differs"
+        assert torch.equal(f1[0], fin[n]), f"sequence {n}: packed final state differs"
+    # perturb sequence 2; sequences 3.. keep their bits
+    y = {key: (val.clone() if torch.is_tensor(val) else val) for key, val in x.items()}
+    y["v"][cu[2]:cu[3]] += 1.0
+    y["log_alpha"][cu[2]:cu[3]] *= 2
+    out2, fin2 = run_gpu(y)
+    assert torch.equal(out2[cu[3]:], out[cu[3]:])
+    assert torch.equal(fin2[3:], fin[3:])
+    assert torch.equal(out2[:cu[2]], out[:cu[2]])
+    assert not torch.equal(fin2[2], fin[2])
+
+
+def test_canaries_outside_outputs_untouched():
+    lens = [77, 5]
+    x = synth.make_inputs(lens, 2, torch.bfloat16, seed=9, device=DEV)
+    T, H = sum(lens), 2
+    pad = 4096
+    out_buf = torch.full((pad + T * H * 128 + pad,), -12345.0, dtype=torch.bfloat16, device=DEV)
+    fin_buf = torch.full((pad + 2 * H * 128 * 128 + pad,), 777.0, dtype=torch.float32,
+                         device=DEV)
+    out = out_buf[pad:pad + T * H * 128].view(T, H, 128)
+    fin = fin_buf[pad:pad + 2 * H * 128 * 128].view(2, H, 128, 128)
+    run_gpu(x, out=out, final_state=fin)
+    assert (out_buf[:pad] == -12345.0).all() and (out_buf[-pad:] == -12345.0).all()
+    assert (fin_buf[:pad] == 777.0).all() and (fin_buf[-pad:] == 777.0).all()
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", out.float().cpu().numpy(), o_ref)
+
+
+def test_init_state_may_alias_final_state():
+    x = synth.make_inputs([150, 64, 3], 2, torch.bfloat16, seed=10, device=DEV)
+    ref_out, ref_fin = run_gpu(x)
+    state = x["init_state"].clone()
+    out, fin = kda().fwd_chunked(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                 x["cu_seqlens"], x["seqlens"], init_state=state,
+                                 final_state=state)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out) and torch.equal(state, ref_fin)
+
+
+def test_resume_from_saved_state_and_decode_continuation():
+    T, T1, H = 300, 130, 2
+    x = synth.make_inputs([T + 1], H, torch.bfloat16, seed=11, device=DEV)
+    part = lambda a, b: {**{key: x[key][a:b].contiguous() for key in
+                            ("q", "k", "v", "log_alpha", "beta")},
+                         "cu_seqlens": torch.tensor([0, b - a], dtype=torch.int32, device=DEV),
+                         "seqlens": [b - a], "init_state": x["init_state"]}
+    full_out, full_fin = run_gpu(part(0, T + 1))
+    a_out, a_fin = run_gpu(part(0, T1))
+    pb = part(T1, T)
+    pb["init_state"] = a_fin
+    b_out, b_fin = run_gpu(pb)
+    o_ref, s_ref = run_oracle(part(0, T))
+    assert_close("resumed out", torch.cat([a_out, b_out]).float().cpu().numpy(), o_ref)
+    assert_close("resumed state", b_fin.cpu().numpy(), s_ref)
+    # one more token through the decode path equals the prefill's last token
+    state = b_fin.clone()
+    xt = {key: x[key][T:T + 1].contiguous() for key in ("q", "k", "v", "log_alpha", "beta")}
+    o_dec = kda().decode_step(xt["q"], xt["k"], xt["v"], xt["log_alpha"], xt["beta"], state)
+    torch.cuda.synchronize()
+    o_ref1, s_ref1 = run_oracle(part(0, T + 1), windows=[(T, T + 1)])
+    assert_close("decode after prefill out", o_dec.float().cpu().numpy(), o_ref1)
+    assert_close("decode after prefill state", state.cpu().numpy(), s_ref1)
+    assert_close("prefill(T+1) last", full_out[T:].float().cpu().numpy(), o_ref1)
+
+
+def test_deterministic():
+    x = synth.make_inputs([513, 77], 3, torch.bfloat16, seed=12, device=DEV)
+    o1, f1 = run_gpu(x)
+    o2, f2 = run_gpu(x)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+def test_decay_range_is_reported():
+    x = synth.make_inputs([64], 1, torch.bfloat16, seed=13, device=DEV)
+    x["log_alpha"] = torch.full_like(x["log_alpha"], -6.0)  # 64 tokens: G_C = -384
+    assert kda().read_device_status() == 0
+    run_gpu(x)
+    assert kda().read_device_status() == -6
+    assert kda().read_device_status() == 0  # cleared by the read
+
+
+# ------------------------------- full-size workloads -----------------------------------
+def _windows_per_sequence(seqlens, head=128, tail=128):
+    wins, t0 = [], 0
+    for L in seqlens:
+        if L:
+            wins.append((t0, t0 + min(L, head)))
+            if L > head:
+                wins.append((max(t0 + head, t0 + L - tail), t0 + L))
+        t0 += L
+    return wins
+
+
+def test_prefill_4x8k_full_size():
+    w = synth.workloads()["prefill_4x8k"]
+    x = synth.make_workload(w, device=DEV)
+    out, fin = run_gpu(x)
+    wins = _windows_per_sequence(x["seqlens"], 512, 512)
+    o_ref, s_ref = run_oracle(x, windows=wins)
+    assert_close("out", rows_of(out, wins).float().cpu().numpy(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+    check_status()
+
+
+def test_long_256k_full_size_error_does_not_grow():
+    w = synth.workloads()["long_256k"]
+    x = synth.make_workload(w, device=DEV)
+    out, fin = run_gpu(x)
+    T = x["q"].shape[0]
+    W = 16384
+    wins = [(0, W), (T - W, T)]
+    o_ref, s_ref = run_oracle(x, windows=wins)
+    o = rows_of(out, wins).float().cpu().numpy()
+    first = errors(o[:W], o_ref[:W])
+    last = errors(o[W:], o_ref[W:])
+    assert_close("out first 16K", o[:W], o_ref[:W])
+    assert_close("out last 16K", o[W:], o_ref[W:])
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+    assert tuple(fin.shape) == (1, 16, 128, 128)
+    assert last[0] <= 2.0 * first[0], (first, last)
+    check_status()
+
+
+def test_varlen_64_full_size():
+    w = synth.workloads()["varlen_64"]
+    x = synth.make_workload(w, device=DEV)
+    out, fin = run_gpu(x)
+    wins = _windows_per_sequence(x["seqlens"])
+    o_ref, s_ref = run_oracle(x, windows=wins)
+    assert_close("out", rows_of(out, wins).float().cpu().numpy(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+    check_status()
