@@ -98,9 +98,15 @@ kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, c
     int* status = status_word();
     if (!status) return KDA_ERR_CUDA;
     uint64_t launches = 0;
-    cudaError_t e = kda::launch_prefill(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v,
-                                        log_alpha, beta, init_state, cu_seqlens, out,
-                                        final_state, status, (cudaStream_t)stream, &launches);
+    cudaError_t e;
+    if (desc->in_dtype == KDA_BF16)
+        e = kda::launch_prefill_tc(desc->num_seqs, desc->num_heads, desc->total_tokens, q, k, v,
+                                   log_alpha, beta, init_state, cu_seqlens, out, final_state,
+                                   status, (cudaStream_t)stream, &launches);
+    else
+        e = kda::launch_prefill(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v,
+                                log_alpha, beta, init_state, cu_seqlens, out, final_state,
+                                status, (cudaStream_t)stream, &launches);
     g_launches += launches;
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -55,4 +55,10 @@ cudaError_t launch_prefill(int dtype, int num_seqs, int heads, const void* q, co
                            const float* init_state, const int32_t* cu_seqlens, void* out,
                            float* final_state, int* status, cudaStream_t stream,
                            uint64_t* launches);
+
+cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, const void* q,
+                              const void* k, const void* v, const void* g, const void* beta,
+                              const float* init_state, const int32_t* cu_seqlens, void* out,
+                              float* final_state, int* status, cudaStream_t stream,
+                              uint64_t* launches);
 }  // namespace kda
