@@ -14,8 +14,9 @@
 // (the last line is diag(e^{G_C}) S + K_bar^T U with K_bar = k e^{G_C-G} = K_m diag(e^r)).
 //
 // GB300 mapping.  One CTA per (sequence, head), 14 warps:
-//   warp 0      TMA producer: q, k, g chunks into double-buffered slots; v single-buffered
-//   warp 1      MMA issuer: one thread, event loop over six groups of tcgen05.mma
+//   warp 0      prep MMA issuer (one thread): the chunk-local products of chunk c+1, and the
+//               TMA load of the next v chunk; it also issues the first q, k, g, v loads
+//   warp 1      serial MMA issuer (one thread): the state products of chunk c
 //   warps 2-9   prep: decay factors, A/P epilogue, 64x64 inverse, W epilogue (chunk c+1)
 //   warps 10-13 serial epilogue: U^T to TMEM, O^T to HBM, state rescale (chunk c)
 // so the chunk-parallel work of chunk c+1 overlaps the serial state pass of chunk c.  The
@@ -68,11 +69,13 @@ constexpr uint32_t OFF_WN1 = 163840;     // slot 1
 constexpr uint32_t OFF_TB0 = 180224;     // T diag(beta): 64 x 64 (8 KB), slot 0
 constexpr uint32_t OFF_TB1 = 188416;     // slot 1
 constexpr uint32_t OFF_KML = 196608;     // K_m lo 64 x 128 (16 KB); after M1: A/T fp32 [64][68]
-constexpr uint32_t OFF_Y = OFF_KML + 17408 + 1024;  // 3 x 16 x 16 fp32 block products
-constexpr uint32_t OFF_BETA = OFF_Y + 3072;         // 64 fp32
+constexpr uint32_t OFF_Y = OFF_KML + 17408;         // 4 x 16 x 16 fp32 blocks (N^2, N^3)
+constexpr uint32_t OFF_PART = OFF_Y + 4096;         // 16 x 128 fp32 token-group sums / prefixes
+constexpr uint32_t OFF_GC = OFF_PART + 8192;        // 128 fp32: chunk log-decay G_C
+constexpr uint32_t OFF_BETA = OFF_GC + 512;         // 64 fp32
 constexpr uint32_t OFF_ER = OFF_BETA + 256;         // 4 x 128 fp32: e^{r} ring
-constexpr uint32_t OFF_PART = OFF_ER + 2048;        // 2 x 128 fp32 partial sums
-constexpr uint32_t OFF_BAR = OFF_PART + 1024;       // mbarriers
+constexpr uint32_t OFF_SC = OFF_ER + 2048;          // 4 x 128 fp32: e^{r_{c-1} + r_c} ring
+constexpr uint32_t OFF_BAR = OFF_SC + 2048;         // mbarriers
 constexpr int NBAR = 24;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 64;
@@ -81,20 +84,21 @@ static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
 // barrier indices
 enum {
-    B_FULL0 = 0, B_FULL1, B_SLOTFREE0, B_SLOTFREE1, B_VFULL, B_VFREE,
+    B_FULL0 = 0, B_FULL1, B_VFREE0, B_VFREE1, B_VFULL, B_SPARE,
     B_FACT0, B_FACT1, B_AP0, B_AP1, B_TB0, B_TB1, B_WDONE0, B_WDONE1, B_WN0, B_WN1,
-    B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_COUNT
+    B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_UFREE0, B_UFREE1, B_COUNT
 };
 static_assert(B_COUNT <= NBAR, "barrier slots");
 
 // TMEM columns (512 allocated)
 constexpr uint32_t T_S = 0;      // X: fp32 state, lanes = value channel, cols = key channel
 constexpr uint32_t T_O = 128;    // O^T (64 cols)
-constexpr uint32_t T_U = 192;    // U^T (64 cols)
+constexpr uint32_t T_U0 = 192;   // U^T, even chunks (64 cols)
 constexpr uint32_t T_P = 256;    // [A ; P] raw tiles, then W^T (64 cols)
 constexpr uint32_t T_SA = 320;   // bf16 copy of X (A operand, 64 cols)
 constexpr uint32_t T_UH = 384;   // bf16 U^T hi (A operand, 32 cols)
 constexpr uint32_t T_UL = 416;   // bf16 U^T lo (32 cols)
+constexpr uint32_t T_U1 = 448;   // U^T, odd chunks (64 cols)
 
 struct TcParams {
     const bf16* beta;
@@ -111,6 +115,83 @@ __device__ __forceinline__ void named_bar(int id, int n) {
 }
 
 __device__ __forceinline__ float bf2f(bf16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
+                      pack_bf16(f[6], f[7]));
+}
+
+// ---- 16 x 16 fp32 block products on the tensor cores (tf32 inputs, fp32 accumulate) ----
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// acc += (xs * X + n2 - n3) Yb for 16 x 16 blocks; n2 / n3 (leading dim 16) may be null.
+__device__ __forceinline__ void block_mma(float (&acc)[2][4], const float* X, int ldx, float xs,
+                                          const float* n2, const float* n3, const float* Yb,
+                                          int ldy, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const int k0 = 8 * ks;
+        const int r[4] = {g, g + 8, g, g + 8};
+        const int cc[4] = {k0 + t, k0 + t, k0 + t + 4, k0 + t + 4};
+        uint32_t a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float x = xs * X[r[i] * ldx + cc[i]];
+            if (n2) x += n2[r[i] * 16 + cc[i]];
+            if (n3) x -= n3[r[i] * 16 + cc[i]];
+            a[i] = to_tf32(x);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int n0 = 8 * nt;
+            mma_tf32(acc[nt], a, to_tf32(Yb[(k0 + t) * ldy + n0 + g]),
+                     to_tf32(Yb[(k0 + t + 4) * ldy + n0 + g]));
+        }
+    }
+}
+__device__ __forceinline__ void block_product(float (&acc)[2][4], const float* X, int ldx, float xs,
+                                              const float* n2, const float* n3, const float* Yb,
+                                              int ldy, int lane) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    block_mma(acc, X, ldx, xs, n2, n3, Yb, ldy, lane);
+}
+__device__ __forceinline__ void block_product_acc(float (&acc)[2][4], const float* X, int ldx,
+                                                  const float* Yb, int ldy, int lane) {
+    block_mma(acc, X, ldx, 1.f, nullptr, nullptr, Yb, ldy, lane);
+}
+__device__ __forceinline__ void store_block(float* D, int ld, const float (&acc)[2][4], int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        *reinterpret_cast<float2*>(D + g * ld + 8 * nt + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2*>(D + (g + 8) * ld + 8 * nt + 2 * t) =
+            make_float2(acc[nt][2], acc[nt][3]);
+    }
+}
+// block pairs (I, J), I > J, of the 4 x 4 block-lower 64 x 64 matrix, one per prep warp
+__device__ __forceinline__ int pair_i(int w) { return w < 1 ? 1 : (w < 3 ? 2 : 3); }
+__device__ __forceinline__ int pair_j(int w) { const int I = pair_i(w); return w - I * (I - 1) / 2; }
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                          int* status) {
@@ -158,9 +239,12 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 8);
+    volatile int* kqg_issued = reinterpret_cast<volatile int*>(sm + OFF_MISC + 16);
     float* beta_s = reinterpret_cast<float*>(sm + OFF_BETA);
     float* er = reinterpret_cast<float*>(sm + OFF_ER);
     float* part = reinterpret_cast<float*>(sm + OFF_PART);
+    float* gc_s = reinterpret_cast<float*>(sm + OFF_GC);
+    float* sc = reinterpret_cast<float*>(sm + OFF_SC);
 
     if (warp == kWarpTma) {
         tmem_alloc(tmem_slot, 512);
@@ -169,6 +253,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (tid == 32) {
         for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
+        *kqg_issued = 0;
         mbar_init_fence();
     }
     tc_fence_before();
@@ -176,176 +261,147 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    const uint32_t a_kq[2] = {saddr(sm + OFF_KQ0), saddr(sm + OFF_KQ1)};
+    const uint32_t a_kmh[2] = {saddr(sm + OFF_KMH0), saddr(sm + OFF_KMH1)};
+    const uint32_t a_p[2] = {saddr(sm + OFF_P0), saddr(sm + OFF_P1)};
+    const uint32_t a_wn[2] = {saddr(sm + OFF_WN0), saddr(sm + OFF_WN1)};
+    const uint32_t a_tb[2] = {saddr(sm + OFF_TB0), saddr(sm + OFF_TB1)};
+    // TMA issue helpers (q, k, g of chunk c into slot c & 1; v of chunk c)
+    auto issue_kqg = [&](int c) {
+        const int s = c & 1;
+        unsigned char* kq = sm + (s ? OFF_KQ1 : OFF_KQ0);
+        unsigned char* wn = sm + (s ? OFF_WN1 : OFF_WN0);
+        uint64_t* full = &bars[B_FULL0 + s];
+        const int t0 = (int)(seq0 + (int64_t)kChunk * c);
+        mbar_arrive_expect_tx(full, 49152);
+        tma_load_3d(kq + 0, &tm_k, full, 0, h, t0);
+        tma_load_3d(kq + 16384, &tm_k, full, 64, h, t0);
+        tma_load_3d(kq + 8192, &tm_q, full, 0, h, t0);
+        tma_load_3d(kq + 24576, &tm_q, full, 64, h, t0);
+        tma_load_3d(wn + 0, &tm_g, full, 0, h, t0);
+        tma_load_3d(wn + 8192, &tm_g, full, 64, h, t0);
+        *kqg_issued = c + 1;
+    };
+    auto issue_v = [&](int c) {
+        const int t0 = (int)(seq0 + (int64_t)kChunk * c);
+        mbar_arrive_expect_tx(&bars[B_VFULL], 16384);
+        tma_load_3d(sm + OFF_V, &tm_v, &bars[B_VFULL], 0, h, t0);
+        tma_load_3d(sm + OFF_V + 8192, &tm_v, &bars[B_VFULL], 64, h, t0);
+    };
+
     if (warp == kWarpTma) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ prep MMA issuer
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_g);
-            auto issue_kqg = [&](int c) {
-                const int s = c & 1;
-                unsigned char* kq = sm + (s ? OFF_KQ1 : OFF_KQ0);
-                unsigned char* wn = sm + (s ? OFF_WN1 : OFF_WN0);
-                uint64_t* full = &bars[B_FULL0 + s];
-                const int t0 = (int)(seq0 + (int64_t)kChunk * c);
-                mbar_arrive_expect_tx(full, 49152);
-                tma_load_3d(kq + 0, &tm_k, full, 0, h, t0);
-                tma_load_3d(kq + 16384, &tm_k, full, 64, h, t0);
-                tma_load_3d(kq + 8192, &tm_q, full, 0, h, t0);
-                tma_load_3d(kq + 24576, &tm_q, full, 64, h, t0);
-                tma_load_3d(wn + 0, &tm_g, full, 0, h, t0);
-                tma_load_3d(wn + 8192, &tm_g, full, 64, h, t0);
-            };
-            auto issue_v = [&](int c) {
-                const int t0 = (int)(seq0 + (int64_t)kChunk * c);
-                mbar_arrive_expect_tx(&bars[B_VFULL], 16384);
-                tma_load_3d(sm + OFF_V, &tm_v, &bars[B_VFULL], 0, h, t0);
-                tma_load_3d(sm + OFF_V + 8192, &tm_v, &bars[B_VFULL], 64, h, t0);
-            };
             issue_kqg(0);
             issue_v(0);
             if (nchunks > 1) issue_kqg(1);
-            int next_kqg = 2, next_v = 1;
-            long long last = clock64();
-            while ((next_kqg < nchunks || next_v < nchunks) && !*abort_flag) {
-                bool prog = false;
-                if (next_v < nchunks && mbar_try_wait(&bars[B_VFREE], (next_v - 1) & 1)) {
-                    issue_v(next_v++);
-                    prog = true;
-                }
-                if (next_kqg < nchunks &&
-                    mbar_try_wait(&bars[B_SLOTFREE0 + (next_kqg & 1)], ((next_kqg - 2) >> 1) & 1)) {
-                    issue_kqg(next_kqg++);
-                    prog = true;
-                }
-                if (prog) {
-                    last = clock64();
-                } else if (clock64() - last > kWaitLimit) {
-                    *abort_flag = 1;
-                    report_status(p.status, kStatusTimeout);
-                }
-            }
-            if (*abort_flag) {
-                // drain: let every issued copy land before the CTA can exit
-                const int issued[2] = {(next_kqg + 1) / 2, next_kqg / 2};
-                for (int s = 0; s < 2; ++s)
-                    if (issued[s] > 0) mbar_wait(&bars[B_FULL0 + s], (issued[s] - 1) & 1, kWaitLimit);
-                mbar_wait(&bars[B_VFULL], (next_v - 1) & 1, kWaitLimit);
-            }
-        }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t rS = tmem + T_S, rO = tmem + T_O, rU = tmem + T_U, rP = tmem + T_P;
-            const uint32_t rSA = tmem + T_SA, rUH = tmem + T_UH, rUL = tmem + T_UL;
-            const uint32_t a_kq[2] = {saddr(sm + OFF_KQ0), saddr(sm + OFF_KQ1)};
-            const uint32_t a_kmh[2] = {saddr(sm + OFF_KMH0), saddr(sm + OFF_KMH1)};
-            const uint32_t a_p[2] = {saddr(sm + OFF_P0), saddr(sm + OFF_P1)};
-            const uint32_t a_wn[2] = {saddr(sm + OFF_WN0), saddr(sm + OFF_WN1)};
-            const uint32_t a_tb[2] = {saddr(sm + OFF_TB0), saddr(sm + OFF_TB1)};
+            const uint32_t rP = tmem + T_P;
             const uint32_t a_kml = saddr(sm + OFF_KML), a_v = saddr(sm + OFF_V);
             const uint32_t id_kk64 = idesc_bf16(128, 64, false, false);
             const uint32_t id_mk64 = idesc_bf16(128, 64, true, false);
-            const uint32_t id_km64 = idesc_bf16(128, 64, false, true);
-            const uint32_t id_km128 = idesc_bf16(128, 128, false, true);
-            int c1 = 0, c2 = 0, c3 = 0, c4 = 0, c56 = 0;
-            long long last = clock64();
-            while (c56 < nchunks && !*abort_flag) {
-                bool prog = false;
-                // M5 + M6: O^T += U^T P^T (3 split terms), X += U^T K_m (2 split terms)
-                if (c56 < c4 && mbar_try_wait(&bars[B_UREADY], c56 & 1)) {
-                    tc_fence_after();
-                    const int s = c56 & 1;
-                    for (int j = 0; j < 4; ++j)
-                        mma_ts(rO, rUH + 8 * j, smem_desc(a_p[s] + 32 * j, 16, 1024), id_kk64, 1);
-                    for (int j = 0; j < 4; ++j)
-                        mma_ts(rO, rUL + 8 * j, smem_desc(a_p[s] + 32 * j, 16, 1024), id_kk64, 1);
-                    for (int j = 0; j < 4; ++j)
-                        mma_ts(rO, rUH + 8 * j, smem_desc(a_p[s] + 8192 + 32 * j, 16, 1024),
-                               id_kk64, 1);
-                    for (int j = 0; j < 4; ++j)
-                        mma_ts(rS, rUH + 8 * j, smem_desc(a_kmh[s] + 2048 * j, 8192, 1024),
-                               id_km128, 1);
-                    for (int j = 0; j < 4; ++j)
-                        mma_ts(rS, rUL + 8 * j, smem_desc(a_kmh[s] + 2048 * j, 8192, 1024),
-                               id_km128, 1);
-                    mma_commit(&bars[B_OSDONE]);
-                    mma_commit(&bars[B_SLOTFREE0 + s]);
-                    ++c56;
-                    prog = true;
-                }
-                // M4: O^T = X Q_r^T, U^T += X (-W)^T
-                if (c4 < c3 && c4 == c56 &&
-                    mbar_try_wait(&bars[B_WN0 + (c4 & 1)], (c4 >> 1) & 1) &&
-                    mbar_try_wait(&bars[B_SREADY], c4 & 1)) {
-                    tc_fence_after();
-                    const int s = c4 & 1;
-                    for (int j = 0; j < 8; ++j)
-                        mma_ts(rO, rSA + 8 * j,
-                               smem_desc(a_kq[s] + 8192 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
-                               id_kk64, j > 0);
-                    for (int j = 0; j < 8; ++j)
-                        mma_ts(rU, rSA + 8 * j, smem_desc(a_wn[s] + 2048 * j, 16384, 1024), id_km64,
-                               1);
-                    mma_commit(&bars[B_XDONE]);
-                    ++c4;
-                    prog = true;
-                }
-                // M3: U_bar^T = V^T (T diag(beta))^T
-                if (c3 < c2 && c3 <= c56 && mbar_try_wait(&bars[B_VFULL], c3 & 1)) {
-                    const int s = c3 & 1;
-                    for (int j = 0; j < 4; ++j)
-                        mma_ss(rU, smem_desc(a_v + 2048 * j, 8192, 1024),
-                               smem_desc(a_tb[s] + 32 * j, 16, 1024), id_mk64, j > 0);
-                    mma_commit(&bars[B_VFREE]);
-                    ++c3;
-                    prog = true;
-                }
-                // M2: W^T = K_p^T (T diag(beta))^T
-                if (c2 < c1 && mbar_try_wait(&bars[B_TB0 + (c2 & 1)], (c2 >> 1) & 1)) {
-                    tc_fence_after();
-                    const int s = c2 & 1;
-                    for (int j = 0; j < 4; ++j)
-                        mma_ss(rP, smem_desc(a_kq[s] + 2048 * j, 16384, 1024),
-                               smem_desc(a_tb[s] + 32 * j, 16, 1024), id_mk64, j > 0);
-                    mma_commit(&bars[B_WDONE0 + s]);
-                    ++c2;
-                    prog = true;
-                }
+            int v_issued = 1;
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c & 1;
                 // M1: [K_p ; Q_r] (K_m hi + K_m lo)^T
-                if (c1 < nchunks && c1 <= c2 &&
-                    mbar_try_wait(&bars[B_FACT0 + (c1 & 1)], (c1 >> 1) & 1)) {
-                    tc_fence_after();
-                    const int s = c1 & 1;
-                    for (int j = 0; j < 8; ++j)
-                        mma_ss(rP, smem_desc(a_kq[s] + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
-                               smem_desc(a_kmh[s] + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024),
-                               id_kk64, j > 0);
-                    for (int j = 0; j < 8; ++j)
-                        mma_ss(rP, smem_desc(a_kq[s] + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
-                               smem_desc(a_kml + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024),
-                               id_kk64, 1);
-                    mma_commit(&bars[B_AP0 + s]);
-                    ++c1;
-                    prog = true;
-                }
-                if (prog) {
-                    last = clock64();
-                } else if (clock64() - last > kWaitLimit) {
-                    *abort_flag = 1;
-                    report_status(p.status, kStatusTimeout);
+                if (!wait_bar(&bars[B_FACT0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                for (int j = 0; j < 8; ++j)
+                    mma_ss(rP, smem_desc(a_kq[s] + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
+                           smem_desc(a_kmh[s] + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024), id_kk64,
+                           j > 0);
+                for (int j = 0; j < 8; ++j)
+                    mma_ss(rP, smem_desc(a_kq[s] + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
+                           smem_desc(a_kml + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024), id_kk64, 1);
+                mma_commit(&bars[B_AP0 + s]);
+                // M2: W^T = K_p^T (T diag(beta))^T
+                if (!wait_bar(&bars[B_TB0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                for (int j = 0; j < 4; ++j)
+                    mma_ss(rP, smem_desc(a_kq[s] + 2048 * j, 16384, 1024),
+                           smem_desc(a_tb[s] + 32 * j, 16, 1024), id_mk64, j > 0);
+                mma_commit(&bars[B_WDONE0 + s]);
+                // M3: U_bar^T = V^T (T diag(beta))^T into this chunk's U^T buffer, once the
+                // epilogue has read that buffer two chunks ago and v has landed.  (A per-slot
+                // barrier: a single one could run two phases ahead of this wait.)
+                if (c >= 2 &&
+                    !wait_bar(&bars[B_UFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
+                    break;
+                if (!wait_bar(&bars[B_VFULL], c & 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                const uint32_t rU = tmem + (s ? T_U1 : T_U0);
+                for (int j = 0; j < 4; ++j)
+                    mma_ss(rU, smem_desc(a_v + 2048 * j, 8192, 1024),
+                           smem_desc(a_tb[s] + 32 * j, 16, 1024), id_mk64, j > 0);
+                mma_commit(&bars[B_VFREE0 + s]);
+                // the v buffer is free once M3 has read it: load the next chunk's v
+                if (c + 1 < nchunks) {
+                    if (!wait_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                    issue_v(c + 1);
+                    v_issued = c + 2;
                 }
             }
-            // every issued MMA completes before TMEM can be released
             mma_commit(&bars[B_DRAIN]);
             mbar_wait(&bars[B_DRAIN], 0, kWaitLimit);
+            if (*abort_flag) {  // let every issued copy land before the CTA can exit
+                mbar_wait(&bars[B_VFULL], (v_issued - 1) & 1, kWaitLimit);
+                const int nk = *kqg_issued;
+                for (int c = nk - 2; c < nk; ++c)
+                    if (c >= 0) mbar_wait(&bars[B_FULL0 + (c & 1)], (c >> 1) & 1, kWaitLimit);
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ serial MMA issuer
+        if (lane == 0) {
+            const uint32_t rS = tmem + T_S, rO = tmem + T_O;
+            const uint32_t rSA = tmem + T_SA, rUH = tmem + T_UH, rUL = tmem + T_UL;
+            const uint32_t id_kk64 = idesc_bf16(128, 64, false, false);
+            const uint32_t id_km64 = idesc_bf16(128, 64, false, true);
+            const uint32_t id_km128 = idesc_bf16(128, 128, false, true);
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c & 1;
+                const uint32_t rU = tmem + (s ? T_U1 : T_U0);
+                // M4: O^T = X Q_r^T, U^T += X (-W)^T
+                if (!wait_bar(&bars[B_WN0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                if (!wait_bar(&bars[B_SREADY], c & 1, abort_flag, p.status)) break;
+                if (!wait_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                for (int j = 0; j < 8; ++j)
+                    mma_ts(rO, rSA + 8 * j,
+                           smem_desc(a_kq[s] + 8192 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
+                           id_kk64, j > 0);
+                for (int j = 0; j < 8; ++j)
+                    mma_ts(rU, rSA + 8 * j, smem_desc(a_wn[s] + 2048 * j, 16384, 1024), id_km64, 1);
+                mma_commit(&bars[B_XDONE]);
+                // M5 + M6: O^T += U^T P^T (3 split terms), X += U^T K_m (2 split terms)
+                if (!wait_bar(&bars[B_UREADY], c & 1, abort_flag, p.status)) break;
+                tc_fence_after();
+                for (int j = 0; j < 4; ++j)
+                    mma_ts(rO, rUH + 8 * j, smem_desc(a_p[s] + 32 * j, 16, 1024), id_kk64, 1);
+                for (int j = 0; j < 4; ++j)
+                    mma_ts(rO, rUL + 8 * j, smem_desc(a_p[s] + 32 * j, 16, 1024), id_kk64, 1);
+                for (int j = 0; j < 4; ++j)
+                    mma_ts(rO, rUH + 8 * j, smem_desc(a_p[s] + 8192 + 32 * j, 16, 1024), id_kk64, 1);
+                for (int j = 0; j < 4; ++j)
+                    mma_ts(rS, rUH + 8 * j, smem_desc(a_kmh[s] + 2048 * j, 8192, 1024), id_km128, 1);
+                for (int j = 0; j < 4; ++j)
+                    mma_ts(rS, rUL + 8 * j, smem_desc(a_kmh[s] + 2048 * j, 8192, 1024), id_km128, 1);
+                mma_commit(&bars[B_OSDONE]);
+            }
+            // every issued MMA completes before TMEM can be released
+            mma_commit(&bars[B_SPARE]);
+            mbar_wait(&bars[B_SPARE], 0, kWaitLimit);
         }
     } else if (warp < kWarpEpi0) {
         // ------------------------------------------------------------ prep (warps 2-9)
         const int tp = tid - kWarpPrep0 * 32;
-        const int ch = tp & 127;
-        const int half = tp >> 7;
+        const int cg = tp & 15;         // channel group of the factor pass
+        const int tg = tp >> 4;         // token group of the factor pass
+        const int c8 = 8 * cg;
+        const int wp = warp - kWarpPrep0;
         const int q4 = warp & 3;
         const int colhalf = (warp - kWarpPrep0) >> 2;
         const int row_abs = 32 * q4 + lane;
@@ -362,52 +418,98 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             unsigned char* wn = sm + (s ? OFF_WN1 : OFF_WN0);
             unsigned char* pt = sm + (s ? OFF_P1 : OFF_P0);
             unsigned char* tb = sm + (s ? OFF_TB1 : OFF_TB0);
-            float* ers = er + (c & 3) * kDim;
             if (!wait_bar(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
 
-            // ---- decay factors: two threads per key channel, 32 tokens each ----
+            // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7 ----
+            uint4 graw[4];
             {
-                float acc = 0.f;
-#pragma unroll 8
-                for (int i = 0; i < 32; ++i) {
-                    const int t = 32 * half + i;
-                    if (t < valid)
-                        acc += bf2f(*reinterpret_cast<const bf16*>(wn + sw128_offset(t, ch, 64)));
+                float gs[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) gs[j] = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = 4 * tg + i;
+                    graw[i] = t < valid ? *reinterpret_cast<const uint4*>(wn + sw128_offset(t, c8, 64))
+                                        : make_uint4(0u, 0u, 0u, 0u);
+                    float gv[8];
+                    unpack8(graw[i], gv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) gs[j] += gv[j];
                 }
-                part[half * kDim + ch] = acc;
+                *reinterpret_cast<float4*>(part + tg * kDim + c8) = make_float4(gs[0], gs[1], gs[2], gs[3]);
+                *reinterpret_cast<float4*>(part + tg * kDim + c8 + 4) = make_float4(gs[4], gs[5], gs[6], gs[7]);
                 if (tp < kChunk)
                     beta_s[tp] = tp < valid ? bf2f(p.beta[(tok0 + tp) * H + h]) : 0.f;
             }
             named_bar(kBarPrep, kPrepThreads);
+            if (tp < kDim) {  // exclusive prefix over the 16 token groups, and the chunk total
+                float run = 0.f;
+#pragma unroll
+                for (int g16 = 0; g16 < 16; ++g16) {
+                    const float v = part[g16 * kDim + tp];
+                    part[g16 * kDim + tp] = run;
+                    run += v;
+                }
+                gc_s[tp] = run;
+            }
+            named_bar(kBarPrep, kPrepThreads);
             {
-                const float GC = part[ch] + part[kDim + ch];
-                const float r = 0.5f * GC;
-                float G = half ? part[ch] : 0.f;
+                float G[8], r[8];
+                {
+                    const float4 a = *reinterpret_cast<const float4*>(part + tg * kDim + c8);
+                    const float4 b = *reinterpret_cast<const float4*>(part + tg * kDim + c8 + 4);
+                    const float4 ga = *reinterpret_cast<const float4*>(gc_s + c8);
+                    const float4 gb = *reinterpret_cast<const float4*>(gc_s + c8 + 4);
+                    G[0] = a.x; G[1] = a.y; G[2] = a.z; G[3] = a.w;
+                    G[4] = b.x; G[5] = b.y; G[6] = b.z; G[7] = b.w;
+                    r[0] = 0.5f * ga.x; r[1] = 0.5f * ga.y; r[2] = 0.5f * ga.z; r[3] = 0.5f * ga.w;
+                    r[4] = 0.5f * gb.x; r[5] = 0.5f * gb.y; r[6] = 0.5f * gb.z; r[7] = 0.5f * gb.w;
+                }
                 bool bad = false;
-#pragma unroll 4
-                for (int i = 0; i < 32; ++i) {
-                    const int t = 32 * half + i;
-                    const float gv =
-                        t < valid ? bf2f(*reinterpret_cast<const bf16*>(wn + sw128_offset(t, ch, 64)))
-                                  : 0.f;
-                    G += gv;
-                    const float d = G - r;
-                    bad |= fabsf(d) > kMaxExponentTC;
-                    const float e = exp2f(d * kLog2eTC);
-                    const float ei = exp2f(-d * kLog2eTC);
-                    bf16* pk = reinterpret_cast<bf16*>(kq + sw128_offset(t, ch, 128));
-                    bf16* pq = reinterpret_cast<bf16*>(kq + sw128_offset(64 + t, ch, 128));
-                    const float kv = bf2f(*pk), qv = bf2f(*pq);
-                    *pk = __float2bfloat16_rn(kv * e);
-                    *pq = __float2bfloat16_rn(qv * e);
-                    const float km = kv * ei;
-                    const bf16 kmh_v = __float2bfloat16_rn(km);
-                    const uint32_t om = sw128_offset(t, ch, 64);
-                    *reinterpret_cast<bf16*>(kmh + om) = kmh_v;
-                    *reinterpret_cast<bf16*>(kml + om) = __float2bfloat16_rn(km - bf2f(kmh_v));
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = 4 * tg + i;
+                    float gv[8], kv[8], qv[8];
+                    unpack8(graw[i], gv);
+                    uint4* pk = reinterpret_cast<uint4*>(kq + sw128_offset(t, c8, 128));
+                    uint4* pq = reinterpret_cast<uint4*>(kq + sw128_offset(64 + t, c8, 128));
+                    unpack8(*pk, kv);
+                    unpack8(*pq, qv);
+                    float kp[8], qr[8], km[8], kmlo[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        G[j] += gv[j];
+                        const float d = (G[j] - r[j]) * kLog2eTC;
+                        bad |= fabsf(d) > kMaxExponentTC * kLog2eTC;
+                        const float e = ex2_approx(d);
+                        const float ei = ex2_approx(-d);
+                        kp[j] = kv[j] * e;
+                        qr[j] = qv[j] * e;
+                        km[j] = kv[j] * ei;
+                    }
+                    const uint4 kmh_v = pack8(km);
+                    float kmh_f[8];
+                    unpack8(kmh_v, kmh_f);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) kmlo[j] = km[j] - kmh_f[j];
+                    *pk = pack8(kp);
+                    *pq = pack8(qr);
+                    const uint32_t om = sw128_offset(t, c8, 64);
+                    *reinterpret_cast<uint4*>(kmh + om) = kmh_v;
+                    *reinterpret_cast<uint4*>(kml + om) = pack8(kmlo);
                 }
                 if (bad) report_status(p.status, kStatusDecayRange);
-                if (half == 0) ers[ch] = exp2f(r * kLog2eTC);
+                if (tg == 0) {
+                    float* ers = er + (c & 3) * kDim + c8;
+                    float* scs = sc + (c & 3) * kDim + c8;
+                    const float* erp = er + ((c + 3) & 3) * kDim + c8;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float e = ex2_approx(r[j] * kLog2eTC);
+                        ers[j] = e;
+                        scs[j] = c > 0 ? erp[j] * e : e;
+                    }
+                }
             }
             fence_async_shared();
             named_bar(kBarPrep, kPrepThreads);
@@ -474,41 +576,63 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 for (int i = 0; i < 16; ++i) Tb[i * LDA_T + col] = x[i];
             }
             named_bar(kBarPrep, kPrepThreads);
-            // ---- off-diagonal blocks: T_IJ = -T_II sum_{K=J}^{I-1} A_IK T_KJ ----
-            for (int I = 1; I < 4; ++I) {
-                for (int e = tp; e < I * 256; e += kPrepThreads) {
-                    const int J = e >> 8, i = (e >> 4) & 15, j = e & 15;
-                    float y = 0.f;
-                    for (int K = J; K < I; ++K) {
-                        const float* Arow = Am + (16 * I + i) * LDA_T + 16 * K;
-                        const float* Tcol = Am + (16 * K) * LDA_T + 16 * J + j;
-#pragma unroll
-                        for (int x = 0; x < 16; ++x) y = fmaf(Arow[x], Tcol[x * LDA_T], y);
-                    }
-                    Y[e] = y;
-                }
-                named_bar(kBarPrep, kPrepThreads);
-                for (int e = tp; e < I * 256; e += kPrepThreads) {
-                    const int J = e >> 8, i = (e >> 4) & 15, j = e & 15;
-                    const float* Trow = Am + (16 * I + i) * LDA_T + 16 * I;
-                    const float* Ycol = Y + J * 256 + j;
-                    float y = 0.f;
-#pragma unroll
-                    for (int x = 0; x < 16; ++x) y = fmaf(Trow[x], Ycol[x * 16], y);
-                    Am[(16 * I + i) * LDA_T + 16 * J + j] = -y;
-                }
-                named_bar(kBarPrep, kPrepThreads);
+            // ---- off-diagonal blocks on the tensor cores (tf32), with D = blockdiag(T_II) and
+            //      N = D A_off (block-nilpotent):  T = (I - N + N^2 - N^3) D ----
+            if (wp < 6) {  // N_IJ = T_II A_IJ, in place of A_IJ
+                const int I = pair_i(wp), J = pair_j(wp);
+                float acc[2][4];
+                block_product(acc, Am + (16 * I) * LDA_T + 16 * I, LDA_T, 1.f, nullptr, 0,
+                              Am + (16 * I) * LDA_T + 16 * J, LDA_T, lane);
+                __syncwarp();
+                store_block(Am + (16 * I) * LDA_T + 16 * J, LDA_T, acc, lane);
             }
-            // ---- T diag(beta) as the bf16 K-major operand ----
-            for (int e = tp; e < kChunk * 8; e += kPrepThreads) {
-                const int t = e >> 3, j8 = (e & 7) * 8;
-                uint32_t w[4];
+            named_bar(kBarPrep, kPrepThreads);
+            if (wp < 3) {  // N^2_20, N^2_31 (then N^3_30 = N^2_31 N_10), N^2_30
+                float acc[2][4];
+                if (wp == 0) {
+                    block_product(acc, Am + 32 * LDA_T + 16, LDA_T, 1.f, nullptr, 0,
+                                  Am + 16 * LDA_T, LDA_T, lane);
+                    store_block(Y + 0 * 256, 16, acc, lane);
+                } else if (wp == 1) {
+                    block_product(acc, Am + 48 * LDA_T + 32, LDA_T, 1.f, nullptr, 0,
+                                  Am + 32 * LDA_T + 16, LDA_T, lane);
+                    store_block(Y + 1 * 256, 16, acc, lane);
+                    __syncwarp();
+                    block_product(acc, Y + 1 * 256, 16, 1.f, nullptr, 0, Am + 16 * LDA_T, LDA_T,
+                                  lane);
+                    store_block(Y + 3 * 256, 16, acc, lane);
+                } else {
+                    block_product(acc, Am + 48 * LDA_T + 16, LDA_T, 1.f, nullptr, 0,
+                                  Am + 16 * LDA_T, LDA_T, lane);
+                    block_product_acc(acc, Am + 48 * LDA_T + 32, LDA_T, Am + 32 * LDA_T, LDA_T, lane);
+                    store_block(Y + 2 * 256, 16, acc, lane);
+                }
+            }
+            named_bar(kBarPrep, kPrepThreads);
+            if (wp < 6) {  // T_IJ = C_IJ T_JJ with C = -N + N^2 - N^3 (block by block)
+                const int I = pair_i(wp), J = pair_j(wp);
+                const float* n2 = (I == 2 && J == 0) ? Y : (I == 3 && J == 1) ? Y + 256
+                                : (I == 3 && J == 0) ? Y + 512 : nullptr;
+                const float* n3 = (I == 3 && J == 0) ? Y + 768 : nullptr;
+                float acc[2][4];
+                block_product(acc, Am + (16 * I) * LDA_T + 16 * J, LDA_T, -1.f, n2, n3,
+                              Am + (16 * J) * LDA_T + 16 * J, LDA_T, lane);
+                __syncwarp();
+                store_block(Am + (16 * I) * LDA_T + 16 * J, LDA_T, acc, lane);
+            }
+            named_bar(kBarPrep, kPrepThreads);
+            // ---- T diag(beta) as the bf16 K-major operand (two 8-column pieces per thread) ----
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    w[u] = pack_bf16(Am[t * LDA_T + j8 + 2 * u] * beta_s[j8 + 2 * u],
-                                     Am[t * LDA_T + j8 + 2 * u + 1] * beta_s[j8 + 2 * u + 1]);
+            for (int rep = 0; rep < 2; ++rep) {
+                const int e = tp + rep * kPrepThreads;
+                const int t = e >> 3, j8 = (e & 7) * 8;
+                const float4 a0 = *reinterpret_cast<const float4*>(Am + t * LDA_T + j8);
+                const float4 a1 = *reinterpret_cast<const float4*>(Am + t * LDA_T + j8 + 4);
+                const float4 b0 = *reinterpret_cast<const float4*>(beta_s + j8);
+                const float4 b1 = *reinterpret_cast<const float4*>(beta_s + j8 + 4);
                 *reinterpret_cast<uint4*>(tb + sw128_offset(t, j8, 64)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
+                    make_uint4(pack_bf16(a0.x * b0.x, a0.y * b0.y), pack_bf16(a0.z * b0.z, a0.w * b0.w),
+                               pack_bf16(a1.x * b1.x, a1.y * b1.y), pack_bf16(a1.z * b1.z, a1.w * b1.w));
             }
             fence_async_shared();
             named_bar(kBarPrep, kPrepThreads);
@@ -570,56 +694,59 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             // ---- E1: U^T -> bf16 hi/lo A operands ----
             if (!(ok = wait_bar(&bars[B_XDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
-            {
-                uint32_t u[32], hi[32], lo[32];
 #pragma unroll
-                for (int g2 = 0; g2 < 2; ++g2) {
-                    tmem_ld32(tmem + T_U + 32 * g2 + lane_off, u);
+            for (int g2 = 0; g2 < 2; ++g2) {
+                uint32_t u[32], hi[16], lo[16];
+                tmem_ld32(tmem + ((c & 1) ? T_U1 : T_U0) + 32 * g2 + lane_off, u);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float x0 = __uint_as_float(u[2 * j]), x1 = __uint_as_float(u[2 * j + 1]);
-                        const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                        hi[16 * g2 + j] = pack_bf16(bf2f(h0), bf2f(h1));
-                        lo[16 * g2 + j] = pack_bf16(x0 - bf2f(h0), x1 - bf2f(h1));
-                    }
+                for (int j = 0; j < 16; ++j) {
+                    const float x0 = __uint_as_float(u[2 * j]), x1 = __uint_as_float(u[2 * j + 1]);
+                    hi[j] = pack_bf16(x0, x1);
+                    lo[j] = pack_bf16(x0 - __uint_as_float(hi[j] << 16),
+                                      x1 - __uint_as_float(hi[j] & 0xffff0000u));
                 }
-                tmem_st32(tmem + T_UH + lane_off, hi);
-                tmem_st32(tmem + T_UL + lane_off, lo);
-                tmem_st_wait();
+                tmem_st16(tmem + T_UH + 16 * g2 + lane_off, hi);
+                tmem_st16(tmem + T_UL + 16 * g2 + lane_off, lo);
             }
+            tmem_st_wait();
             tc_fence_before();
             named_bar(kBarEpi, kEpiThreads);
-            if (te == 0) mbar_arrive(&bars[B_UREADY]);
+            if (te == 0) {
+                mbar_arrive(&bars[B_UREADY]);
+                mbar_arrive(&bars[B_UFREE0 + (c & 1)]);
+            }
 
             // ---- E2: O to HBM, state rescale ----
             if (!(ok = wait_bar(&bars[B_OSDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
+            // every MMA that reads slot c & 1 has completed: refill it with chunk c + 2
+            if (te == 0 && c + 2 < nchunks) issue_kqg(c + 2);
             {
-                uint32_t o[32];
+                uint32_t o[64];
+                tmem_ld64(tmem + T_O + lane_off, o);
+                bf16* op = p.out + (tok0 * H + h) * kDim + vch;
+                const int64_t tstride = (int64_t)H * kDim;
 #pragma unroll
-                for (int g2 = 0; g2 < 2; ++g2) {
-                    tmem_ld32(tmem + T_O + 32 * g2 + lane_off, o);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int t = 32 * g2 + j;
-                        if (t < valid)
-                            p.out[((tok0 + t) * H + h) * kDim + vch] =
-                                __float2bfloat16_rn(__uint_as_float(o[j]));
-                    }
-                }
+                for (int t = 0; t < 64; ++t)
+                    if (t < valid) op[t * tstride] = __float2bfloat16_rn(__uint_as_float(o[t]));
             }
-            const float* ec = er + (c & 3) * kDim;
             if (c + 1 < nchunks) {
                 if (!(ok = wait_bar(&bars[B_FACT0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, abort_flag,
                                     p.status)))
                     break;
-                const float* en = er + ((c + 1) & 3) * kDim;
+                const float* scn = sc + ((c + 1) & 3) * kDim;
+#pragma unroll
                 for (int cc = 0; cc < kDim; cc += 32) {
                     uint32_t x[32], xb[16];
                     tmem_ld32(tmem + T_S + cc + lane_off, x);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        x[j] = __float_as_uint(__uint_as_float(x[j]) * (ec[cc + j] * en[cc + j]));
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 f = *reinterpret_cast<const float4*>(scn + cc + j);
+                        x[j] = __float_as_uint(__uint_as_float(x[j]) * f.x);
+                        x[j + 1] = __float_as_uint(__uint_as_float(x[j + 1]) * f.y);
+                        x[j + 2] = __float_as_uint(__uint_as_float(x[j + 2]) * f.z);
+                        x[j + 3] = __float_as_uint(__uint_as_float(x[j + 3]) * f.w);
+                    }
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         xb[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
@@ -631,6 +758,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 named_bar(kBarEpi, kEpiThreads);
                 if (te == 0) mbar_arrive(&bars[B_SREADY]);
             } else if (p.final_state) {
+                const float* ec = er + (c & 3) * kDim;
                 float* fs = p.final_state + unit * (kDim * kDim);
                 for (int cc = 0; cc < kDim; cc += 32) {
                     uint32_t x[32];

@@ -56,6 +56,30 @@ def block_inverse_unit_lower(A: np.ndarray, block: int = 16) -> np.ndarray:
     return T
 
 
+def block_inverse_nilpotent(A: np.ndarray, block: int = 16) -> np.ndarray:
+    """(I + A)^{-1} in the form the prefill kernel evaluates it: the 16x16 diagonal blocks by
+    forward substitution, then with D = blockdiag((I + A_II)^{-1}) and N = D A_off (strictly
+    block-lower, so N^4 = 0 for four blocks): (I + A)^{-1} = (I - N + N^2 - N^3) D."""
+    C = A.shape[0]
+    nb = C // block
+    D = np.zeros_like(A)
+    for b in range(nb):
+        s = slice(b * block, (b + 1) * block)
+        Ab = A[s, s]
+        X = np.zeros((block, block))
+        for col in range(block):
+            for i in range(block):
+                X[i, col] = (1.0 if i == col else 0.0) - Ab[i, :i] @ X[:i, col]
+        D[s, s] = X
+    A_off = A.copy()
+    for b in range(nb):
+        s = slice(b * block, (b + 1) * block)
+        A_off[s, s] = 0.0
+    N = D @ A_off
+    I = np.eye(C)
+    return (I - N + N @ N - N @ N @ N) @ D
+
+
 def chunk_step(S, q, k, v, g, beta):
     """One chunk (rows beyond the sequence already zero-padded).  Returns (O, S_new)."""
     C = q.shape[0]

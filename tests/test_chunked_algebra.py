@@ -7,8 +7,8 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.chunked_restatement import (block_inverse_unit_lower, unit_forward,
-                                       unit_forward_segmented)
+from tests.chunked_restatement import (block_inverse_nilpotent, block_inverse_unit_lower,
+                                       unit_forward, unit_forward_segmented)
 
 
 def _inputs(L, d, seed, gate=0.1, dv=None):
@@ -42,6 +42,14 @@ def test_neumann_doubling_exact_for_16x16_strictly_lower():
         A = np.tril(rng.standard_normal((64, 64)) * 0.3, -1)
         T = block_inverse_unit_lower(A)
         _close(T, np.linalg.inv(np.eye(64) + A), 1e-11)
+
+
+def test_block_nilpotent_inverse_form():
+    """The kernel's form: diagonal blocks by substitution, then (I - N + N^2 - N^3) D."""
+    rng = np.random.default_rng(1)
+    for scale in (0.05, 0.3, 0.5):
+        A = np.tril(rng.standard_normal((64, 64)) * scale, -1)
+        _close(block_inverse_nilpotent(A), np.linalg.inv(np.eye(64) + A), 1e-10)
 
 
 @pytest.mark.parametrize("L", [1, 15, 16, 17, 63, 64, 65, 200])

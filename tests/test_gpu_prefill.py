@@ -20,11 +20,14 @@ def kda():
     return m
 
 
-def run_gpu(x, init=True, **kw):
+def run_gpu(x, init=True, expect_status=0, **kw):
     out, fin = kda().fwd_chunked(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
                                  x["cu_seqlens"], x["seqlens"],
                                  init_state=x["init_state"] if init else None, **kw)
     torch.cuda.synchronize()
+    if expect_status is not None:
+        st = kda().read_device_status()
+        assert st == expect_status, f"device status {st} (expected {expect_status})"
     return out, fin
 
 
@@ -165,8 +168,7 @@ def test_decay_range_is_reported():
     x = synth.make_inputs([64], 1, torch.bfloat16, seed=13, device=DEV)
     x["log_alpha"] = torch.full_like(x["log_alpha"], -6.0)  # 64 tokens: G_C = -384
     assert kda().read_device_status() == 0
-    run_gpu(x)
-    assert kda().read_device_status() == -6
+    run_gpu(x, expect_status=-6)
     assert kda().read_device_status() == 0  # cleared by the read
 
 
