@@ -216,6 +216,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip timing the long-context and varlen prefill workloads")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
@@ -300,6 +302,35 @@ def main():
                                "algorithmic_bytes_per_launch": dbytes}}
         del dd, dout
 
+    # ---------------- the other prefill workloads (reported, not the headline) ------------
+    extra = None
+    if not args.no_extra:
+        extra = {}
+        for key in ("long_256k", "varlen_64"):
+            we = synth.workloads()[key]
+            xe = synth.make_workload(we, device=dev)
+            oute = torch.empty_like(xe["q"])
+            fine = torch.empty((len(we.lengths), we.heads, D, D), dtype=torch.float32, device=dev)
+            wse = torch.empty(max(1, kda.fwd_workspace_bytes(xe["seqlens"], we.heads)),
+                              dtype=torch.uint8, device=dev)
+
+            def estep_x():
+                kda.fwd_chunked(xe["q"], xe["k"], xe["v"], xe["log_alpha"], xe["beta"],
+                                xe["cu_seqlens"], xe["seqlens"], init_state=xe["init_state"],
+                                out=oute, final_state=fine, workspace=wse)
+
+            for _ in range(2):
+                estep_x()
+            k_x = max(2, min(args.steps, 5))
+            ms_x = max_over_ranks(time_device(estep_x, k_x, stream), world)
+            Tx = xe["q"].shape[0]
+            bytes_x = Tx * we.heads * BYTES_PER_TOKEN_HEAD + len(we.lengths) * we.heads * 2 * STATE_BYTES
+            extra[key] = {"workload": we.name, "tokens": Tx, "ms_per_step": ms_x, "steps": k_x,
+                          "value": Tx * world / (ms_x * 1e-3) / 1e6, "unit": "Mtokens/s",
+                          "hbm_frac_of_roofline": bytes_x / (ms_x * 1e-3) / 1e9 / hbm_peak,
+                          "plan": kda.fwd_plan(xe["seqlens"], we.heads)}
+            del xe, oute, fine, wse
+
     # ---------------- end to end (host buffers, copies inside the timed region) ------------
     e2e = None
     if not args.no_e2e:
@@ -355,7 +386,7 @@ def main():
                        "l2": "inputs larger than L2 (%.2f GB read per step)" % (alg_bytes / 1e9)},
             "roofline": roofline, "cpu_baseline": cpu_base, "e2e": e2e,
             "clocks": getattr(clk, "result", None), "gpu_launches": launches,
-            "decode": decode,
+            "decode": decode, "other_prefill_workloads": extra,
         }
         print(json.dumps(line), flush=True)
     barrier(world)

@@ -5,10 +5,12 @@ The compute lives in a C-ABI shared library of hand-written sm_103a CUDA kernels
 argument marshalling only, every step of the operator runs in the library's kernels.
 The library is loaded lazily on first use and its absence is an error, never a fallback.
 """
+from . import binding  # noqa: F401
 from .binding import (  # noqa: F401
     KdaError,
     decode_step,
     fwd_chunked,
+    fwd_plan,
     fwd_workspace_bytes,
     launch_count,
     library_path,

@@ -1,5 +1,6 @@
 // kda_api.cu — the C ABI declared in include/kda.h: host-side checks, the work plan, the
 // sticky device status word, and the kernel launches.  No allocation happens here.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -61,13 +62,21 @@ kda_status kda_fwd_plan(const kda_desc* desc, kda_plan_info* info) {
     if (st != KDA_OK) return st;
     kda_plan_info p = {};
     p.chunk_size = kda::kChunk;
-    p.segment_chunks = 0;
+    p.segment_chunks = kda::kSegChunks;
+    int64_t slots = 0;
     for (int32_t n = 0; n < desc->num_seqs; ++n) {
         const int64_t L = desc->host_seqlens[n];
+        const int ns = kda::num_segments(L);
         p.chunks += (L + kda::kChunk - 1) / kda::kChunk;
-        p.work_items += 1;
+        p.work_items += ns;
+        if (ns > 1) {
+            p.split_sequences += 1;
+            slots += ns;
+        }
     }
-    p.workspace_bytes = 0;
+    // three fp32 arrays [slots][H][128][128], each 256-byte aligned
+    const size_t per = (size_t)slots * desc->num_heads * 128 * 128 * sizeof(float);
+    p.workspace_bytes = slots ? 3 * per : 0;
     *info = p;
     return KDA_OK;
 }
@@ -93,15 +102,25 @@ kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, c
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
         !aligned16(out) || !aligned16(init_state) || !aligned16(final_state))
         return KDA_ERR_INVALID_ARG;
-    if (plan.workspace_bytes > 0 && (!workspace || workspace_bytes < plan.workspace_bytes))
+    if (plan.workspace_bytes > 0 && (!workspace || workspace_bytes < plan.workspace_bytes ||
+                                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
         return KDA_ERR_WORKSPACE;
     int* status = status_word();
     if (!status) return KDA_ERR_CUDA;
     uint64_t launches = 0;
     cudaError_t e;
+    kda::SegWorkspace ws = {nullptr, nullptr, nullptr, 1};
+    if (plan.workspace_bytes > 0) {
+        const size_t per = plan.workspace_bytes / 3;
+        ws.tilde = static_cast<float*>(workspace);
+        ws.trans = reinterpret_cast<float*>(static_cast<char*>(workspace) + per);
+        ws.in = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * per);
+        for (int32_t n = 0; n < desc->num_seqs; ++n)
+            ws.max_segments = std::max(ws.max_segments, kda::num_segments(desc->host_seqlens[n]));
+    }
     if (desc->in_dtype == KDA_BF16)
         e = kda::launch_prefill_tc(desc->num_seqs, desc->num_heads, desc->total_tokens, q, k, v,
-                                   log_alpha, beta, init_state, cu_seqlens, out, final_state,
+                                   log_alpha, beta, init_state, cu_seqlens, out, final_state, ws,
                                    status, (cudaStream_t)stream, &launches);
     else
         e = kda::launch_prefill(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v,

@@ -12,6 +12,16 @@ namespace kda {
 constexpr int kDim = 128;     // d_k = d_v
 constexpr int kChunk = 64;    // tokens per chunk of the prefill path
 
+// Segment plan of the prefill (intra-device context parallelism).  A sequence longer than
+// kSplitChunks chunks is cut into segments of kSegChunks chunks; the plan depends on the
+// sequence's own length only, so packing never changes a sequence's results.
+constexpr int kSegChunks = 128;
+constexpr int kSplitChunks = 256;
+__host__ __device__ __forceinline__ int num_segments(int64_t len) {
+    const int64_t nc = (len + kChunk - 1) / kChunk;
+    return nc > kSplitChunks ? (int)((nc + kSegChunks - 1) / kSegChunks) : 1;
+}
+
 // Device status codes written into the sticky status word (same values as kda_status).
 constexpr int kStatusDecayRange = KDA_ERR_DECAY_RANGE;
 constexpr int kStatusTimeout = KDA_ERR_TIMEOUT;
@@ -56,9 +66,18 @@ cudaError_t launch_prefill(int dtype, int num_seqs, int heads, const void* q, co
                            float* final_state, int* status, cudaStream_t stream,
                            uint64_t* launches);
 
+// Workspace of the segmented prefill: three arrays of [slots][H][128][128] fp32 (segment
+// states from zero, segment transitions, composed incoming states).
+struct SegWorkspace {
+    float* tilde;
+    float* trans;
+    float* in;
+    int max_segments;  // 1 when no sequence is split (the workspace is then unused)
+};
+
 cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, const void* q,
                               const void* k, const void* v, const void* g, const void* beta,
                               const float* init_state, const int32_t* cu_seqlens, void* out,
-                              float* final_state, int* status, cudaStream_t stream,
-                              uint64_t* launches);
+                              float* final_state, const SegWorkspace& ws, int* status,
+                              cudaStream_t stream, uint64_t* launches);
 }  // namespace kda

@@ -25,8 +25,8 @@
 // the A operand, so no state byte goes through shared memory.  Every operand tile is used in
 // the layout TMA or the producing warp writes naturally (K-major or MN-major 128B-swizzled).
 //
-// Precision: P, U and K_m enter the tensor core as two bf16 terms (hi + lo), which removes
-// their rounding from the heavy tail of the output error; everything accumulates in fp32.
+// Precision: P and U enter the tensor core as two bf16 terms (hi + lo), which removes their
+// rounding from the heavy tail of the output error; everything accumulates in fp32.
 //
 // Every wait is bounded; on expiry the CTA records KDA_ERR_TIMEOUT and drains.
 #include <cudaTypedefs.h>
@@ -57,18 +57,21 @@ constexpr float kMaxExponentTC = 80.f;
 constexpr int LDA_T = 68;       // fp32 row stride of the 64 x 64 A / T matrix
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
-constexpr uint32_t OFF_KQ0 = 0;          // [K_p ; Q_r] slot 0: 128 rows x 128 cols (32 KB)
-constexpr uint32_t OFF_KQ1 = 32768;      // slot 1
-constexpr uint32_t OFF_KMH0 = 65536;     // K_m hi slot 0: 64 x 128 (16 KB)
-constexpr uint32_t OFF_KMH1 = 81920;     // slot 1
-constexpr uint32_t OFF_V = 98304;        // v: 64 x 128 (16 KB)
-constexpr uint32_t OFF_P0 = 114688;      // P hi (8 KB) + P lo (8 KB), slot 0
-constexpr uint32_t OFF_P1 = 131072;      // slot 1
-constexpr uint32_t OFF_WN0 = 147456;     // g (as loaded), then -W^T: 128 x 64 (16 KB), slot 0
-constexpr uint32_t OFF_WN1 = 163840;     // slot 1
+// Slot tile [K_p ; Q_r ; g -> -W]: 192 rows x 128 cols, two column regions of 24 KB.  Rows
+// 0-127 are the A operand of the intra-chunk product, rows 64-191 the B operand of the
+// state product, rows 128-191 first hold g (as loaded) and then -W.
+constexpr int KQW_ROWS = 192;
+constexpr uint32_t KQW_REGION = KQW_ROWS * 128;   // 24576
+constexpr uint32_t OFF_KQW0 = 0;         // slot 0 (48 KB)
+constexpr uint32_t OFF_KQW1 = 49152;     // slot 1
+constexpr uint32_t OFF_KMH0 = 98304;     // K_m hi slot 0: 64 x 128 (16 KB)
+constexpr uint32_t OFF_KMH1 = 114688;    // slot 1
+constexpr uint32_t OFF_V = 131072;       // v: 64 x 128 (16 KB)
+constexpr uint32_t OFF_P0 = 147456;      // P hi (8 KB) + P lo (8 KB), slot 0
+constexpr uint32_t OFF_P1 = 163840;      // slot 1
 constexpr uint32_t OFF_TB0 = 180224;     // T diag(beta): 64 x 64 (8 KB), slot 0
 constexpr uint32_t OFF_TB1 = 188416;     // slot 1
-constexpr uint32_t OFF_KML = 196608;     // K_m lo 64 x 128 (16 KB); after M1: A/T fp32 [64][68]
+constexpr uint32_t OFF_KML = 196608;     // A / T fp32 [64][68] of the 64 x 64 inverse
 constexpr uint32_t OFF_Y = OFF_KML + 17408;         // 4 x 16 x 16 fp32 blocks (N^2, N^3)
 constexpr uint32_t OFF_PART = OFF_Y + 4096;         // 16 x 128 fp32 token-group sums / prefixes
 constexpr uint32_t OFF_GC = OFF_PART + 8192;        // 128 fp32: chunk log-decay G_C
@@ -92,13 +95,10 @@ static_assert(B_COUNT <= NBAR, "barrier slots");
 
 // TMEM columns (512 allocated)
 constexpr uint32_t T_S = 0;      // X: fp32 state, lanes = value channel, cols = key channel
-constexpr uint32_t T_O = 128;    // O^T (64 cols)
-constexpr uint32_t T_U0 = 192;   // U^T, even chunks (64 cols)
+constexpr uint32_t T_X0 = 128;   // even chunks: [O^T (64) | U^T (64)]; U^T becomes bf16 hi|lo
 constexpr uint32_t T_P = 256;    // [A ; P] raw tiles, then W^T (64 cols)
 constexpr uint32_t T_SA = 320;   // bf16 copy of X (A operand, 64 cols)
-constexpr uint32_t T_UH = 384;   // bf16 U^T hi (A operand, 32 cols)
-constexpr uint32_t T_UL = 416;   // bf16 U^T lo (32 cols)
-constexpr uint32_t T_U1 = 448;   // U^T, odd chunks (64 cols)
+constexpr uint32_t T_X1 = 384;   // odd chunks
 
 struct TcParams {
     const bf16* beta;
@@ -107,8 +107,15 @@ struct TcParams {
     bf16* out;
     float* final_state;
     int* status;
+    float* ws_tilde;   // segment states from zero        [slots][H][128][128]
+    float* ws_trans;   // segment transitions             [slots][H][128][128]
+    float* ws_in;      // composed incoming states        [slots][H][128][128]
     int H;
+    int pass;          // 0: whole sequences + pass A of split ones; 1: pass B of split ones
 };
+
+// What one CTA does (chosen from the sequence length and blockIdx.z).
+enum { ITEM_WHOLE = 0, ITEM_TILDE = 1, ITEM_TRANS = 2, ITEM_SEGMENT = 3 };
 
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -189,6 +196,21 @@ __device__ __forceinline__ void store_block(float* D, int ld, const float (&acc)
             make_float2(acc[nt][2], acc[nt][3]);
     }
 }
+// Block (I, J) of T diag(beta) as bf16 into the 64 x 64 128B-swizzled operand tile.
+__device__ __forceinline__ void store_block_tb(unsigned char* tb, int I, int J,
+                                               const float (&acc)[2][4], const float* beta_s,
+                                               int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int col = 16 * J + 8 * nt + 2 * t;
+        const float b0 = beta_s[col], b1 = beta_s[col + 1];
+        *reinterpret_cast<uint32_t*>(tb + sw128_offset(16 * I + g, col, 64)) =
+            pack_bf16(acc[nt][0] * b0, acc[nt][1] * b1);
+        *reinterpret_cast<uint32_t*>(tb + sw128_offset(16 * I + g + 8, col, 64)) =
+            pack_bf16(acc[nt][2] * b0, acc[nt][3] * b1);
+    }
+}
 // block pairs (I, J), I > J, of the 4 x 4 block-lower 64 x 64 matrix, one per prep warp
 __device__ __forceinline__ int pair_i(int w) { return w < 1 ? 1 : (w < 3 ? 2 : 3); }
 __device__ __forceinline__ int pair_j(int w) { const int I = pair_i(w); return w - I * (I - 1) / 2; }
@@ -199,6 +221,24 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            *abort_flag = 1;
+            report_status(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+// Issuer threads poll with a short suspend-time hint: a plain try_wait is woken late when the
+// phase is completed by another thread's arrive, and a tight test_wait loop takes issue slots
+// from the compute warps sharing the sub-partition.
+__device__ __forceinline__ bool spin_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait_hint(bar, parity, 40)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitLimit) {
             *abort_flag = 1;
@@ -222,15 +262,55 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int n = blockIdx.x;
     const int h = blockIdx.y;
     const int H = p.H;
-    const int64_t seq0 = p.cu_seqlens[n];
-    const int L = p.cu_seqlens[n + 1] - (int)seq0;
+    const int64_t seq_begin = p.cu_seqlens[n];
+    const int64_t seq_len = p.cu_seqlens[n + 1] - seq_begin;
     const int64_t unit = (int64_t)n * H + h;
+    const int nseg = num_segments(seq_len);
+
+    // ---- work item of this CTA ----
+    int item;
+    int sigma = 0;
+    if (p.pass == 0) {
+        if (nseg == 1) {
+            if (blockIdx.z != 0) return;
+            item = ITEM_WHOLE;
+        } else {
+            sigma = blockIdx.z >> 1;
+            if (sigma >= nseg - 1) return;
+            item = (blockIdx.z & 1) ? ITEM_TRANS : ITEM_TILDE;
+        }
+    } else {
+        if (nseg == 1 || (int)blockIdx.z >= nseg) return;
+        sigma = blockIdx.z;
+        item = ITEM_SEGMENT;
+    }
+    const int64_t seg_tokens = (int64_t)kSegChunks * kChunk;
+    const int64_t seq0 = item == ITEM_WHOLE ? seq_begin : seq_begin + sigma * seg_tokens;
+    const int L = (int)(item == ITEM_WHOLE ? seq_len : min(seg_tokens, seq_len - sigma * seg_tokens));
+    int64_t slot = 0;  // workspace slot of (sequence, segment)
+    if (item != ITEM_WHOLE) {
+        int64_t base = 0;
+        for (int m = 0; m < n; ++m) {
+            const int ns = num_segments((int64_t)p.cu_seqlens[m + 1] - p.cu_seqlens[m]);
+            if (ns > 1) base += ns;
+        }
+        slot = ((base + sigma) * H + h) * (int64_t)(kDim * kDim);
+    }
+    const bool has_out = item == ITEM_WHOLE || item == ITEM_SEGMENT;
+    const bool zero_v = item == ITEM_TRANS;
+    const float* init_src = item == ITEM_WHOLE
+                                ? (p.init_state ? p.init_state + unit * (kDim * kDim) : nullptr)
+                                : (item == ITEM_SEGMENT ? p.ws_in + slot : nullptr);
+    float* final_dst = item == ITEM_WHOLE ? (p.final_state ? p.final_state + unit * (kDim * kDim) : nullptr)
+                       : item == ITEM_TILDE ? p.ws_tilde + slot
+                       : item == ITEM_TRANS ? p.ws_trans + slot
+                       : (sigma == nseg - 1 && p.final_state ? p.final_state + unit * (kDim * kDim)
+                                                              : nullptr);
 
     if (L <= 0) {  // empty sequence: the final state is the initial state
-        if (p.final_state) {
-            float* dst = p.final_state + unit * (kDim * kDim);
-            const float* src = p.init_state ? p.init_state + unit * (kDim * kDim) : nullptr;
-            for (int e = tid; e < kDim * kDim; e += blockDim.x) dst[e] = src ? src[e] : 0.f;
+        if (final_dst) {
+            for (int e = tid; e < kDim * kDim; e += blockDim.x)
+                final_dst[e] = init_src ? init_src[e] : 0.f;
         }
         return;
     }
@@ -250,6 +330,11 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    for (int e = tid; e < 2 * 8192 / 16; e += blockDim.x)
+        reinterpret_cast<uint4*>(sm + OFF_TB0)[e] = make_uint4(0u, 0u, 0u, 0u);
+    if (zero_v)  // a transition item carries zero values: v stays zero, never loaded
+        for (int e = tid; e < 16384 / 16; e += blockDim.x)
+            reinterpret_cast<uint4*>(sm + OFF_V)[e] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 32) {
         for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
@@ -261,28 +346,32 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const uint32_t a_kq[2] = {saddr(sm + OFF_KQ0), saddr(sm + OFF_KQ1)};
-    const uint32_t a_kmh[2] = {saddr(sm + OFF_KMH0), saddr(sm + OFF_KMH1)};
-    const uint32_t a_p[2] = {saddr(sm + OFF_P0), saddr(sm + OFF_P1)};
-    const uint32_t a_wn[2] = {saddr(sm + OFF_WN0), saddr(sm + OFF_WN1)};
-    const uint32_t a_tb[2] = {saddr(sm + OFF_TB0), saddr(sm + OFF_TB1)};
+    const uint32_t a_base = saddr(sm);
+    // shared addresses of the per-slot tiles (slot s = chunk & 1)
+    auto a_kq = [&](int s) { return a_base + (s ? OFF_KQW1 : OFF_KQW0); };
+    auto a_kmh = [&](int s) { return a_base + (s ? OFF_KMH1 : OFF_KMH0); };
+    auto a_p = [&](int s) { return a_base + (s ? OFF_P1 : OFF_P0); };
+    auto a_tb = [&](int s) { return a_base + (s ? OFF_TB1 : OFF_TB0); };
     // TMA issue helpers (q, k, g of chunk c into slot c & 1; v of chunk c)
     auto issue_kqg = [&](int c) {
         const int s = c & 1;
-        unsigned char* kq = sm + (s ? OFF_KQ1 : OFF_KQ0);
-        unsigned char* wn = sm + (s ? OFF_WN1 : OFF_WN0);
+        unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
         uint64_t* full = &bars[B_FULL0 + s];
         const int t0 = (int)(seq0 + (int64_t)kChunk * c);
         mbar_arrive_expect_tx(full, 49152);
-        tma_load_3d(kq + 0, &tm_k, full, 0, h, t0);
-        tma_load_3d(kq + 16384, &tm_k, full, 64, h, t0);
-        tma_load_3d(kq + 8192, &tm_q, full, 0, h, t0);
-        tma_load_3d(kq + 24576, &tm_q, full, 64, h, t0);
-        tma_load_3d(wn + 0, &tm_g, full, 0, h, t0);
-        tma_load_3d(wn + 8192, &tm_g, full, 64, h, t0);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            tma_load_3d(kq + r * KQW_REGION, &tm_k, full, 64 * r, h, t0);
+            tma_load_3d(kq + r * KQW_REGION + 8192, &tm_q, full, 64 * r, h, t0);
+            tma_load_3d(kq + r * KQW_REGION + 16384, &tm_g, full, 64 * r, h, t0);
+        }
         *kqg_issued = c + 1;
     };
     auto issue_v = [&](int c) {
+        if (zero_v) {
+            mbar_arrive(&bars[B_VFULL]);
+            return;
+        }
         const int t0 = (int)(seq0 + (int64_t)kChunk * c);
         mbar_arrive_expect_tx(&bars[B_VFULL], 16384);
         tma_load_3d(sm + OFF_V, &tm_v, &bars[B_VFULL], 0, h, t0);
@@ -300,46 +389,53 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             issue_v(0);
             if (nchunks > 1) issue_kqg(1);
             const uint32_t rP = tmem + T_P;
-            const uint32_t a_kml = saddr(sm + OFF_KML), a_v = saddr(sm + OFF_V);
+            const uint32_t a_v = saddr(sm + OFF_V);
             const uint32_t id_kk64 = idesc_bf16(128, 64, false, false);
             const uint32_t id_mk64 = idesc_bf16(128, 64, true, false);
             int v_issued = 1;
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c & 1;
-                // M1: [K_p ; Q_r] (K_m hi + K_m lo)^T
-                if (!wait_bar(&bars[B_FACT0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                // M1: [K_p ; Q_r] K_m^T
+                if (!spin_bar(&bars[B_FACT0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
                 tc_fence_after();
-                for (int j = 0; j < 8; ++j)
-                    mma_ss(rP, smem_desc(a_kq[s] + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
-                           smem_desc(a_kmh[s] + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024), id_kk64,
-                           j > 0);
-                for (int j = 0; j < 8; ++j)
-                    mma_ss(rP, smem_desc(a_kq[s] + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
-                           smem_desc(a_kml + (j >> 2) * 8192 + (j & 3) * 32, 16, 1024), id_kk64, 1);
+                {
+                    const uint64_t dq = smem_desc(a_kq(s), 16, 1024);
+                    const uint64_t dh = smem_desc(a_kmh(s), 16, 1024);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)  // 16 B descriptor units: K step 32 B
+                        mma_ss(rP, dq + (j >> 2) * (KQW_REGION >> 4) + (j & 3) * 2,
+                               dh + (j >> 2) * 512 + (j & 3) * 2, id_kk64, j > 0);
+                }
                 mma_commit(&bars[B_AP0 + s]);
                 // M2: W^T = K_p^T (T diag(beta))^T
-                if (!wait_bar(&bars[B_TB0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                if (!spin_bar(&bars[B_TB0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
                 tc_fence_after();
-                for (int j = 0; j < 4; ++j)
-                    mma_ss(rP, smem_desc(a_kq[s] + 2048 * j, 16384, 1024),
-                           smem_desc(a_tb[s] + 32 * j, 16, 1024), id_mk64, j > 0);
+                {
+                    const uint64_t da = smem_desc(a_kq(s), KQW_REGION, 1024);
+                    const uint64_t db = smem_desc(a_tb(s), 16, 1024);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_ss(rP, da + 128 * j, db + 2 * j, id_mk64, j > 0);
+                }
                 mma_commit(&bars[B_WDONE0 + s]);
                 // M3: U_bar^T = V^T (T diag(beta))^T into this chunk's U^T buffer, once the
                 // epilogue has read that buffer two chunks ago and v has landed.  (A per-slot
                 // barrier: a single one could run two phases ahead of this wait.)
                 if (c >= 2 &&
-                    !wait_bar(&bars[B_UFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
+                    !spin_bar(&bars[B_UFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
                     break;
-                if (!wait_bar(&bars[B_VFULL], c & 1, abort_flag, p.status)) break;
+                if (!spin_bar(&bars[B_VFULL], c & 1, abort_flag, p.status)) break;
                 tc_fence_after();
-                const uint32_t rU = tmem + (s ? T_U1 : T_U0);
-                for (int j = 0; j < 4; ++j)
-                    mma_ss(rU, smem_desc(a_v + 2048 * j, 8192, 1024),
-                           smem_desc(a_tb[s] + 32 * j, 16, 1024), id_mk64, j > 0);
+                const uint32_t rU = tmem + (s ? T_X1 : T_X0) + 64;
+                {
+                    const uint64_t da = smem_desc(a_v, 8192, 1024);
+                    const uint64_t db = smem_desc(a_tb(s), 16, 1024);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_ss(rU, da + 128 * j, db + 2 * j, id_mk64, j > 0);
+                }
                 mma_commit(&bars[B_VFREE0 + s]);
                 // the v buffer is free once M3 has read it: load the next chunk's v
                 if (c + 1 < nchunks) {
-                    if (!wait_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                    if (!spin_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
                     issue_v(c + 1);
                     v_issued = c + 2;
                 }
@@ -356,39 +452,48 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ serial MMA issuer
         if (lane == 0) {
-            const uint32_t rS = tmem + T_S, rO = tmem + T_O;
-            const uint32_t rSA = tmem + T_SA, rUH = tmem + T_UH, rUL = tmem + T_UL;
+            const uint32_t rS = tmem + T_S, rSA = tmem + T_SA;
             const uint32_t id_kk64 = idesc_bf16(128, 64, false, false);
-            const uint32_t id_km64 = idesc_bf16(128, 64, false, true);
+            const uint32_t id_kk128 = idesc_bf16(128, 128, false, false);
             const uint32_t id_km128 = idesc_bf16(128, 128, false, true);
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c & 1;
-                const uint32_t rU = tmem + (s ? T_U1 : T_U0);
-                // M4: O^T = X Q_r^T, U^T += X (-W)^T
-                if (!wait_bar(&bars[B_WN0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
-                if (!wait_bar(&bars[B_SREADY], c & 1, abort_flag, p.status)) break;
-                if (!wait_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                const uint32_t rX = tmem + (s ? T_X1 : T_X0);  // [O^T | U^T]
+                // M4: [O^T | U^T] += X [Q_r ; -W]^T  (O^T starts at zero, U^T at U_bar^T)
+                if (!spin_bar(&bars[B_WN0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                if (!spin_bar(&bars[B_SREADY], c & 1, abort_flag, p.status)) break;
+                if (!spin_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
                 tc_fence_after();
-                for (int j = 0; j < 8; ++j)
-                    mma_ts(rO, rSA + 8 * j,
-                           smem_desc(a_kq[s] + 8192 + (j >> 2) * 16384 + (j & 3) * 32, 16, 1024),
-                           id_kk64, j > 0);
-                for (int j = 0; j < 8; ++j)
-                    mma_ts(rU, rSA + 8 * j, smem_desc(a_wn[s] + 2048 * j, 16384, 1024), id_km64, 1);
+                {
+                    const uint64_t db = smem_desc(a_kq(s) + 8192, 16, 1024);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        mma_ts(rX, rSA + 8 * j, db + (j >> 2) * (KQW_REGION >> 4) + (j & 3) * 2,
+                               id_kk128, 1);
+                }
                 mma_commit(&bars[B_XDONE]);
-                // M5 + M6: O^T += U^T P^T (3 split terms), X += U^T K_m (2 split terms)
-                if (!wait_bar(&bars[B_UREADY], c & 1, abort_flag, p.status)) break;
+                // M5 + M6: O^T += U^T P^T (3 split terms), X += U^T K_m (2 split terms);
+                // U^T hi / lo sit in place of U^T (cols 64-95 / 96-127 of this chunk's block)
+                if (!spin_bar(&bars[B_UREADY], c & 1, abort_flag, p.status)) break;
                 tc_fence_after();
-                for (int j = 0; j < 4; ++j)
-                    mma_ts(rO, rUH + 8 * j, smem_desc(a_p[s] + 32 * j, 16, 1024), id_kk64, 1);
-                for (int j = 0; j < 4; ++j)
-                    mma_ts(rO, rUL + 8 * j, smem_desc(a_p[s] + 32 * j, 16, 1024), id_kk64, 1);
-                for (int j = 0; j < 4; ++j)
-                    mma_ts(rO, rUH + 8 * j, smem_desc(a_p[s] + 8192 + 32 * j, 16, 1024), id_kk64, 1);
-                for (int j = 0; j < 4; ++j)
-                    mma_ts(rS, rUH + 8 * j, smem_desc(a_kmh[s] + 2048 * j, 8192, 1024), id_km128, 1);
-                for (int j = 0; j < 4; ++j)
-                    mma_ts(rS, rUL + 8 * j, smem_desc(a_kmh[s] + 2048 * j, 8192, 1024), id_km128, 1);
+                {
+                    const uint32_t rUH = rX + 64, rUL = rX + 96;
+                    const uint64_t dph = smem_desc(a_p(s), 16, 1024);
+                    const uint64_t dpl = smem_desc(a_p(s) + 8192, 16, 1024);
+                    const uint64_t dk = smem_desc(a_kmh(s), 8192, 1024);
+                    if (has_out) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) mma_ts(rX, rUH + 8 * j, dph + 2 * j, id_kk64, 1);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) mma_ts(rX, rUL + 8 * j, dph + 2 * j, id_kk64, 1);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) mma_ts(rX, rUH + 8 * j, dpl + 2 * j, id_kk64, 1);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_ts(rS, rUH + 8 * j, dk + 128 * j, id_km128, 1);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_ts(rS, rUL + 8 * j, dk + 128 * j, id_km128, 1);
+                }
                 mma_commit(&bars[B_OSDONE]);
             }
             // every issued MMA completes before TMEM can be released
@@ -407,15 +512,14 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int row_abs = 32 * q4 + lane;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         float* Am = reinterpret_cast<float*>(sm + OFF_KML);
+        float beta_next = (tp < min(kChunk, L)) ? bf2f(p.beta[seq0 * H + (int64_t)tp * H + h]) : 0.f;
         float* Y = reinterpret_cast<float*>(sm + OFF_Y);
-        unsigned char* kml = sm + OFF_KML;
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1;
             const int valid = min(kChunk, L - kChunk * c);
             const int64_t tok0 = seq0 + (int64_t)kChunk * c;
-            unsigned char* kq = sm + (s ? OFF_KQ1 : OFF_KQ0);
+            unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
             unsigned char* kmh = sm + (s ? OFF_KMH1 : OFF_KMH0);
-            unsigned char* wn = sm + (s ? OFF_WN1 : OFF_WN0);
             unsigned char* pt = sm + (s ? OFF_P1 : OFF_P0);
             unsigned char* tb = sm + (s ? OFF_TB1 : OFF_TB0);
             if (!wait_bar(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
@@ -429,7 +533,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int t = 4 * tg + i;
-                    graw[i] = t < valid ? *reinterpret_cast<const uint4*>(wn + sw128_offset(t, c8, 64))
+                    graw[i] = t < valid ? *reinterpret_cast<const uint4*>(kq + sw128_offset(128 + t, c8, KQW_ROWS))
                                         : make_uint4(0u, 0u, 0u, 0u);
                     float gv[8];
                     unpack8(graw[i], gv);
@@ -438,17 +542,23 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
                 *reinterpret_cast<float4*>(part + tg * kDim + c8) = make_float4(gs[0], gs[1], gs[2], gs[3]);
                 *reinterpret_cast<float4*>(part + tg * kDim + c8 + 4) = make_float4(gs[4], gs[5], gs[6], gs[7]);
-                if (tp < kChunk)
-                    beta_s[tp] = tp < valid ? bf2f(p.beta[(tok0 + tp) * H + h]) : 0.f;
+                if (tp < kChunk) {
+                    beta_s[tp] = beta_next;
+                    // fetch the next chunk's beta now; it is needed one chunk later
+                    const int vn = min(kChunk, L - kChunk * (c + 1));
+                    beta_next = tp < vn ? bf2f(p.beta[(tok0 + kChunk + tp) * H + h]) : 0.f;
+                }
             }
             named_bar(kBarPrep, kPrepThreads);
             if (tp < kDim) {  // exclusive prefix over the 16 token groups, and the chunk total
+                float v[16];
+#pragma unroll
+                for (int g16 = 0; g16 < 16; ++g16) v[g16] = part[g16 * kDim + tp];
                 float run = 0.f;
 #pragma unroll
                 for (int g16 = 0; g16 < 16; ++g16) {
-                    const float v = part[g16 * kDim + tp];
                     part[g16 * kDim + tp] = run;
-                    run += v;
+                    run += v[g16];
                 }
                 gc_s[tp] = run;
             }
@@ -465,17 +575,23 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     r[0] = 0.5f * ga.x; r[1] = 0.5f * ga.y; r[2] = 0.5f * ga.z; r[3] = 0.5f * ga.w;
                     r[4] = 0.5f * gb.x; r[5] = 0.5f * gb.y; r[6] = 0.5f * gb.z; r[7] = 0.5f * gb.w;
                 }
+                // load every k and q piece of this thread first (the stores below are in place)
+                uint4 kraw[4], qraw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = 4 * tg + i;
+                    kraw[i] = *reinterpret_cast<const uint4*>(kq + sw128_offset(t, c8, KQW_ROWS));
+                    qraw[i] = *reinterpret_cast<const uint4*>(kq + sw128_offset(64 + t, c8, KQW_ROWS));
+                }
                 bool bad = false;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int t = 4 * tg + i;
                     float gv[8], kv[8], qv[8];
                     unpack8(graw[i], gv);
-                    uint4* pk = reinterpret_cast<uint4*>(kq + sw128_offset(t, c8, 128));
-                    uint4* pq = reinterpret_cast<uint4*>(kq + sw128_offset(64 + t, c8, 128));
-                    unpack8(*pk, kv);
-                    unpack8(*pq, qv);
-                    float kp[8], qr[8], km[8], kmlo[8];
+                    unpack8(kraw[i], kv);
+                    unpack8(qraw[i], qv);
+                    float kp[8], qr[8], km[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         G[j] += gv[j];
@@ -487,16 +603,10 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         qr[j] = qv[j] * e;
                         km[j] = kv[j] * ei;
                     }
-                    const uint4 kmh_v = pack8(km);
-                    float kmh_f[8];
-                    unpack8(kmh_v, kmh_f);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) kmlo[j] = km[j] - kmh_f[j];
-                    *pk = pack8(kp);
-                    *pq = pack8(qr);
+                    *reinterpret_cast<uint4*>(kq + sw128_offset(t, c8, KQW_ROWS)) = pack8(kp);
+                    *reinterpret_cast<uint4*>(kq + sw128_offset(64 + t, c8, KQW_ROWS)) = pack8(qr);
                     const uint32_t om = sw128_offset(t, c8, 64);
-                    *reinterpret_cast<uint4*>(kmh + om) = kmh_v;
-                    *reinterpret_cast<uint4*>(kml + om) = pack8(kmlo);
+                    *reinterpret_cast<uint4*>(kmh + om) = pack8(km);
                 }
                 if (bad) report_status(p.status, kStatusDecayRange);
                 if (tg == 0) {
@@ -572,8 +682,13 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
                 __syncwarp();
                 float* Tb = Am + (16 * b) * LDA_T + 16 * b;
+                const float bc = beta_s[16 * b + col];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) Tb[i * LDA_T + col] = x[i];
+                for (int i = 0; i < 16; ++i) {
+                    Tb[i * LDA_T + col] = x[i];
+                    *reinterpret_cast<bf16*>(tb + sw128_offset(16 * b + i, 16 * b + col, 64)) =
+                        __float2bfloat16_rn(x[i] * bc);
+                }
             }
             named_bar(kBarPrep, kPrepThreads);
             // ---- off-diagonal blocks on the tensor cores (tf32), with D = blockdiag(T_II) and
@@ -617,43 +732,22 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 float acc[2][4];
                 block_product(acc, Am + (16 * I) * LDA_T + 16 * J, LDA_T, -1.f, n2, n3,
                               Am + (16 * J) * LDA_T + 16 * J, LDA_T, lane);
-                __syncwarp();
-                store_block(Am + (16 * I) * LDA_T + 16 * J, LDA_T, acc, lane);
-            }
-            named_bar(kBarPrep, kPrepThreads);
-            // ---- T diag(beta) as the bf16 K-major operand (two 8-column pieces per thread) ----
-#pragma unroll
-            for (int rep = 0; rep < 2; ++rep) {
-                const int e = tp + rep * kPrepThreads;
-                const int t = e >> 3, j8 = (e & 7) * 8;
-                const float4 a0 = *reinterpret_cast<const float4*>(Am + t * LDA_T + j8);
-                const float4 a1 = *reinterpret_cast<const float4*>(Am + t * LDA_T + j8 + 4);
-                const float4 b0 = *reinterpret_cast<const float4*>(beta_s + j8);
-                const float4 b1 = *reinterpret_cast<const float4*>(beta_s + j8 + 4);
-                *reinterpret_cast<uint4*>(tb + sw128_offset(t, j8, 64)) =
-                    make_uint4(pack_bf16(a0.x * b0.x, a0.y * b0.y), pack_bf16(a0.z * b0.z, a0.w * b0.w),
-                               pack_bf16(a1.x * b1.x, a1.y * b1.y), pack_bf16(a1.z * b1.z, a1.w * b1.w));
+                store_block_tb(tb, I, J, acc, beta_s, lane);
             }
             fence_async_shared();
             named_bar(kBarPrep, kPrepThreads);
             if (tp == 0) mbar_arrive(&bars[B_TB0 + s]);
 
-            // ---- -W^T into the [c][t] operand tile ----
+            // ---- -W into rows 128-191 of the slot tile (K-major [t][c]) ----
             if (!wait_bar(&bars[B_WDONE0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
             tc_fence_after();
             {
                 uint32_t v[32];
-                tmem_ld32(tmem + T_P + 32 * colhalf + lane_off, v);
+                tmem_ld32(tmem + T_P + 32 * colhalf + lane_off, v);  // W^T[c = row_abs][t]
 #pragma unroll
-                for (int j8 = 0; j8 < 4; ++j8) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        w[u] = pack_bf16(-__uint_as_float(v[8 * j8 + 2 * u]),
-                                         -__uint_as_float(v[8 * j8 + 2 * u + 1]));
-                    *reinterpret_cast<uint4*>(wn + sw128_offset(row_abs, 32 * colhalf + 8 * j8, 128)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
+                for (int j = 0; j < 32; ++j)
+                    *reinterpret_cast<bf16*>(kq + sw128_offset(128 + 32 * colhalf + j, row_abs, KQW_ROWS)) =
+                        __float2bfloat16_rn(-__uint_as_float(v[j]));
             }
             tc_fence_before();
             fence_async_shared();
@@ -667,14 +761,15 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int vch = 32 * q4 + lane;  // value channel = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         bool ok = wait_bar(&bars[B_FACT0], 0, abort_flag, p.status);
-        if (ok) {  // X_0 = S0^T diag(e^{r_0})
+        if (ok) {  // X_0 = S0^T diag(e^{r_0}); S0 = 0, I (transition items) or the given state
             const float* e0 = er;
-            const float* s0 = p.init_state ? p.init_state + unit * (kDim * kDim) : nullptr;
+            const float* s0 = init_src;
             for (int cc = 0; cc < kDim; cc += 32) {
                 uint32_t x[32], xb[16];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const float sv = s0 ? s0[(cc + j) * kDim + vch] : 0.f;
+                    const float sv = s0 ? s0[(cc + j) * kDim + vch]
+                                        : (item == ITEM_TRANS && cc + j == vch ? 1.f : 0.f);
                     x[j] = __float_as_uint(sv * e0[cc + j]);
                 }
 #pragma unroll
@@ -683,54 +778,55 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tmem_st32(tmem + T_S + cc + lane_off, x);
                 tmem_st16(tmem + T_SA + cc / 2 + lane_off, xb);
             }
+            {  // O^T of both chunk blocks starts at zero
+                uint32_t z[64];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) z[j] = 0u;
+                tmem_st64(tmem + T_X0 + lane_off, z);
+                tmem_st64(tmem + T_X1 + lane_off, z);
+            }
             tmem_st_wait();
             tc_fence_before();
             named_bar(kBarEpi, kEpiThreads);
             if (te == 0) mbar_arrive(&bars[B_SREADY]);
         }
         for (int c = 0; ok && c < nchunks; ++c) {
+            const uint32_t rX = tmem + ((c & 1) ? T_X1 : T_X0) + lane_off;
             const int valid = min(kChunk, L - kChunk * c);
             const int64_t tok0 = seq0 + (int64_t)kChunk * c;
             // ---- E1: U^T -> bf16 hi/lo A operands ----
             if (!(ok = wait_bar(&bars[B_XDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
+            {
+                // read all 64 columns of U^T before writing hi / lo over them
+                uint32_t u[64], lo[32];
+                tmem_ld64(rX + 64, u);
 #pragma unroll
-            for (int g2 = 0; g2 < 2; ++g2) {
-                uint32_t u[32], hi[16], lo[16];
-                tmem_ld32(tmem + ((c & 1) ? T_U1 : T_U0) + 32 * g2 + lane_off, u);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < 32; ++j) {
                     const float x0 = __uint_as_float(u[2 * j]), x1 = __uint_as_float(u[2 * j + 1]);
-                    hi[j] = pack_bf16(x0, x1);
-                    lo[j] = pack_bf16(x0 - __uint_as_float(hi[j] << 16),
-                                      x1 - __uint_as_float(hi[j] & 0xffff0000u));
+                    const uint32_t hi = pack_bf16(x0, x1);
+                    lo[j] = pack_bf16(x0 - __uint_as_float(hi << 16),
+                                      x1 - __uint_as_float(hi & 0xffff0000u));
+                    u[j] = hi;  // u[2j], u[2j+1] are consumed; slot j <= 2j is free
                 }
-                tmem_st16(tmem + T_UH + 16 * g2 + lane_off, hi);
-                tmem_st16(tmem + T_UL + 16 * g2 + lane_off, lo);
+                uint32_t hi32[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) hi32[j] = u[j];
+                tmem_st32(rX + 64, hi32);
+                tmem_st32(rX + 96, lo);
             }
             tmem_st_wait();
             tc_fence_before();
             named_bar(kBarEpi, kEpiThreads);
-            if (te == 0) {
-                mbar_arrive(&bars[B_UREADY]);
-                mbar_arrive(&bars[B_UFREE0 + (c & 1)]);
-            }
+            if (te == 0) mbar_arrive(&bars[B_UREADY]);
 
-            // ---- E2: O to HBM, state rescale ----
+            // ---- E2: state rescale first (the next chunk's M4 waits on it), then O to HBM ----
             if (!(ok = wait_bar(&bars[B_OSDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
             // every MMA that reads slot c & 1 has completed: refill it with chunk c + 2
             if (te == 0 && c + 2 < nchunks) issue_kqg(c + 2);
-            {
-                uint32_t o[64];
-                tmem_ld64(tmem + T_O + lane_off, o);
-                bf16* op = p.out + (tok0 * H + h) * kDim + vch;
-                const int64_t tstride = (int64_t)H * kDim;
-#pragma unroll
-                for (int t = 0; t < 64; ++t)
-                    if (t < valid) op[t * tstride] = __float2bfloat16_rn(__uint_as_float(o[t]));
-            }
-            if (c + 1 < nchunks) {
+            const bool last = (c + 1 == nchunks);
+            if (!last) {
                 if (!(ok = wait_bar(&bars[B_FACT0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, abort_flag,
                                     p.status)))
                     break;
@@ -757,15 +853,37 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tc_fence_before();
                 named_bar(kBarEpi, kEpiThreads);
                 if (te == 0) mbar_arrive(&bars[B_SREADY]);
-            } else if (p.final_state) {
+            } else if (final_dst) {
                 const float* ec = er + (c & 3) * kDim;
-                float* fs = p.final_state + unit * (kDim * kDim);
+                float* fs = final_dst;
                 for (int cc = 0; cc < kDim; cc += 32) {
                     uint32_t x[32];
                     tmem_ld32(tmem + T_S + cc + lane_off, x);
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         fs[(cc + j) * kDim + vch] = __uint_as_float(x[j]) * ec[cc + j];
+                }
+            }
+            {
+                uint32_t o[64];
+                if (has_out) {
+                    tmem_ld64(rX, o);
+                    bf16* op = p.out + (tok0 * H + h) * kDim + vch;
+                    const int64_t tstride = (int64_t)H * kDim;
+#pragma unroll
+                    for (int t = 0; t < 64; ++t) {
+                        if (t < valid) *op = __float2bfloat16_rn(__uint_as_float(o[t]));
+                        op += tstride;
+                    }
+                }
+                if (!last) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) o[j] = 0u;
+                    tmem_st64(rX, o);  // O^T of this block restarts at zero two chunks later
+                    tmem_st_wait();
+                    tc_fence_before();
+                    named_bar(kBarEpi, kEpiThreads);
+                    if (te == 0) mbar_arrive(&bars[B_UFREE0 + (c & 1)]);
                 }
             }
         }
@@ -775,6 +893,77 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     __syncthreads();
     tc_fence_after();
     if (warp == kWarpTma) tmem_dealloc(tmem, 512);
+}
+
+// Composition of segment effects, one CTA per split (sequence, head):
+//   S_in(0) = initial state;  S_in(s+1) = M_s S_in(s) + S~_s
+// ("k3_training_and_infra_notes", section 4.1: a segment's transition is evaluated without the
+// incoming state and composed exactly afterwards).  fp32 on the CUDA cores; every S_in(s) is
+// written to the workspace for the second pass.
+constexpr int kCombineThreads = 256;
+__global__ void __launch_bounds__(kCombineThreads, 1)
+kda_segment_combine_kernel(const int32_t* __restrict__ cu_seqlens, const float* __restrict__ init_state,
+                           const float* __restrict__ ws_tilde, const float* __restrict__ ws_trans,
+                           float* __restrict__ ws_in, int H) {
+    extern __shared__ __align__(16) float cs[];
+    float* S = cs;                  // [128][128]
+    float* M = cs + kDim * kDim;    // [128][128]
+    const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    const int64_t len = (int64_t)cu_seqlens[n + 1] - cu_seqlens[n];
+    const int nseg = num_segments(len);
+    if (nseg <= 1) return;
+    int64_t base = 0;
+    for (int m = 0; m < n; ++m) {
+        const int ns = num_segments((int64_t)cu_seqlens[m + 1] - cu_seqlens[m]);
+        if (ns > 1) base += ns;
+    }
+    const int64_t unit = (int64_t)n * H + h;
+    const float* s0 = init_state ? init_state + unit * (kDim * kDim) : nullptr;
+    for (int e = tid; e < kDim * kDim / 4; e += kCombineThreads)
+        reinterpret_cast<float4*>(S)[e] =
+            s0 ? reinterpret_cast<const float4*>(s0)[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+    __syncthreads();
+    const int ti = tid >> 4, tj = tid & 15;  // 8 x 8 output tile (rows 8 ti.., cols 8 tj..)
+    for (int sg = 0; sg < nseg; ++sg) {
+        const int64_t off = ((base + sg) * H + h) * (int64_t)(kDim * kDim);
+        for (int e = tid; e < kDim * kDim / 4; e += kCombineThreads)
+            reinterpret_cast<float4*>(ws_in + off)[e] = reinterpret_cast<const float4*>(S)[e];
+        if (sg == nseg - 1) break;
+        for (int e = tid; e < kDim * kDim / 4; e += kCombineThreads)
+            reinterpret_cast<float4*>(M)[e] = reinterpret_cast<const float4*>(ws_trans + off)[e];
+        __syncthreads();
+        float acc[8][8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+#pragma unroll
+            for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+        for (int kk = 0; kk < kDim; ++kk) {
+            float mv[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mv[a] = M[(8 * ti + a) * kDim + kk];
+            const float4 s0v = *reinterpret_cast<const float4*>(S + kk * kDim + 8 * tj);
+            const float4 s1v = *reinterpret_cast<const float4*>(S + kk * kDim + 8 * tj + 4);
+            const float sv[8] = {s0v.x, s0v.y, s0v.z, s0v.w, s1v.x, s1v.y, s1v.z, s1v.w};
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(mv[a], sv[b], acc[a][b]);
+        }
+        __syncthreads();  // everyone is done reading S
+        const float* st = ws_tilde + off;
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+            const int row = 8 * ti + a;
+#pragma unroll
+            for (int b = 0; b < 8; b += 4) {
+                const float4 t4 = *reinterpret_cast<const float4*>(st + row * kDim + 8 * tj + b);
+                *reinterpret_cast<float4*>(S + row * kDim + 8 * tj + b) =
+                    make_float4(acc[a][b] + t4.x, acc[a][b + 1] + t4.y, acc[a][b + 2] + t4.z,
+                                acc[a][b + 3] + t4.w);
+            }
+        }
+        __syncthreads();
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -810,8 +999,8 @@ bool make_map(CUtensorMap* map, const void* base, int64_t T, int H) {
 cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, const void* q,
                               const void* k, const void* v, const void* g, const void* beta,
                               const float* init_state, const int32_t* cu_seqlens, void* out,
-                              float* final_state, int* status, cudaStream_t stream,
-                              uint64_t* launches) {
+                              float* final_state, const SegWorkspace& ws, int* status,
+                              cudaStream_t stream, uint64_t* launches) {
     if (num_seqs <= 0 || heads <= 0) return cudaSuccess;
     CUtensorMap mq, mk, mv, mg;
     const int64_t T = total_tokens > 0 ? total_tokens : 1;
@@ -825,12 +1014,33 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
     prm.out = static_cast<bf16*>(out);
     prm.final_state = final_state;
     prm.status = status;
+    prm.ws_tilde = ws.tilde;
+    prm.ws_trans = ws.trans;
+    prm.ws_in = ws.in;
     prm.H = heads;
+    prm.pass = 0;
     cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    dim3 grid(num_seqs, heads);
-    kda_prefill_tc_kernel<<<grid, kThreadsTC, SMEM_ALLOC, stream>>>(mq, mk, mv, mg, prm);
+    const int zsplit = ws.max_segments > 1 ? 2 * (ws.max_segments - 1) : 1;
+    // pass 0: whole sequences, and pass A (segment states and transitions) of split ones
+    kda_prefill_tc_kernel<<<dim3(num_seqs, heads, zsplit), kThreadsTC, SMEM_ALLOC, stream>>>(
+        mq, mk, mv, mg, prm);
+    if (launches) ++*launches;
+    if ((e = cudaGetLastError()) != cudaSuccess || ws.max_segments <= 1) return e;
+    // compose the incoming state of every segment
+    const int csmem = 2 * kDim * kDim * 4;
+    if ((e = cudaFuncSetAttribute(kda_segment_combine_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, csmem)) != cudaSuccess)
+        return e;
+    kda_segment_combine_kernel<<<dim3(num_seqs, heads), kCombineThreads, csmem, stream>>>(
+        cu_seqlens, init_state, ws.tilde, ws.trans, ws.in, heads);
+    if (launches) ++*launches;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // pass B: every segment of the split sequences from its composed incoming state
+    prm.pass = 1;
+    kda_prefill_tc_kernel<<<dim3(num_seqs, heads, ws.max_segments), kThreadsTC, SMEM_ALLOC,
+                            stream>>>(mq, mk, mv, mg, prm);
     if (launches) ++*launches;
     return cudaGetLastError();
 }

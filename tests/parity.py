@@ -35,5 +35,12 @@ def assert_close(name, gpu, ref, rel_tol=REL_L2_TOL, max_tol=MAX_ABS_TOL):
     g = np.asarray(gpu, dtype=np.float64)
     assert np.isfinite(g).all(), f"{name}: non-finite values"
     rel, mx = errors(g, ref)
+    log = os.environ.get("KDA_PARITY_LOG")
+    if log:
+        import json
+        test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": test, "name": name, "rel_l2": rel, "max_over_rms": mx,
+                                "n": int(g.size)}) + "\n")
     assert rel <= rel_tol and mx <= max_tol, f"{name}: rel_l2={rel:.3e} max/rms={mx:.3e}"
     return rel, mx

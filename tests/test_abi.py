@@ -59,6 +59,22 @@ def test_plan_counts_chunks_per_sequence(lib):
     assert info["work_items"] >= len(lens)
 
 
+def test_plan_splits_long_sequences_by_length_only(lib):
+    from kimi_delta_attention_03_gb300 import binding
+    H = 3
+    lens = [16384, 16385, 262144, 5]  # 256 chunks (whole), 257 (3 segments), 4096 (32), 1
+    info = binding.fwd_plan(lens, H)
+    assert info["segment_chunks"] == 128
+    assert info["split_sequences"] == 2
+    assert info["work_items"] == 1 + 3 + 32 + 1
+    slots = 3 + 32
+    assert info["workspace_bytes"] == 3 * slots * H * 128 * 128 * 4
+    assert binding.fwd_workspace_bytes(lens, H) == info["workspace_bytes"]
+    # the plan of a sequence does not depend on its neighbours
+    assert binding.fwd_plan([16385], H)["work_items"] == 3
+    assert binding.fwd_plan([100, 200], H)["workspace_bytes"] == 0
+
+
 def test_host_argument_checks(lib):
     from kimi_delta_attention_03_gb300 import binding
     P = ctypes.c_void_p

@@ -223,3 +223,38 @@ def test_varlen_64_full_size():
     assert_close("out", rows_of(out, wins).float().cpu().numpy(), o_ref)
     assert_close("final_state", fin.cpu().numpy(), s_ref)
     check_status()
+
+
+# ------------------------------ segment parallelism ------------------------------------
+def test_segmented_sequences_match_oracle():
+    """Sequences above 256 chunks run as segments (transition + state-from-zero per segment,
+    composed, then rerun); the result equals the token loop."""
+    lens = [20000, 100, 17000, 16384]  # 313, 2, 266, 256 chunks: split, whole, split, whole
+    x = synth.make_inputs(lens, 2, torch.bfloat16, seed=31, device=DEV)
+    info = kda().binding.fwd_plan(lens, 2)
+    assert info["split_sequences"] == 2 and info["work_items"] == 3 + 1 + 3 + 1
+    out, fin = run_gpu(x)
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+
+
+def test_segmented_packing_is_bit_exact_and_aliasing_safe():
+    lens = [70, 20000, 0, 33]
+    x = synth.make_inputs(lens, 2, torch.bfloat16, seed=32, device=DEV)
+    out, fin = run_gpu(x)
+    cu = x["cu_seqlens"].cpu().tolist()
+    for n, L in enumerate(lens):
+        lo, hi = cu[n], cu[n + 1]
+        xs = {key: x[key][lo:hi].contiguous() for key in ("q", "k", "v", "log_alpha", "beta")}
+        xs["init_state"] = x["init_state"][n:n + 1].contiguous()
+        xs["cu_seqlens"] = torch.tensor([0, L], dtype=torch.int32, device=DEV)
+        xs["seqlens"] = [L]
+        o1, f1 = run_gpu(xs)
+        assert torch.equal(o1, out[lo:hi]) and torch.equal(f1[0], fin[n]), f"sequence {n}"
+    state = x["init_state"].clone()
+    out2, _ = kda().fwd_chunked(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                x["cu_seqlens"], x["seqlens"], init_state=state,
+                                final_state=state)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, out) and torch.equal(state, fin)
