@@ -24,8 +24,9 @@
  *     write strength itself (already passed through a sigmoid).  No scale is applied to q.
  *   - Only d_k = d_v = 128 is supported.
  *   - Ownership: the caller owns and allocates every buffer (device memory unless marked
- *     host).  The library never allocates or frees memory and keeps no per-call state; the
- *     only global is the sticky device status word read by kda_read_device_status().
+ *     host).  The library never allocates or frees memory and keeps no per-call state; its
+ *     only globals are the sticky device status word read by kda_read_device_status() and
+ *     the fixed scratch array behind kda_fwd_chunked_noalloc().
  *   - Every compute entry point is asynchronous on `stream` (NULL = legacy default stream).
  *     Host-side argument checks are synchronous and return before anything is launched.
  *   - Errors: KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED / KDA_ERR_WORKSPACE from the host
@@ -124,6 +125,34 @@ kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, c
                            const void* log_alpha, const void* beta, const float* init_state,
                            const int32_t* cu_seqlens, void* out, float* final_state,
                            void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_fwd_chunked_noalloc — kda_fwd_chunked for callers that cannot allocate device memory.
+ *
+ * No counterpart in the paper: this is a deployment convenience.  Some callers cannot supply
+ * the scratch workspace kda_fwd_chunked asks for, because they may not call cudaMalloc where
+ * they run (inside an allocator or memory-pool callback, in a host that forbids device
+ * allocation, or on a latency-critical path where an allocation could synchronise the
+ * device).  This variant takes the same arguments minus the workspace and uses a scratch array
+ * built into the library instead; it allocates nothing and calls no allocating routine.
+ *
+ *   - The scratch array is KDA_NOALLOC_SCRATCH_BYTES (48 MiB) of device memory that every GPU
+ *     which loads this library holds until the process exits.
+ *   - A call whose kda_fwd_workspace_bytes(desc) exceeds KDA_NOALLOC_SCRATCH_BYTES returns
+ *     KDA_ERR_WORKSPACE before launching anything (for example H = 16 heads fit up to 16
+ *     segments of 8192 tokens in total).  Calls that need no workspace always run.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; nothing in it has to
+ *     start at zero.  Calls that overlap on the GPU (different streams, or different host
+ *     threads) race on the array: serialise them.
+ * Everything else — arguments, layouts, results, errors — is as for kda_fwd_chunked.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)48 << 20)
+kda_status kda_fwd_chunked_noalloc(const kda_desc* desc, const void* q, const void* k,
+                                   const void* v, const void* log_alpha, const void* beta,
+                                   const float* init_state, const int32_t* cu_seqlens, void* out,
+                                   float* final_state, kda_stream_t stream);
 
 /*
  * kda_decode_step — one decode token per (sequence, head), state updated in place.

@@ -52,6 +52,8 @@ SIGNATURES = {
     "kda_fwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(KdaDesc)]),
     "kda_fwd_chunked": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P,
                                        _P, _P, ctypes.c_size_t, _P]),
+    "kda_fwd_chunked_noalloc": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P,
+                                               _P, _P, _P, _P]),
     "kda_decode_step": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P]),
     "kda_read_device_status": (ctypes.c_int, [_P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -156,6 +158,41 @@ def fwd_chunked(q, k, v, log_alpha, beta, cu_seqlens, seqlens, init_state=None, 
                              _stream_handle(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, "kda_fwd_chunked")
+    return out, final_state
+
+
+def fwd_chunked_noalloc(q, k, v, log_alpha, beta, cu_seqlens, seqlens, init_state=None,
+                        out=None, final_state=None, stream=None):
+    """Chunked prefill through kda_fwd_chunked_noalloc: for callers that cannot allocate
+    device scratch, the library's built-in 48 MiB array serves as the segment workspace (a
+    call needing more raises KdaError(KDA_ERR_WORKSPACE)).  ``out`` and ``final_state`` must be
+    given: this path allocates nothing.  Calls share the array, so overlapping calls on
+    different streams must not be issued."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("fwd_chunked_noalloc needs CUDA tensors")
+    T, H, d = q.shape
+    N = len(seqlens)
+    dt = q.dtype
+    for name, t, shp in (("k", k, (T, H, d)), ("v", v, (T, H, d)),
+                         ("log_alpha", log_alpha, (T, H, d)), ("beta", beta, (T, H)),
+                         ("out", out, (T, H, d))):
+        if t is None:
+            raise ValueError(f"{name} must be given")
+        _check_io(name, t, shp, dt, dev)
+    _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    if init_state is not None:
+        _check_io("init_state", init_state, (N, H, d, d), torch.float32, dev)
+    if final_state is not None:
+        _check_io("final_state", final_state, (N, H, d, d), torch.float32, dev)
+    desc = make_desc(seqlens, H, dt, d)
+    st = lib.kda_fwd_chunked_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(log_alpha), _ptr(beta), _ptr(init_state),
+                                     _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                     _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fwd_chunked_noalloc")
     return out, final_state
 
 
