@@ -216,6 +216,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--case", default="full", choices=["full", "small"],
+                    help="small: a reduced prefill (4 x 4096 tokens, 8 heads) and decode "
+                         "(64 x 96) for ncu section captures; not a benchmark figure")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip timing the long-context and varlen prefill workloads")
     args = ap.parse_args()
@@ -235,8 +238,15 @@ def main():
     stream = torch.cuda.current_stream(dev)
     hbm_peak, tc_peak, peak_kind = peaks()
 
+    if args.case == "small":
+        args.no_extra = args.no_e2e = args.no_cpu_baseline = True
+
     # ---------------- prefill (headline) ----------------
     w = synth.workloads()["prefill_4x8k"]
+    if args.case == "small":
+        from dataclasses import replace
+        w = replace(w, name="prefill_small (B=4, T=4096, H=8, bf16; profiling case)",
+                    lengths=(4096,) * 4, heads=8)
     x = synth.make_workload(w, device=dev)
     T, H = x["q"].shape[0], w.heads
     out = torch.empty_like(x["q"])
@@ -277,7 +287,8 @@ def main():
     decode = None
     if not args.no_decode:
         wd = synth.workloads()["decode_512x96"]
-        dd = synth.make_decode_inputs(512, 96, torch.bfloat16, seed=wd.seed,
+        n_dec = 64 if args.case == "small" else 512
+        dd = synth.make_decode_inputs(n_dec, 96, torch.bfloat16, seed=wd.seed,
                                       state_std=wd.s0_std, device=dev)
         dout = torch.empty_like(dd["q"])
 
@@ -290,7 +301,7 @@ def main():
         barrier(world)
         dms = time_device(dstep, args.steps, stream)
         dms = max_over_ranks(dms, world)
-        dunits = 512 * 96
+        dunits = n_dec * 96
         dbytes = dunits * (2 * STATE_BYTES + BYTES_PER_TOKEN_HEAD)
         dgbs = dbytes / (dms * 1e-3) / 1e9
         decode = {"metric": "decode state-update GB/s", "value": dgbs * world, "unit": "GB/s",
