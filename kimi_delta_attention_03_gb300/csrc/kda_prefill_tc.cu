@@ -72,16 +72,17 @@ constexpr uint32_t OFF_P1 = 163840;      // slot 1
 constexpr uint32_t OFF_TB0 = 180224;     // T diag(beta): 64 x 64 (8 KB), slot 0
 constexpr uint32_t OFF_TB1 = 188416;     // slot 1
 constexpr uint32_t OFF_KML = 196608;     // A / T fp32 [64][68] of the 64 x 64 inverse
-constexpr uint32_t OFF_Y = OFF_KML + 17408;         // 4 x 16 x 16 fp32 blocks (N^2, N^3)
-constexpr uint32_t OFF_PART = OFF_Y + 4096;         // 16 x 128 fp32 token-group sums / prefixes
+constexpr uint32_t OFF_PART = OFF_KML + 17408;      // 16 x 128 fp32 token-group sums / prefixes
+constexpr uint32_t OFF_Y = OFF_PART;                // 4 x 16 x 16 fp32 blocks (N^2, N^3); the
+                                                    // factor pass and the inverse never overlap
 constexpr uint32_t OFF_GC = OFF_PART + 8192;        // 128 fp32: chunk log-decay G_C
-constexpr uint32_t OFF_BETA = OFF_GC + 512;         // 64 fp32
-constexpr uint32_t OFF_ER = OFF_BETA + 256;         // 4 x 128 fp32: e^{r} ring
+constexpr uint32_t OFF_BETA = OFF_GC + 512;         // 2 x 64 fp32 ring
+constexpr uint32_t OFF_ER = OFF_BETA + 512;         // 4 x 128 fp32: e^{r} ring
 constexpr uint32_t OFF_SC = OFF_ER + 2048;          // 4 x 128 fp32: e^{r_{c-1} + r_c} ring
 constexpr uint32_t OFF_BAR = OFF_SC + 2048;         // mbarriers
-constexpr int NBAR = 24;
-constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag
-constexpr uint32_t SMEM_USED = OFF_MISC + 64;
+constexpr int NBAR = 28;
+constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag, copies issued
+constexpr uint32_t SMEM_USED = OFF_MISC + 48;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
@@ -89,14 +90,16 @@ static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 enum {
     B_FULL0 = 0, B_FULL1, B_VFREE0, B_VFREE1, B_VFULL, B_SPARE,
     B_FACT0, B_FACT1, B_AP0, B_AP1, B_TB0, B_TB1, B_WDONE0, B_WDONE1, B_WN0, B_WN1,
-    B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_UFREE0, B_UFREE1, B_COUNT
+    B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_UFREE0, B_UFREE1, B_KMFREE0, B_KMFREE1,
+    B_SDONE, B_PFREE0, B_PFREE1, B_COUNT
 };
 static_assert(B_COUNT <= NBAR, "barrier slots");
 
 // TMEM columns (512 allocated)
 constexpr uint32_t T_S = 0;      // X: fp32 state, lanes = value channel, cols = key channel
-constexpr uint32_t T_X0 = 128;   // even chunks: [O^T (64) | U^T (64)]; U^T becomes bf16 hi|lo
-constexpr uint32_t T_P = 256;    // [A ; P] raw tiles, then W^T (64 cols)
+constexpr uint32_t T_X0 = 128;   // even chunks: [O^T (64) | U^T (64)]; U^T becomes bf16 hi|lo;
+                                 // the O^T columns first hold W^T of the chunk
+constexpr uint32_t T_P = 256;    // [A ; P] raw tiles (64 cols)
 constexpr uint32_t T_SA = 320;   // bf16 copy of X (A operand, 64 cols)
 constexpr uint32_t T_X1 = 384;   // odd chunks
 
@@ -393,44 +396,48 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const uint32_t id_kk64 = idesc_bf16(128, 64, false, false);
             const uint32_t id_mk64 = idesc_bf16(128, 64, true, false);
             int v_issued = 1;
-            for (int c = 0; c < nchunks; ++c) {
+            // M1: [K_p ; Q_r] K_m^T of chunk c into the raw A / P tile
+            auto issue_m1 = [&](const int c) -> bool {
                 const int s = c & 1;
-                // M1: [K_p ; Q_r] K_m^T
-                if (!spin_bar(&bars[B_FACT0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                if (!spin_bar(&bars[B_FACT0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
                 tc_fence_after();
-                {
-                    const uint64_t dq = smem_desc(a_kq(s), 16, 1024);
-                    const uint64_t dh = smem_desc(a_kmh(s), 16, 1024);
+                const uint64_t dq = smem_desc(a_kq(s), 16, 1024);
+                const uint64_t dh = smem_desc(a_kmh(s), 16, 1024);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)  // 16 B descriptor units: K step 32 B
-                        mma_ss(rP, dq + (j >> 2) * (KQW_REGION >> 4) + (j & 3) * 2,
-                               dh + (j >> 2) * 512 + (j & 3) * 2, id_kk64, j > 0);
-                }
+                for (int j = 0; j < 8; ++j)  // 16 B descriptor units: K step 32 B
+                    mma_ss(rP, dq + (j >> 2) * (KQW_REGION >> 4) + (j & 3) * 2,
+                           dh + (j >> 2) * 512 + (j & 3) * 2, id_kk64, j > 0);
                 mma_commit(&bars[B_AP0 + s]);
-                // M2: W^T = K_p^T (T diag(beta))^T
+                return true;
+            };
+            bool run = issue_m1(0);
+            for (int c = 0; run && c < nchunks; ++c) {
+                const int s = c & 1;
+                // M2: W^T = K_p^T (T diag(beta))^T into the O^T columns of this chunk's block,
+                // once the epilogue has read that block two chunks ago.  (A per-slot barrier: a
+                // single one could run two phases ahead of this wait.)
                 if (!spin_bar(&bars[B_TB0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                if (c >= 2 &&
+                    !spin_bar(&bars[B_UFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
+                    break;
                 tc_fence_after();
+                const uint32_t rX = tmem + (s ? T_X1 : T_X0);
                 {
                     const uint64_t da = smem_desc(a_kq(s), KQW_REGION, 1024);
                     const uint64_t db = smem_desc(a_tb(s), 16, 1024);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) mma_ss(rP, da + 128 * j, db + 2 * j, id_mk64, j > 0);
+                    for (int j = 0; j < 4; ++j) mma_ss(rX, da + 128 * j, db + 2 * j, id_mk64, j > 0);
                 }
                 mma_commit(&bars[B_WDONE0 + s]);
-                // M3: U_bar^T = V^T (T diag(beta))^T into this chunk's U^T buffer, once the
-                // epilogue has read that buffer two chunks ago and v has landed.  (A per-slot
-                // barrier: a single one could run two phases ahead of this wait.)
-                if (c >= 2 &&
-                    !spin_bar(&bars[B_UFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
-                    break;
+                // M3: U_bar^T = V^T (T diag(beta))^T into the U^T columns, once v has landed
                 if (!spin_bar(&bars[B_VFULL], c & 1, abort_flag, p.status)) break;
                 tc_fence_after();
-                const uint32_t rU = tmem + (s ? T_X1 : T_X0) + 64;
                 {
                     const uint64_t da = smem_desc(a_v, 8192, 1024);
                     const uint64_t db = smem_desc(a_tb(s), 16, 1024);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) mma_ss(rU, da + 128 * j, db + 2 * j, id_mk64, j > 0);
+                    for (int j = 0; j < 4; ++j)
+                        mma_ss(rX + 64, da + 128 * j, db + 2 * j, id_mk64, j > 0);
                 }
                 mma_commit(&bars[B_VFREE0 + s]);
                 // the v buffer is free once M3 has read it: load the next chunk's v
@@ -439,6 +446,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     issue_v(c + 1);
                     v_issued = c + 2;
                 }
+                // the next chunk's factors follow this chunk's inverse
+                if (c + 1 < nchunks && !issue_m1(c + 1)) break;
             }
             mma_commit(&bars[B_DRAIN]);
             mbar_wait(&bars[B_DRAIN], 0, kWaitLimit);
@@ -472,15 +481,26 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                id_kk128, 1);
                 }
                 mma_commit(&bars[B_XDONE]);
-                // M5 + M6: O^T += U^T P^T (3 split terms), X += U^T K_m (2 split terms);
+                // M6 + M5: X += U^T K_m (2 split terms), O^T += U^T P^T (3 split terms);
                 // U^T hi / lo sit in place of U^T (cols 64-95 / 96-127 of this chunk's block)
                 if (!spin_bar(&bars[B_UREADY], c & 1, abort_flag, p.status)) break;
+                // keep these off the tensor pipe while chunk c+1's inverse uses mma.sync
+                if (c + 1 < nchunks &&
+                    !spin_bar(&bars[B_TB0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, abort_flag, p.status))
+                    break;
                 tc_fence_after();
                 {
                     const uint32_t rUH = rX + 64, rUL = rX + 96;
                     const uint64_t dph = smem_desc(a_p(s), 16, 1024);
                     const uint64_t dpl = smem_desc(a_p(s) + 8192, 16, 1024);
                     const uint64_t dk = smem_desc(a_kmh(s), 8192, 1024);
+                    // the state update first: the next chunk waits on it, the output does not
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_ts(rS, rUH + 8 * j, dk + 128 * j, id_km128, 1);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_ts(rS, rUL + 8 * j, dk + 128 * j, id_km128, 1);
+                    mma_commit(&bars[B_KMFREE0 + s]);  // K_m of this slot has been read
+                    mma_commit(&bars[B_SDONE]);
                     if (has_out) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) mma_ts(rX, rUH + 8 * j, dph + 2 * j, id_kk64, 1);
@@ -489,11 +509,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                         for (int j = 0; j < 4; ++j) mma_ts(rX, rUH + 8 * j, dpl + 2 * j, id_kk64, 1);
                     }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) mma_ts(rS, rUH + 8 * j, dk + 128 * j, id_km128, 1);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) mma_ts(rS, rUL + 8 * j, dk + 128 * j, id_km128, 1);
                 }
+                mma_commit(&bars[B_PFREE0 + s]);  // P of this slot has been read
                 mma_commit(&bars[B_OSDONE]);
             }
             // every issued MMA completes before TMEM can be released
@@ -514,20 +531,23 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         float* Am = reinterpret_cast<float*>(sm + OFF_KML);
         float beta_next = (tp < min(kChunk, L)) ? bf2f(p.beta[seq0 * H + (int64_t)tp * H + h]) : 0.f;
         float* Y = reinterpret_cast<float*>(sm + OFF_Y);
-        for (int c = 0; c < nchunks; ++c) {
+        // beta of chunk c (two chunks are live: the next chunk's factors are made before this
+        // chunk's W epilogue)
+        auto beta_ring = [&](int c) { return beta_s + (c & 1) * kChunk; };
+        // decay factors of chunk c (from its q, k, g tile)
+        auto factor = [&](const int c) -> bool {
             const int s = c & 1;
             const int valid = min(kChunk, L - kChunk * c);
             const int64_t tok0 = seq0 + (int64_t)kChunk * c;
             unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
             unsigned char* kmh = sm + (s ? OFF_KMH1 : OFF_KMH0);
-            unsigned char* pt = sm + (s ? OFF_P1 : OFF_P0);
-            unsigned char* tb = sm + (s ? OFF_TB1 : OFF_TB0);
-            if (!wait_bar(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+            if (!wait_bar(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
 
             // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7 ----
             uint4 graw[4];
             {
                 float gs[8];
+                float gmax = 0.f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) gs[j] = 0.f;
 #pragma unroll
@@ -538,12 +558,18 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     float gv[8];
                     unpack8(graw[i], gv);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) gs[j] += gv[j];
+                    for (int j = 0; j < 8; ++j) {
+                        gs[j] += gv[j];
+                        gmax = fmaxf(gmax, gv[j]);
+                    }
                 }
+                // With every g <= 0 the cumulative decay G is monotone, so |G - r| <= |G_C| / 2
+                // and one check per channel (in the scan below) bounds every factor.
+                if (gmax > 0.f) report_status(p.status, kStatusDecayRange);
                 *reinterpret_cast<float4*>(part + tg * kDim + c8) = make_float4(gs[0], gs[1], gs[2], gs[3]);
                 *reinterpret_cast<float4*>(part + tg * kDim + c8 + 4) = make_float4(gs[4], gs[5], gs[6], gs[7]);
                 if (tp < kChunk) {
-                    beta_s[tp] = beta_next;
+                    beta_ring(c)[tp] = beta_next;
                     // fetch the next chunk's beta now; it is needed one chunk later
                     const int vn = min(kChunk, L - kChunk * (c + 1));
                     beta_next = tp < vn ? bf2f(p.beta[(tok0 + kChunk + tp) * H + h]) : 0.f;
@@ -561,6 +587,11 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     run += v[g16];
                 }
                 gc_s[tp] = run;
+                if (fabsf(0.5f * run) > kMaxExponentTC) report_status(p.status, kStatusDecayRange);
+                // e^{r} of this chunk and the state scale e^{r_{c-1} + r_c}
+                const float e = ex2_approx((0.5f * kLog2eTC) * run);
+                er[(c & 3) * kDim + tp] = e;
+                sc[(c & 3) * kDim + tp] = c > 0 ? er[((c + 3) & 3) * kDim + tp] * e : e;
             }
             named_bar(kBarPrep, kPrepThreads);
             {
@@ -570,10 +601,14 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const float4 b = *reinterpret_cast<const float4*>(part + tg * kDim + c8 + 4);
                     const float4 ga = *reinterpret_cast<const float4*>(gc_s + c8);
                     const float4 gb = *reinterpret_cast<const float4*>(gc_s + c8 + 4);
-                    G[0] = a.x; G[1] = a.y; G[2] = a.z; G[3] = a.w;
-                    G[4] = b.x; G[5] = b.y; G[6] = b.z; G[7] = b.w;
-                    r[0] = 0.5f * ga.x; r[1] = 0.5f * ga.y; r[2] = 0.5f * ga.z; r[3] = 0.5f * ga.w;
-                    r[4] = 0.5f * gb.x; r[5] = 0.5f * gb.y; r[6] = 0.5f * gb.z; r[7] = 0.5f * gb.w;
+                    // G - r in log2 units (the factors are exp2 of it), from the exclusive prefix
+                    const float hl = 0.5f * kLog2eTC;
+                    r[0] = hl * ga.x; r[1] = hl * ga.y; r[2] = hl * ga.z; r[3] = hl * ga.w;
+                    r[4] = hl * gb.x; r[5] = hl * gb.y; r[6] = hl * gb.z; r[7] = hl * gb.w;
+                    G[0] = fmaf(a.x, kLog2eTC, -r[0]); G[1] = fmaf(a.y, kLog2eTC, -r[1]);
+                    G[2] = fmaf(a.z, kLog2eTC, -r[2]); G[3] = fmaf(a.w, kLog2eTC, -r[3]);
+                    G[4] = fmaf(b.x, kLog2eTC, -r[4]); G[5] = fmaf(b.y, kLog2eTC, -r[5]);
+                    G[6] = fmaf(b.z, kLog2eTC, -r[6]); G[7] = fmaf(b.w, kLog2eTC, -r[7]);
                 }
                 // load every k and q piece of this thread first (the stores below are in place)
                 uint4 kraw[4], qraw[4];
@@ -583,7 +618,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     kraw[i] = *reinterpret_cast<const uint4*>(kq + sw128_offset(t, c8, KQW_ROWS));
                     qraw[i] = *reinterpret_cast<const uint4*>(kq + sw128_offset(64 + t, c8, KQW_ROWS));
                 }
-                bool bad = false;
+                uint4 kmp[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int t = 4 * tg + i;
@@ -594,54 +629,55 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     float kp[8], qr[8], km[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        G[j] += gv[j];
-                        const float d = (G[j] - r[j]) * kLog2eTC;
-                        bad |= fabsf(d) > kMaxExponentTC * kLog2eTC;
-                        const float e = ex2_approx(d);
-                        const float ei = ex2_approx(-d);
+                        G[j] = fmaf(gv[j], kLog2eTC, G[j]);  // G - r, log2 units
+                        const float e = ex2_approx(G[j]);
+                        const float ei = ex2_approx(-G[j]);
                         kp[j] = kv[j] * e;
                         qr[j] = qv[j] * e;
                         km[j] = kv[j] * ei;
                     }
                     *reinterpret_cast<uint4*>(kq + sw128_offset(t, c8, KQW_ROWS)) = pack8(kp);
                     *reinterpret_cast<uint4*>(kq + sw128_offset(64 + t, c8, KQW_ROWS)) = pack8(qr);
-                    const uint32_t om = sw128_offset(t, c8, 64);
-                    *reinterpret_cast<uint4*>(kmh + om) = pack8(km);
+                    kmp[i] = pack8(km);
                 }
-                if (bad) report_status(p.status, kStatusDecayRange);
-                if (tg == 0) {
-                    float* ers = er + (c & 3) * kDim + c8;
-                    float* scs = sc + (c & 3) * kDim + c8;
-                    const float* erp = er + ((c + 3) & 3) * kDim + c8;
+                // K_m of this slot is overwritten only after M6 two chunks back has read it
+                if (c >= 2 &&
+                    !wait_bar(&bars[B_KMFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
+                    return false;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float e = ex2_approx(r[j] * kLog2eTC);
-                        ers[j] = e;
-                        scs[j] = c > 0 ? erp[j] * e : e;
-                    }
-                }
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint4*>(kmh + sw128_offset(4 * tg + i, c8, 64)) = kmp[i];
             }
             fence_async_shared();
             named_bar(kBarPrep, kPrepThreads);
             if (tp == 0) mbar_arrive(&bars[B_FACT0 + s]);
-
+            return true;
+        };
+        // A and P of chunk c from TMEM
+        auto ap_epilogue = [&](const int c) -> bool {
+            const int s = c & 1;
+            unsigned char* pt = sm + (s ? OFF_P1 : OFF_P0);
             // ---- A (rows 0-63) and P (rows 64-127) from TMEM ----
-            if (!wait_bar(&bars[B_AP0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+            if (!wait_bar(&bars[B_AP0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
+            if (c >= 2 &&
+                !wait_bar(&bars[B_PFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
+                return false;
             tc_fence_after();
             {
                 uint32_t v[32];
                 tmem_ld32(tmem + T_P + 32 * colhalf + lane_off, v);
                 if (row_abs < kChunk) {
                     const int t = row_abs;
-                    const float bt = beta_s[t];
+                    const float bt = beta_ring(c)[t];
+                    // only the strictly lower triangle is ever read, so it is stored unmasked
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
                         float4 o;
                         const int col = 32 * colhalf + 4 * j4;
-                        o.x = col + 0 < t ? bt * __uint_as_float(v[4 * j4 + 0]) : 0.f;
-                        o.y = col + 1 < t ? bt * __uint_as_float(v[4 * j4 + 1]) : 0.f;
-                        o.z = col + 2 < t ? bt * __uint_as_float(v[4 * j4 + 2]) : 0.f;
-                        o.w = col + 3 < t ? bt * __uint_as_float(v[4 * j4 + 3]) : 0.f;
+                        o.x = bt * __uint_as_float(v[4 * j4 + 0]);
+                        o.y = bt * __uint_as_float(v[4 * j4 + 1]);
+                        o.z = bt * __uint_as_float(v[4 * j4 + 2]);
+                        o.w = bt * __uint_as_float(v[4 * j4 + 3]);
                         *reinterpret_cast<float4*>(Am + t * LDA_T + col) = o;
                     }
                 } else {
@@ -667,22 +703,27 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             tc_fence_before();
             named_bar(kBarPrep, kPrepThreads);
-
+            return true;
+        };
+        // T diag(beta) of chunk c
+        auto inverse = [&](const int c) -> void {
+            const int s = c & 1;
+            unsigned char* tb = sm + (s ? OFF_TB1 : OFF_TB0);
             // ---- T = (I + A)^{-1}: 16x16 diagonal blocks by forward substitution ----
             if (tp < 64) {
                 const int b = tp >> 4, col = tp & 15;
                 const float* Ab = Am + (16 * b) * LDA_T + 16 * b;
                 float x[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float sacc = (i == col) ? 1.f : 0.f;
+                for (int i = 0; i < 16; ++i) {  // four partial sums shorten the dependency chain
+                    float s4[4] = {(i == col) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int j = 0; j < i; ++j) sacc = fmaf(-Ab[i * LDA_T + j], x[j], sacc);
-                    x[i] = sacc;
+                    for (int j = 0; j < i; ++j) s4[j & 3] = fmaf(-Ab[i * LDA_T + j], x[j], s4[j & 3]);
+                    x[i] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
                 }
                 __syncwarp();
                 float* Tb = Am + (16 * b) * LDA_T + 16 * b;
-                const float bc = beta_s[16 * b + col];
+                const float bc = beta_ring(c)[16 * b + col];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     Tb[i * LDA_T + col] = x[i];
@@ -732,27 +773,59 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 float acc[2][4];
                 block_product(acc, Am + (16 * I) * LDA_T + 16 * J, LDA_T, -1.f, n2, n3,
                               Am + (16 * J) * LDA_T + 16 * J, LDA_T, lane);
-                store_block_tb(tb, I, J, acc, beta_s, lane);
+                store_block_tb(tb, I, J, acc, beta_ring(c), lane);
             }
             fence_async_shared();
             named_bar(kBarPrep, kPrepThreads);
             if (tp == 0) mbar_arrive(&bars[B_TB0 + s]);
-
+        };
+        // -W of chunk c into its slot tile
+        auto w_epilogue = [&](const int c) -> bool {
+            const int s = c & 1;
+            unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
             // ---- -W into rows 128-191 of the slot tile (K-major [t][c]) ----
-            if (!wait_bar(&bars[B_WDONE0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+            if (!wait_bar(&bars[B_WDONE0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
             tc_fence_after();
             {
                 uint32_t v[32];
-                tmem_ld32(tmem + T_P + 32 * colhalf + lane_off, v);  // W^T[c = row_abs][t]
+                const uint32_t rW = tmem + (s ? T_X1 : T_X0) + 32 * colhalf + lane_off;
+                tmem_ld32(rW, v);  // W^T[c = row_abs][t]
+                // Lanes 2i and 2i+1 hold channels ch0 and ch0+1.  They swap one value per token
+                // pair (j, j+4) so that the even lane stores token j and the odd lane token j+4,
+                // each as the bf16 pair (ch0, ch0+1); rows four apart put the two half-warps on
+                // disjoint banks of the swizzled tile.
+                const bool odd = lane & 1;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    *reinterpret_cast<bf16*>(kq + sw128_offset(128 + 32 * colhalf + j, row_abs, KQW_ROWS)) =
-                        __float2bfloat16_rn(-__uint_as_float(v[j]));
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = (jj & 3) + 8 * (jj >> 2);
+                    const float lo = __uint_as_float(v[j]), hi = __uint_as_float(v[j + 4]);
+                    const float recv = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+                    const float a = odd ? recv : lo;  // channel ch0
+                    const float b = odd ? hi : recv;  // channel ch0 + 1
+                    const int t = 128 + 32 * colhalf + j + (odd ? 4 : 0);
+                    *reinterpret_cast<uint32_t*>(kq + sw128_offset(t, row_abs & ~1, KQW_ROWS)) =
+                        pack_bf16(-a, -b);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0u;
+                tmem_st32(rW, v);  // O^T of this chunk accumulates from zero in M4
+                tmem_st_wait();
             }
             tc_fence_before();
             fence_async_shared();
             named_bar(kBarPrep, kPrepThreads);
             if (tp == 0) mbar_arrive(&bars[B_WN0 + s]);
+            return true;
+        };
+        // Software pipeline: the W epilogue of chunk c-1 runs while the tensor core forms A and P
+        // of chunk c, and the factors of chunk c+1 while it forms W of chunk c.
+        if (factor(0)) {
+            for (int c = 0; c < nchunks; ++c) {
+                if (c > 0 && !w_epilogue(c - 1)) break;
+                if (!ap_epilogue(c)) break;
+                inverse(c);
+                if (c + 1 < nchunks ? !factor(c + 1) : !w_epilogue(c)) break;
+            }
         }
     } else {
         // ------------------------------------------------------------ serial epilogue
@@ -778,13 +851,6 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tmem_st32(tmem + T_S + cc + lane_off, x);
                 tmem_st16(tmem + T_SA + cc / 2 + lane_off, xb);
             }
-            {  // O^T of both chunk blocks starts at zero
-                uint32_t z[64];
-#pragma unroll
-                for (int j = 0; j < 64; ++j) z[j] = 0u;
-                tmem_st64(tmem + T_X0 + lane_off, z);
-                tmem_st64(tmem + T_X1 + lane_off, z);
-            }
             tmem_st_wait();
             tc_fence_before();
             named_bar(kBarEpi, kEpiThreads);
@@ -797,6 +863,9 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             // ---- E1: U^T -> bf16 hi/lo A operands ----
             if (!(ok = wait_bar(&bars[B_XDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
+            // M1 and M2 (before W was written) and now M4 have read this slot's K_p / Q_r / -W
+            // tile: refill it with chunk c + 2 (K_m of the slot is guarded by B_KMFREE)
+            if (te == 0 && c + 2 < nchunks) issue_kqg(c + 2);
             {
                 // read all 64 columns of U^T before writing hi / lo over them
                 uint32_t u[64], lo[32];
@@ -821,10 +890,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (te == 0) mbar_arrive(&bars[B_UREADY]);
 
             // ---- E2: state rescale first (the next chunk's M4 waits on it), then O to HBM ----
-            if (!(ok = wait_bar(&bars[B_OSDONE], c & 1, abort_flag, p.status))) break;
+            if (!(ok = wait_bar(&bars[B_SDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
-            // every MMA that reads slot c & 1 has completed: refill it with chunk c + 2
-            if (te == 0 && c + 2 < nchunks) issue_kqg(c + 2);
             const bool last = (c + 1 == nchunks);
             if (!last) {
                 if (!(ok = wait_bar(&bars[B_FACT0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, abort_flag,
@@ -864,23 +931,29 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         fs[(cc + j) * kDim + vch] = __uint_as_float(x[j]) * ec[cc + j];
                 }
             }
+            if (!(ok = wait_bar(&bars[B_OSDONE], c & 1, abort_flag, p.status))) break;
+            tc_fence_after();
             {
                 uint32_t o[64];
                 if (has_out) {
                     tmem_ld64(rX, o);
-                    bf16* op = p.out + (tok0 * H + h) * kDim + vch;
+                    // lanes 2i and 2i+1 (channels e, e+1) swap one value per token pair so that
+                    // the even lane stores token t and the odd lane token t+1 as a bf16 pair
+                    const bool odd = lane & 1;
                     const int64_t tstride = (int64_t)H * kDim;
+                    bf16* op = p.out + ((tok0 + (odd ? 1 : 0)) * H + h) * kDim + (vch & ~1);
 #pragma unroll
-                    for (int t = 0; t < 64; ++t) {
-                        if (t < valid) *op = __float2bfloat16_rn(__uint_as_float(o[t]));
-                        op += tstride;
+                    for (int t = 0; t < 64; t += 2) {
+                        const float lo = __uint_as_float(o[t]), hi = __uint_as_float(o[t + 1]);
+                        const float recv = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+                        const float a = odd ? recv : lo;  // channel e
+                        const float b = odd ? hi : recv;  // channel e + 1
+                        if (t + (odd ? 1 : 0) < valid)
+                            *reinterpret_cast<uint32_t*>(op) = pack_bf16(a, b);
+                        op += 2 * tstride;
                     }
                 }
-                if (!last) {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) o[j] = 0u;
-                    tmem_st64(rX, o);  // O^T of this block restarts at zero two chunks later
-                    tmem_st_wait();
+                if (!last) {  // the block is free for chunk c + 2
                     tc_fence_before();
                     named_bar(kBarEpi, kEpiThreads);
                     if (te == 0) mbar_arrive(&bars[B_UFREE0 + (c & 1)]);
