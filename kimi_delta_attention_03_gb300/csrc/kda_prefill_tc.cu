@@ -218,9 +218,8 @@ __device__ __forceinline__ void store_block_tb(unsigned char* tb, int I, int J,
 __device__ __forceinline__ int pair_i(int w) { return w < 1 ? 1 : (w < 3 ? 2 : 3); }
 __device__ __forceinline__ int pair_j(int w) { const int I = pair_i(w); return w - I * (I - 1) / 2; }
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool wait_bar_poll(uint64_t* bar, uint32_t parity,
+                                           volatile int* abort_flag, int* status) {
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -232,13 +231,17 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
         }
     }
 }
+// Wait for a barrier phase; the polling loop is out of line to keep the kernel's code small.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+    return mbar_try_wait(bar, parity) || wait_bar_poll(bar, parity, abort_flag, status);
+}
 
 // Issuer threads poll with a short suspend-time hint: a plain try_wait is woken late when the
 // phase is completed by another thread's arrive, and a tight test_wait loop takes issue slots
 // from the compute warps sharing the sub-partition.
-__device__ __forceinline__ bool spin_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         int* status) {
-    if (mbar_test(bar, parity)) return true;
+__device__ __noinline__ bool spin_bar_poll(uint64_t* bar, uint32_t parity,
+                                           volatile int* abort_flag, int* status) {
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait_hint(bar, parity, 40)) return true;
@@ -249,6 +252,10 @@ __device__ __forceinline__ bool spin_bar(uint64_t* bar, uint32_t parity, volatil
             return false;
         }
     }
+}
+__device__ __forceinline__ bool spin_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+    return mbar_test(bar, parity) || spin_bar_poll(bar, parity, abort_flag, status);
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
@@ -544,19 +551,19 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (!wait_bar(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
 
             // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7 ----
-            uint4 graw[4];
             {
                 float gs[8];
                 float gmax = 0.f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) gs[j] = 0.f;
-#pragma unroll
+#pragma unroll 1
                 for (int i = 0; i < 4; ++i) {
                     const int t = 4 * tg + i;
-                    graw[i] = t < valid ? *reinterpret_cast<const uint4*>(kq + sw128_offset(128 + t, c8, KQW_ROWS))
-                                        : make_uint4(0u, 0u, 0u, 0u);
+                    uint4 gr = make_uint4(0u, 0u, 0u, 0u);  // g is zero past the sequence end
+                    if (t < valid)
+                        gr = *reinterpret_cast<const uint4*>(kq + sw128_offset(128 + t, c8, KQW_ROWS));
                     float gv[8];
-                    unpack8(graw[i], gv);
+                    unpack8(gr, gv);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         gs[j] += gv[j];
@@ -610,22 +617,25 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     G[4] = fmaf(b.x, kLog2eTC, -r[4]); G[5] = fmaf(b.y, kLog2eTC, -r[5]);
                     G[6] = fmaf(b.z, kLog2eTC, -r[6]); G[7] = fmaf(b.w, kLog2eTC, -r[7]);
                 }
-                // load every k and q piece of this thread first (the stores below are in place)
-                uint4 kraw[4], qraw[4];
-#pragma unroll
+                // K_m of this slot is overwritten only after M6 two chunks back has read it
+                if (c >= 2 &&
+                    !wait_bar(&bars[B_KMFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
+                    return false;
+#pragma unroll 1
                 for (int i = 0; i < 4; ++i) {
+                    // one token per step; rows t, 64 + t and 128 + t of the slot tile (k, q, g)
+                    // share the swizzle phase t & 7, so one offset serves all three, and k, q are
+                    // replaced in place by K_p, Q_r
                     const int t = 4 * tg + i;
-                    kraw[i] = *reinterpret_cast<const uint4*>(kq + sw128_offset(t, c8, KQW_ROWS));
-                    qraw[i] = *reinterpret_cast<const uint4*>(kq + sw128_offset(64 + t, c8, KQW_ROWS));
-                }
-                uint4 kmp[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int t = 4 * tg + i;
+                    const uint32_t o = sw128_offset(t, c8, KQW_ROWS);
+                    uint4 gr = make_uint4(0u, 0u, 0u, 0u);
+                    if (t < valid) gr = *reinterpret_cast<const uint4*>(kq + o + 128 * 128);
+                    const uint4 kr = *reinterpret_cast<const uint4*>(kq + o);
+                    const uint4 qr4 = *reinterpret_cast<const uint4*>(kq + o + 64 * 128);
                     float gv[8], kv[8], qv[8];
-                    unpack8(graw[i], gv);
-                    unpack8(kraw[i], kv);
-                    unpack8(qraw[i], qv);
+                    unpack8(gr, gv);
+                    unpack8(kr, kv);
+                    unpack8(qr4, qv);
                     float kp[8], qr[8], km[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -636,17 +646,10 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         qr[j] = qv[j] * e;
                         km[j] = kv[j] * ei;
                     }
-                    *reinterpret_cast<uint4*>(kq + sw128_offset(t, c8, KQW_ROWS)) = pack8(kp);
-                    *reinterpret_cast<uint4*>(kq + sw128_offset(64 + t, c8, KQW_ROWS)) = pack8(qr);
-                    kmp[i] = pack8(km);
+                    *reinterpret_cast<uint4*>(kq + o) = pack8(kp);
+                    *reinterpret_cast<uint4*>(kq + o + 64 * 128) = pack8(qr);
+                    *reinterpret_cast<uint4*>(kmh + sw128_offset(t, c8, 64)) = pack8(km);
                 }
-                // K_m of this slot is overwritten only after M6 two chunks back has read it
-                if (c >= 2 &&
-                    !wait_bar(&bars[B_KMFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
-                    return false;
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    *reinterpret_cast<uint4*>(kmh + sw128_offset(4 * tg + i, c8, 64)) = kmp[i];
             }
             fence_async_shared();
             named_bar(kBarPrep, kPrepThreads);
@@ -898,7 +901,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                     p.status)))
                     break;
                 const float* scn = sc + ((c + 1) & 3) * kDim;
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < kDim; cc += 32) {
                     uint32_t x[32], xb[16];
                     tmem_ld32(tmem + T_S + cc + lane_off, x);
@@ -923,6 +926,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             } else if (final_dst) {
                 const float* ec = er + (c & 3) * kDim;
                 float* fs = final_dst;
+#pragma unroll 1
                 for (int cc = 0; cc < kDim; cc += 32) {
                     uint32_t x[32];
                     tmem_ld32(tmem + T_S + cc + lane_off, x);
@@ -934,23 +938,26 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (!(ok = wait_bar(&bars[B_OSDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
             {
-                uint32_t o[64];
                 if (has_out) {
-                    tmem_ld64(rX, o);
                     // lanes 2i and 2i+1 (channels e, e+1) swap one value per token pair so that
                     // the even lane stores token t and the odd lane token t+1 as a bf16 pair
                     const bool odd = lane & 1;
                     const int64_t tstride = (int64_t)H * kDim;
                     bf16* op = p.out + ((tok0 + (odd ? 1 : 0)) * H + h) * kDim + (vch & ~1);
+#pragma unroll 1
+                    for (int t0 = 0; t0 < 64; t0 += 16) {
+                        uint32_t o[16];
+                        tmem_ld16(rX + t0, o);
 #pragma unroll
-                    for (int t = 0; t < 64; t += 2) {
-                        const float lo = __uint_as_float(o[t]), hi = __uint_as_float(o[t + 1]);
-                        const float recv = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
-                        const float a = odd ? recv : lo;  // channel e
-                        const float b = odd ? hi : recv;  // channel e + 1
-                        if (t + (odd ? 1 : 0) < valid)
-                            *reinterpret_cast<uint32_t*>(op) = pack_bf16(a, b);
-                        op += 2 * tstride;
+                        for (int t = 0; t < 16; t += 2) {
+                            const float lo = __uint_as_float(o[t]), hi = __uint_as_float(o[t + 1]);
+                            const float recv = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+                            const float a = odd ? recv : lo;  // channel e
+                            const float b = odd ? hi : recv;  // channel e + 1
+                            if (t0 + t + (odd ? 1 : 0) < valid)
+                                *reinterpret_cast<uint32_t*>(op) = pack_bf16(a, b);
+                            op += 2 * tstride;
+                        }
                     }
                 }
                 if (!last) {  // the block is free for chunk c + 2
