@@ -417,41 +417,44 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 mma_commit(&bars[B_AP0 + s]);
                 return true;
             };
-            bool run = issue_m1(0);
-            for (int c = 0; run && c < nchunks; ++c) {
-                const int s = c & 1;
-                // M2: W^T = K_p^T (T diag(beta))^T into the O^T columns of this chunk's block,
-                // once the epilogue has read that block two chunks ago.  (A per-slot barrier: a
-                // single one could run two phases ahead of this wait.)
-                if (!spin_bar(&bars[B_TB0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
-                if (c >= 2 &&
-                    !spin_bar(&bars[B_UFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
-                    break;
-                tc_fence_after();
-                const uint32_t rX = tmem + (s ? T_X1 : T_X0);
-                {
-                    const uint64_t da = smem_desc(a_kq(s), KQW_REGION, 1024);
-                    const uint64_t db = smem_desc(a_tb(s), 16, 1024);
+            for (int c = -1; c < nchunks; ++c) {  // M1 of chunk 0 first, then chunk by chunk
+                if (c >= 0) {
+                    const int s = c & 1;
+                    // M2: W^T = K_p^T (T diag(beta))^T into the O^T columns of this chunk's block,
+                    // once the epilogue has read that block two chunks ago.  (A per-slot barrier: a
+                    // single one could run two phases ahead of this wait.)
+                    if (!spin_bar(&bars[B_TB0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                    if (c >= 2 &&
+                        !spin_bar(&bars[B_UFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
+                        break;
+                    tc_fence_after();
+                    const uint32_t rX = tmem + (s ? T_X1 : T_X0);
+                    {
+                        const uint64_t da = smem_desc(a_kq(s), KQW_REGION, 1024);
+                        const uint64_t db = smem_desc(a_tb(s), 16, 1024);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) mma_ss(rX, da + 128 * j, db + 2 * j, id_mk64, j > 0);
-                }
-                mma_commit(&bars[B_WDONE0 + s]);
-                // M3: U_bar^T = V^T (T diag(beta))^T into the U^T columns, once v has landed
-                if (!spin_bar(&bars[B_VFULL], c & 1, abort_flag, p.status)) break;
-                tc_fence_after();
-                {
-                    const uint64_t da = smem_desc(a_v, 8192, 1024);
-                    const uint64_t db = smem_desc(a_tb(s), 16, 1024);
+                        for (int j = 0; j < 4; ++j)
+                            mma_ss(rX, da + 128 * j, db + 2 * j, id_mk64, j > 0);
+                    }
+                    mma_commit(&bars[B_WDONE0 + s]);
+                    // M3: U_bar^T = V^T (T diag(beta))^T into the U^T columns, once v has landed
+                    if (!spin_bar(&bars[B_VFULL], c & 1, abort_flag, p.status)) break;
+                    tc_fence_after();
+                    {
+                        const uint64_t da = smem_desc(a_v, 8192, 1024);
+                        const uint64_t db = smem_desc(a_tb(s), 16, 1024);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma_ss(rX + 64, da + 128 * j, db + 2 * j, id_mk64, j > 0);
-                }
-                mma_commit(&bars[B_VFREE0 + s]);
-                // the v buffer is free once M3 has read it: load the next chunk's v
-                if (c + 1 < nchunks) {
-                    if (!spin_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
-                    issue_v(c + 1);
-                    v_issued = c + 2;
+                        for (int j = 0; j < 4; ++j)
+                            mma_ss(rX + 64, da + 128 * j, db + 2 * j, id_mk64, j > 0);
+                    }
+                    mma_commit(&bars[B_VFREE0 + s]);
+                    // the v buffer is free once M3 has read it: load the next chunk's v
+                    if (c + 1 < nchunks) {
+                        if (!spin_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status))
+                            break;
+                        issue_v(c + 1);
+                        v_issued = c + 2;
+                    }
                 }
                 // the next chunk's factors follow this chunk's inverse
                 if (c + 1 < nchunks && !issue_m1(c + 1)) break;
@@ -693,9 +696,10 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const int col = 32 * colhalf + 8 * j8 + 2 * u;
                             const float x0 = col <= t ? __uint_as_float(v[8 * j8 + 2 * u]) : 0.f;
                             const float x1 = col + 1 <= t ? __uint_as_float(v[8 * j8 + 2 * u + 1]) : 0.f;
-                            const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-                            hi[u] = pack_bf16(bf2f(h0), bf2f(h1));
-                            lo[u] = pack_bf16(x0 - bf2f(h0), x1 - bf2f(h1));
+                            const uint32_t hh = pack_bf16(x0, x1);
+                            hi[u] = hh;
+                            lo[u] = pack_bf16(x0 - __uint_as_float(hh << 16),
+                                              x1 - __uint_as_float(hh & 0xffff0000u));
                         }
                         const uint32_t off = sw128_offset(t, 32 * colhalf + 8 * j8, 64);
                         *reinterpret_cast<uint4*>(pt + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -721,7 +725,13 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 for (int i = 0; i < 16; ++i) {  // four partial sums shorten the dependency chain
                     float s4[4] = {(i == col) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int j = 0; j < i; ++j) s4[j & 3] = fmaf(-Ab[i * LDA_T + j], x[j], s4[j & 3]);
+                    for (int q = 0; 4 * q < i; ++q) {  // row i read four entries at a time
+                        const float4 a = *reinterpret_cast<const float4*>(Ab + i * LDA_T + 4 * q);
+                        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            if (4 * q + u < i) s4[u] = fmaf(-av[u], x[4 * q + u], s4[u]);
+                    }
                     x[i] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
                 }
                 __syncwarp();
@@ -747,25 +757,26 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             named_bar(kBarPrep, kPrepThreads);
             if (wp < 3) {  // N^2_20, N^2_31 (then N^3_30 = N^2_31 N_10), N^2_30
+                // wp 0: N^2_20 = N_21 N_10;  wp 1: N^2_31 = N_32 N_21, then N^3_30 = N^2_31 N_10;
+                // wp 2: N^2_30 = N_31 N_10 + N_32 N_20.  One code path, operands picked per warp.
                 float acc[2][4];
-                if (wp == 0) {
-                    block_product(acc, Am + 32 * LDA_T + 16, LDA_T, 1.f, nullptr, 0,
-                                  Am + 16 * LDA_T, LDA_T, lane);
-                    store_block(Y + 0 * 256, 16, acc, lane);
-                } else if (wp == 1) {
-                    block_product(acc, Am + 48 * LDA_T + 32, LDA_T, 1.f, nullptr, 0,
-                                  Am + 32 * LDA_T + 16, LDA_T, lane);
-                    store_block(Y + 1 * 256, 16, acc, lane);
-                    __syncwarp();
-                    block_product(acc, Y + 1 * 256, 16, 1.f, nullptr, 0, Am + 16 * LDA_T, LDA_T,
-                                  lane);
-                    store_block(Y + 3 * 256, 16, acc, lane);
-                } else {
-                    block_product(acc, Am + 48 * LDA_T + 16, LDA_T, 1.f, nullptr, 0,
-                                  Am + 16 * LDA_T, LDA_T, lane);
-                    block_product_acc(acc, Am + 48 * LDA_T + 32, LDA_T, Am + 32 * LDA_T, LDA_T, lane);
-                    store_block(Y + 2 * 256, 16, acc, lane);
+                block_product(acc,
+                              Am + (wp == 0 ? 32 * LDA_T + 16 : wp == 1 ? 48 * LDA_T + 32 : 48 * LDA_T + 16),
+                              LDA_T, 1.f, nullptr, nullptr,
+                              Am + (wp == 1 ? 32 * LDA_T + 16 : 16 * LDA_T), LDA_T, lane);
+                if (wp != 0) {
+                    if (wp == 1) {
+                        store_block(Y + 256, 16, acc, lane);
+                        __syncwarp();
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+                            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+                    }
+                    block_mma(acc, wp == 1 ? Y + 256 : Am + 48 * LDA_T + 32, wp == 1 ? 16 : LDA_T,
+                              1.f, nullptr, nullptr, Am + (wp == 1 ? 16 * LDA_T : 32 * LDA_T), LDA_T,
+                              lane);
                 }
+                store_block(Y + 256 * (wp == 0 ? 0 : wp == 1 ? 3 : 2), 16, acc, lane);
             }
             named_bar(kBarPrep, kPrepThreads);
             if (wp < 6) {  // T_IJ = C_IJ T_JJ with C = -N + N^2 - N^3 (block by block)
@@ -793,21 +804,21 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 uint32_t v[32];
                 const uint32_t rW = tmem + (s ? T_X1 : T_X0) + 32 * colhalf + lane_off;
                 tmem_ld32(rW, v);  // W^T[c = row_abs][t]
-                // Lanes 2i and 2i+1 hold channels ch0 and ch0+1.  They swap one value per token
-                // pair (j, j+4) so that the even lane stores token j and the odd lane token j+4,
-                // each as the bf16 pair (ch0, ch0+1); rows four apart put the two half-warps on
-                // disjoint banks of the swizzled tile.
+                // Lanes 2i and 2i+1 hold channels ch0 and ch0+1.  Each packs its own tokens
+                // (j, j+4) and the two swap words: the even lane stores the low halves (token j),
+                // the odd lane the high halves (token j+4), each as the bf16 pair (ch0, ch0+1).
+                // Rows four apart put the two half-warps on disjoint banks of the swizzled tile.
                 const bool odd = lane & 1;
+                const uint32_t sel = odd ? 0x3276u : 0x5410u;
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int j = (jj & 3) + 8 * (jj >> 2);
-                    const float lo = __uint_as_float(v[j]), hi = __uint_as_float(v[j + 4]);
-                    const float recv = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
-                    const float a = odd ? recv : lo;  // channel ch0
-                    const float b = odd ? hi : recv;  // channel ch0 + 1
+                    const uint32_t mine =
+                        pack_bf16(-__uint_as_float(v[j]), -__uint_as_float(v[j + 4]));
+                    const uint32_t partner = __shfl_xor_sync(0xffffffffu, mine, 1);
                     const int t = 128 + 32 * colhalf + j + (odd ? 4 : 0);
                     *reinterpret_cast<uint32_t*>(kq + sw128_offset(t, row_abs & ~1, KQW_ROWS)) =
-                        pack_bf16(-a, -b);
+                        __byte_perm(mine, partner, sel);
                 }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0u;
@@ -822,13 +833,14 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         };
         // Software pipeline: the W epilogue of chunk c-1 runs while the tensor core forms A and P
         // of chunk c, and the factors of chunk c+1 while it forms W of chunk c.
-        if (factor(0)) {
-            for (int c = 0; c < nchunks; ++c) {
-                if (c > 0 && !w_epilogue(c - 1)) break;
+        // Each phase has a single call site (the lambdas are inlined where they are called).
+        for (int c = -1; c <= nchunks; ++c) {
+            if (c >= 1 && !w_epilogue(c - 1)) break;
+            if (c >= 0 && c < nchunks) {
                 if (!ap_epilogue(c)) break;
                 inverse(c);
-                if (c + 1 < nchunks ? !factor(c + 1) : !w_epilogue(c)) break;
             }
+            if (c + 1 < nchunks && !factor(c + 1)) break;
         }
     } else {
         // ------------------------------------------------------------ serial epilogue
@@ -939,9 +951,10 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc_fence_after();
             {
                 if (has_out) {
-                    // lanes 2i and 2i+1 (channels e, e+1) swap one value per token pair so that
+                    // lanes 2i and 2i+1 (channels e, e+1) swap their packed token pairs so that
                     // the even lane stores token t and the odd lane token t+1 as a bf16 pair
                     const bool odd = lane & 1;
+                    const uint32_t sel = odd ? 0x3276u : 0x5410u;  // as in the W epilogue
                     const int64_t tstride = (int64_t)H * kDim;
                     bf16* op = p.out + ((tok0 + (odd ? 1 : 0)) * H + h) * kDim + (vch & ~1);
 #pragma unroll 1
@@ -950,12 +963,11 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         tmem_ld16(rX + t0, o);
 #pragma unroll
                         for (int t = 0; t < 16; t += 2) {
-                            const float lo = __uint_as_float(o[t]), hi = __uint_as_float(o[t + 1]);
-                            const float recv = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
-                            const float a = odd ? recv : lo;  // channel e
-                            const float b = odd ? hi : recv;  // channel e + 1
+                            const uint32_t mine =
+                                pack_bf16(__uint_as_float(o[t]), __uint_as_float(o[t + 1]));
+                            const uint32_t partner = __shfl_xor_sync(0xffffffffu, mine, 1);
                             if (t0 + t + (odd ? 1 : 0) < valid)
-                                *reinterpret_cast<uint32_t*>(op) = pack_bf16(a, b);
+                                *reinterpret_cast<uint32_t*>(op) = __byte_perm(mine, partner, sel);
                             op += 2 * tstride;
                         }
                     }
