@@ -154,21 +154,36 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 // acc += (xs * X + n2 - n3) Yb for 16 x 16 blocks; n2 / n3 (leading dim 16) may be null.
+// Four 8 x 4 fp32 tiles (as 8 x 8 b16 matrices) in one instruction: lane l gives the address
+// of row l & 7 of tile l >> 3, and register i of lane l receives tile i's element
+// (l / 4, l % 4).  Rows must start on 16-byte boundaries.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const float* row) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr(row))
+                 : "memory");
+}
+// acc += (xs X + n2 - n3) Yb for 16 x 16 blocks (n2, n3 optional, stride 16).  The A fragments
+// (rows g, g + 8; columns k0 + t, k0 + t + 4) come from ldmatrix: tiles (rows 0-7 | 8-15) x
+// (columns k0..k0+3 | k0+4..k0+7).
 __device__ __forceinline__ void block_mma(float (&acc)[2][4], const float* X, int ldx, float xs,
                                           const float* n2, const float* n3, const float* Yb,
                                           int ldy, int lane) {
     const int g = lane >> 2, t = lane & 3;
+    const int mrow = (lane & 7) + ((lane & 8) ? 8 : 0), mcol = (lane & 16) ? 4 : 0;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
         const int k0 = 8 * ks;
-        const int r[4] = {g, g + 8, g, g + 8};
-        const int cc[4] = {k0 + t, k0 + t, k0 + t + 4, k0 + t + 4};
         uint32_t a[4];
+        ldsm_x4(a, X + mrow * ldx + k0 + mcol);
+        uint32_t a2[4] = {0u, 0u, 0u, 0u}, a3[4] = {0u, 0u, 0u, 0u};
+        if (n2) ldsm_x4(a2, n2 + mrow * 16 + k0 + mcol);
+        if (n3) ldsm_x4(a3, n3 + mrow * 16 + k0 + mcol);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float x = xs * X[r[i] * ldx + cc[i]];
-            if (n2) x += n2[r[i] * 16 + cc[i]];
-            if (n3) x -= n3[r[i] * 16 + cc[i]];
+            float x = xs * __uint_as_float(a[i]);
+            if (n2) x += __uint_as_float(a2[i]);
+            if (n3) x -= __uint_as_float(a3[i]);
             a[i] = to_tf32(x);
         }
 #pragma unroll
@@ -237,14 +252,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     return mbar_try_wait(bar, parity) || wait_bar_poll(bar, parity, abort_flag, status);
 }
 
-// Issuer threads poll with a short suspend-time hint: a plain try_wait is woken late when the
-// phase is completed by another thread's arrive, and a tight test_wait loop takes issue slots
-// from the compute warps sharing the sub-partition.
+// The issuer threads' wait: a first non-blocking probe, then the same try_wait loop as the
+// other warps (measured: no slower than shorter suspend hints or a test_wait spin).
 __device__ __noinline__ bool spin_bar_poll(uint64_t* bar, uint32_t parity,
                                            volatile int* abort_flag, int* status) {
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait_hint(bar, parity, 40)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitLimit) {
             *abort_flag = 1;
@@ -559,7 +573,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 float gmax = 0.f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) gs[j] = 0.f;
-#pragma unroll 1
+#pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int t = 4 * tg + i;
                     uint4 gr = make_uint4(0u, 0u, 0u, 0u);  // g is zero past the sequence end
@@ -810,19 +824,22 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // Rows four apart put the two half-warps on disjoint banks of the swizzled tile.
                 const bool odd = lane & 1;
                 const uint32_t sel = odd ? 0x3276u : 0x5410u;
+                // Rows t0 + j with j & 7 in 0..3 have swizzle phase (t0 + (j & 3)) & 7, so four
+                // row bases per thread serve every store, plus a compile-time row offset.
+                const int t0 = 128 + 32 * colhalf + (odd ? 4 : 0);
+                unsigned char* wb[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    wb[m] = kq + sw128_offset(t0 + m, row_abs & ~1, KQW_ROWS) - m * 128;
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     const int j = (jj & 3) + 8 * (jj >> 2);
                     const uint32_t mine =
                         pack_bf16(-__uint_as_float(v[j]), -__uint_as_float(v[j + 4]));
                     const uint32_t partner = __shfl_xor_sync(0xffffffffu, mine, 1);
-                    const int t = 128 + 32 * colhalf + j + (odd ? 4 : 0);
-                    *reinterpret_cast<uint32_t*>(kq + sw128_offset(t, row_abs & ~1, KQW_ROWS)) =
-                        __byte_perm(mine, partner, sel);
+                    *reinterpret_cast<uint32_t*>(wb[j & 3] + j * 128) = __byte_perm(mine, partner, sel);
                 }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0u;
-                tmem_st32(rW, v);  // O^T of this chunk accumulates from zero in M4
+                tmem_st32_zero(rW);  // O^T of this chunk accumulates from zero in M4
                 tmem_st_wait();
             }
             tc_fence_before();
