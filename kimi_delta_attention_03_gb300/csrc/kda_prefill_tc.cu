@@ -700,6 +700,41 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         o.w = bt * __uint_as_float(v[4 * j4 + 3]);
                         *reinterpret_cast<float4*>(Am + t * LDA_T + col) = o;
                     }
+                    // ---- T = (I + A)^{-1}, diagonal 16 x 16 blocks by forward substitution.
+                    // The warp that stored a diagonal 32 x 32 quadrant of A inverts its two
+                    // blocks right away (16 lanes per block, one column each) while the other
+                    // warps are still on P.
+                    if (q4 == colhalf) {
+                        __syncwarp();
+                        const int b = 2 * q4 + (lane >> 4), col = lane & 15;
+                        unsigned char* tb = sm + (s ? OFF_TB1 : OFF_TB0);
+                        const float* Ab = Am + (16 * b) * LDA_T + 16 * b;
+                        float x[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {  // four partial sums shorten the chain
+                            float s4[4] = {(i == col) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int q = 0; 4 * q < i; ++q) {  // row i, four entries at a time
+                                const float4 a4 =
+                                    *reinterpret_cast<const float4*>(Ab + i * LDA_T + 4 * q);
+                                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                                for (int u = 0; u < 4; ++u)
+                                    if (4 * q + u < i) s4[u] = fmaf(-av[u], x[4 * q + u], s4[u]);
+                            }
+                            x[i] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                        }
+                        __syncwarp();
+                        float* Tb = Am + (16 * b) * LDA_T + 16 * b;
+                        const float bc = beta_ring(c)[16 * b + col];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            Tb[i * LDA_T + col] = x[i];
+                            *reinterpret_cast<bf16*>(
+                                tb + sw128_offset(16 * b + i, 16 * b + col, 64)) =
+                                __float2bfloat16_rn(x[i] * bc);
+                        }
+                    }
                 } else {
                     const int t = row_abs - kChunk;
 #pragma unroll
@@ -730,35 +765,6 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         auto inverse = [&](const int c) -> void {
             const int s = c & 1;
             unsigned char* tb = sm + (s ? OFF_TB1 : OFF_TB0);
-            // ---- T = (I + A)^{-1}: 16x16 diagonal blocks by forward substitution ----
-            if (tp < 64) {
-                const int b = tp >> 4, col = tp & 15;
-                const float* Ab = Am + (16 * b) * LDA_T + 16 * b;
-                float x[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {  // four partial sums shorten the dependency chain
-                    float s4[4] = {(i == col) ? 1.f : 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int q = 0; 4 * q < i; ++q) {  // row i read four entries at a time
-                        const float4 a = *reinterpret_cast<const float4*>(Ab + i * LDA_T + 4 * q);
-                        const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            if (4 * q + u < i) s4[u] = fmaf(-av[u], x[4 * q + u], s4[u]);
-                    }
-                    x[i] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                }
-                __syncwarp();
-                float* Tb = Am + (16 * b) * LDA_T + 16 * b;
-                const float bc = beta_ring(c)[16 * b + col];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    Tb[i * LDA_T + col] = x[i];
-                    *reinterpret_cast<bf16*>(tb + sw128_offset(16 * b + i, 16 * b + col, 64)) =
-                        __float2bfloat16_rn(x[i] * bc);
-                }
-            }
-            named_bar(kBarPrep, kPrepThreads);
             // ---- off-diagonal blocks on the tensor cores (tf32), with D = blockdiag(T_II) and
             //      N = D A_off (block-nilpotent):  T = (I - N + N^2 - N^3) D ----
             if (wp < 6) {  // N_IJ = T_II A_IJ, in place of A_IJ
