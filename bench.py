@@ -350,19 +350,17 @@ def main():
         host["init_state"] = x["init_state"].cpu().pin_memory()
         host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         host_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
-        dev_in = {nm: torch.empty_like(x[nm]) for nm in names}
-        dev_in["init_state"] = torch.empty_like(x["init_state"])
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = host_out.numel() * host_out.element_size() + host_fin.numel() * 4
 
+        groups = 4
+        h2d += 4 * (len(x["seqlens"]) + groups)  # the per-part cumulative lengths
+
         def estep():
-            for nm, t in host.items():
-                dev_in[nm].copy_(t, non_blocking=True)
-            kda.fwd_chunked(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["log_alpha"],
-                            dev_in["beta"], x["cu_seqlens"], x["seqlens"],
-                            init_state=dev_in["init_state"], out=out, final_state=fin)
-            host_out.copy_(out, non_blocking=True)
-            host_fin.copy_(fin, non_blocking=True)
+            # the public host-buffer call: copies in, kernels, copies out, overlapped by part
+            kda.fwd_chunked_host(host["q"], host["k"], host["v"], host["log_alpha"], host["beta"],
+                                 x["seqlens"], init_state=host["init_state"], out=host_out,
+                                 final_state=host_fin, groups=groups)
 
         for _ in range(2):
             estep()
@@ -371,7 +369,7 @@ def main():
         ems = max_over_ranks(time_device(estep, esteps, stream), world)
         e2e = {"value": tokens_all / (ems * 1e-3) / 1e6, "unit": "Mtokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
-               "steps": esteps}
+               "steps": esteps, "api": "fwd_chunked_host", "parts": groups}
 
     # ---------------- CPU baseline (oracle, rank 0 only, N = 1 only) ----------------
     cpu_base = None

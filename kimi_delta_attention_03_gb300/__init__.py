@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     KdaError,
     decode_step,
     fwd_chunked,
+    fwd_chunked_host,
     fwd_plan,
     fwd_workspace_bytes,
     launch_count,
@@ -19,6 +20,7 @@ from .binding import (  # noqa: F401
 )
 
 __all__ = [
-    "KdaError", "decode_step", "fwd_chunked", "fwd_workspace_bytes", "launch_count",
+    "KdaError", "decode_step", "fwd_chunked", "fwd_chunked_host", "fwd_workspace_bytes",
+    "launch_count",
     "library_path", "load_library", "read_device_status",
 ]

@@ -157,6 +157,29 @@ def test_resume_from_saved_state_and_decode_continuation():
     assert_close("prefill(T+1) last", full_out[T:].float().cpu().numpy(), o_ref1)
 
 
+@pytest.mark.parametrize("groups", [1, 2, 3, 8])
+@pytest.mark.parametrize("init", [True, False])
+def test_host_buffer_call_matches_device_call(groups, init):
+    """fwd_chunked_host (pinned host buffers, copies and kernels overlapped by part) gives the
+    bits of one device call, and matches the oracle."""
+    lens = [1000, 64, 3, 2048, 0, 517, 130]
+    x = synth.make_inputs(lens, 4, torch.bfloat16, seed=21, device=DEV)
+    out_d, fin_d = run_gpu(x, init=init)
+    host = {nm: x[nm].cpu().pin_memory() for nm in ("q", "k", "v", "log_alpha", "beta")}
+    s0 = x["init_state"].cpu().pin_memory() if init else None
+    out_h, fin_h = kda().fwd_chunked_host(host["q"], host["k"], host["v"], host["log_alpha"],
+                                          host["beta"], x["seqlens"], init_state=s0,
+                                          groups=groups)
+    assert out_h.device.type == "cpu" and fin_h.device.type == "cpu"
+    assert torch.equal(out_h, out_d.cpu())
+    assert torch.equal(fin_h, fin_d.cpu())
+    check_status()
+    if groups == 3 and init:
+        o_ref, s_ref = run_oracle(x)
+        assert_close("out", out_h.float().numpy(), o_ref)
+        assert_close("final_state", fin_h.numpy(), s_ref)
+
+
 def test_deterministic():
     x = synth.make_inputs([513, 77], 3, torch.bfloat16, seed=12, device=DEV)
     o1, f1 = run_gpu(x)
