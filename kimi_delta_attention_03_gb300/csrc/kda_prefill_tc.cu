@@ -359,6 +359,11 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (zero_v)  // a transition item carries zero values: v stays zero, never loaded
         for (int e = tid; e < 16384 / 16; e += blockDim.x)
             reinterpret_cast<uint4*>(sm + OFF_V)[e] = make_uint4(0u, 0u, 0u, 0u);
+    if (!has_out)  // no outputs: q is never loaded and its rows stay zero (Q_r unused)
+        for (int e = tid; e < 4 * 8192 / 16; e += blockDim.x)
+            reinterpret_cast<uint4*>(sm + ((e >> 10) ? OFF_KQW1 : OFF_KQW0) +
+                                     ((e >> 9) & 1) * KQW_REGION + 8192)[e & 511] =
+                make_uint4(0u, 0u, 0u, 0u);
     if (tid == 32) {
         for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
@@ -382,11 +387,12 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
         uint64_t* full = &bars[B_FULL0 + s];
         const int t0 = (int)(seq0 + (int64_t)kChunk * c);
-        mbar_arrive_expect_tx(full, 49152);
+        mbar_arrive_expect_tx(full, has_out ? 49152 : 32768);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             tma_load_3d(kq + r * KQW_REGION, &tm_k, full, 64 * r, h, t0);
-            tma_load_3d(kq + r * KQW_REGION + 8192, &tm_q, full, 64 * r, h, t0);
+            if (has_out)  // q only shapes outputs
+                tma_load_3d(kq + r * KQW_REGION + 8192, &tm_q, full, 64 * r, h, t0);
             tma_load_3d(kq + r * KQW_REGION + 16384, &tm_g, full, 64 * r, h, t0);
         }
         *kqg_issued = c + 1;
@@ -735,7 +741,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                 __float2bfloat16_rn(x[i] * bc);
                         }
                     }
-                } else {
+                } else if (has_out) {  // P only shapes outputs
                     const int t = row_abs - kChunk;
 #pragma unroll
                     for (int j8 = 0; j8 < 4; ++j8) {
