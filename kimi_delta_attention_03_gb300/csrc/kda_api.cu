@@ -121,7 +121,8 @@ kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, c
     if (desc->in_dtype == KDA_BF16)
         e = kda::launch_prefill_tc(desc->num_seqs, desc->num_heads, desc->total_tokens, q, k, v,
                                    log_alpha, beta, init_state, cu_seqlens, out, final_state, ws,
-                                   status, (cudaStream_t)stream, &launches);
+                                   status, (cudaStream_t)stream, &launches,
+                                   desc->host_seqlens);
     else
         e = kda::launch_prefill(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v,
                                 log_alpha, beta, init_state, cu_seqlens, out, final_state,

@@ -14,9 +14,12 @@ constexpr int kChunk = 64;    // tokens per chunk of the prefill path
 
 // Segment plan of the prefill (intra-device context parallelism).  A sequence longer than
 // kSplitChunks chunks is cut into segments of kSegChunks chunks; the plan depends on the
-// sequence's own length only, so packing never changes a sequence's results.
+// sequence's own length only, so packing never changes a sequence's results.  A split
+// sequence costs about three passes over its tokens (segment states from zero, segment
+// transitions, then the outputs), so only sequences whose single pass would outlast a
+// typical batch (above 64K tokens) are split.
 constexpr int kSegChunks = 128;
-constexpr int kSplitChunks = 256;
+constexpr int kSplitChunks = 1024;
 __host__ __device__ __forceinline__ int num_segments(int64_t len) {
     const int64_t nc = (len + kChunk - 1) / kChunk;
     return nc > kSplitChunks ? (int)((nc + kSegChunks - 1) / kSegChunks) : 1;
@@ -75,9 +78,21 @@ struct SegWorkspace {
     int max_segments;  // 1 when no sequence is split (the workspace is then unused)
 };
 
+// Dispatch order of the prefill CTAs: sequences ranked by chunk count, longest first (ties in
+// packing order), so that the longest units start in the first wave.  Only the order in which
+// units are scheduled changes; every unit computes the same bits wherever it runs.
+constexpr int kMaxOrdered = 2048;
+struct SeqOrder {
+    int32_t count;                  // ranked sequences; 0 = packing order
+    uint16_t seq[kMaxOrdered];      // seq[rank] = sequence index
+};
+
+// host_seqlens (optional, host memory): the sequence lengths, used only to rank the sequences
+// for dispatch; without them the CTAs run in packing order.
 cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, const void* q,
                               const void* k, const void* v, const void* g, const void* beta,
                               const float* init_state, const int32_t* cu_seqlens, void* out,
                               float* final_state, const SegWorkspace& ws, int* status,
-                              cudaStream_t stream, uint64_t* launches);
+                              cudaStream_t stream, uint64_t* launches,
+                              const int32_t* host_seqlens = nullptr);
 }  // namespace kda

@@ -31,7 +31,10 @@
 // Every wait is bounded; on expiry the CTA records KDA_ERR_TIMEOUT and drains.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
+#include <numeric>
+#include <vector>
 
 #include "kda_common.cuh"
 #include "kda_sm100.cuh"
@@ -276,16 +279,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
 kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_g, const TcParams p) {
+                      const __grid_constant__ CUtensorMap tm_g, const TcParams p,
+                      const __grid_constant__ SeqOrder order) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int n = blockIdx.x;
-    const int h = blockIdx.y;
     const int H = p.H;
+    // blockIdx.x = rank * H + head: all heads of the longest sequence dispatch first
+    const int rank = (int)(blockIdx.x / (unsigned)H);
+    const int h = (int)(blockIdx.x % (unsigned)H);
+    const int n = rank < order.count ? (int)order.seq[rank] : rank;
     const int64_t seq_begin = p.cu_seqlens[n];
     const int64_t seq_len = p.cu_seqlens[n + 1] - seq_begin;
     const int64_t unit = (int64_t)n * H + h;
@@ -1121,8 +1127,21 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
                               const void* k, const void* v, const void* g, const void* beta,
                               const float* init_state, const int32_t* cu_seqlens, void* out,
                               float* final_state, const SegWorkspace& ws, int* status,
-                              cudaStream_t stream, uint64_t* launches) {
+                              cudaStream_t stream, uint64_t* launches,
+                              const int32_t* host_seqlens) {
     if (num_seqs <= 0 || heads <= 0) return cudaSuccess;
+    const int64_t units = (int64_t)num_seqs * heads;
+    if (units > INT32_MAX) return cudaErrorInvalidValue;
+    SeqOrder order;
+    order.count = 0;
+    if (host_seqlens && num_seqs <= kMaxOrdered) {
+        std::vector<int> idx(num_seqs);
+        std::iota(idx.begin(), idx.end(), 0);
+        auto nc = [&](int i) { return ((int64_t)host_seqlens[i] + kChunk - 1) / kChunk; };
+        std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return nc(a) > nc(b); });
+        for (int r = 0; r < num_seqs; ++r) order.seq[r] = (uint16_t)idx[r];
+        order.count = num_seqs;
+    }
     CUtensorMap mq, mk, mv, mg;
     const int64_t T = total_tokens > 0 ? total_tokens : 1;
     if (!make_map(&mq, q, T, heads) || !make_map(&mk, k, T, heads) ||
@@ -1145,8 +1164,8 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
     if (e != cudaSuccess) return e;
     const int zsplit = ws.max_segments > 1 ? 2 * (ws.max_segments - 1) : 1;
     // pass 0: whole sequences, and pass A (segment states and transitions) of split ones
-    kda_prefill_tc_kernel<<<dim3(num_seqs, heads, zsplit), kThreadsTC, SMEM_ALLOC, stream>>>(
-        mq, mk, mv, mg, prm);
+    kda_prefill_tc_kernel<<<dim3((unsigned)units, 1, zsplit), kThreadsTC, SMEM_ALLOC, stream>>>(
+        mq, mk, mv, mg, prm, order);
     if (launches) ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess || ws.max_segments <= 1) return e;
     // compose the incoming state of every segment
@@ -1160,8 +1179,8 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // pass B: every segment of the split sequences from its composed incoming state
     prm.pass = 1;
-    kda_prefill_tc_kernel<<<dim3(num_seqs, heads, ws.max_segments), kThreadsTC, SMEM_ALLOC,
-                            stream>>>(mq, mk, mv, mg, prm);
+    kda_prefill_tc_kernel<<<dim3((unsigned)units, 1, ws.max_segments), kThreadsTC, SMEM_ALLOC,
+                            stream>>>(mq, mk, mv, mg, prm, order);
     if (launches) ++*launches;
     return cudaGetLastError();
 }

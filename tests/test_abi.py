@@ -62,16 +62,16 @@ def test_plan_counts_chunks_per_sequence(lib):
 def test_plan_splits_long_sequences_by_length_only(lib):
     from kimi_delta_attention_03_gb300 import binding
     H = 3
-    lens = [16384, 16385, 262144, 5]  # 256 chunks (whole), 257 (3 segments), 4096 (32), 1
+    lens = [65536, 65537, 262144, 5]  # 1024 chunks (whole), 1025 (9 segments), 4096 (32), 1
     info = binding.fwd_plan(lens, H)
     assert info["segment_chunks"] == 128
     assert info["split_sequences"] == 2
-    assert info["work_items"] == 1 + 3 + 32 + 1
-    slots = 3 + 32
+    assert info["work_items"] == 1 + 9 + 32 + 1
+    slots = 9 + 32
     assert info["workspace_bytes"] == 3 * slots * H * 128 * 128 * 4
     assert binding.fwd_workspace_bytes(lens, H) == info["workspace_bytes"]
     # the plan of a sequence does not depend on its neighbours
-    assert binding.fwd_plan([16385], H)["work_items"] == 3
+    assert binding.fwd_plan([65537], H)["work_items"] == 9
     assert binding.fwd_plan([100, 200], H)["workspace_bytes"] == 0
 
 

@@ -250,12 +250,12 @@ def test_varlen_64_full_size():
 
 # ------------------------------ segment parallelism ------------------------------------
 def test_segmented_sequences_match_oracle():
-    """Sequences above 256 chunks run as segments (transition + state-from-zero per segment,
+    """Sequences above 1024 chunks run as segments (transition + state-from-zero per segment,
     composed, then rerun); the result equals the token loop."""
-    lens = [20000, 100, 17000, 16384]  # 313, 2, 266, 256 chunks: split, whole, split, whole
+    lens = [70000, 100, 66000, 65536]  # 1094, 2, 1032, 1024 chunks: split, whole, split, whole
     x = synth.make_inputs(lens, 2, torch.bfloat16, seed=31, device=DEV)
     info = kda().binding.fwd_plan(lens, 2)
-    assert info["split_sequences"] == 2 and info["work_items"] == 3 + 1 + 3 + 1
+    assert info["split_sequences"] == 2 and info["work_items"] == 9 + 1 + 9 + 1
     out, fin = run_gpu(x)
     o_ref, s_ref = run_oracle(x)
     assert_close("out", out.float().cpu().numpy(), o_ref)
@@ -263,7 +263,7 @@ def test_segmented_sequences_match_oracle():
 
 
 def test_segmented_packing_is_bit_exact_and_aliasing_safe():
-    lens = [70, 20000, 0, 33]
+    lens = [70, 70000, 0, 33]
     x = synth.make_inputs(lens, 2, torch.bfloat16, seed=32, device=DEV)
     out, fin = run_gpu(x)
     cu = x["cu_seqlens"].cpu().tolist()
