@@ -719,7 +719,6 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     if (q4 == colhalf) {
                         __syncwarp();
                         const int b = 2 * q4 + (lane >> 4), col = lane & 15;
-                        unsigned char* tb = sm + (s ? OFF_TB1 : OFF_TB0);
                         const float* Ab = Am + (16 * b) * LDA_T + 16 * b;
                         float x[16];
 #pragma unroll
@@ -738,14 +737,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         }
                         __syncwarp();
                         float* Tb = Am + (16 * b) * LDA_T + 16 * b;
-                        const float bc = beta_ring(c)[16 * b + col];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            Tb[i * LDA_T + col] = x[i];
-                            *reinterpret_cast<bf16*>(
-                                tb + sw128_offset(16 * b + i, 16 * b + col, 64)) =
-                                __float2bfloat16_rn(x[i] * bc);
-                        }
+                        for (int i = 0; i < 16; ++i) Tb[i * LDA_T + col] = x[i];
                     }
                 } else if (has_out) {  // P only shapes outputs
                     const int t = row_abs - kChunk;
@@ -820,6 +813,21 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 block_product(acc, Am + (16 * I) * LDA_T + 16 * J, LDA_T, -1.f, n2, n3,
                               Am + (16 * J) * LDA_T + 16 * J, LDA_T, lane);
                 store_block_tb(tb, I, J, acc, beta_ring(c), lane);
+            } else {  // the diagonal blocks T_II, two per warp, into the bf16 operand tile
+                const int g = lane >> 2, tq = lane & 3;
+#pragma unroll 1
+                for (int I = 2 * (wp - 6); I < 2 * (wp - 6) + 2; ++I) {
+                    const float* Tb = Am + 16 * I * (LDA_T + 1);
+                    float acc[2][4];
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const float2 u = *reinterpret_cast<const float2*>(Tb + g * LDA_T + 8 * nt + 2 * tq);
+                        const float2 w =
+                            *reinterpret_cast<const float2*>(Tb + (g + 8) * LDA_T + 8 * nt + 2 * tq);
+                        acc[nt][0] = u.x; acc[nt][1] = u.y; acc[nt][2] = w.x; acc[nt][3] = w.y;
+                    }
+                    store_block_tb(tb, I, I, acc, beta_ring(c), lane);
+                }
             }
             fence_async_shared();
             named_bar(kBarPrep, kPrepThreads);
