@@ -60,9 +60,11 @@ constexpr float kMaxExponentTC = 80.f;
 constexpr int LDA_T = 68;       // fp32 row stride of the 64 x 64 A / T matrix
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
-// Slot tile [K_p ; Q_r ; g -> -W]: 192 rows x 128 cols, two column regions of 24 KB.  Rows
-// 0-127 are the A operand of the intra-chunk product, rows 64-191 the B operand of the
-// state product, rows 128-191 first hold g (as loaded) and then -W.
+// Slot tile [k -> K_p -> -W ; q -> Q_r ; g]: 192 rows x 128 cols, two column regions of 24 KB.
+// Rows 0-127 are the A operand of the intra-chunk product ([K_p ; Q_r]) and later the B operand
+// of the state product ([-W ; Q_r], -W written over K_p once M2 has read it).  Rows 128-191
+// hold g, which is only read by the decay scan and the factor pass, so g of chunk c + 2 is
+// loaded as soon as those are done with chunk c, while k and q wait for M4 of chunk c.
 constexpr int KQW_ROWS = 192;
 constexpr uint32_t KQW_REGION = KQW_ROWS * 128;   // 24576
 constexpr uint32_t OFF_KQW0 = 0;         // slot 0 (48 KB)
@@ -75,15 +77,13 @@ constexpr uint32_t OFF_P1 = 163840;      // slot 1
 constexpr uint32_t OFF_TB0 = 180224;     // T diag(beta): 64 x 64 (8 KB), slot 0
 constexpr uint32_t OFF_TB1 = 188416;     // slot 1
 constexpr uint32_t OFF_KML = 196608;     // A / T fp32 [64][68] of the 64 x 64 inverse
-constexpr uint32_t OFF_PART = OFF_KML + 17408;      // 16 x 128 fp32 token-group sums / prefixes
-constexpr uint32_t OFF_Y = OFF_PART;                // 4 x 16 x 16 fp32 blocks (N^2, N^3); the
-                                                    // factor pass and the inverse never overlap
+constexpr uint32_t OFF_PART = OFF_KML + 17408;      // 16 x 128 fp32 token-group prefixes
 constexpr uint32_t OFF_GC = OFF_PART + 8192;        // 128 fp32: chunk log-decay G_C
 constexpr uint32_t OFF_BETA = OFF_GC + 512;         // 2 x 64 fp32 ring
 constexpr uint32_t OFF_ER = OFF_BETA + 512;         // 4 x 128 fp32: e^{r} ring
 constexpr uint32_t OFF_SC = OFF_ER + 2048;          // 4 x 128 fp32: e^{r_{c-1} + r_c} ring
 constexpr uint32_t OFF_BAR = OFF_SC + 2048;         // mbarriers
-constexpr int NBAR = 28;
+constexpr int NBAR = 32;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag, copies issued
 constexpr uint32_t SMEM_USED = OFF_MISC + 48;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
@@ -94,13 +94,13 @@ enum {
     B_FULL0 = 0, B_FULL1, B_VFREE0, B_VFREE1, B_VFULL, B_SPARE,
     B_FACT0, B_FACT1, B_AP0, B_AP1, B_TB0, B_TB1, B_WDONE0, B_WDONE1, B_WN0, B_WN1,
     B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_UFREE0, B_UFREE1, B_KMFREE0, B_KMFREE1,
-    B_SDONE, B_PFREE0, B_PFREE1, B_COUNT
+    B_SDONE, B_PFREE0, B_PFREE1, B_SCAN0, B_SCAN1, B_GFULL0, B_GFULL1, B_COUNT
 };
 static_assert(B_COUNT <= NBAR, "barrier slots");
 
 // TMEM columns (512 allocated)
 constexpr uint32_t T_S = 0;      // X: fp32 state, lanes = value channel, cols = key channel
-constexpr uint32_t T_X0 = 128;   // even chunks: [O^T (64) | U^T (64)]; U^T becomes bf16 hi|lo;
+constexpr uint32_t T_X0 = 128;   // even chunks: [U^T (64) | O^T (64)]; U^T becomes bf16 hi|lo;
                                  // the O^T columns first hold W^T of the chunk
 constexpr uint32_t T_P = 256;    // [A ; P] raw tiles (64 cols)
 constexpr uint32_t T_SA = 320;   // bf16 copy of X (A operand, 64 cols)
@@ -156,7 +156,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// acc += (xs * X + n2 - n3) Yb for 16 x 16 blocks; n2 / n3 (leading dim 16) may be null.
+// acc += (xs * X + n2 - n3) Yb for 16 x 16 blocks; n2 / n3 (leading dim LDA_T) may be null.
 // Four 8 x 4 fp32 tiles (as 8 x 8 b16 matrices) in one instruction: lane l gives the address
 // of row l & 7 of tile l >> 3, and register i of lane l receives tile i's element
 // (l / 4, l % 4).  Rows must start on 16-byte boundaries.
@@ -166,7 +166,7 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const float* row) {
                  : "r"(saddr(row))
                  : "memory");
 }
-// acc += (xs X + n2 - n3) Yb for 16 x 16 blocks (n2, n3 optional, stride 16).  The A fragments
+// acc += (xs X + n2 - n3) Yb for 16 x 16 blocks (n2, n3 optional, stride LDA_T).  The A fragments
 // (rows g, g + 8; columns k0 + t, k0 + t + 4) come from ldmatrix: tiles (rows 0-7 | 8-15) x
 // (columns k0..k0+3 | k0+4..k0+7).
 __device__ __forceinline__ void block_mma(float (&acc)[2][4], const float* X, int ldx, float xs,
@@ -180,8 +180,8 @@ __device__ __forceinline__ void block_mma(float (&acc)[2][4], const float* X, in
         uint32_t a[4];
         ldsm_x4(a, X + mrow * ldx + k0 + mcol);
         uint32_t a2[4] = {0u, 0u, 0u, 0u}, a3[4] = {0u, 0u, 0u, 0u};
-        if (n2) ldsm_x4(a2, n2 + mrow * 16 + k0 + mcol);
-        if (n3) ldsm_x4(a3, n3 + mrow * 16 + k0 + mcol);
+        if (n2) ldsm_x4(a2, n2 + mrow * LDA_T + k0 + mcol);
+        if (n3) ldsm_x4(a3, n3 + mrow * LDA_T + k0 + mcol);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             float x = xs * __uint_as_float(a[i]);
@@ -273,6 +273,60 @@ __device__ __noinline__ bool spin_bar_poll(uint64_t* bar, uint32_t parity,
 __device__ __forceinline__ bool spin_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                          int* status) {
     return mbar_test(bar, parity) || spin_bar_poll(bar, parity, abort_flag, status);
+}
+
+// Cumulative decay of chunk cs for the epilogue warp group, thread te = key channel: exclusive
+// prefixes of g at the 16 four-token groups (into the prefix array), G_C, e^{r} with
+// r = G_C / 2, and the state scale e^{r_{cs-1} + r_cs}.  Group sums first, then the prefix over
+// the groups.  One call site, out of line: inlined, it raises the epilogue loop's spills.
+__device__ __noinline__ bool decay_scan(unsigned char* sm, int cs, int L, int te,
+                                        volatile int* abort_flag, int* status) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    float* part = reinterpret_cast<float*>(sm + OFF_PART);
+    float* gc_s = reinterpret_cast<float*>(sm + OFF_GC);
+    float* er = reinterpret_cast<float*>(sm + OFF_ER);
+    float* sc = reinterpret_cast<float*>(sm + OFF_SC);
+    const int s2 = cs & 1;
+    if (!wait_bar(&bars[B_GFULL0 + s2], (cs >> 1) & 1, abort_flag, status)) return false;
+    const int valid = min(kChunk, L - kChunk * cs);
+    // g is row 128 + t of the slot tile; (128 + t) & 7 == t & 7
+    const unsigned char* gcol =
+        sm + (s2 ? OFF_KQW1 : OFF_KQW0) + (te >> 6) * KQW_REGION + 128 * 128 + ((te & 7) << 1);
+    const int chunk16 = (te & 63) >> 3;
+    float run = 0.f, gmax = 0.f;
+#pragma unroll 1
+    for (int t16 = 0; t16 < kChunk; t16 += 16) {
+        // sixteen tokens' loads in flight at once; rows past the sequence end hold other
+        // tokens (or zeros) and are masked after the load
+        float gv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            gv[i] = __bfloat162float(*reinterpret_cast<const bf16*>(
+                gcol + (t16 + i) * 128 + ((chunk16 ^ (i & 7)) << 4)));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float gs = 0.f;
+#pragma unroll
+            for (int i = 4 * q; i < 4 * q + 4; ++i) {
+                const float x = t16 + i < valid ? gv[i] : 0.f;  // g is zero past the end
+                gs += x;
+                gmax = fmaxf(gmax, x);
+            }
+            part[((t16 >> 2) + q) * kDim + te] = run;
+            run += gs;
+        }
+    }
+    // With every g <= 0 the cumulative decay G is monotone, so |G - r| <= |G_C| / 2 and one
+    // check per channel bounds every factor.
+    if (gmax > 0.f) report_status(status, kStatusDecayRange);
+    gc_s[te] = run;
+    if (fabsf(0.5f * run) > kMaxExponentTC) report_status(status, kStatusDecayRange);
+    const float e = ex2_approx((0.5f * kLog2eTC) * run);
+    er[(cs & 3) * kDim + te] = e;
+    sc[(cs & 3) * kDim + te] = cs > 0 ? er[((cs + 3) & 3) * kDim + te] * e : e;
+    named_bar(kBarEpi, kEpiThreads);
+    if (te == 0) mbar_arrive(&bars[B_SCAN0 + s2]);
+    return true;
 }
 
 __global__ void __launch_bounds__(kThreadsTC, 1)
@@ -387,21 +441,30 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     auto a_kmh = [&](int s) { return a_base + (s ? OFF_KMH1 : OFF_KMH0); };
     auto a_p = [&](int s) { return a_base + (s ? OFF_P1 : OFF_P0); };
     auto a_tb = [&](int s) { return a_base + (s ? OFF_TB1 : OFF_TB0); };
-    // TMA issue helpers (q, k, g of chunk c into slot c & 1; v of chunk c)
-    auto issue_kqg = [&](int c) {
+    // TMA issue helpers: k, q of chunk c into slot c & 1 (once M4 two chunks back has read the
+    // slot), g of chunk c (once the factor pass two chunks back has read it), v of chunk c
+    auto issue_kq = [&](int c) {
         const int s = c & 1;
         unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
         uint64_t* full = &bars[B_FULL0 + s];
         const int t0 = (int)(seq0 + (int64_t)kChunk * c);
-        mbar_arrive_expect_tx(full, has_out ? 49152 : 32768);
+        mbar_arrive_expect_tx(full, has_out ? 32768 : 16384);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             tma_load_3d(kq + r * KQW_REGION, &tm_k, full, 64 * r, h, t0);
             if (has_out)  // q only shapes outputs
                 tma_load_3d(kq + r * KQW_REGION + 8192, &tm_q, full, 64 * r, h, t0);
-            tma_load_3d(kq + r * KQW_REGION + 16384, &tm_g, full, 64 * r, h, t0);
         }
         *kqg_issued = c + 1;
+    };
+    auto issue_g = [&](int c) {
+        const int s = c & 1;
+        unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
+        uint64_t* full = &bars[B_GFULL0 + s];
+        const int t0 = (int)(seq0 + (int64_t)kChunk * c);
+        mbar_arrive_expect_tx(full, 16384);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) tma_load_3d(kq + r * KQW_REGION + 16384, &tm_g, full, 64 * r, h, t0);
     };
     auto issue_v = [&](int c) {
         if (zero_v) {
@@ -421,9 +484,14 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_g);
-            issue_kqg(0);
+            issue_g(0);
+            issue_kq(0);
             issue_v(0);
-            if (nchunks > 1) issue_kqg(1);
+            if (nchunks > 1) {
+                issue_g(1);
+                issue_kq(1);
+            }
+            int g_issued = min(nchunks, 2);
             const uint32_t rP = tmem + T_P;
             const uint32_t a_v = saddr(sm + OFF_V);
             const uint32_t id_kk64 = idesc_bf16(128, 64, false, false);
@@ -433,6 +501,11 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             auto issue_m1 = [&](const int c) -> bool {
                 const int s = c & 1;
                 if (!spin_bar(&bars[B_FACT0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
+                // the factor pass and the scan have read g of chunk c: load g of chunk c + 2
+                if (c + 2 < nchunks) {
+                    issue_g(c + 2);
+                    g_issued = c + 3;
+                }
                 tc_fence_after();
                 const uint64_t dq = smem_desc(a_kq(s), 16, 1024);
                 const uint64_t dh = smem_desc(a_kmh(s), 16, 1024);
@@ -460,7 +533,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const uint64_t db = smem_desc(a_tb(s), 16, 1024);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            mma_ss(rX, da + 128 * j, db + 2 * j, id_mk64, j > 0);
+                            mma_ss(rX + 64, da + 128 * j, db + 2 * j, id_mk64, j > 0);
                     }
                     mma_commit(&bars[B_WDONE0 + s]);
                     // M3: U_bar^T = V^T (T diag(beta))^T into the U^T columns, once v has landed
@@ -471,7 +544,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const uint64_t db = smem_desc(a_tb(s), 16, 1024);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            mma_ss(rX + 64, da + 128 * j, db + 2 * j, id_mk64, j > 0);
+                            mma_ss(rX, da + 128 * j, db + 2 * j, id_mk64, j > 0);
                     }
                     mma_commit(&bars[B_VFREE0 + s]);
                     // the v buffer is free once M3 has read it: load the next chunk's v
@@ -492,6 +565,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const int nk = *kqg_issued;
                 for (int c = nk - 2; c < nk; ++c)
                     if (c >= 0) mbar_wait(&bars[B_FULL0 + (c & 1)], (c >> 1) & 1, kWaitLimit);
+                for (int c = g_issued - 2; c < g_issued; ++c)
+                    if (c >= 0) mbar_wait(&bars[B_GFULL0 + (c & 1)], (c >> 1) & 1, kWaitLimit);
             }
         }
     } else if (warp == kWarpMma) {
@@ -503,14 +578,14 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const uint32_t id_km128 = idesc_bf16(128, 128, false, true);
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c & 1;
-                const uint32_t rX = tmem + (s ? T_X1 : T_X0);  // [O^T | U^T]
-                // M4: [O^T | U^T] += X [Q_r ; -W]^T  (O^T starts at zero, U^T at U_bar^T)
+                const uint32_t rX = tmem + (s ? T_X1 : T_X0);  // [U^T | O^T]
+                // M4: [U^T | O^T] += X [-W ; Q_r]^T  (U^T starts at U_bar^T, O^T at zero)
                 if (!spin_bar(&bars[B_WN0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
                 if (!spin_bar(&bars[B_SREADY], c & 1, abort_flag, p.status)) break;
                 if (!spin_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
                 tc_fence_after();
                 {
-                    const uint64_t db = smem_desc(a_kq(s) + 8192, 16, 1024);
+                    const uint64_t db = smem_desc(a_kq(s), 16, 1024);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         mma_ts(rX, rSA + 8 * j, db + (j >> 2) * (KQW_REGION >> 4) + (j & 3) * 2,
@@ -518,7 +593,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
                 mma_commit(&bars[B_XDONE]);
                 // M6 + M5: X += U^T K_m (2 split terms), O^T += U^T P^T (3 split terms);
-                // U^T hi / lo sit in place of U^T (cols 64-95 / 96-127 of this chunk's block)
+                // U^T hi / lo sit in place of U^T (cols 0-31 / 32-63 of this chunk's block)
                 if (!spin_bar(&bars[B_UREADY], c & 1, abort_flag, p.status)) break;
                 // keep these off the tensor pipe while chunk c+1's inverse uses mma.sync
                 if (c + 1 < nchunks &&
@@ -526,7 +601,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     break;
                 tc_fence_after();
                 {
-                    const uint32_t rUH = rX + 64, rUL = rX + 96;
+                    const uint32_t rUH = rX, rUL = rX + 32, rO = rX + 64;
                     const uint64_t dph = smem_desc(a_p(s), 16, 1024);
                     const uint64_t dpl = smem_desc(a_p(s) + 8192, 16, 1024);
                     const uint64_t dk = smem_desc(a_kmh(s), 8192, 1024);
@@ -539,11 +614,11 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     mma_commit(&bars[B_SDONE]);
                     if (has_out) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) mma_ts(rX, rUH + 8 * j, dph + 2 * j, id_kk64, 1);
+                        for (int j = 0; j < 4; ++j) mma_ts(rO, rUH + 8 * j, dph + 2 * j, id_kk64, 1);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) mma_ts(rX, rUL + 8 * j, dph + 2 * j, id_kk64, 1);
+                        for (int j = 0; j < 4; ++j) mma_ts(rO, rUL + 8 * j, dph + 2 * j, id_kk64, 1);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) mma_ts(rX, rUH + 8 * j, dpl + 2 * j, id_kk64, 1);
+                        for (int j = 0; j < 4; ++j) mma_ts(rO, rUH + 8 * j, dpl + 2 * j, id_kk64, 1);
                     }
                 }
                 mma_commit(&bars[B_PFREE0 + s]);  // P of this slot has been read
@@ -566,7 +641,9 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         float* Am = reinterpret_cast<float*>(sm + OFF_KML);
         float beta_next = (tp < min(kChunk, L)) ? bf2f(p.beta[seq0 * H + (int64_t)tp * H + h]) : 0.f;
-        float* Y = reinterpret_cast<float*>(sm + OFF_Y);
+        // scratch of the inverse: the four blocks of the upper quadrant of A / T (rows 0-31,
+        // columns 32-63), which no step stores or reads otherwise
+        auto Yb = [&](int k) { return Am + (k >> 1) * 16 * LDA_T + 32 + (k & 1) * 16; };
         // beta of chunk c (two chunks are live: the next chunk's factors are made before this
         // chunk's W epilogue)
         auto beta_ring = [&](int c) { return beta_s + (c & 1) * kChunk; };
@@ -579,57 +656,18 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             unsigned char* kmh = sm + (s ? OFF_KMH1 : OFF_KMH0);
             if (!wait_bar(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
 
-            // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7 ----
-            {
-                float gs[8];
-                float gmax = 0.f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) gs[j] = 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int t = 4 * tg + i;
-                    uint4 gr = make_uint4(0u, 0u, 0u, 0u);  // g is zero past the sequence end
-                    if (t < valid)
-                        gr = *reinterpret_cast<const uint4*>(kq + sw128_offset(128 + t, c8, KQW_ROWS));
-                    float gv[8];
-                    unpack8(gr, gv);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        gs[j] += gv[j];
-                        gmax = fmaxf(gmax, gv[j]);
-                    }
-                }
-                // With every g <= 0 the cumulative decay G is monotone, so |G - r| <= |G_C| / 2
-                // and one check per channel (in the scan below) bounds every factor.
-                if (gmax > 0.f) report_status(p.status, kStatusDecayRange);
-                *reinterpret_cast<float4*>(part + tg * kDim + c8) = make_float4(gs[0], gs[1], gs[2], gs[3]);
-                *reinterpret_cast<float4*>(part + tg * kDim + c8 + 4) = make_float4(gs[4], gs[5], gs[6], gs[7]);
-                if (tp < kChunk) {
-                    beta_ring(c)[tp] = beta_next;
-                    // fetch the next chunk's beta now; it is needed one chunk later
-                    const int vn = min(kChunk, L - kChunk * (c + 1));
-                    beta_next = tp < vn ? bf2f(p.beta[(tok0 + kChunk + tp) * H + h]) : 0.f;
-                }
+            // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7.
+            // The token-group prefixes of g, G_C and e^{r} come from the epilogue warps' scan.
+            if (tp < kChunk) {
+                beta_ring(c)[tp] = beta_next;
+                // fetch the next chunk's beta now; it is needed one chunk later
+                const int vn = min(kChunk, L - kChunk * (c + 1));
+                beta_next = tp < vn ? bf2f(p.beta[(tok0 + kChunk + tp) * H + h]) : 0.f;
             }
-            named_bar(kBarPrep, kPrepThreads);
-            if (tp < kDim) {  // exclusive prefix over the 16 token groups, and the chunk total
-                float v[16];
-#pragma unroll
-                for (int g16 = 0; g16 < 16; ++g16) v[g16] = part[g16 * kDim + tp];
-                float run = 0.f;
-#pragma unroll
-                for (int g16 = 0; g16 < 16; ++g16) {
-                    part[g16 * kDim + tp] = run;
-                    run += v[g16];
-                }
-                gc_s[tp] = run;
-                if (fabsf(0.5f * run) > kMaxExponentTC) report_status(p.status, kStatusDecayRange);
-                // e^{r} of this chunk and the state scale e^{r_{c-1} + r_c}
-                const float e = ex2_approx((0.5f * kLog2eTC) * run);
-                er[(c & 3) * kDim + tp] = e;
-                sc[(c & 3) * kDim + tp] = c > 0 ? er[((c + 3) & 3) * kDim + tp] * e : e;
-            }
-            named_bar(kBarPrep, kPrepThreads);
+            // g has landed (the scan waited for it too) and its prefixes are in place
+            if (!wait_bar(&bars[B_GFULL0 + s], (c >> 1) & 1, abort_flag, p.status) ||
+                !wait_bar(&bars[B_SCAN0 + s], (c >> 1) & 1, abort_flag, p.status))
+                return false;
             {
                 float G[8], r[8];
                 {
@@ -701,16 +739,19 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 if (row_abs < kChunk) {
                     const int t = row_abs;
                     const float bt = beta_ring(c)[t];
-                    // only the strictly lower triangle is ever read, so it is stored unmasked
+                    // only the strictly lower triangle is ever read, so it is stored unmasked;
+                    // the upper quadrant (rows 0-31, columns 32-63) is the inverse's scratch
+                    if (colhalf <= q4) {
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        float4 o;
-                        const int col = 32 * colhalf + 4 * j4;
-                        o.x = bt * __uint_as_float(v[4 * j4 + 0]);
-                        o.y = bt * __uint_as_float(v[4 * j4 + 1]);
-                        o.z = bt * __uint_as_float(v[4 * j4 + 2]);
-                        o.w = bt * __uint_as_float(v[4 * j4 + 3]);
-                        *reinterpret_cast<float4*>(Am + t * LDA_T + col) = o;
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            float4 o;
+                            const int col = 32 * colhalf + 4 * j4;
+                            o.x = bt * __uint_as_float(v[4 * j4 + 0]);
+                            o.y = bt * __uint_as_float(v[4 * j4 + 1]);
+                            o.z = bt * __uint_as_float(v[4 * j4 + 2]);
+                            o.w = bt * __uint_as_float(v[4 * j4 + 3]);
+                            *reinterpret_cast<float4*>(Am + t * LDA_T + col) = o;
+                        }
                     }
                     // ---- T = (I + A)^{-1}, diagonal 16 x 16 blocks by forward substitution.
                     // The warp that stored a diagonal 32 x 32 quadrant of A inverts its two
@@ -791,24 +832,24 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                               Am + (wp == 1 ? 32 * LDA_T + 16 : 16 * LDA_T), LDA_T, lane);
                 if (wp != 0) {
                     if (wp == 1) {
-                        store_block(Y + 256, 16, acc, lane);
+                        store_block(Yb(1), LDA_T, acc, lane);
                         __syncwarp();
 #pragma unroll
                         for (int nt = 0; nt < 2; ++nt)
                             acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
                     }
-                    block_mma(acc, wp == 1 ? Y + 256 : Am + 48 * LDA_T + 32, wp == 1 ? 16 : LDA_T,
+                    block_mma(acc, wp == 1 ? Yb(1) : Am + 48 * LDA_T + 32, LDA_T,
                               1.f, nullptr, nullptr, Am + (wp == 1 ? 16 * LDA_T : 32 * LDA_T), LDA_T,
                               lane);
                 }
-                store_block(Y + 256 * (wp == 0 ? 0 : wp == 1 ? 3 : 2), 16, acc, lane);
+                store_block(Yb(wp == 0 ? 0 : wp == 1 ? 3 : 2), LDA_T, acc, lane);
             }
             named_bar(kBarPrep, kPrepThreads);
             if (wp < 6) {  // T_IJ = C_IJ T_JJ with C = -N + N^2 - N^3 (block by block)
                 const int I = pair_i(wp), J = pair_j(wp);
-                const float* n2 = (I == 2 && J == 0) ? Y : (I == 3 && J == 1) ? Y + 256
-                                : (I == 3 && J == 0) ? Y + 512 : nullptr;
-                const float* n3 = (I == 3 && J == 0) ? Y + 768 : nullptr;
+                const float* n2 = (I == 2 && J == 0) ? Yb(0) : (I == 3 && J == 1) ? Yb(1)
+                                : (I == 3 && J == 0) ? Yb(2) : nullptr;
+                const float* n3 = (I == 3 && J == 0) ? Yb(3) : nullptr;
                 float acc[2][4];
                 block_product(acc, Am + (16 * I) * LDA_T + 16 * J, LDA_T, -1.f, n2, n3,
                               Am + (16 * J) * LDA_T + 16 * J, LDA_T, lane);
@@ -837,12 +878,12 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         auto w_epilogue = [&](const int c) -> bool {
             const int s = c & 1;
             unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
-            // ---- -W into rows 128-191 of the slot tile (K-major [t][c]) ----
+            // ---- -W into rows 0-63 of the slot tile (K-major [t][c]), over K_p ----
             if (!wait_bar(&bars[B_WDONE0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
             tc_fence_after();
             {
                 uint32_t v[32];
-                const uint32_t rW = tmem + (s ? T_X1 : T_X0) + 32 * colhalf + lane_off;
+                const uint32_t rW = tmem + (s ? T_X1 : T_X0) + 64 + 32 * colhalf + lane_off;
                 tmem_ld32(rW, v);  // W^T[c = row_abs][t]
                 // Lanes 2i and 2i+1 hold channels ch0 and ch0+1.  Each packs its own tokens
                 // (j, j+4) and the two swap words: the even lane stores the low halves (token j),
@@ -852,7 +893,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const uint32_t sel = odd ? 0x3276u : 0x5410u;
                 // Rows t0 + j with j & 7 in 0..3 have swizzle phase (t0 + (j & 3)) & 7, so four
                 // row bases per thread serve every store, plus a compile-time row offset.
-                const int t0 = 128 + 32 * colhalf + (odd ? 4 : 0);
+                const int t0 = 32 * colhalf + (odd ? 4 : 0);
                 unsigned char* wb[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
@@ -891,70 +932,80 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int q4 = warp & 3;
         const int vch = 32 * q4 + lane;  // value channel = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-        bool ok = wait_bar(&bars[B_FACT0], 0, abort_flag, p.status);
-        if (ok) {  // X_0 = S0^T diag(e^{r_0}); S0 = 0, I (transition items) or the given state
-            const float* e0 = er;
-            const float* s0 = init_src;
-            for (int cc = 0; cc < kDim; cc += 32) {
-                uint32_t x[32], xb[16];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float sv = s0 ? s0[(cc + j) * kDim + vch]
-                                        : (item == ITEM_TRANS && cc + j == vch ? 1.f : 0.f);
-                    x[j] = __float_as_uint(sv * e0[cc + j]);
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    xb[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
-                tmem_st32(tmem + T_S + cc + lane_off, x);
-                tmem_st16(tmem + T_SA + cc / 2 + lane_off, xb);
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            named_bar(kBarEpi, kEpiThreads);
-            if (te == 0) mbar_arrive(&bars[B_SREADY]);
-        }
-        for (int c = 0; ok && c < nchunks; ++c) {
+        auto scan = [&](const int cs) -> bool {
+            return decay_scan(sm, cs, L, te, abort_flag, p.status);
+        };
+        bool ok = true;
+        // c = -2 and -1 only scan chunks 0 and 1 (and set up X_0): one code path for the scan
+        for (int c = -2; ok && c < nchunks; ++c) {
             const uint32_t rX = tmem + ((c & 1) ? T_X1 : T_X0) + lane_off;
             const int valid = min(kChunk, L - kChunk * c);
             const int64_t tok0 = seq0 + (int64_t)kChunk * c;
-            // ---- E1: U^T -> bf16 hi/lo A operands ----
-            if (!(ok = wait_bar(&bars[B_XDONE], c & 1, abort_flag, p.status))) break;
-            tc_fence_after();
-            // M1 and M2 (before W was written) and now M4 have read this slot's K_p / Q_r / -W
-            // tile: refill it with chunk c + 2 (K_m of the slot is guarded by B_KMFREE)
-            if (te == 0 && c + 2 < nchunks) issue_kqg(c + 2);
-            {
-                // read all 64 columns of U^T before writing hi / lo over them
-                uint32_t u[64], lo[32];
-                tmem_ld64(rX + 64, u);
+            if (c == -1) {  // X_0 = S0^T diag(e^{r_0}); S0 = 0, I (transition items) or given
+                const float* e0 = er;
+                const float* s0 = init_src;
+                for (int cc = 0; cc < kDim; cc += 32) {
+                    uint32_t x[32], xb[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float x0 = __uint_as_float(u[2 * j]), x1 = __uint_as_float(u[2 * j + 1]);
-                    const uint32_t hi = pack_bf16(x0, x1);
-                    lo[j] = pack_bf16(x0 - __uint_as_float(hi << 16),
-                                      x1 - __uint_as_float(hi & 0xffff0000u));
-                    u[j] = hi;  // u[2j], u[2j+1] are consumed; slot j <= 2j is free
+                    for (int j = 0; j < 32; ++j) {
+                        const float sv = s0 ? s0[(cc + j) * kDim + vch]
+                                            : (item == ITEM_TRANS && cc + j == vch ? 1.f : 0.f);
+                        x[j] = __float_as_uint(sv * e0[cc + j]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        xb[j] = pack_bf16(__uint_as_float(x[2 * j]), __uint_as_float(x[2 * j + 1]));
+                    tmem_st32(tmem + T_S + cc + lane_off, x);
+                    tmem_st16(tmem + T_SA + cc / 2 + lane_off, xb);
                 }
-                uint32_t hi32[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) hi32[j] = u[j];
-                tmem_st32(rX + 64, hi32);
-                tmem_st32(rX + 96, lo);
+                tmem_st_wait();
+                tc_fence_before();
+                named_bar(kBarEpi, kEpiThreads);
+                if (te == 0) mbar_arrive(&bars[B_SREADY]);
+                // chunk 1 reuses the prefix array once the prep warps have read chunk 0's
+                if (nchunks > 1 && !(ok = wait_bar(&bars[B_FACT0], 0, abort_flag, p.status))) break;
             }
-            tmem_st_wait();
-            tc_fence_before();
-            named_bar(kBarEpi, kEpiThreads);
-            if (te == 0) mbar_arrive(&bars[B_UREADY]);
+            if (c >= 0) {
+                // ---- E1: U^T -> bf16 hi/lo A operands ----
+                if (!(ok = wait_bar(&bars[B_XDONE], c & 1, abort_flag, p.status))) break;
+                tc_fence_after();
+                // M1, M2 and now M4 have read this slot's K_p / Q_r / -W rows: refill k and q with
+                // chunk c + 2 (g was refilled after the factor pass; K_m is guarded by B_KMFREE)
+                if (te == 0 && c + 2 < nchunks) issue_kq(c + 2);
+                {
+                    // read all 64 columns of U^T before writing hi / lo over them
+                    uint32_t u[64], lo[32];
+                    tmem_ld64(rX, u);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float x0 = __uint_as_float(u[2 * j]), x1 = __uint_as_float(u[2 * j + 1]);
+                        const uint32_t hi = pack_bf16(x0, x1);
+                        lo[j] = pack_bf16(x0 - __uint_as_float(hi << 16),
+                                          x1 - __uint_as_float(hi & 0xffff0000u));
+                        u[j] = hi;  // u[2j], u[2j+1] are consumed; slot j <= 2j is free
+                    }
+                    uint32_t hi32[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) hi32[j] = u[j];
+                    tmem_st32(rX, hi32);
+                    tmem_st32(rX + 32, lo);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                named_bar(kBarEpi, kEpiThreads);
+                if (te == 0) mbar_arrive(&bars[B_UREADY]);
+            }
+            // The cumulative decay of chunk c + 2 (its g landed a chunk ago).  The prep warps
+            // read chunk c + 1's prefixes before the W epilogue of chunk c, so before XDONE of
+            // chunk c.
+            if (c + 2 < nchunks && !(ok = scan(c + 2))) break;
+            if (c < 0) continue;
 
             // ---- E2: state rescale first (the next chunk's M4 waits on it), then O to HBM ----
             if (!(ok = wait_bar(&bars[B_SDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
             const bool last = (c + 1 == nchunks);
-            if (!last) {
-                if (!(ok = wait_bar(&bars[B_FACT0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, abort_flag,
-                                    p.status)))
-                    break;
+            if (!last) {  // the scale of chunk c + 1 is from this warp group's own scan
                 const float* scn = sc + ((c + 1) & 3) * kDim;
 #pragma unroll 1
                 for (int cc = 0; cc < kDim; cc += 32) {
@@ -1003,7 +1054,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll 1
                     for (int t0 = 0; t0 < 64; t0 += 16) {
                         uint32_t o[16];
-                        tmem_ld16(rX + t0, o);
+                        tmem_ld16(rX + 64 + t0, o);
 #pragma unroll
                         for (int t = 0; t < 16; t += 2) {
                             const uint32_t mine =
