@@ -83,7 +83,7 @@ constexpr uint32_t OFF_BETA = OFF_GC + 512;         // 2 x 64 fp32 ring
 constexpr uint32_t OFF_ER = OFF_BETA + 512;         // 4 x 128 fp32: e^{r} ring
 constexpr uint32_t OFF_SC = OFF_ER + 2048;          // 4 x 128 fp32: e^{r_{c-1} + r_c} ring
 constexpr uint32_t OFF_BAR = OFF_SC + 2048;         // mbarriers
-constexpr int NBAR = 32;
+constexpr int NBAR = 34;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag, copies issued
 constexpr uint32_t SMEM_USED = OFF_MISC + 48;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
@@ -94,7 +94,7 @@ enum {
     B_FULL0 = 0, B_FULL1, B_VFREE0, B_VFREE1, B_VFULL, B_SPARE,
     B_FACT0, B_FACT1, B_AP0, B_AP1, B_TB0, B_TB1, B_WDONE0, B_WDONE1, B_WN0, B_WN1,
     B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_UFREE0, B_UFREE1, B_KMFREE0, B_KMFREE1,
-    B_SDONE, B_PFREE0, B_PFREE1, B_SCAN0, B_SCAN1, B_GFULL0, B_GFULL1, B_COUNT
+    B_SDONE, B_PFREE0, B_PFREE1, B_SCAN0, B_SCAN1, B_GFULL0, B_GFULL1, B_M6ISS, B_COUNT
 };
 static_assert(B_COUNT <= NBAR, "barrier slots");
 
@@ -523,6 +523,9 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     // once the epilogue has read that block two chunks ago.  (A per-slot barrier: a
                     // single one could run two phases ahead of this wait.)
                     if (!spin_bar(&bars[B_TB0 + s], (c >> 1) & 1, abort_flag, p.status)) break;
+                    // M6 of chunk c - 1 (queued at the same moment) goes first: the factors of
+                    // chunk c + 1 wait on it to free K_m, while W of chunk c is needed later
+                    if (c >= 1 && !spin_bar(&bars[B_M6ISS], (c - 1) & 1, abort_flag, p.status)) break;
                     if (c >= 2 &&
                         !spin_bar(&bars[B_UFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
                         break;
@@ -612,6 +615,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     for (int j = 0; j < 4; ++j) mma_ts(rS, rUL + 8 * j, dk + 128 * j, id_km128, 1);
                     mma_commit(&bars[B_KMFREE0 + s]);  // K_m of this slot has been read
                     mma_commit(&bars[B_SDONE]);
+                    mbar_arrive(&bars[B_M6ISS]);  // M6 is queued: the next M2 may follow it
                     if (has_out) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) mma_ts(rO, rUH + 8 * j, dph + 2 * j, id_kk64, 1);
