@@ -644,7 +644,9 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int row_abs = 32 * q4 + lane;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         float* Am = reinterpret_cast<float*>(sm + OFF_KML);
-        float beta_next = (tp < min(kChunk, L)) ? bf2f(p.beta[seq0 * H + (int64_t)tp * H + h]) : 0.f;
+        const unsigned short* beta_u = reinterpret_cast<const unsigned short*>(p.beta) + seq0 * H + h;
+        unsigned short beta_raw = 0;  // raw bf16 bits; converted one chunk after the load
+        if (tp < min(kChunk, L)) beta_raw = beta_u[(int64_t)tp * H];
         // scratch of the inverse: the four blocks of the upper quadrant of A / T (rows 0-31,
         // columns 32-63), which no step stores or reads otherwise
         auto Yb = [&](int k) { return Am + (k >> 1) * 16 * LDA_T + 32 + (k & 1) * 16; };
@@ -663,10 +665,13 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7.
             // The token-group prefixes of g, G_C and e^{r} come from the epilogue warps' scan.
             if (tp < kChunk) {
-                beta_ring(c)[tp] = beta_next;
+                beta_ring(c)[tp] = __uint_as_float((uint32_t)beta_raw << 16);
                 // fetch the next chunk's beta now; it is needed one chunk later
                 const int vn = min(kChunk, L - kChunk * (c + 1));
-                beta_next = tp < vn ? bf2f(p.beta[(tok0 + kChunk + tp) * H + h]) : 0.f;
+                if (tp < vn)
+                    beta_raw = beta_u[((int64_t)kChunk * (c + 1) + tp) * H];
+                else
+                    beta_raw = 0;
             }
             // g has landed (the scan waited for it too) and its prefixes are in place
             if (!wait_bar(&bars[B_GFULL0 + s], (c >> 1) & 1, abort_flag, p.status) ||
