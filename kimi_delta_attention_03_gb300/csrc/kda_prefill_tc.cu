@@ -14,11 +14,12 @@
 // (the last line is diag(e^{G_C}) S + K_bar^T U with K_bar = k e^{G_C-G} = K_m diag(e^r)).
 //
 // GB300 mapping.  One CTA per (sequence, head), 14 warps:
-//   warp 0      prep MMA issuer (one thread): the chunk-local products of chunk c+1, and the
-//               TMA load of the next v chunk; it also issues the first q, k, g, v loads
+//   warp 0      prep MMA issuer (one thread): the chunk-local products of chunk c+1, the TMA
+//               loads of v and of g two chunks ahead; it also issues the first q, k, g, v loads
 //   warp 1      serial MMA issuer (one thread): the state products of chunk c
-//   warps 2-9   prep: decay factors, A/P epilogue, 64x64 inverse, W epilogue (chunk c+1)
-//   warps 10-13 serial epilogue: U^T to TMEM, O^T to HBM, state rescale (chunk c)
+//   warps 2-9   prep: exponential factors, A/P epilogue, 64x64 inverse, W epilogue (chunk c+1)
+//   warps 10-13 serial epilogue: U^T to TMEM, the cumulative decay of chunk c+2, state rescale,
+//               O^T to HBM (chunk c), and the k, q refill of chunk c+2
 // so the chunk-parallel work of chunk c+1 overlaps the serial state pass of chunk c.  The
 // state lives in TMEM (fp32, transposed so that value channels are TMEM lanes) for the whole
 // sequence; its bf16 operand copy and U^T are also kept in TMEM and fed to the tensor core as
