@@ -1091,20 +1091,25 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (warp == kWarpTma) tmem_dealloc(tmem, 512);
 }
 
-// Composition of segment effects, one CTA per split (sequence, head):
+// Composition of segment effects:
 //   S_in(0) = initial state;  S_in(s+1) = M_s S_in(s) + S~_s
 // ("k3_training_and_infra_notes", section 4.1: a segment's transition is evaluated without the
 // incoming state and composed exactly afterwards).  fp32 on the CUDA cores; every S_in(s) is
-// written to the workspace for the second pass.
+// written to the workspace for the second pass.  The value channels (columns of S) evolve
+// independently, so each split (sequence, head) runs as kCombineColBlocks CTAs, one per block of
+// 16 columns, which spreads the serial chain over many SMs.
 constexpr int kCombineThreads = 256;
+constexpr int kCombineColBlocks = 8;
+constexpr int kCombineCols = kDim / kCombineColBlocks;  // 16
+constexpr int kCombineLdM = kDim + 2;  // M is kept transposed, rows padded against bank conflicts
 __global__ void __launch_bounds__(kCombineThreads, 1)
 kda_segment_combine_kernel(const int32_t* __restrict__ cu_seqlens, const float* __restrict__ init_state,
                            const float* __restrict__ ws_tilde, const float* __restrict__ ws_trans,
                            float* __restrict__ ws_in, int H) {
     extern __shared__ __align__(16) float cs[];
-    float* S = cs;                  // [128][128]
-    float* M = cs + kDim * kDim;    // [128][128]
-    const int n = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+    float* Mt = cs;                         // [128][130]: Mt[k][row] = M[row][k]
+    float* S = cs + kDim * kCombineLdM;     // [128][16]: columns 16 cb .. 16 cb + 15 of the state
+    const int n = blockIdx.x, h = blockIdx.y, cb = blockIdx.z, tid = threadIdx.x;
     const int64_t len = (int64_t)cu_seqlens[n + 1] - cu_seqlens[n];
     const int nseg = num_segments(len);
     if (nseg <= 1) return;
@@ -1114,49 +1119,51 @@ kda_segment_combine_kernel(const int32_t* __restrict__ cu_seqlens, const float* 
         if (ns > 1) base += ns;
     }
     const int64_t unit = (int64_t)n * H + h;
+    const int c0 = kCombineCols * cb;
+    // element e of the slice (4 floats): row e >> 2, columns c0 + 4 (e & 3) ..
+    auto slice = [&](int e) { return (e >> 2) * kDim + c0 + 4 * (e & 3); };
     const float* s0 = init_state ? init_state + unit * (kDim * kDim) : nullptr;
-    for (int e = tid; e < kDim * kDim / 4; e += kCombineThreads)
+    for (int e = tid; e < kDim * kCombineCols / 4; e += kCombineThreads)
         reinterpret_cast<float4*>(S)[e] =
-            s0 ? reinterpret_cast<const float4*>(s0)[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+            s0 ? *reinterpret_cast<const float4*>(s0 + slice(e)) : make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
-    const int ti = tid >> 4, tj = tid & 15;  // 8 x 8 output tile (rows 8 ti.., cols 8 tj..)
+    const int r = 2 * (tid >> 2), cc = 4 * (tid & 3);  // rows r, r + 1; slice columns cc .. cc + 3
     for (int sg = 0; sg < nseg; ++sg) {
         const int64_t off = ((base + sg) * H + h) * (int64_t)(kDim * kDim);
-        for (int e = tid; e < kDim * kDim / 4; e += kCombineThreads)
-            reinterpret_cast<float4*>(ws_in + off)[e] = reinterpret_cast<const float4*>(S)[e];
+        for (int e = tid; e < kDim * kCombineCols / 4; e += kCombineThreads)
+            *reinterpret_cast<float4*>(ws_in + off + slice(e)) = reinterpret_cast<const float4*>(S)[e];
         if (sg == nseg - 1) break;
-        for (int e = tid; e < kDim * kDim / 4; e += kCombineThreads)
-            reinterpret_cast<float4*>(M)[e] = reinterpret_cast<const float4*>(ws_trans + off)[e];
-        __syncthreads();
-        float acc[8][8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a)
-#pragma unroll
-            for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
-        for (int kk = 0; kk < kDim; ++kk) {
-            float mv[8];
-#pragma unroll
-            for (int a = 0; a < 8; ++a) mv[a] = M[(8 * ti + a) * kDim + kk];
-            const float4 s0v = *reinterpret_cast<const float4*>(S + kk * kDim + 8 * tj);
-            const float4 s1v = *reinterpret_cast<const float4*>(S + kk * kDim + 8 * tj + 4);
-            const float sv[8] = {s0v.x, s0v.y, s0v.z, s0v.w, s1v.x, s1v.y, s1v.z, s1v.w};
-#pragma unroll
-            for (int a = 0; a < 8; ++a)
-#pragma unroll
-                for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(mv[a], sv[b], acc[a][b]);
+        for (int e = tid; e < kDim * kDim / 4; e += kCombineThreads) {
+            const int row = e & (kDim - 1), k4 = 4 * (e >> 7);  // neighbouring lanes: rows
+            const float4 v = *reinterpret_cast<const float4*>(ws_trans + off + row * kDim + k4);
+            Mt[(k4 + 0) * kCombineLdM + row] = v.x;
+            Mt[(k4 + 1) * kCombineLdM + row] = v.y;
+            Mt[(k4 + 2) * kCombineLdM + row] = v.z;
+            Mt[(k4 + 3) * kCombineLdM + row] = v.w;
         }
-        __syncthreads();  // everyone is done reading S
+        __syncthreads();
+        float acc[2][4];
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 4
+        for (int kk = 0; kk < kDim; ++kk) {  // the same summation order for every element
+            const float2 mm = *reinterpret_cast<const float2*>(Mt + kk * kCombineLdM + r);
+            const float m0 = mm.x, m1 = mm.y;
+            const float4 sv = *reinterpret_cast<const float4*>(S + kk * kCombineCols + cc);
+            acc[0][0] = fmaf(m0, sv.x, acc[0][0]); acc[0][1] = fmaf(m0, sv.y, acc[0][1]);
+            acc[0][2] = fmaf(m0, sv.z, acc[0][2]); acc[0][3] = fmaf(m0, sv.w, acc[0][3]);
+            acc[1][0] = fmaf(m1, sv.x, acc[1][0]); acc[1][1] = fmaf(m1, sv.y, acc[1][1]);
+            acc[1][2] = fmaf(m1, sv.z, acc[1][2]); acc[1][3] = fmaf(m1, sv.w, acc[1][3]);
+        }
+        __syncthreads();  // everyone is done reading S and M
         const float* st = ws_tilde + off;
 #pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            const int row = 8 * ti + a;
-#pragma unroll
-            for (int b = 0; b < 8; b += 4) {
-                const float4 t4 = *reinterpret_cast<const float4*>(st + row * kDim + 8 * tj + b);
-                *reinterpret_cast<float4*>(S + row * kDim + 8 * tj + b) =
-                    make_float4(acc[a][b] + t4.x, acc[a][b + 1] + t4.y, acc[a][b + 2] + t4.z,
-                                acc[a][b + 3] + t4.w);
-            }
+        for (int a = 0; a < 2; ++a) {
+            const float4 t4 = *reinterpret_cast<const float4*>(st + (r + a) * kDim + c0 + cc);
+            *reinterpret_cast<float4*>(S + (r + a) * kCombineCols + cc) =
+                make_float4(acc[a][0] + t4.x, acc[a][1] + t4.y, acc[a][2] + t4.z, acc[a][3] + t4.w);
         }
         __syncthreads();
     }
@@ -1238,11 +1245,12 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
     if (launches) ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess || ws.max_segments <= 1) return e;
     // compose the incoming state of every segment
-    const int csmem = 2 * kDim * kDim * 4;
+    const int csmem = (kDim * kCombineLdM + kDim * kCombineCols) * 4;
     if ((e = cudaFuncSetAttribute(kda_segment_combine_kernel,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, csmem)) != cudaSuccess)
         return e;
-    kda_segment_combine_kernel<<<dim3(num_seqs, heads), kCombineThreads, csmem, stream>>>(
+    kda_segment_combine_kernel<<<dim3(num_seqs, heads, kCombineColBlocks), kCombineThreads, csmem,
+                                 stream>>>(
         cu_seqlens, init_state, ws.tilde, ws.trans, ws.in, heads);
     if (launches) ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
