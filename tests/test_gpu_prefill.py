@@ -70,6 +70,27 @@ def test_ragged_lengths(dtype):
     check_status()
 
 
+def test_more_sequences_than_the_ranked_dispatch_covers():
+    """Beyond 2,048 sequences the CTAs run in packing order instead of longest first; the
+    results match the oracle, and the first sequences keep their bits from a small batch that
+    is dispatched longest first."""
+    rng = np.random.default_rng(11)
+    lens = [int(x) for x in rng.integers(0, 141, size=2100)]
+    x = synth.make_inputs(lens, 1, torch.bfloat16, seed=12, device=DEV)
+    out, fin = run_gpu(x)
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+    k = 40
+    cu = x["cu_seqlens"].cpu().tolist()
+    xs = {key: x[key][:cu[k]].contiguous() for key in ("q", "k", "v", "log_alpha", "beta")}
+    xs["init_state"] = x["init_state"][:k].contiguous()
+    xs["cu_seqlens"] = x["cu_seqlens"][:k + 1].contiguous()
+    xs["seqlens"] = lens[:k]
+    o1, f1 = run_gpu(xs)
+    assert torch.equal(o1, out[:cu[k]]) and torch.equal(f1, fin[:k])
+
+
 def test_no_initial_state():
     x = synth.make_inputs([100, 33], 2, torch.bfloat16, seed=6, device=DEV)
     out, fin = run_gpu(x, init=False)
