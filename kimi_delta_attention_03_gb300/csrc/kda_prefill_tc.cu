@@ -61,17 +61,20 @@ constexpr float kMaxExponentTC = 80.f;
 constexpr int LDA_T = 68;       // fp32 row stride of the 64 x 64 A / T matrix
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
-// Slot tile [k -> K_p -> -W ; q -> Q_r ; g]: 192 rows x 128 cols, two column regions of 24 KB.
-// Rows 0-127 are the A operand of the intra-chunk product ([K_p ; Q_r]) and later the B operand
-// of the state product ([-W ; Q_r], -W written over K_p once M2 has read it).  Rows 128-191
-// hold g, which is only read by the decay scan and the factor pass, so g of chunk c + 2 is
-// loaded as soon as those are done with chunk c, while k and q wait for M4 of chunk c.
-constexpr int KQW_ROWS = 192;
-constexpr uint32_t KQW_REGION = KQW_ROWS * 128;   // 24576
-constexpr uint32_t OFF_KQW0 = 0;         // slot 0 (48 KB)
-constexpr uint32_t OFF_KQW1 = 49152;     // slot 1
-constexpr uint32_t OFF_KMH0 = 98304;     // K_m hi slot 0: 64 x 128 (16 KB)
-constexpr uint32_t OFF_KMH1 = 114688;    // slot 1
+// Slot tile [k -> K_p -> -W ; q -> Q_r]: 128 rows x 128 cols, two column regions of 16 KB.  It
+// is the A operand of the intra-chunk product ([K_p ; Q_r]) and later the B operand of the state
+// product ([-W ; Q_r], -W written over K_p once M2 has read it); k and q of chunk c + 2 wait for
+// M4 of chunk c.  g has one buffer of its own: only the decay scan and the factor pass read it,
+// so g of chunk c + 1 is loaded as soon as the factor pass of chunk c is done.  K_m has three
+// slots, so the factor pass of chunk c waits for M6 of chunk c - 3 rather than c - 2.
+constexpr int KQW_ROWS = 128;
+constexpr uint32_t KQW_REGION = KQW_ROWS * 128;   // 16384
+constexpr uint32_t OFF_KQW0 = 0;         // slot 0 (32 KB)
+constexpr uint32_t OFF_KQW1 = 32768;     // slot 1
+constexpr uint32_t OFF_G = 65536;        // g: 64 x 128 (16 KB), two column regions of 8 KB
+constexpr uint32_t OFF_KMH0 = 81920;     // K_m slot 0: 64 x 128 (16 KB)
+constexpr uint32_t OFF_KMH1 = 98304;     // slot 1
+constexpr uint32_t OFF_KMH2 = 114688;    // slot 2
 constexpr uint32_t OFF_V = 131072;       // v: 64 x 128 (16 KB)
 constexpr uint32_t OFF_P0 = 147456;      // P hi (8 KB) + P lo (8 KB), slot 0
 constexpr uint32_t OFF_P1 = 163840;      // slot 1
@@ -94,8 +97,8 @@ static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 enum {
     B_FULL0 = 0, B_FULL1, B_VFREE0, B_VFREE1, B_VFULL, B_SPARE,
     B_FACT0, B_FACT1, B_AP0, B_AP1, B_TB0, B_TB1, B_WDONE0, B_WDONE1, B_WN0, B_WN1,
-    B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_UFREE0, B_UFREE1, B_KMFREE0, B_KMFREE1,
-    B_SDONE, B_PFREE0, B_PFREE1, B_SCAN0, B_SCAN1, B_GFULL0, B_GFULL1, B_M6ISS, B_COUNT
+    B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_UFREE0, B_UFREE1, B_KMFREE0, B_KMFREE1, B_KMFREE2,
+    B_SDONE, B_PFREE0, B_PFREE1, B_SCAN0, B_SCAN1, B_GFULL, B_M6ISS, B_COUNT
 };
 static_assert(B_COUNT <= NBAR, "barrier slots");
 
@@ -288,11 +291,10 @@ __device__ __noinline__ bool decay_scan(unsigned char* sm, int cs, int L, int te
     float* er = reinterpret_cast<float*>(sm + OFF_ER);
     float* sc = reinterpret_cast<float*>(sm + OFF_SC);
     const int s2 = cs & 1;
-    if (!wait_bar(&bars[B_GFULL0 + s2], (cs >> 1) & 1, abort_flag, status)) return false;
+    if (!wait_bar(&bars[B_GFULL], cs & 1, abort_flag, status)) return false;
     const int valid = min(kChunk, L - kChunk * cs);
-    // g is row 128 + t of the slot tile; (128 + t) & 7 == t & 7
-    const unsigned char* gcol =
-        sm + (s2 ? OFF_KQW1 : OFF_KQW0) + (te >> 6) * KQW_REGION + 128 * 128 + ((te & 7) << 1);
+    // g of token t is row t of its column region
+    const unsigned char* gcol = sm + OFF_G + (te >> 6) * 8192 + ((te & 7) << 1);
     const int chunk16 = (te & 63) >> 3;
     float run = 0.f, gmax = 0.f;
 #pragma unroll 1
@@ -439,7 +441,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t a_base = saddr(sm);
     // shared addresses of the per-slot tiles (slot s = chunk & 1)
     auto a_kq = [&](int s) { return a_base + (s ? OFF_KQW1 : OFF_KQW0); };
-    auto a_kmh = [&](int s) { return a_base + (s ? OFF_KMH1 : OFF_KMH0); };
+    auto kmh_off = [](int c) { const int s3 = c % 3; return s3 == 0 ? OFF_KMH0 : s3 == 1 ? OFF_KMH1 : OFF_KMH2; };
+    auto a_kmh = [&](int c) { return a_base + kmh_off(c); };  // K_m slot of chunk c
     auto a_p = [&](int s) { return a_base + (s ? OFF_P1 : OFF_P0); };
     auto a_tb = [&](int s) { return a_base + (s ? OFF_TB1 : OFF_TB0); };
     // TMA issue helpers: k, q of chunk c into slot c & 1 (once M4 two chunks back has read the
@@ -459,13 +462,11 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         *kqg_issued = c + 1;
     };
     auto issue_g = [&](int c) {
-        const int s = c & 1;
-        unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
-        uint64_t* full = &bars[B_GFULL0 + s];
+        uint64_t* full = &bars[B_GFULL];
         const int t0 = (int)(seq0 + (int64_t)kChunk * c);
         mbar_arrive_expect_tx(full, 16384);
 #pragma unroll
-        for (int r = 0; r < 2; ++r) tma_load_3d(kq + r * KQW_REGION + 16384, &tm_g, full, 64 * r, h, t0);
+        for (int r = 0; r < 2; ++r) tma_load_3d(sm + OFF_G + r * 8192, &tm_g, full, 64 * r, h, t0);
     };
     auto issue_v = [&](int c) {
         if (zero_v) {
@@ -488,11 +489,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             issue_g(0);
             issue_kq(0);
             issue_v(0);
-            if (nchunks > 1) {
-                issue_g(1);
-                issue_kq(1);
-            }
-            int g_issued = min(nchunks, 2);
+            if (nchunks > 1) issue_kq(1);
+            int g_issued = 1;
             const uint32_t rP = tmem + T_P;
             const uint32_t a_v = saddr(sm + OFF_V);
             const uint32_t id_kk64 = idesc_bf16(128, 64, false, false);
@@ -502,14 +500,14 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             auto issue_m1 = [&](const int c) -> bool {
                 const int s = c & 1;
                 if (!spin_bar(&bars[B_FACT0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
-                // the factor pass and the scan have read g of chunk c: load g of chunk c + 2
-                if (c + 2 < nchunks) {
-                    issue_g(c + 2);
-                    g_issued = c + 3;
+                // the factor pass and the scan have read g of chunk c: load g of chunk c + 1
+                if (c + 1 < nchunks) {
+                    issue_g(c + 1);
+                    g_issued = c + 2;
                 }
                 tc_fence_after();
                 const uint64_t dq = smem_desc(a_kq(s), 16, 1024);
-                const uint64_t dh = smem_desc(a_kmh(s), 16, 1024);
+                const uint64_t dh = smem_desc(a_kmh(c), 16, 1024);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)  // 16 B descriptor units: K step 32 B
                     mma_ss(rP, dq + (j >> 2) * (KQW_REGION >> 4) + (j & 3) * 2,
@@ -569,8 +567,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const int nk = *kqg_issued;
                 for (int c = nk - 2; c < nk; ++c)
                     if (c >= 0) mbar_wait(&bars[B_FULL0 + (c & 1)], (c >> 1) & 1, kWaitLimit);
-                for (int c = g_issued - 2; c < g_issued; ++c)
-                    if (c >= 0) mbar_wait(&bars[B_GFULL0 + (c & 1)], (c >> 1) & 1, kWaitLimit);
+                mbar_wait(&bars[B_GFULL], (g_issued - 1) & 1, kWaitLimit);
             }
         }
     } else if (warp == kWarpMma) {
@@ -608,13 +605,13 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const uint32_t rUH = rX, rUL = rX + 32, rO = rX + 64;
                     const uint64_t dph = smem_desc(a_p(s), 16, 1024);
                     const uint64_t dpl = smem_desc(a_p(s) + 8192, 16, 1024);
-                    const uint64_t dk = smem_desc(a_kmh(s), 8192, 1024);
+                    const uint64_t dk = smem_desc(a_kmh(c), 8192, 1024);
                     // the state update first: the next chunk waits on it, the output does not
 #pragma unroll
                     for (int j = 0; j < 4; ++j) mma_ts(rS, rUH + 8 * j, dk + 128 * j, id_km128, 1);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) mma_ts(rS, rUL + 8 * j, dk + 128 * j, id_km128, 1);
-                    mma_commit(&bars[B_KMFREE0 + s]);  // K_m of this slot has been read
+                    mma_commit(&bars[B_KMFREE0 + c % 3]);  // K_m of this slot has been read
                     mma_commit(&bars[B_SDONE]);
                     mbar_arrive(&bars[B_M6ISS]);  // M6 is queued: the next M2 may follow it
                     if (has_out) {
@@ -660,7 +657,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int valid = min(kChunk, L - kChunk * c);
             const int64_t tok0 = seq0 + (int64_t)kChunk * c;
             unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
-            unsigned char* kmh = sm + (s ? OFF_KMH1 : OFF_KMH0);
+            unsigned char* kmh = sm + kmh_off(c);
             if (!wait_bar(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
 
             // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7.
@@ -675,7 +672,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     beta_raw = 0;
             }
             // g has landed (the scan waited for it too) and its prefixes are in place
-            if (!wait_bar(&bars[B_GFULL0 + s], (c >> 1) & 1, abort_flag, p.status) ||
+            if (!wait_bar(&bars[B_GFULL], c & 1, abort_flag, p.status) ||
                 !wait_bar(&bars[B_SCAN0 + s], (c >> 1) & 1, abort_flag, p.status))
                 return false;
             {
@@ -694,19 +691,20 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     G[4] = fmaf(b.x, kLog2eTC, -r[4]); G[5] = fmaf(b.y, kLog2eTC, -r[5]);
                     G[6] = fmaf(b.z, kLog2eTC, -r[6]); G[7] = fmaf(b.w, kLog2eTC, -r[7]);
                 }
-                // K_m of this slot is overwritten only after M6 two chunks back has read it
-                if (c >= 2 &&
-                    !wait_bar(&bars[B_KMFREE0 + s], ((c - 2) >> 1) & 1, abort_flag, p.status))
+                // K_m of this slot is overwritten only after M6 three chunks back has read it
+                if (c >= 3 && !wait_bar(&bars[B_KMFREE0 + c % 3], ((c - 3) / 3) & 1, abort_flag,
+                                        p.status))
                     return false;
 #pragma unroll 1
                 for (int i = 0; i < 4; ++i) {
-                    // one token per step; rows t, 64 + t and 128 + t of the slot tile (k, q, g)
-                    // share the swizzle phase t & 7, so one offset serves all three, and k, q are
-                    // replaced in place by K_p, Q_r
+                    // one token per step: rows t and 64 + t of the slot tile (k, q; they share the
+                    // swizzle phase t & 7, so one offset serves both, and they are replaced in
+                    // place by K_p, Q_r) and row t of the g buffer
                     const int t = 4 * tg + i;
                     const uint32_t o = sw128_offset(t, c8, KQW_ROWS);
                     uint4 gr = make_uint4(0u, 0u, 0u, 0u);
-                    if (t < valid) gr = *reinterpret_cast<const uint4*>(kq + o + 128 * 128);
+                    if (t < valid)
+                        gr = *reinterpret_cast<const uint4*>(sm + OFF_G + sw128_offset(t, c8, 64));
                     const uint4 kr = *reinterpret_cast<const uint4*>(kq + o);
                     const uint4 qr4 = *reinterpret_cast<const uint4*>(kq + o + 64 * 128);
                     float gv[8], kv[8], qv[8];
