@@ -15,7 +15,7 @@
 //
 // GB300 mapping.  One CTA per (sequence, head), 14 warps:
 //   warp 0      prep MMA issuer (one thread): the chunk-local products of chunk c+1, the TMA
-//               loads of v and of g two chunks ahead; it also issues the first q, k, g, v loads
+//               loads of v and of g one chunk ahead; it also issues the first q, k, g, v loads
 //   warp 1      serial MMA issuer (one thread): the state products of chunk c
 //   warps 2-9   prep: exponential factors, A/P epilogue, 64x64 inverse, W epilogue (chunk c+1)
 //   warps 10-13 serial epilogue: U^T to TMEM, the cumulative decay of chunk c+2, state rescale,
@@ -446,7 +446,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     auto a_p = [&](int s) { return a_base + (s ? OFF_P1 : OFF_P0); };
     auto a_tb = [&](int s) { return a_base + (s ? OFF_TB1 : OFF_TB0); };
     // TMA issue helpers: k, q of chunk c into slot c & 1 (once M4 two chunks back has read the
-    // slot), g of chunk c (once the factor pass two chunks back has read it), v of chunk c
+    // slot), g of chunk c (once the factor pass of chunk c - 1 has read it), v of chunk c
     auto issue_kq = [&](int c) {
         const int s = c & 1;
         unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
