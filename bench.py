@@ -341,6 +341,27 @@ def main():
                           "hbm_frac_of_roofline": bytes_x / (ms_x * 1e-3) / 1e9 / hbm_peak,
                           "plan": kda.fwd_plan(xe["seqlens"], we.heads)}
             del xe, oute, fine, wse
+        # the headline prefill with a state checkpoint every 512 tokens (prefix-cache use)
+        every = 512
+        ckpts = torch.empty((kda.fwd_checkpoint_count(x["seqlens"], H, every), H, D, D),
+                            dtype=torch.float32, device=dev)
+
+        def estep_ck():
+            kda.fwd_chunked_checkpoints(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                        x["cu_seqlens"], x["seqlens"], every,
+                                        init_state=x["init_state"], out=out, final_state=fin,
+                                        checkpoints=ckpts)
+
+        for _ in range(2):
+            estep_ck()
+        k_c = max(2, min(args.steps, 10))
+        ms_c = max_over_ranks(time_device(estep_ck, k_c, stream), world)
+        extra["prefill_4x8k_ckpt512"] = {
+            "workload": w.name + " + state checkpoint every 512 tokens", "tokens": T,
+            "checkpoints": int(ckpts.shape[0]) * H, "ms_per_step": ms_c, "steps": k_c,
+            "value": T * world / (ms_c * 1e-3) / 1e6, "unit": "Mtokens/s",
+            "overhead_vs_plain": ms_c / ms_max - 1.0}
+        del ckpts
 
     # ---------------- end to end (host buffers, copies inside the timed region) ------------
     e2e = None

@@ -127,6 +127,39 @@ kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, c
                            void* workspace, size_t workspace_bytes, kda_stream_t stream);
 
 /*
+ * kda_fwd_checkpoint_count — number of states kda_fwd_chunked_ckpt writes for `desc` and an
+ * interval of `ckpt_every` tokens: the sum over sequences of floor(L_n / ckpt_every).  Host
+ * only.  Returns -1 if the description is invalid or ckpt_every is not a positive multiple of
+ * 64 (the chunk size).
+ */
+int64_t kda_fwd_checkpoint_count(const kda_desc* desc, int32_t ckpt_every);
+
+/*
+ * kda_fwd_chunked_ckpt — kda_fwd_chunked that also writes state checkpoints.
+ *
+ * A prefix cache can resume a sequence only where its recurrent state was saved, and serving
+ * saves it at the block-aligned positions a prefix lookup can reference
+ * ("k3_training_and_infra_notes", section 4.5, KDA-aware prefix cache management; "How Kimi K3
+ * Engineered Its Way to the Frontier", section "KDA states and MLA KV blocks share one paged
+ * pool", Figure 12: a checkpoint at a 512-token hash-block boundary).  For every (sequence,
+ * head) this call writes the fp32 state after the first p tokens, for p = ckpt_every,
+ * 2 ckpt_every, ... up to and including the sequence length, in the layout of final_state.
+ *
+ *   ckpt_every    positive multiple of 64 (the chunk size), in tokens
+ *   ckpt_states   device fp32 [count, H, 128, 128], count = kda_fwd_checkpoint_count(desc,
+ *                 ckpt_every): sequence by sequence, each sequence's positions in increasing
+ *                 order.  Must not alias any other argument; NULL only when count is 0.
+ * Everything else (arguments, layouts, errors) is as for kda_fwd_chunked, and the outputs and
+ * final states are bit-identical to that call's.  bf16 inputs only (KDA_ERR_UNSUPPORTED for
+ * fp32 inputs).
+ */
+kda_status kda_fwd_chunked_ckpt(const kda_desc* desc, const void* q, const void* k,
+                                const void* v, const void* log_alpha, const void* beta,
+                                const float* init_state, const int32_t* cu_seqlens, void* out,
+                                float* final_state, int32_t ckpt_every, float* ckpt_states,
+                                void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * kda_fwd_chunked_noalloc — kda_fwd_chunked for callers that cannot allocate device memory.
  *
  * No counterpart in the paper: this is a deployment convenience.  Some callers cannot supply

@@ -9,7 +9,9 @@ from . import binding  # noqa: F401
 from .binding import (  # noqa: F401
     KdaError,
     decode_step,
+    fwd_checkpoint_count,
     fwd_chunked,
+    fwd_chunked_checkpoints,
     fwd_chunked_host,
     fwd_plan,
     fwd_workspace_bytes,
@@ -20,7 +22,8 @@ from .binding import (  # noqa: F401
 )
 
 __all__ = [
-    "KdaError", "decode_step", "fwd_chunked", "fwd_chunked_host", "fwd_workspace_bytes",
+    "KdaError", "decode_step", "fwd_checkpoint_count", "fwd_chunked", "fwd_chunked_checkpoints",
+    "fwd_chunked_host", "fwd_workspace_bytes",
     "launch_count",
     "library_path", "load_library", "read_device_status",
 ]

@@ -54,6 +54,9 @@ SIGNATURES = {
                                        _P, _P, ctypes.c_size_t, _P]),
     "kda_fwd_chunked_noalloc": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P,
                                                _P, _P, _P, _P]),
+    "kda_fwd_checkpoint_count": (ctypes.c_int64, [ctypes.POINTER(KdaDesc), ctypes.c_int32]),
+    "kda_fwd_chunked_ckpt": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P,
+                                            _P, _P, ctypes.c_int32, _P, _P, ctypes.c_size_t, _P]),
     "kda_decode_step": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P]),
     "kda_read_device_status": (ctypes.c_int, [_P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -159,6 +162,63 @@ def fwd_chunked(q, k, v, log_alpha, beta, cu_seqlens, seqlens, init_state=None, 
     if st != KDA_OK:
         raise KdaError(st, "kda_fwd_chunked")
     return out, final_state
+
+
+def fwd_checkpoint_count(seqlens, num_heads: int, ckpt_every: int,
+                         dtype: torch.dtype = torch.bfloat16) -> int:
+    """Number of states fwd_chunked_checkpoints writes: sum of L_n // ckpt_every (ckpt_every a
+    positive multiple of 64)."""
+    lib = load_library()
+    desc = make_desc(seqlens, num_heads, dtype)
+    n = int(lib.kda_fwd_checkpoint_count(ctypes.byref(desc), int(ckpt_every)))
+    if n < 0:
+        raise KdaError(-1, "kda_fwd_checkpoint_count")
+    return n
+
+
+def fwd_chunked_checkpoints(q, k, v, log_alpha, beta, cu_seqlens, seqlens, ckpt_every: int,
+                            init_state=None, out=None, final_state=None, checkpoints=None,
+                            workspace=None, stream=None):
+    """fwd_chunked that also returns the fp32 state after every ``ckpt_every`` tokens of each
+    sequence (positions ckpt_every, 2 ckpt_every, ... <= L_n), as ``checkpoints`` of shape
+    [count, H, 128, 128]: sequence by sequence, positions in increasing order.  Outputs and
+    final states are bit-identical to fwd_chunked.  Returns (out, final_state, checkpoints)."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("fwd_chunked_checkpoints needs CUDA tensors")
+    T, H, d = q.shape
+    N = len(seqlens)
+    dt = q.dtype
+    for name, t, shp in (("k", k, (T, H, d)), ("v", v, (T, H, d)),
+                         ("log_alpha", log_alpha, (T, H, d)), ("beta", beta, (T, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    if init_state is not None:
+        _check_io("init_state", init_state, (N, H, d, d), torch.float32, dev)
+    if out is None:
+        out = torch.empty((T, H, d), dtype=dt, device=dev)
+    _check_io("out", out, (T, H, d), dt, dev)
+    if final_state is None:
+        final_state = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    _check_io("final_state", final_state, (N, H, d, d), torch.float32, dev)
+    count = fwd_checkpoint_count(seqlens, H, ckpt_every, dt)
+    if checkpoints is None:
+        checkpoints = torch.empty((count, H, d, d), dtype=torch.float32, device=dev)
+    _check_io("checkpoints", checkpoints, (count, H, d, d), torch.float32, dev)
+    desc = make_desc(seqlens, H, dt, d)
+    need = int(lib.kda_fwd_workspace_bytes(ctypes.byref(desc)))
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kda_fwd_chunked_ckpt(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                  _ptr(beta), _ptr(init_state), _ptr(cu_seqlens), _ptr(out),
+                                  _ptr(final_state), int(ckpt_every),
+                                  _ptr(checkpoints) if count else None, _ptr(workspace), ws_bytes,
+                                  _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fwd_chunked_ckpt")
+    return out, final_state, checkpoints
 
 
 def fwd_chunked_noalloc(q, k, v, log_alpha, beta, cu_seqlens, seqlens, init_state=None,

@@ -87,10 +87,16 @@ size_t kda_fwd_workspace_bytes(const kda_desc* desc) {
     return p.workspace_bytes;
 }
 
-kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, const void* v,
-                           const void* log_alpha, const void* beta, const float* init_state,
-                           const int32_t* cu_seqlens, void* out, float* final_state,
-                           void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// kda_fwd_chunked with optional state checkpoints every ckpt_every tokens (0: none).
+kda_status fwd_chunked_impl(const kda_desc* desc, const void* q, const void* k, const void* v,
+                            const void* log_alpha, const void* beta, const float* init_state,
+                            const int32_t* cu_seqlens, void* out, float* final_state,
+                            int32_t ckpt_every, float* ckpt_states, void* workspace,
+                            size_t workspace_bytes, kda_stream_t stream) {
     kda_plan_info plan;
     kda_status st = kda_fwd_plan(desc, &plan);
     if (st != KDA_OK) return st;
@@ -102,6 +108,17 @@ kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, c
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
         !aligned16(out) || !aligned16(init_state) || !aligned16(final_state))
         return KDA_ERR_INVALID_ARG;
+    int64_t ckpts = 0;
+    if (ckpt_every != 0) {
+        ckpts = kda_fwd_checkpoint_count(desc, ckpt_every);
+        if (ckpts < 0) return KDA_ERR_INVALID_ARG;
+        if (ckpts > 0 && desc->in_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+        if (ckpts > 0 && (!ckpt_states || !aligned16(ckpt_states))) return KDA_ERR_INVALID_ARG;
+        const void* c = ckpt_states;
+        if (ckpts > 0 && (c == q || c == k || c == v || c == log_alpha || c == beta || c == out ||
+                          c == init_state || c == final_state))
+            return KDA_ERR_INVALID_ARG;
+    }
     if (plan.workspace_bytes > 0 && (!workspace || workspace_bytes < plan.workspace_bytes ||
                                      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
         return KDA_ERR_WORKSPACE;
@@ -122,13 +139,45 @@ kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, c
         e = kda::launch_prefill_tc(desc->num_seqs, desc->num_heads, desc->total_tokens, q, k, v,
                                    log_alpha, beta, init_state, cu_seqlens, out, final_state, ws,
                                    status, (cudaStream_t)stream, &launches,
-                                   desc->host_seqlens);
+                                   desc->host_seqlens, ckpts > 0 ? ckpt_states : nullptr,
+                                   ckpts > 0 ? ckpt_every / kda::kChunk : 0);
     else
         e = kda::launch_prefill(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v,
                                 log_alpha, beta, init_state, cu_seqlens, out, final_state,
                                 status, (cudaStream_t)stream, &launches);
     g_launches += launches;
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, const void* v,
+                           const void* log_alpha, const void* beta, const float* init_state,
+                           const int32_t* cu_seqlens, void* out, float* final_state,
+                           void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    return fwd_chunked_impl(desc, q, k, v, log_alpha, beta, init_state, cu_seqlens, out,
+                            final_state, 0, nullptr, workspace, workspace_bytes, stream);
+}
+
+int64_t kda_fwd_checkpoint_count(const kda_desc* desc, int32_t ckpt_every) {
+    if (ckpt_every <= 0 || ckpt_every % kda::kChunk != 0) return -1;
+    if (check_desc(desc, true) != KDA_OK) return -1;
+    int64_t count = 0;
+    for (int32_t n = 0; n < desc->num_seqs; ++n) count += desc->host_seqlens[n] / ckpt_every;
+    return count;
+}
+
+kda_status kda_fwd_chunked_ckpt(const kda_desc* desc, const void* q, const void* k,
+                                const void* v, const void* log_alpha, const void* beta,
+                                const float* init_state, const int32_t* cu_seqlens, void* out,
+                                float* final_state, int32_t ckpt_every, float* ckpt_states,
+                                void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    if (ckpt_every <= 0) return KDA_ERR_INVALID_ARG;
+    return fwd_chunked_impl(desc, q, k, v, log_alpha, beta, init_state, cu_seqlens, out,
+                            final_state, ckpt_every, ckpt_states, workspace, workspace_bytes,
+                            stream);
 }
 
 kda_status kda_decode_step(const kda_desc* desc, const void* q, const void* k, const void* v,

@@ -88,11 +88,13 @@ struct SeqOrder {
 };
 
 // host_seqlens (optional, host memory): the sequence lengths, used only to rank the sequences
-// for dispatch; without them the CTAs run in packing order.
+// for dispatch; without them the CTAs run in packing order.  ckpt (optional, device): state
+// checkpoints after every ckpt_chunks chunks of each sequence, [count][H][128][128] fp32.
 cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, const void* q,
                               const void* k, const void* v, const void* g, const void* beta,
                               const float* init_state, const int32_t* cu_seqlens, void* out,
                               float* final_state, const SegWorkspace& ws, int* status,
                               cudaStream_t stream, uint64_t* launches,
-                              const int32_t* host_seqlens = nullptr);
+                              const int32_t* host_seqlens = nullptr, float* ckpt = nullptr,
+                              int ckpt_chunks = 0);
 }  // namespace kda

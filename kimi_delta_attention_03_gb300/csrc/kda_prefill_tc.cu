@@ -120,6 +120,8 @@ struct TcParams {
     float* ws_tilde;   // segment states from zero        [slots][H][128][128]
     float* ws_trans;   // segment transitions             [slots][H][128][128]
     float* ws_in;      // composed incoming states        [slots][H][128][128]
+    float* ckpt;       // state checkpoints [count][H][128][128], or null
+    int ckpt_chunks;   // chunks between checkpoints
     int H;
     int pass;          // 0: whole sequences + pass A of split ones; 1: pass B of split ones
 };
@@ -279,6 +281,19 @@ __device__ __forceinline__ bool spin_bar(uint64_t* bar, uint32_t parity, volatil
     return mbar_test(bar, parity) || spin_bar_poll(bar, parity, abort_flag, status);
 }
 
+// The state after a chunk for one warp's 32 value channels: S[k][v] = X[v][k] e^{r_k} with X
+// read from TMEM at taddr (the warp's lanes, key channels as columns); dst is [128][128] fp32,
+// row = key channel.
+__device__ __forceinline__ void store_state(float* dst, uint32_t taddr, const float* ec, int vch) {
+#pragma unroll 1
+    for (int cc = 0; cc < kDim; cc += 32) {
+        uint32_t x[32];
+        tmem_ld32(taddr + cc, x);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[(cc + j) * kDim + vch] = __uint_as_float(x[j]) * ec[cc + j];
+    }
+}
+
 // Cumulative decay of chunk cs for the epilogue warp group, thread te = key channel: exclusive
 // prefixes of g at the 16 four-token groups (into the prefix array), G_C, e^{r} with
 // r = G_C / 2, and the state scale e^{r_{cs-1} + r_cs}.  Group sums first, then the prefix over
@@ -332,6 +347,8 @@ __device__ __noinline__ bool decay_scan(unsigned char* sm, int cs, int L, int te
     return true;
 }
 
+// kCkpt: the variant that also writes state checkpoints (the plain one carries no trace of it).
+template <bool kCkpt>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -940,6 +957,17 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int q4 = warp & 3;
         const int vch = 32 * q4 + lane;  // value channel = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        // state checkpoints (items with outputs only): this (sequence, head)'s first checkpoint
+        // slot, and the sequence chunk of this item's chunk 0
+        float* ckpt0 = nullptr;
+        if (kCkpt && p.ckpt && has_out) {
+            const int every = kChunk * p.ckpt_chunks;  // token offsets are int32
+            int64_t base = 0;
+#pragma unroll 1
+            for (int m = 0; m < n; ++m) base += (p.cu_seqlens[m + 1] - p.cu_seqlens[m]) / every;
+            ckpt0 = p.ckpt + (base * H + h) * (int64_t)(kDim * kDim);
+        }
+        const int chunk0 = item == ITEM_SEGMENT ? sigma * kSegChunks : 0;
         auto scan = [&](const int cs) -> bool {
             return decay_scan(sm, cs, L, te, abort_flag, p.status);
         };
@@ -1013,6 +1041,15 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (!(ok = wait_bar(&bars[B_SDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
             const bool last = (c + 1 == nchunks);
+            // The state after this chunk is a checkpoint when its sequence position is a
+            // multiple of the interval (a ragged last chunk never is).  S = X diag(e^{r_c}),
+            // transposed back, exactly as the final state.
+            const int done = chunk0 + c + 1;
+            float* ckd = (kCkpt && ckpt0 && valid == kChunk && done % p.ckpt_chunks == 0)
+                             ? ckpt0 + (int64_t)(done / p.ckpt_chunks - 1) * H * (kDim * kDim)
+                             : nullptr;
+            const float* ec = er + (c & 3) * kDim;
+            if (ckd) store_state(ckd, tmem + T_S + lane_off, ec, vch);
             if (!last) {  // the scale of chunk c + 1 is from this warp group's own scan
                 const float* scn = sc + ((c + 1) & 3) * kDim;
 #pragma unroll 1
@@ -1038,16 +1075,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 named_bar(kBarEpi, kEpiThreads);
                 if (te == 0) mbar_arrive(&bars[B_SREADY]);
             } else if (final_dst) {
-                const float* ec = er + (c & 3) * kDim;
-                float* fs = final_dst;
-#pragma unroll 1
-                for (int cc = 0; cc < kDim; cc += 32) {
-                    uint32_t x[32];
-                    tmem_ld32(tmem + T_S + cc + lane_off, x);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        fs[(cc + j) * kDim + vch] = __uint_as_float(x[j]) * ec[cc + j];
-                }
+                store_state(final_dst, tmem + T_S + lane_off, ec, vch);
             }
             if (!(ok = wait_bar(&bars[B_OSDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
@@ -1202,7 +1230,7 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
                               const float* init_state, const int32_t* cu_seqlens, void* out,
                               float* final_state, const SegWorkspace& ws, int* status,
                               cudaStream_t stream, uint64_t* launches,
-                              const int32_t* host_seqlens) {
+                              const int32_t* host_seqlens, float* ckpt, int ckpt_chunks) {
     if (num_seqs <= 0 || heads <= 0) return cudaSuccess;
     const int64_t units = (int64_t)num_seqs * heads;
     if (units > INT32_MAX) return cudaErrorInvalidValue;
@@ -1231,15 +1259,18 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
     prm.ws_tilde = ws.tilde;
     prm.ws_trans = ws.trans;
     prm.ws_in = ws.in;
+    prm.ckpt = ckpt_chunks > 0 ? ckpt : nullptr;
+    prm.ckpt_chunks = ckpt_chunks > 0 ? ckpt_chunks : 1;
     prm.H = heads;
     prm.pass = 0;
-    cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    auto kernel = prm.ckpt ? kda_prefill_tc_kernel<true> : kda_prefill_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const int zsplit = ws.max_segments > 1 ? 2 * (ws.max_segments - 1) : 1;
     // pass 0: whole sequences, and pass A (segment states and transitions) of split ones
-    kda_prefill_tc_kernel<<<dim3((unsigned)units, 1, zsplit), kThreadsTC, SMEM_ALLOC, stream>>>(
-        mq, mk, mv, mg, prm, order);
+    kernel<<<dim3((unsigned)units, 1, zsplit), kThreadsTC, SMEM_ALLOC, stream>>>(mq, mk, mv, mg,
+                                                                                 prm, order);
     if (launches) ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess || ws.max_segments <= 1) return e;
     // compose the incoming state of every segment
@@ -1254,8 +1285,8 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // pass B: every segment of the split sequences from its composed incoming state
     prm.pass = 1;
-    kda_prefill_tc_kernel<<<dim3((unsigned)units, 1, ws.max_segments), kThreadsTC, SMEM_ALLOC,
-                            stream>>>(mq, mk, mv, mg, prm, order);
+    kernel<<<dim3((unsigned)units, 1, ws.max_segments), kThreadsTC, SMEM_ALLOC, stream>>>(
+        mq, mk, mv, mg, prm, order);
     if (launches) ++*launches;
     return cudaGetLastError();
 }

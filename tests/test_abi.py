@@ -75,6 +75,16 @@ def test_plan_splits_long_sequences_by_length_only(lib):
     assert binding.fwd_plan([100, 200], H)["workspace_bytes"] == 0
 
 
+def test_checkpoint_count(lib):
+    from kimi_delta_attention_03_gb300 import binding
+    lens = [0, 63, 64, 511, 512, 1000, 1024]
+    assert binding.fwd_checkpoint_count(lens, 2, 512) == 0 + 0 + 0 + 0 + 1 + 1 + 2
+    assert binding.fwd_checkpoint_count(lens, 2, 64) == 0 + 0 + 1 + 7 + 8 + 15 + 16
+    desc = binding.make_desc(lens, 2, torch.bfloat16)
+    for bad in (0, -64, 100, 32):  # a positive multiple of the 64-token chunk only
+        assert lib.kda_fwd_checkpoint_count(ctypes.byref(desc), bad) == -1
+
+
 def test_host_argument_checks(lib):
     from kimi_delta_attention_03_gb300 import binding
     P = ctypes.c_void_p

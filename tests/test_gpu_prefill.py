@@ -91,6 +91,54 @@ def test_more_sequences_than_the_ranked_dispatch_covers():
     assert torch.equal(o1, out[:cu[k]]) and torch.equal(f1, fin[:k])
 
 
+def _checkpoint_reference(x, lens, every):
+    """Oracle states after every `every` tokens: the final states of the packed prefixes."""
+    cu = x["cu_seqlens"].cpu().tolist()
+    cuts = [(n, m * every) for n, L in enumerate(lens) for m in range(1, L // every + 1)]
+    rows = [torch.arange(cu[n], cu[n] + p_) for n, p_ in cuts]
+    pick = lambda t: torch.cat([t.cpu()[r] for r in rows])
+    cu2 = np.concatenate([[0], np.cumsum([p_ for _, p_ in cuts])]).astype(np.int32)
+    s0 = x["init_state"].cpu()[[n for n, _ in cuts]]
+    _, s_ref = oracle.recurrence(pick(x["q"]), pick(x["k"]), pick(x["v"]), pick(x["log_alpha"]),
+                                 pick(x["beta"]), cu2, state_in=s0, want_out=False,
+                                 threads=oracle_threads())
+    return s_ref
+
+
+@pytest.mark.parametrize("every", [64, 256])
+def test_checkpoints_match_oracle_prefix_states(every):
+    """The state after every `every` tokens of each sequence equals the token loop's state on
+    that prefix; outputs and final states stay those of the plain call, bit for bit."""
+    lens = [1100, 64, 513, 0, 2085, 255]
+    x = synth.make_inputs(lens, 2, torch.bfloat16, seed=21, device=DEV)
+    out, fin, ck = kda().fwd_chunked_checkpoints(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                                 x["cu_seqlens"], x["seqlens"], every,
+                                                 init_state=x["init_state"])
+    torch.cuda.synchronize()
+    check_status()
+    o0, f0 = run_gpu(x)
+    assert torch.equal(out, o0) and torch.equal(fin, f0)
+    s_ref = _checkpoint_reference(x, lens, every)
+    assert ck.shape[0] == s_ref.shape[0] == sum(L // every for L in lens)
+    assert_close("checkpoints", ck.cpu().numpy(), s_ref)
+
+
+def test_checkpoints_of_a_segmented_sequence():
+    """A sequence above 64K tokens runs as segments; checkpoints that fall inside segments and
+    on their boundaries come out of the second pass with the right positions."""
+    lens = [70000, 300]
+    every = 3072  # 48 chunks: not aligned to the 128-chunk segments
+    x = synth.make_inputs(lens, 1, torch.bfloat16, seed=22, device=DEV)
+    out, fin, ck = kda().fwd_chunked_checkpoints(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                                 x["cu_seqlens"], x["seqlens"], every,
+                                                 init_state=x["init_state"])
+    torch.cuda.synchronize()
+    check_status()
+    s_ref = _checkpoint_reference(x, lens, every)
+    assert ck.shape[0] == 70000 // every
+    assert_close("checkpoints", ck.cpu().numpy(), s_ref)
+
+
 def test_no_initial_state():
     x = synth.make_inputs([100, 33], 2, torch.bfloat16, seed=6, device=DEV)
     out, fin = run_gpu(x, init=False)
