@@ -312,6 +312,30 @@ def main():
                                "traffic": recorded_traffic("kda_decode"),
                                "algorithmic_bytes_per_launch": dbytes}}
         del dd, dout
+        # speculative-decoding window: runs of 4 tokens per sequence (accepted replay, bonus,
+        # draft), 2 of them committed; the state crosses HBM once each way
+        run, keep = 4, 2
+        xw = synth.make_inputs([run] * n_dec, 96, torch.bfloat16, seed=wd.seed, s0_std=wd.s0_std,
+                               device=dev)
+        wstate = xw["init_state"]
+        wout = torch.empty_like(xw["q"])
+        wcommit = torch.full((n_dec,), keep, dtype=torch.int32, device=dev)
+
+        def wstep():
+            kda.decode_window(xw["q"], xw["k"], xw["v"], xw["log_alpha"], xw["beta"],
+                              xw["cu_seqlens"], xw["seqlens"], wstate, commit=wcommit, out=wout)
+
+        for _ in range(args.warmup):
+            wstep()
+        barrier(world)
+        wms = max_over_ranks(time_device(wstep, args.steps, stream), world)
+        wbytes = dunits * (2 * STATE_BYTES + run * BYTES_PER_TOKEN_HEAD)
+        decode["window"] = {"workload": f"{n_dec} sequences x 96 heads, runs of {run} tokens, "
+                                        f"{keep} committed", "ms_per_step": wms,
+                            "tokens_per_s": n_dec * run * world / (wms * 1e-3),
+                            "hbm_gbs": wbytes / (wms * 1e-3) / 1e9,
+                            "hbm_frac": wbytes / (wms * 1e-3) / 1e9 / hbm_peak}
+        del xw, wstate, wout, wcommit
 
     # ---------------- the other prefill workloads (reported, not the headline) ------------
     extra = None

@@ -204,6 +204,34 @@ kda_status kda_decode_step(const kda_desc* desc, const void* q, const void* k, c
                            kda_stream_t stream);
 
 /*
+ * kda_decode_window — a run of decode tokens per sequence in one pass over the state.
+ *
+ * Speculative decoding verifies a window of drafted tokens and must then move each state to
+ * the last accepted token.  The state after any accepted prefix follows from the drafted
+ * tokens' projected inputs, which are far smaller than the state, so only those are cached:
+ * the accepted tokens are replayed on-chip together with the bonus token and the next draft
+ * window in one recurrent loop, and the state is written back once
+ * ("k3_training_and_infra_notes", section 4.5, KDA decoding).  For every (sequence, head):
+ * starting from `state`, the tokens of sequence n (rows cu_seqlens[n] .. cu_seqlens[n+1] - 1)
+ * run through the recurrence of kda_decode_step one after another; each token's output is
+ * computed from the state after the tokens before it; the state after the first commit[n]
+ * tokens is written back.
+ *
+ *   desc          num_seqs = N; host_seqlens required: per-sequence run lengths, 0 .. 64
+ *   q, k, log_alpha, v  device [T, H, 128];  beta: [T, H]  (T = total_tokens, desc->in_dtype)
+ *   cu_seqlens    device int32 [N + 1], differences = host_seqlens
+ *   state         device fp32 [N, H, 128, 128]; overwritten with the state after the first
+ *                 commit[n] tokens of run n, left untouched when that count is 0
+ *   out           device [T, H, 128] of desc->in_dtype, or NULL to skip the outputs
+ *   commit        device int32 [N] (each clamped to 0 .. run length), or NULL to commit every
+ *                 token
+ * A run of one token with commit 1 gives the bits of kda_decode_step.
+ */
+kda_status kda_decode_window(const kda_desc* desc, const void* q, const void* k, const void* v,
+                             const void* log_alpha, const void* beta, const int32_t* cu_seqlens,
+                             float* state, void* out, const int32_t* commit, kda_stream_t stream);
+
+/*
  * kda_read_device_status — synchronise `stream`, then return and clear the sticky device
  * status word of the current device (KDA_OK when no kernel reported a problem).
  */

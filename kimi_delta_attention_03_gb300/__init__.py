@@ -9,6 +9,7 @@ from . import binding  # noqa: F401
 from .binding import (  # noqa: F401
     KdaError,
     decode_step,
+    decode_window,
     fwd_checkpoint_count,
     fwd_chunked,
     fwd_chunked_checkpoints,
@@ -22,7 +23,7 @@ from .binding import (  # noqa: F401
 )
 
 __all__ = [
-    "KdaError", "decode_step", "fwd_checkpoint_count", "fwd_chunked", "fwd_chunked_checkpoints",
+    "KdaError", "decode_step", "decode_window", "fwd_checkpoint_count", "fwd_chunked", "fwd_chunked_checkpoints",
     "fwd_chunked_host", "fwd_workspace_bytes",
     "launch_count",
     "library_path", "load_library", "read_device_status",

@@ -58,6 +58,8 @@ SIGNATURES = {
     "kda_fwd_chunked_ckpt": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P,
                                             _P, _P, ctypes.c_int32, _P, _P, ctypes.c_size_t, _P]),
     "kda_decode_step": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kda_decode_window": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P,
+                                         _P, _P]),
     "kda_read_device_status": (ctypes.c_int, [_P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kda_launch_count": (ctypes.c_uint64, []),
@@ -368,6 +370,41 @@ def decode_step(q, k, v, log_alpha, beta, state, out=None, stream=None):
                              _ptr(beta), _ptr(state), _ptr(out), _stream_handle(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_step")
+    return out
+
+
+def decode_window(q, k, v, log_alpha, beta, cu_seqlens, seqlens, state, commit=None, out=None,
+                  want_out: bool = True, stream=None):
+    """A run of decode tokens per sequence in one pass over the state (speculative decoding:
+    replayed accepted tokens, the bonus token and the next draft window).  q, k, log_alpha, v:
+    [T, H, 128]; beta: [T, H]; cu_seqlens: int32 [N+1] on the device, seqlens the same run
+    lengths (0..64) on the host; state [N, H, 128, 128] fp32.  Every token's output is
+    returned; the state after the first commit[n] tokens of run n is written back into
+    ``state`` (commit: int32 [N] on the device, or None to commit every token)."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("decode_window needs CUDA tensors")
+    T, H, d = q.shape
+    N = len(seqlens)
+    dt = q.dtype
+    for name, t, shp in (("k", k, (T, H, d)), ("v", v, (T, H, d)),
+                         ("log_alpha", log_alpha, (T, H, d)), ("beta", beta, (T, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    _check_io("state", state, (N, H, d, d), torch.float32, dev)
+    if commit is not None:
+        _check_io("commit", commit, (N,), torch.int32, dev)
+    if out is None and want_out:
+        out = torch.empty((T, H, d), dtype=dt, device=dev)
+    if out is not None:
+        _check_io("out", out, (T, H, d), dt, dev)
+    desc = make_desc(seqlens, H, dt, d)
+    st = lib.kda_decode_window(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                               _ptr(beta), _ptr(cu_seqlens), _ptr(state), _ptr(out), _ptr(commit),
+                               _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_window")
     return out
 
 

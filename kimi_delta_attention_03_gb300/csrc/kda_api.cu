@@ -205,6 +205,28 @@ kda_status kda_decode_step(const kda_desc* desc, const void* q, const void* k, c
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status kda_decode_window(const kda_desc* desc, const void* q, const void* k, const void* v,
+                             const void* log_alpha, const void* beta, const int32_t* cu_seqlens,
+                             float* state, void* out, const int32_t* commit, kda_stream_t stream) {
+    kda_status st = check_desc(desc, true);
+    if (st != KDA_OK) return st;
+    for (int32_t n = 0; n < desc->num_seqs; ++n)
+        if (desc->host_seqlens[n] > 64) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !state) return KDA_ERR_INVALID_ARG;
+    if (desc->total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta)) return KDA_ERR_INVALID_ARG;
+    if (out && (out == q || out == k || out == v || out == log_alpha || out == beta ||
+                out == (const void*)state))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state)) return KDA_ERR_INVALID_ARG;
+    int* status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    cudaError_t e = kda::launch_decode_window(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k,
+                                              v, log_alpha, beta, cu_seqlens, state, out, commit,
+                                              (cudaStream_t)stream);
+    g_launches += 1;
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status kda_read_device_status(kda_stream_t stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KDA_ERR_CUDA;
     int* p = status_word();

@@ -63,6 +63,11 @@ cudaError_t launch_decode(int dtype, int64_t units, int heads, const void* q, co
                           const void* v, const void* g, const void* beta, float* state,
                           void* out, int* status, cudaStream_t stream);
 
+cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void* q,
+                                 const void* k, const void* v, const void* g, const void* beta,
+                                 const int32_t* cu_seqlens, float* state, void* out,
+                                 const int32_t* commit, cudaStream_t stream);
+
 cudaError_t launch_prefill(int dtype, int num_seqs, int heads, const void* q, const void* k,
                            const void* v, const void* g, const void* beta,
                            const float* init_state, const int32_t* cu_seqlens, void* out,

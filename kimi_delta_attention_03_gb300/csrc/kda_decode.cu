@@ -102,7 +102,128 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     }
 }
 
+// A run of tokens per (sequence, head) in one pass over the state: the replayed accepted
+// tokens, the bonus token and the next draft window of speculative decoding share one
+// recurrent loop, the state read once and written once ("k3_training_and_infra_notes",
+// section 4.5, KDA decoding: cache the draft tokens' projected inputs, rebuild the accepted
+// states on-chip, write back once).  Sequence n's tokens are rows cu[n] .. cu[n+1] - 1 of the
+// inputs (layout [T, H, 128], as the prefill's); every token's output is written (when out is
+// given) from the state after the run's earlier tokens; the state after the first commit[n]
+// tokens is written back (nothing when commit[n] = 0; all of them when commit is null).  Per
+// token the arithmetic is the single-token step's, in the same order.
+template <typename TIn>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
+                         const TIn* __restrict__ v, const TIn* __restrict__ g,
+                         const TIn* __restrict__ beta, const int32_t* __restrict__ cu_seqlens,
+                         float* __restrict__ state, TIn* __restrict__ out,
+                         const int32_t* __restrict__ commit, int64_t units, int H) {
+    __shared__ float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_u[kDim];
+    __shared__ __align__(16) float s_rx[8][kDim];
+    __shared__ __align__(16) float s_ry[8][kDim];
+    __shared__ float s_kq;
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+
+    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const int64_t n = unit / H;
+        const int h = (int)(unit - n * H);
+        const int64_t t0 = cu_seqlens[n];
+        const int len = (int)(cu_seqlens[n + 1] - t0);
+        const int ncommit = commit ? min(max(commit[n], 0), len) : len;
+        if (len <= 0) continue;
+        float* S = state + unit * (int64_t)(kDim * kDim);
+        float4 s[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
+
+#pragma unroll 1
+        for (int t = 0; t < len; ++t) {
+            const int64_t row = (t0 + t) * H + h;
+            if (tid < kDim) {
+                const int64_t e = row * kDim + tid;
+                s_k[tid] = io<TIn>::to_f(k[e]);
+                s_q[tid] = io<TIn>::to_f(q[e]);
+                s_a[tid] = expf(io<TIn>::to_f(g[e]));
+                s_v[tid] = io<TIn>::to_f(v[e]);
+            }
+            const float b = io<TIn>::to_f(beta[row]);
+            __syncthreads();
+
+            float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+            float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const int i = warp + 8 * r;
+                const float a = s_a[i], kk = s_k[i], qq = s_q[i];
+                s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
+                x0 = fmaf(kk, s[r].x, x0); x1 = fmaf(kk, s[r].y, x1);
+                x2 = fmaf(kk, s[r].z, x2); x3 = fmaf(kk, s[r].w, x3);
+                y0 = fmaf(qq, s[r].x, y0); y1 = fmaf(qq, s[r].y, y1);
+                y2 = fmaf(qq, s[r].z, y2); y3 = fmaf(qq, s[r].w, y3);
+            }
+            reinterpret_cast<float4*>(s_rx[warp])[lane] = make_float4(x0, x1, x2, x3);
+            reinterpret_cast<float4*>(s_ry[warp])[lane] = make_float4(y0, y1, y2, y3);
+            if (warp == 0) {
+                float p = 0.f;
+#pragma unroll
+                for (int m = 0; m < kDim / 32; ++m)
+                    p = fmaf(s_k[lane + 32 * m], s_q[lane + 32 * m], p);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+                if (lane == 0) s_kq = p;
+            }
+            __syncthreads();
+
+            if (tid < kDim) {
+                float x = 0.f, y = 0.f;
+#pragma unroll
+                for (int w8 = 0; w8 < 8; ++w8) { x += s_rx[w8][tid]; y += s_ry[w8][tid]; }
+                const float u = b * (s_v[tid] - x);
+                s_u[tid] = u;
+                if (out) out[row * kDim + tid] = io<TIn>::from_f(fmaf(s_kq, u, y));
+            }
+            __syncthreads();
+
+            const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
+            const bool store = (t + 1 == ncommit);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const float kk = s_k[warp + 8 * r];
+                s[r].x = fmaf(kk, u4.x, s[r].x); s[r].y = fmaf(kk, u4.y, s[r].y);
+                s[r].z = fmaf(kk, u4.z, s[r].z); s[r].w = fmaf(kk, u4.w, s[r].w);
+                if (store) __stcs(reinterpret_cast<float4*>(S + (warp + 8 * r) * kDim) + lane, s[r]);
+            }
+            __syncthreads();  // shared vectors are rewritten by the next token
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void* q,
+                                 const void* k, const void* v, const void* g, const void* beta,
+                                 const int32_t* cu_seqlens, float* state, void* out,
+                                 const int32_t* commit, cudaStream_t stream) {
+    const int64_t units = (int64_t)num_seqs * heads;
+    if (units <= 0) return cudaSuccess;
+    const int64_t max_grid = 1LL << 30;
+    const unsigned grid = (unsigned)(units < max_grid ? units : max_grid);
+    if (dtype == KDA_BF16) {
+        using T = __nv_bfloat16;
+        kda_decode_window_kernel<T><<<grid, kDecodeThreads, 0, stream>>>(
+            (const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta, cu_seqlens, state,
+            (T*)out, commit, units, heads);
+    } else {
+        kda_decode_window_kernel<float><<<grid, kDecodeThreads, 0, stream>>>(
+            (const float*)q, (const float*)k, (const float*)v, (const float*)g,
+            (const float*)beta, cu_seqlens, state, (float*)out, commit, units, heads);
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode(int dtype, int64_t units, int heads, const void* q, const void* k,
                           const void* v, const void* g, const void* beta, float* state,

@@ -69,3 +69,86 @@ def test_decode_512x96_full_size_sampled():
     after = d["state"][n_idx.to(DEV), h_idx.to(DEV)].cpu()[:, None]
     assert_close("state", after.numpy(), s_ref)
     assert kda().read_device_status() == 0
+
+
+# ------------------------------ decode windows (speculative decoding) -------------------------
+def _window_inputs(lens, H, seed):
+    x = synth.make_inputs(lens, H, torch.bfloat16, seed=seed, device=DEV)
+    x["init_state"] = x["init_state"] * 2.0  # N(0, 0.02^2), as the decode workload
+    return x
+
+
+def test_decode_window_outputs_and_committed_states_match_oracle():
+    """Every token's output equals the token loop's; the state written back is the token loop's
+    state after the first commit[n] tokens of each run, and is left untouched for commit 0."""
+    lens = [5, 1, 0, 8, 64, 3, 17]
+    commit = [5, 0, 0, 3, 64, 2, 40]  # 40 is clamped to the run length 17
+    H = 3
+    x = _window_inputs(lens, H, seed=31)
+    state = x["init_state"].clone()
+    out = kda().decode_window(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                              x["seqlens"], state,
+                              commit=torch.tensor(commit, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    o_ref, _ = oracle.recurrence(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), x["log_alpha"].cpu(),
+                                 x["beta"].cpu(), x["cu_seqlens"].cpu(),
+                                 state_in=x["init_state"].cpu(), want_state=False,
+                                 threads=oracle_threads())
+    assert_close("out", out.float().cpu().numpy(), o_ref)
+    # committed states: the oracle's final states of the committed prefixes
+    cu = x["cu_seqlens"].cpu().tolist()
+    c = [min(cm, L) for cm, L in zip(commit, lens)]
+    rows = [torch.arange(cu[n], cu[n] + c[n]) for n in range(len(lens))]
+    pick = lambda t: torch.cat([t.cpu()[r] for r in rows])
+    cu2 = np.concatenate([[0], np.cumsum(c)]).astype(np.int32)
+    _, s_ref = oracle.recurrence(pick(x["q"]), pick(x["k"]), pick(x["v"]), pick(x["log_alpha"]),
+                                 pick(x["beta"]), cu2, state_in=x["init_state"].cpu(),
+                                 want_out=False, threads=oracle_threads())
+    assert_close("state", state.cpu().numpy(), s_ref)
+    for n in range(len(lens)):
+        if c[n] == 0:
+            assert torch.equal(state[n], x["init_state"][n])
+
+
+def test_decode_window_of_single_tokens_equals_decode_step():
+    N, H = 9, 4
+    d = synth.make_decode_inputs(N, H, torch.bfloat16, seed=32, device=DEV)
+    s1 = d["state"].clone()
+    s2 = d["state"].clone()
+    o1 = kda().decode_step(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], s1)
+    cu = torch.arange(N + 1, dtype=torch.int32, device=DEV)
+    o2 = kda().decode_window(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], cu, [1] * N, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+def test_decode_window_verify_then_commit():
+    """Verify a draft window without touching the state, then replay the accepted prefix and
+    commit it: the outputs do not depend on the commit counts, and the committed state is the
+    one a full run would have left after those tokens."""
+    lens = [6, 6, 6, 6]
+    accepted = [0, 2, 5, 6]
+    H = 2
+    x = _window_inputs(lens, H, seed=33)
+    state = x["init_state"].clone()
+    zeros = torch.zeros(len(lens), dtype=torch.int32, device=DEV)
+    o_verify = kda().decode_window(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                   x["cu_seqlens"], x["seqlens"], state, commit=zeros)
+    torch.cuda.synchronize()
+    assert torch.equal(state, x["init_state"])
+    o_commit = kda().decode_window(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                   x["cu_seqlens"], x["seqlens"], state,
+                                   commit=torch.tensor(accepted, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(o_verify, o_commit)
+    # a full commit of the same runs passes through the accepted states on the way
+    for n, a in enumerate(accepted):
+        if a == 0:
+            assert torch.equal(state[n], x["init_state"][n])
+    ref = x["init_state"].clone()
+    kda().decode_window(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                        x["seqlens"], ref, commit=torch.tensor([6] * 4, dtype=torch.int32,
+                                                               device=DEV), want_out=False)
+    torch.cuda.synchronize()
+    assert torch.equal(state[3], ref[3])  # accepted the whole window
