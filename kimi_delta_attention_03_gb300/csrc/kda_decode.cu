@@ -140,17 +140,28 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         for (int r = 0; r < 16; ++r)
             s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
 
+        // the next token's inputs are fetched into registers while this token is computed
+        TIn nk{}, nq{}, ng{}, nv{}, nb{};
+        auto fetch = [&](int t) {
+            const int64_t row = (t0 + t) * H + h;
+            if (tid < kDim) {
+                const int64_t e = row * kDim + tid;
+                nk = k[e]; nq = q[e]; ng = g[e]; nv = v[e];
+            }
+            nb = beta[row];
+        };
+        fetch(0);
 #pragma unroll 1
         for (int t = 0; t < len; ++t) {
             const int64_t row = (t0 + t) * H + h;
             if (tid < kDim) {
-                const int64_t e = row * kDim + tid;
-                s_k[tid] = io<TIn>::to_f(k[e]);
-                s_q[tid] = io<TIn>::to_f(q[e]);
-                s_a[tid] = expf(io<TIn>::to_f(g[e]));
-                s_v[tid] = io<TIn>::to_f(v[e]);
+                s_k[tid] = io<TIn>::to_f(nk);
+                s_q[tid] = io<TIn>::to_f(nq);
+                s_a[tid] = expf(io<TIn>::to_f(ng));
+                s_v[tid] = io<TIn>::to_f(nv);
             }
-            const float b = io<TIn>::to_f(beta[row]);
+            const float b = io<TIn>::to_f(nb);
+            if (t + 1 < len) fetch(t + 1);
             __syncthreads();
 
             float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
