@@ -210,10 +210,6 @@ __device__ __forceinline__ void block_product(float (&acc)[2][4], const float* X
     for (int nt = 0; nt < 2; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     block_mma(acc, X, ldx, xs, n2, n3, Yb, ldy, lane);
 }
-__device__ __forceinline__ void block_product_acc(float (&acc)[2][4], const float* X, int ldx,
-                                                  const float* Yb, int ldy, int lane) {
-    block_mma(acc, X, ldx, 1.f, nullptr, nullptr, Yb, ldy, lane);
-}
 __device__ __forceinline__ void store_block(float* D, int ld, const float (&acc)[2][4], int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
