@@ -133,7 +133,6 @@ __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-__device__ __forceinline__ float bf2f(bf16 x) { return __bfloat162float(x); }
 
 __device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -668,7 +667,6 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         auto factor = [&](const int c) -> bool {
             const int s = c & 1;
             const int valid = min(kChunk, L - kChunk * c);
-            const int64_t tok0 = seq0 + (int64_t)kChunk * c;
             unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
             unsigned char* kmh = sm + kmh_off(c);
             if (!wait_bar(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
