@@ -113,6 +113,27 @@ def test_host_argument_checks(lib):
                                P(0x2000), None) == -1
 
 
+def test_checkpoint_and_window_argument_checks(lib):
+    # refused on the host before any device pointer is touched
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    ck = lambda d, every, states=P(0x4000): lib.kda_fwd_chunked_ckpt(
+        ctypes.byref(d), fake, fake, fake, fake, fake, None, fake, P(0x2000), None, every,
+        states, None, 0, None)
+    assert ck(_desc([512, 100]), 0) == -1                       # no interval
+    assert ck(_desc([512, 100]), 100) == -1                     # not a multiple of 64
+    assert ck(_desc([512, 100], dtype=torch.float32), 256) == -2  # bf16 only
+    assert ck(_desc([512, 100]), 256, states=None) == -1        # checkpoints but no buffer
+    assert ck(_desc([512, 100]), 256, states=fake) == -1        # buffer aliases an input
+    win = lambda d, state=P(0x3000): lib.kda_decode_window(
+        ctypes.byref(d), fake, fake, fake, fake, fake, fake, state, P(0x2000), None, None)
+    assert win(_desc([4, 65])) == -1                            # runs of at most 64 tokens
+    assert win(_desc([4, 5]), state=None) == -1                 # no state
+    d = _desc([4, 5])
+    d.host_seqlens = None
+    assert win(d) == -1                                         # run lengths are required
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import kimi_delta_attention_03_gb300 as kda
     x = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
