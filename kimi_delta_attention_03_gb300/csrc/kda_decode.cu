@@ -140,6 +140,30 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         for (int r = 0; r < 16; ++r)
             s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
 
+        // The grid is persistent: the state and the token rows of this CTA's next unit are
+        // pulled into L2 while this unit's tokens run, so its loads find them there.
+        const int64_t nu = unit + gridDim.x;
+        if (nu < units) {
+            if (tid < 4) {
+                const float* nxt = state + nu * (int64_t)(kDim * kDim) + tid * 4096;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], 16384;" ::"l"(nxt) : "memory");
+            }
+            constexpr int kLine = 128 / (int)sizeof(TIn);  // elements per 128-byte line
+            constexpr int kLines = kDim / kLine;
+            const int64_t nn = nu / H;
+            const int nh = (int)(nu - nn * H);
+            const int64_t nt0 = cu_seqlens[nn];
+            const int nlen = (int)(cu_seqlens[nn + 1] - nt0);
+            for (int i = tid; i < nlen * 4 * kLines; i += kDecodeThreads) {
+                const int tok = i / (4 * kLines), rem = i - tok * 4 * kLines;
+                const int which = rem / kLines, line = rem - which * kLines;
+                const TIn* src = which == 0 ? k : which == 1 ? q : which == 2 ? g : v;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                    src + ((nt0 + tok) * H + nh) * kDim + line * kLine));
+            }
+            if (tid < nlen) asm volatile("prefetch.global.L2 [%0];" ::"l"(beta + (nt0 + tid) * H + nh));
+        }
+
         // the next token's inputs are fetched into registers while this token is computed
         TIn nk{}, nq{}, ng{}, nv{}, nb{};
         auto fetch = [&](int t) {
@@ -221,8 +245,19 @@ cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void*
                                  const int32_t* commit, cudaStream_t stream) {
     const int64_t units = (int64_t)num_seqs * heads;
     if (units <= 0) return cudaSuccess;
-    const int64_t max_grid = 1LL << 30;
-    const unsigned grid = (unsigned)(units < max_grid ? units : max_grid);
+    // persistent grid: one CTA per resident slot, each taking units in strides of the grid
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess)
+        err = dtype == KDA_BF16
+                  ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                        &per_sm, kda_decode_window_kernel<__nv_bfloat16>, kDecodeThreads, 0)
+                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                        &per_sm, kda_decode_window_kernel<float>, kDecodeThreads, 0);
+    if (err != cudaSuccess) return err;
+    const int64_t slots = (int64_t)(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+    const unsigned grid = (unsigned)(units < slots ? units : slots);
     if (dtype == KDA_BF16) {
         using T = __nv_bfloat16;
         kda_decode_window_kernel<T><<<grid, kDecodeThreads, 0, stream>>>(
