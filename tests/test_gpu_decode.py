@@ -152,3 +152,42 @@ def test_decode_window_verify_then_commit():
                                                                device=DEV), want_out=False)
     torch.cuda.synchronize()
     assert torch.equal(state[3], ref[3])  # accepted the whole window
+
+
+def test_decode_window_many_units_equals_token_steps():
+    """More (sequence, head) units than the window kernel's persistent grid has CTAs, so each
+    CTA takes several units and prefetches the next one's state and token rows while it works.
+    Outputs and committed states are bit for bit those of single-token steps taken token by
+    token (the window repeats the step's arithmetic in the same order; the step itself is
+    checked against the oracle above)."""
+    rng = np.random.default_rng(34)
+    N, H = 300, 4
+    lens = rng.integers(0, 65, N).tolist()
+    lens[0], lens[1], lens[2] = 64, 0, 1
+    commit = [int(rng.integers(0, L + 1)) for L in lens]
+    x = _window_inputs(lens, H, seed=34)
+    state = x["init_state"].clone()
+    out = kda().decode_window(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                              lens, state,
+                              commit=torch.tensor(commit, dtype=torch.int32, device=DEV))
+    cu = x["cu_seqlens"].cpu().tolist()
+    work = x["init_state"].clone()
+    committed = x["init_state"].clone()
+    ref_out = torch.zeros_like(out)
+    for j in range(max(lens)):
+        act = [n for n in range(N) if lens[n] > j]
+        rows = torch.tensor([cu[n] + j for n in act], device=DEV)
+        ia = torch.tensor(act, device=DEV)
+        s = work[ia].contiguous()
+        sel = {key: x[key][rows].contiguous() for key in ("q", "k", "v", "log_alpha", "beta")}
+        ref_out[rows] = kda().decode_step(sel["q"], sel["k"], sel["v"], sel["log_alpha"],
+                                          sel["beta"], s)
+        work[ia] = s
+        done = [n for n in act if commit[n] == j + 1]
+        if done:
+            idx = torch.tensor(done, device=DEV)
+            committed[idx] = work[idx]
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    assert torch.equal(out, ref_out)
+    assert torch.equal(state, committed)
