@@ -9,7 +9,11 @@ the token loop forget / erase-and-write / read of flash-linear-attention's ``nai
 shown on "How Kimi K3 Engineered Its Way to the Frontier", section "How KDA updates its
 state".  This module only builds the shared object with gcc and marshals arrays to it.
 
-Every function here is pinned by ``tests/test_oracle_pins.py``; there is no unpinned entry.
+The input prologue (raw projections -> q, k, v, g, beta) is plain numpy fp64 in
+``input_prologue.py``, exported here as ``prologue``.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_prologue.py``; there is no unpinned entry.
 """
 from __future__ import annotations
 
@@ -19,6 +23,8 @@ import subprocess
 import threading
 
 import numpy as np
+
+from .input_prologue import prologue  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_oracle.c")
