@@ -232,6 +232,66 @@ kda_status kda_decode_window(const kda_desc* desc, const void* q, const void* k,
                              float* state, void* out, const int32_t* commit, kda_stream_t stream);
 
 /*
+ * Input prologue: the recurrence's inputs from a layer's raw per-token projections.
+ *
+ * Queries and keys of a KDA layer pass through Swish and are then L2-normalised over their
+ * 128 channels; values pass through Swish ("Kimi K3" (ai.thesatyajit.com), section "Kimi Delta
+ * Attention: constant-size memory over a million tokens").  The decay is K3's gate with a lower
+ * bound, log_alpha = lower_bound * sigmoid(exp(A_log[h]) * (g_raw + dt_bias[h, :])), which keeps
+ * every log_alpha inside (lower_bound, 0) ("How Kimi K3 Engineered Its Way to the Frontier",
+ * section "How KDA updates its state").  beta arrives as logits and passes through a sigmoid
+ * (FlashKDA's forward, section "FlashKDA: the equation, shipped as a kernel").  Readings where
+ * the sources are silent: the L2 norm divides by sqrt(sum of squares + 1e-6); q is multiplied
+ * by q_scale after its norm.  The short convolution that precedes Swish in the layer is the
+ * caller's: the raw q, k, v here are its outputs.
+ *
+ * Arithmetic (fp32, every result rounded to bf16 where an unfused pipeline would store it):
+ *   sigmoid(x) = 1 / (1 + 2^(-x log2 e)) with the hardware exp2 and reciprocal approximations
+ *   (about 1e-6 relative error); Swish(x) = x sigmoid(x); the row norm sums the squares of eight
+ *   consecutive channels in order and then adds the sixteen partial sums pairwise (strides 1,
+ *   2, 4, 8).
+ */
+typedef struct {
+  const float* A_log;    /* device fp32 [H]: per-head log decay rate */
+  const float* dt_bias;  /* device fp32 [H, 128], or NULL for none */
+  float lower_bound;     /* in [-80, 0): most negative log_alpha (K3 uses -5) */
+  float q_scale;         /* finite, > 0: factor on the normalised q (1/sqrt(128) is usual) */
+} kda_prologue_params;
+
+/*
+ * kda_prologue — the prologue alone, as an elementwise pass over HBM (for decode steps and
+ * windows, or any caller that wants the transformed inputs).
+ *
+ *   desc          total_tokens rows, num_heads heads; in_dtype must be KDA_BF16;
+ *                 host_seqlens unused (may be NULL)
+ *   q_raw, k_raw, v_raw, g_raw   device bf16 [T, H, 128]
+ *   beta_logit    device bf16 [T, H]
+ *   q, k, v, log_alpha           device bf16 [T, H, 128] outputs
+ *   beta          device bf16 [T, H] output
+ * Outputs must not alias inputs or each other.  Returns KDA_ERR_UNSUPPORTED for fp32 inputs.
+ */
+kda_status kda_prologue(const kda_desc* desc, const kda_prologue_params* prm, const void* q_raw,
+                        const void* k_raw, const void* v_raw, const void* g_raw,
+                        const void* beta_logit, void* q, void* k, void* v, void* log_alpha,
+                        void* beta, kda_stream_t stream);
+
+/*
+ * kda_fwd_chunked_prologue — kda_fwd_chunked on raw projections, with the prologue fused into
+ * the prefill's load path: the transformed q, k, v, log_alpha and beta never go to HBM.
+ *
+ * Arguments as kda_fwd_chunked, with q_raw, k_raw, v_raw, g_raw and beta_logit (layouts as q, k,
+ * v, log_alpha and beta) in place of the transformed inputs and `prm` as for kda_prologue.
+ * Outputs and final states are bit-identical to kda_prologue followed by kda_fwd_chunked.
+ * bf16 inputs only (KDA_ERR_UNSUPPORTED for fp32 inputs).
+ */
+kda_status kda_fwd_chunked_prologue(const kda_desc* desc, const kda_prologue_params* prm,
+                                    const void* q_raw, const void* k_raw, const void* v_raw,
+                                    const void* g_raw, const void* beta_logit,
+                                    const float* init_state, const int32_t* cu_seqlens, void* out,
+                                    float* final_state, void* workspace, size_t workspace_bytes,
+                                    kda_stream_t stream);
+
+/*
  * kda_read_device_status — synchronise `stream`, then return and clear the sticky device
  * status word of the current device (KDA_OK when no kernel reported a problem).
  */

@@ -14,17 +14,19 @@ from .binding import (  # noqa: F401
     fwd_chunked,
     fwd_chunked_checkpoints,
     fwd_chunked_host,
+    fwd_chunked_prologue,
     fwd_plan,
     fwd_workspace_bytes,
     launch_count,
     library_path,
     load_library,
+    prologue,
     read_device_status,
 )
 
 __all__ = [
     "KdaError", "decode_step", "decode_window", "fwd_checkpoint_count", "fwd_chunked", "fwd_chunked_checkpoints",
-    "fwd_chunked_host", "fwd_workspace_bytes",
+    "fwd_chunked_host", "fwd_chunked_prologue", "fwd_workspace_bytes", "prologue",
     "launch_count",
     "library_path", "load_library", "read_device_status",
 ]

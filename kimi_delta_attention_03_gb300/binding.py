@@ -45,6 +45,11 @@ class KdaPlanInfo(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t)]
 
 
+class KdaPrologueParams(ctypes.Structure):
+    _fields_ = [("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("lower_bound", ctypes.c_float), ("q_scale", ctypes.c_float)]
+
+
 # exported symbol -> (restype, argtypes)
 _P = ctypes.c_void_p
 SIGNATURES = {
@@ -57,6 +62,11 @@ SIGNATURES = {
     "kda_fwd_checkpoint_count": (ctypes.c_int64, [ctypes.POINTER(KdaDesc), ctypes.c_int32]),
     "kda_fwd_chunked_ckpt": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P,
                                             _P, _P, ctypes.c_int32, _P, _P, ctypes.c_size_t, _P]),
+    "kda_prologue": (ctypes.c_int, [ctypes.POINTER(KdaDesc), ctypes.POINTER(KdaPrologueParams),
+                                    _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kda_fwd_chunked_prologue": (ctypes.c_int, [ctypes.POINTER(KdaDesc),
+                                                ctypes.POINTER(KdaPrologueParams), _P, _P, _P,
+                                                _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "kda_decode_step": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P]),
     "kda_decode_window": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P,
                                          _P, _P]),
@@ -163,6 +173,83 @@ def fwd_chunked(q, k, v, log_alpha, beta, cu_seqlens, seqlens, init_state=None, 
                              _stream_handle(stream, dev))
     if st != KDA_OK:
         raise KdaError(st, "kda_fwd_chunked")
+    return out, final_state
+
+
+def _prologue_params(A_log, dt_bias, lower_bound, q_scale, H, d, dev):
+    _check_io("A_log", A_log, (H,), torch.float32, dev)
+    if dt_bias is not None:
+        _check_io("dt_bias", dt_bias, (H, d), torch.float32, dev)
+    return KdaPrologueParams(A_log.data_ptr(), None if dt_bias is None else dt_bias.data_ptr(),
+                             float(lower_bound), float(q_scale))
+
+
+def prologue(q_raw, k_raw, v_raw, g_raw, beta_logit, A_log, dt_bias=None,
+             lower_bound: float = -5.0, q_scale: float = 128 ** -0.5, stream=None):
+    """The input prologue alone: raw bf16 projections q_raw, k_raw, g_raw, v_raw [T, H, 128] and
+    beta_logit [T, H] -> (q, k, v, log_alpha, beta), bf16.  A_log: fp32 [H]; dt_bias: fp32
+    [H, 128] or None."""
+    lib = load_library()
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise ValueError("prologue needs CUDA tensors")
+    T, H, d = q_raw.shape
+    dt = q_raw.dtype
+    for name, t, shp in (("k_raw", k_raw, (T, H, d)), ("v_raw", v_raw, (T, H, d)),
+                         ("g_raw", g_raw, (T, H, d)), ("beta_logit", beta_logit, (T, H))):
+        _check_io(name, t, shp, dt, dev)
+    prm = _prologue_params(A_log, dt_bias, lower_bound, q_scale, H, d, dev)
+    outs = [torch.empty((T, H, d), dtype=dt, device=dev) for _ in range(4)]
+    beta = torch.empty((T, H), dtype=dt, device=dev)
+    desc = make_desc([T], H, dt, d)
+    st = lib.kda_prologue(ctypes.byref(desc), ctypes.byref(prm), _ptr(q_raw), _ptr(k_raw),
+                          _ptr(v_raw), _ptr(g_raw), _ptr(beta_logit), _ptr(outs[0]),
+                          _ptr(outs[1]), _ptr(outs[2]), _ptr(outs[3]), _ptr(beta),
+                          _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prologue")
+    return outs[0], outs[1], outs[2], outs[3], beta
+
+
+def fwd_chunked_prologue(q_raw, k_raw, v_raw, g_raw, beta_logit, cu_seqlens, seqlens, A_log,
+                         dt_bias=None, lower_bound: float = -5.0, q_scale: float = 128 ** -0.5,
+                         init_state=None, out=None, final_state=None,
+                         want_final_state: bool = True, workspace=None, stream=None):
+    """Chunked KDA prefill on raw projections, the prologue fused into the kernel (arguments
+    as ``prologue`` and ``fwd_chunked``).  Returns (out, final_state)."""
+    lib = load_library()
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise ValueError("fwd_chunked_prologue needs CUDA tensors")
+    T, H, d = q_raw.shape
+    N = len(seqlens)
+    dt = q_raw.dtype
+    for name, t, shp in (("k_raw", k_raw, (T, H, d)), ("v_raw", v_raw, (T, H, d)),
+                         ("g_raw", g_raw, (T, H, d)), ("beta_logit", beta_logit, (T, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    prm = _prologue_params(A_log, dt_bias, lower_bound, q_scale, H, d, dev)
+    if init_state is not None:
+        _check_io("init_state", init_state, (N, H, d, d), torch.float32, dev)
+    if out is None:
+        out = torch.empty((T, H, d), dtype=dt, device=dev)
+    _check_io("out", out, (T, H, d), dt, dev)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    if final_state is not None:
+        _check_io("final_state", final_state, (N, H, d, d), torch.float32, dev)
+    desc = make_desc(seqlens, H, dt, d)
+    need = int(lib.kda_fwd_workspace_bytes(ctypes.byref(desc)))
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.kda_fwd_chunked_prologue(ctypes.byref(desc), ctypes.byref(prm), _ptr(q_raw),
+                                      _ptr(k_raw), _ptr(v_raw), _ptr(g_raw), _ptr(beta_logit),
+                                      _ptr(init_state), _ptr(cu_seqlens), _ptr(out),
+                                      _ptr(final_state), _ptr(workspace), ws_bytes,
+                                      _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fwd_chunked_prologue")
     return out, final_state
 
 

@@ -2,6 +2,7 @@
 // sticky device status word, and the kernel launches.  No allocation happens here.
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "kda_common.cuh"
@@ -52,6 +53,16 @@ kda_status check_desc(const kda_desc* d, bool need_lengths) {
     return KDA_OK;
 }
 
+// The prologue's parameters: a per-head rate, an optional 16-byte aligned bias, a finite lower
+// bound in [-80, 0) (so one token's decay stays inside the prefill's exponent range) and a
+// finite positive q scale.
+bool check_prologue(const kda_prologue_params* prm) {
+    if (!prm || !prm->A_log || !aligned16(prm->dt_bias)) return false;
+    if (!std::isfinite(prm->lower_bound) || prm->lower_bound >= 0.f || prm->lower_bound < -80.f)
+        return false;
+    return std::isfinite(prm->q_scale) && prm->q_scale > 0.f;
+}
+
 }  // namespace
 
 extern "C" {
@@ -96,10 +107,17 @@ kda_status fwd_chunked_impl(const kda_desc* desc, const void* q, const void* k, 
                             const void* log_alpha, const void* beta, const float* init_state,
                             const int32_t* cu_seqlens, void* out, float* final_state,
                             int32_t ckpt_every, float* ckpt_states, void* workspace,
-                            size_t workspace_bytes, kda_stream_t stream) {
+                            size_t workspace_bytes, kda_stream_t stream,
+                            const kda_prologue_params* pro = nullptr) {
     kda_plan_info plan;
     kda_status st = kda_fwd_plan(desc, &plan);
     if (st != KDA_OK) return st;
+    kda::ProParams pp = {};
+    if (pro) {
+        if (desc->in_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+        if (!check_prologue(pro)) return KDA_ERR_INVALID_ARG;
+        pp = {pro->A_log, pro->dt_bias, pro->lower_bound, pro->q_scale};
+    }
     if (!cu_seqlens) return KDA_ERR_INVALID_ARG;
     if (desc->total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !out))
         return KDA_ERR_INVALID_ARG;
@@ -140,7 +158,7 @@ kda_status fwd_chunked_impl(const kda_desc* desc, const void* q, const void* k, 
                                    log_alpha, beta, init_state, cu_seqlens, out, final_state, ws,
                                    status, (cudaStream_t)stream, &launches,
                                    desc->host_seqlens, ckpts > 0 ? ckpt_states : nullptr,
-                                   ckpts > 0 ? ckpt_every / kda::kChunk : 0);
+                                   ckpts > 0 ? ckpt_every / kda::kChunk : 0, pro ? &pp : nullptr);
     else
         e = kda::launch_prefill(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v,
                                 log_alpha, beta, init_state, cu_seqlens, out, final_state,
@@ -178,6 +196,42 @@ kda_status kda_fwd_chunked_ckpt(const kda_desc* desc, const void* q, const void*
     return fwd_chunked_impl(desc, q, k, v, log_alpha, beta, init_state, cu_seqlens, out,
                             final_state, ckpt_every, ckpt_states, workspace, workspace_bytes,
                             stream);
+}
+
+kda_status kda_fwd_chunked_prologue(const kda_desc* desc, const kda_prologue_params* prm,
+                                    const void* q_raw, const void* k_raw, const void* v_raw,
+                                    const void* g_raw, const void* beta_logit,
+                                    const float* init_state, const int32_t* cu_seqlens, void* out,
+                                    float* final_state, void* workspace, size_t workspace_bytes,
+                                    kda_stream_t stream) {
+    if (!prm) return KDA_ERR_INVALID_ARG;
+    return fwd_chunked_impl(desc, q_raw, k_raw, v_raw, g_raw, beta_logit, init_state, cu_seqlens,
+                            out, final_state, 0, nullptr, workspace, workspace_bytes, stream, prm);
+}
+
+kda_status kda_prologue(const kda_desc* desc, const kda_prologue_params* prm, const void* q_raw,
+                        const void* k_raw, const void* v_raw, const void* g_raw,
+                        const void* beta_logit, void* q, void* k, void* v, void* log_alpha,
+                        void* beta, kda_stream_t stream) {
+    kda_status st = check_desc(desc, false);
+    if (st != KDA_OK) return st;
+    if (desc->in_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!check_prologue(prm)) return KDA_ERR_INVALID_ARG;
+    if (desc->total_tokens == 0) return KDA_OK;
+    const void* in[5] = {q_raw, k_raw, v_raw, g_raw, beta_logit};
+    const void* outs[5] = {q, k, v, log_alpha, beta};
+    for (int i = 0; i < 5; ++i) {
+        if (!in[i] || !outs[i]) return KDA_ERR_INVALID_ARG;
+        if (i < 4 && (!aligned16(in[i]) || !aligned16(outs[i]))) return KDA_ERR_INVALID_ARG;
+        for (int j = 0; j < 5; ++j)
+            if (outs[i] == in[j] || (j != i && outs[i] == outs[j])) return KDA_ERR_INVALID_ARG;
+    }
+    cudaError_t e = kda::launch_prologue(desc->total_tokens * desc->num_heads, desc->num_heads,
+                                         q_raw, k_raw, v_raw, g_raw, beta_logit, prm->A_log,
+                                         prm->dt_bias, prm->lower_bound, prm->q_scale, q, k, v,
+                                         log_alpha, beta, (cudaStream_t)stream);
+    g_launches += 1;
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status kda_decode_step(const kda_desc* desc, const void* q, const void* k, const void* v,
@@ -257,6 +311,6 @@ const char* kda_status_string(kda_status s) {
 
 uint64_t kda_launch_count(void) { return g_launches.load(); }
 
-int32_t kda_version(void) { return 1; }
+int32_t kda_version(void) { return 2; }
 
 }  // extern "C"

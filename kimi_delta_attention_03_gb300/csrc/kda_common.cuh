@@ -92,14 +92,31 @@ struct SeqOrder {
     uint16_t seq[kMaxOrdered];      // seq[rank] = sequence index
 };
 
+// Input prologue parameters (raw projections in; see kda_prologue.cuh).
+struct ProParams {
+    const float* A_log;    // [H]
+    const float* dt_bias;  // [H][128] or null
+    float lower_bound;
+    float q_scale;
+};
+
 // host_seqlens (optional, host memory): the sequence lengths, used only to rank the sequences
 // for dispatch; without them the CTAs run in packing order.  ckpt (optional, device): state
 // checkpoints after every ckpt_chunks chunks of each sequence, [count][H][128][128] fp32.
+// pro (optional): q, k, v, g and beta are raw projections and the prologue runs in the kernel
+// (not combined with checkpoints).
 cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, const void* q,
                               const void* k, const void* v, const void* g, const void* beta,
                               const float* init_state, const int32_t* cu_seqlens, void* out,
                               float* final_state, const SegWorkspace& ws, int* status,
                               cudaStream_t stream, uint64_t* launches,
                               const int32_t* host_seqlens = nullptr, float* ckpt = nullptr,
-                              int ckpt_chunks = 0);
+                              int ckpt_chunks = 0, const ProParams* pro = nullptr);
+
+// The prologue alone over `rows` (token, head) rows, bf16 in and out.
+cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const void* k_raw,
+                            const void* v_raw, const void* g_raw, const void* beta_logit,
+                            const float* A_log, const float* dt_bias, float lower_bound,
+                            float q_scale, void* q, void* k, void* v, void* g, void* beta,
+                            cudaStream_t stream);
 }  // namespace kda

@@ -38,6 +38,7 @@
 #include <vector>
 
 #include "kda_common.cuh"
+#include "kda_prologue.cuh"
 #include "kda_sm100.cuh"
 
 namespace kda {
@@ -98,7 +99,9 @@ enum {
     B_FULL0 = 0, B_FULL1, B_VFREE0, B_VFREE1, B_VFULL, B_SPARE,
     B_FACT0, B_FACT1, B_AP0, B_AP1, B_TB0, B_TB1, B_WDONE0, B_WDONE1, B_WN0, B_WN1,
     B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_UFREE0, B_UFREE1, B_KMFREE0, B_KMFREE1, B_KMFREE2,
-    B_SDONE, B_PFREE0, B_PFREE1, B_SCAN0, B_SCAN1, B_GFULL, B_M6ISS, B_COUNT
+    B_SDONE, B_PFREE0, B_PFREE1, B_SCAN0, B_SCAN1, B_GFULL, B_M6ISS,
+    B_VPRO,  // prologue variant: v of the chunk has been through Swish
+    B_COUNT
 };
 static_assert(B_COUNT <= NBAR, "barrier slots");
 
@@ -124,6 +127,11 @@ struct TcParams {
     int ckpt_chunks;   // chunks between checkpoints
     int H;
     int pass;          // 0: whole sequences + pass A of split ones; 1: pass B of split ones
+    // input prologue (the kPro variant): q, k, v, g, beta are raw projections
+    const float* pro_A_log;    // [H]
+    const float* pro_dt_bias;  // [H][128] or null
+    float pro_lb;              // lower bound of log alpha
+    float pro_q_scale;
 };
 
 // What one CTA does (chosen from the sequence length and blockIdx.z).
@@ -293,8 +301,12 @@ __device__ __forceinline__ void store_state(float* dst, uint32_t taddr, const fl
 // prefixes of g at the 16 four-token groups (into the prefix array), G_C, e^{r} with
 // r = G_C / 2, and the state scale e^{r_{cs-1} + r_cs}.  Group sums first, then the prefix over
 // the groups.  One call site, out of line: inlined, it raises the epilogue loop's spills.
-__device__ __noinline__ bool decay_scan(unsigned char* sm, int cs, int L, int te,
-                                        volatile int* abort_flag, int* status) {
+// kPro: g is the raw gate input; each value goes through the bounded gate (rounded to bf16, as
+// an unfused prologue would store it) and is written back for the factor pass.
+template <bool kPro>
+__device__ __forceinline__ bool decay_scan_body(unsigned char* sm, int cs, int L, int te,
+                                                volatile int* abort_flag, int* status, float dt,
+                                                float a, float lb) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     float* part = reinterpret_cast<float*>(sm + OFF_PART);
     float* gc_s = reinterpret_cast<float*>(sm + OFF_GC);
@@ -316,6 +328,14 @@ __device__ __noinline__ bool decay_scan(unsigned char* sm, int cs, int L, int te
         for (int i = 0; i < 16; ++i)
             gv[i] = __bfloat162float(*reinterpret_cast<const bf16*>(
                 gcol + (t16 + i) * 128 + ((chunk16 ^ (i & 7)) << 4)));
+        if constexpr (kPro) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                gv[i] = pro_gate(gv[i], dt, a, lb);
+                *reinterpret_cast<bf16*>(const_cast<unsigned char*>(gcol) + (t16 + i) * 128 +
+                                         ((chunk16 ^ (i & 7)) << 4)) = __float2bfloat16_rn(gv[i]);
+            }
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float gs = 0.f;
@@ -337,13 +357,26 @@ __device__ __noinline__ bool decay_scan(unsigned char* sm, int cs, int L, int te
     const float e = ex2_approx((0.5f * kLog2eTC) * run);
     er[(cs & 3) * kDim + te] = e;
     sc[(cs & 3) * kDim + te] = cs > 0 ? er[((cs + 3) & 3) * kDim + te] * e : e;
+    if constexpr (kPro) fence_async_shared();  // the gated g is overwritten by the next TMA load
     named_bar(kBarEpi, kEpiThreads);
     if (te == 0) mbar_arrive(&bars[B_SCAN0 + s2]);
     return true;
 }
 
-// kCkpt: the variant that also writes state checkpoints (the plain one carries no trace of it).
-template <bool kCkpt>
+__device__ __noinline__ bool decay_scan(unsigned char* sm, int cs, int L, int te,
+                                        volatile int* abort_flag, int* status) {
+    return decay_scan_body<false>(sm, cs, L, te, abort_flag, status, 0.f, 0.f, 0.f);
+}
+__device__ __noinline__ bool decay_scan_pro(unsigned char* sm, int cs, int L, int te,
+                                            volatile int* abort_flag, int* status, float dt,
+                                            float a, float lb) {
+    return decay_scan_body<true>(sm, cs, L, te, abort_flag, status, dt, a, lb);
+}
+
+// kCkpt: the variant that also writes state checkpoints; kPro: the variant that takes raw
+// projections and runs the input prologue on the tiles as they arrive (the plain kernel carries
+// no trace of either).
+template <bool kCkpt, bool kPro>
 __global__ void __launch_bounds__(kThreadsTC, 1)
 kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -551,7 +584,9 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     }
                     mma_commit(&bars[B_WDONE0 + s]);
                     // M3: U_bar^T = V^T (T diag(beta))^T into the U^T columns, once v has landed
-                    if (!spin_bar(&bars[B_VFULL], c & 1, abort_flag, p.status)) break;
+                    // (and, for raw inputs, has been through Swish)
+                    if (!spin_bar(&bars[kPro ? B_VPRO : B_VFULL], c & 1, abort_flag, p.status))
+                        break;
                     tc_fence_after();
                     {
                         const uint64_t da = smem_desc(a_v, 8192, 1024);
@@ -674,7 +709,9 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7.
             // The token-group prefixes of g, G_C and e^{r} come from the epilogue warps' scan.
             if (tp < kChunk) {
-                beta_ring(c)[tp] = __uint_as_float((uint32_t)beta_raw << 16);
+                float bt = __uint_as_float((uint32_t)beta_raw << 16);
+                if constexpr (kPro) bt = tp < valid ? round_bf16(pro_sigmoid(bt)) : 0.f;
+                beta_ring(c)[tp] = bt;
                 // fetch the next chunk's beta now; it is needed one chunk later
                 const int vn = min(kChunk, L - kChunk * (c + 1));
                 if (tp < vn)
@@ -722,6 +759,10 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     unpack8(gr, gv);
                     unpack8(kr, kv);
                     unpack8(qr4, qv);
+                    if constexpr (kPro) {  // raw k, q: Swish, then the row norm (16 lanes a row)
+                        pro_swish_l2(kv, 1.f);
+                        pro_swish_l2(qv, p.pro_q_scale);
+                    }
                     float kp[8], qr[8], km[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -937,11 +978,33 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         // Software pipeline: the W epilogue of chunk c-1 runs while the tensor core forms A and P
         // of chunk c, and the factors of chunk c+1 while it forms W of chunk c.
         // Each phase has a single call site (the lambdas are inlined where they are called).
+        // kPro: Swish on v of chunk c in place before M3 of chunk c reads it
+        auto v_prologue = [&](const int c) -> bool {
+            if (!wait_bar(&bars[B_VFULL], c & 1, abort_flag, p.status)) return false;
+            if (!zero_v) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4* src = reinterpret_cast<uint4*>(sm + OFF_V) + tp + kPrepThreads * j;
+                    float x[8];
+                    unpack8(*src, x);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) x[i] = pro_swish(x[i]);
+                    *src = pack8(x);
+                }
+            }
+            fence_async_shared();
+            named_bar(kBarPrep, kPrepThreads);
+            if (tp == 0) mbar_arrive(&bars[B_VPRO]);
+            return true;
+        };
         for (int c = -1; c <= nchunks; ++c) {
             if (c >= 1 && !w_epilogue(c - 1)) break;
             if (c >= 0 && c < nchunks) {
                 if (!ap_epilogue(c)) break;
                 inverse(c);
+                if constexpr (kPro) {
+                    if (!v_prologue(c)) break;
+                }
             }
             if (c + 1 < nchunks && !factor(c + 1)) break;
         }
@@ -962,8 +1025,17 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             ckpt0 = p.ckpt + (base * H + h) * (int64_t)(kDim * kDim);
         }
         const int chunk0 = item == ITEM_SEGMENT ? sigma * kSegChunks : 0;
+        float pro_dt = 0.f, pro_a = 0.f, pro_lb = 0.f;
+        if constexpr (kPro) {
+            pro_dt = p.pro_dt_bias ? p.pro_dt_bias[h * kDim + te] : 0.f;
+            pro_a = pro_gate_rate(p.pro_A_log, h);
+            pro_lb = p.pro_lb;
+        }
         auto scan = [&](const int cs) -> bool {
-            return decay_scan(sm, cs, L, te, abort_flag, p.status);
+            if constexpr (kPro)
+                return decay_scan_pro(sm, cs, L, te, abort_flag, p.status, pro_dt, pro_a, pro_lb);
+            else
+                return decay_scan(sm, cs, L, te, abort_flag, p.status);
         };
         bool ok = true;
         // c = -2 and -1 only scan chunks 0 and 1 (and set up X_0): one code path for the scan
@@ -1224,7 +1296,8 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
                               const float* init_state, const int32_t* cu_seqlens, void* out,
                               float* final_state, const SegWorkspace& ws, int* status,
                               cudaStream_t stream, uint64_t* launches,
-                              const int32_t* host_seqlens, float* ckpt, int ckpt_chunks) {
+                              const int32_t* host_seqlens, float* ckpt, int ckpt_chunks,
+                              const ProParams* pro) {
     if (num_seqs <= 0 || heads <= 0) return cudaSuccess;
     const int64_t units = (int64_t)num_seqs * heads;
     if (units > INT32_MAX) return cudaErrorInvalidValue;
@@ -1255,9 +1328,16 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
     prm.ws_in = ws.in;
     prm.ckpt = ckpt_chunks > 0 ? ckpt : nullptr;
     prm.ckpt_chunks = ckpt_chunks > 0 ? ckpt_chunks : 1;
+    prm.pro_A_log = pro ? pro->A_log : nullptr;
+    prm.pro_dt_bias = pro ? pro->dt_bias : nullptr;
+    prm.pro_lb = pro ? pro->lower_bound : 0.f;
+    prm.pro_q_scale = pro ? pro->q_scale : 1.f;
     prm.H = heads;
     prm.pass = 0;
-    auto kernel = prm.ckpt ? kda_prefill_tc_kernel<true> : kda_prefill_tc_kernel<false>;
+    if (pro && prm.ckpt) return cudaErrorInvalidValue;
+    auto kernel = pro ? kda_prefill_tc_kernel<false, true>
+                      : prm.ckpt ? kda_prefill_tc_kernel<true, false>
+                                 : kda_prefill_tc_kernel<false, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_ALLOC);
     if (e != cudaSuccess) return e;

@@ -108,6 +108,44 @@ def make_inputs(lengths, heads: int, dtype: torch.dtype, seed: int, gate_scale: 
     }
 
 
+def make_raw_inputs(lengths, heads: int, seed: int, s0_std: float | None = 0.01, device="cpu",
+                    dt_center: float = -4.0, d: int = D_K) -> dict:
+    """Raw per-token projections for the input prologue, layout [T_tot, H, d], bf16.
+
+    q_raw, k_raw, v_raw, g_raw and beta_logit are N(0, 1) (the short-convolution outputs and
+    logits a layer would produce; the sources give no distribution).  A_log ~ 0.25 N(0, 1) per
+    head and dt_bias ~ dt_center + 0.5 N(0, 1) per (head, channel), fp32, so that the bounded
+    gate's output sits mostly in (-0.5, 0) with a tail towards the bound.  Also returns
+    init_state, cu_seqlens and seqlens as ``make_inputs`` does."""
+    lengths = [int(x) for x in lengths]
+    if any(x < 0 for x in lengths):
+        raise ValueError("bad lengths")
+    n, T = len(lengths), sum(lengths)
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    f32, bf = torch.float32, torch.bfloat16
+    q = torch.randn(T, heads, d, generator=gen, device=dev, dtype=f32)
+    k = torch.randn(T, heads, d, generator=gen, device=dev, dtype=f32)
+    v = torch.randn(T, heads, d, generator=gen, device=dev, dtype=f32)
+    b_logit = torch.randn(T, heads, generator=gen, device=dev, dtype=f32)
+    g = torch.randn(T, heads, d, generator=gen, device=dev, dtype=f32)
+    A_log = torch.randn(heads, generator=gen, device=dev, dtype=f32) * 0.25
+    dt_bias = dt_center + torch.randn(heads, d, generator=gen, device=dev, dtype=f32) * 0.5
+    s0 = None
+    if s0_std is not None:
+        s0 = torch.randn(n, heads, d, d, generator=gen, device=dev, dtype=f32) * s0_std
+    cu = torch.zeros(n + 1, dtype=torch.int32)
+    if n:
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    return {
+        "q_raw": q.to(bf).contiguous(), "k_raw": k.to(bf).contiguous(),
+        "v_raw": v.to(bf).contiguous(), "g_raw": g.to(bf).contiguous(),
+        "beta_logit": b_logit.to(bf).contiguous(), "A_log": A_log.contiguous(),
+        "dt_bias": dt_bias.contiguous(), "init_state": s0, "cu_seqlens": cu.to(dev),
+        "seqlens": lengths,
+    }
+
+
 def make_workload(w: Workload, device="cpu", heads: int | None = None,
                   lengths=None) -> dict:
     """Inputs of workload ``w`` (optionally with fewer heads or other lengths)."""

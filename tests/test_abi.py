@@ -134,6 +134,44 @@ def test_checkpoint_and_window_argument_checks(lib):
     assert win(d) == -1                                         # run lengths are required
 
 
+def test_prologue_argument_checks(lib):
+    from kimi_delta_attention_03_gb300.binding import KdaPrologueParams
+    P = ctypes.c_void_p
+    fake, fake2 = P(0x1000), P(0x5000)
+    ok = dict(A_log=0x7000, dt_bias=None, lower_bound=-5.0, q_scale=0.125)
+
+    def prm(**kw):
+        a = dict(ok, **kw)
+        return KdaPrologueParams(a["A_log"], a["dt_bias"], a["lower_bound"], a["q_scale"])
+
+    def fused(d, p):
+        return lib.kda_fwd_chunked_prologue(ctypes.byref(d), p, fake, fake, fake, fake, fake,
+                                            None, fake, P(0x2000), None, None, 0, None)
+    d = _desc([128, 64])
+    assert fused(d, None) == -1                                          # no parameters
+    assert fused(d, ctypes.byref(prm(A_log=None))) == -1                 # no A_log
+    assert fused(d, ctypes.byref(prm(dt_bias=0x7004))) == -1             # misaligned dt_bias
+    assert fused(d, ctypes.byref(prm(lower_bound=0.0))) == -1            # bound must be < 0
+    assert fused(d, ctypes.byref(prm(lower_bound=-100.0))) == -1         # beyond the range
+    assert fused(d, ctypes.byref(prm(lower_bound=float("nan")))) == -1
+    assert fused(d, ctypes.byref(prm(q_scale=0.0))) == -1
+    assert fused(d, ctypes.byref(prm(q_scale=float("inf")))) == -1
+    assert fused(_desc([128, 64], dtype=torch.float32), ctypes.byref(prm())) == -2  # bf16 only
+
+    def alone(d, p, outs=(0x2000, 0x2400, 0x2800, 0x2c00, 0x3000), ins=None):
+        ins = ins or (0x1000, 0x1400, 0x1800, 0x1c00, 0x2000 - 0x100)
+        return lib.kda_prologue(ctypes.byref(d), p, *[P(x) for x in ins],
+                                *[None if x is None else P(x) for x in outs], None)
+    p = ctypes.byref(prm())
+    assert alone(_desc([64]), None) == -1
+    assert alone(_desc([64]), p, outs=(0x1000, 0x2400, 0x2800, 0x2c00, 0x3000)) == -1  # aliases
+    assert alone(_desc([64]), p, outs=(0x2000, 0x2000, 0x2800, 0x2c00, 0x3000)) == -1  # repeats
+    assert alone(_desc([64]), p, outs=(0x2000, 0x2400, None, 0x2c00, 0x3000)) == -1    # missing
+    assert alone(_desc([64]), p, outs=(0x2008, 0x2400, 0x2800, 0x2c00, 0x3000)) == -1  # unaligned
+    assert alone(_desc([64], dtype=torch.float32), p) == -2
+    assert alone(_desc([0]), p) == 0                     # nothing to do: no launch, no error
+
+
 def test_binding_refuses_cpu_tensors(lib):
     import kimi_delta_attention_03_gb300 as kda
     x = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
