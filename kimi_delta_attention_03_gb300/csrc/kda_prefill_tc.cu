@@ -705,6 +705,21 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
             unsigned char* kmh = sm + kmh_off(c);
             if (!wait_bar(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
+            if constexpr (kPro) {
+                // raw k, q -> Swish, row norm, bf16, in place.  This needs only the k / q tiles,
+                // so it runs before the wait for the decay scan, off the serial chain.
+#pragma unroll 1
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t o = sw128_offset(4 * tg + i, c8, KQW_ROWS);
+                    float kv[8], qv[8];
+                    unpack8(*reinterpret_cast<const uint4*>(kq + o), kv);
+                    unpack8(*reinterpret_cast<const uint4*>(kq + o + 64 * 128), qv);
+                    pro_swish_l2(kv, 1.f);
+                    pro_swish_l2(qv, p.pro_q_scale);
+                    *reinterpret_cast<uint4*>(kq + o) = pack8(kv);
+                    *reinterpret_cast<uint4*>(kq + o + 64 * 128) = pack8(qv);
+                }
+            }
 
             // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7.
             // The token-group prefixes of g, G_C and e^{r} come from the epilogue warps' scan.
@@ -759,10 +774,6 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     unpack8(gr, gv);
                     unpack8(kr, kv);
                     unpack8(qr4, qv);
-                    if constexpr (kPro) {  // raw k, q: Swish, then the row norm (16 lanes a row)
-                        pro_swish_l2(kv, 1.f);
-                        pro_swish_l2(qv, p.pro_q_scale);
-                    }
                     float kp[8], qr[8], km[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {

@@ -44,26 +44,29 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
          row += warps) {
         const int h = (int)(row % H);
         const int64_t base = row * kDim;
-        {   // q (lanes 0-15) or k (lanes 16-31): Swish, then the row norm
-            const bool is_q = lane < 16;
-            const int64_t e = base + 8 * (lane & 15);
+        // every load of the row first: one memory round trip per row
+        const bool is_q = lane < 16;  // lanes 0-15: the q row; lanes 16-31: the k row
+        const int64_t eqk = base + 8 * (lane & 15);
+        const int64_t evg = base + 4 * lane;    // v and g: four channels per lane
+        const uint4 qk = __ldcs(reinterpret_cast<const uint4*>((is_q ? q_raw : k_raw) + eqk));
+        const uint2 vr = __ldcs(reinterpret_cast<const uint2*>(v_raw + evg));
+        const uint2 gr = __ldcs(reinterpret_cast<const uint2*>(g_raw + evg));
+        const float b_logit = lane == 0 ? __bfloat162float(beta_logit[row]) : 0.f;
+        float dt[4] = {0.f, 0.f, 0.f, 0.f};
+        if (dt_bias) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dt_bias + h * kDim + 4 * lane);
+            dt[0] = d4.x; dt[1] = d4.y; dt[2] = d4.z; dt[3] = d4.w;
+        }
+        const float na = pro_gate_rate(A_log, h);
+        {   // q or k: Swish, then the row norm
             float x[8];
-            unpack8_bf16(__ldcs(reinterpret_cast<const uint4*>((is_q ? q_raw : k_raw) + e)), x);
+            unpack8_bf16(qk, x);
             pro_swish_l2(x, is_q ? q_scale : 1.f);
-            __stcs(reinterpret_cast<uint4*>((is_q ? q : k) + e),
+            __stcs(reinterpret_cast<uint4*>((is_q ? q : k) + eqk),
                    make_uint4(pack2_bf16(x[0], x[1]), pack2_bf16(x[2], x[3]),
                               pack2_bf16(x[4], x[5]), pack2_bf16(x[6], x[7])));
         }
-        {   // v: Swish; g: the bounded gate (four channels per lane)
-            const int64_t e = base + 4 * lane;
-            const uint2 vr = __ldcs(reinterpret_cast<const uint2*>(v_raw + e));
-            const uint2 gr = __ldcs(reinterpret_cast<const uint2*>(g_raw + e));
-            const float ha = pro_gate_rate(A_log, h);
-            float dt[4] = {0.f, 0.f, 0.f, 0.f};
-            if (dt_bias) {
-                const float4 d4 = *reinterpret_cast<const float4*>(dt_bias + h * kDim + 4 * lane);
-                dt[0] = d4.x; dt[1] = d4.y; dt[2] = d4.z; dt[3] = d4.w;
-            }
+        {   // v: Swish; g: the bounded gate
             const uint32_t vw[2] = {vr.x, vr.y}, gw[2] = {gr.x, gr.y};
             uint32_t vo[2], go[2];
 #pragma unroll
@@ -71,14 +74,13 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
                 const float v0 = __uint_as_float(vw[i] << 16), v1 = __uint_as_float(vw[i] & 0xffff0000u);
                 const float g0 = __uint_as_float(gw[i] << 16), g1 = __uint_as_float(gw[i] & 0xffff0000u);
                 vo[i] = pack2_bf16(pro_swish(v0), pro_swish(v1));
-                go[i] = pack2_bf16(pro_gate(g0, dt[2 * i], ha, lower_bound),
-                                   pro_gate(g1, dt[2 * i + 1], ha, lower_bound));
+                go[i] = pack2_bf16(pro_gate(g0, dt[2 * i], na, lower_bound),
+                                   pro_gate(g1, dt[2 * i + 1], na, lower_bound));
             }
-            __stcs(reinterpret_cast<uint2*>(v + e), make_uint2(vo[0], vo[1]));
-            __stcs(reinterpret_cast<uint2*>(g + e), make_uint2(go[0], go[1]));
+            __stcs(reinterpret_cast<uint2*>(v + evg), make_uint2(vo[0], vo[1]));
+            __stcs(reinterpret_cast<uint2*>(g + evg), make_uint2(go[0], go[1]));
         }
-        if (lane == 0)
-            beta[row] = __float2bfloat16_rn(pro_sigmoid(__bfloat162float(beta_logit[row])));
+        if (lane == 0) beta[row] = __float2bfloat16_rn(pro_sigmoid(b_logit));
     }
 }
 

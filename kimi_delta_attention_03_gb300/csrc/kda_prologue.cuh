@@ -7,10 +7,12 @@
 // state": the decay gate lower_bound * sigmoid(exp(A_log) * (g + dt_bias)).  FlashKDA's forward,
 // section "FlashKDA: the equation, shipped as a kernel": beta = sigmoid(beta logits)).
 //
-// sigmoid(x) = 1 / (1 + 2^{-x log2 e}) on the SFU's exp2 and reciprocal approximations: about
-// 1e-6 relative error for every x, including the small decays near 0 that a tanh-based form
-// (0.5 + 0.5 tanh(x / 2)) would get from a cancellation.  Every prologue output is rounded to
-// bf16 where an unfused pipeline would store it.
+// The gate and beta use sigmoid(x) = 1 / (1 + 2^{-x log2 e}) on the SFU's exp2 and reciprocal
+// approximations: about 1e-6 relative error for every x, including the small decays near 0 that
+// a tanh-based form (0.5 + 0.5 tanh(x / 2)) would lose to a cancellation.  Swish uses that
+// tanh form, one SFU operation instead of two: its absolute error (about |x| 2.5e-4) is small
+// against the row it belongs to.  Every prologue output is rounded to bf16 where an unfused
+// pipeline would store it.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -22,6 +24,11 @@ constexpr float kProNormEps = 1e-6f;  // added to the sum of squares of the L2 n
 __device__ __forceinline__ float ex2_sfu(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float tanh_sfu(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 __device__ __forceinline__ float rcp_sfu(float x) {
@@ -39,17 +46,21 @@ __device__ __forceinline__ float pro_sigmoid(float x) {
     return rcp_sfu(__fadd_rn(1.f, ex2_sfu(__fmul_rn(-1.4426950408889634f, x))));
 }
 
-// Swish(x) = x sigmoid(x)
-__device__ __forceinline__ float pro_swish(float x) { return __fmul_rn(x, pro_sigmoid(x)); }
-
-// log alpha = lb sigmoid(a (g + dt)), rounded to bf16
-__device__ __forceinline__ float pro_gate(float g, float dt, float a, float lb) {
-    return round_bf16(__fmul_rn(lb, pro_sigmoid(__fmul_rn(a, __fadd_rn(g, dt)))));
+// Swish(x) = x sigmoid(x) = h + h tanh(h) with h = x / 2
+__device__ __forceinline__ float pro_swish(float x) {
+    const float h = __fmul_rn(0.5f, x);
+    return fmaf(h, tanh_sfu(h), h);
 }
 
-// a = exp(A_log[h]) for head h
+// log alpha = lb sigmoid(a (g + dt)) = lb / (1 + 2^{na (g + dt)}) with na = -a log2 e, rounded
+// to bf16
+__device__ __forceinline__ float pro_gate(float g, float dt, float na, float lb) {
+    return round_bf16(__fmul_rn(lb, rcp_sfu(__fadd_rn(1.f, ex2_sfu(__fmul_rn(na, __fadd_rn(g, dt)))))));
+}
+
+// na = -exp(A_log[h]) log2 e for head h
 __device__ __forceinline__ float pro_gate_rate(const float* A_log, int h) {
-    return expf(A_log[h]);
+    return __fmul_rn(-1.4426950408889634f, expf(A_log[h]));
 }
 
 // Sum over a 128-channel row held as eight consecutive channels per lane of a 16-lane group

@@ -1,7 +1,7 @@
 """GPU parity of the input prologue (raw projections -> q, k, v, log alpha, beta):
 
 - the standalone prologue kernel against the fp64 oracle, element by element, within one bf16
-  rounding of each output;
+  rounding of each output (plus, for the Swish outputs, the SFU tanh's error against the row);
 - the prologue fused into the prefill against the unfused pipeline (standalone prologue, then
   the plain prefill), bit for bit, including an empty sequence, ragged tails, a segmented
   sequence and no dt_bias;
@@ -54,8 +54,12 @@ def test_prologue_kernel_matches_oracle(dt_bias):
     for name, got, want in zip(("q", "k", "v", "log_alpha", "beta"), outs, ref):
         assert got.dtype == torch.bfloat16
         g = got.float().cpu().numpy().astype(np.float64)
-        # one bf16 rounding (at most 2^-8 relative) of a value computed to ~1e-6 in fp32
+        # one bf16 rounding (at most 2^-8 relative) of a value computed in fp32: to ~1e-6 for
+        # log alpha and beta (exp2 / reciprocal sigmoid); Swish uses the SFU tanh, whose error
+        # (about |x| 2.5e-4 before the norm) is bounded against the RMS of the row
         tol = 2.0 ** -8 * np.abs(want) * (1 + 1e-4) + 1e-7
+        if name in ("q", "k", "v"):
+            tol = tol + 3e-3 * np.sqrt(np.mean(want * want, axis=-1, keepdims=True))
         bad = np.abs(g - want) > tol
         assert not bad.any(), f"{name}: {int(bad.sum())} elements off, first at " \
                               f"{np.argwhere(bad)[0]}: {g[bad][0]} vs {want[bad][0]}"
