@@ -8,7 +8,8 @@
 // One warp per (token, head) row: lanes 0-15 hold the q row and lanes 16-31 the k row, eight
 // consecutive channels each (one 16-byte load), the layout of the fused prefill's factor pass, so
 // both reduce the row norms in the same order; v and g are four channels per lane.  The pass is
-// HBM-bound: 1,026 bytes read and 1,026 written per row.
+// HBM-bound: 1,026 bytes read and 1,026 written per row; the grid is persistent and every warp
+// keeps its next row's loads in flight while it computes the current one.
 #include "kda_common.cuh"
 #include "kda_prologue.cuh"
 
@@ -31,6 +32,35 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
 }
 
+// The raw inputs of one row, as this lane loads them.
+struct ProRow {
+    uint4 qk;     // eight q channels (lanes 0-15) or eight k channels (lanes 16-31)
+    uint2 v, g;   // four channels each
+    float b;      // beta logit (lane 0)
+    float4 dt;    // dt_bias of the lane's four g channels
+};
+
+__device__ __forceinline__ ProRow load_row(const bf16* __restrict__ q_raw,
+                                           const bf16* __restrict__ k_raw,
+                                           const bf16* __restrict__ v_raw,
+                                           const bf16* __restrict__ g_raw,
+                                           const bf16* __restrict__ beta_logit,
+                                           const float* __restrict__ dt_bias, int64_t row, int h,
+                                           int lane) {
+    ProRow r;
+    const int64_t base = row * kDim;
+    r.qk = __ldcs(reinterpret_cast<const uint4*>((lane < 16 ? q_raw : k_raw) + base +
+                                                 8 * (lane & 15)));
+    r.v = __ldcs(reinterpret_cast<const uint2*>(v_raw + base + 4 * lane));
+    r.g = __ldcs(reinterpret_cast<const uint2*>(g_raw + base + 4 * lane));
+    r.b = lane == 0 ? __bfloat162float(beta_logit[row]) : 0.f;
+    r.dt = dt_bias ? *reinterpret_cast<const float4*>(dt_bias + h * kDim + 4 * lane)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    return r;
+}
+
+// Persistent grid: each warp walks rows in strides of the grid and loads its next row while it
+// computes the current one, so two rows per warp are in flight.
 __global__ void __launch_bounds__(kProThreads)
 kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_raw,
                     const bf16* __restrict__ v_raw, const bf16* __restrict__ g_raw,
@@ -40,34 +70,29 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
                     bf16* __restrict__ g, bf16* __restrict__ beta, int64_t rows, int H) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (kProThreads / 32);
-    for (int64_t row = (int64_t)blockIdx.x * (kProThreads / 32) + (threadIdx.x >> 5); row < rows;
-         row += warps) {
-        const int h = (int)(row % H);
+    int64_t row = (int64_t)blockIdx.x * (kProThreads / 32) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    int h = (int)(row % H);
+    ProRow cur = load_row(q_raw, k_raw, v_raw, g_raw, beta_logit, dt_bias, row, h, lane);
+    while (true) {
+        const int64_t next = row + warps;
+        const int hn = (int)(next % H);
+        ProRow nxt = cur;
+        if (next < rows) nxt = load_row(q_raw, k_raw, v_raw, g_raw, beta_logit, dt_bias, next, hn, lane);
         const int64_t base = row * kDim;
-        // every load of the row first: one memory round trip per row
         const bool is_q = lane < 16;  // lanes 0-15: the q row; lanes 16-31: the k row
-        const int64_t eqk = base + 8 * (lane & 15);
-        const int64_t evg = base + 4 * lane;    // v and g: four channels per lane
-        const uint4 qk = __ldcs(reinterpret_cast<const uint4*>((is_q ? q_raw : k_raw) + eqk));
-        const uint2 vr = __ldcs(reinterpret_cast<const uint2*>(v_raw + evg));
-        const uint2 gr = __ldcs(reinterpret_cast<const uint2*>(g_raw + evg));
-        const float b_logit = lane == 0 ? __bfloat162float(beta_logit[row]) : 0.f;
-        float dt[4] = {0.f, 0.f, 0.f, 0.f};
-        if (dt_bias) {
-            const float4 d4 = *reinterpret_cast<const float4*>(dt_bias + h * kDim + 4 * lane);
-            dt[0] = d4.x; dt[1] = d4.y; dt[2] = d4.z; dt[3] = d4.w;
-        }
-        const float na = pro_gate_rate(A_log, h);
         {   // q or k: Swish, then the row norm
             float x[8];
-            unpack8_bf16(qk, x);
+            unpack8_bf16(cur.qk, x);
             pro_swish_l2(x, is_q ? q_scale : 1.f);
-            __stcs(reinterpret_cast<uint4*>((is_q ? q : k) + eqk),
+            __stcs(reinterpret_cast<uint4*>((is_q ? q : k) + base + 8 * (lane & 15)),
                    make_uint4(pack2_bf16(x[0], x[1]), pack2_bf16(x[2], x[3]),
                               pack2_bf16(x[4], x[5]), pack2_bf16(x[6], x[7])));
         }
-        {   // v: Swish; g: the bounded gate
-            const uint32_t vw[2] = {vr.x, vr.y}, gw[2] = {gr.x, gr.y};
+        {   // v: Swish; g: the bounded gate (four channels per lane)
+            const float na = pro_gate_rate(A_log, h);
+            const float dt[4] = {cur.dt.x, cur.dt.y, cur.dt.z, cur.dt.w};
+            const uint32_t vw[2] = {cur.v.x, cur.v.y}, gw[2] = {cur.g.x, cur.g.y};
             uint32_t vo[2], go[2];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
@@ -77,10 +102,14 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
                 go[i] = pack2_bf16(pro_gate(g0, dt[2 * i], na, lower_bound),
                                    pro_gate(g1, dt[2 * i + 1], na, lower_bound));
             }
-            __stcs(reinterpret_cast<uint2*>(v + evg), make_uint2(vo[0], vo[1]));
-            __stcs(reinterpret_cast<uint2*>(g + evg), make_uint2(go[0], go[1]));
+            __stcs(reinterpret_cast<uint2*>(v + base + 4 * lane), make_uint2(vo[0], vo[1]));
+            __stcs(reinterpret_cast<uint2*>(g + base + 4 * lane), make_uint2(go[0], go[1]));
         }
-        if (lane == 0) beta[row] = __float2bfloat16_rn(pro_sigmoid(b_logit));
+        if (lane == 0) beta[row] = __float2bfloat16_rn(pro_sigmoid(cur.b));
+        if (next >= rows) break;
+        row = next;
+        h = hn;
+        cur = nxt;
     }
 }
 
@@ -92,9 +121,17 @@ cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const vo
                             float q_scale, void* q, void* k, void* v, void* g, void* beta,
                             cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess)
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_prologue_kernel,
+                                                            kProThreads, 0);
+    if (err != cudaSuccess) return err;
     const int64_t per_block = kProThreads / 32;
-    const int64_t blocks = (rows + per_block - 1) / per_block;
-    const unsigned grid = (unsigned)(blocks < (1LL << 30) ? blocks : (1LL << 30));
+    const int64_t need = (rows + per_block - 1) / per_block;
+    const int64_t slots = (int64_t)(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+    const unsigned grid = (unsigned)(need < slots ? need : slots);
     kda_prologue_kernel<<<grid, kProThreads, 0, stream>>>(
         (const bf16*)q_raw, (const bf16*)k_raw, (const bf16*)v_raw, (const bf16*)g_raw,
         (const bf16*)beta_logit, A_log, dt_bias, lower_bound, q_scale, (bf16*)q, (bf16*)k,
