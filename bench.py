@@ -233,9 +233,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--case", default="full", choices=["full", "small"],
+    ap.add_argument("--case", default="full", choices=["full", "small", "small_prologue"],
                     help="small: a reduced prefill (4 x 4096 tokens, 8 heads) and decode "
-                         "(64 x 96) for ncu section captures; not a benchmark figure")
+                         "(64 x 96) for ncu section captures; small_prologue: the same prefill "
+                         "plus the fused and unfused input prologue; not benchmark figures")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip timing the long-context and varlen prefill workloads")
     args = ap.parse_args()
@@ -255,12 +256,13 @@ def main():
     stream = torch.cuda.current_stream(dev)
     hbm_peak, tc_peak, peak_kind = peaks()
 
-    if args.case == "small":
+    small = args.case in ("small", "small_prologue")
+    if small:
         args.no_extra = args.no_e2e = args.no_cpu_baseline = True
 
     # ---------------- prefill (headline) ----------------
     w = synth.workloads()["prefill_4x8k"]
-    if args.case == "small":
+    if small:
         from dataclasses import replace
         w = replace(w, name="prefill_small (B=4, T=4096, H=8, bf16; profiling case)",
                     lengths=(4096,) * 4, heads=8)
@@ -304,7 +306,7 @@ def main():
     decode = None
     if not args.no_decode:
         wd = synth.workloads()["decode_512x96"]
-        n_dec = 64 if args.case == "small" else 512
+        n_dec = 64 if small else 512
         dd = synth.make_decode_inputs(n_dec, 96, torch.bfloat16, seed=wd.seed,
                                       state_std=wd.s0_std, device=dev)
         dout = torch.empty_like(dd["q"])
@@ -403,6 +405,9 @@ def main():
             "value": T * world / (ms_c * 1e-3) / 1e6, "unit": "Mtokens/s",
             "overhead_vs_plain": ms_c / ms_max - 1.0}
         del ckpts
+
+    if not args.no_extra or args.case == "small_prologue":
+        extra = {} if extra is None else extra
         # the headline prefill on raw projections: the input prologue fused into the kernel,
         # against the unfused pipeline (the standalone prologue pass, then the plain prefill)
         xr = synth.make_raw_inputs(x["seqlens"], H, seed=w.seed, s0_std=w.s0_std, device=dev)
