@@ -1,6 +1,7 @@
-"""The compute calls under CUDA graph capture: a captured prefill, decode step and decode
-window replay to the same bits as eager calls on the same buffers (serving loops are replayed
-from graphs, so the calls must launch nothing that capture forbids)."""
+"""The compute calls under CUDA graph capture: a captured prefill (plain and with the fused input
+prologue), decode step and decode window replay to the same bits as eager calls on the same
+buffers (serving loops are replayed from graphs, so the calls must launch nothing that capture
+forbids)."""
 import pytest
 import torch
 
@@ -36,6 +37,34 @@ def test_prefill_replays_from_a_graph():
                           x["seqlens"], init_state=x["init_state"], out=out, final_state=fin)
     for _ in range(2):
         out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, out_e) and torch.equal(fin, fin_e)
+    assert kda().read_device_status() == 0
+
+
+def test_prologue_prefill_replays_from_a_graph():
+    lens = [700, 64, 1300, 5]
+    x = synth.make_raw_inputs(lens, 4, seed=53, device=DEV)
+    raw = (x["q_raw"], x["k_raw"], x["v_raw"], x["g_raw"], x["beta_logit"])
+    out_e, fin_e = kda().fwd_chunked_prologue(*raw, x["cu_seqlens"], x["seqlens"], x["A_log"],
+                                              x["dt_bias"], init_state=x["init_state"])
+    out = torch.empty_like(out_e)
+    fin = torch.empty_like(fin_e)
+    call = lambda: kda().fwd_chunked_prologue(*raw, x["cu_seqlens"], x["seqlens"], x["A_log"],
+                                              x["dt_bias"], init_state=x["init_state"], out=out,
+                                              final_state=fin)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(2):
+        out.zero_()
+        fin.zero_()
         graph.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, out_e) and torch.equal(fin, fin_e)
