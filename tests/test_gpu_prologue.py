@@ -109,3 +109,48 @@ def test_fused_prologue_matches_oracle():
     o64, s64 = oracle.recurrence(q, k, v, g, b, cu, state_in=s0, threads=oracle_threads())
     assert_close("out vs fp64 prologue", out.float().cpu().numpy(), o64, max_tol=np.inf)
     assert_close("state vs fp64 prologue", fin.cpu().numpy(), s64, max_tol=np.inf)
+
+
+def test_fused_prologue_full_size_equals_unfused_and_sampled_oracle():
+    """The 4 x 8192-token, 32-head workload in the benchmark's launch configuration: the fused
+    call equals the unfused pipeline bit for bit, and three (sequence, head) units checked one
+    by one against the oracle (oracle prologue, rounded as the contract states, then the token
+    loop)."""
+    w = synth.workloads()["prefill_4x8k"]
+    x = synth.make_raw_inputs(list(w.lengths), w.heads, seed=w.seed, s0_std=w.s0_std, device=DEV)
+    out, fin = kda().fwd_chunked_prologue(*_raw_args(x), x["cu_seqlens"], x["seqlens"],
+                                          x["A_log"], x["dt_bias"], lower_bound=LB, q_scale=QS,
+                                          init_state=x["init_state"])
+    q, k, v, g, b = kda().prologue(*_raw_args(x), x["A_log"], x["dt_bias"], lower_bound=LB,
+                                   q_scale=QS)
+    o2, s2 = kda().fwd_chunked(q, k, v, g, b, x["cu_seqlens"], x["seqlens"],
+                               init_state=x["init_state"])
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    assert torch.equal(out, o2) and torch.equal(fin, s2)
+    del q, k, v, g, b, o2, s2
+    L = w.lengths[0]
+    to_bf16 = lambda a: torch.from_numpy(a).to(torch.bfloat16)
+    for n, h in ((0, 0), (2, 17), (3, 31)):
+        rows = slice(n * L, (n + 1) * L)
+        pick = lambda t: t[rows, h:h + 1].cpu()
+        ref_in = oracle.prologue(*(pick(t) for t in _raw_args(x)), x["A_log"][h:h + 1].cpu(),
+                                 x["dt_bias"][h:h + 1].cpu(), lower_bound=LB, q_scale=QS)
+        o_ref, s_ref = oracle.recurrence(*map(to_bf16, ref_in), [0, L],
+                                         state_in=x["init_state"][n:n + 1, h:h + 1].cpu())
+        assert_close(f"out[{n},{h}]", out[rows, h:h + 1].float().cpu().numpy(), o_ref)
+        assert_close(f"state[{n},{h}]", fin[n:n + 1, h:h + 1].cpu().numpy(), s_ref)
+
+
+def test_fused_prologue_reports_a_decay_beyond_the_chunk_range():
+    """Raw gates far above zero with no bias put every log alpha near the lower bound (-5): a
+    64-token chunk then decays by about 320 in log space, beyond the chunked prefill's range.
+    The call reports KDA_ERR_DECAY_RANGE in the device status word instead of returning silently
+    wrong results (as kda_fwd_chunked does for the same log alpha)."""
+    x = _raw([256, 70], 2, seed=44, dt_bias=False)
+    x["g_raw"] = torch.full_like(x["g_raw"], 10.0)
+    assert kda().read_device_status() == 0
+    kda().fwd_chunked_prologue(*_raw_args(x), x["cu_seqlens"], x["seqlens"], x["A_log"], None,
+                               lower_bound=LB, q_scale=QS, init_state=x["init_state"])
+    assert kda().read_device_status() == -6
+    assert kda().read_device_status() == 0  # read and cleared
