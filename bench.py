@@ -330,7 +330,6 @@ def main():
                                "peak_kind": peak_kind,
                                "traffic": recorded_traffic("kda_decode"),
                                "algorithmic_bytes_per_launch": dbytes}}
-        del dd, dout
         # speculative-decoding window: runs of 4 tokens per sequence (accepted replay, bonus,
         # draft), 2 of them committed; the state crosses HBM once each way
         run, keep = 4, 2
@@ -354,7 +353,42 @@ def main():
                             "tokens_per_s": n_dec * run * world / (wms * 1e-3),
                             "hbm_gbs": wbytes / (wms * 1e-3) / 1e9,
                             "hbm_frac": wbytes / (wms * 1e-3) / 1e9 / hbm_peak}
-        del xw, wstate, wout, wcommit
+        # the same step and window on raw projections, the input prologue fused into the kernels
+        xp = synth.make_raw_inputs([1] * n_dec, 96, seed=wd.seed, s0_std=None, device=dev)
+        xpw = synth.make_raw_inputs([run] * n_dec, 96, seed=wd.seed, s0_std=None, device=dev)
+        praw = lambda z: (z["q_raw"], z["k_raw"], z["v_raw"], z["g_raw"], z["beta_logit"])
+
+        def pstep():
+            kda.decode_step_prologue(*praw(xp), dd["state"], xp["A_log"], xp["dt_bias"], out=dout)
+
+        def pwstep():
+            kda.decode_window_prologue(*praw(xpw), xpw["cu_seqlens"], xpw["seqlens"], wstate,
+                                       xpw["A_log"], xpw["dt_bias"], commit=wcommit, out=wout)
+
+        def ustep():  # unfused: the prologue pass, then the plain step
+            q_, k_, v_, g_, b_ = kda.prologue(*praw(xp), xp["A_log"], xp["dt_bias"])
+            kda.decode_step(q_, k_, v_, g_, b_, dd["state"], out=dout)
+
+        def uwstep():
+            q_, k_, v_, g_, b_ = kda.prologue(*praw(xpw), xpw["A_log"], xpw["dt_bias"])
+            kda.decode_window(q_, k_, v_, g_, b_, xpw["cu_seqlens"], xpw["seqlens"], wstate,
+                              commit=wcommit, out=wout)
+
+        ptimes = {}
+        for name, fn in (("step", pstep), ("window", pwstep), ("step_unfused", ustep),
+                         ("window_unfused", uwstep)):
+            for _ in range(args.warmup):
+                fn()
+            barrier(world)
+            ptimes[name] = max_over_ranks(time_device(fn, args.steps, stream), world)
+        decode["prologue"] = {
+            "workload": "the same step and window on raw projections (prologue fused)",
+            "step_ms": ptimes["step"], "step_hbm_gbs": dbytes / (ptimes["step"] * 1e-3) / 1e9,
+            "window_ms": ptimes["window"],
+            "window_hbm_gbs": wbytes / (ptimes["window"] * 1e-3) / 1e9,
+            "unfused_step_ms": ptimes["step_unfused"],
+            "unfused_window_ms": ptimes["window_unfused"]}
+        del xw, wstate, wout, wcommit, xp, xpw, dd, dout
 
     # ---------------- the other prefill workloads (reported, not the headline) ------------
     extra = None

@@ -292,6 +292,27 @@ kda_status kda_fwd_chunked_prologue(const kda_desc* desc, const kda_prologue_par
                                     kda_stream_t stream);
 
 /*
+ * kda_decode_step_prologue, kda_decode_window_prologue — kda_decode_step and kda_decode_window
+ * on raw projections, with the input prologue (as for kda_prologue) fused into the decode kernels:
+ * K3's decode reads a token's projected inputs and normalises and gates them on-chip in the same
+ * kernel as the recurrence ("k3_training_and_infra_notes", section 4.5, KDA decoding).
+ *
+ * Arguments as kda_decode_step / kda_decode_window, with q_raw, k_raw, v_raw, g_raw and
+ * beta_logit in place of q, k, v, log_alpha and beta, and `prm` as for kda_prologue.  Outputs
+ * and states are bit-identical to kda_prologue followed by the plain call.  bf16 inputs only
+ * (KDA_ERR_UNSUPPORTED for fp32 inputs).
+ */
+kda_status kda_decode_step_prologue(const kda_desc* desc, const kda_prologue_params* prm,
+                                    const void* q_raw, const void* k_raw, const void* v_raw,
+                                    const void* g_raw, const void* beta_logit, float* state,
+                                    void* out, kda_stream_t stream);
+kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_params* prm,
+                                      const void* q_raw, const void* k_raw, const void* v_raw,
+                                      const void* g_raw, const void* beta_logit,
+                                      const int32_t* cu_seqlens, float* state, void* out,
+                                      const int32_t* commit, kda_stream_t stream);
+
+/*
  * kda_read_device_status — synchronise `stream`, then return and clear the sticky device
  * status word of the current device (KDA_OK when no kernel reported a problem).
  */

@@ -9,7 +9,9 @@ from . import binding  # noqa: F401
 from .binding import (  # noqa: F401
     KdaError,
     decode_step,
+    decode_step_prologue,
     decode_window,
+    decode_window_prologue,
     fwd_checkpoint_count,
     fwd_chunked,
     fwd_chunked_checkpoints,
@@ -25,7 +27,7 @@ from .binding import (  # noqa: F401
 )
 
 __all__ = [
-    "KdaError", "decode_step", "decode_window", "fwd_checkpoint_count", "fwd_chunked", "fwd_chunked_checkpoints",
+    "KdaError", "decode_step", "decode_step_prologue", "decode_window", "decode_window_prologue", "fwd_checkpoint_count", "fwd_chunked", "fwd_chunked_checkpoints",
     "fwd_chunked_host", "fwd_chunked_prologue", "fwd_workspace_bytes", "prologue",
     "launch_count",
     "library_path", "load_library", "read_device_status",

@@ -68,6 +68,12 @@ SIGNATURES = {
                                                 ctypes.POINTER(KdaPrologueParams), _P, _P, _P,
                                                 _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "kda_decode_step": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kda_decode_step_prologue": (ctypes.c_int, [ctypes.POINTER(KdaDesc),
+                                                ctypes.POINTER(KdaPrologueParams), _P, _P, _P,
+                                                _P, _P, _P, _P, _P]),
+    "kda_decode_window_prologue": (ctypes.c_int, [ctypes.POINTER(KdaDesc),
+                                                  ctypes.POINTER(KdaPrologueParams), _P, _P, _P,
+                                                  _P, _P, _P, _P, _P, _P, _P]),
     "kda_decode_window": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P,
                                          _P, _P]),
     "kda_read_device_status": (ctypes.c_int, [_P]),
@@ -506,3 +512,66 @@ def read_device_status(stream=None) -> int:
 
 def launch_count() -> int:
     return int(load_library().kda_launch_count())
+
+
+def decode_step_prologue(q_raw, k_raw, v_raw, g_raw, beta_logit, state, A_log, dt_bias=None,
+                         lower_bound: float = -5.0, q_scale: float = 128 ** -0.5, out=None,
+                         stream=None):
+    """``decode_step`` on raw projections, the input prologue fused into the kernel (arguments
+    as ``decode_step`` and ``prologue``).  Returns out [N, H, 128]."""
+    lib = load_library()
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise ValueError("decode_step_prologue needs CUDA tensors")
+    N, H, d = q_raw.shape
+    dt = q_raw.dtype
+    for name, t, shp in (("k_raw", k_raw, (N, H, d)), ("v_raw", v_raw, (N, H, d)),
+                         ("g_raw", g_raw, (N, H, d)), ("beta_logit", beta_logit, (N, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("state", state, (N, H, d, d), torch.float32, dev)
+    prm = _prologue_params(A_log, dt_bias, lower_bound, q_scale, H, d, dev)
+    if out is None:
+        out = torch.empty((N, H, d), dtype=dt, device=dev)
+    _check_io("out", out, (N, H, d), dt, dev)
+    desc = make_desc([1] * N, H, dt, d)
+    st = lib.kda_decode_step_prologue(ctypes.byref(desc), ctypes.byref(prm), _ptr(q_raw),
+                                      _ptr(k_raw), _ptr(v_raw), _ptr(g_raw), _ptr(beta_logit),
+                                      _ptr(state), _ptr(out), _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_step_prologue")
+    return out
+
+
+def decode_window_prologue(q_raw, k_raw, v_raw, g_raw, beta_logit, cu_seqlens, seqlens, state,
+                           A_log, dt_bias=None, lower_bound: float = -5.0,
+                           q_scale: float = 128 ** -0.5, commit=None, out=None,
+                           want_out: bool = True, stream=None):
+    """``decode_window`` on raw projections, the input prologue fused into the kernel
+    (arguments as ``decode_window`` and ``prologue``)."""
+    lib = load_library()
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise ValueError("decode_window_prologue needs CUDA tensors")
+    T, H, d = q_raw.shape
+    N = len(seqlens)
+    dt = q_raw.dtype
+    for name, t, shp in (("k_raw", k_raw, (T, H, d)), ("v_raw", v_raw, (T, H, d)),
+                         ("g_raw", g_raw, (T, H, d)), ("beta_logit", beta_logit, (T, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    _check_io("state", state, (N, H, d, d), torch.float32, dev)
+    if commit is not None:
+        _check_io("commit", commit, (N,), torch.int32, dev)
+    prm = _prologue_params(A_log, dt_bias, lower_bound, q_scale, H, d, dev)
+    if out is None and want_out:
+        out = torch.empty((T, H, d), dtype=dt, device=dev)
+    if out is not None:
+        _check_io("out", out, (T, H, d), dt, dev)
+    desc = make_desc(seqlens, H, dt, d)
+    st = lib.kda_decode_window_prologue(ctypes.byref(desc), ctypes.byref(prm), _ptr(q_raw),
+                                        _ptr(k_raw), _ptr(v_raw), _ptr(g_raw), _ptr(beta_logit),
+                                        _ptr(cu_seqlens), _ptr(state), _ptr(out), _ptr(commit),
+                                        _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_window_prologue")
+    return out

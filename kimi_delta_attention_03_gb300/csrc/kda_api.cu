@@ -63,6 +63,68 @@ bool check_prologue(const kda_prologue_params* prm) {
     return std::isfinite(prm->q_scale) && prm->q_scale > 0.f;
 }
 
+kda_status decode_step_impl(const kda_desc* desc, const void* q, const void* k,
+                                   const void* v, const void* log_alpha, const void* beta,
+                                   float* state, void* out, kda_stream_t stream,
+                                   const kda_prologue_params* pro) {
+    kda_status st = check_desc(desc, false);
+    if (st != KDA_OK) return st;
+    kda::ProParams pp = {};
+    if (pro) {
+        if (desc->in_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+        if (!check_prologue(pro)) return KDA_ERR_INVALID_ARG;
+        pp = {pro->A_log, pro->dt_bias, pro->lower_bound, pro->q_scale};
+    }
+    if (desc->total_tokens != desc->num_seqs) return KDA_ERR_INVALID_ARG;
+    if (desc->host_seqlens) {
+        for (int32_t n = 0; n < desc->num_seqs; ++n)
+            if (desc->host_seqlens[n] != 1) return KDA_ERR_INVALID_ARG;
+    }
+    if (!q || !k || !v || !log_alpha || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+    if (out == q || out == k || out == v || out == log_alpha || out == beta ||
+        out == (const void*)state)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state)) return KDA_ERR_INVALID_ARG;
+    int* status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    const int64_t units = (int64_t)desc->num_seqs * desc->num_heads;
+    cudaError_t e = kda::launch_decode(desc->in_dtype, units, desc->num_heads, q, k, v,
+                                       log_alpha, beta, state, out, status,
+                                       (cudaStream_t)stream, pro ? &pp : nullptr);
+    g_launches += 1;
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status decode_window_impl(const kda_desc* desc, const void* q, const void* k,
+                                     const void* v, const void* log_alpha, const void* beta,
+                                     const int32_t* cu_seqlens, float* state, void* out,
+                                     const int32_t* commit, kda_stream_t stream,
+                                     const kda_prologue_params* pro) {
+    kda_status st = check_desc(desc, true);
+    if (st != KDA_OK) return st;
+    kda::ProParams pp = {};
+    if (pro) {
+        if (desc->in_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+        if (!check_prologue(pro)) return KDA_ERR_INVALID_ARG;
+        pp = {pro->A_log, pro->dt_bias, pro->lower_bound, pro->q_scale};
+    }
+    for (int32_t n = 0; n < desc->num_seqs; ++n)
+        if (desc->host_seqlens[n] > 64) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens || !state) return KDA_ERR_INVALID_ARG;
+    if (desc->total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta)) return KDA_ERR_INVALID_ARG;
+    if (out && (out == q || out == k || out == v || out == log_alpha || out == beta ||
+                out == (const void*)state))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state)) return KDA_ERR_INVALID_ARG;
+    int* status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    cudaError_t e = kda::launch_decode_window(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k,
+                                              v, log_alpha, beta, cu_seqlens, state, out, commit,
+                                              (cudaStream_t)stream, pro ? &pp : nullptr);
+    g_launches += 1;
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -237,48 +299,32 @@ kda_status kda_prologue(const kda_desc* desc, const kda_prologue_params* prm, co
 kda_status kda_decode_step(const kda_desc* desc, const void* q, const void* k, const void* v,
                            const void* log_alpha, const void* beta, float* state, void* out,
                            kda_stream_t stream) {
-    kda_status st = check_desc(desc, false);
-    if (st != KDA_OK) return st;
-    if (desc->total_tokens != desc->num_seqs) return KDA_ERR_INVALID_ARG;
-    if (desc->host_seqlens) {
-        for (int32_t n = 0; n < desc->num_seqs; ++n)
-            if (desc->host_seqlens[n] != 1) return KDA_ERR_INVALID_ARG;
-    }
-    if (!q || !k || !v || !log_alpha || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
-    if (out == q || out == k || out == v || out == log_alpha || out == beta ||
-        out == (const void*)state)
-        return KDA_ERR_INVALID_ARG;
-    if (!aligned16(state)) return KDA_ERR_INVALID_ARG;
-    int* status = status_word();
-    if (!status) return KDA_ERR_CUDA;
-    const int64_t units = (int64_t)desc->num_seqs * desc->num_heads;
-    cudaError_t e = kda::launch_decode(desc->in_dtype, units, desc->num_heads, q, k, v,
-                                       log_alpha, beta, state, out, status,
-                                       (cudaStream_t)stream);
-    g_launches += 1;
-    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return decode_step_impl(desc, q, k, v, log_alpha, beta, state, out, stream, nullptr);
+}
+
+kda_status kda_decode_step_prologue(const kda_desc* desc, const kda_prologue_params* prm,
+                                    const void* q_raw, const void* k_raw, const void* v_raw,
+                                    const void* g_raw, const void* beta_logit, float* state,
+                                    void* out, kda_stream_t stream) {
+    if (!prm) return KDA_ERR_INVALID_ARG;
+    return decode_step_impl(desc, q_raw, k_raw, v_raw, g_raw, beta_logit, state, out, stream, prm);
 }
 
 kda_status kda_decode_window(const kda_desc* desc, const void* q, const void* k, const void* v,
                              const void* log_alpha, const void* beta, const int32_t* cu_seqlens,
                              float* state, void* out, const int32_t* commit, kda_stream_t stream) {
-    kda_status st = check_desc(desc, true);
-    if (st != KDA_OK) return st;
-    for (int32_t n = 0; n < desc->num_seqs; ++n)
-        if (desc->host_seqlens[n] > 64) return KDA_ERR_INVALID_ARG;
-    if (!cu_seqlens || !state) return KDA_ERR_INVALID_ARG;
-    if (desc->total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta)) return KDA_ERR_INVALID_ARG;
-    if (out && (out == q || out == k || out == v || out == log_alpha || out == beta ||
-                out == (const void*)state))
-        return KDA_ERR_INVALID_ARG;
-    if (!aligned16(state)) return KDA_ERR_INVALID_ARG;
-    int* status = status_word();
-    if (!status) return KDA_ERR_CUDA;
-    cudaError_t e = kda::launch_decode_window(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k,
-                                              v, log_alpha, beta, cu_seqlens, state, out, commit,
-                                              (cudaStream_t)stream);
-    g_launches += 1;
-    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return decode_window_impl(desc, q, k, v, log_alpha, beta, cu_seqlens, state, out, commit,
+                              stream, nullptr);
+}
+
+kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_params* prm,
+                                      const void* q_raw, const void* k_raw, const void* v_raw,
+                                      const void* g_raw, const void* beta_logit,
+                                      const int32_t* cu_seqlens, float* state, void* out,
+                                      const int32_t* commit, kda_stream_t stream) {
+    if (!prm) return KDA_ERR_INVALID_ARG;
+    return decode_window_impl(desc, q_raw, k_raw, v_raw, g_raw, beta_logit, cu_seqlens, state,
+                              out, commit, stream, prm);
 }
 
 kda_status kda_read_device_status(kda_stream_t stream) {

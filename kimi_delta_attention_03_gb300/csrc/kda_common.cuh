@@ -59,14 +59,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 // Launchers implemented in the kernel translation units (called by kda_api.cu).
 namespace kda {
-cudaError_t launch_decode(int dtype, int64_t units, int heads, const void* q, const void* k,
-                          const void* v, const void* g, const void* beta, float* state,
-                          void* out, int* status, cudaStream_t stream);
-
-cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void* q,
-                                 const void* k, const void* v, const void* g, const void* beta,
-                                 const int32_t* cu_seqlens, float* state, void* out,
-                                 const int32_t* commit, cudaStream_t stream);
 
 cudaError_t launch_prefill(int dtype, int num_seqs, int heads, const void* q, const void* k,
                            const void* v, const void* g, const void* beta,
@@ -112,6 +104,19 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
                               cudaStream_t stream, uint64_t* launches,
                               const int32_t* host_seqlens = nullptr, float* ckpt = nullptr,
                               int ckpt_chunks = 0, const ProParams* pro = nullptr);
+
+// Decode step and window; pro (optional, bf16 only): the inputs are raw projections and the
+// prologue runs in the kernel.
+cudaError_t launch_decode(int dtype, int64_t units, int heads, const void* q, const void* k,
+                          const void* v, const void* g, const void* beta, float* state,
+                          void* out, int* status, cudaStream_t stream,
+                          const ProParams* pro = nullptr);
+
+cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void* q,
+                                 const void* k, const void* v, const void* g, const void* beta,
+                                 const int32_t* cu_seqlens, float* state, void* out,
+                                 const int32_t* commit, cudaStream_t stream,
+                                 const ProParams* pro = nullptr);
 
 // The prologue alone over `rows` (token, head) rows, bf16 in and out.
 cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const void* k_raw,

@@ -17,19 +17,54 @@
 // so the updated state never has to be re-read.  Loads and stores are streaming (evict-first)
 // because every byte is touched once.
 #include "kda_common.cuh"
+#include "kda_prologue.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kDecodeThreads = 256;
 
-template <typename TIn>
+// The input prologue of the decode variants that take raw projections (kPro): per head rate and
+// bias of the gate, its lower bound, and the q scale (arithmetic in kda_prologue.cuh).
+struct DecPro {
+    const float* A_log;    // [H]
+    const float* dt_bias;  // [H][128] or null
+    float lb;
+    float q_scale;
+    int H;
+};
+
+// The row norms of one token.  On entry thread tid < 128 has written Swish(k_raw), Swish(q_raw)
+// of channel tid into sw_k, sw_q (fp32) and a barrier has passed.  Each of warps 0-3 forms both
+// norms itself, in the order of the standalone prologue (eight in-order FMAs per lane of a 16-lane
+// group, then the 1-2-4-8 butterfly), and writes its own 32 channels, scaled and rounded to bf16,
+// into s_k, s_q.  The caller's next barrier publishes them.
+__device__ __forceinline__ void decode_norms(const float* sw_k, const float* sw_q, float* s_k,
+                                             float* s_q, float q_scale, int tid) {
+    if (tid < kDim) {
+        const int lane = tid & 31;
+        const int cg = lane & 15;
+        const float* row = lane < 16 ? sw_k : sw_q;
+        float x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = row[8 * cg + j];
+        const float ss = row_sum_squares16(x);
+        const float inv = __fmul_rn(rsqrtf(__fadd_rn(ss, kProNormEps)), lane < 16 ? 1.f : q_scale);
+        const float ik = __shfl_sync(0xffffffffu, inv, 0);
+        const float iq = __shfl_sync(0xffffffffu, inv, 16);
+        s_k[tid] = round_bf16(__fmul_rn(sw_k[tid], ik));
+        s_q[tid] = round_bf16(__fmul_rn(sw_q[tid], iq));
+    }
+}
+
+template <typename TIn, bool kPro>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                   const TIn* __restrict__ v, const TIn* __restrict__ g,
                   const TIn* __restrict__ beta, float* __restrict__ state,
-                  TIn* __restrict__ out, int64_t units) {
+                  TIn* __restrict__ out, int64_t units, const DecPro pro) {
     __shared__ float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_u[kDim];
+    __shared__ float sw_k[kPro ? kDim : 1], sw_q[kPro ? kDim : 1];  // Swish of raw k, q
     __shared__ __align__(16) float s_rx[8][kDim];
     __shared__ __align__(16) float s_ry[8][kDim];
     __shared__ float s_kq;
@@ -45,15 +80,32 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         for (int r = 0; r < 16; ++r)
             s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
 
-        if (tid < kDim) {
-            const int64_t e = unit * kDim + tid;
-            s_k[tid] = io<TIn>::to_f(k[e]);
-            s_q[tid] = io<TIn>::to_f(q[e]);
-            s_a[tid] = expf(io<TIn>::to_f(g[e]));
-            s_v[tid] = io<TIn>::to_f(v[e]);
+        float b;
+        if constexpr (kPro) {  // raw projections: the prologue first
+            const int h = (int)(unit % pro.H);
+            if (tid < kDim) {
+                const int64_t e = unit * kDim + tid;
+                sw_k[tid] = pro_swish(io<TIn>::to_f(k[e]));
+                sw_q[tid] = pro_swish(io<TIn>::to_f(q[e]));
+                const float dt = pro.dt_bias ? pro.dt_bias[h * kDim + tid] : 0.f;
+                s_a[tid] = expf(pro_gate(io<TIn>::to_f(g[e]), dt, pro_gate_rate(pro.A_log, h), pro.lb));
+                s_v[tid] = round_bf16(pro_swish(io<TIn>::to_f(v[e])));
+            }
+            b = round_bf16(pro_sigmoid(io<TIn>::to_f(beta[unit])));
+            __syncthreads();
+            decode_norms(sw_k, sw_q, s_k, s_q, pro.q_scale, tid);
+            __syncthreads();
+        } else {
+            if (tid < kDim) {
+                const int64_t e = unit * kDim + tid;
+                s_k[tid] = io<TIn>::to_f(k[e]);
+                s_q[tid] = io<TIn>::to_f(q[e]);
+                s_a[tid] = expf(io<TIn>::to_f(g[e]));
+                s_v[tid] = io<TIn>::to_f(v[e]);
+            }
+            b = io<TIn>::to_f(beta[unit]);
+            __syncthreads();
         }
-        const float b = io<TIn>::to_f(beta[unit]);
-        __syncthreads();
 
         float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
         float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
@@ -111,14 +163,16 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 // given) from the state after the run's earlier tokens; the state after the first commit[n]
 // tokens is written back (nothing when commit[n] = 0; all of them when commit is null).  Per
 // token the arithmetic is the single-token step's, in the same order.
-template <typename TIn>
+template <typename TIn, bool kPro>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                          const TIn* __restrict__ v, const TIn* __restrict__ g,
                          const TIn* __restrict__ beta, const int32_t* __restrict__ cu_seqlens,
                          float* __restrict__ state, TIn* __restrict__ out,
-                         const int32_t* __restrict__ commit, int64_t units, int H) {
+                         const int32_t* __restrict__ commit, int64_t units, int H,
+                         const DecPro pro) {
     __shared__ float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_u[kDim];
+    __shared__ float sw_k[kPro ? kDim : 1], sw_q[kPro ? kDim : 1];  // Swish of raw k, q
     __shared__ __align__(16) float s_rx[8][kDim];
     __shared__ __align__(16) float s_ry[8][kDim];
     __shared__ float s_kq;
@@ -139,6 +193,11 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 #pragma unroll
         for (int r = 0; r < 16; ++r)
             s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
+        float pro_dt = 0.f, pro_na = 0.f;
+        if constexpr (kPro) {
+            pro_dt = pro.dt_bias && tid < kDim ? pro.dt_bias[h * kDim + tid] : 0.f;
+            pro_na = pro_gate_rate(pro.A_log, h);
+        }
 
         // The grid is persistent: the state and the token rows of this CTA's next unit are
         // pulled into L2 while this unit's tokens run, so its loads find them there.
@@ -178,15 +237,30 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 #pragma unroll 1
         for (int t = 0; t < len; ++t) {
             const int64_t row = (t0 + t) * H + h;
-            if (tid < kDim) {
-                s_k[tid] = io<TIn>::to_f(nk);
-                s_q[tid] = io<TIn>::to_f(nq);
-                s_a[tid] = expf(io<TIn>::to_f(ng));
-                s_v[tid] = io<TIn>::to_f(nv);
+            float b;
+            if constexpr (kPro) {  // raw projections: the prologue first
+                if (tid < kDim) {
+                    sw_k[tid] = pro_swish(io<TIn>::to_f(nk));
+                    sw_q[tid] = pro_swish(io<TIn>::to_f(nq));
+                    s_a[tid] = expf(pro_gate(io<TIn>::to_f(ng), pro_dt, pro_na, pro.lb));
+                    s_v[tid] = round_bf16(pro_swish(io<TIn>::to_f(nv)));
+                }
+                b = round_bf16(pro_sigmoid(io<TIn>::to_f(nb)));
+                if (t + 1 < len) fetch(t + 1);
+                __syncthreads();
+                decode_norms(sw_k, sw_q, s_k, s_q, pro.q_scale, tid);
+                __syncthreads();
+            } else {
+                if (tid < kDim) {
+                    s_k[tid] = io<TIn>::to_f(nk);
+                    s_q[tid] = io<TIn>::to_f(nq);
+                    s_a[tid] = expf(io<TIn>::to_f(ng));
+                    s_v[tid] = io<TIn>::to_f(nv);
+                }
+                b = io<TIn>::to_f(nb);
+                if (t + 1 < len) fetch(t + 1);
+                __syncthreads();
             }
-            const float b = io<TIn>::to_f(nb);
-            if (t + 1 < len) fetch(t + 1);
-            __syncthreads();
 
             float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
             float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
@@ -242,52 +316,58 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void* q,
                                  const void* k, const void* v, const void* g, const void* beta,
                                  const int32_t* cu_seqlens, float* state, void* out,
-                                 const int32_t* commit, cudaStream_t stream) {
+                                 const int32_t* commit, cudaStream_t stream, const ProParams* pro) {
     const int64_t units = (int64_t)num_seqs * heads;
     if (units <= 0) return cudaSuccess;
+    if (pro && dtype != KDA_BF16) return cudaErrorInvalidValue;
+    using T = __nv_bfloat16;
+    const DecPro dp = pro ? DecPro{pro->A_log, pro->dt_bias, pro->lower_bound, pro->q_scale, heads}
+                          : DecPro{nullptr, nullptr, 0.f, 1.f, heads};
+    auto kernel = pro ? kda_decode_window_kernel<T, true> : kda_decode_window_kernel<T, false>;
     // persistent grid: one CTA per resident slot, each taking units in strides of the grid
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err == cudaSuccess)
         err = dtype == KDA_BF16
-                  ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                        &per_sm, kda_decode_window_kernel<__nv_bfloat16>, kDecodeThreads, 0)
+                  ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kDecodeThreads, 0)
                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                        &per_sm, kda_decode_window_kernel<float>, kDecodeThreads, 0);
+                        &per_sm, kda_decode_window_kernel<float, false>, kDecodeThreads, 0);
     if (err != cudaSuccess) return err;
     const int64_t slots = (int64_t)(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
     const unsigned grid = (unsigned)(units < slots ? units : slots);
     if (dtype == KDA_BF16) {
-        using T = __nv_bfloat16;
-        kda_decode_window_kernel<T><<<grid, kDecodeThreads, 0, stream>>>(
+        kernel<<<grid, kDecodeThreads, 0, stream>>>(
             (const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta, cu_seqlens, state,
-            (T*)out, commit, units, heads);
+            (T*)out, commit, units, heads, dp);
     } else {
-        kda_decode_window_kernel<float><<<grid, kDecodeThreads, 0, stream>>>(
+        kda_decode_window_kernel<float, false><<<grid, kDecodeThreads, 0, stream>>>(
             (const float*)q, (const float*)k, (const float*)v, (const float*)g,
-            (const float*)beta, cu_seqlens, state, (float*)out, commit, units, heads);
+            (const float*)beta, cu_seqlens, state, (float*)out, commit, units, heads, dp);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_decode(int dtype, int64_t units, int heads, const void* q, const void* k,
                           const void* v, const void* g, const void* beta, float* state,
-                          void* out, int* status, cudaStream_t stream) {
-    (void)heads;
+                          void* out, int* status, cudaStream_t stream, const ProParams* pro) {
     (void)status;
     if (units <= 0) return cudaSuccess;
+    if (pro && dtype != KDA_BF16) return cudaErrorInvalidValue;
+    const DecPro dp = pro ? DecPro{pro->A_log, pro->dt_bias, pro->lower_bound, pro->q_scale, heads}
+                          : DecPro{nullptr, nullptr, 0.f, 1.f, heads};
     const int64_t max_grid = 1LL << 30;
     const unsigned grid = (unsigned)(units < max_grid ? units : max_grid);
     if (dtype == KDA_BF16) {
         using T = __nv_bfloat16;
-        kda_decode_kernel<T><<<grid, kDecodeThreads, 0, stream>>>(
+        auto kernel = pro ? kda_decode_kernel<T, true> : kda_decode_kernel<T, false>;
+        kernel<<<grid, kDecodeThreads, 0, stream>>>(
             (const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta, state, (T*)out,
-            units);
+            units, dp);
     } else {
-        kda_decode_kernel<float><<<grid, kDecodeThreads, 0, stream>>>(
+        kda_decode_kernel<float, false><<<grid, kDecodeThreads, 0, stream>>>(
             (const float*)q, (const float*)k, (const float*)v, (const float*)g,
-            (const float*)beta, state, (float*)out, units);
+            (const float*)beta, state, (float*)out, units, dp);
     }
     return cudaGetLastError();
 }

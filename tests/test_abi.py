@@ -170,6 +170,19 @@ def test_prologue_argument_checks(lib):
     assert alone(_desc([64]), p, outs=(0x2008, 0x2400, 0x2800, 0x2c00, 0x3000)) == -1  # unaligned
     assert alone(_desc([64], dtype=torch.float32), p) == -2
     assert alone(_desc([0]), p) == 0                     # nothing to do: no launch, no error
+    # decode step and window on raw projections
+    step = lambda d, pp: lib.kda_decode_step_prologue(ctypes.byref(d), pp, fake, fake, fake, fake,
+                                                       fake, P(0x3000), P(0x2000), None)
+    assert step(_desc([1, 1]), None) == -1
+    assert step(_desc([1, 1]), ctypes.byref(prm(q_scale=-1.0))) == -1
+    assert step(_desc([1, 1], dtype=torch.float32), ctypes.byref(prm())) == -2
+    win = lambda d, pp: lib.kda_decode_window_prologue(ctypes.byref(d), pp, fake, fake, fake, fake,
+                                                        fake, fake, P(0x3000), P(0x2000), None,
+                                                        None)
+    assert win(_desc([4, 5]), None) == -1
+    assert win(_desc([4, 5]), ctypes.byref(prm(lower_bound=1.0))) == -1
+    assert win(_desc([4, 5], dtype=torch.float32), ctypes.byref(prm())) == -2
+    assert win(_desc([4, 65]), ctypes.byref(prm())) == -1   # runs of at most 64 tokens
 
 
 def test_binding_refuses_cpu_tensors(lib):

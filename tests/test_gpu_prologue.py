@@ -154,3 +154,48 @@ def test_fused_prologue_reports_a_decay_beyond_the_chunk_range():
                                lower_bound=LB, q_scale=QS, init_state=x["init_state"])
     assert kda().read_device_status() == -6
     assert kda().read_device_status() == 0  # read and cleared
+
+
+# ------------------------------ decode on raw projections ------------------------------------
+def test_decode_step_prologue_equals_prologue_then_step_and_oracle():
+    N, H = 300, 4
+    x = _raw([1] * N, H, seed=45)
+    state0 = (torch.randn(N, H, 128, 128, generator=torch.Generator(device=DEV).manual_seed(45),
+                          device=DEV) * 0.02)
+    s1, s2 = state0.clone(), state0.clone()
+    o1 = kda().decode_step_prologue(*_raw_args(x), s1, x["A_log"], x["dt_bias"], lower_bound=LB,
+                                    q_scale=QS)
+    q, k, v, g, b = kda().prologue(*_raw_args(x), x["A_log"], x["dt_bias"], lower_bound=LB,
+                                   q_scale=QS)
+    o2 = kda().decode_step(q, k, v, g, b, s2)
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+    # oracle: the prologue (rounded as the contract states), then the decode step, on a sample
+    to_bf16 = lambda a: torch.from_numpy(a).to(torch.bfloat16)
+    idx = [0, 7, 150, 299]
+    ref_in = _oracle_inputs(x)
+    sel = lambda a: to_bf16(a[idx])
+    o_ref, s_ref = oracle.decode_step(*map(sel, ref_in), state0[idx].cpu())
+    assert_close("out", o1[idx].float().cpu().numpy(), o_ref)
+    assert_close("state", s1[idx].cpu().numpy(), s_ref)
+
+
+def test_decode_window_prologue_equals_prologue_then_window():
+    rng = np.random.default_rng(46)
+    N, H = 200, 4  # more units than the window kernel's persistent grid has CTAs
+    lens = rng.integers(0, 17, N).tolist()
+    lens[0], lens[1] = 64, 0
+    commit = torch.tensor([int(rng.integers(0, L + 1)) for L in lens], dtype=torch.int32,
+                          device=DEV)
+    x = _raw(lens, H, seed=46)
+    state0 = x["init_state"] * 2.0
+    s1, s2 = state0.clone(), state0.clone()
+    o1 = kda().decode_window_prologue(*_raw_args(x), x["cu_seqlens"], lens, s1, x["A_log"],
+                                      x["dt_bias"], lower_bound=LB, q_scale=QS, commit=commit)
+    q, k, v, g, b = kda().prologue(*_raw_args(x), x["A_log"], x["dt_bias"], lower_bound=LB,
+                                   q_scale=QS)
+    o2 = kda().decode_window(q, k, v, g, b, x["cu_seqlens"], lens, s2, commit=commit)
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
