@@ -16,9 +16,17 @@ What it follows:
 - beta arrives as logits and passes through a sigmoid (same page, section "FlashKDA: the
   equation, shipped as a kernel").
 
+The short convolution itself (``short_conv``, ``prologue_conv``): a causal depthwise convolution
+along each sequence's tokens with kernel size 4 and a cache of the 3 preceding raw inputs per
+channel, three caches per layer (q, k, v) ("How Kimi K3 Engineered Its Way to the Frontier",
+section "What the hybrid saves": three ShortConv caches with a kernel size of 4, 216 KiB per
+layer in bf16).
+
 Readings where the pages are silent: the L2 norm divides by sqrt(sum of squares + eps) with
 eps = 1e-6 (a zero row stays zero); q is multiplied by ``q_scale`` after normalisation (the
-pages apply no scale; callers pass 1/sqrt(128) for the usual attention scaling).
+pages apply no scale; callers pass 1/sqrt(128) for the usual attention scaling); the
+convolution has no bias, tap 3 multiplies the current token, and inputs before a sequence's first
+token come from its cache (zeros when none is given).
 
 Exported as ``oracle.prologue``.  Pinned by ``tests/test_oracle_prologue.py`` (closed forms, symmetries and invariants).
 """
@@ -80,3 +88,43 @@ def prologue(q_raw, k_raw, v_raw, g_raw, beta_logit, A_log, dt_bias=None,
     g = lower_bound_gate(g_raw, A_log, dt_bias, lower_bound)
     beta = sigmoid(beta_logit)
     return q, k, v, g, beta
+
+
+def short_conv(x, w, cu_seqlens, state=None):
+    """Causal depthwise convolution of kernel 4 along each sequence's tokens.
+
+    x: [T, H, d] (raw inputs); w: [H, d, 4], tap 3 on the current token; cu_seqlens: [N+1];
+    state: [N, 3, H, d], the 3 inputs before each sequence's first token, oldest first (None:
+    zeros).  y_t = sum_j w[:, :, j] x_{t-3+j}.  Returns (y [T, H, d], state_out [N, 3, H, d]:
+    the last 3 inputs of each sequence, continuing from ``state`` when it is shorter)."""
+    x = _f64(x)
+    w = _f64(w)
+    cu = [int(c) for c in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+    T, H, d = x.shape
+    N = len(cu) - 1
+    y = np.zeros((T, H, d))
+    state_out = np.zeros((N, 3, H, d))
+    for n in range(N):
+        a, b = cu[n], cu[n + 1]
+        prev = _f64(state[n]) if state is not None else np.zeros((3, H, d))
+        ext = np.concatenate([prev, x[a:b]], axis=0)  # ext[t + 3] is x_{a + t}
+        L = b - a
+        for j in range(4):
+            y[a:b] += w[:, :, j] * ext[j:j + L]
+        state_out[n] = ext[-3:]
+    return y, state_out
+
+
+def prologue_conv(q_raw, k_raw, v_raw, g_raw, beta_logit, A_log, dt_bias, w_q, w_k, w_v,
+                  cu_seqlens, conv_state=None, lower_bound: float = -5.0, q_scale: float = 1.0,
+                  eps: float = L2_EPS):
+    """The short convolution of q, k and v, then ``prologue``.  conv_state: [N, 3, 3, H, d]
+    (tensor q/k/v, then the 3 cached inputs oldest first) or None.  Returns (q, k, v, g, beta,
+    conv_state_out [N, 3, 3, H, d])."""
+    st = [None if conv_state is None else _f64(conv_state)[:, i] for i in range(3)]
+    qc, sq = short_conv(q_raw, w_q, cu_seqlens, st[0])
+    kc, sk = short_conv(k_raw, w_k, cu_seqlens, st[1])
+    vc, sv = short_conv(v_raw, w_v, cu_seqlens, st[2])
+    q, k, v, g, beta = prologue(qc, kc, vc, g_raw, beta_logit, A_log, dt_bias, lower_bound,
+                                q_scale, eps)
+    return q, k, v, g, beta, np.stack([sq, sk, sv], axis=1)

@@ -153,3 +153,87 @@ def test_planted_prologue_mistakes_are_caught(old, new):
         except (AssertionError, ValueError, IndexError):
             failed += 1
     assert failed > 0, f"no pin caught: {new}"
+
+
+# ------------------------------ the short convolution ----------------------------------------
+def pin_conv(P):
+    rng = np.random.default_rng(8)
+    T, H, d = 11, 2, 128
+    x = rng.standard_normal((T, H, d))
+    cu = [0, 7, 7, 11]                        # three sequences, the middle one empty
+    ident = np.zeros((H, d, 4)); ident[..., 3] = 1.0
+    y, st = P.short_conv(x, ident, cu)
+    assert np.array_equal(y, x)               # tap 3 alone is the identity
+    assert np.array_equal(st[0], x[4:7]) and np.array_equal(st[2], x[8:11])
+    assert np.all(st[1] == 0)                 # an empty sequence passes its (zero) cache through
+    delay = np.zeros((H, d, 4)); delay[..., 0] = 1.0
+    y, _ = P.short_conv(x, delay, cu)
+    assert np.array_equal(y[3:7], x[0:4]) and np.all(y[0:3] == 0)   # a 3-token delay
+    assert np.all(y[7:10] == 0) and np.array_equal(y[10], x[7])     # reset at each sequence start
+    # hand-worked taps at one asymmetric (head, channel): x_t = t + 1, w = (1, 2, 3, 4)
+    w = np.zeros((H, d, 4)); w[1, 5] = [1.0, 2.0, 3.0, 4.0]
+    xs = np.zeros((T, H, d)); xs[:, 1, 5] = np.arange(1, T + 1)
+    y, _ = P.short_conv(xs, w, [0, T])
+    assert y[5, 1, 5] == 1 * 3 + 2 * 4 + 3 * 5 + 4 * 6 and y[1, 1, 5] == 3 * 1 + 4 * 2
+    assert np.count_nonzero(y[:, 0]) == 0 and np.count_nonzero(y[:, 1, 4]) == 0
+    # two calls with the cache equal one call
+    wr = rng.standard_normal((H, d, 4))
+    y1, s1 = P.short_conv(x, wr, [0, T])
+    ya, sa = P.short_conv(x[:5], wr, [0, 5])
+    yb, sb = P.short_conv(x[5:], wr, [0, T - 5], state=sa)
+    assert np.allclose(np.concatenate([ya, yb]), y1, rtol=0, atol=1e-13) and np.array_equal(sb, s1)
+    # with a cache, the first outputs see the cached inputs: y_0 = w0 c0 + w1 c1 + w2 c2 + w3 x0
+    c = rng.standard_normal((1, 3, H, d))
+    y, _ = P.short_conv(x[:2], wr, [0, 2], state=c)
+    want = wr[..., 0] * c[0, 0] + wr[..., 1] * c[0, 1] + wr[..., 2] * c[0, 2] + wr[..., 3] * x[0]
+    assert np.allclose(y[0], want, rtol=0, atol=1e-13)
+
+
+def pin_conv_cache_size(P):
+    # three caches of the 3 inputs before the next token, 96 heads x 128 channels, bf16: the
+    # pages' 216 KiB per layer
+    x = np.zeros((4, 96, 128))
+    _, st = P.short_conv(x, np.zeros((96, 128, 4)), [0, 4])
+    assert 3 * st[0].size * 2 == 216 * 1024
+
+
+def test_conv_pins():
+    pin_conv(P_REAL)
+    pin_conv_cache_size(P_REAL)
+
+
+def test_prologue_conv_composes_conv_and_prologue():
+    rng = np.random.default_rng(9)
+    T, H, d = 9, 2, 128
+    raw = [rng.standard_normal((T, H, d)) for _ in range(4)] + [rng.standard_normal((T, H))]
+    A, dt = rng.standard_normal(H), rng.standard_normal((H, d))
+    ws = [rng.standard_normal((H, d, 4)) for _ in range(3)]
+    cs = rng.standard_normal((2, 3, 3, H, d))
+    cu = [0, 4, 9]
+    out = oracle.input_prologue.prologue_conv(*raw, A, dt, *ws, cu, cs, q_scale=0.5)
+    conv = [P_REAL.short_conv(raw[i], ws[i], cu, cs[:, i]) for i in range(3)]
+    ref = P_REAL.prologue(conv[0][0], conv[1][0], conv[2][0], raw[3], raw[4], A, dt, q_scale=0.5)
+    for a, b in zip(out[:5], ref):
+        assert np.array_equal(a, b)
+    assert np.array_equal(out[5][:, 1], conv[1][1])
+
+
+CONV_MISTAKES = [
+    ("            y[a:b] += w[:, :, j] * ext[j:j + L]", "            y[a:b] += w[:, :, 3 - j] * ext[j:j + L]"),
+    ("            y[a:b] += w[:, :, j] * ext[j:j + L]", "            y[a:b] += w[:, :, j] * ext[j + 1:j + 1 + L]"),
+    ("        state_out[n] = ext[-3:]", "        state_out[n] = ext[:3]"),
+    ("        prev = _f64(state[n]) if state is not None else np.zeros((3, H, d))",
+     "        prev = _f64(state[n]) if state is not None else (ext[-3:] if n else np.zeros((3, H, d)))"),
+]
+
+
+@pytest.mark.parametrize("old,new", CONV_MISTAKES)
+def test_planted_conv_mistakes_are_caught(old, new):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "input_prologue.py")).read()
+    assert src.count(old) == 1, old
+    mod = types.ModuleType("prologue_mutant")
+    exec(compile(src.replace(old, new), "prologue_mutant", "exec"), mod.__dict__)
+    with pytest.raises((AssertionError, ValueError, IndexError, NameError, UnboundLocalError)):
+        with np.errstate(all="ignore"):
+            pin_conv(mod)
+            pin_conv_cache_size(mod)
