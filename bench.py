@@ -460,9 +460,19 @@ def main():
             kda.fwd_chunked(q_, k_, v_, g_, b_, xr["cu_seqlens"], xr["seqlens"],
                             init_state=xr["init_state"], out=out, final_state=fin)
 
+        gen_w = torch.Generator(device=dev).manual_seed(w.seed)
+        conv_w = [torch.randn(H, D, 4, generator=gen_w, device=dev) * 0.5 for _ in range(3)]
+        conv_cache = torch.zeros(len(w.lengths), 3, 3, H, D, dtype=torch.bfloat16, device=dev)
+
+        def estep_pc():  # the short convolution and the prologue, cache updated in place
+            return kda.prologue_conv(*raw, xr["cu_seqlens"], xr["seqlens"], xr["A_log"], *conv_w,
+                                     dt_bias=xr["dt_bias"], cache_in=conv_cache,
+                                     cache_out=conv_cache)
+
         k_p = max(2, min(args.steps, 10))
         times = {}
-        for name, fn in (("fused", estep_pf), ("unfused", estep_pu), ("prologue", estep_pp)):
+        for name, fn in (("fused", estep_pf), ("unfused", estep_pu), ("prologue", estep_pp),
+                         ("prologue_conv", estep_pc)):
             for _ in range(2):
                 fn()
             times[name] = max_over_ranks(time_device(fn, k_p, stream), world)
@@ -475,8 +485,10 @@ def main():
             "fused_saving_vs_unfused": 1.0 - times["fused"] / times["unfused"],
             "overhead_vs_plain": times["fused"] / ms_max - 1.0,
             "prologue_kernel_ms": times["prologue"],
-            "prologue_kernel_hbm_frac": pro_bytes / (times["prologue"] * 1e-3) / 1e9 / hbm_peak}
-        del xr, raw
+            "prologue_kernel_hbm_frac": pro_bytes / (times["prologue"] * 1e-3) / 1e9 / hbm_peak,
+            "prologue_conv_ms": times["prologue_conv"],
+            "prologue_conv_hbm_frac": pro_bytes / (times["prologue_conv"] * 1e-3) / 1e9 / hbm_peak}
+        del xr, raw, conv_w, conv_cache
 
     # ---------------- end to end (host buffers, copies inside the timed region) ------------
     e2e = None

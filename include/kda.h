@@ -276,6 +276,43 @@ kda_status kda_prologue(const kda_desc* desc, const kda_prologue_params* prm, co
                         void* beta, kda_stream_t stream);
 
 /*
+ * kda_prologue_conv — the short convolution of q, k and v, then the prologue, as one pass.
+ *
+ * A KDA layer produces q, k and v by a short convolution followed by the prologue ("Kimi K3"
+ * (ai.thesatyajit.com), section "Kimi Delta Attention…"); the convolution is causal and
+ * depthwise with kernel size 4, and serving keeps three of its caches per request and layer
+ * ("How Kimi K3 Engineered Its Way to the Frontier", section "What the hybrid saves": 216 KiB per
+ * layer in bf16).  Per (sequence, head, channel): y_t = sum_{j=0..3} w[j] x_{t-3+j}, no bias,
+ * w[3] on the current token, inputs before the sequence's first token from the cache (zeros when
+ * cache_in is NULL); accumulated in fp32 in the order j = 0..3 and passed to the prologue
+ * unrounded.  log_alpha and beta get no convolution.
+ *
+ *   desc          as for kda_fwd_chunked (host_seqlens required); in_dtype KDA_BF16
+ *   conv->w_q, w_k, w_v   device fp32 [H, 128, 4], 16-byte aligned
+ *   conv->cache_in        device bf16 [N, 3, 3, H, 128] (tensor q/k/v, then the 3 inputs before
+ *                         each sequence, oldest first), or NULL for zeros
+ *   conv->cache_out       device bf16, same layout: each sequence's last 3 raw inputs after the
+ *                         call (continuing from cache_in when shorter), or NULL; may equal
+ *                         cache_in (updated in place)
+ *   cu_seqlens    device int32 [N+1]
+ * Other arguments and outputs as for kda_prologue.  The outputs feed kda_fwd_chunked (or the
+ * decode calls); a run split into consecutive calls with the cache carried equals one call.
+ */
+typedef struct {
+  const float* w_q;      /* device fp32 [H, 128, 4] */
+  const float* w_k;
+  const float* w_v;
+  const void* cache_in;  /* device bf16 [N, 3, 3, H, 128] or NULL */
+  void* cache_out;       /* device bf16 [N, 3, 3, H, 128] or NULL; may equal cache_in */
+} kda_conv_params;
+
+kda_status kda_prologue_conv(const kda_desc* desc, const kda_prologue_params* prm,
+                             const kda_conv_params* conv, const int32_t* cu_seqlens,
+                             const void* q_raw, const void* k_raw, const void* v_raw,
+                             const void* g_raw, const void* beta_logit, void* q, void* k, void* v,
+                             void* log_alpha, void* beta, kda_stream_t stream);
+
+/*
  * kda_fwd_chunked_prologue — kda_fwd_chunked on raw projections, with the prologue fused into
  * the prefill's load path: the transformed q, k, v, log_alpha and beta never go to HBM.
  *

@@ -50,6 +50,11 @@ class KdaPrologueParams(ctypes.Structure):
                 ("lower_bound", ctypes.c_float), ("q_scale", ctypes.c_float)]
 
 
+class KdaConvParams(ctypes.Structure):
+    _fields_ = [("w_q", ctypes.c_void_p), ("w_k", ctypes.c_void_p), ("w_v", ctypes.c_void_p),
+                ("cache_in", ctypes.c_void_p), ("cache_out", ctypes.c_void_p)]
+
+
 # exported symbol -> (restype, argtypes)
 _P = ctypes.c_void_p
 SIGNATURES = {
@@ -67,6 +72,10 @@ SIGNATURES = {
     "kda_fwd_chunked_prologue": (ctypes.c_int, [ctypes.POINTER(KdaDesc),
                                                 ctypes.POINTER(KdaPrologueParams), _P, _P, _P,
                                                 _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "kda_prologue_conv": (ctypes.c_int, [ctypes.POINTER(KdaDesc),
+                                         ctypes.POINTER(KdaPrologueParams),
+                                         ctypes.POINTER(KdaConvParams), _P, _P, _P, _P, _P, _P,
+                                         _P, _P, _P, _P, _P, _P]),
     "kda_decode_step": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P]),
     "kda_decode_step_prologue": (ctypes.c_int, [ctypes.POINTER(KdaDesc),
                                                 ctypes.POINTER(KdaPrologueParams), _P, _P, _P,
@@ -575,3 +584,42 @@ def decode_window_prologue(q_raw, k_raw, v_raw, g_raw, beta_logit, cu_seqlens, s
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_window_prologue")
     return out
+
+
+def prologue_conv(q_raw, k_raw, v_raw, g_raw, beta_logit, cu_seqlens, seqlens, A_log, w_q, w_k,
+                  w_v, dt_bias=None, cache_in=None, cache_out=None, lower_bound: float = -5.0,
+                  q_scale: float = 128 ** -0.5, stream=None):
+    """The short convolution (kernel 4) of q_raw, k_raw, v_raw, then the input prologue.
+    w_q, w_k, w_v: fp32 [H, 128, 4]; cache_in / cache_out: bf16 [N, 3, 3, H, 128] or None
+    (cache_out may be cache_in).  Returns (q, k, v, log_alpha, beta), bf16."""
+    lib = load_library()
+    dev = q_raw.device
+    if dev.type != "cuda":
+        raise ValueError("prologue_conv needs CUDA tensors")
+    T, H, d = q_raw.shape
+    N = len(seqlens)
+    dt = q_raw.dtype
+    for name, t, shp in (("k_raw", k_raw, (T, H, d)), ("v_raw", v_raw, (T, H, d)),
+                         ("g_raw", g_raw, (T, H, d)), ("beta_logit", beta_logit, (T, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    for name, w in (("w_q", w_q), ("w_k", w_k), ("w_v", w_v)):
+        _check_io(name, w, (H, d, 4), torch.float32, dev)
+    for name, c in (("cache_in", cache_in), ("cache_out", cache_out)):
+        if c is not None:
+            _check_io(name, c, (N, 3, 3, H, d), dt, dev)
+    prm = _prologue_params(A_log, dt_bias, lower_bound, q_scale, H, d, dev)
+    conv = KdaConvParams(w_q.data_ptr(), w_k.data_ptr(), w_v.data_ptr(),
+                         None if cache_in is None else cache_in.data_ptr(),
+                         None if cache_out is None else cache_out.data_ptr())
+    outs = [torch.empty((T, H, d), dtype=dt, device=dev) for _ in range(4)]
+    beta = torch.empty((T, H), dtype=dt, device=dev)
+    desc = make_desc(seqlens, H, dt, d)
+    st = lib.kda_prologue_conv(ctypes.byref(desc), ctypes.byref(prm), ctypes.byref(conv),
+                               _ptr(cu_seqlens), _ptr(q_raw), _ptr(k_raw), _ptr(v_raw),
+                               _ptr(g_raw), _ptr(beta_logit), _ptr(outs[0]), _ptr(outs[1]),
+                               _ptr(outs[2]), _ptr(outs[3]), _ptr(beta),
+                               _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prologue_conv")
+    return outs[0], outs[1], outs[2], outs[3], beta

@@ -296,6 +296,40 @@ kda_status kda_prologue(const kda_desc* desc, const kda_prologue_params* prm, co
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status kda_prologue_conv(const kda_desc* desc, const kda_prologue_params* prm,
+                             const kda_conv_params* conv, const int32_t* cu_seqlens,
+                             const void* q_raw, const void* k_raw, const void* v_raw,
+                             const void* g_raw, const void* beta_logit, void* q, void* k, void* v,
+                             void* log_alpha, void* beta, kda_stream_t stream) {
+    kda_status st = check_desc(desc, true);
+    if (st != KDA_OK) return st;
+    if (desc->in_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!check_prologue(prm) || !conv || !cu_seqlens) return KDA_ERR_INVALID_ARG;
+    if (!conv->w_q || !conv->w_k || !conv->w_v || !aligned16(conv->w_q) || !aligned16(conv->w_k) ||
+        !aligned16(conv->w_v) || !aligned16(conv->cache_in) || !aligned16(conv->cache_out))
+        return KDA_ERR_INVALID_ARG;
+    const void* in[5] = {q_raw, k_raw, v_raw, g_raw, beta_logit};
+    const void* outs[5] = {q, k, v, log_alpha, beta};
+    if (desc->total_tokens > 0) {
+        for (int i = 0; i < 5; ++i) {
+            if (!in[i] || !outs[i]) return KDA_ERR_INVALID_ARG;
+            if (i < 4 && (!aligned16(in[i]) || !aligned16(outs[i]))) return KDA_ERR_INVALID_ARG;
+            for (int j = 0; j < 5; ++j)
+                if (outs[i] == in[j] || (j != i && outs[i] == outs[j])) return KDA_ERR_INVALID_ARG;
+        }
+    }
+    const void* co = conv->cache_out;
+    for (int i = 0; i < 5; ++i)
+        if (co && (co == in[i] || co == outs[i])) return KDA_ERR_INVALID_ARG;
+    cudaError_t e = kda::launch_prologue_conv(
+        desc->total_tokens * desc->num_heads, desc->num_heads, desc->num_seqs, q_raw, k_raw, v_raw,
+        g_raw, beta_logit, prm->A_log, prm->dt_bias, prm->lower_bound, prm->q_scale, conv->w_q,
+        conv->w_k, conv->w_v, conv->cache_in, conv->cache_out, cu_seqlens, q, k, v, log_alpha,
+        beta, (cudaStream_t)stream);
+    g_launches += (desc->total_tokens > 0 ? 1 : 0) + (conv->cache_out ? 1 : 0);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status kda_decode_step(const kda_desc* desc, const void* q, const void* k, const void* v,
                            const void* log_alpha, const void* beta, float* state, void* out,
                            kda_stream_t stream) {

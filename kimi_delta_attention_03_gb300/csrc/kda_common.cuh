@@ -124,4 +124,14 @@ cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const vo
                             const float* A_log, const float* dt_bias, float lower_bound,
                             float q_scale, void* q, void* k, void* v, void* g, void* beta,
                             cudaStream_t stream);
+
+// The short convolution (kernel 4, cached) and the prologue over `rows` (token, head) rows; the
+// cache after the call is written when cache_out is given (it may equal cache_in).
+cudaError_t launch_prologue_conv(int64_t rows, int heads, int num_seqs, const void* q_raw,
+                                 const void* k_raw, const void* v_raw, const void* g_raw,
+                                 const void* beta_logit, const float* A_log, const float* dt_bias,
+                                 float lower_bound, float q_scale, const float* w_q,
+                                 const float* w_k, const float* w_v, const void* cache_in,
+                                 void* cache_out, const int32_t* cu_seqlens, void* q, void* k,
+                                 void* v, void* g, void* beta, cudaStream_t stream);
 }  // namespace kda

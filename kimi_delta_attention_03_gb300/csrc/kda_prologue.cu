@@ -113,6 +113,152 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
     }
 }
 
+// ---- the short convolution in front of the prologue ----
+// Causal depthwise convolution of kernel 4 along each sequence's tokens, y_t = sum_j w_j x_{t-3+j}
+// per (head, channel), with the 3 inputs before a sequence's first token taken from its cache
+// ("How Kimi K3 Engineered Its Way to the Frontier", section "What the hybrid saves": three
+// ShortConv caches of kernel size 4 per layer).  Cache layout: bf16 [N][3 tensors q, k, v][3
+// inputs, oldest first][H][128].  The convolution is in fp32 and feeds the prologue unrounded.
+
+// x_{tp} of `src` for one lane's channels: a raw row of the sequence, or the cache before it
+template <int kN>
+__device__ __forceinline__ void conv_tap(const bf16* __restrict__ src, const bf16* __restrict__ cache,
+                                         int64_t tp, int64_t a, int n, int tensor, int h, int H,
+                                         int ch, float (&x)[kN]) {
+    const bf16* p = nullptr;
+    if (tp >= a) p = src + (tp * H + h) * kDim + ch;
+    else if (cache) p = cache + ((((int64_t)n * 3 + tensor) * 3 + (tp - a + 3)) * H + h) * kDim + ch;
+    if (!p) {
+#pragma unroll
+        for (int i = 0; i < kN; ++i) x[i] = 0.f;
+        return;
+    }
+    if constexpr (kN == 8) {
+        unpack8_bf16(*reinterpret_cast<const uint4*>(p), x);
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        x[0] = __uint_as_float(u.x << 16); x[1] = __uint_as_float(u.x & 0xffff0000u);
+        x[2] = __uint_as_float(u.y << 16); x[3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+}
+
+// y for one lane's kN channels of token t: taps 0..3 on x_{t-3} .. x_t, accumulated in that order
+template <int kN>
+__device__ __forceinline__ void conv_row(const bf16* __restrict__ src, const bf16* __restrict__ cache,
+                                         const float* __restrict__ w, int64_t t, int64_t a, int n,
+                                         int tensor, int h, int H, int ch, float (&y)[kN]) {
+    float4 wv[kN];  // taps of each channel
+#pragma unroll
+    for (int i = 0; i < kN; ++i)
+        wv[i] = *reinterpret_cast<const float4*>(w + ((int64_t)h * kDim + ch + i) * 4);
+#pragma unroll
+    for (int i = 0; i < kN; ++i) y[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float x[kN];
+        conv_tap<kN>(src, cache, t - 3 + j, a, n, tensor, h, H, ch, x);
+#pragma unroll
+        for (int i = 0; i < kN; ++i) {
+            const float wj = j == 0 ? wv[i].x : j == 1 ? wv[i].y : j == 2 ? wv[i].z : wv[i].w;
+            y[i] = fmaf(wj, x[i], y[i]);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kProThreads)
+kda_prologue_conv_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_raw,
+                         const bf16* __restrict__ v_raw, const bf16* __restrict__ g_raw,
+                         const bf16* __restrict__ beta_logit, const float* __restrict__ A_log,
+                         const float* __restrict__ dt_bias, float lower_bound, float q_scale,
+                         const float* __restrict__ w_q, const float* __restrict__ w_k,
+                         const float* __restrict__ w_v, const bf16* __restrict__ cache,
+                         const int32_t* __restrict__ cu_seqlens, int num_seqs,
+                         bf16* __restrict__ q, bf16* __restrict__ k, bf16* __restrict__ v,
+                         bf16* __restrict__ g, bf16* __restrict__ beta, int64_t rows, int H) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (kProThreads / 32);
+    for (int64_t row = (int64_t)blockIdx.x * (kProThreads / 32) + (threadIdx.x >> 5); row < rows;
+         row += warps) {
+        const int64_t t = row / H;
+        const int h = (int)(row - t * H);
+        // the sequence of token t: the last n with cu_seqlens[n] <= t
+        int lo = 0, hi = num_seqs;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cu_seqlens[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int64_t a = cu_seqlens[lo];
+        const int64_t base = row * kDim;
+        {   // q (lanes 0-15) or k (lanes 16-31): convolution, Swish, row norm
+            const bool is_q = lane < 16;
+            const int ch = 8 * (lane & 15);
+            float y[8];
+            conv_row<8>(is_q ? q_raw : k_raw, cache, is_q ? w_q : w_k, t, a, lo, is_q ? 0 : 1, h, H,
+                        ch, y);
+            pro_swish_l2(y, is_q ? q_scale : 1.f);
+            *reinterpret_cast<uint4*>((is_q ? q : k) + base + ch) =
+                make_uint4(pack2_bf16(y[0], y[1]), pack2_bf16(y[2], y[3]), pack2_bf16(y[4], y[5]),
+                           pack2_bf16(y[6], y[7]));
+        }
+        {   // v: convolution, Swish; g: the bounded gate (no convolution)
+            const int ch = 4 * lane;
+            float y[4];
+            conv_row<4>(v_raw, cache, w_v, t, a, lo, 2, h, H, ch, y);
+            const uint2 gr = *reinterpret_cast<const uint2*>(g_raw + base + ch);
+            const float gv[4] = {__uint_as_float(gr.x << 16), __uint_as_float(gr.x & 0xffff0000u),
+                                 __uint_as_float(gr.y << 16), __uint_as_float(gr.y & 0xffff0000u)};
+            const float na = pro_gate_rate(A_log, h);
+            float dt[4] = {0.f, 0.f, 0.f, 0.f};
+            if (dt_bias) {
+                const float4 d4 = *reinterpret_cast<const float4*>(dt_bias + h * kDim + ch);
+                dt[0] = d4.x; dt[1] = d4.y; dt[2] = d4.z; dt[3] = d4.w;
+            }
+            *reinterpret_cast<uint2*>(v + base + ch) =
+                make_uint2(pack2_bf16(pro_swish(y[0]), pro_swish(y[1])),
+                           pack2_bf16(pro_swish(y[2]), pro_swish(y[3])));
+            *reinterpret_cast<uint2*>(g + base + ch) =
+                make_uint2(pack2_bf16(pro_gate(gv[0], dt[0], na, lower_bound),
+                                      pro_gate(gv[1], dt[1], na, lower_bound)),
+                           pack2_bf16(pro_gate(gv[2], dt[2], na, lower_bound),
+                                      pro_gate(gv[3], dt[3], na, lower_bound)));
+        }
+        if (lane == 0)
+            beta[row] = __float2bfloat16_rn(pro_sigmoid(__bfloat162float(beta_logit[row])));
+    }
+}
+
+// The cache after the call: each sequence's last 3 raw inputs (continuing from the cache before
+// it when the sequence is shorter).  One thread per (sequence, tensor, head, channel); it reads
+// all three values before writing, so cache_out may be cache_in.
+__global__ void kda_conv_cache_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_raw,
+                                      const bf16* __restrict__ v_raw, const bf16* cache_in,
+                                      bf16* cache_out, const int32_t* __restrict__ cu_seqlens,
+                                      int num_seqs, int H) {
+    const int64_t total = (int64_t)num_seqs * 3 * H * kDim;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(e % kDim);
+        const int64_t r1 = e / kDim;
+        const int h = (int)(r1 % H);
+        const int64_t r2 = r1 / H;
+        const int tensor = (int)(r2 % 3);
+        const int n = (int)(r2 / 3);
+        const int64_t a = cu_seqlens[n], b = cu_seqlens[n + 1];
+        const bf16* src = tensor == 0 ? q_raw : tensor == 1 ? k_raw : v_raw;
+        bf16 x[3];
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const int64_t p = b - 3 + i;
+            if (p >= a) x[i] = src[(p * H + h) * kDim + c];
+            else if (cache_in) x[i] = cache_in[((((int64_t)n * 3 + tensor) * 3 + (p - a + 3)) * H + h) * kDim + c];
+            else x[i] = __float2bfloat16_rn(0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            cache_out[((((int64_t)n * 3 + tensor) * 3 + i) * H + h) * kDim + c] = x[i];
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const void* k_raw,
@@ -137,6 +283,37 @@ cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const vo
         (const bf16*)beta_logit, A_log, dt_bias, lower_bound, q_scale, (bf16*)q, (bf16*)k,
         (bf16*)v, (bf16*)g, (bf16*)beta, rows, heads);
     return cudaGetLastError();
+}
+
+cudaError_t launch_prologue_conv(int64_t rows, int heads, int num_seqs, const void* q_raw,
+                                 const void* k_raw, const void* v_raw, const void* g_raw,
+                                 const void* beta_logit, const float* A_log, const float* dt_bias,
+                                 float lower_bound, float q_scale, const float* w_q,
+                                 const float* w_k, const float* w_v, const void* cache_in,
+                                 void* cache_out, const int32_t* cu_seqlens, void* q, void* k,
+                                 void* v, void* g, void* beta, cudaStream_t stream) {
+    if (rows > 0) {
+        const int64_t per_block = kProThreads / 32;
+        const int64_t blocks = (rows + per_block - 1) / per_block;
+        const unsigned grid = (unsigned)(blocks < (1LL << 30) ? blocks : (1LL << 30));
+        kda_prologue_conv_kernel<<<grid, kProThreads, 0, stream>>>(
+            (const bf16*)q_raw, (const bf16*)k_raw, (const bf16*)v_raw, (const bf16*)g_raw,
+            (const bf16*)beta_logit, A_log, dt_bias, lower_bound, q_scale, w_q, w_k, w_v,
+            (const bf16*)cache_in, cu_seqlens, num_seqs, (bf16*)q, (bf16*)k, (bf16*)v, (bf16*)g,
+            (bf16*)beta, rows, heads);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (cache_out) {
+        const int64_t total = (int64_t)num_seqs * 3 * heads * kDim;
+        const int64_t blocks = (total + 255) / 256;
+        const unsigned grid = (unsigned)(blocks < (1LL << 30) ? blocks : (1LL << 30));
+        kda_conv_cache_kernel<<<grid, 256, 0, stream>>>(
+            (const bf16*)q_raw, (const bf16*)k_raw, (const bf16*)v_raw, (const bf16*)cache_in,
+            (bf16*)cache_out, cu_seqlens, num_seqs, heads);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
 }
 
 }  // namespace kda

@@ -183,6 +183,21 @@ def test_prologue_argument_checks(lib):
     assert win(_desc([4, 5]), ctypes.byref(prm(lower_bound=1.0))) == -1
     assert win(_desc([4, 5], dtype=torch.float32), ctypes.byref(prm())) == -2
     assert win(_desc([4, 65]), ctypes.byref(prm())) == -1   # runs of at most 64 tokens
+    # the short convolution in front of the prologue
+    from kimi_delta_attention_03_gb300.binding import KdaConvParams
+    cv = lambda **kw: KdaConvParams(kw.get("w_q", 0x8000), 0x8400, 0x8800, kw.get("cin", None),
+                                    kw.get("cout", None))
+    conv = lambda d, pp, c: lib.kda_prologue_conv(
+        ctypes.byref(d), pp, c, P(0x9000), P(0x1000), P(0x1400), P(0x1800), P(0x1c00), P(0x1f00),
+        P(0x2000), P(0x2400), P(0x2800), P(0x2c00), P(0x3000), None)
+    assert conv(_desc([64, 3]), ctypes.byref(prm()), None) == -1              # no conv parameters
+    assert conv(_desc([64, 3]), ctypes.byref(prm()), ctypes.byref(cv(w_q=None))) == -1
+    assert conv(_desc([64, 3]), ctypes.byref(prm()), ctypes.byref(cv(w_q=0x8004))) == -1  # unaligned
+    assert conv(_desc([64, 3]), ctypes.byref(prm()), ctypes.byref(cv(cout=0x1000))) == -1  # aliases
+    assert conv(_desc([64, 3], dtype=torch.float32), ctypes.byref(prm()), ctypes.byref(cv())) == -2
+    d = _desc([64, 3])
+    d.host_seqlens = None
+    assert conv(d, ctypes.byref(prm()), ctypes.byref(cv())) == -1             # lengths required
 
 
 def test_binding_refuses_cpu_tensors(lib):

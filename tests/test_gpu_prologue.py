@@ -199,3 +199,67 @@ def test_decode_window_prologue_equals_prologue_then_window():
     torch.cuda.synchronize()
     assert kda().read_device_status() == 0
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+# ------------------------------ the short convolution ----------------------------------------
+def _conv_weights(H, seed):
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    return [torch.randn(H, 128, 4, generator=gen, device=DEV) * 0.5 for _ in range(3)]
+
+
+def test_prologue_conv_matches_oracle():
+    lens = [300, 2, 0, 65, 1]
+    H = 3
+    x = _raw(lens, H, seed=47)
+    w = _conv_weights(H, 47)
+    N = len(lens)
+    cache_in = (torch.randn(N, 3, 3, H, 128, generator=torch.Generator(device=DEV).manual_seed(7),
+                            device=DEV)).to(torch.bfloat16)
+    cache_out = torch.empty_like(cache_in)
+    outs = kda().prologue_conv(*_raw_args(x), x["cu_seqlens"], lens, x["A_log"], *w,
+                               dt_bias=x["dt_bias"], cache_in=cache_in, cache_out=cache_out,
+                               lower_bound=LB, q_scale=QS)
+    torch.cuda.synchronize()
+    ref = oracle.input_prologue.prologue_conv(
+        *_raw_args(x), x["A_log"], x["dt_bias"], *(t.cpu() for t in w), x["cu_seqlens"].cpu(),
+        cache_in.cpu(), lower_bound=LB, q_scale=QS)
+    for name, got, want in zip(("q", "k", "v", "log_alpha", "beta"), outs, ref[:5]):
+        g = got.float().cpu().numpy().astype(np.float64)
+        tol = 2.0 ** -8 * np.abs(want) * (1 + 1e-4) + 1e-7
+        if name in ("q", "k", "v"):  # plus the SFU tanh of Swish (and fp32 convolution sums)
+            tol = tol + 3e-3 * np.sqrt(np.mean(want * want, axis=-1, keepdims=True))
+        bad = np.abs(g - want) > tol
+        assert not bad.any(), f"{name}: {int(bad.sum())} elements off"
+    assert np.array_equal(cache_out.float().cpu().numpy(), ref[5])
+
+
+def test_prologue_conv_split_calls_equal_one_call():
+    """Each sequence's tokens in two calls, the cache carried in place between them, give the
+    bits of one call."""
+    lens = [130, 5, 64, 2]
+    H = 2
+    x = _raw(lens, H, seed=48)
+    w = _conv_weights(H, 48)
+    N = len(lens)
+    one = kda().prologue_conv(*_raw_args(x), x["cu_seqlens"], lens, x["A_log"], *w,
+                              dt_bias=x["dt_bias"], lower_bound=LB, q_scale=QS)
+    cu = x["cu_seqlens"].cpu().tolist()
+    first = [L // 2 for L in lens]
+    parts = ([(cu[n], cu[n] + first[n]) for n in range(N)],
+             [(cu[n] + first[n], cu[n + 1]) for n in range(N)])
+    cache = torch.zeros(N, 3, 3, H, 128, dtype=torch.bfloat16, device=DEV)
+    pieces = []
+    for rng_ in parts:
+        rows = torch.cat([torch.arange(a, b) for a, b in rng_]).to(DEV)
+        sub_lens = [b - a for a, b in rng_]
+        sub_cu = torch.tensor([0] + np.cumsum(sub_lens).tolist(), dtype=torch.int32, device=DEV)
+        raw = [t[rows].contiguous() for t in _raw_args(x)]
+        out = kda().prologue_conv(*raw, sub_cu, sub_lens, x["A_log"], *w, dt_bias=x["dt_bias"],
+                                  cache_in=cache, cache_out=cache, lower_bound=LB, q_scale=QS)
+        pieces.append((rows, out))
+    torch.cuda.synchronize()
+    for i in range(5):
+        merged = torch.empty_like(one[i])
+        for rows, out in pieces:
+            merged[rows] = out[i]
+        assert torch.equal(merged, one[i])
