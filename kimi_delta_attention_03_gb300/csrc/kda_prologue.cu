@@ -120,6 +120,8 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
 // ShortConv caches of kernel size 4 per layer).  Cache layout: bf16 [N][3 tensors q, k, v][3
 // inputs, oldest first][H][128].  The convolution is in fp32 and feeds the prologue unrounded.
 
+constexpr int kConvRun = 16;  // consecutive tokens of one head per warp
+
 // x_{tp} of `src` for one lane's channels: a raw row of the sequence, or the cache before it
 template <int kN>
 __device__ __forceinline__ void conv_tap(const bf16* __restrict__ src, const bf16* __restrict__ cache,
@@ -142,29 +144,37 @@ __device__ __forceinline__ void conv_tap(const bf16* __restrict__ src, const bf1
     }
 }
 
-// y for one lane's kN channels of token t: taps 0..3 on x_{t-3} .. x_t, accumulated in that order
+// The convolution along a run of tokens for one lane's kN channels of one tensor: the window
+// x_{t-3} .. x_t slides one token per step (refilled from the cache or zeros at each sequence
+// start); the taps are re-read each step from L1 (the run keeps them there), and taps 0..3
+// accumulate in that order.
 template <int kN>
-__device__ __forceinline__ void conv_row(const bf16* __restrict__ src, const bf16* __restrict__ cache,
-                                         const float* __restrict__ w, int64_t t, int64_t a, int n,
-                                         int tensor, int h, int H, int ch, float (&y)[kN]) {
-    float4 wv[kN];  // taps of each channel
+struct ConvLane {
+    const float* wp;   // taps of the lane's first channel: [kN][4]
+    float win[3][kN];  // x_{t-3}, x_{t-2}, x_{t-1}
+    __device__ __forceinline__ void fill(const bf16* __restrict__ src, const bf16* __restrict__ cache,
+                                         int64_t t, int64_t a, int n, int tensor, int h, int H,
+                                         int ch) {
 #pragma unroll
-    for (int i = 0; i < kN; ++i)
-        wv[i] = *reinterpret_cast<const float4*>(w + ((int64_t)h * kDim + ch + i) * 4);
-#pragma unroll
-    for (int i = 0; i < kN; ++i) y[i] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float x[kN];
-        conv_tap<kN>(src, cache, t - 3 + j, a, n, tensor, h, H, ch, x);
+        for (int j = 0; j < 3; ++j) conv_tap<kN>(src, cache, t - 3 + j, a, n, tensor, h, H, ch, win[j]);
+    }
+    __device__ __forceinline__ void step(const float (&x)[kN], float (&y)[kN]) {
 #pragma unroll
         for (int i = 0; i < kN; ++i) {
-            const float wj = j == 0 ? wv[i].x : j == 1 ? wv[i].y : j == 2 ? wv[i].z : wv[i].w;
-            y[i] = fmaf(wj, x[i], y[i]);
+            const float4 w = __ldg(reinterpret_cast<const float4*>(wp) + i);
+            float acc = 0.f;
+            acc = fmaf(w.x, win[0][i], acc);
+            acc = fmaf(w.y, win[1][i], acc);
+            acc = fmaf(w.z, win[2][i], acc);
+            y[i] = fmaf(w.w, x[i], acc);
+            win[0][i] = win[1][i];
+            win[1][i] = win[2][i];
+            win[2][i] = x[i];
         }
     }
-}
+};
 
+// One warp per (head, run of kConvRun consecutive tokens); runs may cross sequence boundaries.
 __global__ void __launch_bounds__(kProThreads)
 kda_prologue_conv_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_raw,
                          const bf16* __restrict__ v_raw, const bf16* __restrict__ g_raw,
@@ -174,56 +184,85 @@ kda_prologue_conv_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict_
                          const float* __restrict__ w_v, const bf16* __restrict__ cache,
                          const int32_t* __restrict__ cu_seqlens, int num_seqs,
                          bf16* __restrict__ q, bf16* __restrict__ k, bf16* __restrict__ v,
-                         bf16* __restrict__ g, bf16* __restrict__ beta, int64_t rows, int H) {
+                         bf16* __restrict__ g, bf16* __restrict__ beta, int64_t T, int H) {
     const int lane = threadIdx.x & 31;
+    const bool is_q = lane < 16;  // lanes 0-15: q channels; lanes 16-31: k channels
+    const int chqk = 8 * (lane & 15), chv = 4 * lane;
+    const int64_t runs = (T + kConvRun - 1) / kConvRun;
+    const int64_t items = runs * H;
     const int64_t warps = (int64_t)gridDim.x * (kProThreads / 32);
-    for (int64_t row = (int64_t)blockIdx.x * (kProThreads / 32) + (threadIdx.x >> 5); row < rows;
-         row += warps) {
-        const int64_t t = row / H;
-        const int h = (int)(row - t * H);
-        // the sequence of token t: the last n with cu_seqlens[n] <= t
+    for (int64_t item = (int64_t)blockIdx.x * (kProThreads / 32) + (threadIdx.x >> 5); item < items;
+         item += warps) {
+        const int h = (int)(item % H);
+        const int64_t t0 = (item / H) * kConvRun;
+        const int64_t t1 = t0 + kConvRun < T ? t0 + kConvRun : T;
+        // the sequence of token t0: the last n with cu_seqlens[n] <= t0
         int lo = 0, hi = num_seqs;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (cu_seqlens[mid] <= t) lo = mid; else hi = mid;
+            if (cu_seqlens[mid] <= t0) lo = mid; else hi = mid;
         }
-        const int64_t a = cu_seqlens[lo];
-        const int64_t base = row * kDim;
-        {   // q (lanes 0-15) or k (lanes 16-31): convolution, Swish, row norm
-            const bool is_q = lane < 16;
-            const int ch = 8 * (lane & 15);
-            float y[8];
-            conv_row<8>(is_q ? q_raw : k_raw, cache, is_q ? w_q : w_k, t, a, lo, is_q ? 0 : 1, h, H,
-                        ch, y);
+        int n = lo;
+        int64_t a = cu_seqlens[n], b = cu_seqlens[n + 1];
+        ConvLane<8> cqk;
+        ConvLane<4> cv;
+        cqk.wp = (is_q ? w_q : w_k) + ((int64_t)h * kDim + chqk) * 4;
+        cv.wp = w_v + ((int64_t)h * kDim + chv) * 4;
+        const bf16* src_qk = is_q ? q_raw : k_raw;
+        cqk.fill(src_qk, cache, t0, a, n, is_q ? 0 : 1, h, H, chqk);
+        cv.fill(v_raw, cache, t0, a, n, 2, h, H, chv);
+        const float na = pro_gate_rate(A_log, h);
+        float dt[4] = {0.f, 0.f, 0.f, 0.f};
+        if (dt_bias) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dt_bias + h * kDim + chv);
+            dt[0] = d4.x; dt[1] = d4.y; dt[2] = d4.z; dt[3] = d4.w;
+        }
+        // this token's raw inputs, loaded one token ahead
+        auto fetch = [&](int64_t t, uint4& qk, uint2& vr, uint2& gr) {
+            const int64_t base = (t * H + h) * kDim;
+            qk = __ldcs(reinterpret_cast<const uint4*>(src_qk + base + chqk));
+            vr = __ldcs(reinterpret_cast<const uint2*>(v_raw + base + chv));
+            gr = __ldcs(reinterpret_cast<const uint2*>(g_raw + base + chv));
+        };
+        uint4 nqk;
+        uint2 nvr, ngr;
+        fetch(t0, nqk, nvr, ngr);
+#pragma unroll 1
+        for (int64_t t = t0; t < t1; ++t) {
+            const uint4 cqk_raw = nqk;
+            const uint2 vr = nvr, gr = ngr;
+            if (t + 1 < t1) fetch(t + 1, nqk, nvr, ngr);
+            if (t >= b) {  // a new sequence starts at t (skipping empty ones): refill the window
+                do { ++n; a = cu_seqlens[n]; b = cu_seqlens[n + 1]; } while (t >= b);
+                cqk.fill(src_qk, cache, t, a, n, is_q ? 0 : 1, h, H, chqk);
+                cv.fill(v_raw, cache, t, a, n, 2, h, H, chv);
+            }
+            const int64_t base = (t * H + h) * kDim;
+            float xqk[8], xv[4];
+            unpack8_bf16(cqk_raw, xqk);
+            xv[0] = __uint_as_float(vr.x << 16); xv[1] = __uint_as_float(vr.x & 0xffff0000u);
+            xv[2] = __uint_as_float(vr.y << 16); xv[3] = __uint_as_float(vr.y & 0xffff0000u);
+            float y[8], yv[4];
+            cqk.step(xqk, y);
+            cv.step(xv, yv);
             pro_swish_l2(y, is_q ? q_scale : 1.f);
-            *reinterpret_cast<uint4*>((is_q ? q : k) + base + ch) =
+            *reinterpret_cast<uint4*>((is_q ? q : k) + base + chqk) =
                 make_uint4(pack2_bf16(y[0], y[1]), pack2_bf16(y[2], y[3]), pack2_bf16(y[4], y[5]),
                            pack2_bf16(y[6], y[7]));
-        }
-        {   // v: convolution, Swish; g: the bounded gate (no convolution)
-            const int ch = 4 * lane;
-            float y[4];
-            conv_row<4>(v_raw, cache, w_v, t, a, lo, 2, h, H, ch, y);
-            const uint2 gr = *reinterpret_cast<const uint2*>(g_raw + base + ch);
             const float gv[4] = {__uint_as_float(gr.x << 16), __uint_as_float(gr.x & 0xffff0000u),
                                  __uint_as_float(gr.y << 16), __uint_as_float(gr.y & 0xffff0000u)};
-            const float na = pro_gate_rate(A_log, h);
-            float dt[4] = {0.f, 0.f, 0.f, 0.f};
-            if (dt_bias) {
-                const float4 d4 = *reinterpret_cast<const float4*>(dt_bias + h * kDim + ch);
-                dt[0] = d4.x; dt[1] = d4.y; dt[2] = d4.z; dt[3] = d4.w;
-            }
-            *reinterpret_cast<uint2*>(v + base + ch) =
-                make_uint2(pack2_bf16(pro_swish(y[0]), pro_swish(y[1])),
-                           pack2_bf16(pro_swish(y[2]), pro_swish(y[3])));
-            *reinterpret_cast<uint2*>(g + base + ch) =
+            *reinterpret_cast<uint2*>(v + base + chv) =
+                make_uint2(pack2_bf16(pro_swish(yv[0]), pro_swish(yv[1])),
+                           pack2_bf16(pro_swish(yv[2]), pro_swish(yv[3])));
+            *reinterpret_cast<uint2*>(g + base + chv) =
                 make_uint2(pack2_bf16(pro_gate(gv[0], dt[0], na, lower_bound),
                                       pro_gate(gv[1], dt[1], na, lower_bound)),
                            pack2_bf16(pro_gate(gv[2], dt[2], na, lower_bound),
                                       pro_gate(gv[3], dt[3], na, lower_bound)));
+            if (lane == 0)
+                beta[t * H + h] =
+                    __float2bfloat16_rn(pro_sigmoid(__bfloat162float(beta_logit[t * H + h])));
         }
-        if (lane == 0)
-            beta[row] = __float2bfloat16_rn(pro_sigmoid(__bfloat162float(beta_logit[row])));
     }
 }
 
@@ -294,13 +333,15 @@ cudaError_t launch_prologue_conv(int64_t rows, int heads, int num_seqs, const vo
                                  void* v, void* g, void* beta, cudaStream_t stream) {
     if (rows > 0) {
         const int64_t per_block = kProThreads / 32;
-        const int64_t blocks = (rows + per_block - 1) / per_block;
+        const int64_t T = rows / heads;
+        const int64_t items = (T + kConvRun - 1) / kConvRun * heads;
+        const int64_t blocks = (items + per_block - 1) / per_block;
         const unsigned grid = (unsigned)(blocks < (1LL << 30) ? blocks : (1LL << 30));
         kda_prologue_conv_kernel<<<grid, kProThreads, 0, stream>>>(
             (const bf16*)q_raw, (const bf16*)k_raw, (const bf16*)v_raw, (const bf16*)g_raw,
             (const bf16*)beta_logit, A_log, dt_bias, lower_bound, q_scale, w_q, w_k, w_v,
             (const bf16*)cache_in, cu_seqlens, num_seqs, (bf16*)q, (bf16*)k, (bf16*)v, (bf16*)g,
-            (bf16*)beta, rows, heads);
+            (bf16*)beta, T, heads);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
