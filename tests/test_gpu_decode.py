@@ -191,3 +191,30 @@ def test_decode_window_many_units_equals_token_steps():
     assert kda().read_device_status() == 0
     assert torch.equal(out, ref_out)
     assert torch.equal(state, committed)
+
+
+def test_decode_window_fp32_inputs_match_oracle():
+    """The window kernel's fp32-input instantiation: ragged runs, partial commits."""
+    lens = [3, 0, 9, 1, 20]
+    commit = [2, 0, 9, 0, 11]
+    H = 2
+    x = synth.make_inputs(lens, H, torch.float32, seed=35, device=DEV)
+    x["init_state"] = x["init_state"] * 2.0
+    state = x["init_state"].clone()
+    out = kda().decode_window(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                              lens, state,
+                              commit=torch.tensor(commit, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    assert out.dtype == torch.float32
+    o_ref, _ = oracle.recurrence(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), x["log_alpha"].cpu(),
+                                 x["beta"].cpu(), x["cu_seqlens"].cpu(),
+                                 state_in=x["init_state"].cpu(), want_state=False)
+    assert_close("out", out.cpu().numpy(), o_ref)
+    cu = x["cu_seqlens"].cpu().tolist()
+    rows = [torch.arange(cu[n], cu[n] + commit[n]) for n in range(len(lens))]
+    pick = lambda t: torch.cat([t.cpu()[r] for r in rows])
+    cu2 = np.concatenate([[0], np.cumsum(commit)]).astype(np.int32)
+    _, s_ref = oracle.recurrence(pick(x["q"]), pick(x["k"]), pick(x["v"]), pick(x["log_alpha"]),
+                                 pick(x["beta"]), cu2, state_in=x["init_state"].cpu(),
+                                 want_out=False)
+    assert_close("state", state.cpu().numpy(), s_ref)
