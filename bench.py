@@ -296,7 +296,7 @@ def main():
     t_tc = alg_flops / (tc_peak * 1e12)
     roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved_gbs / hbm_peak, "peak_kind": peak_kind,
-                "traffic": recorded_traffic("kda_prefill"),
+                "traffic": recorded_traffic("kda_prefill") if args.case == "full" else None,
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "tensor_achieved_tflops": achieved_tf, "tensor_peak_tflops": tc_peak,
                 "tensor_frac": achieved_tf / tc_peak,
@@ -328,7 +328,8 @@ def main():
                   "roofline": {"bound": "hbm", "achieved": dgbs, "peak": hbm_peak,
                                "unit": "GB/s", "frac": dgbs / hbm_peak,
                                "peak_kind": peak_kind,
-                               "traffic": recorded_traffic("kda_decode"),
+                               "traffic": (recorded_traffic("kda_decode")
+                                           if args.case == "full" else None),
                                "algorithmic_bytes_per_launch": dbytes}}
         # speculative-decoding window: runs of 4 tokens per sequence (accepted replay, bonus,
         # draft), 2 of them committed; the state crosses HBM once each way
