@@ -298,13 +298,16 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
             __syncthreads();
 
             const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
-            const bool store = (t + 1 == ncommit);
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 const float kk = s_k[warp + 8 * r];
                 s[r].x = fmaf(kk, u4.x, s[r].x); s[r].y = fmaf(kk, u4.y, s[r].y);
                 s[r].z = fmaf(kk, u4.z, s[r].z); s[r].w = fmaf(kk, u4.w, s[r].w);
-                if (store) __stcs(reinterpret_cast<float4*>(S + (warp + 8 * r) * kDim) + lane, s[r]);
+            }
+            if (t + 1 == ncommit) {  // uniform: the state stores issue only on the commit token
+#pragma unroll
+                for (int r = 0; r < 16; ++r)
+                    __stcs(reinterpret_cast<float4*>(S + (warp + 8 * r) * kDim) + lane, s[r]);
             }
             __syncthreads();  // shared vectors are rewritten by the next token
         }
