@@ -350,6 +350,16 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
                                       const int32_t* commit, kda_stream_t stream);
 
 /*
+ * kda_selftest_wait_timeout — diagnostic: launch one CTA that waits, through the kernels' own
+ * bounded-wait code, on a barrier phase nothing completes.  The wait gives up after its limit
+ * (about 2 s) and records KDA_ERR_TIMEOUT in the sticky status word, which
+ * kda_read_device_status() then returns; the context stays usable.  Every wait of the compute
+ * kernels is bounded the same way, so a lost arrival (a defect, or a fault elsewhere) ends as a
+ * status code rather than a hang.  Returns KDA_OK once launched.
+ */
+kda_status kda_selftest_wait_timeout(kda_stream_t stream);
+
+/*
  * kda_read_device_status — synchronise `stream`, then return and clear the sticky device
  * status word of the current device (KDA_OK when no kernel reported a problem).
  */

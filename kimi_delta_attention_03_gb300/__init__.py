@@ -25,11 +25,12 @@ from .binding import (  # noqa: F401
     prologue,
     prologue_conv,
     read_device_status,
+    selftest_wait_timeout,
 )
 
 __all__ = [
     "KdaError", "decode_step", "decode_step_prologue", "decode_window", "decode_window_prologue", "fwd_checkpoint_count", "fwd_chunked", "fwd_chunked_checkpoints",
     "fwd_chunked_host", "fwd_chunked_prologue", "fwd_workspace_bytes", "prologue", "prologue_conv",
     "launch_count",
-    "library_path", "load_library", "read_device_status",
+    "library_path", "load_library", "read_device_status", "selftest_wait_timeout",
 ]

@@ -86,6 +86,7 @@ SIGNATURES = {
     "kda_decode_window": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P,
                                          _P, _P]),
     "kda_read_device_status": (ctypes.c_int, [_P]),
+    "kda_selftest_wait_timeout": (ctypes.c_int, [_P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kda_launch_count": (ctypes.c_uint64, []),
     "kda_version": (ctypes.c_int32, []),
@@ -623,3 +624,15 @@ def prologue_conv(q_raw, k_raw, v_raw, g_raw, beta_logit, cu_seqlens, seqlens, A
     if st != KDA_OK:
         raise KdaError(st, "kda_prologue_conv")
     return outs[0], outs[1], outs[2], outs[3], beta
+
+
+def selftest_wait_timeout(stream=None, device=None) -> int:
+    """Launch the bounded-wait self-test (one CTA whose wait runs out after about 2 s) and
+    return the device status it leaves (KDA_ERR_TIMEOUT, -5, when the bound works)."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    h = _stream_handle(stream, dev)
+    st = lib.kda_selftest_wait_timeout(h)
+    if st != KDA_OK:
+        raise KdaError(st, "kda_selftest_wait_timeout")
+    return int(lib.kda_read_device_status(h))

@@ -361,6 +361,14 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
                               out, commit, stream, prm);
 }
 
+kda_status kda_selftest_wait_timeout(kda_stream_t stream) {
+    int* status = status_word();
+    if (!status) return KDA_ERR_CUDA;
+    cudaError_t e = kda::launch_wait_selftest(status, (cudaStream_t)stream);
+    g_launches += 1;
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status kda_read_device_status(kda_stream_t stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KDA_ERR_CUDA;
     int* p = status_word();

@@ -125,6 +125,9 @@ cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const vo
                             float q_scale, void* q, void* k, void* v, void* g, void* beta,
                             cudaStream_t stream);
 
+// One CTA whose bounded wait runs out: the status word then reads KDA_ERR_TIMEOUT.
+cudaError_t launch_wait_selftest(int* status, cudaStream_t stream);
+
 // The short convolution (kernel 4, cached) and the prologue over `rows` (token, head) rows; the
 // cache after the call is written when cache_out is given (it may equal cache_in).
 cudaError_t launch_prologue_conv(int64_t rows, int heads, int num_seqs, const void* q_raw,

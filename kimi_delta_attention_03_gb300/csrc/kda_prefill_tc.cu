@@ -373,6 +373,23 @@ __device__ __noinline__ bool decay_scan_pro(unsigned char* sm, int cs, int L, in
     return decay_scan_body<true>(sm, cs, L, te, abort_flag, status, dt, a, lb);
 }
 
+// Self-test of the bounded waits: one CTA waits, through the kernels' own helper, on a barrier
+// phase that nothing completes.  After kWaitLimit cycles (about 2 s) the wait gives up, records
+// KDA_ERR_TIMEOUT in the status word and returns; the CTA holds no TMEM and issues no copies or
+// MMAs, so it exits cleanly and the context stays usable.
+__global__ void kda_wait_selftest_kernel(int* status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (wait_bar(&bar, 0, &abort_flag, status) && threadIdx.x == 0)
+        report_status(status, KDA_ERR_INVALID_ARG);  // the phase cannot complete: never reached
+}
+
 // kCkpt: the variant that also writes state checkpoints; kPro: the variant that takes raw
 // projections and runs the input prologue on the tiles as they arrive (the plain kernel carries
 // no trace of either).
@@ -1373,6 +1390,11 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
     kernel<<<dim3((unsigned)units, 1, ws.max_segments), kThreadsTC, SMEM_ALLOC, stream>>>(
         mq, mk, mv, mg, prm, order);
     if (launches) ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int* status, cudaStream_t stream) {
+    kda_wait_selftest_kernel<<<1, 32, 0, stream>>>(status);
     return cudaGetLastError();
 }
 
