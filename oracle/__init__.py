@@ -12,8 +12,11 @@ state".  This module only builds the shared object with gcc and marshals arrays 
 The input prologue (raw projections -> q, k, v, g, beta) is plain numpy fp64 in
 ``input_prologue.py``, exported here as ``prologue``.
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` and
-``tests/test_oracle_prologue.py``; there is no unpinned entry.
+The gradients of the recurrence (``recurrence_backward``) come from reverse-mode automatic
+differentiation of the same token loop written in torch float64 (``backward.py``).
+
+Every function here is pinned by ``tests/test_oracle_pins.py``, ``tests/test_oracle_prologue.py``
+and ``tests/test_oracle_backward.py``; there is no unpinned entry.
 """
 from __future__ import annotations
 
@@ -25,6 +28,7 @@ import threading
 import numpy as np
 
 from .input_prologue import prologue  # noqa: F401  (re-exported)
+from .backward import recurrence_backward  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kda_oracle.c")
