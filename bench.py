@@ -11,6 +11,7 @@ on the host cores, on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import csv
 import hashlib
 import io
@@ -490,6 +491,29 @@ def main():
             "prologue_conv_ms": times["prologue_conv"],
             "prologue_conv_hbm_frac": pro_bytes / (times["prologue_conv"] * 1e-3) / 1e9 / hbm_peak}
         del xr, raw, conv_w, conv_cache
+
+    # ---------------- backward (gradients) on the headline workload ----------------
+    if not args.no_extra:
+        gen_b = torch.Generator(device=dev).manual_seed(w.seed)
+        d_out = torch.randn(T, H, D, generator=gen_b, device=dev)
+        bws = torch.empty(max(16, kda.binding.load_library().kda_bwd_workspace_bytes(
+            ctypes.byref(kda.binding.make_desc(x["seqlens"], H, x["q"].dtype)))),
+            dtype=torch.uint8, device=dev)
+
+        def bstep():
+            return kda.bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                           x["seqlens"], d_out, init_state=x["init_state"], workspace=bws)
+
+        bstep()
+        ms_b = max_over_ranks(time_device(bstep, 2, stream), world)
+        # the gradient outputs are fp32: 5 x 512 B + 4 B per token-head, plus the inputs and
+        # d_out read (1,026 + 512 B) and 2 x 64 KiB of states per unit
+        extra["backward_4x8k"] = {
+            "workload": w.name + ": gradients of q, k, v, log alpha, beta and the initial state",
+            "tokens": T, "ms_per_step": ms_b, "steps": 2,
+            "value": T * world / (ms_b * 1e-3) / 1e6, "unit": "Mtokens/s",
+            "workspace_bytes": int(bws.numel())}
+        del d_out, bws
 
     # ---------------- end to end (host buffers, copies inside the timed region) ------------
     e2e = None

@@ -350,6 +350,33 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
                                       const int32_t* commit, kda_stream_t stream);
 
 /*
+ * kda_bwd — gradients of the recurrence (the backward pass) for training.
+ *
+ * For the forward of kda_fwd_chunked (the token loop of "How Kimi K3 Engineered Its Way to the
+ * Frontier", section "How KDA updates its state") and the gradient d_out of a loss with respect to
+ * every output (and optionally d_state with respect to the final states), returns the gradients
+ * with respect to q, k, v, log_alpha, beta and the initial states.  Reverse mode through the token
+ * loop on CUDA cores, fp32, with the states recomputed from every 16th one kept in the workspace:
+ * correct for any gate the forward accepts (no chunk exponent range applies), not tuned for speed.
+ *
+ *   desc          as for kda_fwd_chunked (host_seqlens required); q, k, v, log_alpha, beta of
+ *                 desc->in_dtype, layouts as there
+ *   init_state    device fp32 [N, H, 128, 128] or NULL (zeros)
+ *   d_out         device fp32 [T, H, 128]
+ *   d_state       device fp32 [N, H, 128, 128] or NULL (no loss on the final states)
+ *   dq, dk, dv, dlog_alpha   device fp32 [T, H, 128]; dbeta device fp32 [T, H];
+ *   dinit_state   device fp32 [N, H, 128, 128]
+ *   workspace     device, at least kda_bwd_workspace_bytes(desc) bytes, 16-byte aligned
+ * Outputs must not alias inputs or each other.
+ */
+size_t kda_bwd_workspace_bytes(const kda_desc* desc);
+kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const void* v,
+                   const void* log_alpha, const void* beta, const float* init_state,
+                   const int32_t* cu_seqlens, const float* d_out, const float* d_state, float* dq,
+                   float* dk, float* dv, float* dlog_alpha, float* dbeta, float* dinit_state,
+                   void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
  * kda_selftest_wait_timeout — diagnostic: launch one CTA that waits, through the kernels' own
  * bounded-wait code, on a barrier phase nothing completes.  The wait gives up after its limit
  * (about 2 s) and records KDA_ERR_TIMEOUT in the sticky status word, which

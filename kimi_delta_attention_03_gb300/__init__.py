@@ -8,6 +8,7 @@ The library is loaded lazily on first use and its absence is an error, never a f
 from . import binding  # noqa: F401
 from .binding import (  # noqa: F401
     KdaError,
+    bwd,
     decode_step,
     decode_step_prologue,
     decode_window,
@@ -29,7 +30,7 @@ from .binding import (  # noqa: F401
 )
 
 __all__ = [
-    "KdaError", "decode_step", "decode_step_prologue", "decode_window", "decode_window_prologue", "fwd_checkpoint_count", "fwd_chunked", "fwd_chunked_checkpoints",
+    "KdaError", "bwd", "decode_step", "decode_step_prologue", "decode_window", "decode_window_prologue", "fwd_checkpoint_count", "fwd_chunked", "fwd_chunked_checkpoints",
     "fwd_chunked_host", "fwd_chunked_prologue", "fwd_workspace_bytes", "prologue", "prologue_conv",
     "launch_count",
     "library_path", "load_library", "read_device_status", "selftest_wait_timeout",

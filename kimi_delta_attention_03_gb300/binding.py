@@ -87,6 +87,9 @@ SIGNATURES = {
                                          _P, _P]),
     "kda_read_device_status": (ctypes.c_int, [_P]),
     "kda_selftest_wait_timeout": (ctypes.c_int, [_P]),
+    "kda_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(KdaDesc)]),
+    "kda_bwd": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                               _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "kda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "kda_launch_count": (ctypes.c_uint64, []),
     "kda_version": (ctypes.c_int32, []),
@@ -636,3 +639,40 @@ def selftest_wait_timeout(stream=None, device=None) -> int:
     if st != KDA_OK:
         raise KdaError(st, "kda_selftest_wait_timeout")
     return int(lib.kda_read_device_status(h))
+
+
+def bwd(q, k, v, log_alpha, beta, cu_seqlens, seqlens, d_out, init_state=None, d_state=None,
+        workspace=None, stream=None):
+    """Gradients of the recurrence: given d_out (fp32 [T, H, 128], the gradient of a loss with
+    respect to the outputs) and optionally d_state (fp32 [N, H, 128, 128], with respect to the
+    final states), returns (dq, dk, dv, dlog_alpha, dbeta, dinit_state), fp32."""
+    lib = load_library()
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("bwd needs CUDA tensors")
+    T, H, d = q.shape
+    N = len(seqlens)
+    dt = q.dtype
+    for name, t, shp in (("k", k, (T, H, d)), ("v", v, (T, H, d)),
+                         ("log_alpha", log_alpha, (T, H, d)), ("beta", beta, (T, H))):
+        _check_io(name, t, shp, dt, dev)
+    _check_io("cu_seqlens", cu_seqlens, (N + 1,), torch.int32, dev)
+    _check_io("d_out", d_out, (T, H, d), torch.float32, dev)
+    for name, t in (("init_state", init_state), ("d_state", d_state)):
+        if t is not None:
+            _check_io(name, t, (N, H, d, d), torch.float32, dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq, dk, dv, dg = (torch.empty((T, H, d), **f32) for _ in range(4))
+    dbeta = torch.empty((T, H), **f32)
+    dinit = torch.empty((N, H, d, d), **f32)
+    desc = make_desc(seqlens, H, dt, d)
+    need = int(lib.kda_bwd_workspace_bytes(ctypes.byref(desc)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    st = lib.kda_bwd(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                     _ptr(init_state), _ptr(cu_seqlens), _ptr(d_out), _ptr(d_state), _ptr(dq),
+                     _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dinit), _ptr(workspace),
+                     workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_bwd")
+    return dq, dk, dv, dg, dbeta, dinit

@@ -361,6 +361,53 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
                               out, commit, stream, prm);
 }
 
+size_t kda_bwd_workspace_bytes(const kda_desc* desc) {
+    if (check_desc(desc, true) != KDA_OK) return 0;
+    int64_t nb_max = 0;
+    for (int32_t n = 0; n < desc->num_seqs; ++n)
+        nb_max = std::max<int64_t>(nb_max, (desc->host_seqlens[n] + 15) / 16);
+    const int64_t per_unit = (nb_max + 16) * 128 * 128;
+    return (size_t)per_unit * desc->num_seqs * desc->num_heads * sizeof(float);
+}
+
+kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const void* v,
+                   const void* log_alpha, const void* beta, const float* init_state,
+                   const int32_t* cu_seqlens, const float* d_out, const float* d_state, float* dq,
+                   float* dk, float* dv, float* dlog_alpha, float* dbeta, float* dinit_state,
+                   void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    kda_status st = check_desc(desc, true);
+    if (st != KDA_OK) return st;
+    if (!cu_seqlens || !dinit_state) return KDA_ERR_INVALID_ARG;
+    const void* in[9] = {q, k, v, log_alpha, beta, init_state, d_out, d_state, cu_seqlens};
+    const void* outs[6] = {dq, dk, dv, dlog_alpha, dbeta, dinit_state};
+    if (desc->total_tokens > 0) {
+        for (int i = 0; i < 7; ++i)
+            if (i != 5 && !in[i]) return KDA_ERR_INVALID_ARG;
+        for (int i = 0; i < 5; ++i)
+            if (!outs[i]) return KDA_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < 6; ++i) {
+        if (outs[i] && !aligned16(outs[i])) return KDA_ERR_INVALID_ARG;
+        for (int j = 0; j < 9; ++j)
+            if (outs[i] && outs[i] == in[j]) return KDA_ERR_INVALID_ARG;
+        for (int j = 0; j < i; ++j)
+            if (outs[i] && outs[i] == outs[j]) return KDA_ERR_INVALID_ARG;
+    }
+    if (!aligned16(init_state) || !aligned16(d_state) || !aligned16(d_out))
+        return KDA_ERR_INVALID_ARG;
+    const size_t need = kda_bwd_workspace_bytes(desc);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+    int64_t nb_max = 0;
+    for (int32_t n = 0; n < desc->num_seqs; ++n)
+        nb_max = std::max<int64_t>(nb_max, (desc->host_seqlens[n] + 15) / 16);
+    cudaError_t e = kda::launch_backward(
+        desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v, log_alpha, beta, cu_seqlens,
+        init_state, d_out, d_state, dq, dk, dv, dlog_alpha, dbeta, dinit_state,
+        static_cast<float*>(workspace), (nb_max + 16) * 128 * 128, (cudaStream_t)stream);
+    g_launches += 1;
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status kda_selftest_wait_timeout(kda_stream_t stream) {
     int* status = status_word();
     if (!status) return KDA_ERR_CUDA;

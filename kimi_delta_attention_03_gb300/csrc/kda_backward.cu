@@ -1,0 +1,256 @@
+// kda_backward.cu — gradients of the KDA recurrence (the backward pass), on CUDA cores.
+//
+// Forward, per (sequence, head) unit and token t ("How Kimi K3 Engineered Its Way to the Frontier",
+// section "How KDA updates its state"):
+//     S' = diag(a_t) S,  a_t = exp(g_t);   r = v_t - S'^T k_t;   u = beta_t r;
+//     S  <- S' + k_t u^T;                  o_t = S^T q_t
+// Reverse mode, given dS (the gradient of the state after token t, carried backwards) and do_t:
+//     dS += q_t do_t^T;     dq_t = S_t do_t = S' do_t + k_t (u . do_t)
+//     du = dS^T k_t;        dv_t = beta_t du;      dbeta_t = du . r
+//     dk_t = dS u - beta_t S' du
+//     dS' = dS - beta_t k_t du^T;   dg_t = rowsum(dS' * S');   dS <- diag(a_t) dS'
+// and the gradient of the initial state is dS after the first token.
+//
+// One CTA of 256 threads per unit; thread (warp w, lane l) holds rows {w + 8 r : r < 16} and
+// columns 4l .. 4l+3 of S', and of dS, in registers (the decode step's layout).  A forward sweep
+// stores the state before every 16-token block into the caller's workspace; the reverse sweep
+// recomputes each block's states from its stored start (keeping the 16 of them in the workspace)
+// and walks the block backwards.  Column sums go through shared memory, row sums through warp
+// shuffles.  fp32 throughout.  This is a correctness-first kernel: it reads and writes 128 KB of
+// workspace per token and unit, against the forward's chunked tensor-core path.
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kBwdThreads = 256;
+constexpr int kBwdBlock = 16;  // tokens per stored state
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+template <typename TIn>
+struct BwdArgs {
+    const TIn *q, *k, *v, *g, *beta;
+    const int32_t* cu_seqlens;
+    const float* init_state;  // [N][H][128][128] or null
+    const float* d_out;       // [T][H][128]
+    const float* d_state;     // [N][H][128][128] or null
+    float *dq, *dk, *dv, *dg, *dbeta, *d_init;
+    float* work;              // per unit: (nb_max + kBwdBlock) states of 128 x 128
+    int64_t work_per_unit;    // floats
+    int H;
+};
+
+template <typename TIn>
+__global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<TIn> p) {
+    __shared__ float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_do[kDim];
+    __shared__ float s_u[kDim], s_r[kDim], s_du[kDim];
+    __shared__ __align__(16) float s_part[8][kDim];
+    __shared__ float s_ud;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t unit = blockIdx.x;
+    const int n = (int)(unit / p.H), h = (int)(unit - (int64_t)n * p.H);
+    const int64_t t0 = p.cu_seqlens[n];
+    const int L = (int)(p.cu_seqlens[n + 1] - t0);
+    const int nb = (L + kBwdBlock - 1) / kBwdBlock;
+    float* ck = p.work + unit * p.work_per_unit;      // [nb][128 * 128]: state before block b
+    float* blk = ck + (int64_t)nb * kDim * kDim;     // [kBwdBlock][128 * 128]: within a block
+    const int64_t sbase = unit * (int64_t)(kDim * kDim);
+
+    auto ld_state = [&](const float* src, float4 (&x)[16]) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            x[r] = src ? reinterpret_cast<const float4*>(src + (warp + 8 * r) * kDim)[lane]
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto st_state = [&](float* dst, const float4 (&x)[16]) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) reinterpret_cast<float4*>(dst + (warp + 8 * r) * kDim)[lane] = x[r];
+    };
+    // token t's inputs into shared memory (k, q, a = exp(g), v, and d_out when asked)
+    auto stage = [&](int t, bool with_grad) -> float {
+        const int64_t row = (t0 + t) * p.H + h;
+        if (tid < kDim) {
+            const int64_t e = row * kDim + tid;
+            s_k[tid] = io<TIn>::to_f(p.k[e]);
+            s_q[tid] = io<TIn>::to_f(p.q[e]);
+            s_a[tid] = expf(io<TIn>::to_f(p.g[e]));
+            s_v[tid] = io<TIn>::to_f(p.v[e]);
+            if (with_grad) s_do[tid] = p.d_out[e];
+        }
+        return io<TIn>::to_f(p.beta[row]);
+    };
+    // S' = diag(a) S in place, and the per-warp partial column sums of k_i S'_ij into s_part
+    auto decay_and_x = [&](float4 (&S)[16]) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const int i = warp + 8 * r;
+            const float a = s_a[i], kk = s_k[i];
+            S[r].x *= a; S[r].y *= a; S[r].z *= a; S[r].w *= a;
+            x.x = fmaf(kk, S[r].x, x.x); x.y = fmaf(kk, S[r].y, x.y);
+            x.z = fmaf(kk, S[r].z, x.z); x.w = fmaf(kk, S[r].w, x.w);
+        }
+        reinterpret_cast<float4*>(s_part[warp])[lane] = x;
+    };
+    // r = v - S'^T k and u = beta r into s_r, s_u (threads < 128)
+    auto make_u = [&](float b) {
+        if (tid < kDim) {
+            float x = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) x += s_part[w][tid];
+            const float r = s_v[tid] - x;
+            s_r[tid] = r;
+            s_u[tid] = b * r;
+        }
+    };
+    // one forward token: S <- diag(a) S + k u^T
+    auto fwd_step = [&](int t, float4 (&S)[16]) {
+        const float b = stage(t, false);
+        __syncthreads();
+        decay_and_x(S);
+        __syncthreads();
+        make_u(b);
+        __syncthreads();
+        const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float kk = s_k[warp + 8 * r];
+            S[r].x = fmaf(kk, u4.x, S[r].x); S[r].y = fmaf(kk, u4.y, S[r].y);
+            S[r].z = fmaf(kk, u4.z, S[r].z); S[r].w = fmaf(kk, u4.w, S[r].w);
+        }
+        __syncthreads();  // the shared vectors are rewritten by the next token
+    };
+
+    float4 S[16], dS[16];
+    // ---- forward sweep: the state before every block
+    ld_state(p.init_state ? p.init_state + sbase : nullptr, S);
+#pragma unroll 1
+    for (int b = 0; b < nb; ++b) {
+        st_state(ck + (int64_t)b * kDim * kDim, S);
+        const int te = min(L, (b + 1) * kBwdBlock);
+#pragma unroll 1
+        for (int t = b * kBwdBlock; t < te; ++t) fwd_step(t, S);
+    }
+    // ---- reverse sweep
+    ld_state(p.d_state ? p.d_state + sbase : nullptr, dS);
+#pragma unroll 1
+    for (int b = nb - 1; b >= 0; --b) {
+        const int tb = b * kBwdBlock, te = min(L, tb + kBwdBlock);
+        __syncthreads();  // this block's stored states are rewritten below
+        ld_state(ck + (int64_t)b * kDim * kDim, S);
+#pragma unroll 1
+        for (int t = tb; t < te; ++t) {
+            st_state(blk + (int64_t)(t - tb) * kDim * kDim, S);
+            fwd_step(t, S);
+        }
+#pragma unroll 1
+        for (int t = te - 1; t >= tb; --t) {
+            const int64_t row = (t0 + t) * p.H + h;
+            ld_state(blk + (int64_t)(t - tb) * kDim * kDim, S);  // the state before token t
+            const float b_t = stage(t, true);
+            __syncthreads();
+            decay_and_x(S);  // S is now S'
+            __syncthreads();
+            make_u(b_t);
+            __syncthreads();
+            // dS += q do^T; partial column sums of k_i dS_ij; u . do
+            {
+                const float4 do4 = reinterpret_cast<const float4*>(s_do)[lane];
+                float4 dup = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const int i = warp + 8 * r;
+                    const float qq = s_q[i], kk = s_k[i];
+                    dS[r].x = fmaf(qq, do4.x, dS[r].x); dS[r].y = fmaf(qq, do4.y, dS[r].y);
+                    dS[r].z = fmaf(qq, do4.z, dS[r].z); dS[r].w = fmaf(qq, do4.w, dS[r].w);
+                    dup.x = fmaf(kk, dS[r].x, dup.x); dup.y = fmaf(kk, dS[r].y, dup.y);
+                    dup.z = fmaf(kk, dS[r].z, dup.z); dup.w = fmaf(kk, dS[r].w, dup.w);
+                }
+                reinterpret_cast<float4*>(s_part[warp])[lane] = dup;
+                if (warp == 0) {
+                    const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
+                    const float ud = warp_sum(u4.x * do4.x + u4.y * do4.y + u4.z * do4.z + u4.w * do4.w);
+                    if (lane == 0) s_ud = ud;
+                }
+            }
+            __syncthreads();
+            if (tid < kDim) {  // du = dS^T k; dv = beta du
+                float du = 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) du += s_part[w][tid];
+                s_du[tid] = du;
+                p.dv[row * kDim + tid] = b_t * du;
+            }
+            __syncthreads();
+            {
+                const float4 du4 = reinterpret_cast<const float4*>(s_du)[lane];
+                const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
+                const float4 do4 = reinterpret_cast<const float4*>(s_do)[lane];
+                const float ud = s_ud;
+                if (warp == 0) {  // dbeta = du . r
+                    const float4 r4 = reinterpret_cast<const float4*>(s_r)[lane];
+                    const float db = warp_sum(du4.x * r4.x + du4.y * r4.y + du4.z * r4.z + du4.w * r4.w);
+                    if (lane == 0) p.dbeta[row] = db;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const int i = warp + 8 * r;
+                    const float kk = s_k[i], a = s_a[i];
+                    // dq_i = (S' do)_i + k_i (u . do); dk_i = (dS u)_i - beta (S' du)_i
+                    float pq = S[r].x * do4.x + S[r].y * do4.y + S[r].z * do4.z + S[r].w * do4.w;
+                    float pk = dS[r].x * u4.x + dS[r].y * u4.y + dS[r].z * u4.z + dS[r].w * u4.w -
+                               b_t * (S[r].x * du4.x + S[r].y * du4.y + S[r].z * du4.z + S[r].w * du4.w);
+                    // dS' = dS - beta k du^T; dg_i = rowsum(dS' * S'); dS <- diag(a) dS'
+                    const float bk = b_t * kk;
+                    dS[r].x = fmaf(-bk, du4.x, dS[r].x); dS[r].y = fmaf(-bk, du4.y, dS[r].y);
+                    dS[r].z = fmaf(-bk, du4.z, dS[r].z); dS[r].w = fmaf(-bk, du4.w, dS[r].w);
+                    float pg = dS[r].x * S[r].x + dS[r].y * S[r].y + dS[r].z * S[r].z + dS[r].w * S[r].w;
+                    dS[r].x *= a; dS[r].y *= a; dS[r].z *= a; dS[r].w *= a;
+                    pq = warp_sum(pq);
+                    pk = warp_sum(pk);
+                    pg = warp_sum(pg);
+                    if (lane == 0) {
+                        p.dq[row * kDim + i] = fmaf(kk, ud, pq);
+                        p.dk[row * kDim + i] = pk;
+                        p.dg[row * kDim + i] = pg;
+                    }
+                }
+            }
+            __syncthreads();  // the shared vectors are rewritten by the previous token
+        }
+    }
+    st_state(p.d_init + sbase, dS);
+}
+
+}  // namespace
+
+cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, const void* k,
+                            const void* v, const void* g, const void* beta,
+                            const int32_t* cu_seqlens, const float* init_state,
+                            const float* d_out, const float* d_state, float* dq, float* dk,
+                            float* dv, float* dg, float* dbeta, float* d_init, float* work,
+                            int64_t work_per_unit, cudaStream_t stream) {
+    const int64_t units = (int64_t)num_seqs * heads;
+    if (units <= 0) return cudaSuccess;
+    if (dtype == KDA_BF16) {
+        using T = __nv_bfloat16;
+        const BwdArgs<T> a{(const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta,
+                           cu_seqlens, init_state, d_out, d_state, dq, dk, dv, dg, dbeta, d_init,
+                           work, work_per_unit, heads};
+        kda_bwd_kernel<T><<<(unsigned)units, kBwdThreads, 0, stream>>>(a);
+    } else {
+        const BwdArgs<float> a{(const float*)q, (const float*)k, (const float*)v, (const float*)g,
+                               (const float*)beta, cu_seqlens, init_state, d_out, d_state, dq,
+                               dk, dv, dg, dbeta, d_init, work, work_per_unit, heads};
+        kda_bwd_kernel<float><<<(unsigned)units, kBwdThreads, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

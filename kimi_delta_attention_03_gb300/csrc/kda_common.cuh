@@ -125,6 +125,15 @@ cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const vo
                             float q_scale, void* q, void* k, void* v, void* g, void* beta,
                             cudaStream_t stream);
 
+// Gradients of the recurrence: one CTA per (sequence, head); work holds work_per_unit floats per
+// unit ((blocks of 16 tokens in the longest sequence + 16) states of 128 x 128).
+cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, const void* k,
+                            const void* v, const void* g, const void* beta,
+                            const int32_t* cu_seqlens, const float* init_state,
+                            const float* d_out, const float* d_state, float* dq, float* dk,
+                            float* dv, float* dg, float* dbeta, float* d_init, float* work,
+                            int64_t work_per_unit, cudaStream_t stream);
+
 // One CTA whose bounded wait runs out: the status word then reads KDA_ERR_TIMEOUT.
 cudaError_t launch_wait_selftest(int* status, cudaStream_t stream);
 
