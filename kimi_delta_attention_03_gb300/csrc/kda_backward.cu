@@ -32,6 +32,27 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+// Sixteen row sums across the warp at once (a reduce-scatter): halving exchanges over lane bits
+// 0..3 leave each lane one partial of one row, and a last exchange over bit 4 completes it.  Lane
+// l (and l + 16) ends with the sum for row index bitreverse4(l & 15).  16 shuffles instead of 80.
+__device__ __forceinline__ float warp_sum16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        const int half = 8 >> s;                 // values kept after this step
+        const bool upper = (lane >> s) & 1;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << s);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+__device__ __forceinline__ int bitrev4(int x) {
+    return ((x & 1) << 3) | ((x & 2) << 1) | ((x & 4) >> 1) | ((x & 8) >> 3);
+}
+
 template <typename TIn>
 struct BwdArgs {
     const TIn *q, *k, *v, *g, *beta;
@@ -198,28 +219,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
                     const float db = warp_sum(du4.x * r4.x + du4.y * r4.y + du4.z * r4.z + du4.w * r4.w);
                     if (lane == 0) p.dbeta[row] = db;
                 }
+                // row sums in three passes of 16 (one per gradient), each a warp reduce-scatter
+                const int rr = bitrev4(lane & 15);  // the row (of this warp's 16) this lane ends with
+                float part[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const int i = warp + 8 * r;
-                    const float kk = s_k[i], a = s_a[i];
-                    // dq_i = (S' do)_i + k_i (u . do); dk_i = (dS u)_i - beta (S' du)_i
-                    float pq = S[r].x * do4.x + S[r].y * do4.y + S[r].z * do4.z + S[r].w * do4.w;
-                    float pk = dS[r].x * u4.x + dS[r].y * u4.y + dS[r].z * u4.z + dS[r].w * u4.w -
-                               b_t * (S[r].x * du4.x + S[r].y * du4.y + S[r].z * du4.z + S[r].w * du4.w);
-                    // dS' = dS - beta k du^T; dg_i = rowsum(dS' * S'); dS <- diag(a) dS'
-                    const float bk = b_t * kk;
+                for (int r = 0; r < 16; ++r)  // dq_i = (S' do)_i + k_i (u . do)
+                    part[r] = S[r].x * do4.x + S[r].y * do4.y + S[r].z * do4.z + S[r].w * do4.w;
+                {
+                    const float sum = warp_sum16(part, lane);
+                    const int i = warp + 8 * rr;
+                    if (lane < 16) p.dq[row * kDim + i] = fmaf(s_k[i], ud, sum);
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r)  // dk_i = (dS u)_i - beta (S' du)_i
+                    part[r] = dS[r].x * u4.x + dS[r].y * u4.y + dS[r].z * u4.z + dS[r].w * u4.w -
+                              b_t * (S[r].x * du4.x + S[r].y * du4.y + S[r].z * du4.z + S[r].w * du4.w);
+                {
+                    const float sum = warp_sum16(part, lane);
+                    if (lane < 16) p.dk[row * kDim + warp + 8 * rr] = sum;
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {  // dS' = dS - beta k du^T; dg_i = rowsum(dS' * S')
+                    const float bk = b_t * s_k[warp + 8 * r];
                     dS[r].x = fmaf(-bk, du4.x, dS[r].x); dS[r].y = fmaf(-bk, du4.y, dS[r].y);
                     dS[r].z = fmaf(-bk, du4.z, dS[r].z); dS[r].w = fmaf(-bk, du4.w, dS[r].w);
-                    float pg = dS[r].x * S[r].x + dS[r].y * S[r].y + dS[r].z * S[r].z + dS[r].w * S[r].w;
+                    part[r] = dS[r].x * S[r].x + dS[r].y * S[r].y + dS[r].z * S[r].z + dS[r].w * S[r].w;
+                    const float a = s_a[warp + 8 * r];  // dS <- diag(a) dS'
                     dS[r].x *= a; dS[r].y *= a; dS[r].z *= a; dS[r].w *= a;
-                    pq = warp_sum(pq);
-                    pk = warp_sum(pk);
-                    pg = warp_sum(pg);
-                    if (lane == 0) {
-                        p.dq[row * kDim + i] = fmaf(kk, ud, pq);
-                        p.dk[row * kDim + i] = pk;
-                        p.dg[row * kDim + i] = pg;
-                    }
+                }
+                {
+                    const float sum = warp_sum16(part, lane);
+                    if (lane < 16) p.dg[row * kDim + warp + 8 * rr] = sum;
                 }
             }
             __syncthreads();  // the shared vectors are rewritten by the previous token
