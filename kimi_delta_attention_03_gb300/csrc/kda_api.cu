@@ -361,13 +361,18 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
                               out, commit, stream, prm);
 }
 
-size_t kda_bwd_workspace_bytes(const kda_desc* desc) {
-    if (check_desc(desc, true) != KDA_OK) return 0;
+// Backward workspace per (sequence, head), in floats: one state per 16 tokens of the longest
+// sequence, the 16 decayed states of the block being reversed, and their 16 (u, r) vector pairs.
+static int64_t bwd_floats_per_unit(const kda_desc* desc) {
     int64_t nb_max = 0;
     for (int32_t n = 0; n < desc->num_seqs; ++n)
         nb_max = std::max<int64_t>(nb_max, (desc->host_seqlens[n] + 15) / 16);
-    const int64_t per_unit = (nb_max + 16) * 128 * 128;
-    return (size_t)per_unit * desc->num_seqs * desc->num_heads * sizeof(float);
+    return (nb_max + 16) * 128 * 128 + 16 * 2 * 128;
+}
+
+size_t kda_bwd_workspace_bytes(const kda_desc* desc) {
+    if (check_desc(desc, true) != KDA_OK) return 0;
+    return (size_t)bwd_floats_per_unit(desc) * desc->num_seqs * desc->num_heads * sizeof(float);
 }
 
 kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const void* v,
@@ -397,13 +402,10 @@ kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const voi
         return KDA_ERR_INVALID_ARG;
     const size_t need = kda_bwd_workspace_bytes(desc);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
-    int64_t nb_max = 0;
-    for (int32_t n = 0; n < desc->num_seqs; ++n)
-        nb_max = std::max<int64_t>(nb_max, (desc->host_seqlens[n] + 15) / 16);
     cudaError_t e = kda::launch_backward(
         desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v, log_alpha, beta, cu_seqlens,
         init_state, d_out, d_state, dq, dk, dv, dlog_alpha, dbeta, dinit_state,
-        static_cast<float*>(workspace), (nb_max + 16) * 128 * 128, (cudaStream_t)stream);
+        static_cast<float*>(workspace), bwd_floats_per_unit(desc), (cudaStream_t)stream);
     g_launches += 1;
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -61,7 +61,8 @@ struct BwdArgs {
     const float* d_out;       // [T][H][128]
     const float* d_state;     // [N][H][128][128] or null
     float *dq, *dk, *dv, *dg, *dbeta, *d_init;
-    float* work;              // per unit: (nb_max + kBwdBlock) states of 128 x 128
+    float* work;              // per unit: (nb_max + kBwdBlock) states of 128 x 128, then
+                              // kBwdBlock pairs of 128-vectors (u, r)
     int64_t work_per_unit;    // floats
     int H;
 };
@@ -80,7 +81,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
     const int L = (int)(p.cu_seqlens[n + 1] - t0);
     const int nb = (L + kBwdBlock - 1) / kBwdBlock;
     float* ck = p.work + unit * p.work_per_unit;      // [nb][128 * 128]: state before block b
-    float* blk = ck + (int64_t)nb * kDim * kDim;     // [kBwdBlock][128 * 128]: within a block
+    float* blk = ck + (int64_t)nb * kDim * kDim;     // [kBwdBlock][128 * 128]: S' within a block
+    float* blk_ur = p.work + unit * p.work_per_unit + p.work_per_unit - kBwdBlock * 2 * kDim;
     const int64_t sbase = unit * (int64_t)(kDim * kDim);
 
     auto ld_state = [&](const float* src, float4 (&x)[16]) {
@@ -93,16 +95,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
 #pragma unroll
         for (int r = 0; r < 16; ++r) reinterpret_cast<float4*>(dst + (warp + 8 * r) * kDim)[lane] = x[r];
     };
-    // token t's inputs into shared memory (k, q, a = exp(g), v, and d_out when asked)
-    auto stage = [&](int t, bool with_grad) -> float {
+    // token t's inputs into shared memory: k, a = exp(g) and v for a forward step; k, a, q,
+    // d_out and the stored (u, r) for a reverse step (ur non-null)
+    auto stage = [&](int t, const float* ur) -> float {
         const int64_t row = (t0 + t) * p.H + h;
         if (tid < kDim) {
             const int64_t e = row * kDim + tid;
             s_k[tid] = io<TIn>::to_f(p.k[e]);
-            s_q[tid] = io<TIn>::to_f(p.q[e]);
             s_a[tid] = expf(io<TIn>::to_f(p.g[e]));
-            s_v[tid] = io<TIn>::to_f(p.v[e]);
-            if (with_grad) s_do[tid] = p.d_out[e];
+            if (ur) {
+                s_q[tid] = io<TIn>::to_f(p.q[e]);
+                s_do[tid] = p.d_out[e];
+                s_u[tid] = ur[tid];
+                s_r[tid] = ur[kDim + tid];
+            } else {
+                s_v[tid] = io<TIn>::to_f(p.v[e]);
+            }
         }
         return io<TIn>::to_f(p.beta[row]);
     };
@@ -119,8 +127,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
         }
         reinterpret_cast<float4*>(s_part[warp])[lane] = x;
     };
-    // r = v - S'^T k and u = beta r into s_r, s_u (threads < 128)
-    auto make_u = [&](float b) {
+    // r = v - S'^T k and u = beta r into s_r, s_u (threads < 128), and into keep_ur when given
+    auto make_u = [&](float b, float* keep_ur) {
         if (tid < kDim) {
             float x = 0.f;
 #pragma unroll
@@ -128,15 +136,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
             const float r = s_v[tid] - x;
             s_r[tid] = r;
             s_u[tid] = b * r;
+            if (keep_ur) {
+                keep_ur[tid] = b * r;
+                keep_ur[kDim + tid] = r;
+            }
         }
     };
-    // one forward token: S <- diag(a) S + k u^T
-    auto fwd_step = [&](int t, float4 (&S)[16]) {
-        const float b = stage(t, false);
+    // one forward token: S <- diag(a) S + k u^T; keeps S' = diag(a) S and (u, r) when asked
+    auto fwd_step = [&](int t, float4 (&S)[16], float* keep_s, float* keep_ur) {
+        const float b = stage(t, nullptr);
         __syncthreads();
         decay_and_x(S);
+        if (keep_s) st_state(keep_s, S);
         __syncthreads();
-        make_u(b);
+        make_u(b, keep_ur);
         __syncthreads();
         const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
 #pragma unroll
@@ -156,7 +169,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
         st_state(ck + (int64_t)b * kDim * kDim, S);
         const int te = min(L, (b + 1) * kBwdBlock);
 #pragma unroll 1
-        for (int t = b * kBwdBlock; t < te; ++t) fwd_step(t, S);
+        for (int t = b * kBwdBlock; t < te; ++t) fwd_step(t, S, nullptr, nullptr);
     }
     // ---- reverse sweep
     ld_state(p.d_state ? p.d_state + sbase : nullptr, dS);
@@ -166,19 +179,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
         __syncthreads();  // this block's stored states are rewritten below
         ld_state(ck + (int64_t)b * kDim * kDim, S);
 #pragma unroll 1
-        for (int t = tb; t < te; ++t) {
-            st_state(blk + (int64_t)(t - tb) * kDim * kDim, S);
-            fwd_step(t, S);
-        }
+        for (int t = tb; t < te; ++t)
+            fwd_step(t, S, blk + (int64_t)(t - tb) * kDim * kDim, blk_ur + (t - tb) * 2 * kDim);
 #pragma unroll 1
         for (int t = te - 1; t >= tb; --t) {
             const int64_t row = (t0 + t) * p.H + h;
-            ld_state(blk + (int64_t)(t - tb) * kDim * kDim, S);  // the state before token t
-            const float b_t = stage(t, true);
-            __syncthreads();
-            decay_and_x(S);  // S is now S'
-            __syncthreads();
-            make_u(b_t);
+            ld_state(blk + (int64_t)(t - tb) * kDim * kDim, S);  // S' = diag(a_t) S_{t-1}
+            const float b_t = stage(t, blk_ur + (t - tb) * 2 * kDim);
             __syncthreads();
             // dS += q do^T; partial column sums of k_i dS_ij; u . do
             {
