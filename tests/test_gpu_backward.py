@@ -44,3 +44,22 @@ def test_backward_matches_oracle(dtype, with_init, with_dstate):
     # the empty sequence passes the final-state gradient straight through
     want = d_state[1] if d_state is not None else torch.zeros_like(got[5][1])
     assert torch.equal(got[5][1], want)
+
+
+def test_backward_long_sequence():
+    """2048 tokens cross 128 recompute blocks (the state at every 16th token kept, the rest
+    replayed); a second sequence of 17 tokens ends on a one-token block."""
+    lens, H = [2048, 17], 1
+    x = synth.make_inputs(lens, H, torch.bfloat16, seed=73, device=DEV)
+    gen = torch.Generator(device=DEV).manual_seed(74)
+    d_out = torch.randn(sum(lens), H, 128, generator=gen, device=DEV)
+    d_state = torch.randn(len(lens), H, 128, 128, generator=gen, device=DEV) * 0.1
+    got = kda().bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                    x["seqlens"], d_out, init_state=x["init_state"], d_state=d_state)
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    ref = oracle.recurrence_backward(
+        x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), x["log_alpha"].cpu(), x["beta"].cpu(),
+        x["cu_seqlens"].cpu(), d_out.cpu(), state_in=x["init_state"].cpu(), d_state=d_state.cpu())
+    for name, g, r in zip(NAMES, got, ref):
+        assert_close(name, g.cpu().numpy(), r)
