@@ -95,24 +95,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
 #pragma unroll
         for (int r = 0; r < 16; ++r) reinterpret_cast<float4*>(dst + (warp + 8 * r) * kDim)[lane] = x[r];
     };
-    // token t's inputs into shared memory: k, a = exp(g) and v for a forward step; k, a, q,
-    // d_out and the stored (u, r) for a reverse step (ur non-null)
-    auto stage = [&](int t, const float* ur) -> float {
+    // One token's inputs, held raw in registers from their load to their staging, so that the next
+    // token's loads are in flight while this one computes: k, g and v for a forward step; k, g,
+    // q, d_out and the stored (u, r) for a reverse step (ur non-null).  Threads >= 128 load beta only.
+    struct Tok {
+        TIn k, g, v, q, b;
+        float d, u, r;
+    };
+    auto fetch = [&](int t, const float* ur) -> Tok {
+        Tok x;
         const int64_t row = (t0 + t) * p.H + h;
+        x.b = p.beta[row];
         if (tid < kDim) {
             const int64_t e = row * kDim + tid;
-            s_k[tid] = io<TIn>::to_f(p.k[e]);
-            s_a[tid] = expf(io<TIn>::to_f(p.g[e]));
+            x.k = p.k[e];
+            x.g = p.g[e];
             if (ur) {
-                s_q[tid] = io<TIn>::to_f(p.q[e]);
-                s_do[tid] = p.d_out[e];
-                s_u[tid] = ur[tid];
-                s_r[tid] = ur[kDim + tid];
+                x.q = p.q[e];
+                x.d = p.d_out[e];
+                x.u = ur[tid];
+                x.r = ur[kDim + tid];
             } else {
-                s_v[tid] = io<TIn>::to_f(p.v[e]);
+                x.v = p.v[e];
             }
         }
-        return io<TIn>::to_f(p.beta[row]);
+        return x;
+    };
+    // a fetched token into shared memory (a = exp(g)); returns its beta
+    auto stage = [&](const Tok& x, bool reverse) -> float {
+        if (tid < kDim) {
+            s_k[tid] = io<TIn>::to_f(x.k);
+            s_a[tid] = expf(io<TIn>::to_f(x.g));
+            if (reverse) {
+                s_q[tid] = io<TIn>::to_f(x.q);
+                s_do[tid] = x.d;
+                s_u[tid] = x.u;
+                s_r[tid] = x.r;
+            } else {
+                s_v[tid] = io<TIn>::to_f(x.v);
+            }
+        }
+        return io<TIn>::to_f(x.b);
     };
     // S' = diag(a) S in place, and the per-warp partial column sums of k_i S'_ij into s_part
     auto decay_and_x = [&](float4 (&S)[16]) {
@@ -143,8 +166,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
         }
     };
     // one forward token: S <- diag(a) S + k u^T; keeps S' = diag(a) S and (u, r) when asked
-    auto fwd_step = [&](int t, float4 (&S)[16], float* keep_s, float* keep_ur) {
-        const float b = stage(t, nullptr);
+    // nx holds token t's inputs on entry and token t_next's (when t_next >= 0) on return
+    auto fwd_step = [&](float4 (&S)[16], float* keep_s, float* keep_ur, Tok& nx, int t_next) {
+        const float b = stage(nx, false);
+        if (t_next >= 0) nx = fetch(t_next, nullptr);
         __syncthreads();
         decay_and_x(S);
         if (keep_s) st_state(keep_s, S);
@@ -164,12 +189,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
     float4 S[16], dS[16];
     // ---- forward sweep: the state before every block
     ld_state(p.init_state ? p.init_state + sbase : nullptr, S);
+    Tok nx;
+    if (L > 0) nx = fetch(0, nullptr);
 #pragma unroll 1
     for (int b = 0; b < nb; ++b) {
         st_state(ck + (int64_t)b * kDim * kDim, S);
         const int te = min(L, (b + 1) * kBwdBlock);
 #pragma unroll 1
-        for (int t = b * kBwdBlock; t < te; ++t) fwd_step(t, S, nullptr, nullptr);
+        for (int t = b * kBwdBlock; t < te; ++t) fwd_step(S, nullptr, nullptr, nx, t + 1 < L ? t + 1 : -1);
     }
     // ---- reverse sweep
     ld_state(p.d_state ? p.d_state + sbase : nullptr, dS);
@@ -178,14 +205,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
         const int tb = b * kBwdBlock, te = min(L, tb + kBwdBlock);
         __syncthreads();  // this block's stored states are rewritten below
         ld_state(ck + (int64_t)b * kDim * kDim, S);
+        nx = fetch(tb, nullptr);
 #pragma unroll 1
         for (int t = tb; t < te; ++t)
-            fwd_step(t, S, blk + (int64_t)(t - tb) * kDim * kDim, blk_ur + (t - tb) * 2 * kDim);
+            fwd_step(S, blk + (int64_t)(t - tb) * kDim * kDim, blk_ur + (t - tb) * 2 * kDim, nx,
+                     t + 1 < te ? t + 1 : -1);
+        // the (u, r) a reverse step fetches were written by this thread in the replay above
+        nx = fetch(te - 1, blk_ur + (te - 1 - tb) * 2 * kDim);
 #pragma unroll 1
         for (int t = te - 1; t >= tb; --t) {
             const int64_t row = (t0 + t) * p.H + h;
             ld_state(blk + (int64_t)(t - tb) * kDim * kDim, S);  // S' = diag(a_t) S_{t-1}
-            const float b_t = stage(t, blk_ur + (t - tb) * 2 * kDim);
+            const float b_t = stage(nx, true);
+            if (t > tb) nx = fetch(t - 1, blk_ur + (t - 1 - tb) * 2 * kDim);
             __syncthreads();
             // dS += q do^T; partial column sums of k_i dS_ij; u . do
             {
