@@ -206,3 +206,33 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         kda.fwd_chunked(x, x, x, x, torch.zeros(4, 2, dtype=torch.bfloat16),
                         torch.tensor([0, 4], dtype=torch.int32), [4])
+
+
+def test_backward_host_checks(lib):
+    """The backward's workspace size and the argument checks it makes before any launch."""
+    from kimi_delta_attention_03_gb300 import binding
+    P = ctypes.c_void_p
+    lens, H = [0, 5, 33, 2048], 3
+    desc = binding.make_desc(lens, H, torch.bfloat16)
+    # per (sequence, head): a state per 16 tokens of the longest sequence, 16 block states and
+    # 16 (u, r) vector pairs, all fp32
+    per_unit = (2048 // 16 + 16) * 128 * 128 + 16 * 2 * 128
+    need = lib.kda_bwd_workspace_bytes(ctypes.byref(desc))
+    assert need == per_unit * len(lens) * H * 4
+    assert lib.kda_bwd_workspace_bytes(None) == 0
+    ins = [P(0x1000 + 0x100 * i) for i in range(5)]          # q, k, v, log_alpha, beta
+    cu, d_out = P(0x2000), P(0x2100)
+    outs = [P(0x3000 + 0x100 * i) for i in range(6)]          # dq, dk, dv, dg, dbeta, dinit
+    ws = P(0x10000)
+
+    def call(outs=outs, ws=ws, ws_bytes=need, d_out=d_out):
+        return lib.kda_bwd(ctypes.byref(desc), *ins, None, cu, d_out, None, *outs, ws,
+                           ws_bytes, None)
+    assert call(outs=outs[:5] + [None]) == -1                 # no initial-state gradient buffer
+    assert call(outs=[ins[0]] + outs[1:]) == -1               # dq aliases q
+    assert call(outs=[outs[0], outs[0]] + outs[2:]) == -1     # two outputs alias
+    assert call(d_out=None) == -1                             # no output gradient
+    assert call(outs=[P(0x3004)] + outs[1:]) == -1            # output not 16-byte aligned
+    assert call(ws_bytes=need - 1) == -3                      # workspace too small
+    assert call(ws=None) == -3                                # no workspace
+    assert call(ws=P(0x10008)) == -3                          # workspace not 16-byte aligned
