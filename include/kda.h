@@ -366,8 +366,12 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
  *   d_state       device fp32 [N, H, 128, 128] or NULL (no loss on the final states)
  *   dq, dk, dv, dlog_alpha   device fp32 [T, H, 128]; dbeta device fp32 [T, H];
  *   dinit_state   device fp32 [N, H, 128, 128]
- *   workspace     device, at least kda_bwd_workspace_bytes(desc) bytes, 16-byte aligned
- * Outputs must not alias inputs or each other.
+ *   workspace     device, at least kda_bwd_workspace_bytes(desc) bytes, 16-byte aligned:
+ *                 per (sequence, head), fp32, one state per 16 tokens of the longest sequence,
+ *                 16 states of the block being reversed and 16 pairs of 128-vectors (u, r);
+ *                 contents on return are unspecified
+ * Outputs must not alias inputs or each other.  Argument, alignment and workspace errors return
+ * KDA_ERR_INVALID_ARG / KDA_ERR_WORKSPACE before anything is launched.
  */
 size_t kda_bwd_workspace_bytes(const kda_desc* desc);
 kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const void* v,
