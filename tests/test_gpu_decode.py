@@ -25,7 +25,7 @@ def test_decode_small(dtype):
     o_ref, s_ref = oracle.decode_step(d["q"].cpu(), d["k"].cpu(), d["v"].cpu(),
                                       d["log_alpha"].cpu(), d["beta"].cpu(), before)
     assert o.dtype == dtype
-    assert_close("out", o.float().cpu().numpy(), o_ref)
+    assert_close("out", o.cpu(), o_ref)
     assert_close("state", d["state"].cpu().numpy(), s_ref)
 
 
@@ -44,7 +44,7 @@ def test_decode_three_steps_equal_three_token_recurrence():
                                      x["log_alpha"].cpu(), x["beta"].cpu(),
                                      x["cu_seqlens"].cpu(), state_in=x["init_state"].cpu())
     o = torch.stack(outs, 1).reshape(N * steps, H, 128)
-    assert_close("out", o.float().cpu().numpy(), o_ref)
+    assert_close("out", o.cpu(), o_ref)
     assert_close("state", state.cpu().numpy(), s_ref)
 
 
@@ -65,7 +65,7 @@ def test_decode_512x96_full_size_sampled():
                                      pick(d["log_alpha"]), pick(d["beta"]),
                                      np.arange(769, dtype=np.int32), state_in=before[:, None],
                                      threads=oracle_threads())
-    assert_close("out", pick(o).float().numpy(), o_ref)
+    assert_close("out", pick(o), o_ref)
     after = d["state"][n_idx.to(DEV), h_idx.to(DEV)].cpu()[:, None]
     assert_close("state", after.numpy(), s_ref)
     assert kda().read_device_status() == 0
@@ -95,7 +95,7 @@ def test_decode_window_outputs_and_committed_states_match_oracle():
                                  x["beta"].cpu(), x["cu_seqlens"].cpu(),
                                  state_in=x["init_state"].cpu(), want_state=False,
                                  threads=oracle_threads())
-    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("out", out.cpu(), o_ref)
     # committed states: the oracle's final states of the committed prefixes
     cu = x["cu_seqlens"].cpu().tolist()
     c = [min(cm, L) for cm, L in zip(commit, lens)]
