@@ -119,8 +119,8 @@ kda_status decode_window_impl(const kda_desc* desc, const void* q, const void* k
     int* status = status_word();
     if (!status) return KDA_ERR_CUDA;
     cudaError_t e = kda::launch_decode_window(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k,
-                                              v, log_alpha, beta, cu_seqlens, state, out, commit,
-                                              (cudaStream_t)stream, pro ? &pp : nullptr);
+                                              v, log_alpha, beta, cu_seqlens, state, state, out,
+                                              commit, (cudaStream_t)stream, pro ? &pp : nullptr);
     g_launches += 1;
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -221,10 +221,12 @@ kda_status fwd_chunked_impl(const kda_desc* desc, const void* q, const void* k, 
                                    status, (cudaStream_t)stream, &launches,
                                    desc->host_seqlens, ckpts > 0 ? ckpt_states : nullptr,
                                    ckpts > 0 ? ckpt_every / kda::kChunk : 0, pro ? &pp : nullptr);
-    else
-        e = kda::launch_prefill(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v,
-                                log_alpha, beta, init_state, cu_seqlens, out, final_state,
-                                status, (cudaStream_t)stream, &launches);
+    else {  // fp32 inputs: the token loop in fp32 over whole sequences (exact for every gate)
+        e = kda::launch_decode_window(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v,
+                                      log_alpha, beta, cu_seqlens, init_state, final_state, out,
+                                      nullptr, (cudaStream_t)stream);
+        ++launches;
+    }
     g_launches += launches;
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

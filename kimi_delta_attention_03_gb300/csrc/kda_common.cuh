@@ -60,12 +60,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // Launchers implemented in the kernel translation units (called by kda_api.cu).
 namespace kda {
 
-cudaError_t launch_prefill(int dtype, int num_seqs, int heads, const void* q, const void* k,
-                           const void* v, const void* g, const void* beta,
-                           const float* init_state, const int32_t* cu_seqlens, void* out,
-                           float* final_state, int* status, cudaStream_t stream,
-                           uint64_t* launches);
-
 // Workspace of the segmented prefill: three arrays of [slots][H][128][128] fp32 (segment
 // states from zero, segment transitions, composed incoming states).
 struct SegWorkspace {
@@ -112,11 +106,13 @@ cudaError_t launch_decode(int dtype, int64_t units, int heads, const void* q, co
                           void* out, int* status, cudaStream_t stream,
                           const ProParams* pro = nullptr);
 
+// The state is read from state_in (zeros when null) and written to state_out (skipped when
+// null); they may be the same array.  Also the prefill of fp32 inputs (commit null).
 cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void* q,
                                  const void* k, const void* v, const void* g, const void* beta,
-                                 const int32_t* cu_seqlens, float* state, void* out,
-                                 const int32_t* commit, cudaStream_t stream,
-                                 const ProParams* pro = nullptr);
+                                 const int32_t* cu_seqlens, const float* state_in,
+                                 float* state_out, void* out, const int32_t* commit,
+                                 cudaStream_t stream, const ProParams* pro = nullptr);
 
 // The prologue alone over `rows` (token, head) rows, bf16 in and out.
 cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const void* k_raw,

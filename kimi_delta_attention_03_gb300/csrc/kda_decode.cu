@@ -162,13 +162,17 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 // inputs (layout [T, H, 128], as the prefill's); every token's output is written (when out is
 // given) from the state after the run's earlier tokens; the state after the first commit[n]
 // tokens is written back (nothing when commit[n] = 0; all of them when commit is null).  Per
-// token the arithmetic is the single-token step's, in the same order.
+// token the arithmetic is the single-token step's, in the same order.  The state is read from
+// state_in (zeros when null) and written to state_out (skipped when null); the two may be the
+// same array, as each unit reads its state before writing it.  A unit with no tokens copies
+// its state across when the two differ.  With fp32 inputs the prefill runs through this
+// kernel too: whole sequences, every token committed, exact fp32 arithmetic.
 template <typename TIn, bool kPro>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
 kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                          const TIn* __restrict__ v, const TIn* __restrict__ g,
                          const TIn* __restrict__ beta, const int32_t* __restrict__ cu_seqlens,
-                         float* __restrict__ state, TIn* __restrict__ out,
+                         const float* state_in, float* state_out, TIn* __restrict__ out,
                          const int32_t* __restrict__ commit, int64_t units, int H,
                          const DecPro pro) {
     __shared__ float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_u[kDim];
@@ -187,12 +191,20 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         const int64_t t0 = cu_seqlens[n];
         const int len = (int)(cu_seqlens[n + 1] - t0);
         const int ncommit = commit ? min(max(commit[n], 0), len) : len;
-        if (len <= 0) continue;
-        float* S = state + unit * (int64_t)(kDim * kDim);
+        const float* Sin = state_in ? state_in + unit * (int64_t)(kDim * kDim) : nullptr;
+        float* S = state_out ? state_out + unit * (int64_t)(kDim * kDim) : nullptr;
+        if (len <= 0) {
+            if (S && S != Sin)
+                for (int e = tid; e < kDim * kDim / 4; e += kDecodeThreads)
+                    reinterpret_cast<float4*>(S)[e] =
+                        Sin ? reinterpret_cast<const float4*>(Sin)[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+            continue;
+        }
         float4 s[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r)
-            s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
+            s[r] = Sin ? __ldcs(reinterpret_cast<const float4*>(Sin + (warp + 8 * r) * kDim) + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
         float pro_dt = 0.f, pro_na = 0.f;
         if constexpr (kPro) {
             pro_dt = pro.dt_bias && tid < kDim ? pro.dt_bias[h * kDim + tid] : 0.f;
@@ -203,8 +215,8 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         // pulled into L2 while this unit's tokens run, so its loads find them there.
         const int64_t nu = unit + gridDim.x;
         if (nu < units) {
-            if (tid < 4) {
-                const float* nxt = state + nu * (int64_t)(kDim * kDim) + tid * 4096;
+            if (tid < 4 && state_in) {
+                const float* nxt = state_in + nu * (int64_t)(kDim * kDim) + tid * 4096;
                 asm volatile("cp.async.bulk.prefetch.L2.global [%0], 16384;" ::"l"(nxt) : "memory");
             }
             constexpr int kLine = 128 / (int)sizeof(TIn);  // elements per 128-byte line
@@ -212,7 +224,7 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
             const int64_t nn = nu / H;
             const int nh = (int)(nu - nn * H);
             const int64_t nt0 = cu_seqlens[nn];
-            const int nlen = (int)(cu_seqlens[nn + 1] - nt0);
+            const int nlen = min((int)(cu_seqlens[nn + 1] - nt0), 64);  // the first tokens
             for (int i = tid; i < nlen * 4 * kLines; i += kDecodeThreads) {
                 const int tok = i / (4 * kLines), rem = i - tok * 4 * kLines;
                 const int which = rem / kLines, line = rem - which * kLines;
@@ -304,7 +316,7 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                 s[r].x = fmaf(kk, u4.x, s[r].x); s[r].y = fmaf(kk, u4.y, s[r].y);
                 s[r].z = fmaf(kk, u4.z, s[r].z); s[r].w = fmaf(kk, u4.w, s[r].w);
             }
-            if (t + 1 == ncommit) {  // uniform: the state stores issue only on the commit token
+            if (t + 1 == ncommit && S) {  // uniform: the stores issue only on the commit token
 #pragma unroll
                 for (int r = 0; r < 16; ++r)
                     __stcs(reinterpret_cast<float4*>(S + (warp + 8 * r) * kDim) + lane, s[r]);
@@ -318,8 +330,9 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 
 cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void* q,
                                  const void* k, const void* v, const void* g, const void* beta,
-                                 const int32_t* cu_seqlens, float* state, void* out,
-                                 const int32_t* commit, cudaStream_t stream, const ProParams* pro) {
+                                 const int32_t* cu_seqlens, const float* state_in,
+                                 float* state_out, void* out, const int32_t* commit,
+                                 cudaStream_t stream, const ProParams* pro) {
     const int64_t units = (int64_t)num_seqs * heads;
     if (units <= 0) return cudaSuccess;
     if (pro && dtype != KDA_BF16) return cudaErrorInvalidValue;
@@ -341,12 +354,13 @@ cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void*
     const unsigned grid = (unsigned)(units < slots ? units : slots);
     if (dtype == KDA_BF16) {
         kernel<<<grid, kDecodeThreads, 0, stream>>>(
-            (const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta, cu_seqlens, state,
-            (T*)out, commit, units, heads, dp);
+            (const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta, cu_seqlens,
+            state_in, state_out, (T*)out, commit, units, heads, dp);
     } else {
         kda_decode_window_kernel<float, false><<<grid, kDecodeThreads, 0, stream>>>(
             (const float*)q, (const float*)k, (const float*)v, (const float*)g,
-            (const float*)beta, cu_seqlens, state, (float*)out, commit, units, heads, dp);
+            (const float*)beta, cu_seqlens, state_in, state_out, (float*)out, commit, units,
+            heads, dp);
     }
     return cudaGetLastError();
 }
