@@ -333,9 +333,9 @@ def fwd_chunked_noalloc(q, k, v, log_alpha, beta, cu_seqlens, seqlens, init_stat
                         out=None, final_state=None, stream=None):
     """Chunked prefill through kda_fwd_chunked_noalloc: for callers that cannot allocate
     device scratch, the library's built-in 48 MiB array serves as the segment workspace (a
-    call needing more raises KdaError(KDA_ERR_WORKSPACE)).  ``out`` and ``final_state`` must be
-    given: this path allocates nothing.  Calls share the array, so overlapping calls on
-    different streams must not be issued."""
+    call needing more raises KdaError(KDA_ERR_WORKSPACE)).  ``out`` must be given, as this path
+    allocates nothing; ``final_state`` may be None to skip the final states.  Calls share the
+    array, so overlapping calls on different streams must not be issued."""
     lib = load_library()
     dev = q.device
     if dev.type != "cuda":

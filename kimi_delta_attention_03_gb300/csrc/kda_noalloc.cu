@@ -50,11 +50,14 @@ extern "C" kda_status kda_fwd_chunked_noalloc(const kda_desc* desc, const void* 
     kda_status st = kda_fwd_plan(desc, &plan);
     if (st != KDA_OK) return st;
     if (plan.workspace_bytes > kNoAllocScratchBytes) return KDA_ERR_WORKSPACE;
+    // Resolve the array's address on every call, whether or not this one needs scratch, so
+    // that the first call on a device does the lookup and later (possibly captured) calls
+    // only read the cached address.
+    void* scratch = scratch_address();
+    if (!scratch) return KDA_ERR_CUDA;
     if (plan.workspace_bytes == 0)  // nothing is split: no scratch is touched
         return kda_fwd_chunked(desc, q, k, v, log_alpha, beta, init_state, cu_seqlens, out,
                                final_state, nullptr, 0, stream);
-    void* scratch = scratch_address();
-    if (!scratch) return KDA_ERR_CUDA;
     // Every workspace slot that is read is first written by the same call, so the array needs
     // no clearing between calls.
     return kda_fwd_chunked(desc, q, k, v, log_alpha, beta, init_state, cu_seqlens, out,
