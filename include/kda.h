@@ -30,8 +30,8 @@
  *   - Every compute entry point is asynchronous on `stream` (NULL = legacy default stream).
  *     Host-side argument checks are synchronous and return before anything is launched.
  *   - Errors: KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED / KDA_ERR_WORKSPACE from the host
- *     checks, KDA_ERR_CUDA when a launch fails.  Conditions found on the device (a chunk's
- *     cumulative log-decay outside the supported range) set the sticky device status word;
+ *     checks, KDA_ERR_CUDA when a launch fails.  Conditions found on the device (a gate outside
+ *     the supported domain, a bounded wait that gave up) set the sticky device status word;
  *     the kernels never trap or abort.
  */
 #ifndef KDA_GB300_H
@@ -54,7 +54,7 @@ typedef enum kda_status {
     KDA_ERR_WORKSPACE = -3,    /* workspace missing or smaller than kda_fwd_workspace_bytes */
     KDA_ERR_CUDA = -4,         /* a CUDA launch or query failed                             */
     KDA_ERR_TIMEOUT = -5,      /* a bounded device-side wait gave up (device status word)   */
-    KDA_ERR_DECAY_RANGE = -6   /* a chunk's cumulative log-decay left the supported range   */
+    KDA_ERR_DECAY_RANGE = -6   /* log_alpha > 0, or below -20 (see kda_fwd_chunked)         */
 } kda_status;
 
 typedef enum kda_dtype { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
@@ -120,6 +120,19 @@ size_t kda_fwd_workspace_bytes(const kda_desc* desc);
  *
  * Bit-exactness: a sequence's results depend only on its own inputs and length, never on
  * the other sequences packed with it.
+ *
+ * Gate domain: every log_alpha in [-20, 0] is computed; this contains K3's bounded gate,
+ * lower_bound * sigmoid(...) with lower_bound = -5 ("How Kimi K3 Engineered Its Way to the
+ * Frontier", section "How KDA updates its state").  A chunk is a decay window: it starts where
+ * the previous one ended, stays inside one 64-token block of the sequence, and is the longest
+ * run of whole four-token groups (or the rest of the block) whose cumulative log-decay stays
+ * within 80 in every channel, so every exponential factor of the chunkwise form is at most
+ * e^40 in magnitude.  Ordinary gates give whole 64-token chunks; faster decay gives shorter
+ * chunks (16 tokens at log_alpha = -5) and a proportionally slower call.  A positive log_alpha,
+ * or a four-token group decaying by more than 80 in one channel (only possible below -20),
+ * sets KDA_ERR_DECAY_RANGE in the device status word and leaves out and final_state
+ * unspecified.  fp32 inputs (KDA_FP32) run the token loop itself in fp32, one pass over each
+ * sequence, exact for every log_alpha <= 0 (no range applies).
  */
 kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, const void* v,
                            const void* log_alpha, const void* beta, const float* init_state,
@@ -254,7 +267,8 @@ kda_status kda_decode_window(const kda_desc* desc, const void* q, const void* k,
 typedef struct {
   const float* A_log;    /* device fp32 [H]: per-head log decay rate */
   const float* dt_bias;  /* device fp32 [H, 128], or NULL for none */
-  float lower_bound;     /* in [-80, 0): most negative log_alpha (K3 uses -5) */
+  float lower_bound;     /* in [-80, 0): most negative log_alpha (K3 uses -5); the chunked
+                            prefill computes log_alpha >= -20 (see kda_fwd_chunked) */
   float q_scale;         /* finite, > 0: factor on the normalised q (1/sqrt(128) is usual) */
 } kda_prologue_params;
 

@@ -3,8 +3,8 @@
 //
 // Method ("How Kimi K3 Engineered Its Way to the Frontier", section "FlashKDA steps the state
 // once per 16 tokens"; the KDA recurrence from section "How KDA updates its state"): per
-// 64-token chunk, aligned to the sequence start and zero-padded at the end, with
-// G = within-chunk inclusive cumsum of g, G_C its last row and r = G_C / 2 per key channel:
+// chunk of at most 64 tokens, zero-padded at the end, with G = within-chunk inclusive cumsum of
+// g, G_C its last row and r = G_C / 2 per key channel:
 //   Q_r = q e^{G-r}   K_p = k e^{G-r}   K_m = k e^{r-G}
 //   A   = strict_lower(diag(beta) K_p K_m^T)   P = lower_incl(Q_r K_m^T)   T = (I + A)^{-1}
 //   W   = T diag(beta) K_p                     U_bar = T diag(beta) V
@@ -12,6 +12,18 @@
 //   U^T = U_bar^T - X W^T      O^T = X Q_r^T + U^T P^T
 //   S^T <- (X + U^T K_m) diag(e^r)
 // (the last line is diag(e^{G_C}) S + K_bar^T U with K_bar = k e^{G_C-G} = K_m diag(e^r)).
+//
+// Decay windows.  Every factor above is an exponential of |G - r| <= |G_C| / 2, and the state
+// scale between chunks is e^{r_{c-1} + r_c}; all stay normal fp32 (and bf16) numbers when
+// |G_C| <= 80 in every channel.  The bounded gate allows up to 5 per token, 320 over 64 tokens,
+// so a chunk is a window of the sequence: it starts where the previous one ended, never
+// crosses a multiple of 64 tokens from the sequence start, and is the longest run of whole
+// four-token groups (or the rest of the 64-token block) whose decay stays within 80 in every
+// channel.  With ordinary gates every window is a whole 64-token block; a block that decays
+// faster runs as two to sixteen windows, each through the same pipeline (its tiles are loaded
+// from the window's first token and the rows past its end are masked as padding).  A
+// four-token group that alone decays by more than 80 (log_alpha below -20) is reported as
+// KDA_ERR_DECAY_RANGE, as is a positive log_alpha.
 //
 // GB300 mapping.  One CTA per (sequence, head), 14 warps:
 //   warp 0      prep MMA issuer (one thread): the chunk-local products of chunk c+1, the TMA
@@ -27,7 +39,11 @@
 // the layout TMA or the producing warp writes naturally (K-major or MN-major 128B-swizzled).
 //
 // Precision: P and U enter the tensor core as two bf16 terms (hi + lo), which removes their
-// rounding from the heavy tail of the output error; everything accumulates in fp32.
+// rounding from the heavy tail of the output error; everything accumulates in fp32.  Two terms
+// that fast decay makes dominant get more: in a chunk whose decay exceeds kHeavyDecay in some
+// channel, P's diagonal q_t . k_t (its decay factor is exactly 1) is formed in fp32 from the
+// raw tiles rather than from the bf16-rounded factor tiles; and the state update of a work
+// item's last chunk (the state it returns) adds K_m's bf16 rounding residue as a third term.
 //
 // Every wait is bounded; on expiry the CTA records KDA_ERR_TIMEOUT and drains.
 #include <cudaTypedefs.h>
@@ -58,7 +74,10 @@ constexpr int kBarPrep = 1;     // named barrier ids
 constexpr int kBarEpi = 2;
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (about 2 s)
 constexpr float kLog2eTC = 1.4426950408889634f;
-constexpr float kMaxExponentTC = 80.f;
+constexpr float kWindowDecay = 80.f;  // largest |G_C| of a window (so |G - r| <= 40)
+constexpr float kHeavyDecay = 16.f;   // chunks decaying faster in some channel form P's diagonal
+                                      // from the raw q, k (it then dominates the output)
+constexpr int kWinRing = 8;     // window records kept: the oldest reader is two chunks behind
 constexpr int LDA_T = 68;       // fp32 row stride of the 64 x 64 A / T matrix
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
@@ -88,9 +107,13 @@ constexpr uint32_t OFF_BETA = OFF_GC + 512;         // 2 x 64 fp32 ring
 constexpr uint32_t OFF_ER = OFF_BETA + 512;         // 4 x 128 fp32: e^{r} ring
 constexpr uint32_t OFF_SC = OFF_ER + 2048;          // 4 x 128 fp32: e^{r_{c-1} + r_c} ring
 constexpr uint32_t OFF_BAR = OFF_SC + 2048;         // mbarriers
-constexpr int NBAR = 34;
+constexpr int NBAR = 36;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;   // tmem slot, abort flag, copies issued
-constexpr uint32_t SMEM_USED = OFF_MISC + 48;
+constexpr uint32_t OFF_WIN = OFF_MISC + 48;         // kWinRing x {first token, length, fast, 0}
+constexpr uint32_t OFF_WMIN = OFF_WIN + kWinRing * 16;  // 4 ints: per-warp window group counts
+constexpr uint32_t OFF_QK = OFF_WMIN + 16;         // 4 x 64 fp32: q_t . k_t by chunk (P's diagonal)
+constexpr uint32_t OFF_HEAVY = OFF_QK + 1024;       // 4 ints: per-warp flags of the rare path
+constexpr uint32_t SMEM_USED = OFF_HEAVY + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 
@@ -101,6 +124,7 @@ enum {
     B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_UFREE0, B_UFREE1, B_KMFREE0, B_KMFREE1, B_KMFREE2,
     B_SDONE, B_PFREE0, B_PFREE1, B_SCAN0, B_SCAN1, B_GFULL, B_M6ISS,
     B_VPRO,  // prologue variant: v of the chunk has been through Swish
+    B_KQPRO0, B_KQPRO1,  // prologue variant: k, q of the slot are transformed (256 arrivals)
     B_COUNT
 };
 static_assert(B_COUNT <= NBAR, "barrier slots");
@@ -139,6 +163,17 @@ enum { ITEM_WHOLE = 0, ITEM_TILDE = 1, ITEM_TRANS = 2, ITEM_SEGMENT = 3 };
 
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Named barrier that also returns whether `pred` holds in any participating thread.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
 }
 
 
@@ -297,32 +332,136 @@ __device__ __forceinline__ void store_state(float* dst, uint32_t taddr, const fl
     }
 }
 
-// Cumulative decay of chunk cs for the epilogue warp group, thread te = key channel: exclusive
-// prefixes of g at the 16 four-token groups (into the prefix array), G_C, e^{r} with
-// r = G_C / 2, and the state scale e^{r_{cs-1} + r_cs}.  Group sums first, then the prefix over
-// the groups.  One call site, out of line: inlined, it raises the epilogue loop's spills.
+// Shorten chunk cs's window when some channel's decay over the vmax tokens the scan covered
+// exceeds the bound: nok is this channel's count of leading four-token groups within it, and
+// the smallest count over the channels, nmin, sets the window's length 4 nmin.  Tokens past the
+// window count as padding (g = 0), so the prefixes of later groups, G_C, e^{r} and the state
+// scale become those of the window.  Each thread rewrites its own channel's entries.  Inlined
+// into the (out-of-line) scan: a call there would make every scan save registers.
+__device__ __forceinline__ int shorten_window(unsigned char* sm, int cs, int te, int nok, int vmax,
+                                           int* status) {
+    float* part = reinterpret_cast<float*>(sm + OFF_PART);
+    float* gc_s = reinterpret_cast<float*>(sm + OFF_GC);
+    float* er = reinterpret_cast<float*>(sm + OFF_ER);
+    float* sc = reinterpret_cast<float*>(sm + OFF_SC);
+    int* wmin = reinterpret_cast<int*>(sm + OFF_WMIN);
+    const int wm = (int)__reduce_min_sync(0xffffffffu, (unsigned)nok);
+    if ((te & 31) == 0) wmin[te >> 5] = wm;
+    named_bar(kBarEpi, kEpiThreads);
+    const int4 m4 = *reinterpret_cast<const int4*>(wmin);
+    int nmin = min(min(m4.x, m4.y), min(m4.z, m4.w));
+    if (nmin == 0) {  // one four-token group alone decays beyond the range: log_alpha < -20
+        if (te == 0) report_status(status, kStatusDecayRange);
+        nmin = 1;
+    }
+    const int len = min(vmax, 4 * nmin);
+    if (len < vmax) {
+        const float G = part[nmin * kDim + te];  // decay after the window's 4 nmin tokens
+#pragma unroll 1
+        for (int gi = nmin + 1; gi < 16; ++gi) part[gi * kDim + te] = G;
+        gc_s[te] = G;
+        const float e = ex2_approx((0.5f * kLog2eTC) * G);
+        er[(cs & 3) * kDim + te] = e;
+        sc[(cs & 3) * kDim + te] = cs > 0 ? er[((cs + 3) & 3) * kDim + te] * e : e;
+    }
+    named_bar(kBarEpi, kEpiThreads);
+    return len;
+}
+
+// The extra terms of chunk cs, for the chunks that need them (inlined into the scan, which the
+// factor pass of the chunk waits for; thread te of the epilogue group):
+//   heavy: q_t . k_t in fp32 from the chunk's bf16 k and q tiles (thread t < 64), for P's
+//          diagonal: under fast decay that term dominates o_t;
+//   last:  the work item's last chunk: K_m's bf16 rounding residue k e^{r-G} - K_m (column te),
+//          with the factor pass's own arithmetic for K_m, into the K_m slot after this chunk's
+//          (free once M6 of chunk cs - 2 has read it), for a third term of the final state update.
+// The k, q tiles are read before the factor pass replaces them (it waits for the scan).
+template <bool kPro>
+__device__ __forceinline__ bool scan_extra(unsigned char* sm, int cs, int te, int len, bool heavy,
+                                           bool last, volatile int* abort_flag, int* status) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    const int s2 = cs & 1;
+    // k and q of the chunk have landed (the prologue variant: and are transformed)
+    if (!wait_bar(&bars[(kPro ? B_KQPRO0 : B_FULL0) + s2], (cs >> 1) & 1, abort_flag, status))
+        return false;
+    const unsigned char* kq = sm + (s2 ? OFF_KQW1 : OFF_KQW0);
+    if (heavy && te < kChunk) {
+        float d = 0.f;
+#pragma unroll 4
+        for (int c8 = 0; c8 < kDim; c8 += 8) {
+            const uint32_t o = sw128_offset(te, c8, KQW_ROWS);
+            float kv[8], qv[8];
+            unpack8(*reinterpret_cast<const uint4*>(kq + o), kv);
+            unpack8(*reinterpret_cast<const uint4*>(kq + o + 64 * 128), qv);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) d = fmaf(qv[j], kv[j], d);
+        }
+        reinterpret_cast<float*>(sm + OFF_QK)[(cs & 3) * kChunk + te] = d;
+    }
+    if (last) {
+        const int sl = (cs + 1) % 3;
+        if (cs >= 2 && !wait_bar(&bars[B_KMFREE0 + sl], ((cs - 2) / 3) & 1, abort_flag, status))
+            return false;
+        unsigned char* dst = sm + (sl == 0 ? OFF_KMH0 : sl == 1 ? OFF_KMH1 : OFF_KMH2);
+        const float* part = reinterpret_cast<const float*>(sm + OFF_PART);
+        const float r = (0.5f * kLog2eTC) * reinterpret_cast<const float*>(sm + OFF_GC)[te];
+#pragma unroll 1
+        for (int tg = 0; tg < 16; ++tg) {
+            float G = fmaf(part[tg * kDim + te], kLog2eTC, -r);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = 4 * tg + i;
+                const float gv = t < len ? __bfloat162float(*reinterpret_cast<const bf16*>(
+                                               sm + OFF_G + sw128_offset(t, te, 64)))
+                                         : 0.f;
+                G = fmaf(gv, kLog2eTC, G);
+                const float km = __bfloat162float(*reinterpret_cast<const bf16*>(
+                                     kq + sw128_offset(t, te, KQW_ROWS))) *
+                                 ex2_approx(-G);
+                *reinterpret_cast<bf16*>(dst + sw128_offset(t, te, 64)) =
+                    __float2bfloat16_rn(km - round_bf16(km));
+            }
+        }
+        fence_async_shared();  // read by the tensor core
+    }
+    named_bar(kBarEpi, kEpiThreads);
+    return true;
+}
+
+// Cumulative decay of chunk cs for the epilogue warp group, thread te = key channel: the
+// chunk's window (first token and length), the exclusive prefixes of g at its 16 four-token
+// groups (into the prefix array), G_C, e^{r} with r = G_C / 2, and the state scale
+// e^{r_{cs-1} + r_cs}.  Group sums first, then the prefix over the groups.  The window starts
+// where chunk cs - 1's ended and first covers the rest of its 64-token block (the g tile was
+// loaded from its first token); each channel counts the leading groups whose prefix stays
+// within kWindowDecay, and the smallest count over the channels sets the window's length.
+// One call site, out of line: inlined, it raises the epilogue loop's spills.
 // kPro: g is the raw gate input; each value goes through the bounded gate (rounded to bf16, as
 // an unfused prologue would store it) and is written back for the factor pass.
+// Returns -1 when a wait gave up, 0 when the chunk is released (the common case), or 1 when
+// the chunk needs the rare path (scan_rare: a shorter window, or the extra terms).
 template <bool kPro>
-__device__ __forceinline__ bool decay_scan_body(unsigned char* sm, int cs, int L, int te,
-                                                volatile int* abort_flag, int* status, float dt,
-                                                float a, float lb) {
+__device__ __forceinline__ int decay_scan_body(unsigned char* sm, int cs, int L, int te,
+                                               volatile int* abort_flag, int* status, float dt,
+                                               float a, float lb) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     float* part = reinterpret_cast<float*>(sm + OFF_PART);
     float* gc_s = reinterpret_cast<float*>(sm + OFF_GC);
     float* er = reinterpret_cast<float*>(sm + OFF_ER);
     float* sc = reinterpret_cast<float*>(sm + OFF_SC);
+    int4* win = reinterpret_cast<int4*>(sm + OFF_WIN);
     const int s2 = cs & 1;
-    if (!wait_bar(&bars[B_GFULL], cs & 1, abort_flag, status)) return false;
-    const int valid = min(kChunk, L - kChunk * cs);
+    const int t0 = cs == 0 ? 0 : win[(cs - 1) & (kWinRing - 1)].x + win[(cs - 1) & (kWinRing - 1)].y;
+    const int vmax = min(L - t0, kChunk - (t0 & (kChunk - 1)));
+    if (!wait_bar(&bars[B_GFULL], cs & 1, abort_flag, status)) return -1;
     // g of token t is row t of its column region
     const unsigned char* gcol = sm + OFF_G + (te >> 6) * 8192 + ((te & 7) << 1);
     const int chunk16 = (te & 63) >> 3;
     float run = 0.f, gmax = 0.f;
 #pragma unroll 1
     for (int t16 = 0; t16 < kChunk; t16 += 16) {
-        // sixteen tokens' loads in flight at once; rows past the sequence end hold other
-        // tokens (or zeros) and are masked after the load
+        // sixteen tokens' loads in flight at once; rows past the window hold other tokens (or
+        // zeros) and are masked after the load
         float gv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -341,7 +480,7 @@ __device__ __forceinline__ bool decay_scan_body(unsigned char* sm, int cs, int L
             float gs = 0.f;
 #pragma unroll
             for (int i = 4 * q; i < 4 * q + 4; ++i) {
-                const float x = t16 + i < valid ? gv[i] : 0.f;  // g is zero past the end
+                const float x = t16 + i < vmax ? gv[i] : 0.f;  // g is zero past the window
                 gs += x;
                 gmax = fmaxf(gmax, x);
             }
@@ -349,28 +488,80 @@ __device__ __forceinline__ bool decay_scan_body(unsigned char* sm, int cs, int L
             run += gs;
         }
     }
-    // With every g <= 0 the cumulative decay G is monotone, so |G - r| <= |G_C| / 2 and one
-    // check per channel bounds every factor.
     if (gmax > 0.f) report_status(status, kStatusDecayRange);
+    const bool heavy = fabsf(run) > kHeavyDecay;  // this channel decays fast
     gc_s[te] = run;
-    if (fabsf(0.5f * run) > kMaxExponentTC) report_status(status, kStatusDecayRange);
     const float e = ex2_approx((0.5f * kLog2eTC) * run);
     er[(cs & 3) * kDim + te] = e;
     sc[(cs & 3) * kDim + te] = cs > 0 ? er[((cs + 3) & 3) * kDim + te] * e : e;
     if constexpr (kPro) fence_async_shared();  // the gated g is overwritten by the next TMA load
+    // the barrier tells every thread whether some channel needs the rare path: fast decay
+    // (which includes every window that must be shortened, as kWindowDecay > kHeavyDecay); the
+    // item's last chunk takes it too
+    if (named_bar_or(kBarEpi, kEpiThreads, heavy) || t0 + vmax >= L) return 1;
+    if (te == 0) {
+        win[cs & (kWinRing - 1)] = make_int4(t0, vmax, 0, 0);
+        mbar_arrive(&bars[B_SCAN0 + s2]);
+    }
+    return 0;
+}
+
+// The rare path of chunk cs's scan, out of line so that the common scan stays small: shorten
+// the window if some channel needs it, add the extra terms for a fast-decaying chunk or the
+// item's last chunk, then release the chunk.
+template <bool kPro>
+__device__ __forceinline__ bool scan_rare_body(unsigned char* sm, int cs, int L, int te,
+                                               volatile int* abort_flag, int* status) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    int4* win = reinterpret_cast<int4*>(sm + OFF_WIN);
+    int* flags = reinterpret_cast<int*>(sm + OFF_HEAVY);
+    const float* part = reinterpret_cast<const float*>(sm + OFF_PART);
+    const float gc = reinterpret_cast<const float*>(sm + OFF_GC)[te];
+    const int t0 = cs == 0 ? 0 : win[(cs - 1) & (kWinRing - 1)].x + win[(cs - 1) & (kWinRing - 1)].y;
+    const int vmax = min(L - t0, kChunk - (t0 & (kChunk - 1)));
+    // this channel's leading four-token groups whose decay stays within the window bound (the
+    // prefix after group i is the exclusive prefix of group i + 1); |G| only grows, as g <= 0
+    int nok = 0;
+#pragma unroll 1
+    for (int gi = 1; gi <= 16; ++gi)
+        nok += fabsf(gi < 16 ? part[gi * kDim + te] : gc) <= kWindowDecay ? 1 : 0;
+    // per warp: bit 0 some channel decays fast, bit 1 the window must be shorter than vmax
+    const unsigned heavy = __any_sync(0xffffffffu, fabsf(gc) > kHeavyDecay);
+    const unsigned shrt = __any_sync(0xffffffffu, 4 * nok < vmax);
+    if ((te & 31) == 0) flags[te >> 5] = (heavy ? 1 : 0) | (shrt ? 2 : 0);
     named_bar(kBarEpi, kEpiThreads);
-    if (te == 0) mbar_arrive(&bars[B_SCAN0 + s2]);
+    const int4 f = *reinterpret_cast<const int4*>(flags);
+    const int fo = f.x | f.y | f.z | f.w;
+    int len = vmax;
+    if (fo & 2) len = shorten_window(sm, cs, te, nok, vmax, status);
+    const bool fast = fo != 0;  // a shortened window counts as fast-decaying
+    if (fast || t0 + len >= L) {  // the extra terms
+        if (!scan_extra<kPro>(sm, cs, te, len, fast, t0 + len >= L, abort_flag, status))
+            return false;
+    }
+    if (te == 0) {
+        win[cs & (kWinRing - 1)] = make_int4(t0, len, fast ? 1 : 0, 0);
+        mbar_arrive(&bars[B_SCAN0 + (cs & 1)]);
+    }
     return true;
 }
 
-__device__ __noinline__ bool decay_scan(unsigned char* sm, int cs, int L, int te,
-                                        volatile int* abort_flag, int* status) {
+__device__ __noinline__ int decay_scan(unsigned char* sm, int cs, int L, int te,
+                                       volatile int* abort_flag, int* status) {
     return decay_scan_body<false>(sm, cs, L, te, abort_flag, status, 0.f, 0.f, 0.f);
 }
-__device__ __noinline__ bool decay_scan_pro(unsigned char* sm, int cs, int L, int te,
-                                            volatile int* abort_flag, int* status, float dt,
-                                            float a, float lb) {
+__device__ __noinline__ int decay_scan_pro(unsigned char* sm, int cs, int L, int te,
+                                           volatile int* abort_flag, int* status, float dt,
+                                           float a, float lb) {
     return decay_scan_body<true>(sm, cs, L, te, abort_flag, status, dt, a, lb);
+}
+__device__ __noinline__ bool scan_rare(unsigned char* sm, int cs, int L, int te,
+                                       volatile int* abort_flag, int* status) {
+    return scan_rare_body<false>(sm, cs, L, te, abort_flag, status);
+}
+__device__ __noinline__ bool scan_rare_pro(unsigned char* sm, int cs, int L, int te,
+                                           volatile int* abort_flag, int* status) {
+    return scan_rare_body<true>(sm, cs, L, te, abort_flag, status);
 }
 
 // Self-test of the bounded waits: one CTA waits, through the kernels' own helper, on a barrier
@@ -463,8 +654,6 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         return;
     }
-    const int nchunks = (L + kChunk - 1) / kChunk;
-
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC + 8);
@@ -474,6 +663,15 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     float* part = reinterpret_cast<float*>(sm + OFF_PART);
     float* gc_s = reinterpret_cast<float*>(sm + OFF_GC);
     float* sc = reinterpret_cast<float*>(sm + OFF_SC);
+    const int4* win = reinterpret_cast<const int4*>(sm + OFF_WIN);
+    // Chunk c covers tokens [t0, t0 + len) of this item, win[c % kWinRing] = {t0, len}, written by
+    // the decay scan of chunk c before it releases the chunk (barrier B_SCAN).  win_end(c) is
+    // where chunk c + 1 starts; there is a chunk c + 1 iff win_end(c) < L.
+    auto win_end = [&](int c) {
+        const int2 w = *reinterpret_cast<const int2*>(&win[c & (kWinRing - 1)]);
+        return w.x + w.y;
+    };
+    auto win_start = [&](int c) { return c == 0 ? 0 : win_end(c - 1); };
 
     if (warp == kWarpTma) {
         tmem_alloc(tmem_slot, 512);
@@ -490,7 +688,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                                      ((e >> 9) & 1) * KQW_REGION + 8192)[e & 511] =
                 make_uint4(0u, 0u, 0u, 0u);
     if (tid == 32) {
-        for (int i = 0; i < B_COUNT; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < B_COUNT; ++i)
+            mbar_init(&bars[i], i == B_KQPRO0 || i == B_KQPRO1 ? kPrepThreads : 1);
         *abort_flag = 0;
         *kqg_issued = 0;
         mbar_init_fence();
@@ -513,7 +712,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int s = c & 1;
         unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
         uint64_t* full = &bars[B_FULL0 + s];
-        const int t0 = (int)(seq0 + (int64_t)kChunk * c);
+        const int t0 = (int)(seq0 + win_start(c));
         mbar_arrive_expect_tx(full, has_out ? 32768 : 16384);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -525,7 +724,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     };
     auto issue_g = [&](int c) {
         uint64_t* full = &bars[B_GFULL];
-        const int t0 = (int)(seq0 + (int64_t)kChunk * c);
+        const int t0 = (int)(seq0 + win_start(c));
         mbar_arrive_expect_tx(full, 16384);
 #pragma unroll
         for (int r = 0; r < 2; ++r) tma_load_3d(sm + OFF_G + r * 8192, &tm_g, full, 64 * r, h, t0);
@@ -535,7 +734,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_arrive(&bars[B_VFULL]);
             return;
         }
-        const int t0 = (int)(seq0 + (int64_t)kChunk * c);
+        const int t0 = (int)(seq0 + win_start(c));
         mbar_arrive_expect_tx(&bars[B_VFULL], 16384);
         tma_load_3d(sm + OFF_V, &tm_v, &bars[B_VFULL], 0, h, t0);
         tma_load_3d(sm + OFF_V + 8192, &tm_v, &bars[B_VFULL], 64, h, t0);
@@ -548,10 +747,11 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_g);
-            issue_g(0);
+            // k and q first: their copy count is published before the scan of chunk 0 can
+            // start (the epilogue issues k and q of chunk 1 once chunk 0's window is known)
             issue_kq(0);
+            issue_g(0);
             issue_v(0);
-            if (nchunks > 1) issue_kq(1);
             int g_issued = 1;
             const uint32_t rP = tmem + T_P;
             const uint32_t a_v = saddr(sm + OFF_V);
@@ -563,7 +763,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const int s = c & 1;
                 if (!spin_bar(&bars[B_FACT0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
                 // the factor pass and the scan have read g of chunk c: load g of chunk c + 1
-                if (c + 1 < nchunks) {
+                if (win_end(c) < L) {
                     issue_g(c + 1);
                     g_issued = c + 2;
                 }
@@ -577,7 +777,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 mma_commit(&bars[B_AP0 + s]);
                 return true;
             };
-            for (int c = -1; c < nchunks; ++c) {  // M1 of chunk 0 first, then chunk by chunk
+            for (int c = -1;; ++c) {  // M1 of chunk 0 first, then chunk by chunk
                 if (c >= 0) {
                     const int s = c & 1;
                     // M2: W^T = K_p^T (T diag(beta))^T into the O^T columns of this chunk's block,
@@ -614,15 +814,14 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     }
                     mma_commit(&bars[B_VFREE0 + s]);
                     // the v buffer is free once M3 has read it: load the next chunk's v
-                    if (c + 1 < nchunks) {
-                        if (!spin_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status))
-                            break;
-                        issue_v(c + 1);
-                        v_issued = c + 2;
-                    }
+                    if (win_end(c) >= L) break;  // chunk c was the last
+                    if (!spin_bar(&bars[B_VFREE0 + s], (c >> 1) & 1, abort_flag, p.status))
+                        break;
+                    issue_v(c + 1);
+                    v_issued = c + 2;
                 }
                 // the next chunk's factors follow this chunk's inverse
-                if (c + 1 < nchunks && !issue_m1(c + 1)) break;
+                if (!issue_m1(c + 1)) break;
             }
             mma_commit(&bars[B_DRAIN]);
             mbar_wait(&bars[B_DRAIN], 0, kWaitLimit);
@@ -641,7 +840,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const uint32_t id_kk64 = idesc_bf16(128, 64, false, false);
             const uint32_t id_kk128 = idesc_bf16(128, 128, false, false);
             const uint32_t id_km128 = idesc_bf16(128, 128, false, true);
-            for (int c = 0; c < nchunks; ++c) {
+            for (int c = 0;; ++c) {
                 const int s = c & 1;
                 const uint32_t rX = tmem + (s ? T_X1 : T_X0);  // [U^T | O^T]
                 // M4: [U^T | O^T] += X [-W ; Q_r]^T  (U^T starts at U_bar^T, O^T at zero)
@@ -660,8 +859,9 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // M6 + M5: X += U^T K_m (2 split terms), O^T += U^T P^T (3 split terms);
                 // U^T hi / lo sit in place of U^T (cols 0-31 / 32-63 of this chunk's block)
                 if (!spin_bar(&bars[B_UREADY], c & 1, abort_flag, p.status)) break;
+                const bool more = win_end(c) < L;
                 // keep these off the tensor pipe while chunk c+1's inverse uses mma.sync
-                if (c + 1 < nchunks &&
+                if (more &&
                     !spin_bar(&bars[B_TB0 + ((c + 1) & 1)], ((c + 1) >> 1) & 1, abort_flag, p.status))
                     break;
                 tc_fence_after();
@@ -675,6 +875,12 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     for (int j = 0; j < 4; ++j) mma_ts(rS, rUH + 8 * j, dk + 128 * j, id_km128, 1);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) mma_ts(rS, rUL + 8 * j, dk + 128 * j, id_km128, 1);
+                    if (!more) {  // the final state: K_m's residue too (in the next K_m slot)
+                        const uint64_t dkr = smem_desc(a_kmh(c + 1), 8192, 1024);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            mma_ts(rS, rUH + 8 * j, dkr + 128 * j, id_km128, 1);
+                    }
                     mma_commit(&bars[B_KMFREE0 + c % 3]);  // K_m of this slot has been read
                     mma_commit(&bars[B_SDONE]);
                     mbar_arrive(&bars[B_M6ISS]);  // M6 is queued: the next M2 may follow it
@@ -689,6 +895,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
                 mma_commit(&bars[B_PFREE0 + s]);  // P of this slot has been read
                 mma_commit(&bars[B_OSDONE]);
+                if (!more) break;
             }
             // every issued MMA completes before TMEM can be released
             mma_commit(&bars[B_SPARE]);
@@ -706,8 +913,13 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int row_abs = 32 * q4 + lane;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
         float* Am = reinterpret_cast<float*>(sm + OFF_KML);
+        const float* qk_s = reinterpret_cast<const float*>(sm + OFF_QK);
+        // chunk c decays faster than kHeavyDecay in some channel (recorded by its scan)
+        auto chunk_heavy = [&](int c) { return win[c & (kWinRing - 1)].z != 0; };
         const unsigned short* beta_u = reinterpret_cast<const unsigned short*>(p.beta) + seq0 * H + h;
         unsigned short beta_raw = 0;  // raw bf16 bits; converted one chunk after the load
+        int beta_t0 = 0;              // item token where the rows in beta_raw start
+        int t0_next = 0;              // first token of the next chunk to factor (its scan's)
         if (tp < min(kChunk, L)) beta_raw = beta_u[(int64_t)tp * H];
         // scratch of the inverse: the four blocks of the upper quadrant of A / T (rows 0-31,
         // columns 32-63), which no step stores or reads otherwise
@@ -718,7 +930,6 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         // decay factors of chunk c (from its q, k, g tile)
         auto factor = [&](const int c) -> bool {
             const int s = c & 1;
-            const int valid = min(kChunk, L - kChunk * c);
             unsigned char* kq = sm + (s ? OFF_KQW1 : OFF_KQW0);
             unsigned char* kmh = sm + kmh_off(c);
             if (!wait_bar(&bars[B_FULL0 + s], (c >> 1) & 1, abort_flag, p.status)) return false;
@@ -736,25 +947,36 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     *reinterpret_cast<uint4*>(kq + o) = pack8(kv);
                     *reinterpret_cast<uint4*>(kq + o + 64 * 128) = pack8(qv);
                 }
+                mbar_arrive(&bars[B_KQPRO0 + s]);  // the scan may read the transformed tiles
             }
 
             // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7.
-            // The token-group prefixes of g, G_C and e^{r} come from the epilogue warps' scan.
+            // The window, the token-group prefixes of g, G_C and e^{r} come from the epilogue
+            // warps' scan.
             if (tp < kChunk) {
+                // beta of the rest of the 64-token block from the chunk's first token (its window
+                // length is not known yet), prefetched one chunk ago for the block start; a chunk
+                // that starts inside a block (after a shortened window) loads it now
+                const int t0c = t0_next;  // where chunk c - 1's window ended
+                const int vm = min(L - t0c, kChunk - (t0c & (kChunk - 1)));
+                if (beta_t0 != t0c) beta_raw = tp < vm ? beta_u[((int64_t)t0c + tp) * H] : 0;
                 float bt = __uint_as_float((uint32_t)beta_raw << 16);
-                if constexpr (kPro) bt = tp < valid ? round_bf16(pro_sigmoid(bt)) : 0.f;
+                if constexpr (kPro) bt = tp < vm ? round_bf16(pro_sigmoid(bt)) : 0.f;
                 beta_ring(c)[tp] = bt;
-                // fetch the next chunk's beta now; it is needed one chunk later
-                const int vn = min(kChunk, L - kChunk * (c + 1));
-                if (tp < vn)
-                    beta_raw = beta_u[((int64_t)kChunk * (c + 1) + tp) * H];
-                else
-                    beta_raw = 0;
+                // fetch the next block's beta now; it is needed one chunk later
+                const int tn = (t0c & ~(kChunk - 1)) + kChunk;
+                const int vn = min(L - tn, kChunk);
+                beta_raw = tp < vn ? beta_u[((int64_t)tn + tp) * H] : 0;
+                beta_t0 = tn;
             }
             // g has landed (the scan waited for it too) and its prefixes are in place
             if (!wait_bar(&bars[B_GFULL], c & 1, abort_flag, p.status) ||
                 !wait_bar(&bars[B_SCAN0 + s], (c >> 1) & 1, abort_flag, p.status))
                 return false;
+            const int2 wc = *reinterpret_cast<const int2*>(&win[c & (kWinRing - 1)]);
+            const int valid = wc.y;  // rows past the window are padding
+            t0_next = wc.x + wc.y;
+            if (tp < kChunk && tp >= valid) beta_ring(c)[tp] = 0.f;
             {
                 float G[8], r[8];
                 {
@@ -888,6 +1110,21 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         *reinterpret_cast<uint4*>(pt + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                         *reinterpret_cast<uint4*>(pt + 8192 + off) =
                             make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    }
+                    if (colhalf == (t >> 5) && chunk_heavy(c)) {  // it stored P[t][t]: use q_t . k_t
+                        const float qkt = qk_s[(c & 3) * kChunk + t];
+                        const uint32_t hh = pack_bf16(qkt, 0.f);
+                        const uint32_t ll = pack_bf16(qkt - __uint_as_float(hh << 16), 0.f);
+                        uint32_t* ph = reinterpret_cast<uint32_t*>(
+                            pt + sw128_offset(t, t & ~7, 64) + ((t & 7) >> 1) * 4);
+                        uint32_t* pl = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(ph) + 8192);
+                        if (t & 1) {  // the high half of the pair (t - 1, t)
+                            *ph = (*ph & 0xffffu) | (hh << 16);
+                            *pl = (*pl & 0xffffu) | (ll << 16);
+                        } else {      // the low half of (t, t + 1); column t + 1 is zero
+                            *ph = hh;
+                            *pl = ll;
+                        }
                     }
                 }
             }
@@ -1025,16 +1262,21 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (tp == 0) mbar_arrive(&bars[B_VPRO]);
             return true;
         };
-        for (int c = -1; c <= nchunks; ++c) {
+        bool cur = false;  // chunk c exists
+        for (int c = -1;; ++c) {
             if (c >= 1 && !w_epilogue(c - 1)) break;
-            if (c >= 0 && c < nchunks) {
+            if (c >= 0) {
+                if (!cur) break;  // the W epilogue of the last chunk was the final step
                 if (!ap_epilogue(c)) break;
                 inverse(c);
                 if constexpr (kPro) {
                     if (!v_prologue(c)) break;
                 }
             }
-            if (c + 1 < nchunks && !factor(c + 1)) break;
+            // chunk c's window is known: factor(c) waited for its scan
+            const bool next = c < 0 || win_end(c) < L;
+            if (next && !factor(c + 1)) break;
+            cur = next;
         }
     } else {
         // ------------------------------------------------------------ serial epilogue
@@ -1060,17 +1302,19 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             pro_lb = p.pro_lb;
         }
         auto scan = [&](const int cs) -> bool {
-            if constexpr (kPro)
-                return decay_scan_pro(sm, cs, L, te, abort_flag, p.status, pro_dt, pro_a, pro_lb);
-            else
-                return decay_scan(sm, cs, L, te, abort_flag, p.status);
+            const int r = kPro ? decay_scan_pro(sm, cs, L, te, abort_flag, p.status, pro_dt,
+                                                pro_a, pro_lb)
+                               : decay_scan(sm, cs, L, te, abort_flag, p.status);
+            if (r <= 0) return r == 0;
+            return kPro ? scan_rare_pro(sm, cs, L, te, abort_flag, p.status)
+                        : scan_rare(sm, cs, L, te, abort_flag, p.status);
         };
         bool ok = true;
-        // c = -2 and -1 only scan chunks 0 and 1 (and set up X_0): one code path for the scan
-        for (int c = -2; ok && c < nchunks; ++c) {
+        // c = -2 and -1 only scan chunks 0 and 1 (and set up X_0): one code path for the scan.
+        // Chunk c + 1 exists iff win_end(c) < L, known once chunk c's scan is done (two chunks
+        // ahead of this loop).
+        for (int c = -2; ok; ++c) {
             const uint32_t rX = tmem + ((c & 1) ? T_X1 : T_X0) + lane_off;
-            const int valid = min(kChunk, L - kChunk * c);
-            const int64_t tok0 = seq0 + (int64_t)kChunk * c;
             if (c == -1) {  // X_0 = S0^T diag(e^{r_0}); S0 = 0, I (transition items) or given
                 const float* e0 = er;
                 const float* s0 = init_src;
@@ -1093,7 +1337,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 named_bar(kBarEpi, kEpiThreads);
                 if (te == 0) mbar_arrive(&bars[B_SREADY]);
                 // chunk 1 reuses the prefix array once the prep warps have read chunk 0's
-                if (nchunks > 1 && !(ok = wait_bar(&bars[B_FACT0], 0, abort_flag, p.status))) break;
+                if (win_end(0) < L && !(ok = wait_bar(&bars[B_FACT0], 0, abort_flag, p.status)))
+                    break;
             }
             if (c >= 0) {
                 // ---- E1: U^T -> bf16 hi/lo A operands ----
@@ -1101,7 +1346,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tc_fence_after();
                 // M1, M2 and now M4 have read this slot's K_p / Q_r / -W rows: refill k and q with
                 // chunk c + 2 (g was refilled after the factor pass; K_m is guarded by B_KMFREE)
-                if (te == 0 && c + 2 < nchunks) issue_kq(c + 2);
+                if (te == 0 && win_end(c) < L && win_end(c + 1) < L) issue_kq(c + 2);
                 {
                     // read all 64 columns of U^T before writing hi / lo over them
                     uint32_t u[64], lo[32];
@@ -1128,18 +1373,25 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             // The cumulative decay of chunk c + 2 (its g landed a chunk ago).  The prep warps
             // read chunk c + 1's prefixes before the W epilogue of chunk c, so before XDONE of
             // chunk c.
-            if (c + 2 < nchunks && !(ok = scan(c + 2))) break;
+            const bool scan_next = c == -2 || ((c < 0 || win_end(c) < L) && win_end(c + 1) < L);
+            if (scan_next && !(ok = scan(c + 2))) break;
+            // k and q of chunk 1, once chunk 0's window has fixed where chunk 1 starts
+            if (c == -2 && te == 0 && win_end(0) < L) issue_kq(1);
             if (c < 0) continue;
 
             // ---- E2: state rescale first (the next chunk's M4 waits on it), then O to HBM ----
             if (!(ok = wait_bar(&bars[B_SDONE], c & 1, abort_flag, p.status))) break;
             tc_fence_after();
-            const bool last = (c + 1 == nchunks);
-            // The state after this chunk is a checkpoint when its sequence position is a
-            // multiple of the interval (a ragged last chunk never is).  S = X diag(e^{r_c}),
-            // transposed back, exactly as the final state.
-            const int done = chunk0 + c + 1;
-            float* ckd = (kCkpt && ckpt0 && valid == kChunk && done % p.ckpt_chunks == 0)
+            const int2 wc = *reinterpret_cast<const int2*>(&win[c & (kWinRing - 1)]);
+            const int valid = wc.y;
+            const int64_t tok0 = seq0 + wc.x;
+            const bool last = wc.x + wc.y >= L;
+            // The state after this chunk is a checkpoint when its window ends on a 64-token
+            // block whose sequence position is a multiple of the interval (a ragged last chunk
+            // never is).  S = X diag(e^{r_c}), transposed back, exactly as the final state.
+            const int pos = wc.x + wc.y;
+            const int done = chunk0 + pos / kChunk;
+            float* ckd = (kCkpt && ckpt0 && (pos & (kChunk - 1)) == 0 && done % p.ckpt_chunks == 0)
                              ? ckpt0 + (int64_t)(done / p.ckpt_chunks - 1) * H * (kDim * kDim)
                              : nullptr;
             const float* ec = er + (c & 3) * kDim;
@@ -1202,6 +1454,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     if (te == 0) mbar_arrive(&bars[B_UFREE0 + (c & 1)]);
                 }
             }
+            if (last) break;
         }
     }
 

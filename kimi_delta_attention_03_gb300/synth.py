@@ -12,6 +12,9 @@ Attention": q and k are L2-normalised per head; alpha in (0,1)^{d_k}; beta in (0
   q, k ~ N(0,1), L2-normalised over the d_k channels of each (token, head); q *= 1/sqrt(d_k)
   v ~ N(0,1);  beta = sigmoid(N(0,1));  log_alpha = -softplus(N(0,1)) * gate_scale
   S0 ~ N(0, s0_std^2) per entry (zeros when s0_std is None).
+With ``bounded_gate=lb`` the gate instead spans K3's whole bounded range: log_alpha =
+lb * sigmoid(2 N(0,1)) lies in (lb, 0) with mean lb / 2 ("How Kimi K3 Engineered Its Way to the
+Frontier", section "How KDA updates its state": the gate is a lower bound times a sigmoid).
 """
 from __future__ import annotations
 
@@ -71,7 +74,7 @@ def workloads() -> dict:
 
 def make_inputs(lengths, heads: int, dtype: torch.dtype, seed: int, gate_scale: float = 0.1,
                 s0_std: float | None = 0.01, device="cpu", d_k: int = D_K, d_v: int = D_V,
-                zero_length_ok: bool = True) -> dict:
+                zero_length_ok: bool = True, bounded_gate: float | None = None) -> dict:
     """Packed-varlen inputs with layout [T_tot, H, d] (batch folded into tokens).
 
     Returns a dict with q, k, v, log_alpha ([T,H,d], ``dtype``), beta ([T,H], ``dtype``),
@@ -96,7 +99,10 @@ def make_inputs(lengths, heads: int, dtype: torch.dtype, seed: int, gate_scale: 
     q = F.normalize(q, dim=-1) * (1.0 / math.sqrt(d_k))
     k = F.normalize(k, dim=-1)
     beta = torch.sigmoid(b_logit)
-    log_alpha = -F.softplus(g_noise) * gate_scale
+    if bounded_gate is None:
+        log_alpha = -F.softplus(g_noise) * gate_scale
+    else:
+        log_alpha = bounded_gate * torch.sigmoid(2.0 * g_noise)
     cu = torch.zeros(n + 1, dtype=torch.int32)
     if n:
         cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
@@ -109,14 +115,15 @@ def make_inputs(lengths, heads: int, dtype: torch.dtype, seed: int, gate_scale: 
 
 
 def make_raw_inputs(lengths, heads: int, seed: int, s0_std: float | None = 0.01, device="cpu",
-                    dt_center: float = -4.0, d: int = D_K) -> dict:
+                    dt_center: float = 0.0, d: int = D_K) -> dict:
     """Raw per-token projections for the input prologue, layout [T_tot, H, d], bf16.
 
     q_raw, k_raw, v_raw, g_raw and beta_logit are N(0, 1) (the short-convolution outputs and
     logits a layer would produce; the sources give no distribution).  A_log ~ 0.25 N(0, 1) per
-    head and dt_bias ~ dt_center + 0.5 N(0, 1) per (head, channel), fp32, so that the bounded
-    gate's output sits mostly in (-0.5, 0) with a tail towards the bound.  Also returns
-    init_state, cu_seqlens and seqlens as ``make_inputs`` does."""
+    head and dt_bias ~ dt_center + N(0, 1) per (head, channel), fp32.  With the default centre
+    0 the bounded gate's output spans its whole range (lower_bound, 0) and averages about
+    lower_bound / 2 per token.  Also returns init_state, cu_seqlens and seqlens as
+    ``make_inputs`` does."""
     lengths = [int(x) for x in lengths]
     if any(x < 0 for x in lengths):
         raise ValueError("bad lengths")
@@ -130,7 +137,7 @@ def make_raw_inputs(lengths, heads: int, seed: int, s0_std: float | None = 0.01,
     b_logit = torch.randn(T, heads, generator=gen, device=dev, dtype=f32)
     g = torch.randn(T, heads, d, generator=gen, device=dev, dtype=f32)
     A_log = torch.randn(heads, generator=gen, device=dev, dtype=f32) * 0.25
-    dt_bias = dt_center + torch.randn(heads, d, generator=gen, device=dev, dtype=f32) * 0.5
+    dt_bias = dt_center + torch.randn(heads, d, generator=gen, device=dev, dtype=f32)
     s0 = None
     if s0_std is not None:
         s0 = torch.randn(n, heads, d, d, generator=gen, device=dev, dtype=f32) * s0_std

@@ -63,7 +63,7 @@ def test_ragged_lengths(dtype):
     x = synth.make_inputs(lens, 3, dtype, seed=5, device=DEV)
     out, fin = run_gpu(x)
     o_ref, s_ref = run_oracle(x)
-    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("out", out.cpu(), o_ref)
     assert_close("final_state", fin.cpu().numpy(), s_ref)
     # the zero-length sequence's final state is its initial state, bit for bit
     assert torch.equal(fin[8], x["init_state"][8])
@@ -79,7 +79,7 @@ def test_more_sequences_than_the_ranked_dispatch_covers():
     x = synth.make_inputs(lens, 1, torch.bfloat16, seed=12, device=DEV)
     out, fin = run_gpu(x)
     o_ref, s_ref = run_oracle(x)
-    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("out", out.cpu(), o_ref)
     assert_close("final_state", fin.cpu().numpy(), s_ref)
     k = 40
     cu = x["cu_seqlens"].cpu().tolist()
@@ -143,7 +143,7 @@ def test_no_initial_state():
     x = synth.make_inputs([100, 33], 2, torch.bfloat16, seed=6, device=DEV)
     out, fin = run_gpu(x, init=False)
     o_ref, s_ref = run_oracle(x, init=False)
-    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("out", out.cpu(), o_ref)
     assert_close("final_state", fin.cpu().numpy(), s_ref)
 
 
@@ -186,7 +186,7 @@ def test_canaries_outside_outputs_untouched():
     assert (out_buf[:pad] == -12345.0).all() and (out_buf[-pad:] == -12345.0).all()
     assert (fin_buf[:pad] == 777.0).all() and (fin_buf[-pad:] == 777.0).all()
     o_ref, s_ref = run_oracle(x)
-    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("out", out.cpu(), o_ref)
 
 
 def test_init_state_may_alias_final_state():
@@ -213,7 +213,7 @@ def test_resume_from_saved_state_and_decode_continuation():
     pb["init_state"] = a_fin
     b_out, b_fin = run_gpu(pb)
     o_ref, s_ref = run_oracle(part(0, T))
-    assert_close("resumed out", torch.cat([a_out, b_out]).float().cpu().numpy(), o_ref)
+    assert_close("resumed out", torch.cat([a_out, b_out]).cpu(), o_ref)
     assert_close("resumed state", b_fin.cpu().numpy(), s_ref)
     # one more token through the decode path equals the prefill's last token
     state = b_fin.clone()
@@ -221,9 +221,9 @@ def test_resume_from_saved_state_and_decode_continuation():
     o_dec = kda().decode_step(xt["q"], xt["k"], xt["v"], xt["log_alpha"], xt["beta"], state)
     torch.cuda.synchronize()
     o_ref1, s_ref1 = run_oracle(part(0, T + 1), windows=[(T, T + 1)])
-    assert_close("decode after prefill out", o_dec.float().cpu().numpy(), o_ref1)
+    assert_close("decode after prefill out", o_dec.cpu(), o_ref1)
     assert_close("decode after prefill state", state.cpu().numpy(), s_ref1)
-    assert_close("prefill(T+1) last", full_out[T:].float().cpu().numpy(), o_ref1)
+    assert_close("prefill(T+1) last", full_out[T:].cpu(), o_ref1)
 
 
 @pytest.mark.parametrize("groups", [1, 2, 3, 8])
@@ -245,7 +245,7 @@ def test_host_buffer_call_matches_device_call(groups, init):
     check_status()
     if groups == 3 and init:
         o_ref, s_ref = run_oracle(x)
-        assert_close("out", out_h.float().numpy(), o_ref)
+        assert_close("out", out_h, o_ref)
         assert_close("final_state", fin_h.numpy(), s_ref)
 
 
@@ -256,12 +256,103 @@ def test_deterministic():
     assert torch.equal(o1, o2) and torch.equal(f1, f2)
 
 
+# ------------------------- the bounded gate's whole range ------------------------------
+# K3's gate is lower_bound * sigmoid(...) with lower_bound = -5 ("How Kimi K3 Engineered Its Way
+# to the Frontier", section "How KDA updates its state"), so every log alpha in [-5, 0] is a
+# legitimate input.  A 64-token chunk of such gates decays by up to 320 in one channel; the
+# prefill then runs the block as shorter decay windows and must still match the token loop.
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_bounded_gate_whole_range_matches_oracle(dtype):
+    lens = [1, 15, 16, 17, 63, 64, 65, 130, 0, 200, 127, 513]
+    x = synth.make_inputs(lens, 3, dtype, seed=14, device=DEV, bounded_gate=-5.0)
+    la = x["log_alpha"].float()
+    assert la.min().item() >= -5.0 and la.max().item() <= 0.0
+    out, fin = run_gpu(x)
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", out.cpu(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+
+
+@pytest.mark.parametrize("lg", [-5.0, -4.9, -2.6, -20.0])
+def test_constant_fast_decay_matches_oracle(lg):
+    """Every token at one decay: -5 and -4.9 (16-token windows), -2.6 (a 64-token chunk decays by
+    166: 28-token windows), -20 (the steepest gate the four-token groups cover: 4-token windows).
+    Half the channels decay slowly, so the state still carries information across windows."""
+    lens = [300, 64, 77]
+    x = synth.make_inputs(lens, 2, torch.bfloat16, seed=15, device=DEV)
+    x["log_alpha"][..., :64] = lg
+    out, fin = run_gpu(x)
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", out.cpu(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+
+
+def test_fast_decay_packing_is_bit_exact():
+    """Windows depend on a sequence's own gates only: packed equals separate, bit for bit."""
+    lens = [70, 200, 1, 129]
+    x = synth.make_inputs(lens, 2, torch.bfloat16, seed=16, device=DEV, bounded_gate=-5.0)
+    out, fin = run_gpu(x)
+    cu = x["cu_seqlens"].cpu().tolist()
+    for n, L in enumerate(lens):
+        lo, hi = cu[n], cu[n + 1]
+        xs = {key: x[key][lo:hi].contiguous() for key in ("q", "k", "v", "log_alpha", "beta")}
+        xs["init_state"] = x["init_state"][n:n + 1].contiguous()
+        xs["cu_seqlens"] = torch.tensor([0, L], dtype=torch.int32, device=DEV)
+        xs["seqlens"] = [L]
+        o1, f1 = run_gpu(xs)
+        assert torch.equal(o1, out[lo:hi]) and torch.equal(f1[0], fin[n]), f"sequence {n}"
+
+
+@pytest.mark.parametrize("every", [64, 256])
+def test_fast_decay_checkpoints(every):
+    """Windows never cross a 64-token block, so checkpoints land on window ends; they match the
+    oracle's prefix states and leave outputs and final states bit-identical to the plain call."""
+    lens = [1100, 64, 513, 2085]
+    x = synth.make_inputs(lens, 2, torch.bfloat16, seed=17, device=DEV, bounded_gate=-5.0)
+    out, fin, ck = kda().fwd_chunked_checkpoints(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                                 x["cu_seqlens"], x["seqlens"], every,
+                                                 init_state=x["init_state"])
+    torch.cuda.synchronize()
+    check_status()
+    o0, f0 = run_gpu(x)
+    assert torch.equal(out, o0) and torch.equal(fin, f0)
+    assert_close("checkpoints", ck.cpu().numpy(), _checkpoint_reference(x, lens, every))
+
+
+def test_fast_decay_segmented_sequence():
+    """A split sequence (segments, their transitions, the combine and the second pass) with
+    the bounded gate's whole range; channel 0 decays slowly so the state crosses segments."""
+    lens = [70000, 300]
+    x = synth.make_inputs(lens, 1, torch.bfloat16, seed=18, device=DEV, bounded_gate=-5.0)
+    x["log_alpha"][..., 0] = -0.001
+    out, fin = run_gpu(x)
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", out.cpu(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+
+
 def test_decay_range_is_reported():
+    """Beyond the supported domain of the chunked (bf16) path: a four-token group decaying by
+    more than 80 (log alpha below -20), or a positive log alpha, sets KDA_ERR_DECAY_RANGE."""
     x = synth.make_inputs([64], 1, torch.bfloat16, seed=13, device=DEV)
-    x["log_alpha"] = torch.full_like(x["log_alpha"], -6.0)  # 64 tokens: G_C = -384
+    x["log_alpha"] = torch.full_like(x["log_alpha"], -25.0)  # four tokens: -100
     assert kda().read_device_status() == 0
     run_gpu(x, expect_status=-6)
     assert kda().read_device_status() == 0  # cleared by the read
+    x["log_alpha"] = torch.full_like(x["log_alpha"], -0.01)
+    x["log_alpha"][5, 0, 3] = 0.5
+    run_gpu(x, expect_status=-6)
+
+
+def test_fp32_inputs_compute_any_gate_exactly():
+    """fp32 inputs run the token loop in fp32, which has no exponent range to leave: a gate of
+    -25 matches the oracle to fp32 accuracy."""
+    xf = synth.make_inputs([100, 3], 2, torch.float32, seed=13, device=DEV)
+    xf["log_alpha"][..., :64] = -25.0
+    out, fin = run_gpu(xf)
+    o_ref, s_ref = run_oracle(xf)
+    assert_close("out", out.cpu(), o_ref, rel_tol=1e-5, max_tol=1e-4)
+    assert_close("final_state", fin.cpu().numpy(), s_ref, rel_tol=1e-5, max_tol=1e-4)
 
 
 # ------------------------------- full-size workloads -----------------------------------
@@ -282,7 +373,7 @@ def test_prefill_4x8k_full_size():
     out, fin = run_gpu(x)
     wins = _windows_per_sequence(x["seqlens"], 512, 512)
     o_ref, s_ref = run_oracle(x, windows=wins)
-    assert_close("out", rows_of(out, wins).float().cpu().numpy(), o_ref)
+    assert_close("out", rows_of(out, wins).cpu(), o_ref)
     assert_close("final_state", fin.cpu().numpy(), s_ref)
     check_status()
 
@@ -295,9 +386,9 @@ def test_long_256k_full_size_error_does_not_grow():
     W = 16384
     wins = [(0, W), (T - W, T)]
     o_ref, s_ref = run_oracle(x, windows=wins)
-    o = rows_of(out, wins).float().cpu().numpy()
-    first = errors(o[:W], o_ref[:W])
-    last = errors(o[W:], o_ref[W:])
+    o = rows_of(out, wins).cpu()
+    first = errors(o[:W].float().numpy(), o_ref[:W])
+    last = errors(o[W:].float().numpy(), o_ref[W:])
     assert_close("out first 16K", o[:W], o_ref[:W])
     assert_close("out last 16K", o[W:], o_ref[W:])
     assert_close("final_state", fin.cpu().numpy(), s_ref)
@@ -306,13 +397,26 @@ def test_long_256k_full_size_error_does_not_grow():
     check_status()
 
 
+def test_prefill_4x8k_full_size_fast_decay_half_the_channels():
+    """The benchmark's 4 x 8192-token, 32-head launch with log alpha = -4.9 (near K3's bound) in
+    half the key channels: every 64-token block runs as four 16-token windows."""
+    w = synth.workloads()["prefill_4x8k"]
+    x = synth.make_workload(w, device=DEV)
+    x["log_alpha"][..., :64] = -4.9
+    out, fin = run_gpu(x)
+    wins = _windows_per_sequence(x["seqlens"], 512, 512)
+    o_ref, s_ref = run_oracle(x, windows=wins)
+    assert_close("out", rows_of(out, wins).cpu(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+
+
 def test_varlen_64_full_size():
     w = synth.workloads()["varlen_64"]
     x = synth.make_workload(w, device=DEV)
     out, fin = run_gpu(x)
     wins = _windows_per_sequence(x["seqlens"])
     o_ref, s_ref = run_oracle(x, windows=wins)
-    assert_close("out", rows_of(out, wins).float().cpu().numpy(), o_ref)
+    assert_close("out", rows_of(out, wins).cpu(), o_ref)
     assert_close("final_state", fin.cpu().numpy(), s_ref)
     check_status()
 
@@ -327,7 +431,7 @@ def test_segmented_sequences_match_oracle():
     assert info["split_sequences"] == 2 and info["work_items"] == 9 + 1 + 9 + 1
     out, fin = run_gpu(x)
     o_ref, s_ref = run_oracle(x)
-    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("out", out.cpu(), o_ref)
     assert_close("final_state", fin.cpu().numpy(), s_ref)
 
 

@@ -27,13 +27,11 @@ def kda():
 
 
 def _raw(lens, H, seed, dt_bias=True):
+    # N(0, 1) raw gates, with or without an N(0, 1) bias: log alpha spans the bounded gate's
+    # whole range (lower_bound, 0) and averages about lower_bound / 2 = -2.5 per token
     x = synth.make_raw_inputs(lens, H, seed=seed, device=DEV)
     if not dt_bias:
-        # without the bias, shift the raw gate instead: N(0, 1) raw gates average a log decay of
-        # lower_bound / 2 = -2.5 per token, and a 64-token chunk of that exceeds the prefill's
-        # exponent range (it reports KDA_ERR_DECAY_RANGE, as it should)
         x["dt_bias"] = None
-        x["g_raw"] = (x["g_raw"].float() - 4.0).to(torch.bfloat16)
     return x
 
 
@@ -86,10 +84,11 @@ def test_fused_prologue_equals_prologue_then_prefill(lens, H, dt_bias):
     assert torch.equal(s1, s2)
 
 
-def test_fused_prologue_matches_oracle():
+@pytest.mark.parametrize("dt_bias", [True, False])
+def test_fused_prologue_matches_oracle(dt_bias):
     lens = [300, 64, 0, 129, 1000]
     H = 3
-    x = _raw(lens, H, seed=43)
+    x = _raw(lens, H, seed=43, dt_bias=dt_bias)
     out, fin = kda().fwd_chunked_prologue(*_raw_args(x), x["cu_seqlens"], x["seqlens"],
                                           x["A_log"], x["dt_bias"], lower_bound=LB, q_scale=QS,
                                           init_state=x["init_state"])
@@ -102,22 +101,25 @@ def test_fused_prologue_matches_oracle():
     to_bf16 = lambda a: torch.from_numpy(a).to(torch.bfloat16)
     o_ref, s_ref = oracle.recurrence(*map(to_bf16, (q, k, v, g, b)), cu, state_in=s0,
                                      threads=oracle_threads())
-    assert_close("out", out.float().cpu().numpy(), o_ref)
+    assert_close("out", out.cpu(), o_ref)
     assert_close("state", fin.cpu().numpy(), s_ref)
     # against the unrounded fp64 prologue, the bf16 storage of the inputs costs well under the
     # 1e-2 relative L2 error bound (its element-wise tail is the inputs' rounding, not the kernel's)
     o64, s64 = oracle.recurrence(q, k, v, g, b, cu, state_in=s0, threads=oracle_threads())
-    assert_close("out vs fp64 prologue", out.float().cpu().numpy(), o64, max_tol=np.inf)
+    assert_close("out vs fp64 prologue", out.cpu(), o64, max_tol=np.inf)
     assert_close("state vs fp64 prologue", fin.cpu().numpy(), s64, max_tol=np.inf)
 
 
-def test_fused_prologue_full_size_equals_unfused_and_sampled_oracle():
-    """The 4 x 8192-token, 32-head workload in the benchmark's launch configuration: the fused
-    call equals the unfused pipeline bit for bit, and three (sequence, head) units checked one
-    by one against the oracle (oracle prologue, rounded as the contract states, then the token
-    loop)."""
+@pytest.mark.parametrize("dt_bias", [True, False])
+def test_fused_prologue_full_size_equals_unfused_and_sampled_oracle(dt_bias):
+    """The 4 x 8192-token, 32-head workload in the benchmark's launch configuration, on raw gates
+    with and without a bias (log alpha across the whole bounded range): the fused call equals
+    the unfused pipeline bit for bit, and three (sequence, head) units checked one by one against
+    the oracle (oracle prologue, rounded as the contract states, then the token loop)."""
     w = synth.workloads()["prefill_4x8k"]
     x = synth.make_raw_inputs(list(w.lengths), w.heads, seed=w.seed, s0_std=w.s0_std, device=DEV)
+    if not dt_bias:
+        x["dt_bias"] = None
     out, fin = kda().fwd_chunked_prologue(*_raw_args(x), x["cu_seqlens"], x["seqlens"],
                                           x["A_log"], x["dt_bias"], lower_bound=LB, q_scale=QS,
                                           init_state=x["init_state"])
@@ -134,24 +136,48 @@ def test_fused_prologue_full_size_equals_unfused_and_sampled_oracle():
     for n, h in ((0, 0), (2, 17), (3, 31)):
         rows = slice(n * L, (n + 1) * L)
         pick = lambda t: t[rows, h:h + 1].cpu()
+        dtb = x["dt_bias"][h:h + 1].cpu() if dt_bias else None
         ref_in = oracle.prologue(*(pick(t) for t in _raw_args(x)), x["A_log"][h:h + 1].cpu(),
-                                 x["dt_bias"][h:h + 1].cpu(), lower_bound=LB, q_scale=QS)
+                                 dtb, lower_bound=LB, q_scale=QS)
         o_ref, s_ref = oracle.recurrence(*map(to_bf16, ref_in), [0, L],
                                          state_in=x["init_state"][n:n + 1, h:h + 1].cpu())
-        assert_close(f"out[{n},{h}]", out[rows, h:h + 1].float().cpu().numpy(), o_ref)
+        assert_close(f"out[{n},{h}]", out[rows, h:h + 1].cpu(), o_ref)
         assert_close(f"state[{n},{h}]", fin[n:n + 1, h:h + 1].cpu().numpy(), s_ref)
 
 
-def test_fused_prologue_reports_a_decay_beyond_the_chunk_range():
-    """Raw gates far above zero with no bias put every log alpha near the lower bound (-5): a
-    64-token chunk then decays by about 320 in log space, beyond the chunked prefill's range.
-    The call reports KDA_ERR_DECAY_RANGE in the device status word instead of returning silently
-    wrong results (as kda_fwd_chunked does for the same log alpha)."""
+def test_fused_prologue_at_the_gate_bound_matches_oracle():
+    """Raw gates far above zero put every log alpha at the lower bound (-5): a 64-token block
+    decays by 320 in log space and runs as 16-token windows.  The result equals the unfused
+    pipeline bit for bit and the oracle within the stated bound."""
+    x = _raw([256, 70], 2, seed=44, dt_bias=False)
+    x["g_raw"] = torch.full_like(x["g_raw"], 10.0)
+    out, fin = kda().fwd_chunked_prologue(*_raw_args(x), x["cu_seqlens"], x["seqlens"],
+                                          x["A_log"], None, lower_bound=LB, q_scale=QS,
+                                          init_state=x["init_state"])
+    q, k, v, g, b = kda().prologue(*_raw_args(x), x["A_log"], None, lower_bound=LB, q_scale=QS)
+    o2, s2 = kda().fwd_chunked(q, k, v, g, b, x["cu_seqlens"], x["seqlens"],
+                               init_state=x["init_state"])
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    assert torch.equal(out, o2) and torch.equal(fin, s2)
+    assert LB <= g.float().min().item() <= LB + 0.05
+    to_bf16 = lambda a: torch.from_numpy(a).to(torch.bfloat16)
+    ref_in = oracle.prologue(*_raw_args(x), x["A_log"], None, lower_bound=LB, q_scale=QS)
+    o_ref, s_ref = oracle.recurrence(*map(to_bf16, ref_in), x["cu_seqlens"].cpu(),
+                                     state_in=x["init_state"].cpu(), threads=oracle_threads())
+    assert_close("out", out.cpu(), o_ref)
+    assert_close("state", fin.cpu().numpy(), s_ref)
+
+
+def test_fused_prologue_reports_a_gate_beyond_the_supported_range():
+    """A lower bound of -30 lets a four-token group decay by up to 120 in one channel, beyond
+    what the windows cover; the call reports KDA_ERR_DECAY_RANGE in the device status word
+    instead of returning silently wrong results."""
     x = _raw([256, 70], 2, seed=44, dt_bias=False)
     x["g_raw"] = torch.full_like(x["g_raw"], 10.0)
     assert kda().read_device_status() == 0
     kda().fwd_chunked_prologue(*_raw_args(x), x["cu_seqlens"], x["seqlens"], x["A_log"], None,
-                               lower_bound=LB, q_scale=QS, init_state=x["init_state"])
+                               lower_bound=-30.0, q_scale=QS, init_state=x["init_state"])
     assert kda().read_device_status() == -6
     assert kda().read_device_status() == 0  # read and cleared
 
@@ -177,7 +203,7 @@ def test_decode_step_prologue_equals_prologue_then_step_and_oracle():
     ref_in = _oracle_inputs(x)
     sel = lambda a: to_bf16(a[idx])
     o_ref, s_ref = oracle.decode_step(*map(sel, ref_in), state0[idx].cpu())
-    assert_close("out", o1[idx].float().cpu().numpy(), o_ref)
+    assert_close("out", o1[idx].cpu(), o_ref)
     assert_close("state", s1[idx].cpu().numpy(), s_ref)
 
 
