@@ -61,7 +61,13 @@ typedef enum kda_dtype { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
 
 /* Problem description.  host_seqlens is a HOST array of num_seqs lengths; it must equal the
  * differences of the device cu_seqlens array.  It lets the library size grids and workspace
- * without reading device memory. */
+ * without reading device memory.  The kernels check what they derive from the device array
+ * against it before touching memory: a prefill CTA compares its sequence's length with the
+ * host's (for calls of at most 2,048 sequences) and every derived offset (tokens, segment
+ * workspace slots, checkpoint slots) with the host totals; the backward, decode-window and
+ * fp32 prefill kernels check the token range and the workspace blocks.  A disagreement sets
+ * KDA_ERR_INVALID_ARG in the device status word (read it with kda_read_device_status) and the
+ * affected work item writes nothing. */
 typedef struct kda_desc {
     int32_t num_seqs;            /* N >= 1                                            */
     int32_t num_heads;           /* H >= 1                                            */

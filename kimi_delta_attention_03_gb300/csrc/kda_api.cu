@@ -120,7 +120,8 @@ kda_status decode_window_impl(const kda_desc* desc, const void* q, const void* k
     if (!status) return KDA_ERR_CUDA;
     cudaError_t e = kda::launch_decode_window(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k,
                                               v, log_alpha, beta, cu_seqlens, state, state, out,
-                                              commit, (cudaStream_t)stream, pro ? &pp : nullptr);
+                                              commit, desc->total_tokens, 64, status,
+                                              (cudaStream_t)stream, pro ? &pp : nullptr);
     g_launches += 1;
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -224,7 +225,8 @@ kda_status fwd_chunked_impl(const kda_desc* desc, const void* q, const void* k, 
     else {  // fp32 inputs: the token loop in fp32 over whole sequences (exact for every gate)
         e = kda::launch_decode_window(desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v,
                                       log_alpha, beta, cu_seqlens, init_state, final_state, out,
-                                      nullptr, (cudaStream_t)stream);
+                                      nullptr, desc->total_tokens, INT32_MAX, status,
+                                      (cudaStream_t)stream);
         ++launches;
     }
     g_launches += launches;
@@ -404,10 +406,13 @@ kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const voi
         return KDA_ERR_INVALID_ARG;
     const size_t need = kda_bwd_workspace_bytes(desc);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
+    int* status = status_word();
+    if (!status) return KDA_ERR_CUDA;
     cudaError_t e = kda::launch_backward(
         desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v, log_alpha, beta, cu_seqlens,
         init_state, d_out, d_state, dq, dk, dv, dlog_alpha, dbeta, dinit_state,
-        static_cast<float*>(workspace), bwd_floats_per_unit(desc), (cudaStream_t)stream);
+        static_cast<float*>(workspace), bwd_floats_per_unit(desc), desc->total_tokens, status,
+        (cudaStream_t)stream);
     g_launches += 1;
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -64,6 +64,8 @@ struct BwdArgs {
     float* work;              // per unit: (nb_max + kBwdBlock) states of 128 x 128, then
                               // kBwdBlock pairs of 128-vectors (u, r)
     int64_t work_per_unit;    // floats
+    int64_t total_tokens;     // host T_tot
+    int* status;              // sticky status word
     int H;
 };
 
@@ -80,6 +82,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) kda_bwd_kernel(const BwdArgs<T
     const int64_t t0 = p.cu_seqlens[n];
     const int L = (int)(p.cu_seqlens[n + 1] - t0);
     const int nb = (L + kBwdBlock - 1) / kBwdBlock;
+    // The device cu_seqlens must agree with the host lengths the workspace was sized from: the
+    // tokens stay inside T_tot and the unit's blocks inside its workspace region.
+    if (t0 < 0 || L < 0 || t0 + L > p.total_tokens ||
+        nb > (p.work_per_unit - kBwdBlock * 2 * kDim) / (kDim * kDim) - kBwdBlock) {
+        if (tid == 0) report_status(p.status, KDA_ERR_INVALID_ARG);
+        return;
+    }
     float* ck = p.work + unit * p.work_per_unit;      // [nb][128 * 128]: state before block b
     float* blk = ck + (int64_t)nb * kDim * kDim;     // [kBwdBlock][128 * 128]: S' within a block
     float* blk_ur = p.work + unit * p.work_per_unit + p.work_per_unit - kBwdBlock * 2 * kDim;
@@ -304,19 +313,21 @@ cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, c
                             const int32_t* cu_seqlens, const float* init_state,
                             const float* d_out, const float* d_state, float* dq, float* dk,
                             float* dv, float* dg, float* dbeta, float* d_init, float* work,
-                            int64_t work_per_unit, cudaStream_t stream) {
+                            int64_t work_per_unit, int64_t total_tokens, int* status,
+                            cudaStream_t stream) {
     const int64_t units = (int64_t)num_seqs * heads;
     if (units <= 0) return cudaSuccess;
     if (dtype == KDA_BF16) {
         using T = __nv_bfloat16;
         const BwdArgs<T> a{(const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta,
                            cu_seqlens, init_state, d_out, d_state, dq, dk, dv, dg, dbeta, d_init,
-                           work, work_per_unit, heads};
+                           work, work_per_unit, total_tokens, status, heads};
         kda_bwd_kernel<T><<<(unsigned)units, kBwdThreads, 0, stream>>>(a);
     } else {
         const BwdArgs<float> a{(const float*)q, (const float*)k, (const float*)v, (const float*)g,
                                (const float*)beta, cu_seqlens, init_state, d_out, d_state, dq,
-                               dk, dv, dg, dbeta, d_init, work, work_per_unit, heads};
+                               dk, dv, dg, dbeta, d_init, work, work_per_unit, total_tokens, status,
+                               heads};
         kda_bwd_kernel<float><<<(unsigned)units, kBwdThreads, 0, stream>>>(a);
     }
     return cudaGetLastError();

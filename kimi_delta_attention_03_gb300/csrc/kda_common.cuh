@@ -69,13 +69,23 @@ struct SegWorkspace {
     int max_segments;  // 1 when no sequence is split (the workspace is then unused)
 };
 
-// Dispatch order of the prefill CTAs: sequences ranked by chunk count, longest first (ties in
-// packing order), so that the longest units start in the first wave.  Only the order in which
-// units are scheduled changes; every unit computes the same bits wherever it runs.
+// The host's plan of a prefill call, passed by value to its kernels.
+//  - Dispatch order of the CTAs: sequences ranked by chunk count, longest first (ties in packing
+//    order), so that the longest units start in the first wave.  Only the order in which units
+//    are scheduled changes; every unit computes the same bits wherever it runs.
+//  - The host's sequence lengths and totals, against which every CTA checks what it derives from
+//    the device cu_seqlens before it touches memory (a disagreement sets KDA_ERR_INVALID_ARG and
+//    the CTA returns): its own length (when the call has at most kMaxOrdered sequences), and the
+//    bounds of every derived offset (tokens, segment workspace slots, checkpoint slots).
 constexpr int kMaxOrdered = 2048;
 struct SeqOrder {
-    int32_t count;                  // ranked sequences; 0 = packing order
+    int32_t count;                  // ranked sequences; 0 = packing order, no lengths below
+    int32_t num_seqs;
+    int64_t total_tokens;           // host T_tot
+    int64_t total_slots;            // host segment workspace slots (per head)
+    int64_t total_ckpts;            // host checkpoint count (per head), when checkpoints are written
     uint16_t seq[kMaxOrdered];      // seq[rank] = sequence index
+    int32_t len[kMaxOrdered];       // len[n] = host length of sequence n (when count > 0)
 };
 
 // Input prologue parameters (raw projections in; see kda_prologue.cuh).
@@ -107,11 +117,14 @@ cudaError_t launch_decode(int dtype, int64_t units, int heads, const void* q, co
                           const ProParams* pro = nullptr);
 
 // The state is read from state_in (zeros when null) and written to state_out (skipped when
-// null); they may be the same array.  Also the prefill of fp32 inputs (commit null).
+// null); they may be the same array.  Also the prefill of fp32 inputs (commit null).  A unit
+// whose device cu_seqlens run leaves [0, total_tokens) or exceeds max_len tokens sets
+// KDA_ERR_INVALID_ARG in *status and is skipped.
 cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void* q,
                                  const void* k, const void* v, const void* g, const void* beta,
                                  const int32_t* cu_seqlens, const float* state_in,
                                  float* state_out, void* out, const int32_t* commit,
+                                 int64_t total_tokens, int max_len, int* status,
                                  cudaStream_t stream, const ProParams* pro = nullptr);
 
 // The prologue alone over `rows` (token, head) rows, bf16 in and out.
@@ -128,7 +141,8 @@ cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, c
                             const int32_t* cu_seqlens, const float* init_state,
                             const float* d_out, const float* d_state, float* dq, float* dk,
                             float* dv, float* dg, float* dbeta, float* d_init, float* work,
-                            int64_t work_per_unit, cudaStream_t stream);
+                            int64_t work_per_unit, int64_t total_tokens, int* status,
+                            cudaStream_t stream);
 
 // One CTA whose bounded wait runs out: the status word then reads KDA_ERR_TIMEOUT.
 cudaError_t launch_wait_selftest(int* status, cudaStream_t stream);

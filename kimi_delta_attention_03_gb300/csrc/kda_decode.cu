@@ -174,7 +174,7 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                          const TIn* __restrict__ beta, const int32_t* __restrict__ cu_seqlens,
                          const float* state_in, float* state_out, TIn* __restrict__ out,
                          const int32_t* __restrict__ commit, int64_t units, int H,
-                         const DecPro pro) {
+                         int64_t total_tokens, int max_len, int* status, const DecPro pro) {
     __shared__ float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_u[kDim];
     __shared__ float sw_k[kPro ? kDim : 1], sw_q[kPro ? kDim : 1];  // Swish of raw k, q
     __shared__ __align__(16) float s_rx[8][kDim];
@@ -189,7 +189,13 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         const int64_t n = unit / H;
         const int h = (int)(unit - n * H);
         const int64_t t0 = cu_seqlens[n];
-        const int len = (int)(cu_seqlens[n + 1] - t0);
+        const int64_t len64 = cu_seqlens[n + 1] - t0;
+        if (t0 < 0 || len64 < 0 || t0 + len64 > total_tokens || len64 > max_len) {
+            // the device cu_seqlens disagree with the host lengths the call was checked against
+            if (tid == 0) report_status(status, KDA_ERR_INVALID_ARG);
+            continue;
+        }
+        const int len = (int)len64;
         const int ncommit = commit ? min(max(commit[n], 0), len) : len;
         const float* Sin = state_in ? state_in + unit * (int64_t)(kDim * kDim) : nullptr;
         float* S = state_out ? state_out + unit * (int64_t)(kDim * kDim) : nullptr;
@@ -332,6 +338,7 @@ cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void*
                                  const void* k, const void* v, const void* g, const void* beta,
                                  const int32_t* cu_seqlens, const float* state_in,
                                  float* state_out, void* out, const int32_t* commit,
+                                 int64_t total_tokens, int max_len, int* status,
                                  cudaStream_t stream, const ProParams* pro) {
     const int64_t units = (int64_t)num_seqs * heads;
     if (units <= 0) return cudaSuccess;
@@ -355,12 +362,12 @@ cudaError_t launch_decode_window(int dtype, int num_seqs, int heads, const void*
     if (dtype == KDA_BF16) {
         kernel<<<grid, kDecodeThreads, 0, stream>>>(
             (const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta, cu_seqlens,
-            state_in, state_out, (T*)out, commit, units, heads, dp);
+            state_in, state_out, (T*)out, commit, units, heads, total_tokens, max_len, status, dp);
     } else {
         kda_decode_window_kernel<float, false><<<grid, kDecodeThreads, 0, stream>>>(
             (const float*)q, (const float*)k, (const float*)v, (const float*)g,
             (const float*)beta, cu_seqlens, state_in, state_out, (float*)out, commit, units,
-            heads, dp);
+            heads, total_tokens, max_len, status, dp);
     }
     return cudaGetLastError();
 }

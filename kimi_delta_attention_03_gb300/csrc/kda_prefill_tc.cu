@@ -606,6 +606,9 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int64_t seq_len = p.cu_seqlens[n + 1] - seq_begin;
     const int64_t unit = (int64_t)n * H + h;
     const int nseg = num_segments(seq_len);
+    // the device cu_seqlens must agree with the host plan the buffers were sized from
+    bool bad = seq_begin < 0 || seq_len < 0 || seq_begin + seq_len > order.total_tokens ||
+               (order.count > 0 && seq_len != order.len[n]);
 
     // ---- work item of this CTA ----
     int item;
@@ -634,7 +637,18 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int ns = num_segments((int64_t)p.cu_seqlens[m + 1] - p.cu_seqlens[m]);
             if (ns > 1) base += ns;
         }
+        bad |= base + nseg > order.total_slots;
         slot = ((base + sigma) * H + h) * (int64_t)(kDim * kDim);
+    }
+    if (kCkpt && p.ckpt && !bad) {  // the checkpoints this sequence writes fit the host's count
+        const int every = kChunk * p.ckpt_chunks;
+        int64_t base = 0;
+        for (int m = 0; m <= n; ++m) base += (p.cu_seqlens[m + 1] - p.cu_seqlens[m]) / every;
+        bad |= base > order.total_ckpts;
+    }
+    if (bad) {
+        if (threadIdx.x == 0) report_status(p.status, KDA_ERR_INVALID_ARG);
+        return;
     }
     const bool has_out = item == ITEM_WHOLE || item == ITEM_SEGMENT;
     const bool zero_v = item == ITEM_TRANS;
@@ -1478,7 +1492,8 @@ constexpr int kCombineLdM = kDim + 2;  // M is kept transposed, rows padded agai
 __global__ void __launch_bounds__(kCombineThreads, 1)
 kda_segment_combine_kernel(const int32_t* __restrict__ cu_seqlens, const float* __restrict__ init_state,
                            const float* __restrict__ ws_tilde, const float* __restrict__ ws_trans,
-                           float* __restrict__ ws_in, int H) {
+                           float* __restrict__ ws_in, int H, int* status,
+                           const __grid_constant__ SeqOrder plan) {
     extern __shared__ __align__(16) float cs[];
     float* Mt = cs;                         // [128][130]: Mt[k][row] = M[row][k]
     float* S = cs + kDim * kCombineLdM;     // [128][16]: columns 16 cb .. 16 cb + 15 of the state
@@ -1490,6 +1505,11 @@ kda_segment_combine_kernel(const int32_t* __restrict__ cu_seqlens, const float* 
     for (int m = 0; m < n; ++m) {
         const int ns = num_segments((int64_t)cu_seqlens[m + 1] - cu_seqlens[m]);
         if (ns > 1) base += ns;
+    }
+    // the device cu_seqlens must agree with the host plan the workspace was sized from
+    if (base + nseg > plan.total_slots || (plan.count > 0 && len != plan.len[n])) {
+        if (tid == 0) report_status(status, KDA_ERR_INVALID_ARG);
+        return;
     }
     const int64_t unit = (int64_t)n * H + h;
     const int c0 = kCombineCols * cb;
@@ -1584,12 +1604,29 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
     if (units > INT32_MAX) return cudaErrorInvalidValue;
     SeqOrder order;
     order.count = 0;
+    order.num_seqs = num_seqs;
+    order.total_tokens = total_tokens;
+    order.total_slots = INT64_MAX;  // without host lengths only the token bound is checked
+    order.total_ckpts = INT64_MAX;
+    if (host_seqlens) {
+        int64_t slots = 0, ckpts = 0;
+        for (int n = 0; n < num_seqs; ++n) {
+            const int ns = num_segments(host_seqlens[n]);
+            if (ns > 1) slots += ns;
+            if (ckpt_chunks > 0) ckpts += host_seqlens[n] / (kChunk * ckpt_chunks);
+        }
+        order.total_slots = slots;
+        order.total_ckpts = ckpts;
+    }
     if (host_seqlens && num_seqs <= kMaxOrdered) {
         std::vector<int> idx(num_seqs);
         std::iota(idx.begin(), idx.end(), 0);
         auto nc = [&](int i) { return ((int64_t)host_seqlens[i] + kChunk - 1) / kChunk; };
         std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return nc(a) > nc(b); });
-        for (int r = 0; r < num_seqs; ++r) order.seq[r] = (uint16_t)idx[r];
+        for (int r = 0; r < num_seqs; ++r) {
+            order.seq[r] = (uint16_t)idx[r];
+            order.len[r] = host_seqlens[r];
+        }
         order.count = num_seqs;
     }
     CUtensorMap mq, mk, mv, mg;
@@ -1635,7 +1672,7 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
         return e;
     kda_segment_combine_kernel<<<dim3(num_seqs, heads, kCombineColBlocks), kCombineThreads, csmem,
                                  stream>>>(
-        cu_seqlens, init_state, ws.tilde, ws.trans, ws.in, heads);
+        cu_seqlens, init_state, ws.tilde, ws.trans, ws.in, heads, status, order);
     if (launches) ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // pass B: every segment of the split sequences from its composed incoming state

@@ -63,3 +63,44 @@ def test_backward_long_sequence():
         x["cu_seqlens"].cpu(), d_out.cpu(), state_in=x["init_state"].cpu(), d_state=d_state.cpu())
     for name, g, r in zip(NAMES, got, ref):
         assert_close(name, g.cpu().numpy(), r)
+
+
+def test_backward_device_lengths_beyond_the_workspace_are_reported():
+    """The workspace is sized from the host lengths (one state per 16 tokens of the longest
+    sequence); a device cu_seqlens with a longer sequence (same total) would run past its unit's
+    region, so the kernel checks the block count first and reports KDA_ERR_INVALID_ARG."""
+    host, device = [16, 16], [0, 2, 32]
+    x = synth.make_inputs(host, 1, torch.bfloat16, seed=75, device=DEV)
+    d_out = torch.ones(32, 1, 128, device=DEV)
+    bad_cu = torch.tensor(device, dtype=torch.int32, device=DEV)
+    assert kda().read_device_status() == 0
+    kda().bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], bad_cu, x["seqlens"], d_out,
+              init_state=x["init_state"])
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == -1
+
+
+def test_backward_full_size_first_and_last_unit():
+    """The benchmark's 4 x 8192-token, 32-head backward (a 4.4 GB workspace, so the last unit's
+    offsets pass 2^32 bytes), in the launch the benchmark times; the first and the last
+    (sequence, head) unit compared with the oracle run on those units alone."""
+    w = synth.workloads()["prefill_4x8k"]
+    x = synth.make_workload(w, device=DEV)
+    T, H, N, L = x["q"].shape[0], w.heads, len(w.lengths), w.lengths[0]
+    gen = torch.Generator(device=DEV).manual_seed(76)
+    d_out = torch.randn(T, H, 128, generator=gen, device=DEV)
+    d_state = torch.randn(N, H, 128, 128, generator=gen, device=DEV) * 0.1
+    got = kda().bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                    x["seqlens"], d_out, init_state=x["init_state"], d_state=d_state)
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    for n, h in ((0, 0), (N - 1, H - 1)):
+        rows = slice(n * L, (n + 1) * L)
+        pick = lambda t: t[rows, h:h + 1].cpu()
+        ref = oracle.recurrence_backward(
+            *(pick(x[key]) for key in ("q", "k", "v", "log_alpha", "beta")), [0, L],
+            pick(d_out), state_in=x["init_state"][n:n + 1, h:h + 1].cpu(),
+            d_state=d_state[n:n + 1, h:h + 1].cpu())
+        mine = [t[rows, h:h + 1] for t in got[:5]] + [got[5][n:n + 1, h:h + 1]]
+        for name, g, r in zip(NAMES, mine, ref):
+            assert_close(f"{name}[{n},{h}]", g.cpu().numpy(), r)

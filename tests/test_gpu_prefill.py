@@ -344,6 +344,31 @@ def test_decay_range_is_reported():
     run_gpu(x, expect_status=-6)
 
 
+@pytest.mark.parametrize("host,device", [
+    ([70000, 100], [0, 100, 70100]),  # same total: the split moves to the other sequence
+    ([100, 28], [0, 28, 128]),         # same total, no split
+])
+def test_device_cu_seqlens_disagreeing_with_host_lengths_is_reported(host, device):
+    """Every CTA checks its device-derived length (and every derived offset) against the host
+    plan before it touches memory: a disagreement sets KDA_ERR_INVALID_ARG and nothing is
+    written.  The buffers are sized from the host lengths, and the device lengths keep the same
+    total, so no access could leave them even if a check were missing.  The next call with
+    agreeing arrays still matches the oracle."""
+    x = synth.make_inputs(host, 2, torch.bfloat16, seed=19, device=DEV)
+    bad_cu = torch.tensor(device, dtype=torch.int32, device=DEV)
+    assert kda().read_device_status() == 0
+    out = torch.full_like(x["q"], 7.0)
+    kda().fwd_chunked(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], bad_cu, x["seqlens"],
+                      init_state=x["init_state"], out=out)
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == -1  # KDA_ERR_INVALID_ARG
+    assert (out == 7.0).all()  # no CTA wrote
+    got, fin = run_gpu(x)
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", got.cpu(), o_ref)
+    assert_close("final_state", fin.cpu().numpy(), s_ref)
+
+
 def test_fp32_inputs_compute_any_gate_exactly():
     """fp32 inputs run the token loop in fp32, which has no exponent range to leave: a gate of
     -25 matches the oracle to fp32 accuracy."""
