@@ -75,7 +75,7 @@ constexpr int kBarEpi = 2;
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (about 2 s)
 constexpr float kLog2eTC = 1.4426950408889634f;
 constexpr float kWindowDecay = 80.f;  // largest |G_C| of a window (so |G - r| <= 40)
-constexpr float kHeavyDecay = 16.f;   // chunks decaying faster in some channel form P's diagonal
+constexpr float kHeavyDecay = 48.f;   // chunks decaying faster in some channel form P's diagonal
                                       // from the raw q, k (it then dominates the output)
 constexpr int kWinRing = 8;     // window records kept: the oldest reader is two chunks behind
 constexpr int LDA_T = 68;       // fp32 row stride of the 64 x 64 A / T matrix
@@ -124,7 +124,7 @@ enum {
     B_XDONE, B_UREADY, B_OSDONE, B_SREADY, B_DRAIN, B_UFREE0, B_UFREE1, B_KMFREE0, B_KMFREE1, B_KMFREE2,
     B_SDONE, B_PFREE0, B_PFREE1, B_SCAN0, B_SCAN1, B_GFULL, B_M6ISS,
     B_VPRO,  // prologue variant: v of the chunk has been through Swish
-    B_KQPRO0, B_KQPRO1,  // prologue variant: k, q of the slot are transformed (256 arrivals)
+    B_KQPRO0, B_KQPRO1,  // prologue variant: k, q of the slot are transformed (one per prep warp)
     B_COUNT
 };
 static_assert(B_COUNT <= NBAR, "barrier slots");
@@ -703,7 +703,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                 make_uint4(0u, 0u, 0u, 0u);
     if (tid == 32) {
         for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(&bars[i], i == B_KQPRO0 || i == B_KQPRO1 ? kPrepThreads : 1);
+            mbar_init(&bars[i], i == B_KQPRO0 || i == B_KQPRO1 ? kPrepThreads / 32 : 1);
         *abort_flag = 0;
         *kqg_issued = 0;
         mbar_init_fence();
@@ -961,7 +961,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     *reinterpret_cast<uint4*>(kq + o) = pack8(kv);
                     *reinterpret_cast<uint4*>(kq + o + 64 * 128) = pack8(qv);
                 }
-                mbar_arrive(&bars[B_KQPRO0 + s]);  // the scan may read the transformed tiles
+                __syncwarp();  // the scan may read the transformed tiles
+                if (lane == 0) mbar_arrive(&bars[B_KQPRO0 + s]);
             }
 
             // ---- decay factors: thread (tg, cg) owns tokens 4tg..4tg+3, channels 8cg..8cg+7.
