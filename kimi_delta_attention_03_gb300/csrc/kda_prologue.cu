@@ -120,7 +120,7 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
 // ShortConv caches of kernel size 4 per layer).  Cache layout: bf16 [N][3 tensors q, k, v][3
 // inputs, oldest first][H][128].  The convolution is in fp32 and feeds the prologue unrounded.
 
-constexpr int kConvRun = 16;  // consecutive tokens of one head per warp
+constexpr int kConvRun = 64;  // consecutive tokens of one head per warp
 
 // x_{tp} of `src` for one lane's channels: a raw row of the sequence, or the cache before it
 template <int kN>
@@ -146,11 +146,14 @@ __device__ __forceinline__ void conv_tap(const bf16* __restrict__ src, const bf1
 
 // The convolution along a run of tokens for one lane's kN channels of one tensor: the window
 // x_{t-3} .. x_t slides one token per step (refilled from the cache or zeros at each sequence
-// start); the taps are re-read each step from L1 (the run keeps them there), and taps 0..3
-// accumulate in that order.
+// start); the taps are re-read each step from shared memory, where the CTA staged its head's
+// taps so that each tap's four-channel vectors lie contiguous across the lanes (tp[j * kStride +
+// 4 (kN / 4) h4] for tap j and channel quad h4 of this lane), and taps 0..3 accumulate in that
+// order.
 template <int kN>
 struct ConvLane {
-    const float* wp;   // taps of the lane's first channel: [kN][4]
+    const float4* tp;  // the lane's first channel quad of tap 0
+    static constexpr int kStride = 32;  // float4 between taps
     float win[3][kN];  // x_{t-3}, x_{t-2}, x_{t-1}
     __device__ __forceinline__ void fill(const bf16* __restrict__ src, const bf16* __restrict__ cache,
                                          int64_t t, int64_t a, int n, int tensor, int h, int H,
@@ -160,21 +163,54 @@ struct ConvLane {
     }
     __device__ __forceinline__ void step(const float (&x)[kN], float (&y)[kN]) {
 #pragma unroll
-        for (int i = 0; i < kN; ++i) {
-            const float4 w = __ldg(reinterpret_cast<const float4*>(wp) + i);
-            float acc = 0.f;
-            acc = fmaf(w.x, win[0][i], acc);
-            acc = fmaf(w.y, win[1][i], acc);
-            acc = fmaf(w.z, win[2][i], acc);
-            y[i] = fmaf(w.w, x[i], acc);
-            win[0][i] = win[1][i];
-            win[1][i] = win[2][i];
-            win[2][i] = x[i];
+        for (int h4 = 0; h4 < kN / 4; ++h4) {
+            float w[4][4];  // w[j][c]: tap j of channel 4 h4 + c
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 t = tp[j * kStride + 16 * h4];
+                w[j][0] = t.x; w[j][1] = t.y; w[j][2] = t.z; w[j][3] = t.w;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int i = 4 * h4 + c;
+                float acc = 0.f;
+                acc = fmaf(w[0][c], win[0][i], acc);
+                acc = fmaf(w[1][c], win[1][i], acc);
+                acc = fmaf(w[2][c], win[2][i], acc);
+                y[i] = fmaf(w[3][c], x[i], acc);
+                win[0][i] = win[1][i];
+                win[1][i] = win[2][i];
+                win[2][i] = x[i];
+            }
         }
     }
 };
 
-// One warp per (head, run of kConvRun consecutive tokens); runs may cross sequence boundaries.
+// cp.async of one lane's bytes into shared memory (16, 8 or 4 bytes; both addresses aligned)
+template <int kBytes>
+__device__ __forceinline__ void cp_async(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "n"(kBytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+// One CTA per (head, group of 8 runs of kConvRun consecutive tokens), one run per warp; runs may
+// cross sequence boundaries.  The CTA stages its head's taps in shared memory once.  The raw rows
+// stream through a per-warp ring of kConvStages token slots in shared memory, filled with
+// cp.async kConvStages tokens ahead (each lane copies, and later reads, only its own bytes), so
+// every warp keeps several rows in flight without spending registers on them.  beta takes one
+// token per lane, 32 tokens at a time.
+constexpr int kConvStages = 4;
+struct ConvSlot {
+    uint4 qk[32];  // lane l: eight q (l < 16) or k channels
+    uint2 v[32];   // lane l: four v channels
+    uint2 g[32];   // lane l: four g channels
+};
 __global__ void __launch_bounds__(kProThreads)
 kda_prologue_conv_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_raw,
                          const bf16* __restrict__ v_raw, const bf16* __restrict__ g_raw,
@@ -185,16 +221,39 @@ kda_prologue_conv_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict_
                          const int32_t* __restrict__ cu_seqlens, int num_seqs,
                          bf16* __restrict__ q, bf16* __restrict__ k, bf16* __restrict__ v,
                          bf16* __restrict__ g, bf16* __restrict__ beta, int64_t T, int H) {
-    const int lane = threadIdx.x & 31;
+    __shared__ ConvSlot ring[kProThreads / 32][kConvStages];
+    // the head's taps: q, k as [tensor][tap][channel half][16 lanes] float4, then v as
+    // [tap][32 lanes] float4 (see ConvLane)
+    __shared__ float4 taps[3 * 128];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    ConvSlot* slots = ring[warp];
     const bool is_q = lane < 16;  // lanes 0-15: q channels; lanes 16-31: k channels
     const int chqk = 8 * (lane & 15), chv = 4 * lane;
+    constexpr int kWarps = kProThreads / 32;
     const int64_t runs = (T + kConvRun - 1) / kConvRun;
-    const int64_t items = runs * H;
-    const int64_t warps = (int64_t)gridDim.x * (kProThreads / 32);
-    for (int64_t item = (int64_t)blockIdx.x * (kProThreads / 32) + (threadIdx.x >> 5); item < items;
-         item += warps) {
-        const int h = (int)(item % H);
-        const int64_t t0 = (item / H) * kConvRun;
+    const int64_t groups = (runs + kWarps - 1) / kWarps;
+    int staged = -1;  // head whose taps are in shared memory
+    for (int64_t citem = blockIdx.x; citem < groups * H; citem += gridDim.x) {
+        const int h = (int)(citem / groups);
+        const int64_t run = (citem % groups) * kWarps + warp;
+        if (h != staged) {
+            __syncthreads();  // every warp is done with the previous head's taps
+            float* tf = reinterpret_cast<float*>(taps);
+            for (int e = threadIdx.x; e < 3 * kDim; e += kProThreads) {
+                const int t = e >> 7, c = e & (kDim - 1);
+                const float* wsrc = t == 0 ? w_q : t == 1 ? w_k : w_v;
+                const float4 w4 = *reinterpret_cast<const float4*>(wsrc + ((int64_t)h * kDim + c) * 4);
+                const float wj[4] = {w4.x, w4.y, w4.z, w4.w};
+                const int idx = t < 2 ? t * 128 + ((c >> 2) & 1) * 16 + (c >> 3)
+                                      : 256 + (c >> 2);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tf[(idx + 32 * j) * 4 + (c & 3)] = wj[j];
+            }
+            __syncthreads();
+            staged = h;
+        }
+        if (run >= runs) continue;
+        const int64_t t0 = run * kConvRun;
         const int64_t t1 = t0 + kConvRun < T ? t0 + kConvRun : T;
         // the sequence of token t0: the last n with cu_seqlens[n] <= t0
         int lo = 0, hi = num_seqs;
@@ -206,32 +265,46 @@ kda_prologue_conv_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict_
         int64_t a = cu_seqlens[n], b = cu_seqlens[n + 1];
         ConvLane<8> cqk;
         ConvLane<4> cv;
-        cqk.wp = (is_q ? w_q : w_k) + ((int64_t)h * kDim + chqk) * 4;
-        cv.wp = w_v + ((int64_t)h * kDim + chv) * 4;
+        cqk.tp = taps + (is_q ? 0 : 128) + (lane & 15);
+        cv.tp = taps + 256 + lane;
         const bf16* src_qk = is_q ? q_raw : k_raw;
-        cqk.fill(src_qk, cache, t0, a, n, is_q ? 0 : 1, h, H, chqk);
-        cv.fill(v_raw, cache, t0, a, n, 2, h, H, chv);
         const float na = pro_gate_rate(A_log, h);
         float dt[4] = {0.f, 0.f, 0.f, 0.f};
         if (dt_bias) {
             const float4 d4 = *reinterpret_cast<const float4*>(dt_bias + h * kDim + chv);
             dt[0] = d4.x; dt[1] = d4.y; dt[2] = d4.z; dt[3] = d4.w;
         }
-        // this token's raw inputs, loaded one token ahead
-        auto fetch = [&](int64_t t, uint4& qk, uint2& vr, uint2& gr) {
+        // token t's raw rows into its ring slot
+        auto issue = [&](int64_t t) {
+            ConvSlot& sl = slots[(t - t0) % kConvStages];
             const int64_t base = (t * H + h) * kDim;
-            qk = __ldcs(reinterpret_cast<const uint4*>(src_qk + base + chqk));
-            vr = __ldcs(reinterpret_cast<const uint2*>(v_raw + base + chv));
-            gr = __ldcs(reinterpret_cast<const uint2*>(g_raw + base + chv));
+            cp_async<16>(&sl.qk[lane], src_qk + base + chqk);
+            cp_async<8>(&sl.v[lane], v_raw + base + chv);
+            cp_async<8>(&sl.g[lane], g_raw + base + chv);
         };
-        uint4 nqk;
-        uint2 nvr, ngr;
-        fetch(t0, nqk, nvr, ngr);
+        __syncwarp();  // the ring's previous run is read out
+#pragma unroll
+        for (int i = 0; i < kConvStages; ++i) {  // one commit group per ring slot, even if empty
+            if (t0 + i < t1) issue(t0 + i);
+            cp_async_commit();
+        }
+        cqk.fill(src_qk, cache, t0, a, n, is_q ? 0 : 1, h, H, chqk);
+        cv.fill(v_raw, cache, t0, a, n, 2, h, H, chv);
+        float bl = 0.f;  // beta logit of token t0 + 32 j + lane for the current block j
 #pragma unroll 1
         for (int64_t t = t0; t < t1; ++t) {
-            const uint4 cqk_raw = nqk;
-            const uint2 vr = nvr, gr = ngr;
-            if (t + 1 < t1) fetch(t + 1, nqk, nvr, ngr);
+            const int r = (int)(t - t0);
+            if ((r & 31) == 0) {  // beta: one token per lane, the next 32 tokens
+                const int64_t tb = t + lane;
+                bl = tb < t1 ? __bfloat162float(beta_logit[tb * H + h]) : 0.f;
+                if (tb < t1) beta[tb * H + h] = __float2bfloat16_rn(pro_sigmoid(bl));
+            }
+            cp_async_wait<kConvStages - 1>();  // token t's group has landed (for this lane)
+            const ConvSlot& sl = slots[r % kConvStages];
+            const uint4 cqk_raw = sl.qk[lane];
+            const uint2 vr = sl.v[lane], gr = sl.g[lane];
+            if (t + kConvStages < t1) issue(t + kConvStages);  // the slot is read: refill it
+            cp_async_commit();
             if (t >= b) {  // a new sequence starts at t (skipping empty ones): refill the window
                 do { ++n; a = cu_seqlens[n]; b = cu_seqlens[n + 1]; } while (t >= b);
                 cqk.fill(src_qk, cache, t, a, n, is_q ? 0 : 1, h, H, chqk);
@@ -246,23 +319,21 @@ kda_prologue_conv_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict_
             cqk.step(xqk, y);
             cv.step(xv, yv);
             pro_swish_l2(y, is_q ? q_scale : 1.f);
-            *reinterpret_cast<uint4*>((is_q ? q : k) + base + chqk) =
-                make_uint4(pack2_bf16(y[0], y[1]), pack2_bf16(y[2], y[3]), pack2_bf16(y[4], y[5]),
-                           pack2_bf16(y[6], y[7]));
+            __stcs(reinterpret_cast<uint4*>((is_q ? q : k) + base + chqk),
+                   make_uint4(pack2_bf16(y[0], y[1]), pack2_bf16(y[2], y[3]),
+                              pack2_bf16(y[4], y[5]), pack2_bf16(y[6], y[7])));
             const float gv[4] = {__uint_as_float(gr.x << 16), __uint_as_float(gr.x & 0xffff0000u),
                                  __uint_as_float(gr.y << 16), __uint_as_float(gr.y & 0xffff0000u)};
-            *reinterpret_cast<uint2*>(v + base + chv) =
-                make_uint2(pack2_bf16(pro_swish(yv[0]), pro_swish(yv[1])),
-                           pack2_bf16(pro_swish(yv[2]), pro_swish(yv[3])));
-            *reinterpret_cast<uint2*>(g + base + chv) =
-                make_uint2(pack2_bf16(pro_gate(gv[0], dt[0], na, lower_bound),
-                                      pro_gate(gv[1], dt[1], na, lower_bound)),
-                           pack2_bf16(pro_gate(gv[2], dt[2], na, lower_bound),
-                                      pro_gate(gv[3], dt[3], na, lower_bound)));
-            if (lane == 0)
-                beta[t * H + h] =
-                    __float2bfloat16_rn(pro_sigmoid(__bfloat162float(beta_logit[t * H + h])));
+            __stcs(reinterpret_cast<uint2*>(v + base + chv),
+                   make_uint2(pack2_bf16(pro_swish(yv[0]), pro_swish(yv[1])),
+                              pack2_bf16(pro_swish(yv[2]), pro_swish(yv[3]))));
+            __stcs(reinterpret_cast<uint2*>(g + base + chv),
+                   make_uint2(pack2_bf16(pro_gate(gv[0], dt[0], na, lower_bound),
+                                         pro_gate(gv[1], dt[1], na, lower_bound)),
+                              pack2_bf16(pro_gate(gv[2], dt[2], na, lower_bound),
+                                         pro_gate(gv[3], dt[3], na, lower_bound))));
         }
+        cp_async_wait<0>();  // nothing of this run is in flight when the ring is reused
     }
 }
 
@@ -334,8 +405,8 @@ cudaError_t launch_prologue_conv(int64_t rows, int heads, int num_seqs, const vo
     if (rows > 0) {
         const int64_t per_block = kProThreads / 32;
         const int64_t T = rows / heads;
-        const int64_t items = (T + kConvRun - 1) / kConvRun * heads;
-        const int64_t blocks = (items + per_block - 1) / per_block;
+        const int64_t runs = (T + kConvRun - 1) / kConvRun;
+        const int64_t blocks = (runs + per_block - 1) / per_block * heads;  // (head, 8 runs)
         const unsigned grid = (unsigned)(blocks < (1LL << 30) ? blocks : (1LL << 30));
         kda_prologue_conv_kernel<<<grid, kProThreads, 0, stream>>>(
             (const bf16*)q_raw, (const bf16*)k_raw, (const bf16*)v_raw, (const bf16*)g_raw,
