@@ -29,6 +29,8 @@
  *     the fixed scratch array behind kda_fwd_chunked_noalloc().
  *   - Every compute entry point is asynchronous on `stream` (NULL = legacy default stream).
  *     Host-side argument checks are synchronous and return before anything is launched.
+ *   - With KDA_NVTX=1 in the environment (read once per process), every compute entry point
+ *     wraps its launches in an NVTX range named after the entry point.
  *   - Errors: KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED / KDA_ERR_WORKSPACE from the host
  *     checks, KDA_ERR_CUDA when a launch fails.  Conditions found on the device (a gate outside
  *     the supported domain, a bounded wait that gave up) set the sticky device status word;

@@ -1,8 +1,11 @@
 // kda_api.cu — the C ABI declared in include/kda.h: host-side checks, the work plan, the
 // sticky device status word, and the kernel launches.  No allocation happens here.
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 
 #include "kda_common.cuh"
@@ -10,6 +13,26 @@
 namespace {
 
 std::atomic<uint64_t> g_launches{0};
+
+// Optional NVTX ranges, one per entry-point call, named after the entry point, so that a
+// profiler's timeline shows which library call launched which kernels.  Enabled by KDA_NVTX=1 in
+// the environment (read once per process); otherwise a call costs one branch.
+bool nvtx_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("KDA_NVTX");
+        return e && e[0] == '1';
+    }();
+    return on;
+}
+struct NvtxRange {
+    bool on;
+    explicit NvtxRange(const char* name) : on(nvtx_enabled()) {
+        if (on) nvtxRangePushA(name);
+    }
+    ~NvtxRange() {
+        if (on) nvtxRangePop();
+    }
+};
 
 // One sticky status word per device; kernels write it with atomicCAS(0 -> code).
 __device__ int g_device_status = 0;
@@ -241,6 +264,7 @@ kda_status kda_fwd_chunked(const kda_desc* desc, const void* q, const void* k, c
                            const void* log_alpha, const void* beta, const float* init_state,
                            const int32_t* cu_seqlens, void* out, float* final_state,
                            void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_fwd_chunked");
     return fwd_chunked_impl(desc, q, k, v, log_alpha, beta, init_state, cu_seqlens, out,
                             final_state, 0, nullptr, workspace, workspace_bytes, stream);
 }
@@ -258,6 +282,7 @@ kda_status kda_fwd_chunked_ckpt(const kda_desc* desc, const void* q, const void*
                                 const float* init_state, const int32_t* cu_seqlens, void* out,
                                 float* final_state, int32_t ckpt_every, float* ckpt_states,
                                 void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_fwd_chunked_ckpt");
     if (ckpt_every <= 0) return KDA_ERR_INVALID_ARG;
     return fwd_chunked_impl(desc, q, k, v, log_alpha, beta, init_state, cu_seqlens, out,
                             final_state, ckpt_every, ckpt_states, workspace, workspace_bytes,
@@ -270,6 +295,7 @@ kda_status kda_fwd_chunked_prologue(const kda_desc* desc, const kda_prologue_par
                                     const float* init_state, const int32_t* cu_seqlens, void* out,
                                     float* final_state, void* workspace, size_t workspace_bytes,
                                     kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_fwd_chunked_prologue");
     if (!prm) return KDA_ERR_INVALID_ARG;
     return fwd_chunked_impl(desc, q_raw, k_raw, v_raw, g_raw, beta_logit, init_state, cu_seqlens,
                             out, final_state, 0, nullptr, workspace, workspace_bytes, stream, prm);
@@ -279,6 +305,7 @@ kda_status kda_prologue(const kda_desc* desc, const kda_prologue_params* prm, co
                         const void* k_raw, const void* v_raw, const void* g_raw,
                         const void* beta_logit, void* q, void* k, void* v, void* log_alpha,
                         void* beta, kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_prologue");
     kda_status st = check_desc(desc, false);
     if (st != KDA_OK) return st;
     if (desc->in_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
@@ -305,6 +332,7 @@ kda_status kda_prologue_conv(const kda_desc* desc, const kda_prologue_params* pr
                              const void* q_raw, const void* k_raw, const void* v_raw,
                              const void* g_raw, const void* beta_logit, void* q, void* k, void* v,
                              void* log_alpha, void* beta, kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_prologue_conv");
     kda_status st = check_desc(desc, true);
     if (st != KDA_OK) return st;
     if (desc->in_dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
@@ -337,6 +365,7 @@ kda_status kda_prologue_conv(const kda_desc* desc, const kda_prologue_params* pr
 kda_status kda_decode_step(const kda_desc* desc, const void* q, const void* k, const void* v,
                            const void* log_alpha, const void* beta, float* state, void* out,
                            kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_decode_step");
     return decode_step_impl(desc, q, k, v, log_alpha, beta, state, out, stream, nullptr);
 }
 
@@ -344,6 +373,7 @@ kda_status kda_decode_step_prologue(const kda_desc* desc, const kda_prologue_par
                                     const void* q_raw, const void* k_raw, const void* v_raw,
                                     const void* g_raw, const void* beta_logit, float* state,
                                     void* out, kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_decode_step_prologue");
     if (!prm) return KDA_ERR_INVALID_ARG;
     return decode_step_impl(desc, q_raw, k_raw, v_raw, g_raw, beta_logit, state, out, stream, prm);
 }
@@ -351,6 +381,7 @@ kda_status kda_decode_step_prologue(const kda_desc* desc, const kda_prologue_par
 kda_status kda_decode_window(const kda_desc* desc, const void* q, const void* k, const void* v,
                              const void* log_alpha, const void* beta, const int32_t* cu_seqlens,
                              float* state, void* out, const int32_t* commit, kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_decode_window");
     return decode_window_impl(desc, q, k, v, log_alpha, beta, cu_seqlens, state, out, commit,
                               stream, nullptr);
 }
@@ -360,6 +391,7 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
                                       const void* g_raw, const void* beta_logit,
                                       const int32_t* cu_seqlens, float* state, void* out,
                                       const int32_t* commit, kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_decode_window_prologue");
     if (!prm) return KDA_ERR_INVALID_ARG;
     return decode_window_impl(desc, q_raw, k_raw, v_raw, g_raw, beta_logit, cu_seqlens, state,
                               out, commit, stream, prm);
@@ -384,6 +416,7 @@ kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const voi
                    const int32_t* cu_seqlens, const float* d_out, const float* d_state, float* dq,
                    float* dk, float* dv, float* dlog_alpha, float* dbeta, float* dinit_state,
                    void* workspace, size_t workspace_bytes, kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_bwd");
     kda_status st = check_desc(desc, true);
     if (st != KDA_OK) return st;
     if (!cu_seqlens || !dinit_state) return KDA_ERR_INVALID_ARG;
@@ -418,6 +451,7 @@ kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const voi
 }
 
 kda_status kda_selftest_wait_timeout(kda_stream_t stream) {
+    NvtxRange nvtx_range("kda_selftest_wait_timeout");
     int* status = status_word();
     if (!status) return KDA_ERR_CUDA;
     cudaError_t e = kda::launch_wait_selftest(status, (cudaStream_t)stream);
