@@ -47,9 +47,10 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-# The backward pass sits in a file of its own and no traffic record covers it, so it is left out
-# of the hash that dates the forward kernels' records.
-_UNRECORDED_SOURCES = ("kda_backward.cu",)
+# The backward pass and the host-buffer pipeline (host code only) sit in files of their own that
+# no traffic record covers, so they are left out of the hash that dates the forward kernels'
+# records.
+_UNRECORDED_SOURCES = ("kda_backward.cu", "kda_host.cu")
 
 
 def kernel_source_hash() -> str:
@@ -535,7 +536,8 @@ def main():
         del xr, raw, conv_w, conv_cache, xu, raw_u
 
     # ---------------- backward (gradients) on the headline workload ----------------
-    if not args.no_extra:
+    if not args.no_extra or args.case == "small":
+        extra = {} if extra is None else extra
         gen_b = torch.Generator(device=dev).manual_seed(w.seed)
         d_out = torch.randn(T, H, D, generator=gen_b, device=dev)
         bws = torch.empty(max(16, kda.binding.load_library().kda_bwd_workspace_bytes(
@@ -550,7 +552,7 @@ def main():
         ms_b = max_over_ranks(time_device(bstep, 2, stream), world)
         # the gradient outputs are fp32: 5 x 512 B + 4 B per token-head, plus the inputs and
         # d_out read (1,026 + 512 B) and 2 x 64 KiB of states per unit
-        extra["backward_4x8k"] = {
+        extra["backward_4x8k" if not small else "backward_small"] = {
             "workload": w.name + ": gradients of q, k, v, log alpha, beta and the initial state",
             "tokens": T, "ms_per_step": ms_b, "steps": 2,
             "value": T * world / (ms_b * 1e-3) / 1e6, "unit": "Mtokens/s",
@@ -568,14 +570,17 @@ def main():
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = host_out.numel() * host_out.element_size() + host_fin.numel() * 4
 
-        groups = 4
-        h2d += 4 * (len(x["seqlens"]) + groups)  # the per-part cumulative lengths
+        parts = 8
+        # every part's cumulative lengths (N + 1 int32; every sequence spans every part here)
+        h2d += 4 * parts * (len(x["seqlens"]) + 1)
+        e_ws = torch.empty(kda.fwd_host_workspace_bytes(x["seqlens"], H, x["q"].dtype, parts),
+                           dtype=torch.uint8, device=dev)
 
         def estep():
-            # the public host-buffer call: copies in, kernels, copies out, overlapped by part
+            # the C-ABI host-buffer call: uploads, kernels and downloads overlapped by part
             kda.fwd_chunked_host(host["q"], host["k"], host["v"], host["log_alpha"], host["beta"],
                                  x["seqlens"], init_state=host["init_state"], out=host_out,
-                                 final_state=host_fin, groups=groups)
+                                 final_state=host_fin, parts=parts, workspace=e_ws)
 
         for _ in range(2):
             estep()
@@ -584,7 +589,9 @@ def main():
         ems = max_over_ranks(time_device(estep, esteps, stream), world)
         e2e = {"value": tokens_all / (ems * 1e-3) / 1e6, "unit": "Mtokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
-               "steps": esteps, "api": "fwd_chunked_host", "parts": groups}
+               "steps": esteps, "api": "kda_fwd_chunked_host", "parts": parts,
+               "workspace_bytes": int(e_ws.numel())}
+        del e_ws
 
     # ---------------- CPU baseline (oracle, rank 0 only, N = 1 only) ----------------
     cpu_base = None

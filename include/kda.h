@@ -25,10 +25,12 @@
  *   - Only d_k = d_v = 128 is supported.
  *   - Ownership: the caller owns and allocates every buffer (device memory unless marked
  *     host).  The library never allocates or frees memory and keeps no per-call state; its
- *     only globals are the sticky device status word read by kda_read_device_status() and
- *     the fixed scratch array behind kda_fwd_chunked_noalloc().
- *   - Every compute entry point is asynchronous on `stream` (NULL = legacy default stream).
- *     Host-side argument checks are synchronous and return before anything is launched.
+ *     only globals are the sticky device status word read by kda_read_device_status(), the
+ *     fixed scratch array behind kda_fwd_chunked_noalloc() and the three streams per device
+ *     of kda_fwd_chunked_host().
+ *   - Every compute entry point but kda_fwd_chunked_host is asynchronous on `stream` (NULL =
+ *     legacy default stream).  Host-side argument checks are synchronous and return before
+ *     anything is launched.
  *   - With KDA_NVTX=1 in the environment (read once per process), every compute entry point
  *     wraps its launches in an NVTX range named after the entry point.
  *   - Errors: KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED / KDA_ERR_WORKSPACE from the host
@@ -207,6 +209,51 @@ kda_status kda_fwd_chunked_noalloc(const kda_desc* desc, const void* q, const vo
                                    const void* v, const void* log_alpha, const void* beta,
                                    const float* init_state, const int32_t* cu_seqlens, void* out,
                                    float* final_state, kda_stream_t stream);
+
+/*
+ * kda_fwd_host_workspace_bytes — bytes of device workspace kda_fwd_chunked_host needs for
+ * `desc` cut into `parts` token-range parts.  Host only.  Returns 0 for an invalid desc or
+ * part count.
+ *
+ * kda_fwd_chunked_host — kda_fwd_chunked on HOST buffers: uploads the inputs, runs the prefill
+ * and downloads the results, overlapping the three.
+ *
+ * No counterpart in the paper: a caller whose tensors live in host memory would otherwise copy
+ * everything up, compute, and copy everything down in turn.  The host link is the bound of such
+ * a call, so the tokens are cut into parts and three streams of the library's own (created per
+ * device on first use, kept for the process) overlap the upload of one part, the kernels of the
+ * previous part and the download of the part before that.  Part j covers tokens [b_j, b_{j+1})
+ * of every sequence longer than b_j; the boundaries are multiples of the 64-token chunk chosen
+ * so that the parts hold about equal token counts, and no part spans more than 65,536 tokens
+ * of a sequence (so more parts than asked for can run).  Each part's kernels are one
+ * kda_fwd_chunked call whose initial states are the previous part's final states: a sequence
+ * cut by a boundary is computed as a prefill resumed from its saved fp32 state, which agrees
+ * with one kda_fwd_chunked call within rounding, not bit for bit.  A sequence that lies inside
+ * the first part (for example every sequence, with parts = 1) gets the bits of kda_fwd_chunked.
+ *
+ *   desc          problem description (host), as for kda_fwd_chunked
+ *   q, k, v, log_alpha, beta   HOST inputs, layouts and element type as for kda_fwd_chunked.
+ *                 Page-locked (pinned) memory lets the copies run asynchronously and overlap;
+ *                 pageable memory gives the same results with the copies serialised.
+ *   init_state    HOST fp32 [N, H, 128, 128], or NULL for zeros
+ *   out           HOST [T_tot, H, 128] of desc->in_dtype; must not overlap an input
+ *   final_state   HOST fp32 [N, H, 128, 128], or NULL to skip
+ *   parts         token-range parts, 1..64, or 0 for 8
+ *   workspace     device scratch of at least kda_fwd_host_workspace_bytes(desc, parts) bytes,
+ *                 256-byte aligned: the states in flight, every part's cumulative lengths and
+ *                 three slots of one part's inputs and outputs.  Contents on entry are ignored.
+ *   stream        the call's work starts after the work already queued on this stream.
+ * Unlike the device entry points the call is synchronous: it returns when out and final_state
+ * hold the results (or, after an error, when every copy it issued has finished).  Errors are
+ * those of kda_fwd_chunked, plus KDA_ERR_WORKSPACE for a missing or small workspace and
+ * KDA_ERR_CUDA for a failed copy or stream call.
+ */
+size_t kda_fwd_host_workspace_bytes(const kda_desc* desc, int32_t parts);
+kda_status kda_fwd_chunked_host(const kda_desc* desc, const void* q, const void* k,
+                                const void* v, const void* log_alpha, const void* beta,
+                                const float* init_state, void* out, float* final_state,
+                                int32_t parts, void* workspace, size_t workspace_bytes,
+                                kda_stream_t stream);
 
 /*
  * kda_decode_step — one decode token per (sequence, head), state updated in place.

@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     fwd_chunked,
     fwd_chunked_checkpoints,
     fwd_chunked_host,
+    fwd_host_workspace_bytes,
     fwd_chunked_prologue,
     fwd_plan,
     fwd_workspace_bytes,
@@ -31,7 +32,7 @@ from .binding import (  # noqa: F401
 
 __all__ = [
     "KdaError", "bwd", "decode_step", "decode_step_prologue", "decode_window", "decode_window_prologue", "fwd_checkpoint_count", "fwd_chunked", "fwd_chunked_checkpoints",
-    "fwd_chunked_host", "fwd_chunked_prologue", "fwd_workspace_bytes", "prologue", "prologue_conv",
+    "fwd_chunked_host", "fwd_host_workspace_bytes", "fwd_chunked_prologue", "fwd_workspace_bytes", "prologue", "prologue_conv",
     "launch_count",
     "library_path", "load_library", "read_device_status", "selftest_wait_timeout",
 ]

@@ -64,6 +64,9 @@ SIGNATURES = {
                                        _P, _P, ctypes.c_size_t, _P]),
     "kda_fwd_chunked_noalloc": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P,
                                                _P, _P, _P, _P]),
+    "kda_fwd_host_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(KdaDesc), ctypes.c_int32]),
+    "kda_fwd_chunked_host": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P,
+                                            _P, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "kda_fwd_checkpoint_count": (ctypes.c_int64, [ctypes.POINTER(KdaDesc), ctypes.c_int32]),
     "kda_fwd_chunked_ckpt": (ctypes.c_int, [ctypes.POINTER(KdaDesc), _P, _P, _P, _P, _P, _P, _P,
                                             _P, _P, ctypes.c_int32, _P, _P, ctypes.c_size_t, _P]),
@@ -364,94 +367,57 @@ def fwd_chunked_noalloc(q, k, v, log_alpha, beta, cu_seqlens, seqlens, init_stat
     return out, final_state
 
 
-_host_streams = {}
-
-
-def _split_groups(seqlens, groups: int):
-    """Contiguous sequence ranges with about equal token counts (at most `groups` of them)."""
-    total = sum(int(x) for x in seqlens)
-    bounds, n0, acc = [], 0, 0
-    for n, length in enumerate(seqlens):
-        acc += int(length)
-        if acc * groups >= total * (len(bounds) + 1) or n == len(seqlens) - 1:
-            bounds.append((n0, n + 1))
-            n0 = n + 1
-    return bounds
+def fwd_host_workspace_bytes(seqlens, num_heads: int, dtype: torch.dtype = torch.bfloat16,
+                             parts: int = 0) -> int:
+    lib = load_library()
+    return int(lib.kda_fwd_host_workspace_bytes(ctypes.byref(make_desc(seqlens, num_heads, dtype)),
+                                                int(parts)))
 
 
 def fwd_chunked_host(q, k, v, log_alpha, beta, seqlens, init_state=None, out=None,
-                     final_state=None, groups: int = 4, device=None):
-    """Chunked prefill on HOST tensors (pinned memory): copies in, computes, copies out.
+                     final_state=None, parts: int = 0, workspace=None, device=None):
+    """Chunked prefill on HOST tensors (pinned memory for overlap): ``kda_fwd_chunked_host``.
 
     Same arguments and results as ``fwd_chunked`` except that every tensor lives on the host
-    (cu_seqlens is derived from ``seqlens``).  The call is split by sequence into at most
-    ``groups`` parts, each a ``kda_fwd_chunked`` call of its own, and three streams overlap
-    the host-to-device copy of one part, the kernel of the previous part and the
-    device-to-host copy of the part before it.  A sequence's results do not depend on the
-    other sequences in its call, so they are bit-identical to one ``fwd_chunked`` call.
-    The call returns when ``out`` and ``final_state`` hold the results.
-    """
+    (cu_seqlens is derived from ``seqlens``).  The library cuts the tokens into ``parts``
+    token-range parts (0: its default) and overlaps the upload of one part, the kernels of the
+    previous one and the download of the one before; a sequence cut by a part boundary resumes
+    from its fp32 state, so it agrees with ``fwd_chunked`` within rounding (bit for bit when it
+    lies inside the first part).  ``workspace`` (optional): a uint8 device tensor of at least
+    ``fwd_host_workspace_bytes(seqlens, H, dtype, parts)`` bytes.  The call returns when ``out``
+    and ``final_state`` hold the results."""
+    lib = load_library()
     dev = torch.device(device if device is not None else "cuda")
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     T, H, d = q.shape
     N = len(seqlens)
     dt = q.dtype
-    for name, t in (("q", q), ("k", k), ("v", v), ("log_alpha", log_alpha), ("beta", beta)):
-        if t.device.type != "cpu" or not t.is_contiguous():
-            raise ValueError(f"{name}: expected a contiguous host tensor")
+    cpu = torch.device("cpu")
+    for name, t, shp in (("q", q, (T, H, d)), ("k", k, (T, H, d)), ("v", v, (T, H, d)),
+                         ("log_alpha", log_alpha, (T, H, d)), ("beta", beta, (T, H))):
+        _check_io(name, t, shp, dt, cpu)
+    if init_state is not None:
+        _check_io("init_state", init_state, (N, H, d, d), torch.float32, cpu)
     if out is None:
         out = torch.empty((T, H, d), dtype=dt).pin_memory()
+    _check_io("out", out, (T, H, d), dt, cpu)
     if final_state is None:
         final_state = torch.empty((N, H, d, d), dtype=torch.float32).pin_memory()
-    key = dev.index if dev.index is not None else torch.cuda.current_device()
-    if key not in _host_streams:
-        _host_streams[key] = tuple(torch.cuda.Stream(device=dev) for _ in range(3))
-    s_in, s_run, s_out = _host_streams[key]
-    caller = torch.cuda.current_stream(dev)
-    d_in = {nm: torch.empty(t.shape, dtype=t.dtype, device=dev)
-            for nm, t in (("q", q), ("k", k), ("v", v), ("log_alpha", log_alpha), ("beta", beta))}
-    d_init = None if init_state is None else torch.empty(init_state.shape, dtype=torch.float32,
-                                                         device=dev)
-    d_out = torch.empty((T, H, d), dtype=dt, device=dev)
-    d_fin = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
-    for s in (s_in, s_run, s_out):
-        s.wait_stream(caller)
-    starts = [0]
-    for length in seqlens:
-        starts.append(starts[-1] + int(length))
-    parts = _split_groups(seqlens, max(1, int(groups)))
-    # every part's cumulative lengths (relative to its first token), uploaded once
-    cu_host = torch.tensor([v for n0, n1 in parts
-                            for v in [starts[m] - starts[n0] for m in range(n0, n1 + 1)]],
-                           dtype=torch.int32).pin_memory()
-    with torch.cuda.stream(s_in):
-        cu_dev = cu_host.to(dev, non_blocking=True)
-    cu_off = 0
-    for n0, n1 in parts:
-        t0, t1 = starts[n0], starts[n1]
-        lens = [int(x) for x in seqlens[n0:n1]]
-        d_cu = cu_dev[cu_off:cu_off + (n1 - n0) + 1]
-        cu_off += (n1 - n0) + 1
-        with torch.cuda.stream(s_in):
-            for nm, t in (("q", q), ("k", k), ("v", v), ("log_alpha", log_alpha), ("beta", beta)):
-                d_in[nm][t0:t1].copy_(t[t0:t1], non_blocking=True)
-            if d_init is not None:
-                d_init[n0:n1].copy_(init_state[n0:n1], non_blocking=True)
-            ready = torch.cuda.Event()
-            ready.record(s_in)
-        s_run.wait_event(ready)
-        with torch.cuda.stream(s_run):
-            fwd_chunked(d_in["q"][t0:t1], d_in["k"][t0:t1], d_in["v"][t0:t1],
-                        d_in["log_alpha"][t0:t1], d_in["beta"][t0:t1], d_cu, lens,
-                        init_state=None if d_init is None else d_init[n0:n1],
-                        out=d_out[t0:t1], final_state=d_fin[n0:n1], stream=s_run)
-            computed = torch.cuda.Event()
-            computed.record(s_run)
-        s_out.wait_event(computed)
-        with torch.cuda.stream(s_out):
-            out[t0:t1].copy_(d_out[t0:t1], non_blocking=True)
-            final_state[n0:n1].copy_(d_fin[n0:n1], non_blocking=True)
-    caller.wait_stream(s_out)
-    s_out.synchronize()  # also keeps cu_host alive until its copy has run
+    _check_io("final_state", final_state, (N, H, d, d), torch.float32, cpu)
+    desc = make_desc(seqlens, H, dt)
+    need = int(lib.kda_fwd_host_workspace_bytes(ctypes.byref(desc), int(parts)))
+    if need == 0:
+        raise KdaError(-1, "kda_fwd_host_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    st = lib.kda_fwd_chunked_host(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                  _ptr(beta), _ptr(init_state), _ptr(out), _ptr(final_state),
+                                  int(parts), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(),
+                                  _stream_handle(None, dev))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_fwd_chunked_host")
     return out, final_state
 
 

@@ -113,6 +113,40 @@ def test_host_argument_checks(lib):
                                P(0x2000), None) == -1
 
 
+def test_host_call_workspace_and_checks(lib):
+    """kda_fwd_host_workspace_bytes: states, every part's cumulative lengths and three slots of
+    the largest part; kda_fwd_chunked_host's host-side rejections (no CUDA call is reached)."""
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    size = lambda d, parts: lib.kda_fwd_host_workspace_bytes(ctypes.byref(d), parts)
+    # 4 x 8192 tokens, 32 heads, 8 parts: the last part holds 1/32 of the tokens (256 per
+    # sequence) and the first seven share the rest, rounded up to chunks: boundaries 1152, 2304,
+    # 3456, 4544, 5696, 6848, 7936, so the largest part has 4 x 1,152 rows
+    d = _desc([8192] * 4, H=32)
+    row = 32 * 128 * 2
+    slot = 5 * 4608 * row + 4608 * 32 * 2
+    assert size(d, 8) == 4 * 32 * 65536 + 256 + 3 * slot
+    assert size(d, 0) == size(d, 8)
+    assert size(d, 1) == 4 * 32 * 65536 + 256 + 3 * (5 * 32768 * row + 32768 * 32 * 2)
+    # one part asked for, but no part spans more than 65,536 tokens of a sequence:
+    # parts [0, 65536) and [65536, 70000), the first with 65,636 rows
+    d2 = _desc([70000, 100], H=1)
+    assert size(d2, 1) == 2 * 65536 + 256 + 3 * (5 * 65636 * 256 + 131328)
+    assert size(_desc([4, 5]), -1) == 0 and size(_desc([4, 5]), 65) == 0
+    assert lib.kda_fwd_host_workspace_bytes(None, 0) == 0
+
+    def call(d, ws, nbytes, parts=0, out=P(0x2000)):
+        return lib.kda_fwd_chunked_host(ctypes.byref(d), fake, fake, fake, fake, fake, None, out,
+                                        None, parts, ws, nbytes, None)
+    big = 1 << 30
+    assert call(_desc([4, 5]), None, 0) == -3                    # no workspace
+    assert call(_desc([4, 5]), P(0x100100), 16) == -3            # workspace too small
+    assert call(_desc([4, 5]), P(0x100101), big) == -3           # workspace misaligned
+    assert call(_desc([4, 5]), P(0x100100), big, parts=65) == -1  # too many parts
+    assert call(_desc([4, 5]), P(0x100100), big, out=fake) == -1  # out aliases an input
+    assert call(_desc([4, 5], d=64), P(0x100100), big) == -1     # unsupported head dim
+
+
 def test_checkpoint_and_window_argument_checks(lib):
     # refused on the host before any device pointer is touched
     P = ctypes.c_void_p

@@ -226,27 +226,97 @@ def test_resume_from_saved_state_and_decode_continuation():
     assert_close("prefill(T+1) last", full_out[T:].cpu(), o_ref1)
 
 
-@pytest.mark.parametrize("groups", [1, 2, 3, 8])
+def _host_copies(x, init):
+    host = {nm: x[nm].cpu().pin_memory() for nm in ("q", "k", "v", "log_alpha", "beta")}
+    s0 = x["init_state"].cpu().pin_memory() if init else None
+    return host, s0
+
+
+@pytest.mark.parametrize("parts", [1, 2, 3, 8])
 @pytest.mark.parametrize("init", [True, False])
-def test_host_buffer_call_matches_device_call(groups, init):
-    """fwd_chunked_host (pinned host buffers, copies and kernels overlapped by part) gives the
-    bits of one device call, and matches the oracle."""
+def test_host_buffer_call_matches_oracle(parts, init):
+    """kda_fwd_chunked_host (pinned host buffers; uploads, kernels and downloads overlapped by
+    token-range part) against the oracle.  With one part it is one kernel call over every
+    sequence and gives the bits of the device call; with more, a sequence cut by a part boundary
+    resumes from its fp32 state, and a sequence of at most one chunk (always inside the first
+    part) still gets the device call's bits."""
     lens = [1000, 64, 3, 2048, 0, 517, 130]
     x = synth.make_inputs(lens, 4, torch.bfloat16, seed=21, device=DEV)
     out_d, fin_d = run_gpu(x, init=init)
-    host = {nm: x[nm].cpu().pin_memory() for nm in ("q", "k", "v", "log_alpha", "beta")}
-    s0 = x["init_state"].cpu().pin_memory() if init else None
+    host, s0 = _host_copies(x, init)
     out_h, fin_h = kda().fwd_chunked_host(host["q"], host["k"], host["v"], host["log_alpha"],
-                                          host["beta"], x["seqlens"], init_state=s0,
-                                          groups=groups)
+                                          host["beta"], x["seqlens"], init_state=s0, parts=parts)
     assert out_h.device.type == "cpu" and fin_h.device.type == "cpu"
-    assert torch.equal(out_h, out_d.cpu())
-    assert torch.equal(fin_h, fin_d.cpu())
     check_status()
-    if groups == 3 and init:
-        o_ref, s_ref = run_oracle(x)
-        assert_close("out", out_h, o_ref)
-        assert_close("final_state", fin_h.numpy(), s_ref)
+    o_ref, s_ref = run_oracle(x, init=init)
+    assert_close("out", out_h, o_ref)
+    assert_close("final_state", fin_h.numpy(), s_ref)
+    if parts == 1:
+        assert torch.equal(out_h, out_d.cpu()) and torch.equal(fin_h, fin_d.cpu())
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    for n, length in enumerate(lens):
+        if length <= 64:
+            rows = slice(int(starts[n]), int(starts[n + 1]))
+            assert torch.equal(out_h[rows], out_d.cpu()[rows])
+            assert torch.equal(fin_h[n], fin_d.cpu()[n])
+
+
+def test_host_buffer_call_long_sequence_and_fp32():
+    """A sequence longer than 65,536 tokens is cut into parts of at most that span even with
+    parts = 1 (so no part needs the segment workspace); fp32 inputs take the same pipeline."""
+    x = synth.make_inputs([70000, 100, 0], 1, torch.bfloat16, seed=22, device=DEV)
+    host, s0 = _host_copies(x, True)
+    out_h, fin_h = kda().fwd_chunked_host(host["q"], host["k"], host["v"], host["log_alpha"],
+                                          host["beta"], x["seqlens"], init_state=s0, parts=1)
+    check_status()
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", out_h, o_ref)
+    assert_close("final_state", fin_h.numpy(), s_ref)
+    assert torch.equal(fin_h[2], x["init_state"][2].cpu())  # empty: the initial state
+    x32 = synth.make_inputs([300, 0, 129], 2, torch.float32, seed=23, device=DEV)
+    host, s0 = _host_copies(x32, True)
+    out_h, fin_h = kda().fwd_chunked_host(host["q"], host["k"], host["v"], host["log_alpha"],
+                                          host["beta"], x32["seqlens"], init_state=s0, parts=3)
+    check_status()
+    o_ref, s_ref = run_oracle(x32)
+    assert_close("out fp32", out_h.numpy(), o_ref)
+    assert_close("final_state fp32", fin_h.numpy(), s_ref)
+
+
+def test_host_buffer_call_equal_lengths():
+    """Equal lengths: each part's rows of all sequences move in one strided copy per tensor."""
+    x = synth.make_inputs([300] * 5, 2, torch.bfloat16, seed=24, device=DEV)
+    host, s0 = _host_copies(x, True)
+    out_h, fin_h = kda().fwd_chunked_host(host["q"], host["k"], host["v"], host["log_alpha"],
+                                          host["beta"], x["seqlens"], init_state=s0, parts=4)
+    check_status()
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", out_h, o_ref)
+    assert_close("final_state", fin_h.numpy(), s_ref)
+
+
+def test_host_buffer_call_full_size():
+    """The benchmark's end-to-end call: 4 x 8192 tokens, 32 heads, 8 parts (each copy one
+    strided run over the four sequences).  Every output and state against the device call through the parity gate, and
+    the first and last (sequence, head) units against the oracle run on those units alone."""
+    w = synth.workloads()["prefill_4x8k"]
+    x = synth.make_workload(w, device=DEV)
+    out_d, fin_d = run_gpu(x)
+    host, s0 = _host_copies(x, True)
+    out_h, fin_h = kda().fwd_chunked_host(host["q"], host["k"], host["v"], host["log_alpha"],
+                                          host["beta"], x["seqlens"], init_state=s0, parts=8)
+    check_status()
+    assert_close("out vs device call", out_h, out_d.cpu().float().numpy())
+    assert_close("final_state vs device call", fin_h.numpy(), fin_d.cpu().numpy())
+    L, N, H = w.lengths[0], len(w.lengths), w.heads
+    for n, h in ((0, 0), (N - 1, H - 1)):
+        rows = slice(n * L, (n + 1) * L)
+        o_ref, s_ref = oracle.recurrence(
+            *(x[key][rows, h:h + 1].cpu() for key in ("q", "k", "v", "log_alpha", "beta")),
+            torch.tensor([0, L], dtype=torch.int32),
+            state_in=x["init_state"][n:n + 1, h:h + 1].cpu(), threads=oracle_threads())
+        assert_close(f"out[{n},{h}]", out_h[rows, h:h + 1], o_ref)
+        assert_close(f"final_state[{n},{h}]", fin_h[n:n + 1, h:h + 1].numpy(), s_ref)
 
 
 def test_deterministic():
