@@ -23,6 +23,10 @@
  *     log_alpha is the natural-log gate (alpha = exp(log_alpha), expected <= 0); beta is the
  *     write strength itself (already passed through a sigmoid).  No scale is applied to q.
  *   - Only d_k = d_v = 128 is supported.
+ *   - Device tensors that a kernel reads or writes as 16-byte vectors must be 16-byte aligned
+ *     (every torch allocation is); each entry point states which, and a misaligned one returns
+ *     KDA_ERR_INVALID_ARG.  The prefill entry points need it for q, k, v, log_alpha, out and
+ *     the states.
  *   - Ownership: the caller owns and allocates every buffer (device memory unless marked
  *     host).  The library never allocates or frees memory and keeps no per-call state; its
  *     only globals are the sticky device status word read by kda_read_device_status(), the
@@ -404,8 +408,9 @@ kda_status kda_fwd_chunked_prologue(const kda_desc* desc, const kda_prologue_par
  * kernel as the recurrence ("k3_training_and_infra_notes", section 4.5, KDA decoding).
  *
  * Arguments as kda_decode_step / kda_decode_window, with q_raw, k_raw, v_raw, g_raw and
- * beta_logit in place of q, k, v, log_alpha and beta, and `prm` as for kda_prologue.  Outputs
- * and states are bit-identical to kda_prologue followed by the plain call.  bf16 inputs only
+ * beta_logit in place of q, k, v, log_alpha and beta, and `prm` as for kda_prologue; q_raw and
+ * k_raw must be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).  Outputs and states are
+ * bit-identical to kda_prologue followed by the plain call.  bf16 inputs only
  * (KDA_ERR_UNSUPPORTED for fp32 inputs).
  */
 kda_status kda_decode_step_prologue(const kda_desc* desc, const kda_prologue_params* prm,

@@ -98,6 +98,8 @@ kda_status decode_step_impl(const kda_desc* desc, const void* q, const void* k,
         if (!check_prologue(pro)) return KDA_ERR_INVALID_ARG;
         pp = {pro->A_log, pro->dt_bias, pro->lower_bound, pro->q_scale};
     }
+    // the fused prologue reads q and k rows as 16-byte vectors
+    if (pro && (!aligned16(q) || !aligned16(k))) return KDA_ERR_INVALID_ARG;
     if (desc->total_tokens != desc->num_seqs) return KDA_ERR_INVALID_ARG;
     if (desc->host_seqlens) {
         for (int32_t n = 0; n < desc->num_seqs; ++n)
@@ -133,6 +135,8 @@ kda_status decode_window_impl(const kda_desc* desc, const void* q, const void* k
     }
     for (int32_t n = 0; n < desc->num_seqs; ++n)
         if (desc->host_seqlens[n] > 64) return KDA_ERR_INVALID_ARG;
+    // the fused prologue reads q and k rows as 16-byte vectors
+    if (pro && (!aligned16(q) || !aligned16(k))) return KDA_ERR_INVALID_ARG;
     if (!cu_seqlens || !state) return KDA_ERR_INVALID_ARG;
     if (desc->total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta)) return KDA_ERR_INVALID_ARG;
     if (out && (out == q || out == k || out == v || out == log_alpha || out == beta ||

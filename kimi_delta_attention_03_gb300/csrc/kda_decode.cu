@@ -34,27 +34,48 @@ struct DecPro {
     int H;
 };
 
-// The row norms of one token.  On entry thread tid < 128 has written Swish(k_raw), Swish(q_raw)
-// of channel tid into sw_k, sw_q (fp32) and a barrier has passed.  Each of warps 0-3 forms both
-// norms itself, in the order of the standalone prologue (eight in-order FMAs per lane of a 16-lane
-// group, then the 1-2-4-8 butterfly), and writes its own 32 channels, scaled and rounded to bf16,
-// into s_k, s_q.  The caller's next barrier publishes them.
-__device__ __forceinline__ void decode_norms(const float* sw_k, const float* sw_q, float* s_k,
-                                             float* s_q, float q_scale, int tid) {
-    if (tid < kDim) {
-        const int lane = tid & 31;
-        const int cg = lane & 15;
-        const float* row = lane < 16 ? sw_k : sw_q;
-        float x[8];
+// Raw projections of one token for warp_prologue.  Lane l of the warp that produces channels
+// [32 cw, 32 cw + 32) holds the eight channels 8 (l & 15) .. 8 (l & 15) + 7 of k (l < 16) or q
+// (l >= 16), as one 16-byte vector, and its own channel 32 cw + l of k, q, g and v.
+struct RawTok {
+    uint4 grp;
+    __nv_bfloat16 kc, qc, gc, vc;
+};
+
+__device__ __forceinline__ void load_raw(RawTok& r, const __nv_bfloat16* k,
+                                         const __nv_bfloat16* q, const __nv_bfloat16* g,
+                                         const __nv_bfloat16* v, int64_t row, int cw, int lane) {
+    r.grp = *reinterpret_cast<const uint4*>((lane < 16 ? k : q) + row * kDim + 8 * (lane & 15));
+    const int64_t e = row * kDim + 32 * cw + lane;
+    r.kc = k[e];
+    r.qc = q[e];
+    r.gc = g[e];
+    r.vc = v[e];
+}
+
+// The prologue of one token's channels [32 cw, 32 cw + 32) by one warp, with no barrier: the
+// warp forms both row norms itself, in the order of the standalone prologue (eight in-order FMAs
+// per lane of a 16-lane group, then the 1-2-4-8 butterfly), then writes its channels of k and q
+// (Swish, scaled, rounded to bf16), alpha = exp(gate) and v = Swish(v) (rounded to bf16).
+__device__ __forceinline__ void warp_prologue(const RawTok& r, float dt, float na, float lb,
+                                              float q_scale, int c, int lane, float* s_k,
+                                              float* s_q, float* s_a, float* s_v) {
+    float x[8];
+    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&r.grp);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) x[j] = row[8 * cg + j];
-        const float ss = row_sum_squares16(x);
-        const float inv = __fmul_rn(rsqrtf(__fadd_rn(ss, kProNormEps)), lane < 16 ? 1.f : q_scale);
-        const float ik = __shfl_sync(0xffffffffu, inv, 0);
-        const float iq = __shfl_sync(0xffffffffu, inv, 16);
-        s_k[tid] = round_bf16(__fmul_rn(sw_k[tid], ik));
-        s_q[tid] = round_bf16(__fmul_rn(sw_q[tid], iq));
+    for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(p2[j]);
+        x[2 * j] = pro_swish(f.x);
+        x[2 * j + 1] = pro_swish(f.y);
     }
+    const float ss = row_sum_squares16(x);
+    const float inv = __fmul_rn(rsqrtf(__fadd_rn(ss, kProNormEps)), lane < 16 ? 1.f : q_scale);
+    const float ik = __shfl_sync(0xffffffffu, inv, 0);
+    const float iq = __shfl_sync(0xffffffffu, inv, 16);
+    s_k[c] = round_bf16(__fmul_rn(pro_swish(__bfloat162float(r.kc)), ik));
+    s_q[c] = round_bf16(__fmul_rn(pro_swish(__bfloat162float(r.qc)), iq));
+    s_a[c] = expf(pro_gate(__bfloat162float(r.gc), dt, na, lb));
+    s_v[c] = round_bf16(pro_swish(__bfloat162float(r.vc)));
 }
 
 template <typename TIn, bool kPro>
@@ -64,7 +85,6 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                   const TIn* __restrict__ beta, float* __restrict__ state,
                   TIn* __restrict__ out, int64_t units, const DecPro pro) {
     __shared__ float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_u[kDim];
-    __shared__ float sw_k[kPro ? kDim : 1], sw_q[kPro ? kDim : 1];  // Swish of raw k, q
     __shared__ __align__(16) float s_rx[8][kDim];
     __shared__ __align__(16) float s_ry[8][kDim];
     __shared__ float s_kq;
@@ -76,26 +96,31 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
         float* S = state + unit * (int64_t)(kDim * kDim);
         float4 s[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-            s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
-
         float b;
         if constexpr (kPro) {  // raw projections: the prologue first
+            // The token's raw inputs are requested before the state, so that they arrive first
+            // and the prologue's arithmetic (warps 0-3, 32 channels each) overlaps the state
+            // stream.
             const int h = (int)(unit % pro.H);
-            if (tid < kDim) {
-                const int64_t e = unit * kDim + tid;
-                sw_k[tid] = pro_swish(io<TIn>::to_f(k[e]));
-                sw_q[tid] = pro_swish(io<TIn>::to_f(q[e]));
-                const float dt = pro.dt_bias ? pro.dt_bias[h * kDim + tid] : 0.f;
-                s_a[tid] = expf(pro_gate(io<TIn>::to_f(g[e]), dt, pro_gate_rate(pro.A_log, h), pro.lb));
-                s_v[tid] = round_bf16(pro_swish(io<TIn>::to_f(v[e])));
+            RawTok raw{};
+            float dt = 0.f;
+            if (warp < 4) {
+                load_raw(raw, k, q, g, v, unit, warp, lane);
+                dt = pro.dt_bias ? pro.dt_bias[h * kDim + tid] : 0.f;
             }
-            b = round_bf16(pro_sigmoid(io<TIn>::to_f(beta[unit])));
-            __syncthreads();
-            decode_norms(sw_k, sw_q, s_k, s_q, pro.q_scale, tid);
+            const TIn rb = beta[unit];
+            const float na = pro_gate_rate(pro.A_log, h);
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
+            if (warp < 4)
+                warp_prologue(raw, dt, na, pro.lb, pro.q_scale, tid, lane, s_k, s_q, s_a, s_v);
+            b = round_bf16(pro_sigmoid(io<TIn>::to_f(rb)));
             __syncthreads();
         } else {
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
             if (tid < kDim) {
                 const int64_t e = unit * kDim + tid;
                 s_k[tid] = io<TIn>::to_f(k[e]);
@@ -175,8 +200,12 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                          const float* state_in, float* state_out, TIn* __restrict__ out,
                          const int32_t* __restrict__ commit, int64_t units, int H,
                          int64_t total_tokens, int max_len, int* status, const DecPro pro) {
-    __shared__ float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_u[kDim];
-    __shared__ float sw_k[kPro ? kDim : 1], sw_q[kPro ? kDim : 1];  // Swish of raw k, q
+    // With raw projections the prologue runs one token ahead of the recurrence, on warps 4-7
+    // while warps 0-3 form the token's u, so the token vectors are double-buffered (token t in
+    // buffer t & 1).
+    constexpr int NB = kPro ? 2 : 1;
+    __shared__ float s_k[NB][kDim], s_q[NB][kDim], s_a[NB][kDim], s_v[NB][kDim], s_u[kDim];
+    __shared__ float s_b[NB];
     __shared__ __align__(16) float s_rx[8][kDim];
     __shared__ __align__(16) float s_ry[8][kDim];
     __shared__ float s_kq;
@@ -212,8 +241,8 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
             s[r] = Sin ? __ldcs(reinterpret_cast<const float4*>(Sin + (warp + 8 * r) * kDim) + lane)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
         float pro_dt = 0.f, pro_na = 0.f;
-        if constexpr (kPro) {
-            pro_dt = pro.dt_bias && tid < kDim ? pro.dt_bias[h * kDim + tid] : 0.f;
+        if constexpr (kPro) {  // warps 4-7 run the prologue, channel tid - 128 each
+            pro_dt = pro.dt_bias && tid >= kDim ? pro.dt_bias[h * kDim + tid - kDim] : 0.f;
             pro_na = pro_gate_rate(pro.A_log, h);
         }
 
@@ -241,39 +270,52 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
             if (tid < nlen) asm volatile("prefetch.global.L2 [%0];" ::"l"(beta + (nt0 + tid) * H + nh));
         }
 
-        // the next token's inputs are fetched into registers while this token is computed
+        // the next token's inputs are fetched into registers while this token is computed (with
+        // raw projections, by warps 4-7, two tokens ahead of the recurrence)
         TIn nk{}, nq{}, ng{}, nv{}, nb{};
+        [[maybe_unused]] RawTok raw{};
         auto fetch = [&](int t) {
             const int64_t row = (t0 + t) * H + h;
-            if (tid < kDim) {
-                const int64_t e = row * kDim + tid;
-                nk = k[e]; nq = q[e]; ng = g[e]; nv = v[e];
+            if constexpr (kPro) {
+                if (tid >= kDim) {
+                    load_raw(raw, k, q, g, v, row, warp - 4, lane);
+                    nb = beta[row];
+                }
+            } else {
+                if (tid < kDim) {
+                    const int64_t e = row * kDim + tid;
+                    nk = k[e]; nq = q[e]; ng = g[e]; nv = v[e];
+                }
+                nb = beta[row];
             }
-            nb = beta[row];
+        };
+        // Raw projections: the fetched token's prologue into buffer `buf`, on warps 4-7.
+        [[maybe_unused]] auto pro_token = [&](int buf) {
+            if (tid >= kDim) {
+                warp_prologue(raw, pro_dt, pro_na, pro.lb, pro.q_scale, tid - kDim, lane,
+                              s_k[buf], s_q[buf], s_a[buf], s_v[buf]);
+                if (tid == kDim) s_b[buf] = round_bf16(pro_sigmoid(io<TIn>::to_f(nb)));
+            }
         };
         fetch(0);
+        if constexpr (kPro) {  // token 0's prologue; later tokens' run one token ahead
+            pro_token(0);
+            if (1 < len) fetch(1);
+            __syncthreads();
+        }
 #pragma unroll 1
         for (int t = 0; t < len; ++t) {
             const int64_t row = (t0 + t) * H + h;
+            const int cur = kPro ? (t & 1) : 0;
             float b;
-            if constexpr (kPro) {  // raw projections: the prologue first
-                if (tid < kDim) {
-                    sw_k[tid] = pro_swish(io<TIn>::to_f(nk));
-                    sw_q[tid] = pro_swish(io<TIn>::to_f(nq));
-                    s_a[tid] = expf(pro_gate(io<TIn>::to_f(ng), pro_dt, pro_na, pro.lb));
-                    s_v[tid] = round_bf16(pro_swish(io<TIn>::to_f(nv)));
-                }
-                b = round_bf16(pro_sigmoid(io<TIn>::to_f(nb)));
-                if (t + 1 < len) fetch(t + 1);
-                __syncthreads();
-                decode_norms(sw_k, sw_q, s_k, s_q, pro.q_scale, tid);
-                __syncthreads();
+            if constexpr (kPro) {
+                b = s_b[cur];
             } else {
                 if (tid < kDim) {
-                    s_k[tid] = io<TIn>::to_f(nk);
-                    s_q[tid] = io<TIn>::to_f(nq);
-                    s_a[tid] = expf(io<TIn>::to_f(ng));
-                    s_v[tid] = io<TIn>::to_f(nv);
+                    s_k[0][tid] = io<TIn>::to_f(nk);
+                    s_q[0][tid] = io<TIn>::to_f(nq);
+                    s_a[0][tid] = expf(io<TIn>::to_f(ng));
+                    s_v[0][tid] = io<TIn>::to_f(nv);
                 }
                 b = io<TIn>::to_f(nb);
                 if (t + 1 < len) fetch(t + 1);
@@ -285,7 +327,7 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 const int i = warp + 8 * r;
-                const float a = s_a[i], kk = s_k[i], qq = s_q[i];
+                const float a = s_a[cur][i], kk = s_k[cur][i], qq = s_q[cur][i];
                 s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
                 x0 = fmaf(kk, s[r].x, x0); x1 = fmaf(kk, s[r].y, x1);
                 x2 = fmaf(kk, s[r].z, x2); x3 = fmaf(kk, s[r].w, x3);
@@ -298,7 +340,7 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                 float p = 0.f;
 #pragma unroll
                 for (int m = 0; m < kDim / 32; ++m)
-                    p = fmaf(s_k[lane + 32 * m], s_q[lane + 32 * m], p);
+                    p = fmaf(s_k[cur][lane + 32 * m], s_q[cur][lane + 32 * m], p);
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
                 if (lane == 0) s_kq = p;
@@ -309,16 +351,22 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                 float x = 0.f, y = 0.f;
 #pragma unroll
                 for (int w8 = 0; w8 < 8; ++w8) { x += s_rx[w8][tid]; y += s_ry[w8][tid]; }
-                const float u = b * (s_v[tid] - x);
+                const float u = b * (s_v[cur][tid] - x);
                 s_u[tid] = u;
                 if (out) out[row * kDim + tid] = io<TIn>::from_f(fmaf(s_kq, u, y));
+            }
+            if constexpr (kPro) {  // meanwhile the next token's prologue, into the other buffer
+                if (t + 1 < len) {
+                    pro_token(cur ^ 1);
+                    if (t + 2 < len) fetch(t + 2);
+                }
             }
             __syncthreads();
 
             const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
-                const float kk = s_k[warp + 8 * r];
+                const float kk = s_k[cur][warp + 8 * r];
                 s[r].x = fmaf(kk, u4.x, s[r].x); s[r].y = fmaf(kk, u4.y, s[r].y);
                 s[r].z = fmaf(kk, u4.z, s[r].z); s[r].w = fmaf(kk, u4.w, s[r].w);
             }

@@ -210,6 +210,9 @@ def test_prologue_argument_checks(lib):
     assert step(_desc([1, 1]), None) == -1
     assert step(_desc([1, 1]), ctypes.byref(prm(q_scale=-1.0))) == -1
     assert step(_desc([1, 1], dtype=torch.float32), ctypes.byref(prm())) == -2
+    assert lib.kda_decode_step_prologue(ctypes.byref(_desc([1, 1])), ctypes.byref(prm()),
+                                        P(0x1008), fake, fake, fake, fake, P(0x3000), P(0x2000),
+                                        None) == -1       # q_raw not 16-byte aligned
     win = lambda d, pp: lib.kda_decode_window_prologue(ctypes.byref(d), pp, fake, fake, fake, fake,
                                                         fake, fake, P(0x3000), P(0x2000), None,
                                                         None)
@@ -217,6 +220,9 @@ def test_prologue_argument_checks(lib):
     assert win(_desc([4, 5]), ctypes.byref(prm(lower_bound=1.0))) == -1
     assert win(_desc([4, 5], dtype=torch.float32), ctypes.byref(prm())) == -2
     assert win(_desc([4, 65]), ctypes.byref(prm())) == -1   # runs of at most 64 tokens
+    assert lib.kda_decode_window_prologue(ctypes.byref(_desc([4, 5])), ctypes.byref(prm()), fake,
+                                          P(0x1004), fake, fake, fake, fake, P(0x3000),
+                                          P(0x2000), None, None) == -1  # k_raw not aligned
     # the short convolution in front of the prologue
     from kimi_delta_attention_03_gb300.binding import KdaConvParams
     cv = lambda **kw: KdaConvParams(kw.get("w_q", 0x8000), 0x8400, 0x8800, kw.get("cin", None),
