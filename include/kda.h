@@ -443,7 +443,11 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
  *   workspace     device, at least kda_bwd_workspace_bytes(desc) bytes, 16-byte aligned:
  *                 per (sequence, head), fp32, one state per 16 tokens of the longest sequence,
  *                 16 states of the block being reversed and 16 pairs of 128-vectors (u, r);
- *                 contents on return are unspecified
+ *                 then four partial sums (one per block of 32 value channels) of dq, dk,
+ *                 dlog_alpha and dbeta per token and head; contents on return are unspecified
+ * The gradients are deterministic: the partial sums are added in a fixed order.  A unit whose
+ * device cu_seqlens disagree with the host lengths (KDA_ERR_INVALID_ARG in the device status
+ * word) computes nothing, and its rows of dq, dk, dlog_alpha and dbeta are then unspecified.
  * Outputs must not alias inputs or each other.  Argument, alignment and workspace errors return
  * KDA_ERR_INVALID_ARG / KDA_ERR_WORKSPACE before anything is launched.
  */
