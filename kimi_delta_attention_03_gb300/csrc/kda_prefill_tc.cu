@@ -185,6 +185,23 @@ __device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
         f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
 }
+// Two fp32 products (or fused multiply-adds) in one packed instruction, each rounded as its
+// scalar form is: the same bits, half the issue slots.
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return make_uint4(pack_bf16(f[0], f[1]), pack_bf16(f[2], f[3]), pack_bf16(f[4], f[5]),
                       pack_bf16(f[6], f[7]));
@@ -1030,13 +1047,21 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     unpack8(qr4, qv);
                     float kp[8], qr[8], km[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        G[j] = fmaf(gv[j], kLog2eTC, G[j]);  // G - r, log2 units
-                        const float e = ex2_approx(G[j]);
-                        const float ei = ex2_approx(-G[j]);
-                        kp[j] = kv[j] * e;
-                        qr[j] = qv[j] * e;
-                        km[j] = kv[j] * ei;
+                    for (int j = 0; j < 8; j += 2) {
+                        const float2 g2 = fma_f32x2(make_float2(gv[j], gv[j + 1]),
+                                                    make_float2(kLog2eTC, kLog2eTC),
+                                                    make_float2(G[j], G[j + 1]));
+                        G[j] = g2.x;  // G - r, log2 units
+                        G[j + 1] = g2.y;
+                        const float2 e = make_float2(ex2_approx(G[j]), ex2_approx(G[j + 1]));
+                        const float2 ei = make_float2(ex2_approx(-G[j]), ex2_approx(-G[j + 1]));
+                        const float2 k2 = make_float2(kv[j], kv[j + 1]);
+                        const float2 a = mul_f32x2(k2, e);
+                        const float2 b = mul_f32x2(make_float2(qv[j], qv[j + 1]), e);
+                        const float2 m = mul_f32x2(k2, ei);
+                        kp[j] = a.x; kp[j + 1] = a.y;
+                        qr[j] = b.x; qr[j + 1] = b.y;
+                        km[j] = m.x; km[j + 1] = m.y;
                     }
                     *reinterpret_cast<uint4*>(kq + o) = pack8(kp);
                     *reinterpret_cast<uint4*>(kq + o + 64 * 128) = pack8(qr);
