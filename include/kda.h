@@ -93,7 +93,7 @@ typedef struct kda_plan_info {
     int64_t work_items;       /* (sequence, segment) items per head                        */
     int32_t split_sequences;  /* sequences processed as more than one segment              */
     int32_t chunk_size;       /* tokens per chunk (64)                                     */
-    int32_t segment_chunks;   /* chunks per segment of a split sequence                    */
+    int32_t segment_chunks;   /* longest segment of a split sequence, in chunks (0: none)  */
     int32_t reserved;
     size_t workspace_bytes;   /* what kda_fwd_chunked needs for this description           */
 } kda_plan_info;
@@ -117,9 +117,11 @@ size_t kda_fwd_workspace_bytes(const kda_desc* desc);
  * as the token loop would, by the chunkwise form (64-token chunks aligned to each sequence's
  * own start; intra-chunk work as dense tensor-core tiles; one serial state step per chunk)
  * described in "How Kimi K3 Engineered Its Way to the Frontier", section "FlashKDA steps the
- * state once per 16 tokens".  Long sequences are split into segments whose transitions are
- * evaluated independently of their incoming state and composed exactly afterwards
- * ("k3_training_and_infra_notes", section 4.1, intra-device context parallelism).
+ * state once per 16 tokens".  Long sequences (above 65,536 tokens) are split into segments
+ * whose transitions are evaluated independently of their incoming state and composed exactly
+ * afterwards ("k3_training_and_infra_notes", section 4.1, intra-device context parallelism);
+ * the segment count is a function of the sequence's length and the head count only (see
+ * kda_fwd_plan), picked for the waves of GB300's 152 SMs.
  *
  *   desc          problem description (host)
  *   q, k, v, log_alpha, beta   device inputs, layouts above, element type desc->in_dtype
@@ -199,8 +201,9 @@ kda_status kda_fwd_chunked_ckpt(const kda_desc* desc, const void* q, const void*
  *   - The scratch array is KDA_NOALLOC_SCRATCH_BYTES (48 MiB) of device memory that every GPU
  *     which loads this library holds until the process exits.
  *   - A call whose kda_fwd_workspace_bytes(desc) exceeds KDA_NOALLOC_SCRATCH_BYTES returns
- *     KDA_ERR_WORKSPACE before launching anything (for example H = 16 heads fit up to 16
- *     segments of 8192 tokens in total).  Calls that need no workspace always run.
+ *     KDA_ERR_WORKSPACE before launching anything (the workspace holds 3 x 64 KiB per head
+ *     and segment, so with H = 16 heads 16 segments fit in total).  Calls that need no
+ *     workspace always run.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
  *     with that device current); make that first call before any stream capture.
  *   - Every call shares the one array and leaves its contents behind; nothing in it has to

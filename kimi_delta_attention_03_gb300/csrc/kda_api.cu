@@ -163,16 +163,17 @@ kda_status kda_fwd_plan(const kda_desc* desc, kda_plan_info* info) {
     if (st != KDA_OK) return st;
     kda_plan_info p = {};
     p.chunk_size = kda::kChunk;
-    p.segment_chunks = kda::kSegChunks;
+    p.segment_chunks = 0;
     int64_t slots = 0;
     for (int32_t n = 0; n < desc->num_seqs; ++n) {
         const int64_t L = desc->host_seqlens[n];
-        const int ns = kda::num_segments(L);
+        const kda::SegPlan sp = kda::segment_plan(L, desc->num_heads);
         p.chunks += (L + kda::kChunk - 1) / kda::kChunk;
-        p.work_items += ns;
-        if (ns > 1) {
+        p.work_items += sp.nseg;
+        if (sp.nseg > 1) {
             p.split_sequences += 1;
-            slots += ns;
+            slots += sp.nseg;
+            p.segment_chunks = std::max(p.segment_chunks, sp.seg_chunks);
         }
     }
     // three fp32 arrays [slots][H][128][128], each 256-byte aligned
@@ -241,7 +242,8 @@ kda_status fwd_chunked_impl(const kda_desc* desc, const void* q, const void* k, 
         ws.trans = reinterpret_cast<float*>(static_cast<char*>(workspace) + per);
         ws.in = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * per);
         for (int32_t n = 0; n < desc->num_seqs; ++n)
-            ws.max_segments = std::max(ws.max_segments, kda::num_segments(desc->host_seqlens[n]));
+            ws.max_segments = std::max(ws.max_segments,
+                                       kda::segment_plan(desc->host_seqlens[n], desc->num_heads).nseg);
     }
     if (desc->in_dtype == KDA_BF16)
         e = kda::launch_prefill_tc(desc->num_seqs, desc->num_heads, desc->total_tokens, q, k, v,

@@ -13,16 +13,48 @@ constexpr int kDim = 128;     // d_k = d_v
 constexpr int kChunk = 64;    // tokens per chunk of the prefill path
 
 // Segment plan of the prefill (intra-device context parallelism).  A sequence longer than
-// kSplitChunks chunks is cut into segments of kSegChunks chunks; the plan depends on the
-// sequence's own length only, so packing never changes a sequence's results.  A split
-// sequence costs about three passes over its tokens (segment states from zero, segment
-// transitions, then the outputs), so only sequences whose single pass would outlast a
-// typical batch (above 64K tokens) are split.
-constexpr int kSegChunks = 128;
+// kSplitChunks chunks is cut into segments: a first launch computes every segment's state from
+// zero and its transition (two work items per segment but the last), a second reruns every
+// segment from its composed incoming state (one item each).  A split sequence therefore costs
+// about three passes over its tokens, so only sequences whose single pass would outlast a
+// typical batch (above 64K tokens) are split.  The segment count is picked among a few
+// candidates (128-chunk segments, and one, two or three items per SM per head) by a model of
+// the two launches' waves on kPlanSMs SMs, segments of at least kMinSegChunks chunks: a wave of
+// items costs its segment length, outputs 43 and no outputs 40 per chunk.  The plan is a
+// function of the sequence's own length and the head count only, so packing never changes a
+// sequence's results.  All segments but the last have seg_chunks chunks; the last is shorter
+// or equal and never empty.
 constexpr int kSplitChunks = 1024;
-__host__ __device__ __forceinline__ int num_segments(int64_t len) {
+constexpr int kPlanSMs = 152;
+constexpr int kMinSegChunks = 64;
+struct SegPlan {
+    int nseg;        // 1: the sequence runs whole
+    int seg_chunks;  // chunks per segment (the last may have fewer)
+};
+__host__ __device__ __forceinline__ int64_t segment_plan_cost(int64_t nc, int H, int64_t n) {
+    const int64_t seg = (nc + n - 1) / n;
+    const int64_t w0 = (2 * (int64_t)H * (n - 1) + kPlanSMs - 1) / kPlanSMs;
+    const int64_t w1 = ((int64_t)H * n + kPlanSMs - 1) / kPlanSMs;
+    return seg * (40 * w0 + 43 * w1);
+}
+__host__ __device__ __forceinline__ SegPlan segment_plan(int64_t len, int H) {
     const int64_t nc = (len + kChunk - 1) / kChunk;
-    return nc > kSplitChunks ? (int)((nc + kSegChunks - 1) / kSegChunks) : 1;
+    if (nc <= kSplitChunks) return SegPlan{1, (int)nc};
+    const int64_t cap = nc / kMinSegChunks;
+    int64_t pick = (nc + 127) / 128;
+    int64_t best = segment_plan_cost(nc, H, pick);
+    for (int k = 1; k <= 3; ++k) {
+        int64_t n = (int64_t)k * kPlanSMs / (H > 0 ? H : 1);
+        n = n < cap ? n : cap;
+        n = n > 2 ? n : 2;
+        const int64_t c = segment_plan_cost(nc, H, n);
+        if (c < best) {
+            best = c;
+            pick = n;
+        }
+    }
+    const int64_t seg = (nc + pick - 1) / pick;
+    return SegPlan{(int)((nc + seg - 1) / seg), (int)seg};
 }
 
 // Device status codes written into the sticky status word (same values as kda_status).

@@ -622,7 +622,8 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int64_t seq_begin = p.cu_seqlens[n];
     const int64_t seq_len = p.cu_seqlens[n + 1] - seq_begin;
     const int64_t unit = (int64_t)n * H + h;
-    const int nseg = num_segments(seq_len);
+    const SegPlan sp = segment_plan(seq_len, H);
+    const int nseg = sp.nseg;
     // the device cu_seqlens must agree with the host plan the buffers were sized from
     bool bad = seq_begin < 0 || seq_len < 0 || seq_begin + seq_len > order.total_tokens ||
                (order.count > 0 && seq_len != order.len[n]);
@@ -644,14 +645,14 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         sigma = blockIdx.z;
         item = ITEM_SEGMENT;
     }
-    const int64_t seg_tokens = (int64_t)kSegChunks * kChunk;
+    const int64_t seg_tokens = (int64_t)sp.seg_chunks * kChunk;
     const int64_t seq0 = item == ITEM_WHOLE ? seq_begin : seq_begin + sigma * seg_tokens;
     const int L = (int)(item == ITEM_WHOLE ? seq_len : min(seg_tokens, seq_len - sigma * seg_tokens));
     int64_t slot = 0;  // workspace slot of (sequence, segment)
     if (item != ITEM_WHOLE) {
         int64_t base = 0;
         for (int m = 0; m < n; ++m) {
-            const int ns = num_segments((int64_t)p.cu_seqlens[m + 1] - p.cu_seqlens[m]);
+            const int ns = segment_plan((int64_t)p.cu_seqlens[m + 1] - p.cu_seqlens[m], H).nseg;
             if (ns > 1) base += ns;
         }
         bad |= base + nseg > order.total_slots;
@@ -1334,7 +1335,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
             for (int m = 0; m < n; ++m) base += (p.cu_seqlens[m + 1] - p.cu_seqlens[m]) / every;
             ckpt0 = p.ckpt + (base * H + h) * (int64_t)(kDim * kDim);
         }
-        const int chunk0 = item == ITEM_SEGMENT ? sigma * kSegChunks : 0;
+        const int chunk0 = item == ITEM_SEGMENT ? sigma * sp.seg_chunks : 0;
         float pro_dt = 0.f, pro_a = 0.f, pro_lb = 0.f;
         if constexpr (kPro) {
             pro_dt = p.pro_dt_bias ? p.pro_dt_bias[h * kDim + te] : 0.f;
@@ -1525,11 +1526,11 @@ kda_segment_combine_kernel(const int32_t* __restrict__ cu_seqlens, const float* 
     float* S = cs + kDim * kCombineLdM;     // [128][16]: columns 16 cb .. 16 cb + 15 of the state
     const int n = blockIdx.x, h = blockIdx.y, cb = blockIdx.z, tid = threadIdx.x;
     const int64_t len = (int64_t)cu_seqlens[n + 1] - cu_seqlens[n];
-    const int nseg = num_segments(len);
+    const int nseg = segment_plan(len, H).nseg;
     if (nseg <= 1) return;
     int64_t base = 0;
     for (int m = 0; m < n; ++m) {
-        const int ns = num_segments((int64_t)cu_seqlens[m + 1] - cu_seqlens[m]);
+        const int ns = segment_plan((int64_t)cu_seqlens[m + 1] - cu_seqlens[m], H).nseg;
         if (ns > 1) base += ns;
     }
     // the device cu_seqlens must agree with the host plan the workspace was sized from
@@ -1637,7 +1638,7 @@ cudaError_t launch_prefill_tc(int num_seqs, int heads, int64_t total_tokens, con
     if (host_seqlens) {
         int64_t slots = 0, ckpts = 0;
         for (int n = 0; n < num_seqs; ++n) {
-            const int ns = num_segments(host_seqlens[n]);
+            const int ns = segment_plan(host_seqlens[n], heads).nseg;
             if (ns > 1) slots += ns;
             if (ckpt_chunks > 0) ckpts += host_seqlens[n] / (kChunk * ckpt_chunks);
         }

@@ -60,19 +60,32 @@ def test_plan_counts_chunks_per_sequence(lib):
 
 
 def test_plan_splits_long_sequences_by_length_only(lib):
+    """The segment count is picked among 128-chunk segments and k * 152 / H segments (k = 1, 2,
+    3; at least 64 chunks each) by the wave cost seg * (40 ceil(2H(n-1) / 152) + 43 ceil(Hn /
+    152)), seg = ceil(chunks / n); segments of seg chunks, the last shorter."""
     from kimi_delta_attention_03_gb300 import binding
     H = 3
-    lens = [65536, 65537, 262144, 5]  # 1024 chunks (whole), 1025 (9 segments), 4096 (32), 1
+    # 1024 chunks: whole.  1025 chunks: n = 9 (128-chunk) costs 114 * 83 = 9462, n = 16 (the cap
+    # 1025 // 64) costs 65 * 83 = 5395 -> 16 segments of 65.  4096 chunks: n = 32 costs
+    # 128 * 123 = 15744, n = 50 (152 // 3) costs 82 * 123 = 10086, n = 64 (the cap) costs
+    # 64 * 206 = 13184 -> segments of 82, 50 of them.
+    lens = [65536, 65537, 262144, 5]
     info = binding.fwd_plan(lens, H)
-    assert info["segment_chunks"] == 128
+    assert info["segment_chunks"] == 82
     assert info["split_sequences"] == 2
-    assert info["work_items"] == 1 + 9 + 32 + 1
-    slots = 9 + 32
+    assert info["work_items"] == 1 + 16 + 50 + 1
+    slots = 16 + 50
     assert info["workspace_bytes"] == 3 * slots * H * 128 * 128 * 4
     assert binding.fwd_workspace_bytes(lens, H) == info["workspace_bytes"]
     # the plan of a sequence does not depend on its neighbours
-    assert binding.fwd_plan([65537], H)["work_items"] == 9
+    assert binding.fwd_plan([65537], H)["work_items"] == 16
+    assert binding.fwd_plan([65537], H)["segment_chunks"] == 65
     assert binding.fwd_plan([100, 200], H)["workspace_bytes"] == 0
+    assert binding.fwd_plan([100, 200], H)["segment_chunks"] == 0
+    # 262,144 tokens with 16 heads (the long-sequence workload): 19 segments of 216 chunks
+    # (576 + 304 items, about four and two waves), against 32 of 128 (992 + 512)
+    info = binding.fwd_plan([262144], 16)
+    assert (info["work_items"], info["segment_chunks"]) == (19, 216)
 
 
 def test_checkpoint_count(lib):

@@ -127,7 +127,10 @@ def test_checkpoints_of_a_segmented_sequence():
     """A sequence above 64K tokens runs as segments; checkpoints that fall inside segments and
     on their boundaries come out of the second pass with the right positions."""
     lens = [70000, 300]
-    every = 3072  # 48 chunks: not aligned to the 128-chunk segments
+    # 16 chunks: checkpoints inside the 65-chunk segments, and the 65th on the boundary of
+    # segments 15 and 16 (chunk 1040)
+    every = 1024
+    assert kda().binding.fwd_plan(lens, 1)["segment_chunks"] == 65
     x = synth.make_inputs(lens, 1, torch.bfloat16, seed=22, device=DEV)
     out, fin, ck = kda().fwd_chunked_checkpoints(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
                                                  x["cu_seqlens"], x["seqlens"], every,
@@ -520,10 +523,11 @@ def test_varlen_64_full_size():
 def test_segmented_sequences_match_oracle():
     """Sequences above 1024 chunks run as segments (transition + state-from-zero per segment,
     composed, then rerun); the result equals the token loop."""
-    lens = [70000, 100, 66000, 65536]  # 1094, 2, 1032, 1024 chunks: split, whole, split, whole
+    # 1094, 2, 1032, 1024 chunks: split (17 segments of 65), whole, split (16 of 65), whole
+    lens = [70000, 100, 66000, 65536]
     x = synth.make_inputs(lens, 2, torch.bfloat16, seed=31, device=DEV)
     info = kda().binding.fwd_plan(lens, 2)
-    assert info["split_sequences"] == 2 and info["work_items"] == 9 + 1 + 9 + 1
+    assert info["split_sequences"] == 2 and info["work_items"] == 17 + 1 + 16 + 1
     out, fin = run_gpu(x)
     o_ref, s_ref = run_oracle(x)
     assert_close("out", out.cpu(), o_ref)
