@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kDecodeThreads = 256;
 
+
 // The input prologue of the decode variants that take raw projections (kPro): per head rate and
 // bias of the gate, its lower bound, and the q scale (arithmetic in kda_prologue.cuh).
 struct DecPro {
@@ -322,20 +323,20 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                 __syncthreads();
             }
 
-            float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-            float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+            float2 x01 = make_float2(0.f, 0.f), x23 = x01, y01 = x01, y23 = x01;
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 const int i = warp + 8 * r;
                 const float a = s_a[cur][i], kk = s_k[cur][i], qq = s_q[cur][i];
-                s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
-                x0 = fmaf(kk, s[r].x, x0); x1 = fmaf(kk, s[r].y, x1);
-                x2 = fmaf(kk, s[r].z, x2); x3 = fmaf(kk, s[r].w, x3);
-                y0 = fmaf(qq, s[r].x, y0); y1 = fmaf(qq, s[r].y, y1);
-                y2 = fmaf(qq, s[r].z, y2); y3 = fmaf(qq, s[r].w, y3);
+                const float2 a2 = make_float2(a, a), k2 = make_float2(kk, kk), q2 = make_float2(qq, qq);
+                const float2 s01 = mul_f32x2(make_float2(s[r].x, s[r].y), a2);
+                const float2 s23 = mul_f32x2(make_float2(s[r].z, s[r].w), a2);
+                s[r] = make_float4(s01.x, s01.y, s23.x, s23.y);
+                x01 = fma_f32x2(k2, s01, x01); x23 = fma_f32x2(k2, s23, x23);
+                y01 = fma_f32x2(q2, s01, y01); y23 = fma_f32x2(q2, s23, y23);
             }
-            reinterpret_cast<float4*>(s_rx[warp])[lane] = make_float4(x0, x1, x2, x3);
-            reinterpret_cast<float4*>(s_ry[warp])[lane] = make_float4(y0, y1, y2, y3);
+            reinterpret_cast<float4*>(s_rx[warp])[lane] = make_float4(x01.x, x01.y, x23.x, x23.y);
+            reinterpret_cast<float4*>(s_ry[warp])[lane] = make_float4(y01.x, y01.y, y23.x, y23.y);
             if (warp == 0) {
                 float p = 0.f;
 #pragma unroll
@@ -364,11 +365,14 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
             __syncthreads();
 
             const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
+            const float2 u01 = make_float2(u4.x, u4.y), u23 = make_float2(u4.z, u4.w);
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 const float kk = s_k[cur][warp + 8 * r];
-                s[r].x = fmaf(kk, u4.x, s[r].x); s[r].y = fmaf(kk, u4.y, s[r].y);
-                s[r].z = fmaf(kk, u4.z, s[r].z); s[r].w = fmaf(kk, u4.w, s[r].w);
+                const float2 k2 = make_float2(kk, kk);
+                const float2 s01 = fma_f32x2(k2, u01, make_float2(s[r].x, s[r].y));
+                const float2 s23 = fma_f32x2(k2, u23, make_float2(s[r].z, s[r].w));
+                s[r] = make_float4(s01.x, s01.y, s23.x, s23.y);
             }
             if (t + 1 == ncommit && S) {  // uniform: the stores issue only on the commit token
 #pragma unroll
