@@ -47,17 +47,16 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-# The backward pass and the host-buffer pipeline (host code only) sit in files of their own that
-# no traffic record covers, so they are left out of the hash that dates the forward kernels'
-# records.
-_UNRECORDED_SOURCES = ("kda_backward.cu", "kda_host.cu")
+# The traffic records cover the prefill and decode kernels: the hash that dates them is taken
+# over those kernels' translation units and every shared header they include.
+_RECORDED_SOURCES = ("kda_prefill_tc.cu", "kda_decode.cu")
 
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kimi_delta_attention_03_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")) and f not in _UNRECORDED_SOURCES:
+        if f in _RECORDED_SOURCES or f.endswith(".cuh"):
             h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 

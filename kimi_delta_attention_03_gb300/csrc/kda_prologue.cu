@@ -68,15 +68,20 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
                     const float* __restrict__ dt_bias, float lower_bound, float q_scale,
                     bf16* __restrict__ q, bf16* __restrict__ k, bf16* __restrict__ v,
                     bf16* __restrict__ g, bf16* __restrict__ beta, int64_t rows, int H) {
+    // every head's gate rate, once per CTA (dynamic shared memory of H floats)
+    extern __shared__ float s_na[];
+    for (int i = threadIdx.x; i < H; i += kProThreads) s_na[i] = pro_gate_rate(A_log, i);
+    __syncthreads();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (kProThreads / 32);
     int64_t row = (int64_t)blockIdx.x * (kProThreads / 32) + (threadIdx.x >> 5);
     if (row >= rows) return;
     int h = (int)(row % H);
+    const int h_step = (int)(warps % H);  // the head advances by this much per row step
     ProRow cur = load_row(q_raw, k_raw, v_raw, g_raw, beta_logit, dt_bias, row, h, lane);
     while (true) {
         const int64_t next = row + warps;
-        const int hn = (int)(next % H);
+        const int hn = h + h_step >= H ? h + h_step - H : h + h_step;
         ProRow nxt = cur;
         if (next < rows) nxt = load_row(q_raw, k_raw, v_raw, g_raw, beta_logit, dt_bias, next, hn, lane);
         const int64_t base = row * kDim;
@@ -90,7 +95,7 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
                               pack2_bf16(x[4], x[5]), pack2_bf16(x[6], x[7])));
         }
         {   // v: Swish; g: the bounded gate (four channels per lane)
-            const float na = pro_gate_rate(A_log, h);
+            const float na = s_na[h];
             const float dt[4] = {cur.dt.x, cur.dt.y, cur.dt.z, cur.dt.w};
             const uint32_t vw[2] = {cur.v.x, cur.v.y}, gw[2] = {cur.g.x, cur.g.y};
             uint32_t vo[2], go[2];
@@ -171,16 +176,22 @@ struct ConvLane {
                 w[j][0] = t.x; w[j][1] = t.y; w[j][2] = t.z; w[j][3] = t.w;
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 4; c += 2) {  // two channels per packed FMA, each in tap order
                 const int i = 4 * h4 + c;
-                float acc = 0.f;
-                acc = fmaf(w[0][c], win[0][i], acc);
-                acc = fmaf(w[1][c], win[1][i], acc);
-                acc = fmaf(w[2][c], win[2][i], acc);
-                y[i] = fmaf(w[3][c], x[i], acc);
-                win[0][i] = win[1][i];
-                win[1][i] = win[2][i];
-                win[2][i] = x[i];
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                    acc = fma_f32x2(make_float2(w[j][c], w[j][c + 1]),
+                                    make_float2(win[j][i], win[j][i + 1]), acc);
+                acc = fma_f32x2(make_float2(w[3][c], w[3][c + 1]), make_float2(x[i], x[i + 1]), acc);
+                y[i] = acc.x;
+                y[i + 1] = acc.y;
+#pragma unroll
+                for (int e = i; e < i + 2; ++e) {
+                    win[0][e] = win[1][e];
+                    win[1][e] = win[2][e];
+                    win[2][e] = x[e];
+                }
             }
         }
     }
@@ -377,18 +388,22 @@ cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const vo
                             float q_scale, void* q, void* k, void* v, void* g, void* beta,
                             cudaStream_t stream) {
     if (rows <= 0) return cudaSuccess;
+    const size_t smem = (size_t)heads * sizeof(float);  // the per-head gate rates
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err == cudaSuccess && smem > 48 * 1024)
+        err = cudaFuncSetAttribute(kda_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem);
     if (err == cudaSuccess)
         err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_prologue_kernel,
-                                                            kProThreads, 0);
+                                                            kProThreads, smem);
     if (err != cudaSuccess) return err;
     const int64_t per_block = kProThreads / 32;
     const int64_t need = (rows + per_block - 1) / per_block;
     const int64_t slots = (int64_t)(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
     const unsigned grid = (unsigned)(need < slots ? need : slots);
-    kda_prologue_kernel<<<grid, kProThreads, 0, stream>>>(
+    kda_prologue_kernel<<<grid, kProThreads, smem, stream>>>(
         (const bf16*)q_raw, (const bf16*)k_raw, (const bf16*)v_raw, (const bf16*)g_raw,
         (const bf16*)beta_logit, A_log, dt_bias, lower_bound, q_scale, (bf16*)q, (bf16*)k,
         (bf16*)v, (bf16*)g, (bf16*)beta, rows, heads);
