@@ -88,6 +88,29 @@ def test_plan_splits_long_sequences_by_length_only(lib):
     assert (info["work_items"], info["segment_chunks"]) == (19, 216)
 
 
+def test_segment_plan_covers_every_sequence_without_empty_segments(lib):
+    """For lengths across the split threshold and head counts from 1 to 512: a split sequence has
+    at least two segments of at least 64 chunks, the segments cover its chunks with a non-empty
+    last one ((n - 1) * seg < chunks <= n * seg), and its plan is the same packed with others."""
+    from kimi_delta_attention_03_gb300 import binding
+    lengths = [65536, 65537, 65600, 70000, 100000, 131072, 262144, 262145, 400000, 1048576,
+               3_000_000]
+    for H in (1, 2, 3, 8, 16, 32, 64, 96, 152, 153, 512):
+        for L in lengths:
+            info = binding.fwd_plan([L], H)
+            chunks = (L + 63) // 64
+            n, seg = info["work_items"], info["segment_chunks"]
+            if chunks <= 1024:
+                assert (n, seg, info["split_sequences"]) == (1, 0, 0)
+                continue
+            assert info["split_sequences"] == 1 and n >= 2 and seg >= 64, (L, H, n, seg)
+            assert (n - 1) * seg < chunks <= n * seg, (L, H, n, seg)
+            assert info["workspace_bytes"] == 3 * n * H * 128 * 128 * 4
+        packed = binding.fwd_plan([5] + lengths + [7], H)
+        alone = sum(binding.fwd_plan([L], H)["work_items"] for L in lengths)
+        assert packed["work_items"] == alone + 2
+
+
 def test_checkpoint_count(lib):
     from kimi_delta_attention_03_gb300 import binding
     lens = [0, 63, 64, 511, 512, 1000, 1024]
