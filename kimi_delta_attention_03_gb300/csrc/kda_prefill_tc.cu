@@ -469,11 +469,15 @@ __device__ __forceinline__ int decay_scan_body(unsigned char* sm, int cs, int L,
                 gcol + (t16 + i) * 128 + ((chunk16 ^ (i & 7)) << 4)));
         if constexpr (kPro) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                gv[i] = pro_gate(gv[i], dt, a, lb);
+            for (int i = 0; i < 16; i += 2) {
+                const float2 gg = pro_gate2(make_float2(gv[i], gv[i + 1]), dt, a, lb);
+                gv[i] = gg.x;
+                gv[i + 1] = gg.y;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
                 *reinterpret_cast<bf16*>(const_cast<unsigned char*>(gcol) + (t16 + i) * 128 +
                                          ((chunk16 ^ (i & 7)) << 4)) = __float2bfloat16_rn(gv[i]);
-            }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -957,8 +961,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     float kv[8], qv[8];
                     unpack8(*reinterpret_cast<const uint4*>(kq + o), kv);
                     unpack8(*reinterpret_cast<const uint4*>(kq + o + 64 * 128), qv);
-                    pro_swish_l2(kv, 1.f);
-                    pro_swish_l2(qv, p.pro_q_scale);
+                    pro_swish_l2_kq(kv, qv, p.pro_q_scale);  // packing rounds them to bf16
                     *reinterpret_cast<uint4*>(kq + o) = pack8(kv);
                     *reinterpret_cast<uint4*>(kq + o + 64 * 128) = pack8(qv);
                 }
@@ -1276,8 +1279,7 @@ kda_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     uint4* src = reinterpret_cast<uint4*>(sm + OFF_V) + tp + kPrepThreads * j;
                     float x[8];
                     unpack8(*src, x);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) x[i] = pro_swish(x[i]);
+                    pro_swish8(x);
                     *src = pack8(x);
                 }
             }

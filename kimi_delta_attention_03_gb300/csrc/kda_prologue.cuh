@@ -17,6 +17,8 @@
 
 #include <cuda_bf16.h>
 
+#include "kda_common.cuh"
+
 namespace kda {
 
 constexpr float kProNormEps = 1e-6f;  // added to the sum of squares of the L2 norm
@@ -58,6 +60,14 @@ __device__ __forceinline__ float pro_gate(float g, float dt, float na, float lb)
     return round_bf16(__fmul_rn(lb, rcp_sfu(__fadd_rn(1.f, ex2_sfu(__fmul_rn(na, __fadd_rn(g, dt)))))));
 }
 
+// pro_gate of two values as packed fp32 pairs (the same operations per value, the same bits)
+__device__ __forceinline__ float2 pro_gate2(float2 g, float dt, float na, float lb) {
+    const float2 y = mul_f32x2(make_float2(na, na), add_f32x2(g, make_float2(dt, dt)));
+    const float2 d = add_f32x2(make_float2(1.f, 1.f), make_float2(ex2_sfu(y.x), ex2_sfu(y.y)));
+    const float2 z = mul_f32x2(make_float2(lb, lb), make_float2(rcp_sfu(d.x), rcp_sfu(d.y)));
+    return make_float2(round_bf16(z.x), round_bf16(z.y));
+}
+
 // na = -exp(A_log[h]) log2 e for head h
 __device__ __forceinline__ float pro_gate_rate(const float* A_log, int h) {
     return __fmul_rn(-1.4426950408889634f, expf(A_log[h]));
@@ -83,6 +93,46 @@ __device__ __forceinline__ void pro_swish_l2(float (&x)[8], float scale) {
     const float inv = __fmul_rn(rsqrtf(__fadd_rn(row_sum_squares16(x), kProNormEps)), scale);
 #pragma unroll
     for (int j = 0; j < 8; ++j) x[j] = round_bf16(__fmul_rn(x[j], inv));
+}
+
+// pro_swish_l2 for a row of k and a row of q held by the same 16-lane group, as packed fp32
+// pairs (k, q): the same operations in the same order per value, so the same bits.  The results
+// are left unrounded for a caller that packs them to bf16 (which rounds them as round_bf16 would).
+__device__ __forceinline__ void pro_swish_l2_kq(float (&k)[8], float (&q)[8], float q_scale) {
+    float2 ss = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float2 hh = mul_f32x2(make_float2(0.5f, 0.5f), make_float2(k[j], q[j]));
+        const float2 sw = fma_f32x2(hh, make_float2(tanh_sfu(hh.x), tanh_sfu(hh.y)), hh);
+        k[j] = sw.x;
+        q[j] = sw.y;
+        ss = fma_f32x2(sw, sw, ss);
+    }
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) {
+        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, ss.x, off),
+                                     __shfl_xor_sync(0xffffffffu, ss.y, off));
+        ss = make_float2(__fadd_rn(ss.x, o.x), __fadd_rn(ss.y, o.y));
+    }
+    const float2 inv = make_float2(rsqrtf(__fadd_rn(ss.x, kProNormEps)),
+                                   __fmul_rn(rsqrtf(__fadd_rn(ss.y, kProNormEps)), q_scale));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float2 x = mul_f32x2(make_float2(k[j], q[j]), inv);
+        k[j] = x.x;
+        q[j] = x.y;
+    }
+}
+
+// Swish of eight values as packed fp32 pairs (the same bits as pro_swish on each)
+__device__ __forceinline__ void pro_swish8(float (&x)[8]) {
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        const float2 hh = mul_f32x2(make_float2(0.5f, 0.5f), make_float2(x[j], x[j + 1]));
+        const float2 sw = fma_f32x2(hh, make_float2(tanh_sfu(hh.x), tanh_sfu(hh.y)), hh);
+        x[j] = sw.x;
+        x[j + 1] = sw.y;
+    }
 }
 
 }  // namespace kda
