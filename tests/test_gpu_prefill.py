@@ -298,6 +298,21 @@ def test_host_buffer_call_equal_lengths():
     assert_close("final_state", fin_h.numpy(), s_ref)
 
 
+def test_host_buffer_call_bounded_gate():
+    """Gates over K3's whole bounded range (decay windows shorter than a chunk) through the
+    host-buffer call: sequences resumed from their fp32 state at part boundaries, against the
+    oracle."""
+    lens = [1000, 3000, 17, 0, 640]
+    x = synth.make_inputs(lens, 2, torch.bfloat16, seed=25, device=DEV, bounded_gate=-5.0)
+    host, s0 = _host_copies(x, True)
+    out_h, fin_h = kda().fwd_chunked_host(host["q"], host["k"], host["v"], host["log_alpha"],
+                                          host["beta"], x["seqlens"], init_state=s0, parts=5)
+    check_status()
+    o_ref, s_ref = run_oracle(x)
+    assert_close("out", out_h, o_ref)
+    assert_close("final_state", fin_h.numpy(), s_ref)
+
+
 def test_host_buffer_call_full_size():
     """The benchmark's end-to-end call: 4 x 8192 tokens, 32 heads, 8 parts (each copy one
     strided run over the four sequences).  Every output and state against the device call through the parity gate, and
