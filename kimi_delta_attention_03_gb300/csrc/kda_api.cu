@@ -414,11 +414,11 @@ static int64_t bwd_floats_per_unit(const kda_desc* desc) {
 
 size_t kda_bwd_workspace_bytes(const kda_desc* desc) {
     if (check_desc(desc, true) != KDA_OK) return 0;
-    // the units' regions, then the four column blocks' partial dq, dk, dg (128 floats each) and
-    // dbeta per token and head
+    // the units' regions, then the column blocks' partial dq, dk, dg (128 floats each) and dbeta
+    // per token and head
     const int64_t TH = desc->total_tokens * desc->num_heads;
     return ((size_t)bwd_floats_per_unit(desc) * desc->num_seqs * desc->num_heads +
-            (size_t)4 * TH * (3 * 128 + 1)) * sizeof(float);
+            (size_t)kda::kBwdColBlocks * TH * (3 * 128 + 1)) * sizeof(float);
 }
 
 kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const void* v,

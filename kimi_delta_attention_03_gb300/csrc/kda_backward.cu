@@ -12,17 +12,18 @@
 // and the gradient of the initial state is dS after the first token.
 //
 // The value channels (columns of S) evolve independently: x = S'^T k, u, du = dS^T k and the
-// updates of S and dS act column by column, so each unit runs as kColBlocks CTAs of 128 threads,
-// one per block of 32 columns.  Only the outputs dq, dk, dg and dbeta sum over the columns; each
-// CTA writes its block's partial sums into the workspace, and a second launch adds the four
-// partials in a fixed order, so the gradients do not depend on scheduling.
+// updates of S and dS act column by column, so each unit runs as kBwdColBlocks CTAs of 128
+// threads, one per block of kDim / kBwdColBlocks columns.  Only the outputs dq, dk, dg and dbeta
+// sum over the columns; each CTA writes its block's partial sums into the workspace, and a second
+// launch adds the partials in a fixed order, so the gradients do not depend on scheduling.
 //
-// Thread (warp w, lane l) of a CTA holds columns 4 (l & 7) .. +3 of its block and rows
-// {(l >> 3) + 4 w + 16 r : r < 8} of S', and of dS, in registers (a warp covers four consecutive
-// rows of 32 columns per access).  A forward sweep stores the state before every 16-token block
-// into the caller's workspace; the reverse sweep recomputes each block's states from its stored
-// start (keeping the 16 of them in the workspace) and walks the block backwards.  Column sums and
-// row sums go through shared memory.  fp32 throughout, on CUDA cores.
+// Thread t of a CTA holds one float4 of columns (t % kLanesPerRow) and rows
+// {t / kLanesPerRow + kRowGroups r} of S', and of dS, in registers (with 32-column blocks a warp
+// covers four consecutive rows of 32 columns per access).  A forward sweep stores the state
+// before every 16-token block into the caller's workspace; the reverse sweep recomputes each
+// block's states from its stored start (keeping the 16 of them in the workspace) and walks the
+// block backwards.  Column sums and row sums go through shared memory.  fp32 throughout, on CUDA
+// cores.
 #include <algorithm>
 
 #include "kda_common.cuh"
@@ -32,9 +33,11 @@ namespace {
 
 constexpr int kBwdThreads = 128;
 constexpr int kBwdBlock = 16;   // tokens per stored state
-constexpr int kColBlocks = 4;   // CTAs per unit
-constexpr int kCols = kDim / kColBlocks;  // 32 columns per CTA
-constexpr int kRowsPer = 8;     // rows of S per thread
+constexpr int kCols = kDim / kBwdColBlocks;          // columns per CTA
+constexpr int kLanesPerRow = kCols / 4;                 // lanes that share a row (a float4 each)
+constexpr int kRowGroups = kBwdThreads / kLanesPerRow;  // rows held at once by the CTA
+constexpr int kRowsPer = kDim / kRowGroups;             // rows of S per thread
+constexpr int kColBlocks = kBwdColBlocks;
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -64,13 +67,13 @@ template <typename TIn>
 __global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<TIn> p) {
     __shared__ float s_k[kDim], s_q[kDim], s_a[kDim];
     __shared__ float s_v[kCols], s_do[kCols], s_u[kCols], s_r[kCols], s_du[kCols];
-    __shared__ __align__(16) float s_part[16][kCols];       // per row group, column partials
-    __shared__ __align__(16) float s_rp[3][kDim][8];        // per row, 4-column partials (x8)
+    __shared__ __align__(16) float s_part[kRowGroups][kCols];       // per row group, column partials
+    __shared__ __align__(16) float s_rp[3][kDim][kLanesPerRow];     // per row, 4-column partials
     __shared__ float s_ud;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cq = lane & 7;                  // float4 column group within the block
-    const int rg = (lane >> 3) + 4 * warp;    // row group: rows rg + 16 r
+    const int cq = tid % kLanesPerRow;        // float4 column group within the block
+    const int rg = tid / kLanesPerRow;        // row group: rows rg + kRowGroups r
     const int64_t unit = blockIdx.x / kColBlocks;
     const int cb = (int)(blockIdx.x - unit * kColBlocks);
     const int j0 = cb * kCols;                // first column of this CTA
@@ -100,18 +103,18 @@ __global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<T
     auto ld_full = [&](const float* src, float4 (&x)[kRowsPer]) {
 #pragma unroll
         for (int r = 0; r < kRowsPer; ++r)
-            x[r] = src ? reinterpret_cast<const float4*>(src + (rg + 16 * r) * kDim + j0)[cq]
+            x[r] = src ? reinterpret_cast<const float4*>(src + (rg + kRowGroups * r) * kDim + j0)[cq]
                        : make_float4(0.f, 0.f, 0.f, 0.f);
     };
     auto ld_blk = [&](const float* src, float4 (&x)[kRowsPer]) {
 #pragma unroll
         for (int r = 0; r < kRowsPer; ++r)
-            x[r] = reinterpret_cast<const float4*>(src + (rg + 16 * r) * kCols)[cq];
+            x[r] = reinterpret_cast<const float4*>(src + (rg + kRowGroups * r) * kCols)[cq];
     };
     auto st_blk = [&](float* dst, const float4 (&x)[kRowsPer]) {
 #pragma unroll
         for (int r = 0; r < kRowsPer; ++r)
-            reinterpret_cast<float4*>(dst + (rg + 16 * r) * kCols)[cq] = x[r];
+            reinterpret_cast<float4*>(dst + (rg + kRowGroups * r) * kCols)[cq] = x[r];
     };
     // One token's inputs, held raw in registers from their load to their staging, so that the
     // next token's loads are in flight while this one computes: k, g (row tid) and v (column
@@ -168,7 +171,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<T
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < kRowsPer; ++r) {
-                const int i = rg + 16 * r;
+                const int i = rg + kRowGroups * r;
                 const float a = s_a[i], kk = s_k[i];
                 S[r].x *= a; S[r].y *= a; S[r].z *= a; S[r].w *= a;
                 x.x = fmaf(kk, S[r].x, x.x); x.y = fmaf(kk, S[r].y, x.y);
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<T
         if (tid < kCols) {
             float x = 0.f;
 #pragma unroll
-            for (int w = 0; w < 16; ++w) x += s_part[w][tid];
+            for (int w = 0; w < kRowGroups; ++w) x += s_part[w][tid];
             const float r = s_v[tid] - x;
             s_r[tid] = r;
             s_u[tid] = b * r;
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<T
         const float4 u4 = reinterpret_cast<const float4*>(s_u)[cq];
 #pragma unroll
         for (int r = 0; r < kRowsPer; ++r) {
-            const float kk = s_k[rg + 16 * r];
+            const float kk = s_k[rg + kRowGroups * r];
             S[r].x = fmaf(kk, u4.x, S[r].x); S[r].y = fmaf(kk, u4.y, S[r].y);
             S[r].z = fmaf(kk, u4.z, S[r].z); S[r].w = fmaf(kk, u4.w, S[r].w);
         }
@@ -242,7 +245,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<T
                 float4 dup = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int r = 0; r < kRowsPer; ++r) {
-                    const int i = rg + 16 * r;
+                    const int i = rg + kRowGroups * r;
                     const float qq = s_q[i], kk = s_k[i];
                     dS[r].x = fmaf(qq, do4.x, dS[r].x); dS[r].y = fmaf(qq, do4.y, dS[r].y);
                     dS[r].z = fmaf(qq, do4.z, dS[r].z); dS[r].w = fmaf(qq, do4.w, dS[r].w);
@@ -250,20 +253,24 @@ __global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<T
                     dup.z = fmaf(kk, dS[r].z, dup.z); dup.w = fmaf(kk, dS[r].w, dup.w);
                 }
                 reinterpret_cast<float4*>(s_part[rg])[cq] = dup;
-                if (warp == 0) {
-                    const float ud = warp_sum(s_u[lane] * s_do[lane]);
+                if (warp == 0) {  // every lane takes part; lanes past the block's columns add 0
+                    const float ud = warp_sum(lane < kCols ? s_u[lane] * s_do[lane] : 0.f);
                     if (lane == 0) s_ud = ud;
                 }
             }
             __syncthreads();
-            if (tid < kCols) {  // du = dS^T k; dv = beta du; dbeta partial = du . r
-                float du = 0.f;
+            if (warp == 0) {  // du = dS^T k; dv = beta du; dbeta partial = du . r
+                float dr = 0.f;
+                if (lane < kCols) {
+                    float du = 0.f;
 #pragma unroll
-                for (int w = 0; w < 16; ++w) du += s_part[w][tid];
-                s_du[tid] = du;
-                p.dv[row * kDim + j0 + tid] = b_t * du;
-                const float db = warp_sum(du * s_r[tid]);
-                if (tid == 0) pdb[row] = db;
+                    for (int w = 0; w < kRowGroups; ++w) du += s_part[w][lane];
+                    s_du[lane] = du;
+                    p.dv[row * kDim + j0 + lane] = b_t * du;
+                    dr = du * s_r[lane];
+                }
+                const float db = warp_sum(dr);  // every lane of warp 0 takes part
+                if (lane == 0) pdb[row] = db;
             }
             __syncthreads();
             const float ud = s_ud;
@@ -273,7 +280,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<T
                 const float4 do4 = reinterpret_cast<const float4*>(s_do)[cq];
 #pragma unroll
                 for (int r = 0; r < kRowsPer; ++r) {
-                    const int i = rg + 16 * r;
+                    const int i = rg + kRowGroups * r;
                     // dq_i = (S' do)_i + k_i (u . do); dk_i = (dS u)_i - beta (S' du)_i
                     s_rp[0][i][cq] = S[r].x * do4.x + S[r].y * do4.y + S[r].z * do4.z + S[r].w * do4.w;
                     s_rp[1][i][cq] = dS[r].x * u4.x + dS[r].y * u4.y + dS[r].z * u4.z + dS[r].w * u4.w -
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<T
             {  // this block's partial row sums for row tid (read before the next token's barrier)
                 float sq = 0.f, sk = 0.f, sg = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+                for (int e = 0; e < kLanesPerRow; ++e) {
                     sq += s_rp[0][tid][e];
                     sk += s_rp[1][tid][e];
                     sg += s_rp[2][tid][e];
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<T
         float* dst = p.d_init + sbase;
 #pragma unroll
         for (int r = 0; r < kRowsPer; ++r)
-            reinterpret_cast<float4*>(dst + (rg + 16 * r) * kDim + j0)[cq] = dS[r];
+            reinterpret_cast<float4*>(dst + (rg + kRowGroups * r) * kDim + j0)[cq] = dS[r];
     }
 }
 

@@ -57,6 +57,12 @@ __host__ __device__ __forceinline__ SegPlan segment_plan(int64_t len, int H) {
     return SegPlan{(int)((nc + seg - 1) / seg), (int)seg};
 }
 
+// The backward runs each (sequence, head) unit as kBwdColBlocks CTAs, one per block of value
+// channels; its workspace holds that many partial sums of dq, dk, dlog_alpha and dbeta.  Every
+// CTA lasts its whole sequence, so the count is set for one wave: 4 blocks put the 4 x 8192 x 32
+// workload's 512 CTAs on 152 SMs x 4; 8 blocks (1,024 CTAs at six per SM) need a second wave.
+constexpr int kBwdColBlocks = 4;
+
 // Device status codes written into the sticky status word (same values as kda_status).
 constexpr int kStatusDecayRange = KDA_ERR_DECAY_RANGE;
 constexpr int kStatusTimeout = KDA_ERR_TIMEOUT;
