@@ -2,7 +2,7 @@
 
 Tolerance (stated for bf16 inputs and an fp32 state): both tensors are divided by the
 oracle's RMS over the whole tensor; the gate is relative L2 error <= 1e-2 and max absolute
-error <= 5e-2 of that RMS.  Outputs and final states are judged separately.
+error <= 5e-2 of that RMS.  Outputs and final states are assessed separately.
 
 Outputs stored as bf16 (the operator returns o in its input dtype): each element's own storage
 rounding, half a bf16 unit in the last place of the larger of |gpu| and |ref|, is not counted
