@@ -9,8 +9,9 @@
 // The step is bound by HBM: 64 KiB of state read and 64 KiB written per unit against about
 // 1.3 KFLOP per KiB.  Each CTA (256 threads) owns one unit and keeps the whole decayed state
 // in registers between the read and the write, so S crosses HBM exactly twice:
-//   thread (warp w, lane l) holds rows {w + 8 r : r < 16}, columns 4l .. 4l+3 (one float4
-//   per row; a warp touches one full 512-byte row per access, fully coalesced).
+//   thread (warp w, lane l) holds rows {16 w + r : r < 16}, columns 4l .. 4l+3 (one float4
+//   per row; a warp touches one full 512-byte row per access, fully coalesced; its rows are
+//   contiguous, so their decay, k and q scalars come four to a shared-memory load).
 // The two column reductions x = (D S)^T k and y = (D S)^T q are per-thread partial sums over
 // its 16 rows, then a cross-warp sum through shared memory.  The output uses the identity
 //     o = S_new^T q = y + (k . q) u,
@@ -55,22 +56,40 @@ __device__ __forceinline__ void load_raw(RawTok& r, const __nv_bfloat16* k,
 }
 
 // The prologue of one token's channels [32 cw, 32 cw + 32) by one warp, with no barrier: the
-// warp forms both row norms itself, in the order of the standalone prologue (eight in-order FMAs
-// per lane of a 16-lane group, then the 1-2-4-8 butterfly), then writes its channels of k and q
-// (Swish, scaled, rounded to bf16), alpha = exp(gate) and v = Swish(v) (rounded to bf16).
+// warp forms both row norms itself and writes its channels of k and q (Swish, scaled, rounded to
+// bf16), alpha = exp(gate) and v = Swish(v) (rounded to bf16).  The norms are the standalone
+// prologue's: eight in-order FMAs per lane of a 16-lane group, then the sum over the group that
+// its 1-2-4-8 butterfly forms, which is the balanced binary tree over the 16 lane partials (each
+// pairwise addition is commutative, so every lane of the butterfly ends with exactly that tree).
+// Here each lane reads its group's 16 partials from the warp's 32-float scratch in shared memory
+// and adds the tree itself; two independent shuffles then hand every lane both scales.
+__device__ __forceinline__ float tree_sum16(const float* p) {
+    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4),
+                 c = *reinterpret_cast<const float4*>(p + 8), d = *reinterpret_cast<const float4*>(p + 12);
+    const float l1[8] = {__fadd_rn(a.x, a.y), __fadd_rn(a.z, a.w), __fadd_rn(b.x, b.y),
+                         __fadd_rn(b.z, b.w), __fadd_rn(c.x, c.y), __fadd_rn(c.z, c.w),
+                         __fadd_rn(d.x, d.y), __fadd_rn(d.z, d.w)};
+    const float l2[4] = {__fadd_rn(l1[0], l1[1]), __fadd_rn(l1[2], l1[3]), __fadd_rn(l1[4], l1[5]),
+                         __fadd_rn(l1[6], l1[7])};
+    return __fadd_rn(__fadd_rn(l2[0], l2[1]), __fadd_rn(l2[2], l2[3]));
+}
 __device__ __forceinline__ void warp_prologue(const RawTok& r, float dt, float na, float lb,
-                                              float q_scale, int c, int lane, float* s_k,
-                                              float* s_q, float* s_a, float* s_v) {
-    float x[8];
+                                              float q_scale, int c, int lane, float* scratch,
+                                              float* s_k, float* s_q, float* s_a, float* s_v) {
+    float ss = 0.f;
     const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&r.grp);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float2 f = __bfloat1622float2(p2[j]);
-        x[2 * j] = pro_swish(f.x);
-        x[2 * j + 1] = pro_swish(f.y);
+        const float x0 = pro_swish(f.x), x1 = pro_swish(f.y);
+        ss = fmaf(x0, x0, ss);
+        ss = fmaf(x1, x1, ss);
     }
-    const float ss = row_sum_squares16(x);
-    const float inv = __fmul_rn(rsqrtf(__fadd_rn(ss, kProNormEps)), lane < 16 ? 1.f : q_scale);
+    scratch[lane] = ss;
+    __syncwarp();
+    const float inv = __fmul_rn(rsqrtf(__fadd_rn(tree_sum16(scratch + (lane & 16)), kProNormEps)),
+                                lane < 16 ? 1.f : q_scale);
+    __syncwarp();  // the scratch is rewritten by the warp's next token
     const float ik = __shfl_sync(0xffffffffu, inv, 0);
     const float iq = __shfl_sync(0xffffffffu, inv, 16);
     s_k[c] = round_bf16(__fmul_rn(pro_swish(__bfloat162float(r.kc)), ik));
@@ -85,7 +104,8 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                   const TIn* __restrict__ v, const TIn* __restrict__ g,
                   const TIn* __restrict__ beta, float* __restrict__ state,
                   TIn* __restrict__ out, int64_t units, const DecPro pro) {
-    __shared__ float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_u[kDim];
+    __shared__ __align__(16) float s_k[kDim], s_q[kDim], s_a[kDim], s_v[kDim], s_u[kDim];
+    __shared__ __align__(16) float s_norm[kPro ? 4 : 1][32];  // per prologue warp: norm partials
     __shared__ __align__(16) float s_rx[8][kDim];
     __shared__ __align__(16) float s_ry[8][kDim];
     __shared__ float s_kq;
@@ -113,15 +133,16 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
             const float na = pro_gate_rate(pro.A_log, h);
 #pragma unroll
             for (int r = 0; r < 16; ++r)
-                s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
+                s[r] = __ldcs(reinterpret_cast<const float4*>(S + (16 * warp + r) * kDim) + lane);
             if (warp < 4)
-                warp_prologue(raw, dt, na, pro.lb, pro.q_scale, tid, lane, s_k, s_q, s_a, s_v);
+                warp_prologue(raw, dt, na, pro.lb, pro.q_scale, tid, lane, s_norm[warp], s_k, s_q,
+                              s_a, s_v);
             b = round_bf16(pro_sigmoid(io<TIn>::to_f(rb)));
             __syncthreads();
         } else {
 #pragma unroll
             for (int r = 0; r < 16; ++r)
-                s[r] = __ldcs(reinterpret_cast<const float4*>(S + (warp + 8 * r) * kDim) + lane);
+                s[r] = __ldcs(reinterpret_cast<const float4*>(S + (16 * warp + r) * kDim) + lane);
             if (tid < kDim) {
                 const int64_t e = unit * kDim + tid;
                 s_k[tid] = io<TIn>::to_f(k[e]);
@@ -136,14 +157,22 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
         float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int i = warp + 8 * r;
-            const float a = s_a[i], kk = s_k[i], qq = s_q[i];
-            s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
-            x0 = fmaf(kk, s[r].x, x0); x1 = fmaf(kk, s[r].y, x1);
-            x2 = fmaf(kk, s[r].z, x2); x3 = fmaf(kk, s[r].w, x3);
-            y0 = fmaf(qq, s[r].x, y0); y1 = fmaf(qq, s[r].y, y1);
-            y2 = fmaf(qq, s[r].z, y2); y3 = fmaf(qq, s[r].w, y3);
+        for (int r4 = 0; r4 < 16; r4 += 4) {  // the warp's rows are contiguous: four scalars a load
+            const float4 a4 = *reinterpret_cast<const float4*>(s_a + 16 * warp + r4);
+            const float4 k4 = *reinterpret_cast<const float4*>(s_k + 16 * warp + r4);
+            const float4 q4 = *reinterpret_cast<const float4*>(s_q + 16 * warp + r4);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w},
+                        qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int r = r4 + m;
+                const float a = av[m], kk = kv[m], qq = qv[m];
+                s[r].x *= a; s[r].y *= a; s[r].z *= a; s[r].w *= a;
+                x0 = fmaf(kk, s[r].x, x0); x1 = fmaf(kk, s[r].y, x1);
+                x2 = fmaf(kk, s[r].z, x2); x3 = fmaf(kk, s[r].w, x3);
+                y0 = fmaf(qq, s[r].x, y0); y1 = fmaf(qq, s[r].y, y1);
+                y2 = fmaf(qq, s[r].z, y2); y3 = fmaf(qq, s[r].w, y3);
+            }
         }
         reinterpret_cast<float4*>(s_rx[warp])[lane] = make_float4(x0, x1, x2, x3);
         reinterpret_cast<float4*>(s_ry[warp])[lane] = make_float4(y0, y1, y2, y3);
@@ -170,11 +199,11 @@ kda_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            const float kk = s_k[warp + 8 * r];
+            const float kk = s_k[16 * warp + r];
             float4 o;
             o.x = fmaf(kk, u4.x, s[r].x); o.y = fmaf(kk, u4.y, s[r].y);
             o.z = fmaf(kk, u4.z, s[r].z); o.w = fmaf(kk, u4.w, s[r].w);
-            __stcs(reinterpret_cast<float4*>(S + (warp + 8 * r) * kDim) + lane, o);
+            __stcs(reinterpret_cast<float4*>(S + (16 * warp + r) * kDim) + lane, o);
         }
         __syncthreads();  // shared vectors are rewritten by the next unit of this CTA
     }
@@ -205,8 +234,10 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
     // while warps 0-3 form the token's u, so the token vectors are double-buffered (token t in
     // buffer t & 1).
     constexpr int NB = kPro ? 2 : 1;
-    __shared__ float s_k[NB][kDim], s_q[NB][kDim], s_a[NB][kDim], s_v[NB][kDim], s_u[kDim];
+    __shared__ __align__(16) float s_k[NB][kDim], s_q[NB][kDim], s_a[NB][kDim], s_v[NB][kDim];
+    __shared__ __align__(16) float s_u[kDim];
     __shared__ float s_b[NB];
+    __shared__ __align__(16) float s_norm[kPro ? 4 : 1][32];  // per prologue warp: norm partials
     __shared__ __align__(16) float s_rx[8][kDim];
     __shared__ __align__(16) float s_ry[8][kDim];
     __shared__ float s_kq;
@@ -239,7 +270,7 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         float4 s[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r)
-            s[r] = Sin ? __ldcs(reinterpret_cast<const float4*>(Sin + (warp + 8 * r) * kDim) + lane)
+            s[r] = Sin ? __ldcs(reinterpret_cast<const float4*>(Sin + (16 * warp + r) * kDim) + lane)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
         float pro_dt = 0.f, pro_na = 0.f;
         if constexpr (kPro) {  // warps 4-7 run the prologue, channel tid - 128 each
@@ -294,6 +325,7 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         [[maybe_unused]] auto pro_token = [&](int buf) {
             if (tid >= kDim) {
                 warp_prologue(raw, pro_dt, pro_na, pro.lb, pro.q_scale, tid - kDim, lane,
+                              s_norm[warp - 4],
                               s_k[buf], s_q[buf], s_a[buf], s_v[buf]);
                 if (tid == kDim) s_b[buf] = round_bf16(pro_sigmoid(io<TIn>::to_f(nb)));
             }
@@ -325,15 +357,36 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
 
             float2 x01 = make_float2(0.f, 0.f), x23 = x01, y01 = x01, y23 = x01;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int i = warp + 8 * r;
-                const float a = s_a[cur][i], kk = s_k[cur][i], qq = s_q[cur][i];
-                const float2 a2 = make_float2(a, a), k2 = make_float2(kk, kk), q2 = make_float2(qq, qq);
-                const float2 s01 = mul_f32x2(make_float2(s[r].x, s[r].y), a2);
-                const float2 s23 = mul_f32x2(make_float2(s[r].z, s[r].w), a2);
-                s[r] = make_float4(s01.x, s01.y, s23.x, s23.y);
-                x01 = fma_f32x2(k2, s01, x01); x23 = fma_f32x2(k2, s23, x23);
-                y01 = fma_f32x2(q2, s01, y01); y23 = fma_f32x2(q2, s23, y23);
+            for (int r4 = 0; r4 < 16; r4 += 4) {
+                // contiguous rows: four scalars a load (one at a time with raw projections, whose
+                // prologue already holds the registers the wider loads need)
+                float av[4], kv[4], qv[4];
+                if constexpr (kPro) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        av[m] = s_a[cur][16 * warp + r4 + m];
+                        kv[m] = s_k[cur][16 * warp + r4 + m];
+                        qv[m] = s_q[cur][16 * warp + r4 + m];
+                    }
+                } else {
+                    const float4 a4 = *reinterpret_cast<const float4*>(&s_a[cur][16 * warp + r4]);
+                    const float4 k4 = *reinterpret_cast<const float4*>(&s_k[cur][16 * warp + r4]);
+                    const float4 q4 = *reinterpret_cast<const float4*>(&s_q[cur][16 * warp + r4]);
+                    av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
+                    kv[0] = k4.x; kv[1] = k4.y; kv[2] = k4.z; kv[3] = k4.w;
+                    qv[0] = q4.x; qv[1] = q4.y; qv[2] = q4.z; qv[3] = q4.w;
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int r = r4 + m;
+                    const float2 a2 = make_float2(av[m], av[m]), k2 = make_float2(kv[m], kv[m]),
+                                 q2 = make_float2(qv[m], qv[m]);
+                    const float2 s01 = mul_f32x2(make_float2(s[r].x, s[r].y), a2);
+                    const float2 s23 = mul_f32x2(make_float2(s[r].z, s[r].w), a2);
+                    s[r] = make_float4(s01.x, s01.y, s23.x, s23.y);
+                    x01 = fma_f32x2(k2, s01, x01); x23 = fma_f32x2(k2, s23, x23);
+                    y01 = fma_f32x2(q2, s01, y01); y23 = fma_f32x2(q2, s23, y23);
+                }
             }
             reinterpret_cast<float4*>(s_rx[warp])[lane] = make_float4(x01.x, x01.y, x23.x, x23.y);
             reinterpret_cast<float4*>(s_ry[warp])[lane] = make_float4(y01.x, y01.y, y23.x, y23.y);
@@ -348,27 +401,47 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
             }
             __syncthreads();
 
-            if (tid < kDim) {
-                float x = 0.f, y = 0.f;
+            [[maybe_unused]] float y_keep = 0.f;
+            if constexpr (kPro) {
+                if (tid < kDim) {
+                    float x = 0.f, y = 0.f;
 #pragma unroll
-                for (int w8 = 0; w8 < 8; ++w8) { x += s_rx[w8][tid]; y += s_ry[w8][tid]; }
-                const float u = b * (s_v[cur][tid] - x);
-                s_u[tid] = u;
-                if (out) out[row * kDim + tid] = io<TIn>::from_f(fmaf(s_kq, u, y));
-            }
-            if constexpr (kPro) {  // meanwhile the next token's prologue, into the other buffer
+                    for (int w8 = 0; w8 < 8; ++w8) { x += s_rx[w8][tid]; y += s_ry[w8][tid]; }
+                    const float u = b * (s_v[cur][tid] - x);
+                    s_u[tid] = u;
+                    if (out) out[row * kDim + tid] = io<TIn>::from_f(fmaf(s_kq, u, y));
+                }
+                // meanwhile the next token's prologue on warps 4-7, into the other buffer
                 if (t + 1 < len) {
                     pro_token(cur ^ 1);
                     if (t + 2 < len) fetch(t + 2);
                 }
+            } else {
+                // x on threads 0-127 (then u), y on threads 128-255; the output, which needs u,
+                // is written in the next phase
+                const int j = tid & (kDim - 1);
+                const float(*part)[kDim] = tid < kDim ? s_rx : s_ry;
+                float acc = 0.f;
+#pragma unroll
+                for (int w8 = 0; w8 < 8; ++w8) acc += part[w8][j];
+                if (tid < kDim)
+                    s_u[j] = b * (s_v[cur][j] - acc);
+                else
+                    y_keep = acc;
             }
             __syncthreads();
+            if constexpr (!kPro) {
+                if (tid >= kDim && out) {
+                    const int j = tid - kDim;
+                    out[row * kDim + j] = io<TIn>::from_f(fmaf(s_kq, s_u[j], y_keep));
+                }
+            }
 
             const float4 u4 = reinterpret_cast<const float4*>(s_u)[lane];
             const float2 u01 = make_float2(u4.x, u4.y), u23 = make_float2(u4.z, u4.w);
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
-                const float kk = s_k[cur][warp + 8 * r];
+                const float kk = s_k[cur][16 * warp + r];
                 const float2 k2 = make_float2(kk, kk);
                 const float2 s01 = fma_f32x2(k2, u01, make_float2(s[r].x, s[r].y));
                 const float2 s23 = fma_f32x2(k2, u23, make_float2(s[r].z, s[r].w));
@@ -377,7 +450,7 @@ kda_decode_window_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
             if (t + 1 == ncommit && S) {  // uniform: the stores issue only on the commit token
 #pragma unroll
                 for (int r = 0; r < 16; ++r)
-                    __stcs(reinterpret_cast<float4*>(S + (warp + 8 * r) * kDim) + lane, s[r]);
+                    __stcs(reinterpret_cast<float4*>(S + (16 * warp + r) * kDim) + lane, s[r]);
             }
             __syncthreads();  // shared vectors are rewritten by the next token
         }
