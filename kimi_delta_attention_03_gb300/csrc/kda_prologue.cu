@@ -89,7 +89,7 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
         {   // q or k: Swish, then the row norm
             float x[8];
             unpack8_bf16(cur.qk, x);
-            pro_swish_l2(x, is_q ? q_scale : 1.f);
+            pro_swish_l2_packed(x, is_q ? q_scale : 1.f);  // the packing rounds them to bf16
             __stcs(reinterpret_cast<uint4*>((is_q ? q : k) + base + 8 * (lane & 15)),
                    make_uint4(pack2_bf16(x[0], x[1]), pack2_bf16(x[2], x[3]),
                               pack2_bf16(x[4], x[5]), pack2_bf16(x[6], x[7])));
@@ -101,11 +101,16 @@ kda_prologue_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict__ k_r
             uint32_t vo[2], go[2];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const float v0 = __uint_as_float(vw[i] << 16), v1 = __uint_as_float(vw[i] & 0xffff0000u);
-                const float g0 = __uint_as_float(gw[i] << 16), g1 = __uint_as_float(gw[i] & 0xffff0000u);
-                vo[i] = pack2_bf16(pro_swish(v0), pro_swish(v1));
-                go[i] = pack2_bf16(pro_gate(g0, dt[2 * i], na, lower_bound),
-                                   pro_gate(g1, dt[2 * i + 1], na, lower_bound));
+                const float2 vv = make_float2(__uint_as_float(vw[i] << 16),
+                                              __uint_as_float(vw[i] & 0xffff0000u));
+                const float2 gg = make_float2(__uint_as_float(gw[i] << 16),
+                                              __uint_as_float(gw[i] & 0xffff0000u));
+                const float2 hh = mul_f32x2(make_float2(0.5f, 0.5f), vv);  // Swish, in pairs
+                const float2 sw = fma_f32x2(hh, make_float2(tanh_sfu(hh.x), tanh_sfu(hh.y)), hh);
+                vo[i] = pack2_bf16(sw.x, sw.y);
+                const float2 ga = pro_gate2_dt(gg, make_float2(dt[2 * i], dt[2 * i + 1]), na,
+                                               lower_bound);
+                go[i] = pack2_bf16(ga.x, ga.y);
             }
             __stcs(reinterpret_cast<uint2*>(v + base + 4 * lane), make_uint2(vo[0], vo[1]));
             __stcs(reinterpret_cast<uint2*>(g + base + 4 * lane), make_uint2(go[0], go[1]));
@@ -329,20 +334,28 @@ kda_prologue_conv_kernel(const bf16* __restrict__ q_raw, const bf16* __restrict_
             float y[8], yv[4];
             cqk.step(xqk, y);
             cv.step(xv, yv);
-            pro_swish_l2(y, is_q ? q_scale : 1.f);
+            pro_swish_l2_packed(y, is_q ? q_scale : 1.f);  // the packing rounds them to bf16
             __stcs(reinterpret_cast<uint4*>((is_q ? q : k) + base + chqk),
                    make_uint4(pack2_bf16(y[0], y[1]), pack2_bf16(y[2], y[3]),
                               pack2_bf16(y[4], y[5]), pack2_bf16(y[6], y[7])));
             const float gv[4] = {__uint_as_float(gr.x << 16), __uint_as_float(gr.x & 0xffff0000u),
                                  __uint_as_float(gr.y << 16), __uint_as_float(gr.y & 0xffff0000u)};
-            __stcs(reinterpret_cast<uint2*>(v + base + chv),
-                   make_uint2(pack2_bf16(pro_swish(yv[0]), pro_swish(yv[1])),
-                              pack2_bf16(pro_swish(yv[2]), pro_swish(yv[3]))));
-            __stcs(reinterpret_cast<uint2*>(g + base + chv),
-                   make_uint2(pack2_bf16(pro_gate(gv[0], dt[0], na, lower_bound),
-                                         pro_gate(gv[1], dt[1], na, lower_bound)),
-                              pack2_bf16(pro_gate(gv[2], dt[2], na, lower_bound),
-                                         pro_gate(gv[3], dt[3], na, lower_bound))));
+            {  // v: Swish, in pairs
+                const float2 h01 = mul_f32x2(make_float2(0.5f, 0.5f), make_float2(yv[0], yv[1]));
+                const float2 h23 = mul_f32x2(make_float2(0.5f, 0.5f), make_float2(yv[2], yv[3]));
+                const float2 s01 = fma_f32x2(h01, make_float2(tanh_sfu(h01.x), tanh_sfu(h01.y)), h01);
+                const float2 s23 = fma_f32x2(h23, make_float2(tanh_sfu(h23.x), tanh_sfu(h23.y)), h23);
+                __stcs(reinterpret_cast<uint2*>(v + base + chv),
+                       make_uint2(pack2_bf16(s01.x, s01.y), pack2_bf16(s23.x, s23.y)));
+            }
+            {
+                const float2 g01 = pro_gate2_dt(make_float2(gv[0], gv[1]), make_float2(dt[0], dt[1]),
+                                                na, lower_bound);
+                const float2 g23 = pro_gate2_dt(make_float2(gv[2], gv[3]), make_float2(dt[2], dt[3]),
+                                                na, lower_bound);
+                __stcs(reinterpret_cast<uint2*>(g + base + chv),
+                       make_uint2(pack2_bf16(g01.x, g01.y), pack2_bf16(g23.x, g23.y)));
+            }
         }
         cp_async_wait<0>();  // nothing of this run is in flight when the ring is reused
     }

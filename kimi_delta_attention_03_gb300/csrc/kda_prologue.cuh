@@ -61,6 +61,12 @@ __device__ __forceinline__ float pro_gate(float g, float dt, float na, float lb)
 }
 
 // pro_gate of two values as packed fp32 pairs (the same operations per value, the same bits)
+__device__ __forceinline__ float2 pro_gate2_dt(float2 g, float2 dt, float na, float lb) {
+    const float2 y = mul_f32x2(make_float2(na, na), add_f32x2(g, dt));
+    const float2 d = add_f32x2(make_float2(1.f, 1.f), make_float2(ex2_sfu(y.x), ex2_sfu(y.y)));
+    const float2 z = mul_f32x2(make_float2(lb, lb), make_float2(rcp_sfu(d.x), rcp_sfu(d.y)));
+    return make_float2(round_bf16(z.x), round_bf16(z.y));
+}
 __device__ __forceinline__ float2 pro_gate2(float2 g, float dt, float na, float lb) {
     const float2 y = mul_f32x2(make_float2(na, na), add_f32x2(g, make_float2(dt, dt)));
     const float2 d = add_f32x2(make_float2(1.f, 1.f), make_float2(ex2_sfu(y.x), ex2_sfu(y.y)));
@@ -134,5 +140,19 @@ __device__ __forceinline__ void pro_swish8(float (&x)[8]) {
         x[j + 1] = sw.y;
     }
 }
+
+// pro_swish_l2 with its Swish and scaling on packed fp32 pairs, for a caller that packs the
+// results to bf16 (the packing rounds them as round_bf16 would): the same bits.
+__device__ __forceinline__ void pro_swish_l2_packed(float (&x)[8], float scale) {
+    pro_swish8(x);
+    const float inv = __fmul_rn(rsqrtf(__fadd_rn(row_sum_squares16(x), kProNormEps)), scale);
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        const float2 y = mul_f32x2(make_float2(x[j], x[j + 1]), make_float2(inv, inv));
+        x[j] = y.x;
+        x[j + 1] = y.y;
+    }
+}
+
 
 }  // namespace kda
