@@ -313,6 +313,26 @@ def test_host_buffer_call_bounded_gate():
     assert_close("final_state", fin_h.numpy(), s_ref)
 
 
+def test_host_buffer_call_pageable_memory():
+    """Pageable (not pinned) host inputs and outputs: the copies no longer overlap, but the call
+    gives the same results as with pinned buffers."""
+    lens = [700, 64, 1500]
+    x = synth.make_inputs(lens, 2, torch.bfloat16, seed=26, device=DEV)
+    pinned, s0p = _host_copies(x, True)
+    out_p, fin_p = kda().fwd_chunked_host(pinned["q"], pinned["k"], pinned["v"],
+                                          pinned["log_alpha"], pinned["beta"], x["seqlens"],
+                                          init_state=s0p, parts=4)
+    pageable = {nm: x[nm].cpu() for nm in ("q", "k", "v", "log_alpha", "beta")}
+    assert not pageable["q"].is_pinned()
+    out_h = torch.empty_like(pageable["q"])
+    fin_h = torch.empty((len(lens), 2, 128, 128), dtype=torch.float32)
+    kda().fwd_chunked_host(pageable["q"], pageable["k"], pageable["v"], pageable["log_alpha"],
+                           pageable["beta"], x["seqlens"], init_state=x["init_state"].cpu(),
+                           out=out_h, final_state=fin_h, parts=4)
+    check_status()
+    assert torch.equal(out_h, out_p) and torch.equal(fin_h, fin_p)
+
+
 def test_host_buffer_call_full_size():
     """The benchmark's end-to-end call: 4 x 8192 tokens, 32 heads, 8 parts (each copy one
     strided run over the four sequences).  Every output and state against the device call through the parity gate, and
