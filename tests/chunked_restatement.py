@@ -149,3 +149,99 @@ def unit_forward_segmented(q, k, v, g, beta, S0, seg_len, C=64):
     for (a, b), Si in zip(bounds, s_in):
         O[a:b], S = unit_forward(q[a:b], k[a:b], v[a:b], g[a:b], beta[a:b], Si, C)
     return O, S
+
+
+def _unit_lower_inverse16(A):
+    """(I + A)^{-1} for a strictly lower-triangular A by forward substitution, column by column."""
+    C = A.shape[0]
+    X = np.zeros((C, C))
+    for col in range(C):
+        for i in range(C):
+            X[i, col] = (1.0 if i == col else 0.0) - A[i, :i] @ X[:i, col]
+    return X
+
+
+def backward_prep(k, v, q, g, beta):
+    """Chunk-local factors of the chunked backward (one chunk of C tokens, zero-padded).
+
+    G = cumsum g; r = G_C / 2; a = exp(G_C)
+    K_f = k exp(G), Q_f = q exp(G)                 (decay from the chunk start)
+    K_p = k exp(G - r), K_m = k exp(r - G), Q_r = q exp(G - r)   (mid-chunk reference)
+    K_bar = k exp(G_C - G)                         (decay to the chunk end)
+    At = strict_lower(K_p K_m^T); A = diag(beta) At; P = lower_incl(Q_r K_m^T); T = (I + A)^-1
+    W = T diag(beta) K_f; U_bar = T diag(beta) V; Q' = Q_f - P W
+    """
+    G = np.cumsum(g, axis=0)
+    GC = G[-1]
+    r = GC / 2.0
+    f = dict(G=G, GC=GC, a=np.exp(GC), K_f=k * np.exp(G), Q_f=q * np.exp(G),
+             K_p=k * np.exp(G - r), K_m=k * np.exp(r - G), Q_r=q * np.exp(G - r),
+             K_bar=k * np.exp(GC - G))
+    f["At"] = np.tril(f["K_p"] @ f["K_m"].T, -1)
+    f["P"] = np.tril(f["Q_r"] @ f["K_m"].T, 0)
+    f["T"] = _unit_lower_inverse16(beta[:, None] * f["At"])
+    f["W"] = f["T"] @ (beta[:, None] * f["K_f"])
+    f["U_bar"] = f["T"] @ (beta[:, None] * v)
+    f["Qp"] = f["Q_f"] - f["P"] @ f["W"]
+    return f
+
+
+def backward_chunk_grads(f, q, k, v, beta, dO, S, dE, U):
+    """Gradients of one chunk given its start state S, the gradient dE of its end state and
+    its U = U_bar - W S.  Returns (dq, dk, dv, dG, dbeta) with dG the gradient with respect to
+    the in-chunk cumulative decay G (the caller turns it into dg by a suffix sum)."""
+    dU = f["P"].T @ dO + f["K_bar"] @ dE
+    dY = f["T"].T @ dU
+    R = v - f["K_f"] @ S
+    dbeta = np.sum(dY * R, axis=1)
+    dR = beta[:, None] * dY
+    dA = -np.tril(dY @ U.T, -1)
+    dbeta = dbeta + np.sum(dA * f["At"], axis=1)
+    dAt = beta[:, None] * dA
+    dP = np.tril(dO @ U.T, 0)
+    dK_f = -dR @ S.T
+    dQ_f = dO @ S.T
+    dK_bar = U @ dE.T
+    dK_p = dAt @ f["K_m"]
+    dK_m = dAt.T @ f["K_p"] + dP.T @ f["Q_r"]
+    dQ_r = dP @ f["K_m"]
+    G, GC = f["G"], f["GC"]
+    r = GC / 2.0
+    dk = dK_f * np.exp(G) + dK_p * np.exp(G - r) + dK_m * np.exp(r - G) + dK_bar * np.exp(GC - G)
+    dq = dQ_f * np.exp(G) + dQ_r * np.exp(G - r)
+    dG = (dK_f * f["K_f"] + dK_p * f["K_p"] - dK_m * f["K_m"] - dK_bar * f["K_bar"]
+          + dQ_f * f["Q_f"] + dQ_r * f["Q_r"])
+    dG[-1] += np.sum(dK_bar * f["K_bar"], axis=0) + f["a"] * np.sum(dE * S, axis=1)
+    return dq, dk, dR, dG, dbeta
+
+
+def unit_backward(q, k, v, g, beta, S0, dO, dSN, C=16):
+    """Chunked backward of one unit in three steps: chunk-local factors; the forward chain
+    S_{c+1} = diag(a) S_c + K_bar^T (U_bar - W S_c) and the reverse chain
+    dE_{c-1} = diag(a) dE_c + Q'^T dO - W^T (K_bar dE_c); then per-chunk gradients.
+    Returns (dq, dk, dv, dg, dbeta, dS0)."""
+    L = q.shape[0]
+    chunks = _chunks(L, C)
+    pads = [[_padded(x, c0, c1, C) for x in (q, k, v, g, beta, dO)] for c0, c1 in chunks]
+    facs = [backward_prep(kk, vv, qq, gg, bb) for qq, kk, vv, gg, bb, _ in pads]
+    S, starts, Us = S0.copy(), [], []
+    for f in facs:
+        starts.append(S)
+        U = f["U_bar"] - f["W"] @ S
+        Us.append(U)
+        S = f["a"][:, None] * S + f["K_bar"].T @ U
+    dE, ends = dSN.copy(), [None] * len(facs)
+    for c in range(len(facs) - 1, -1, -1):
+        f, dOc = facs[c], pads[c][5]
+        ends[c] = dE
+        dE = f["a"][:, None] * dE + f["Qp"].T @ dOc - f["W"].T @ (f["K_bar"] @ dE)
+    out = [np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), np.zeros_like(g), np.zeros(L)]
+    for c, (c0, c1) in enumerate(chunks):
+        qq, kk, vv, _, bb, dOc = pads[c]
+        dq, dk, dv, dG, db = backward_chunk_grads(facs[c], qq, kk, vv, bb, dOc, starts[c],
+                                                  ends[c], Us[c])
+        dg = np.cumsum(dG[::-1], axis=0)[::-1]
+        n = c1 - c0
+        for o, x in zip(out, (dq, dk, dv, dg, db)):
+            o[c0:c1] = x[:n]
+    return (*out, dE)

@@ -84,3 +84,28 @@ def test_rectangular_value_dim():
     o_r, s_r = _oracle_unit(*x)
     _close(o_c, o_r)
     _close(s_c, s_r)
+
+
+def _oracle_unit_backward(q, k, v, g, beta, S0, dO, dSN):
+    L = q.shape[0]
+    got = oracle.recurrence_backward(q[:, None], k[:, None], v[:, None], g[:, None],
+                                     beta[:, None], [0, L], dO[:, None],
+                                     state_in=S0[None, None], d_state=dSN[None, None])
+    return [x[:, 0] for x in got[:5]] + [got[5][0, 0]]
+
+
+@pytest.mark.parametrize("L,gate", [(1, 0.1), (15, 0.1), (16, 0.1), (17, 0.1), (50, 0.1),
+                                    (64, 2.0), (37, 6.0)])
+def test_chunked_backward_equals_autograd_of_the_token_loop(L, gate):
+    """The 16-token chunked backward (factors about the chunk's mid reference, forward and
+    reverse state chains, per-chunk gradients, suffix sum of dG) equals reverse-mode autograd
+    of the oracle's token loop: ragged last chunks, and gates down to a mean of -6 per token."""
+    from tests.chunked_restatement import unit_backward
+    q, k, v, g, beta, S0 = _inputs(L, 32, seed=100 + L, gate=gate, dv=24)
+    rng = np.random.default_rng(200 + L)
+    dO = rng.standard_normal((L, 24))
+    dSN = rng.standard_normal((32, 24)) * 0.1
+    got = unit_backward(q, k, v, g, beta, S0, dO, dSN, C=16)
+    ref = _oracle_unit_backward(q, k, v, g, beta, S0, dO, dSN)
+    for a, b in zip(got, ref):
+        _close(a, b, 1e-9)
