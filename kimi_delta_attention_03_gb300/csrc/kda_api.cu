@@ -403,22 +403,10 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
                               out, commit, stream, prm);
 }
 
-// Backward workspace per (sequence, head), in floats: one state per 16 tokens of the longest
-// sequence, the 16 decayed states of the block being reversed, and their 16 (u, r) vector pairs.
-static int64_t bwd_floats_per_unit(const kda_desc* desc) {
-    int64_t nb_max = 0;
-    for (int32_t n = 0; n < desc->num_seqs; ++n)
-        nb_max = std::max<int64_t>(nb_max, (desc->host_seqlens[n] + 15) / 16);
-    return (nb_max + 16) * 128 * 128 + 16 * 2 * 128;
-}
-
 size_t kda_bwd_workspace_bytes(const kda_desc* desc) {
     if (check_desc(desc, true) != KDA_OK) return 0;
-    // the units' regions, then the column blocks' partial dq, dk, dg (128 floats each) and dbeta
-    // per token and head
-    const int64_t TH = desc->total_tokens * desc->num_heads;
-    return ((size_t)bwd_floats_per_unit(desc) * desc->num_seqs * desc->num_heads +
-            (size_t)kda::kBwdColBlocks * TH * (3 * 128 + 1)) * sizeof(float);
+    const int64_t chunks = kda::backward_chunks(desc->host_seqlens, desc->num_seqs);
+    return kda::backward_workspace_floats(desc->num_seqs, desc->num_heads, chunks) * sizeof(float);
 }
 
 kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const void* v,
@@ -454,9 +442,10 @@ kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const voi
     cudaError_t e = kda::launch_backward(
         desc->in_dtype, desc->num_seqs, desc->num_heads, q, k, v, log_alpha, beta, cu_seqlens,
         init_state, d_out, d_state, dq, dk, dv, dlog_alpha, dbeta, dinit_state,
-        static_cast<float*>(workspace), bwd_floats_per_unit(desc), desc->total_tokens, status,
-        (cudaStream_t)stream);
-    g_launches += 1;
+        static_cast<float*>(workspace), kda::backward_chunks(desc->host_seqlens, desc->num_seqs),
+        desc->total_tokens, status, (cudaStream_t)stream);
+    if ((int64_t)desc->num_seqs * desc->num_heads > 0)
+        g_launches += desc->total_tokens > 0 ? 4 : 2;   // index, prep, forward, reverse
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

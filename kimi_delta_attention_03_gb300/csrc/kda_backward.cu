@@ -1,29 +1,40 @@
-// kda_backward.cu — gradients of the KDA recurrence (the backward pass), on CUDA cores.
+// kda_backward.cu — gradients of the KDA recurrence (the backward pass), chunked, on tensor cores.
 //
 // Forward, per (sequence, head) unit and token t ("How Kimi K3 Engineered Its Way to the Frontier",
 // section "How KDA updates its state"):
-//     S' = diag(a_t) S,  a_t = exp(g_t);   r = v_t - S'^T k_t;   u = beta_t r;
-//     S  <- S' + k_t u^T;                  o_t = S^T q_t
-// Reverse mode, given dS (the gradient of the state after token t, carried backwards) and do_t:
-//     dS += q_t do_t^T;     dq_t = S_t do_t = S' do_t + k_t (u . do_t)
-//     du = dS^T k_t;        dv_t = beta_t du;      dbeta_t = du . r
-//     dk_t = dS u - beta_t S' du
-//     dS' = dS - beta_t k_t du^T;   dg_t = rowsum(dS' * S');   dS <- diag(a_t) dS'
-// and the gradient of the initial state is dS after the first token.
+//     S' = diag(exp g_t) S;   u_t = beta_t (v_t - S'^T k_t);   S <- S' + k_t u_t^T;   o_t = S^T q_t
+// The backward steps the state once per 16-token chunk, as the pages' kernel does ("FlashKDA steps
+// the state once per 16 tokens"): a chunk with start state S, end state S+ and chunk-local
+//     G = cumsum g (per key channel), a = exp(G_C), r = G_C / 2
+//     K_f = k e^G, Q_f = q e^G, K_bar = k e^(G_C - G), K_p = k e^(G - r), K_m = k e^(r - G),
+//     Q_r = q e^(G - r)
+//     At = strict_lower(K_p K_m^T), P = lower_incl(Q_r K_m^T), T = (I + diag(beta) At)^-1
+//     R = V - K_f S,  U = T diag(beta) R,  O = Q_f S + P U,  S+ = diag(a) S + K_bar^T U
+// has, for dE the gradient of S+ and dO that of O,
+//     dU = P^T dO + K_bar dE,   dY = T^T dU,   dR = diag(beta) dY   (= dv)
+//     dbeta = rowsum(dY * R) + rowsum(dA * At),   dA = -strict_lower(dY U^T),  dP = lower_incl(dO U^T)
+//     dK_f = -dR S^T, dQ_f = dO S^T, dK_bar = U dE^T, dK_p = diag(beta) dA K_m,
+//     dK_m = (diag(beta) dA)^T K_p + dP^T Q_r, dQ_r = dP K_m
+//     dk = dK_f e^G + dK_p e^(G-r) + dK_m e^(r-G) + dK_bar e^(G_C-G);  dq = dQ_f e^G + dQ_r e^(G-r)
+//     dG = k (dK_f e^G + dK_p e^(G-r) - dK_m e^(r-G) - dK_bar e^(G_C-G)) + q (dQ_f e^G + dQ_r e^(G-r))
+//     dG[last] += sum_t dK_bar K_bar + a * rowsum(dE * S);   dg = suffix sum of dG over the chunk
+//     dS = diag(a) dE + Q_f^T dO - K_f^T dR = diag(a) dE + Q_f^T dO - W^T dU,   W = T diag(beta) K_f
+// The mid-chunk reference r keeps every factor within exp(+-80) when a 16-token chunk decays by at
+// most 160 in every channel (a mean of -10 per token, twice the bounded gate's floor of -5).
 //
-// The value channels (columns of S) evolve independently: x = S'^T k, u, du = dS^T k and the
-// updates of S and dS act column by column, so each unit runs as kBwdColBlocks CTAs of 128
-// threads, one per block of kDim / kBwdColBlocks columns.  Only the outputs dq, dk, dg and dbeta
-// sum over the columns; each CTA writes its block's partial sums into the workspace, and a second
-// launch adds the partials in a fixed order, so the gradients do not depend on scheduling.
-//
-// Thread t of a CTA holds one float4 of columns (t % kLanesPerRow) and rows
-// {t / kLanesPerRow + kRowGroups r} of S', and of dS, in registers (with 32-column blocks a warp
-// covers four consecutive rows of 32 columns per access).  A forward sweep stores the state
-// before every 16-token block into the caller's workspace; the reverse sweep recomputes each
-// block's states from its stored start (keeping the 16 of them in the workspace) and walks the
-// block backwards.  Column sums and row sums go through shared memory.  fp32 throughout, on CUDA
-// cores.
+// Four launches:
+//   index   one CTA: chunk offsets of the sequences from the device cu_seqlens, checked against the
+//           host's chunk total (a disagreement stops the later launches and reports it)
+//   prep    one CTA per (chunk, head): At, P and T (16 x 16 each) into the workspace
+//   forward one CTA per unit: the forward state chain, S^T kept in registers (warp w holds value
+//           channels 16w..16w+15), writing each chunk's start state (fp32) into the workspace
+//   reverse one CTA per unit: chunks in reverse, dE^T in shared memory, every gradient of the chunk
+// All products are m16n8k8 tf32 mma.sync with fp32 accumulation: 16-token tiles are the shape of
+// these instructions, and tf32 operands keep the gradients inside the parity gate where bf16
+// operands do not.  Within an 8-wide k step, MMA slots t and t + 4 take columns 2t and 2t + 1, so
+// that accumulator fragments feed the next product's A operand directly and operand pairs load as
+// 64-bit words.  Shared tiles of 128 fp32 columns use an XOR swizzle that keeps both fragment
+// access patterns (rows g, columns 2t..2t+1 and rows 2t, 2t+1, columns g) free of bank conflicts.
 #include <algorithm>
 
 #include "kda_common.cuh"
@@ -31,361 +42,958 @@
 namespace kda {
 namespace {
 
-constexpr int kBwdThreads = 128;
-constexpr int kBwdBlock = 16;   // tokens per stored state
-constexpr int kCols = kDim / kBwdColBlocks;          // columns per CTA
-constexpr int kLanesPerRow = kCols / 4;                 // lanes that share a row (a float4 each)
-constexpr int kRowGroups = kBwdThreads / kLanesPerRow;  // rows held at once by the CTA
-constexpr int kRowsPer = kDim / kRowGroups;             // rows of S per thread
-constexpr int kColBlocks = kBwdColBlocks;
+constexpr int kBC = 16;           // tokens per backward chunk
+constexpr int kBwdChainThreads = 256;
+constexpr int kPrepThreads = 128;
+constexpr int kTile = kBC * kDim;      // floats in a [16][128] tile
+constexpr int kState = kDim * kDim;    // floats in a state
+constexpr int kSmallLd = 24;           // leading dimension of the 16 x 16 tiles in shared memory
+constexpr int kSmall = kBC * kSmallLd;
+constexpr float kMaxExponent = 80.f;   // |G - r| bound of the factors
 
-__device__ __forceinline__ float warp_sum(float x) {
+__device__ __forceinline__ uint32_t tf32_bits(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(tf32_bits(x)); }
+__device__ __forceinline__ uint32_t bits(float x) { return __float_as_uint(x); }
+__device__ __forceinline__ uint32_t neg(uint32_t x) { return x ^ 0x80000000u; }
+
+__device__ __forceinline__ void mma8(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Element (r, c) of a [rows][128] fp32 tile: columns XORed with 8 * ((r & 3) ^ ((r >> 2) & 1)).
+__device__ __forceinline__ int swz(int r, int c) {
+    return r * kDim + (c ^ ((((r & 3) ^ ((r >> 2) & 1))) << 3));
+}
+
+// A fragment (16 x 8, permuted k) of a row-major tile X[m][k]: rows m0+g, m0+g+8, columns
+// k0+2t, k0+2t+1.
+__device__ __forceinline__ void lda_mk(const float* s, int m0, int k0, int g, int t,
+                                       uint32_t (&a)[4]) {
+    const float2 lo = *reinterpret_cast<const float2*>(s + swz(m0 + g, k0 + 2 * t));
+    const float2 hi = *reinterpret_cast<const float2*>(s + swz(m0 + g + 8, k0 + 2 * t));
+    a[0] = bits(lo.x); a[1] = bits(hi.x); a[2] = bits(lo.y); a[3] = bits(hi.y);
+}
+// A fragment of A[m][k] = X[k][m] (the tile holds the transpose).
+__device__ __forceinline__ void lda_km(const float* s, int m0, int k0, int g, int t,
+                                       uint32_t (&a)[4]) {
+    a[0] = bits(s[swz(k0 + 2 * t, m0 + g)]);
+    a[1] = bits(s[swz(k0 + 2 * t, m0 + g + 8)]);
+    a[2] = bits(s[swz(k0 + 2 * t + 1, m0 + g)]);
+    a[3] = bits(s[swz(k0 + 2 * t + 1, m0 + g + 8)]);
+}
+// B fragment (8 x 8, permuted k) of B[k][n] = X[n][k].
+__device__ __forceinline__ void ldb_nk(const float* s, int n0, int k0, int g, int t,
+                                       uint32_t (&b)[2]) {
+    const float2 v = *reinterpret_cast<const float2*>(s + swz(n0 + g, k0 + 2 * t));
+    b[0] = bits(v.x); b[1] = bits(v.y);
+}
+// B fragment of B[k][n] = X[k][n].
+__device__ __forceinline__ void ldb_kn(const float* s, int k0, int n0, int g, int t,
+                                       uint32_t (&b)[2]) {
+    b[0] = bits(s[swz(k0 + 2 * t, n0 + g)]);
+    b[1] = bits(s[swz(k0 + 2 * t + 1, n0 + g)]);
+}
+// Accumulator rows m0+g, m0+g+8 and columns c0+2t, c0+2t+1 into a swizzled tile.
+__device__ __forceinline__ void st_c(float* s, int m0, int c0, int g, int t, const float (&d)[4]) {
+    *reinterpret_cast<float2*>(s + swz(m0 + g, c0 + 2 * t)) = make_float2(d[0], d[1]);
+    *reinterpret_cast<float2*>(s + swz(m0 + g + 8, c0 + 2 * t)) = make_float2(d[2], d[3]);
+}
+// The same for the 16 x 16 tiles (leading dimension kSmallLd, no swizzle).
+__device__ __forceinline__ void lda_small(const float* s, int k0, int g, int t, uint32_t (&a)[4]) {
+    const float2 lo = *reinterpret_cast<const float2*>(s + g * kSmallLd + k0 + 2 * t);
+    const float2 hi = *reinterpret_cast<const float2*>(s + (g + 8) * kSmallLd + k0 + 2 * t);
+    a[0] = bits(lo.x); a[1] = bits(hi.x); a[2] = bits(lo.y); a[3] = bits(hi.y);
+}
+__device__ __forceinline__ void lda_small_tr(const float* s, int k0, int g, int t,
+                                             uint32_t (&a)[4]) {
+    a[0] = bits(s[(k0 + 2 * t) * kSmallLd + g]);
+    a[1] = bits(s[(k0 + 2 * t) * kSmallLd + g + 8]);
+    a[2] = bits(s[(k0 + 2 * t + 1) * kSmallLd + g]);
+    a[3] = bits(s[(k0 + 2 * t + 1) * kSmallLd + g + 8]);
+}
+
+struct BwdIndex {
+    const int32_t* idx;   // [N + 1] chunk offsets, then the stop flag
+    int N;
+};
+
+// Sequence of global chunk gc: the largest n < N with idx[n] <= gc.
+__device__ __forceinline__ int find_seq(const int32_t* idx, int N, int64_t gc) {
+    int lo = 0, hi = N;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (idx[mid] <= gc) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(1024) kda_bwd_index_kernel(const int32_t* __restrict__ cu,
+                                                             int N, int64_t host_chunks,
+                                                             int64_t total_tokens,
+                                                             int32_t* __restrict__ idx,
+                                                             int* status) {
+    __shared__ long long s_warp[32];
+    __shared__ long long s_carry;
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        s_carry = 0;
+        s_bad = cu[0] < 0;
+        idx[0] = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < N; base += 1024) {
+        const int n = base + tid;
+        long long c = 0;
+        if (n < N) {
+            const long long a = cu[n], b = cu[n + 1];
+            if (b < a || b > total_tokens) s_bad = 1;
+            else c = (b - a + kBC - 1) / kBC;
+        }
+        long long x = c;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-    return x;
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) s_warp[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            long long w = s_warp[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += y;
+            }
+            s_warp[lane] = w;
+        }
+        __syncthreads();
+        const long long incl = s_carry + x + (warp > 0 ? s_warp[warp - 1] : 0);
+        if (n < N) idx[n + 1] = (int32_t)(incl > 0x7fffffffLL ? 0x7fffffff : incl);
+        __syncthreads();
+        if (tid == 1023) s_carry = incl;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        const int stop = s_bad || s_carry != host_chunks;
+        idx[N + 1] = stop;
+        if (stop) report_status(status, KDA_ERR_INVALID_ARG);
+    }
 }
 
 template <typename TIn>
 struct BwdArgs {
     const TIn *q, *k, *v, *g, *beta;
-    const int32_t* cu_seqlens;
+    const int32_t* cu;
     const float* init_state;  // [N][H][128][128] or null
     const float* d_out;       // [T][H][128]
     const float* d_state;     // [N][H][128][128] or null
-    float *dv, *d_init;       // written directly
-    float* part;              // [3][kColBlocks][T][H][128] partial dq, dk, dg, then
-                              // [kColBlocks][T][H] partial dbeta
-    float* work;              // per (unit, column block): (nb_max + kBwdBlock) states of
-                              // 128 x 32, then kBwdBlock pairs of 32-vectors (u, r)
-    int64_t work_per_cta;     // floats
-    int64_t total_tokens;     // host T_tot
-    int* status;              // sticky status word
-    int H;
+    float *dq, *dk, *dv, *dg, *dbeta, *d_init;
+    const int32_t* idx;       // [N + 2]
+    float* tiles;             // [chunks][H][3][16][16]: T, P, At
+    float* states;            // [chunks][H][128][128]: S^T at each chunk's start
+    int* status;
+    int N, H;
 };
 
+// At, P and T of one chunk of one head.
 template <typename TIn>
-__global__ void __launch_bounds__(kBwdThreads, 4) kda_bwd_kernel(const BwdArgs<TIn> p) {
-    __shared__ float s_k[kDim], s_q[kDim], s_a[kDim];
-    __shared__ float s_v[kCols], s_do[kCols], s_u[kCols], s_r[kCols], s_du[kCols];
-    __shared__ __align__(16) float s_part[kRowGroups][kCols];       // per row group, column partials
-    __shared__ __align__(16) float s_rp[3][kDim][kLanesPerRow];     // per row, 4-column partials
-    __shared__ float s_ud;
-
+__global__ void __launch_bounds__(kPrepThreads) kda_bwd_prep_kernel(const BwdArgs<TIn> p) {
+    __shared__ __align__(16) float s_kp[kTile], s_km[kTile], s_qr[kTile];
+    __shared__ float s_at[kBC][kBC + 1];
+    __shared__ float s_beta[kBC];
+    if (p.idx[p.N + 1]) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cq = tid % kLanesPerRow;        // float4 column group within the block
-    const int rg = tid / kLanesPerRow;        // row group: rows rg + kRowGroups r
-    const int64_t unit = blockIdx.x / kColBlocks;
-    const int cb = (int)(blockIdx.x - unit * kColBlocks);
-    const int j0 = cb * kCols;                // first column of this CTA
-    const int n = (int)(unit / p.H), h = (int)(unit - (int64_t)n * p.H);
-    const int64_t t0 = p.cu_seqlens[n];
-    const int L = (int)(p.cu_seqlens[n + 1] - t0);
-    const int nb = (L + kBwdBlock - 1) / kBwdBlock;
-    // The device cu_seqlens must agree with the host lengths the workspace was sized from: the
-    // tokens stay inside T_tot and the unit's blocks inside its workspace region.  Every CTA of
-    // the unit takes the same decision.
-    if (t0 < 0 || L < 0 || t0 + L > p.total_tokens ||
-        nb > (p.work_per_cta - kBwdBlock * 2 * kCols) / (kDim * kCols) - kBwdBlock) {
-        if (tid == 0) report_status(p.status, KDA_ERR_INVALID_ARG);
-        return;
-    }
-    float* ck = p.work + (unit * kColBlocks + cb) * p.work_per_cta;  // [nb][128 * 32]
-    float* blk = ck + (int64_t)nb * kDim * kCols;                      // [16][128 * 32]
-    float* blk_ur = ck + p.work_per_cta - kBwdBlock * 2 * kCols;       // [16][2][32]
-    const int64_t sbase = unit * (int64_t)(kDim * kDim);
-    const int64_t TH = p.total_tokens * p.H;
-    float* pdq = p.part + (int64_t)cb * TH * kDim;
-    float* pdk = p.part + (int64_t)(kColBlocks + cb) * TH * kDim;
-    float* pdg = p.part + (int64_t)(2 * kColBlocks + cb) * TH * kDim;
-    float* pdb = p.part + (int64_t)3 * kColBlocks * TH * kDim + (int64_t)cb * TH;
-
-    // a full [128][128] state (columns j0 .. j0 + 31) or a compact [128][32] one
-    auto ld_full = [&](const float* src, float4 (&x)[kRowsPer]) {
-#pragma unroll
-        for (int r = 0; r < kRowsPer; ++r)
-            x[r] = src ? reinterpret_cast<const float4*>(src + (rg + kRowGroups * r) * kDim + j0)[cq]
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    };
-    auto ld_blk = [&](const float* src, float4 (&x)[kRowsPer]) {
-#pragma unroll
-        for (int r = 0; r < kRowsPer; ++r)
-            x[r] = reinterpret_cast<const float4*>(src + (rg + kRowGroups * r) * kCols)[cq];
-    };
-    auto st_blk = [&](float* dst, const float4 (&x)[kRowsPer]) {
-#pragma unroll
-        for (int r = 0; r < kRowsPer; ++r)
-            reinterpret_cast<float4*>(dst + (rg + kRowGroups * r) * kCols)[cq] = x[r];
-    };
-    // One token's inputs, held raw in registers from their load to their staging, so that the
-    // next token's loads are in flight while this one computes: k, g (row tid) and v (column
-    // j0 + tid, tid < 32) for a forward step; also q (row tid), d_out and the stored (u, r)
-    // (tid < 32) for a reverse step (ur non-null).
-    struct Tok {
-        TIn k, g, v, q, b;
-        float d, u, r;
-    };
-    auto fetch = [&](int t, const float* ur) -> Tok {
-        Tok x;
-        const int64_t row = (t0 + t) * p.H + h;
-        x.b = p.beta[row];
-        const int64_t e = row * kDim + tid;
-        x.k = p.k[e];
-        x.g = p.g[e];
-        if (ur) {
-            x.q = p.q[e];
-            if (tid < kCols) {
-                x.d = p.d_out[row * kDim + j0 + tid];
-                x.u = ur[tid];
-                x.r = ur[kCols + tid];
-            }
-        } else if (tid < kCols) {
-            x.v = p.v[row * kDim + j0 + tid];
-        }
-        return x;
-    };
-    // a fetched token into shared memory (a = exp(g)); returns its beta
-    auto stage = [&](const Tok& x, bool reverse) -> float {
-        s_k[tid] = io<TIn>::to_f(x.k);
-        s_a[tid] = expf(io<TIn>::to_f(x.g));
-        if (reverse) {
-            s_q[tid] = io<TIn>::to_f(x.q);
-            if (tid < kCols) {
-                s_do[tid] = x.d;
-                s_u[tid] = x.u;
-                s_r[tid] = x.r;
-            }
-        } else if (tid < kCols) {
-            s_v[tid] = io<TIn>::to_f(x.v);
-        }
-        return io<TIn>::to_f(x.b);
-    };
-    // one forward token: S' = diag(a) S; x = S'^T k; r = v - x; u = beta r; S <- S' + k u^T.
-    // Keeps S' and (u, r) when asked; nx holds token t's inputs on entry and token t_next's
-    // (when t_next >= 0) on return.
-    auto fwd_step = [&](float4 (&S)[kRowsPer], float* keep_s, float* keep_ur, Tok& nx,
-                        int t_next) {
-        const float b = stage(nx, false);
-        if (t_next >= 0) nx = fetch(t_next, nullptr);
-        __syncthreads();
-        {
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int r = 0; r < kRowsPer; ++r) {
-                const int i = rg + kRowGroups * r;
-                const float a = s_a[i], kk = s_k[i];
-                S[r].x *= a; S[r].y *= a; S[r].z *= a; S[r].w *= a;
-                x.x = fmaf(kk, S[r].x, x.x); x.y = fmaf(kk, S[r].y, x.y);
-                x.z = fmaf(kk, S[r].z, x.z); x.w = fmaf(kk, S[r].w, x.w);
-            }
-            reinterpret_cast<float4*>(s_part[rg])[cq] = x;
-            if (keep_s) st_blk(keep_s, S);
-        }
-        __syncthreads();
-        if (tid < kCols) {
-            float x = 0.f;
-#pragma unroll
-            for (int w = 0; w < kRowGroups; ++w) x += s_part[w][tid];
-            const float r = s_v[tid] - x;
-            s_r[tid] = r;
-            s_u[tid] = b * r;
-            if (keep_ur) {
-                keep_ur[tid] = b * r;
-                keep_ur[kCols + tid] = r;
-            }
-        }
-        __syncthreads();
-        const float4 u4 = reinterpret_cast<const float4*>(s_u)[cq];
-#pragma unroll
-        for (int r = 0; r < kRowsPer; ++r) {
-            const float kk = s_k[rg + kRowGroups * r];
-            S[r].x = fmaf(kk, u4.x, S[r].x); S[r].y = fmaf(kk, u4.y, S[r].y);
-            S[r].z = fmaf(kk, u4.z, S[r].z); S[r].w = fmaf(kk, u4.w, S[r].w);
-        }
-        __syncthreads();  // the shared vectors are rewritten by the next token
-    };
-
-    float4 S[kRowsPer], dS[kRowsPer];
-    // ---- forward sweep: the state before every block
-    ld_full(p.init_state ? p.init_state + sbase : nullptr, S);
-    Tok nx;
-    if (L > 0) nx = fetch(0, nullptr);
-#pragma unroll 1
-    for (int b = 0; b < nb; ++b) {
-        st_blk(ck + (int64_t)b * kDim * kCols, S);
-        const int te = min(L, (b + 1) * kBwdBlock);
-#pragma unroll 1
-        for (int t = b * kBwdBlock; t < te; ++t)
-            fwd_step(S, nullptr, nullptr, nx, t + 1 < L ? t + 1 : -1);
-    }
-    // ---- reverse sweep
-    ld_full(p.d_state ? p.d_state + sbase : nullptr, dS);
-#pragma unroll 1
-    for (int b = nb - 1; b >= 0; --b) {
-        const int tb = b * kBwdBlock, te = min(L, tb + kBwdBlock);
-        __syncthreads();  // this block's stored states are rewritten below
-        ld_blk(ck + (int64_t)b * kDim * kCols, S);
-        nx = fetch(tb, nullptr);
-#pragma unroll 1
-        for (int t = tb; t < te; ++t)
-            fwd_step(S, blk + (int64_t)(t - tb) * kDim * kCols, blk_ur + (t - tb) * 2 * kCols, nx,
-                     t + 1 < te ? t + 1 : -1);
-        // the (u, r) a reverse step fetches were written by this thread in the replay above
-        nx = fetch(te - 1, blk_ur + (te - 1 - tb) * 2 * kCols);
-#pragma unroll 1
-        for (int t = te - 1; t >= tb; --t) {
-            const int64_t row = (t0 + t) * p.H + h;
-            ld_blk(blk + (int64_t)(t - tb) * kDim * kCols, S);  // S' = diag(a_t) S_{t-1}
-            const float k_own = io<TIn>::to_f(nx.k);            // k of row tid
-            const float b_t = stage(nx, true);
-            if (t > tb) nx = fetch(t - 1, blk_ur + (t - 1 - tb) * 2 * kCols);
-            __syncthreads();
-            // dS += q do^T; column partials of k_i dS_ij; u . do over this block's columns
-            {
-                const float4 do4 = reinterpret_cast<const float4*>(s_do)[cq];
-                float4 dup = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int r = 0; r < kRowsPer; ++r) {
-                    const int i = rg + kRowGroups * r;
-                    const float qq = s_q[i], kk = s_k[i];
-                    dS[r].x = fmaf(qq, do4.x, dS[r].x); dS[r].y = fmaf(qq, do4.y, dS[r].y);
-                    dS[r].z = fmaf(qq, do4.z, dS[r].z); dS[r].w = fmaf(qq, do4.w, dS[r].w);
-                    dup.x = fmaf(kk, dS[r].x, dup.x); dup.y = fmaf(kk, dS[r].y, dup.y);
-                    dup.z = fmaf(kk, dS[r].z, dup.z); dup.w = fmaf(kk, dS[r].w, dup.w);
-                }
-                reinterpret_cast<float4*>(s_part[rg])[cq] = dup;
-                if (warp == 0) {  // every lane takes part; lanes past the block's columns add 0
-                    const float ud = warp_sum(lane < kCols ? s_u[lane] * s_do[lane] : 0.f);
-                    if (lane == 0) s_ud = ud;
-                }
-            }
-            __syncthreads();
-            if (warp == 0) {  // du = dS^T k; dv = beta du; dbeta partial = du . r
-                float dr = 0.f;
-                if (lane < kCols) {
-                    float du = 0.f;
-#pragma unroll
-                    for (int w = 0; w < kRowGroups; ++w) du += s_part[w][lane];
-                    s_du[lane] = du;
-                    p.dv[row * kDim + j0 + lane] = b_t * du;
-                    dr = du * s_r[lane];
-                }
-                const float db = warp_sum(dr);  // every lane of warp 0 takes part
-                if (lane == 0) pdb[row] = db;
-            }
-            __syncthreads();
-            const float ud = s_ud;
-            {
-                const float4 du4 = reinterpret_cast<const float4*>(s_du)[cq];
-                const float4 u4 = reinterpret_cast<const float4*>(s_u)[cq];
-                const float4 do4 = reinterpret_cast<const float4*>(s_do)[cq];
-#pragma unroll
-                for (int r = 0; r < kRowsPer; ++r) {
-                    const int i = rg + kRowGroups * r;
-                    // dq_i = (S' do)_i + k_i (u . do); dk_i = (dS u)_i - beta (S' du)_i
-                    s_rp[0][i][cq] = S[r].x * do4.x + S[r].y * do4.y + S[r].z * do4.z + S[r].w * do4.w;
-                    s_rp[1][i][cq] = dS[r].x * u4.x + dS[r].y * u4.y + dS[r].z * u4.z + dS[r].w * u4.w -
-                                     b_t * (S[r].x * du4.x + S[r].y * du4.y + S[r].z * du4.z + S[r].w * du4.w);
-                    // dS' = dS - beta k du^T; dg_i = rowsum(dS' * S'); dS <- diag(a) dS'
-                    const float bk = b_t * s_k[i];
-                    dS[r].x = fmaf(-bk, du4.x, dS[r].x); dS[r].y = fmaf(-bk, du4.y, dS[r].y);
-                    dS[r].z = fmaf(-bk, du4.z, dS[r].z); dS[r].w = fmaf(-bk, du4.w, dS[r].w);
-                    s_rp[2][i][cq] = dS[r].x * S[r].x + dS[r].y * S[r].y + dS[r].z * S[r].z + dS[r].w * S[r].w;
-                    const float a = s_a[i];
-                    dS[r].x *= a; dS[r].y *= a; dS[r].z *= a; dS[r].w *= a;
-                }
-            }
-            __syncthreads();
-            {  // this block's partial row sums for row tid (read before the next token's barrier)
-                float sq = 0.f, sk = 0.f, sg = 0.f;
-#pragma unroll
-                for (int e = 0; e < kLanesPerRow; ++e) {
-                    sq += s_rp[0][tid][e];
-                    sk += s_rp[1][tid][e];
-                    sg += s_rp[2][tid][e];
-                }
-                pdq[row * kDim + tid] = fmaf(k_own, ud, sq);
-                pdk[row * kDim + tid] = sk;
-                pdg[row * kDim + tid] = sg;
-            }
-        }
-    }
-    // d_init: this block's columns of dS after the first token
+    const int64_t gc = blockIdx.x;
+    const int h = blockIdx.y, H = p.H;
+    const int n = find_seq(p.idx, p.N, gc);
+    const int64_t t0 = p.cu[n] + (gc - p.idx[n]) * kBC;
+    const int nt = (int)(p.cu[n + 1] - t0 < kBC ? p.cu[n + 1] - t0 : kBC);
     {
-        float* dst = p.d_init + sbase;
+        const int c = tid;  // key channel
+        float G[kBC], kk[kBC], qq[kBC];
+        float acc = 0.f;
 #pragma unroll
-        for (int r = 0; r < kRowsPer; ++r)
-            reinterpret_cast<float4*>(dst + (rg + kRowGroups * r) * kDim + j0)[cq] = dS[r];
+        for (int i = 0; i < kBC; ++i) {
+            float gv = 0.f, kv = 0.f, qv = 0.f;
+            if (i < nt) {
+                const int64_t e = ((t0 + i) * H + h) * kDim + c;
+                gv = io<TIn>::to_f(p.g[e]);
+                kv = io<TIn>::to_f(p.k[e]);
+                qv = io<TIn>::to_f(p.q[e]);
+            }
+            acc += gv;
+            G[i] = acc;
+            kk[i] = kv;
+            qq[i] = qv;
+        }
+        const float r = 0.5f * G[kBC - 1];
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < kBC; ++i) {
+            const float x = G[i] - r;
+            bad |= !(fabsf(x) <= kMaxExponent);
+            const float ep = expf(x), em = expf(-x);
+            s_kp[swz(i, c)] = tf32r(kk[i] * ep);
+            s_km[swz(i, c)] = tf32r(kk[i] * em);
+            s_qr[swz(i, c)] = tf32r(qq[i] * ep);
+        }
+        if (bad) report_status(p.status, kStatusDecayRange);
+        if (tid < kBC) s_beta[tid] = tid < nt ? io<TIn>::to_f(p.beta[(t0 + tid) * H + h]) : 0.f;
+    }
+    __syncthreads();
+    float* out = p.tiles + (gc * H + h) * (3 * kBC * kBC);
+    {
+        // warps 0, 1: At columns 0-7, 8-15; warps 2, 3: P columns 0-7, 8-15
+        const int g = lane >> 2, t = lane & 3;
+        const float* A = warp < 2 ? s_kp : s_qr;
+        const int n0 = (warp & 1) * 8;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < kDim / 8; ++kk) {
+            uint32_t a[4], b[2];
+            lda_mk(A, 0, 8 * kk, g, t, a);
+            ldb_nk(s_km, n0, 8 * kk, g, t, b);
+            mma8(d, a, b);
+        }
+        const bool strict = warp < 2;
+        float* o = out + (warp < 2 ? 2 : 1) * kBC * kBC;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int row = g + (e >> 1) * 8, col = n0 + 2 * t + (e & 1);
+            const float x = (strict ? col < row : col <= row) ? d[e] : 0.f;
+            o[row * kBC + col] = x;
+            if (strict) s_at[row][col] = x;
+        }
+    }
+    __syncthreads();
+    if (warp == 0 && lane < kBC) {
+        // column j of (I + diag(beta) At)^-1 by forward substitution
+        const int j = lane;
+        float x[kBC];
+#pragma unroll
+        for (int i = 0; i < kBC; ++i) {
+            float acc = i == j ? 1.f : 0.f;
+            float s = 0.f;
+#pragma unroll
+            for (int m = 0; m < i; ++m) s = fmaf(s_at[i][m], x[m], s);
+            x[i] = acc - s_beta[i] * s;
+        }
+#pragma unroll
+        for (int i = 0; i < kBC; ++i) out[i * kBC + j] = x[i];
     }
 }
 
-// dq, dk, dg and dbeta: the sums of the column blocks' partials, in block order.
-__global__ void __launch_bounds__(256) kda_bwd_sum_kernel(const float* __restrict__ part,
-                                                         int64_t TH, float* __restrict__ dq,
-                                                         float* __restrict__ dk,
-                                                         float* __restrict__ dg,
-                                                         float* __restrict__ dbeta) {
-    const int64_t n4 = TH * kDim / 4;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < 3 * n4 + TH; e += stride) {
-        if (e < 3 * n4) {
-            const int which = (int)(e / n4);
-            const int64_t i = e - which * n4;
-            const float4* src = reinterpret_cast<const float4*>(part) + (int64_t)which * kColBlocks * n4 + i;
-            float4 acc = src[0];
+// The forward state chain of one unit: S^T in registers, the start state of every chunk stored.
+template <typename TIn>
+__global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(const BwdArgs<TIn> p) {
+    __shared__ __align__(16) float s_kf[kTile], s_kbar[kTile], s_v[kTile];
+    __shared__ __align__(16) float s_tb[kSmall];
+    __shared__ float s_a[kDim];
+    __shared__ float s_beta[kBC];
+    if (p.idx[p.N + 1]) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int H = p.H;
+    const int n = blockIdx.x / H, h = blockIdx.x - n * H;
+    const int64_t tb = p.cu[n], te = p.cu[n + 1];
+    const int64_t c0 = p.idx[n];
+    const int nch = p.idx[n + 1] - p.idx[n];
+    const int dv0 = 16 * warp;  // value channels of this warp
+    // S^T (value rows dv0.., key columns) as 16 accumulator tiles of 16 x 8
+    float S[kDim / 8][4];
+    {
+        const float* s0 = p.init_state ? p.init_state + ((int64_t)n * H + h) * kState : nullptr;
 #pragma unroll
-            for (int c = 1; c < kColBlocks; ++c) {
-                const float4 x = src[c * n4];
-                acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
+        for (int j = 0; j < kDim / 8; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = dv0 + g + (e >> 1) * 8, col = 8 * j + 2 * t + (e & 1);
+                S[j][e] = s0 ? s0[col * kDim + row] : 0.f;
             }
-            float* o = which == 0 ? dq : which == 1 ? dk : dg;
-            reinterpret_cast<float4*>(o)[i] = acc;
-        } else {
-            const int64_t i = e - 3 * n4;
-            const float* src = part + 3 * kColBlocks * TH * kDim + i;
-            float acc = src[0];
+    }
+    for (int c = 0; c < nch; ++c) {
+        const int64_t slot = (c0 + c) * H + h;
+        const int64_t t0 = tb + (int64_t)c * kBC;
+        const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
+        __syncthreads();
+        if (tid < kDim) {
+            const int ch = tid;
+            float G[kBC], kk[kBC];
+            float acc = 0.f;
 #pragma unroll
-            for (int c = 1; c < kColBlocks; ++c) acc += src[c * TH];
-            dbeta[i] = acc;
+            for (int i = 0; i < kBC; ++i) {
+                float gv = 0.f, kv = 0.f;
+                if (i < nt) {
+                    const int64_t e = ((t0 + i) * H + h) * kDim + ch;
+                    gv = io<TIn>::to_f(p.g[e]);
+                    kv = io<TIn>::to_f(p.k[e]);
+                }
+                acc += gv;
+                G[i] = acc;
+                kk[i] = kv;
+            }
+            const float GC = G[kBC - 1];
+            s_a[ch] = expf(GC);
+#pragma unroll
+            for (int i = 0; i < kBC; ++i) {
+                s_kf[swz(i, ch)] = tf32r(kk[i] * expf(G[i]));
+                s_kbar[swz(i, ch)] = tf32r(kk[i] * expf(GC - G[i]));
+            }
+        } else {
+            const int ch = tid - kDim;
+#pragma unroll
+            for (int i = 0; i < kBC; ++i)
+                s_v[swz(i, ch)] = i < nt ? io<TIn>::to_f(p.v[((t0 + i) * H + h) * kDim + ch]) : 0.f;
+            if (ch < kBC)
+                s_beta[ch] = ch < nt ? io<TIn>::to_f(p.beta[(t0 + ch) * H + h]) : 0.f;
         }
+        __syncthreads();
+        {
+            const float* T = p.tiles + slot * (3 * kBC * kBC);
+            const int i = tid >> 4, s = tid & 15;
+            s_tb[i * kSmallLd + s] = tf32r(T[i * kBC + s] * s_beta[s]);
+        }
+        // the chunk's start state, S^T [value][key]
+        float* dst = p.states + slot * kState;
+#pragma unroll
+        for (int j = 0; j < kDim / 8; ++j) {
+            __stcs(reinterpret_cast<float2*>(dst + (dv0 + g) * kDim + 8 * j + 2 * t),
+                   make_float2(S[j][0], S[j][1]));
+            __stcs(reinterpret_cast<float2*>(dst + (dv0 + g + 8) * kDim + 8 * j + 2 * t),
+                   make_float2(S[j][2], S[j][3]));
+        }
+        // R^T = V^T - S^T K_f^T   (value rows, token columns)
+        float R[2][4];
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                R[jj][e] = s_v[swz(8 * jj + 2 * t + (e & 1), dv0 + g + (e >> 1) * 8)];
+#pragma unroll
+        for (int kk = 0; kk < kDim / 8; ++kk) {
+            const uint32_t a[4] = {neg(tf32_bits(S[kk][0])), neg(tf32_bits(S[kk][2])),
+                                   neg(tf32_bits(S[kk][1])), neg(tf32_bits(S[kk][3]))};
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                uint32_t b[2];
+                ldb_nk(s_kf, 8 * jj, 8 * kk, g, t, b);
+                mma8(R[jj], a, b);
+            }
+        }
+        __syncthreads();  // s_tb complete
+        // U^T = R^T (T diag(beta))^T
+        float U[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            const uint32_t a[4] = {tf32_bits(R[kk][0]), tf32_bits(R[kk][2]), tf32_bits(R[kk][1]),
+                                   tf32_bits(R[kk][3])};
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const float2 v = *reinterpret_cast<const float2*>(
+                    s_tb + (8 * jj + g) * kSmallLd + 8 * kk + 2 * t);
+                const uint32_t b[2] = {bits(v.x), bits(v.y)};
+                mma8(U[jj], a, b);
+            }
+        }
+        // S^T <- S^T diag(a) + U^T K_bar
+#pragma unroll
+        for (int j = 0; j < kDim / 8; ++j) {
+            const float a0 = s_a[8 * j + 2 * t], a1 = s_a[8 * j + 2 * t + 1];
+            S[j][0] *= a0; S[j][1] *= a1; S[j][2] *= a0; S[j][3] *= a1;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            const uint32_t a[4] = {tf32_bits(U[kk][0]), tf32_bits(U[kk][2]), tf32_bits(U[kk][1]),
+                                   tf32_bits(U[kk][3])};
+#pragma unroll
+            for (int j = 0; j < kDim / 8; ++j) {
+                uint32_t b[2];
+                ldb_kn(s_kbar, 8 * kk, 8 * j, g, t, b);
+                mma8(S[j], a, b);
+            }
+        }
+    }
+}
+
+// Shared memory of the reverse kernel, in floats.
+struct RevSmem {
+    static constexpr int E = 0;                       // dE^T [value][key]
+    static constexpr int KF = E + kState;             // K_f      [token][key]
+    static constexpr int KBAR = KF + kTile;           // K_bar    [token][key]
+    static constexpr int QF = KBAR + kTile;           // Q_f      [token][key]
+    static constexpr int W = QF + kTile;              // W        [token][key]
+    static constexpr int KRAW = W + kTile;            // k        [token][key]
+    static constexpr int QRAW = KRAW + kTile;         // q        [token][key]
+    static constexpr int GG = QRAW + kTile;           // G        [token][key]
+    static constexpr int DO = GG + kTile;             // dO       [token][value]
+    static constexpr int RY = DO + kTile;             // V, R, then dY, then dG [token][value|key]
+    static constexpr int UU = RY + kTile;             // U        [token][value]
+    static constexpr int DU = UU + kTile;             // dU       [token][value]
+    static constexpr int T = DU + kTile;              // 16 x 16 tiles
+    static constexpr int P = T + kSmall;
+    static constexpr int AT = P + kSmall;
+    static constexpr int TB = AT + kSmall;
+    static constexpr int DA = TB + kSmall;
+    static constexpr int DP = DA + kSmall;
+    static constexpr int A = DP + kSmall;             // exp(G_C) per key
+    static constexpr int R = A + kDim;                // G_C / 2 per key
+    static constexpr int ES = R + kDim;               // a * rowsum(dE * S) per key
+    static constexpr int CX = ES + kDim;              // sum_t dK_bar K_bar per key
+    static constexpr int BETA = CX + kDim;
+    static constexpr int DBP = BETA + kBC;            // per-warp partial rowsum(dY * R)
+    static constexpr int TOTAL = DBP + 8 * kBC;
+};
+constexpr size_t kRevSmemBytes = RevSmem::TOTAL * sizeof(float);
+
+// The reverse pass of one unit: chunks from last to first, with dE^T (the gradient of the state at
+// the end of the current chunk) in shared memory.
+template <typename TIn>
+__global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(const BwdArgs<TIn> p) {
+    extern __shared__ __align__(16) float sm[];
+    float* sE = sm + RevSmem::E;
+    float* sKf = sm + RevSmem::KF;
+    float* sKbar = sm + RevSmem::KBAR;
+    float* sQf = sm + RevSmem::QF;
+    float* sW = sm + RevSmem::W;
+    float* sK = sm + RevSmem::KRAW;
+    float* sQ = sm + RevSmem::QRAW;
+    float* sG = sm + RevSmem::GG;
+    float* sDO = sm + RevSmem::DO;
+    float* sRY = sm + RevSmem::RY;
+    float* sU = sm + RevSmem::UU;
+    float* sDU = sm + RevSmem::DU;
+    float* sT = sm + RevSmem::T;
+    float* sP = sm + RevSmem::P;
+    float* sAt = sm + RevSmem::AT;
+    float* sTB = sm + RevSmem::TB;
+    float* sDA = sm + RevSmem::DA;
+    float* sDP = sm + RevSmem::DP;
+    float* sA = sm + RevSmem::A;
+    float* sR = sm + RevSmem::R;
+    float* sES = sm + RevSmem::ES;
+    float* sCX = sm + RevSmem::CX;
+    float* sBeta = sm + RevSmem::BETA;
+    float* sDBP = sm + RevSmem::DBP;
+
+    if (p.idx[p.N + 1]) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int H = p.H;
+    const int n = blockIdx.x / H, h = blockIdx.x - n * H;
+    const int64_t tb = p.cu[n], te = p.cu[n + 1];
+    const int64_t c0 = p.idx[n];
+    const int nch = p.idx[n + 1] - p.idx[n];
+    const int64_t ubase = ((int64_t)n * H + h) * kState;
+    const int w16 = 16 * warp;  // this warp's value channels (phases 2, 4a) or key channels (3, 4b)
+
+    // dE^T from the final-state gradient (or zero)
+    for (int e = tid; e < kState; e += kBwdChainThreads) {
+        const int dv = e & (kDim - 1), dk = e >> 7;   // read d_state[dk][dv] coalesced
+        sE[swz(dv, dk)] = p.d_state ? p.d_state[ubase + e] : 0.f;
+    }
+
+    for (int c = nch - 1; c >= 0; --c) {
+        const int64_t slot = (c0 + c) * H + h;
+        const int64_t t0 = tb + (int64_t)c * kBC;
+        const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
+        const float* Sg = p.states + slot * kState;   // S^T at the chunk's start
+        __syncthreads();
+        // ---- phase 1: stage the chunk ----
+        if (tid < kDim) {
+            const int ch = tid;
+            float G[kBC], kk[kBC], qq[kBC];
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < kBC; ++i) {
+                float gv = 0.f, kv = 0.f, qv = 0.f;
+                if (i < nt) {
+                    const int64_t e = ((t0 + i) * H + h) * kDim + ch;
+                    gv = io<TIn>::to_f(p.g[e]);
+                    kv = io<TIn>::to_f(p.k[e]);
+                    qv = io<TIn>::to_f(p.q[e]);
+                }
+                acc += gv;
+                G[i] = acc;
+                kk[i] = kv;
+                qq[i] = qv;
+            }
+            const float GC = G[kBC - 1];
+            sA[ch] = expf(GC);
+            sR[ch] = 0.5f * GC;
+#pragma unroll
+            for (int i = 0; i < kBC; ++i) {
+                const int o = swz(i, ch);
+                const float eg = expf(G[i]);
+                sG[o] = G[i];
+                sK[o] = kk[i];
+                sQ[o] = qq[i];
+                sKf[o] = tf32r(kk[i] * eg);
+                sQf[o] = tf32r(qq[i] * eg);
+                sKbar[o] = tf32r(kk[i] * expf(GC - G[i]));
+            }
+        } else {
+            const int ch = tid - kDim;
+#pragma unroll
+            for (int i = 0; i < kBC; ++i) {
+                const int o = swz(i, ch);
+                const int64_t e = ((t0 + i) * H + h) * kDim + ch;
+                sRY[o] = i < nt ? io<TIn>::to_f(p.v[e]) : 0.f;
+                sDO[o] = i < nt ? tf32r(p.d_out[e]) : 0.f;
+            }
+        }
+        {
+            const float* tl = p.tiles + slot * (3 * kBC * kBC);
+            const int i = tid >> 4, s = tid & 15;
+            sT[i * kSmallLd + s] = tf32r(tl[tid]);
+            sP[i * kSmallLd + s] = tf32r(tl[kBC * kBC + tid]);
+            sAt[i * kSmallLd + s] = tl[2 * kBC * kBC + tid];
+            if (tid < kBC) sBeta[tid] = tid < nt ? io<TIn>::to_f(p.beta[(t0 + tid) * H + h]) : 0.f;
+        }
+        __syncthreads();
+        {
+            const int i = tid >> 4, s = tid & 15;
+            sTB[i * kSmallLd + s] = tf32r(sT[i * kSmallLd + s] * sBeta[s]);
+        }
+        // ---- phase 2 (value channels w16.. of this warp) ----
+        // R = V - K_f S   (token rows, value columns)
+        float R[2][4];
+        {
+            float2 sb[2][kDim / 8];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                for (int kk = 0; kk < kDim / 8; ++kk)
+                    sb[jj][kk] = __ldcs(reinterpret_cast<const float2*>(
+                        Sg + (w16 + 8 * jj + g) * kDim + 8 * kk + 2 * t));
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const float2 lo = *reinterpret_cast<const float2*>(sRY + swz(g, w16 + 8 * jj + 2 * t));
+                const float2 hi = *reinterpret_cast<const float2*>(sRY + swz(g + 8, w16 + 8 * jj + 2 * t));
+                R[jj][0] = lo.x; R[jj][1] = lo.y; R[jj][2] = hi.x; R[jj][3] = hi.y;
+            }
+#pragma unroll
+            for (int kk = 0; kk < kDim / 8; ++kk) {
+                uint32_t a[4];
+                lda_mk(sKf, 0, 8 * kk, g, t, a);
+                a[0] = neg(a[0]); a[1] = neg(a[1]); a[2] = neg(a[2]); a[3] = neg(a[3]);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const uint32_t b[2] = {tf32_bits(sb[jj][kk].x), tf32_bits(sb[jj][kk].y)};
+                    mma8(R[jj], a, b);
+                }
+            }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) st_c(sRY, 0, w16 + 8 * jj, g, t, R[jj]);
+        __syncthreads();  // sTB complete; R of every warp in sRY (only own columns are read)
+        // U = T diag(beta) R
+        {
+            float U[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                uint32_t a[4];
+                lda_small(sTB, 8 * kk, g, t, a);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const uint32_t b[2] = {
+                        tf32_bits(sRY[swz(8 * kk + 2 * t, w16 + 8 * jj + g)]),
+                        tf32_bits(sRY[swz(8 * kk + 2 * t + 1, w16 + 8 * jj + g)])};
+                    mma8(U[jj], a, b);
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                float u[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) u[e] = tf32r(U[jj][e]);
+                st_c(sU, 0, w16 + 8 * jj, g, t, u);
+            }
+        }
+        // dU = K_bar dE + P^T dO
+        {
+            float D[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kk = 0; kk < kDim / 8; ++kk) {
+                uint32_t a[4];
+                lda_mk(sKbar, 0, 8 * kk, g, t, a);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    uint32_t b[2];
+                    const float2 v = *reinterpret_cast<const float2*>(
+                        sE + swz(w16 + 8 * jj + g, 8 * kk + 2 * t));
+                    b[0] = tf32_bits(v.x); b[1] = tf32_bits(v.y);
+                    mma8(D[jj], a, b);
+                }
+            }
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                uint32_t a[4];
+                lda_small_tr(sP, 8 * kk, g, t, a);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    uint32_t b[2];
+                    ldb_kn(sDO, 8 * kk, w16 + 8 * jj, g, t, b);
+                    mma8(D[jj], a, b);
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                float u[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) u[e] = tf32r(D[jj][e]);
+                st_c(sDU, 0, w16 + 8 * jj, g, t, u);
+            }
+        }
+        __syncwarp();
+        // dY = T^T dU; dbeta partial; dv = diag(beta) dY
+        {
+            float Y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                uint32_t a[4];
+                lda_small_tr(sT, 8 * kk, g, t, a);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    uint32_t b[2];
+                    ldb_kn(sDU, 8 * kk, w16 + 8 * jj, g, t, b);
+                    mma8(Y[jj], a, b);
+                }
+            }
+            float pb0 = 0.f, pb1 = 0.f;   // rows g, g + 8
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                pb0 += Y[jj][0] * R[jj][0] + Y[jj][1] * R[jj][1];
+                pb1 += Y[jj][2] * R[jj][2] + Y[jj][3] * R[jj][3];
+            }
+            pb0 += __shfl_xor_sync(0xffffffffu, pb0, 1);
+            pb0 += __shfl_xor_sync(0xffffffffu, pb0, 2);
+            pb1 += __shfl_xor_sync(0xffffffffu, pb1, 1);
+            pb1 += __shfl_xor_sync(0xffffffffu, pb1, 2);
+            if (t == 0) {
+                sDBP[warp * kBC + g] = pb0;
+                sDBP[warp * kBC + g + 8] = pb1;
+            }
+            const float b0 = sBeta[g], b1 = sBeta[g + 8];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int col = w16 + 8 * jj + 2 * t;
+                if (g < nt)
+                    *reinterpret_cast<float2*>(p.dv + ((t0 + g) * H + h) * kDim + col) =
+                        make_float2(b0 * Y[jj][0], b0 * Y[jj][1]);
+                if (g + 8 < nt)
+                    *reinterpret_cast<float2*>(p.dv + ((t0 + g + 8) * H + h) * kDim + col) =
+                        make_float2(b1 * Y[jj][2], b1 * Y[jj][3]);
+            }
+            __syncwarp();   // this warp's reads of R in sRY are done
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                float y[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[e] = tf32r(Y[jj][e]);
+                st_c(sRY, 0, w16 + 8 * jj, g, t, y);
+            }
+        }
+        // W = T diag(beta) K_f   (key columns w16..)
+        {
+            float Wd[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                uint32_t a[4];
+                lda_small(sTB, 8 * kk, g, t, a);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    uint32_t b[2];
+                    ldb_kn(sKf, 8 * kk, w16 + 8 * jj, g, t, b);
+                    mma8(Wd[jj], a, b);
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                float u[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) u[e] = tf32r(Wd[jj][e]);
+                st_c(sW, 0, w16 + 8 * jj, g, t, u);
+            }
+        }
+        __syncthreads();  // dY, U, dU, W of all warps in shared memory
+        // ---- phase 3 (key channels w16.. of this warp) ----
+        float YS[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float QS[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float KB[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+            // S^T rows 8kk+2t, 8kk+2t+1 (value), columns w16 + 8jj + g (key)
+            float es[2] = {0.f, 0.f};
+#pragma unroll 4
+            for (int kk = 0; kk < kDim / 8; ++kk) {
+                float sv[2][2];
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    sv[jj][0] = __ldcs(Sg + (8 * kk + 2 * t) * kDim + w16 + 8 * jj + g);
+                    sv[jj][1] = __ldcs(Sg + (8 * kk + 2 * t + 1) * kDim + w16 + 8 * jj + g);
+                }
+                uint32_t ay[4], ao[4], au[4];
+                lda_mk(sRY, 0, 8 * kk, g, t, ay);
+                lda_mk(sDO, 0, 8 * kk, g, t, ao);
+                lda_mk(sU, 0, 8 * kk, g, t, au);
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const uint32_t b[2] = {tf32_bits(sv[jj][0]), tf32_bits(sv[jj][1])};
+                    mma8(YS[jj], ay, b);
+                    mma8(QS[jj], ao, b);
+                    const float e0 = sE[swz(8 * kk + 2 * t, w16 + 8 * jj + g)];
+                    const float e1 = sE[swz(8 * kk + 2 * t + 1, w16 + 8 * jj + g)];
+                    es[jj] = fmaf(e0, sv[jj][0], fmaf(e1, sv[jj][1], es[jj]));
+                    const uint32_t be[2] = {tf32_bits(e0), tf32_bits(e1)};
+                    mma8(KB[jj], au, be);
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                es[jj] += __shfl_xor_sync(0xffffffffu, es[jj], 1);
+                es[jj] += __shfl_xor_sync(0xffffffffu, es[jj], 2);
+                if (t == 0) sES[w16 + 8 * jj + g] = es[jj];
+            }
+        }
+        // dA = -strict_lower(dY U^T), dP = lower_incl(dO U^T)   (warps 0-3)
+        if (warp < 4) {
+            const float* A = warp < 2 ? sRY : sDO;
+            const int n0 = (warp & 1) * 8;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < kDim / 8; ++kk) {
+                uint32_t a[4], b[2];
+                lda_mk(A, 0, 8 * kk, g, t, a);
+                ldb_nk(sU, n0, 8 * kk, g, t, b);
+                mma8(d, a, b);
+            }
+            float* o = warp < 2 ? sDA : sDP;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = g + (e >> 1) * 8, col = n0 + 2 * t + (e & 1);
+                o[row * kSmallLd + col] =
+                    warp < 2 ? (col < row ? -d[e] : 0.f) : (col <= row ? d[e] : 0.f);
+            }
+        }
+        __syncthreads();  // dA, dP, ES complete; every read of the old dE done
+        // ---- phase 4a: dE^T <- dE^T diag(a) + dO^T Q_f - dU^T W   (value rows w16..) ----
+        {
+            float E[kDim / 8][4];
+#pragma unroll
+            for (int j = 0; j < kDim / 8; ++j) {
+                const float a0 = sA[8 * j + 2 * t], a1 = sA[8 * j + 2 * t + 1];
+                const float2 lo = *reinterpret_cast<const float2*>(sE + swz(w16 + g, 8 * j + 2 * t));
+                const float2 hi = *reinterpret_cast<const float2*>(sE + swz(w16 + g + 8, 8 * j + 2 * t));
+                E[j][0] = lo.x * a0; E[j][1] = lo.y * a1; E[j][2] = hi.x * a0; E[j][3] = hi.y * a1;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                uint32_t ao[4], au[4];
+                lda_km(sDO, w16, 8 * kk, g, t, ao);
+                lda_km(sDU, w16, 8 * kk, g, t, au);
+                au[0] = neg(au[0]); au[1] = neg(au[1]); au[2] = neg(au[2]); au[3] = neg(au[3]);
+#pragma unroll
+                for (int j = 0; j < kDim / 8; ++j) {
+                    uint32_t bq[2], bw[2];
+                    ldb_kn(sQf, 8 * kk, 8 * j, g, t, bq);
+                    ldb_kn(sW, 8 * kk, 8 * j, g, t, bw);
+                    mma8(E[j], ao, bq);
+                    mma8(E[j], au, bw);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kDim / 8; ++j) st_c(sE, w16, 8 * j, g, t, E[j]);
+        }
+        // ---- phase 4b: the chunk's gradients (key channels w16..) ----
+        {
+            float KP[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float KM[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float QR[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const float bg0 = sBeta[g], bg1 = sBeta[g + 8];
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                // A operands: diag(beta) dA, dP (rows t, k = s) and their transposes (rows s, k = t)
+                uint32_t ada[4], adp[4], adat[4], adpt[4];
+                {
+                    const float2 lo = *reinterpret_cast<const float2*>(sDA + g * kSmallLd + 8 * kk + 2 * t);
+                    const float2 hi = *reinterpret_cast<const float2*>(sDA + (g + 8) * kSmallLd + 8 * kk + 2 * t);
+                    ada[0] = tf32_bits(bg0 * lo.x); ada[1] = tf32_bits(bg1 * hi.x);
+                    ada[2] = tf32_bits(bg0 * lo.y); ada[3] = tf32_bits(bg1 * hi.y);
+                }
+                {
+                    const float2 lo = *reinterpret_cast<const float2*>(sDP + g * kSmallLd + 8 * kk + 2 * t);
+                    const float2 hi = *reinterpret_cast<const float2*>(sDP + (g + 8) * kSmallLd + 8 * kk + 2 * t);
+                    adp[0] = tf32_bits(lo.x); adp[1] = tf32_bits(hi.x);
+                    adp[2] = tf32_bits(lo.y); adp[3] = tf32_bits(hi.y);
+                }
+                {
+                    const int r0 = 8 * kk + 2 * t, r1 = r0 + 1;
+                    const float b0 = sBeta[r0], b1 = sBeta[r1];
+                    adat[0] = tf32_bits(b0 * sDA[r0 * kSmallLd + g]);
+                    adat[1] = tf32_bits(b0 * sDA[r0 * kSmallLd + g + 8]);
+                    adat[2] = tf32_bits(b1 * sDA[r1 * kSmallLd + g]);
+                    adat[3] = tf32_bits(b1 * sDA[r1 * kSmallLd + g + 8]);
+                    adpt[0] = tf32_bits(sDP[r0 * kSmallLd + g]);
+                    adpt[1] = tf32_bits(sDP[r0 * kSmallLd + g + 8]);
+                    adpt[2] = tf32_bits(sDP[r1 * kSmallLd + g]);
+                    adpt[3] = tf32_bits(sDP[r1 * kSmallLd + g + 8]);
+                }
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int col = w16 + 8 * jj + g;
+                    const float rr = sR[col];
+                    const int o0 = swz(8 * kk + 2 * t, col), o1 = swz(8 * kk + 2 * t + 1, col);
+                    const float x0 = sG[o0] - rr, x1 = sG[o1] - rr;
+                    const float k0 = sK[o0], k1 = sK[o1];
+                    const float ep0 = expf(x0), ep1 = expf(x1), em0 = expf(-x0), em1 = expf(-x1);
+                    const uint32_t bkm[2] = {tf32_bits(k0 * em0), tf32_bits(k1 * em1)};
+                    const uint32_t bkp[2] = {tf32_bits(k0 * ep0), tf32_bits(k1 * ep1)};
+                    const uint32_t bqr[2] = {tf32_bits(sQ[o0] * ep0), tf32_bits(sQ[o1] * ep1)};
+                    mma8(KP[jj], ada, bkm);
+                    mma8(QR[jj], adp, bkm);
+                    mma8(KM[jj], adat, bkp);
+                    mma8(KM[jj], adpt, bqr);
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = g + (e >> 1) * 8, col = w16 + 8 * jj + 2 * t + (e & 1);
+                    const int o = swz(row, col);
+                    const float Gv = sG[o], kv = sK[o], qv = sQ[o];
+                    const float rr = sR[col], GC = 2.f * rr;
+                    const float eg = expf(Gv), egr = expf(Gv - rr), erg = expf(rr - Gv),
+                                ecg = expf(GC - Gv);
+                    const float dKf = -sBeta[row] * YS[jj][e];
+                    const float kterm = dKf * eg + KP[jj][e] * egr - KM[jj][e] * erg - KB[jj][e] * ecg;
+                    const float qterm = QS[jj][e] * eg + QR[jj][e] * egr;
+                    const float dkv = dKf * eg + KP[jj][e] * egr + KM[jj][e] * erg + KB[jj][e] * ecg;
+                    YS[jj][e] = kv * kterm + qv * qterm;   // dG
+                    QS[jj][e] = qterm;                     // dq
+                    KP[jj][e] = dkv;                       // dk
+                    KB[jj][e] *= kv * ecg;                 // dK_bar * K_bar
+                }
+            }
+            // sum over the chunk's tokens of dK_bar * K_bar, per key column
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                float s0 = KB[jj][0] + KB[jj][2], s1 = KB[jj][1] + KB[jj][3];   // columns 2t, 2t+1
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+                }
+                if (g == 0) {
+                    sCX[w16 + 8 * jj + 2 * t] = s0;
+                    sCX[w16 + 8 * jj + 2 * t + 1] = s1;
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int col = w16 + 8 * jj + 2 * t;
+                if (g < nt) {
+                    const int64_t o = ((t0 + g) * H + h) * kDim + col;
+                    *reinterpret_cast<float2*>(p.dk + o) = make_float2(KP[jj][0], KP[jj][1]);
+                    *reinterpret_cast<float2*>(p.dq + o) = make_float2(QS[jj][0], QS[jj][1]);
+                }
+                if (g + 8 < nt) {
+                    const int64_t o = ((t0 + g + 8) * H + h) * kDim + col;
+                    *reinterpret_cast<float2*>(p.dk + o) = make_float2(KP[jj][2], KP[jj][3]);
+                    *reinterpret_cast<float2*>(p.dq + o) = make_float2(QS[jj][2], QS[jj][3]);
+                }
+                st_c(sRY, 0, w16 + 8 * jj, g, t, YS[jj]);   // dG; dY is no longer read
+            }
+            __syncwarp();
+            if (lane < kBC) {
+                // dg = suffix sum of dG over the chunk (the chunk end also carries the G_C terms)
+                const int col = w16 + lane;
+                float acc = sCX[col] + sA[col] * sES[col];
+                for (int i = kBC - 1; i >= 0; --i) {
+                    acc += sRY[swz(i, col)];
+                    if (i < nt) p.dg[((t0 + i) * H + h) * kDim + col] = acc;
+                }
+            }
+        }
+        if (warp == 7 && lane < kBC && lane < nt) {
+            const int i = lane;
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) acc += sDBP[w * kBC + i];
+#pragma unroll
+            for (int s = 0; s < kBC; ++s) acc = fmaf(sDA[i * kSmallLd + s], sAt[i * kSmallLd + s], acc);
+            p.dbeta[(t0 + i) * H + h] = acc;
+        }
+    }
+    __syncthreads();
+    // the gradient of the initial state, [key][value]
+    for (int e = tid; e < kState; e += kBwdChainThreads) {
+        const int dv = e & (kDim - 1), dk = e >> 7;
+        p.d_init[ubase + e] = sE[swz(dv, dk)];
     }
 }
 
 }  // namespace
+
+size_t backward_workspace_floats(int num_seqs, int heads, int64_t chunks) {
+    const size_t idx_floats = ((size_t)num_seqs + 2 + 63) / 64 * 64;
+    return idx_floats + (size_t)chunks * heads * (3 * kBC * kBC + kState);
+}
+
+int64_t backward_chunks(const int32_t* host_seqlens, int num_seqs) {
+    int64_t c = 0;
+    for (int n = 0; n < num_seqs; ++n) c += ((int64_t)host_seqlens[n] + kBC - 1) / kBC;
+    return c;
+}
 
 cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, const void* k,
                             const void* v, const void* g, const void* beta,
                             const int32_t* cu_seqlens, const float* init_state,
                             const float* d_out, const float* d_state, float* dq, float* dk,
                             float* dv, float* dg, float* dbeta, float* d_init, float* work,
-                            int64_t work_per_unit, int64_t total_tokens, int* status,
+                            int64_t chunks, int64_t total_tokens, int* status,
                             cudaStream_t stream) {
-    const int64_t units = (int64_t)num_seqs * heads;
-    if (units <= 0) return cudaSuccess;
-    // the units' state regions, then the partial sums
-    float* part = work + units * work_per_unit;
-    const int64_t per_cta = work_per_unit / kColBlocks;
-    const unsigned grid = (unsigned)(units * kColBlocks);
-    if (dtype == KDA_BF16) {
-        using T = __nv_bfloat16;
-        const BwdArgs<T> a{(const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta,
-                           cu_seqlens, init_state, d_out, d_state, dv, d_init, part, work,
-                           per_cta, total_tokens, status, heads};
-        kda_bwd_kernel<T><<<grid, kBwdThreads, 0, stream>>>(a);
-    } else {
-        const BwdArgs<float> a{(const float*)q, (const float*)k, (const float*)v, (const float*)g,
-                               (const float*)beta, cu_seqlens, init_state, d_out, d_state, dv,
-                               d_init, part, work, per_cta, total_tokens, status, heads};
-        kda_bwd_kernel<float><<<grid, kBwdThreads, 0, stream>>>(a);
-    }
+    if ((int64_t)num_seqs * heads <= 0) return cudaSuccess;
+    int32_t* idx = reinterpret_cast<int32_t*>(work);
+    const size_t idx_floats = ((size_t)num_seqs + 2 + 63) / 64 * 64;
+    float* tiles = work + idx_floats;
+    float* states = tiles + (size_t)chunks * heads * (3 * kBC * kBC);
+    kda_bwd_index_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, chunks, total_tokens, idx,
+                                                 status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int64_t TH = total_tokens * heads;
-    if (TH > 0) {
-        const int64_t items = 3 * TH * kDim / 4 + TH;
-        const unsigned blocks = (unsigned)std::min<int64_t>((items + 255) / 256, 152 * 16);
-        kda_bwd_sum_kernel<<<blocks, 256, 0, stream>>>(part, TH, dq, dk, dg, dbeta);
-    }
-    return cudaGetLastError();
+    auto run = [&](auto tag) -> cudaError_t {
+        using T = decltype(tag);
+        const BwdArgs<T> a{(const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta,
+                           cu_seqlens, init_state, d_out, d_state, dq, dk, dv, dg, dbeta, d_init,
+                           idx, tiles, states, status, num_seqs, heads};
+        if (chunks > 0) {
+            kda_bwd_prep_kernel<T><<<dim3((unsigned)chunks, (unsigned)heads), kPrepThreads, 0,
+                                     stream>>>(a);
+            cudaError_t err = cudaGetLastError();
+            if (err != cudaSuccess) return err;
+            kda_bwd_forward_kernel<T><<<(unsigned)(num_seqs * heads), kBwdChainThreads, 0,
+                                        stream>>>(a);
+            err = cudaGetLastError();
+            if (err != cudaSuccess) return err;
+        }
+        cudaError_t err = cudaFuncSetAttribute(kda_bwd_reverse_kernel<T>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kRevSmemBytes);
+        if (err != cudaSuccess) return err;
+        kda_bwd_reverse_kernel<T><<<(unsigned)(num_seqs * heads), kBwdChainThreads, kRevSmemBytes,
+                                    stream>>>(a);
+        return cudaGetLastError();
+    };
+    if (dtype == KDA_BF16) return run(__nv_bfloat16{});
+    return run(float{});
 }
 
 }  // namespace kda

@@ -57,12 +57,6 @@ __host__ __device__ __forceinline__ SegPlan segment_plan(int64_t len, int H) {
     return SegPlan{(int)((nc + seg - 1) / seg), (int)seg};
 }
 
-// The backward runs each (sequence, head) unit as kBwdColBlocks CTAs, one per block of value
-// channels; its workspace holds that many partial sums of dq, dk, dlog_alpha and dbeta.  Every
-// CTA lasts its whole sequence, so the count is set for one wave: 4 blocks put the 4 x 8192 x 32
-// workload's 512 CTAs on 152 SMs x 4; 8 blocks (1,024 CTAs at six per SM) need a second wave.
-constexpr int kBwdColBlocks = 4;
-
 // Device status codes written into the sticky status word (same values as kda_status).
 constexpr int kStatusDecayRange = KDA_ERR_DECAY_RANGE;
 constexpr int kStatusTimeout = KDA_ERR_TIMEOUT;
@@ -196,14 +190,18 @@ cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const vo
                             float q_scale, void* q, void* k, void* v, void* g, void* beta,
                             cudaStream_t stream);
 
-// Gradients of the recurrence: one CTA per (sequence, head); work holds work_per_unit floats per
-// unit ((blocks of 16 tokens in the longest sequence + 16) states of 128 x 128).
+// Gradients of the recurrence, chunked by 16 tokens.  `chunks` is the host's chunk total (sum over
+// the sequences of ceil(len / 16)); work holds backward_workspace_floats(num_seqs, heads, chunks)
+// floats: the chunk offsets of the sequences and a stop flag, then per (chunk, head) the 16 x 16
+// tiles T, P and At, then per (chunk, head) the state at the chunk's start.
+size_t backward_workspace_floats(int num_seqs, int heads, int64_t chunks);
+int64_t backward_chunks(const int32_t* host_seqlens, int num_seqs);
 cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, const void* k,
                             const void* v, const void* g, const void* beta,
                             const int32_t* cu_seqlens, const float* init_state,
                             const float* d_out, const float* d_state, float* dq, float* dk,
                             float* dv, float* dg, float* dbeta, float* d_init, float* work,
-                            int64_t work_per_unit, int64_t total_tokens, int* status,
+                            int64_t chunks, int64_t total_tokens, int* status,
                             cudaStream_t stream);
 
 // One CTA whose bounded wait runs out: the status word then reads KDA_ERR_TIMEOUT.

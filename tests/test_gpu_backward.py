@@ -1,7 +1,8 @@
 """GPU parity of the backward pass (gradients of the recurrence) against the fp64 oracle, which
 differentiates the token loop with reverse-mode autograd and is pinned by finite differences of
-the forward oracle.  Sequences cross several 16-token recompute blocks, one is empty, and the
-initial state and the gradient on the final state are each present or absent."""
+the forward oracle.  Sequences cross several 16-token chunks, one is empty, and the initial
+state and the gradient on the final state are each present or absent; gates span the bounded
+gate's whole range, and a chunk that decays beyond the factors' exponent range is reported."""
 import numpy as np
 import pytest
 import torch
@@ -47,8 +48,8 @@ def test_backward_matches_oracle(dtype, with_init, with_dstate):
 
 
 def test_backward_long_sequence():
-    """2048 tokens cross 128 recompute blocks (the state at every 16th token kept, the rest
-    replayed); a second sequence of 17 tokens ends on a one-token block."""
+    """2048 tokens cross 128 chunks of 16 tokens (the state at every chunk start kept); a second
+    sequence of 17 tokens ends on a one-token chunk."""
     lens, H = [2048, 17], 1
     x = synth.make_inputs(lens, H, torch.bfloat16, seed=73, device=DEV)
     gen = torch.Generator(device=DEV).manual_seed(74)
@@ -65,10 +66,55 @@ def test_backward_long_sequence():
         assert_close(name, g.cpu().numpy(), r)
 
 
+def test_backward_bounded_gate_range():
+    """log alpha = -5 sigmoid(2z): the lower-bound gate of "How KDA updates its state" over its
+    whole range (down to -5 per token), ragged lengths, with an initial state and a final-state
+    gradient."""
+    lens, H = [300, 7, 129], 2
+    x = synth.make_inputs(lens, H, torch.bfloat16, seed=77, device=DEV, bounded_gate=-5.0)
+    gen = torch.Generator(device=DEV).manual_seed(78)
+    d_out = torch.randn(sum(lens), H, 128, generator=gen, device=DEV)
+    d_state = torch.randn(len(lens), H, 128, 128, generator=gen, device=DEV) * 0.1
+    got = kda().bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                    x["seqlens"], d_out, init_state=x["init_state"], d_state=d_state)
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    ref = oracle.recurrence_backward(
+        x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), x["log_alpha"].cpu(), x["beta"].cpu(),
+        x["cu_seqlens"].cpu(), d_out.cpu(), state_in=x["init_state"].cpu(), d_state=d_state.cpu())
+    for name, g, r in zip(NAMES, got, ref):
+        assert_close(name, g.cpu().numpy(), r)
+
+
+def test_backward_decay_beyond_the_chunk_range_is_reported():
+    """A 16-token chunk whose decay passes 160 in a channel (here -12 per token) leaves the
+    factors' exponent range: KDA_ERR_DECAY_RANGE, and the next call is still correct."""
+    lens, H = [40], 1
+    x = synth.make_inputs(lens, H, torch.bfloat16, seed=79, device=DEV)
+    la = x["log_alpha"].clone()
+    la[:, :, 5] = -12.0
+    d_out = torch.ones(40, 1, 128, device=DEV)
+    assert kda().read_device_status() == 0
+    kda().bwd(x["q"], x["k"], x["v"], la, x["beta"], x["cu_seqlens"], x["seqlens"], d_out,
+              init_state=x["init_state"])
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == -6
+    got = kda().bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                    x["seqlens"], d_out, init_state=x["init_state"])
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    ref = oracle.recurrence_backward(
+        x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), x["log_alpha"].cpu(), x["beta"].cpu(),
+        x["cu_seqlens"].cpu(), d_out.cpu(), state_in=x["init_state"].cpu())
+    for name, g, r in zip(NAMES, got, ref):
+        assert_close(name, g.cpu().numpy(), r)
+
+
 def test_backward_device_lengths_beyond_the_workspace_are_reported():
-    """The workspace is sized from the host lengths (one state per 16 tokens of the longest
-    sequence); a device cu_seqlens with a longer sequence (same total) would run past its unit's
-    region, so the kernel checks the block count first and reports KDA_ERR_INVALID_ARG."""
+    """The workspace is sized from the host lengths (one record per 16-token chunk); a device
+    cu_seqlens with other lengths and a different chunk total (same token total) would index
+    past it, so the first launch compares the totals, reports KDA_ERR_INVALID_ARG and the later
+    launches compute nothing."""
     host, device = [16, 16], [0, 2, 32]
     x = synth.make_inputs(host, 1, torch.bfloat16, seed=75, device=DEV)
     d_out = torch.ones(32, 1, 128, device=DEV)
