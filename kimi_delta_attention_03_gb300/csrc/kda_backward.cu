@@ -38,6 +38,7 @@
 #include <algorithm>
 
 #include "kda_common.cuh"
+#include "kda_sm100.cuh"
 
 namespace kda {
 namespace {
@@ -47,9 +48,10 @@ constexpr int kBwdChainThreads = 256;
 constexpr int kPrepThreads = 128;
 constexpr int kTile = kBC * kDim;      // floats in a [16][128] tile
 constexpr int kState = kDim * kDim;    // floats in a state
-constexpr int kSmallLd = 24;           // leading dimension of the 16 x 16 tiles in shared memory
+constexpr int kSmallLd = 20;           // leading dimension of the 16 x 16 tiles in shared memory
 constexpr int kSmall = kBC * kSmallLd;
 constexpr float kMaxExponent = 80.f;   // |G - r| bound of the factors
+constexpr long long kBwdWaitLimit = 4000000000LL;   // clock cycles (about 2 s)
 
 __device__ __forceinline__ uint32_t tf32_bits(float x) {
     uint32_t r;
@@ -119,10 +121,32 @@ __device__ __forceinline__ void lda_small_tr(const float* s, int k0, int g, int 
     a[3] = bits(s[(k0 + 2 * t + 1) * kSmallLd + g + 8]);
 }
 
-struct BwdIndex {
-    const int32_t* idx;   // [N + 1] chunk offsets, then the stop flag
-    int N;
-};
+// One channel of a chunk: out[i] = x[(t0 + i) * H + h][ch] for i < nt, zero beyond.  The row
+// index is clamped rather than branched on, so that all 16 loads are in flight together.
+template <typename TIn>
+__device__ __forceinline__ void load_col(const TIn* x, int64_t t0, int nt, int H, int h, int ch,
+                                         float (&out)[kBC]) {
+    TIn raw[kBC];
+#pragma unroll
+    for (int i = 0; i < kBC; ++i) raw[i] = x[((t0 + (i < nt ? i : nt - 1)) * H + h) * kDim + ch];
+#pragma unroll
+    for (int i = 0; i < kBC; ++i) out[i] = i < nt ? io<TIn>::to_f(raw[i]) : 0.f;
+}
+
+// Raw loads of one channel of a chunk, kept unconverted so that they stay in flight until used.
+template <typename TIn>
+__device__ __forceinline__ void load_raw(const TIn* x, int64_t t0, int nt, int H, int h, int ch,
+                                         TIn (&raw)[kBC]) {
+    const TIn* base = x + (t0 * H + h) * kDim + ch;
+    const int64_t stride = (int64_t)H * kDim;
+#pragma unroll
+    for (int i = 0; i < kBC; ++i) raw[i] = base[(i < nt ? i : nt - 1) * stride];
+}
+template <typename TIn>
+__device__ __forceinline__ void convert(const TIn (&raw)[kBC], int nt, float (&out)[kBC]) {
+#pragma unroll
+    for (int i = 0; i < kBC; ++i) out[i] = i < nt ? io<TIn>::to_f(raw[i]) : 0.f;
+}
 
 // Sequence of global chunk gc: the largest n < N with idx[n] <= gc.
 __device__ __forceinline__ int find_seq(const int32_t* idx, int N, int64_t gc) {
@@ -219,21 +243,11 @@ __global__ void __launch_bounds__(kPrepThreads) kda_bwd_prep_kernel(const BwdArg
     {
         const int c = tid;  // key channel
         float G[kBC], kk[kBC], qq[kBC];
-        float acc = 0.f;
+        load_col(p.g, t0, nt, H, h, c, G);
+        load_col(p.k, t0, nt, H, h, c, kk);
+        load_col(p.q, t0, nt, H, h, c, qq);
 #pragma unroll
-        for (int i = 0; i < kBC; ++i) {
-            float gv = 0.f, kv = 0.f, qv = 0.f;
-            if (i < nt) {
-                const int64_t e = ((t0 + i) * H + h) * kDim + c;
-                gv = io<TIn>::to_f(p.g[e]);
-                kv = io<TIn>::to_f(p.k[e]);
-                qv = io<TIn>::to_f(p.q[e]);
-            }
-            acc += gv;
-            G[i] = acc;
-            kk[i] = kv;
-            qq[i] = qv;
-        }
+        for (int i = 1; i < kBC; ++i) G[i] += G[i - 1];
         const float r = 0.5f * G[kBC - 1];
         bool bad = false;
 #pragma unroll
@@ -291,13 +305,32 @@ __global__ void __launch_bounds__(kPrepThreads) kda_bwd_prep_kernel(const BwdArg
     }
 }
 
+// Shared memory of the forward kernel, in floats.
+struct FwdSmem {
+    static constexpr int KF = 0;                   // K_f   [token][key]
+    static constexpr int KBAR = KF + kTile;        // K_bar [token][key]
+    static constexpr int V = KBAR + kTile;         // V     [token][value]
+    static constexpr int TB = V + kTile;           // T diag(beta)
+    static constexpr int A = TB + kSmall;          // exp(G_C) per key
+    static constexpr int ST = A + kDim;            // S^T being stored (swizzled tile)
+    static constexpr int TOTAL = ST + kState;
+};
+constexpr size_t kFwdSmemBytes = FwdSmem::TOTAL * sizeof(float);
+
 // The forward state chain of one unit: S^T in registers, the start state of every chunk stored.
+// Each chunk's inputs are loaded during the previous chunk.  The state, rounded to tf32 (it is
+// only an MMA operand and a factor of one row sum later), leaves through a swizzled shared tile by
+// one 64 KiB bulk asynchronous copy: the workspace holds that tile's image, which the reverse
+// kernel copies back unchanged.
 template <typename TIn>
 __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(const BwdArgs<TIn> p) {
-    __shared__ __align__(16) float s_kf[kTile], s_kbar[kTile], s_v[kTile];
-    __shared__ __align__(16) float s_tb[kSmall];
-    __shared__ float s_a[kDim];
-    __shared__ float s_beta[kBC];
+    extern __shared__ __align__(16) float smf[];
+    float* s_kf = smf + FwdSmem::KF;
+    float* s_kbar = smf + FwdSmem::KBAR;
+    float* s_v = smf + FwdSmem::V;
+    float* s_tb = smf + FwdSmem::TB;
+    float* s_a = smf + FwdSmem::A;
+    float* s_st = smf + FwdSmem::ST;
     if (p.idx[p.N + 1]) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -319,27 +352,37 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(co
                 S[j][e] = s0 ? s0[col * kDim + row] : 0.f;
             }
     }
+    // the next chunk's inputs: warps 0-3 hold g and k of key channel tid, warps 4-7 v of value
+    // channel tid - 128; every thread one element of T and the beta of its column
+    TIn ra[kBC], rb[kBC];
+    float t_el = 0.f, b_col = 0.f;
+    const int s_col = tid & 15;
+    auto issue_inputs = [&](int c) {
+        const int64_t t0 = tb + (int64_t)c * kBC;
+        const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
+        t_el = p.tiles[((c0 + c) * H + h) * (3 * kBC * kBC) + tid];
+        b_col = s_col < nt ? io<TIn>::to_f(p.beta[(t0 + s_col) * H + h]) : 0.f;
+        if (tid < kDim) {
+            load_raw(p.g, t0, nt, H, h, tid, ra);
+            load_raw(p.k, t0, nt, H, h, tid, rb);
+        } else {
+            load_raw(p.v, t0, nt, H, h, tid - kDim, ra);
+        }
+    };
+    if (nch > 0) issue_inputs(0);
     for (int c = 0; c < nch; ++c) {
         const int64_t slot = (c0 + c) * H + h;
         const int64_t t0 = tb + (int64_t)c * kBC;
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncthreads();
         if (tid < kDim) {
             const int ch = tid;
             float G[kBC], kk[kBC];
-            float acc = 0.f;
+            convert(ra, nt, G);
+            convert(rb, nt, kk);
 #pragma unroll
-            for (int i = 0; i < kBC; ++i) {
-                float gv = 0.f, kv = 0.f;
-                if (i < nt) {
-                    const int64_t e = ((t0 + i) * H + h) * kDim + ch;
-                    gv = io<TIn>::to_f(p.g[e]);
-                    kv = io<TIn>::to_f(p.k[e]);
-                }
-                acc += gv;
-                G[i] = acc;
-                kk[i] = kv;
-            }
+            for (int i = 1; i < kBC; ++i) G[i] += G[i - 1];
             const float GC = G[kBC - 1];
             s_a[ch] = expf(GC);
 #pragma unroll
@@ -349,27 +392,28 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(co
             }
         } else {
             const int ch = tid - kDim;
+            float vv[kBC];
+            convert(ra, nt, vv);
 #pragma unroll
-            for (int i = 0; i < kBC; ++i)
-                s_v[swz(i, ch)] = i < nt ? io<TIn>::to_f(p.v[((t0 + i) * H + h) * kDim + ch]) : 0.f;
-            if (ch < kBC)
-                s_beta[ch] = ch < nt ? io<TIn>::to_f(p.beta[(t0 + ch) * H + h]) : 0.f;
+            for (int i = 0; i < kBC; ++i) s_v[swz(i, ch)] = vv[i];
         }
-        __syncthreads();
-        {
-            const float* T = p.tiles + slot * (3 * kBC * kBC);
-            const int i = tid >> 4, s = tid & 15;
-            s_tb[i * kSmallLd + s] = tf32r(T[i * kBC + s] * s_beta[s]);
-        }
-        // the chunk's start state, S^T [value][key]
-        float* dst = p.states + slot * kState;
+        s_tb[(tid >> 4) * kSmallLd + s_col] = tf32r(t_el * b_col);
+        // the chunk's start state S^T [value][key] into the store tile
 #pragma unroll
         for (int j = 0; j < kDim / 8; ++j) {
-            __stcs(reinterpret_cast<float2*>(dst + (dv0 + g) * kDim + 8 * j + 2 * t),
-                   make_float2(S[j][0], S[j][1]));
-            __stcs(reinterpret_cast<float2*>(dst + (dv0 + g + 8) * kDim + 8 * j + 2 * t),
-                   make_float2(S[j][2], S[j][3]));
+            const float st[4] = {tf32r(S[j][0]), tf32r(S[j][1]), tf32r(S[j][2]), tf32r(S[j][3])};
+            st_c(s_st, dv0, 8 * j, g, t, st);
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (tid == 0) {
+            asm volatile(
+                "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
+                "cp.async.bulk.commit_group;" ::"l"(p.states + slot * kState),
+                "r"(smem_u32(s_st)), "n"(kState * 4)
+                : "memory");
+        }
+        if (c + 1 < nch) issue_inputs(c + 1);
         // R^T = V^T - S^T K_f^T   (value rows, token columns)
         float R[2][4];
 #pragma unroll
@@ -388,7 +432,6 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(co
                 mma8(R[jj], a, b);
             }
         }
-        __syncthreads();  // s_tb complete
         // U^T = R^T (T diag(beta))^T
         float U[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -421,6 +464,8 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(co
             }
         }
     }
+    // the store must have completed before the CTA's shared memory is released
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Shared memory of the reverse kernel, in floats.
@@ -449,7 +494,9 @@ struct RevSmem {
     static constexpr int CX = ES + kDim;              // sum_t dK_bar K_bar per key
     static constexpr int BETA = CX + kDim;
     static constexpr int DBP = BETA + kBC;            // per-warp partial rowsum(dY * R)
-    static constexpr int TOTAL = DBP + 8 * kBC;
+    static constexpr int SS = DBP + 8 * kBC;          // S^T [value][key] of the chunk (swizzled)
+    static constexpr int BAR = SS + kState;           // mbarrier of the state's bulk copy
+    static constexpr int TOTAL = BAR + 2;
 };
 constexpr size_t kRevSmemBytes = RevSmem::TOTAL * sizeof(float);
 
@@ -500,31 +547,74 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
         sE[swz(dv, dk)] = p.d_state ? p.d_state[ubase + e] : 0.f;
     }
 
-    for (int c = nch - 1; c >= 0; --c) {
+    // the chunk's start state S^T (the forward kernel's swizzled tile image) into shared memory,
+    // one 64 KiB bulk copy completing on an mbarrier
+    float* sS = sm + RevSmem::SS;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + RevSmem::BAR);
+    uint32_t phase = 0;
+    if (tid == 0) {
+        sm100::mbar_init(bar, 1);
+        sm100::mbar_init_fence();
+    }
+    __syncthreads();
+    auto issue_state = [&](int c) {
+        if (tid == 0) {
+            sm100::mbar_arrive_expect_tx(bar, kState * 4);
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+                "[%3];" ::"r"(smem_u32(sS)),
+                "l"(p.states + ((c0 + c) * H + h) * kState), "n"(kState * 4), "r"(smem_u32(bar))
+                : "memory");
+        }
+    };
+    // the next chunk's inputs, loaded a chunk ahead and converted when staged: warps 0-3 hold
+    // g, k, q of key channel tid; warps 4-7 hold v and dO of value channel tid - 128
+    TIn ra[kBC], rb[kBC], rc[kBC];
+    float rd[kBC];
+    float t_el = 0.f, p_el = 0.f, at_el = 0.f, b_el = 0.f;
+    auto issue_inputs = [&](int c) {
         const int64_t slot = (c0 + c) * H + h;
         const int64_t t0 = tb + (int64_t)c * kBC;
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
-        const float* Sg = p.states + slot * kState;   // S^T at the chunk's start
+        const float* tl = p.tiles + slot * (3 * kBC * kBC);
+        t_el = tl[tid];
+        p_el = tl[kBC * kBC + tid];
+        at_el = tl[2 * kBC * kBC + tid];
+        if (tid < kBC) b_el = tid < nt ? io<TIn>::to_f(p.beta[(t0 + tid) * H + h]) : 0.f;
+        if (tid < kDim) {
+            load_raw(p.g, t0, nt, H, h, tid, ra);
+            load_raw(p.k, t0, nt, H, h, tid, rb);
+            load_raw(p.q, t0, nt, H, h, tid, rc);
+        } else {
+            load_raw(p.v, t0, nt, H, h, tid - kDim, ra);
+            load_raw(p.d_out, t0, nt, H, h, tid - kDim, rd);
+        }
+    };
+    if (nch > 0) {
+        issue_state(nch - 1);
+        issue_inputs(nch - 1);
+    }
+
+    for (int c = nch - 1; c >= 0; --c) {
+        const int64_t t0 = tb + (int64_t)c * kBC;
+        const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
         __syncthreads();
         // ---- phase 1: stage the chunk ----
+        {
+            const int i = tid >> 4, s = tid & 15;
+            sT[i * kSmallLd + s] = tf32r(t_el);
+            sP[i * kSmallLd + s] = tf32r(p_el);
+            sAt[i * kSmallLd + s] = at_el;
+            if (tid < kBC) sBeta[tid] = b_el;
+        }
         if (tid < kDim) {
             const int ch = tid;
             float G[kBC], kk[kBC], qq[kBC];
-            float acc = 0.f;
+            convert(ra, nt, G);
+            convert(rb, nt, kk);
+            convert(rc, nt, qq);
 #pragma unroll
-            for (int i = 0; i < kBC; ++i) {
-                float gv = 0.f, kv = 0.f, qv = 0.f;
-                if (i < nt) {
-                    const int64_t e = ((t0 + i) * H + h) * kDim + ch;
-                    gv = io<TIn>::to_f(p.g[e]);
-                    kv = io<TIn>::to_f(p.k[e]);
-                    qv = io<TIn>::to_f(p.q[e]);
-                }
-                acc += gv;
-                G[i] = acc;
-                kk[i] = kv;
-                qq[i] = qv;
-            }
+            for (int i = 1; i < kBC; ++i) G[i] += G[i - 1];
             const float GC = G[kBC - 1];
             sA[ch] = expf(GC);
             sR[ch] = 0.5f * GC;
@@ -541,23 +631,25 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
             }
         } else {
             const int ch = tid - kDim;
+            float vv[kBC];
+            convert(ra, nt, vv);
 #pragma unroll
             for (int i = 0; i < kBC; ++i) {
                 const int o = swz(i, ch);
-                const int64_t e = ((t0 + i) * H + h) * kDim + ch;
-                sRY[o] = i < nt ? io<TIn>::to_f(p.v[e]) : 0.f;
-                sDO[o] = i < nt ? tf32r(p.d_out[e]) : 0.f;
+                sRY[o] = vv[i];
+                sDO[o] = i < nt ? tf32r(rd[i]) : 0.f;
             }
         }
-        {
-            const float* tl = p.tiles + slot * (3 * kBC * kBC);
-            const int i = tid >> 4, s = tid & 15;
-            sT[i * kSmallLd + s] = tf32r(tl[tid]);
-            sP[i * kSmallLd + s] = tf32r(tl[kBC * kBC + tid]);
-            sAt[i * kSmallLd + s] = tl[2 * kBC * kBC + tid];
-            if (tid < kBC) sBeta[tid] = tid < nt ? io<TIn>::to_f(p.beta[(t0 + tid) * H + h]) : 0.f;
+        // the state's copy; a wait that gives up stops the unit (status KDA_ERR_TIMEOUT)
+        const bool arrived = sm100::mbar_wait(bar, phase, kBwdWaitLimit);
+        phase ^= 1u;
+        if (__syncthreads_or(!arrived)) {
+            if (tid == 0) {
+                report_status(p.status, kStatusTimeout);
+                sm100::mbar_wait(bar, phase ^ 1u, kBwdWaitLimit);
+            }
+            return;
         }
-        __syncthreads();
         {
             const int i = tid >> 4, s = tid & 15;
             sTB[i * kSmallLd + s] = tf32r(sT[i * kSmallLd + s] * sBeta[s]);
@@ -566,13 +658,6 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
         // R = V - K_f S   (token rows, value columns)
         float R[2][4];
         {
-            float2 sb[2][kDim / 8];
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-                for (int kk = 0; kk < kDim / 8; ++kk)
-                    sb[jj][kk] = __ldcs(reinterpret_cast<const float2*>(
-                        Sg + (w16 + 8 * jj + g) * kDim + 8 * kk + 2 * t));
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
                 const float2 lo = *reinterpret_cast<const float2*>(sRY + swz(g, w16 + 8 * jj + 2 * t));
@@ -586,7 +671,8 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
                 a[0] = neg(a[0]); a[1] = neg(a[1]); a[2] = neg(a[2]); a[3] = neg(a[3]);
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
-                    const uint32_t b[2] = {tf32_bits(sb[jj][kk].x), tf32_bits(sb[jj][kk].y)};
+                    uint32_t b[2];
+                    ldb_nk(sS, w16 + 8 * jj, 8 * kk, g, t, b);
                     mma8(R[jj], a, b);
                 }
             }
@@ -736,8 +822,8 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
                 float sv[2][2];
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
-                    sv[jj][0] = __ldcs(Sg + (8 * kk + 2 * t) * kDim + w16 + 8 * jj + g);
-                    sv[jj][1] = __ldcs(Sg + (8 * kk + 2 * t + 1) * kDim + w16 + 8 * jj + g);
+                    sv[jj][0] = sS[swz(8 * kk + 2 * t, w16 + 8 * jj + g)];
+                    sv[jj][1] = sS[swz(8 * kk + 2 * t + 1, w16 + 8 * jj + g)];
                 }
                 uint32_t ay[4], ao[4], au[4];
                 lda_mk(sRY, 0, 8 * kk, g, t, ay);
@@ -745,7 +831,7 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
                 lda_mk(sU, 0, 8 * kk, g, t, au);
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
-                    const uint32_t b[2] = {tf32_bits(sv[jj][0]), tf32_bits(sv[jj][1])};
+                    const uint32_t b[2] = {bits(sv[jj][0]), bits(sv[jj][1])};
                     mma8(YS[jj], ay, b);
                     mma8(QS[jj], ao, b);
                     const float e0 = sE[swz(8 * kk + 2 * t, w16 + 8 * jj + g)];
@@ -782,7 +868,11 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
                     warp < 2 ? (col < row ? -d[e] : 0.f) : (col <= row ? d[e] : 0.f);
             }
         }
-        __syncthreads();  // dA, dP, ES complete; every read of the old dE done
+        __syncthreads();  // dA, dP, ES complete; every read of the old dE and of S done
+        if (c > 0) {
+            issue_state(c - 1);
+            issue_inputs(c - 1);
+        }
         // ---- phase 4a: dE^T <- dE^T diag(a) + dO^T Q_f - dU^T W   (value rows w16..) ----
         {
             float E[kDim / 8][4];
@@ -979,8 +1069,12 @@ cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, c
                                      stream>>>(a);
             cudaError_t err = cudaGetLastError();
             if (err != cudaSuccess) return err;
-            kda_bwd_forward_kernel<T><<<(unsigned)(num_seqs * heads), kBwdChainThreads, 0,
-                                        stream>>>(a);
+            err = cudaFuncSetAttribute(kda_bwd_forward_kernel<T>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kFwdSmemBytes);
+            if (err != cudaSuccess) return err;
+            kda_bwd_forward_kernel<T><<<(unsigned)(num_seqs * heads), kBwdChainThreads,
+                                        kFwdSmemBytes, stream>>>(a);
             err = cudaGetLastError();
             if (err != cudaSuccess) return err;
         }
