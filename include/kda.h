@@ -432,27 +432,30 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
  * For the forward of kda_fwd_chunked (the token loop of "How Kimi K3 Engineered Its Way to the
  * Frontier", section "How KDA updates its state") and the gradient d_out of a loss with respect to
  * every output (and optionally d_state with respect to the final states), returns the gradients
- * with respect to q, k, v, log_alpha, beta and the initial states.  Reverse mode through the token
- * loop on CUDA cores, fp32, with the states recomputed from every 16th one kept in the workspace:
- * correct for any gate the forward accepts (no chunk exponent range applies), not tuned for speed.
+ * with respect to q, k, v, log_alpha, beta and the initial states.  Chunked by 16 tokens (the
+ * pages' state step, "FlashKDA steps the state once per 16 tokens"), on tensor cores (tf32
+ * operands, fp32 accumulation): a forward pass stores the state at every chunk start, a reverse
+ * pass carries the gradient of the state backwards and computes each chunk's gradients.
+ * Domain: in every 16-token chunk, every key channel decays by at most 160 (a mean log_alpha of
+ * -10 per token, twice the bounded gate's floor of -5); a chunk beyond that sets
+ * KDA_ERR_DECAY_RANGE in the device status word and its gradients are then unspecified.
  *
  *   desc          as for kda_fwd_chunked (host_seqlens required); q, k, v, log_alpha, beta of
- *                 desc->in_dtype, layouts as there
+ *                 desc->in_dtype, layouts as there; q, k, v, log_alpha 16-byte aligned
  *   init_state    device fp32 [N, H, 128, 128] or NULL (zeros)
  *   d_out         device fp32 [T, H, 128]
  *   d_state       device fp32 [N, H, 128, 128] or NULL (no loss on the final states)
  *   dq, dk, dv, dlog_alpha   device fp32 [T, H, 128]; dbeta device fp32 [T, H];
  *   dinit_state   device fp32 [N, H, 128, 128]
- *   workspace     device, at least kda_bwd_workspace_bytes(desc) bytes, 16-byte aligned:
- *                 per (sequence, head), fp32, one state per 16 tokens of the longest sequence,
- *                 16 states of the block being reversed and 16 pairs of 128-vectors (u, r);
- *                 then four partial sums (one per block of 32 value channels) of dq, dk,
- *                 dlog_alpha and dbeta per token and head; contents on return are unspecified
- * The gradients are deterministic: the partial sums are added in a fixed order.  A unit whose
- * device cu_seqlens disagree with the host lengths (KDA_ERR_INVALID_ARG in the device status
- * word) computes nothing, and its rows of dq, dk, dlog_alpha and dbeta are then unspecified.
- * Outputs must not alias inputs or each other.  Argument, alignment and workspace errors return
- * KDA_ERR_INVALID_ARG / KDA_ERR_WORKSPACE before anything is launched.
+ *   workspace     device, at least kda_bwd_workspace_bytes(desc) bytes, 16-byte aligned: the
+ *                 sequences' chunk offsets, then per 16-token chunk and head three 16 x 16 fp32
+ *                 tiles and the chunk's start state (128 x 128 fp32); contents on return are
+ *                 unspecified
+ * The gradients are deterministic (no atomics; every sum runs in a fixed order).  If the device
+ * cu_seqlens disagree with the host lengths in their chunk total or run past T, the first launch
+ * sets KDA_ERR_INVALID_ARG in the device status word, nothing else is computed and every output
+ * is unspecified.  Outputs must not alias inputs or each other.  Argument, alignment and
+ * workspace errors return KDA_ERR_INVALID_ARG / KDA_ERR_WORKSPACE before anything is launched.
  */
 size_t kda_bwd_workspace_bytes(const kda_desc* desc);
 kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const void* v,

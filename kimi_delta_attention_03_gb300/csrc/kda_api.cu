@@ -435,6 +435,9 @@ kda_status kda_bwd(const kda_desc* desc, const void* q, const void* k, const voi
     }
     if (!aligned16(init_state) || !aligned16(d_state) || !aligned16(d_out))
         return KDA_ERR_INVALID_ARG;
+    // rows are read four channels at a time
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha))
+        return KDA_ERR_INVALID_ARG;
     const size_t need = kda_bwd_workspace_bytes(desc);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KDA_ERR_WORKSPACE;
     int* status = status_word();

@@ -148,6 +148,46 @@ __device__ __forceinline__ void convert(const TIn (&raw)[kBC], int nt, float (&o
     for (int i = 0; i < kBC; ++i) out[i] = i < nt ? io<TIn>::to_f(raw[i]) : 0.f;
 }
 
+// Four consecutive channels of one row: their raw bits (8 bytes of bf16, 16 of fp32) and fp32.
+template <typename TIn> struct Vec4;
+template <> struct Vec4<__nv_bfloat16> {
+    using T = uint2;
+    static __device__ __forceinline__ float4 unpack(uint2 v) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+};
+template <> struct Vec4<float> {
+    using T = uint4;
+    static __device__ __forceinline__ float4 unpack(uint4 v) {
+        return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                           __uint_as_float(v.w));
+    }
+};
+// Rows t0 .. t0 + 15 (the last valid row repeated past nt) of channels 4 lane .. 4 lane + 3.
+template <typename TIn>
+__device__ __forceinline__ void load_rows4(const TIn* x, int64_t t0, int nt, int H, int h,
+                                           int lane, typename Vec4<TIn>::T (&raw)[kBC]) {
+    const TIn* base = x + (t0 * H + h) * kDim + 4 * lane;
+    const int64_t stride = (int64_t)H * kDim;
+#pragma unroll
+    for (int i = 0; i < kBC; ++i)
+        raw[i] = *reinterpret_cast<const typename Vec4<TIn>::T*>(base + (i < nt ? i : nt - 1) * stride);
+}
+__device__ __forceinline__ float4 ld4(const float* s, int r, int c) {
+    return *reinterpret_cast<const float4*>(s + swz(r, c));
+}
+__device__ __forceinline__ void st4(float* s, int r, int c, float4 v) {
+    *reinterpret_cast<float4*>(s + swz(r, c)) = v;
+}
+__device__ __forceinline__ float4 tf32r4(float4 v) {
+    return make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
+}
+__device__ __forceinline__ float4 zero_if(bool z, float4 v) {
+    return z ? make_float4(0.f, 0.f, 0.f, 0.f) : v;
+}
+
 // Sequence of global chunk gc: the largest n < N with idx[n] <= gc.
 __device__ __forceinline__ int find_seq(const int32_t* idx, int N, int64_t gc) {
     int lo = 0, hi = N;
@@ -310,9 +350,13 @@ struct FwdSmem {
     static constexpr int KF = 0;                   // K_f   [token][key]
     static constexpr int KBAR = KF + kTile;        // K_bar [token][key]
     static constexpr int V = KBAR + kTile;         // V     [token][value]
-    static constexpr int TB = V + kTile;           // T diag(beta)
-    static constexpr int A = TB + kSmall;          // exp(G_C) per key
-    static constexpr int ST = A + kDim;            // S^T being stored (swizzled tile)
+    static constexpr int GG = V + kTile;           // G     [token][key]
+    static constexpr int KRAW = GG + kTile;        // k     [token][key]
+    static constexpr int TB = KRAW + kTile;        // T diag(beta)
+    static constexpr int T = TB + kSmall;          // T
+    static constexpr int A = T + kSmall;           // exp(G_C) per key
+    static constexpr int BETA = A + kDim;
+    static constexpr int ST = BETA + kBC;          // S^T being stored (swizzled tile)
     static constexpr int TOTAL = ST + kState;
 };
 constexpr size_t kFwdSmemBytes = FwdSmem::TOTAL * sizeof(float);
@@ -352,21 +396,26 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(co
                 S[j][e] = s0 ? s0[col * kDim + row] : 0.f;
             }
     }
-    // the next chunk's inputs: warps 0-3 hold g and k of key channel tid, warps 4-7 v of value
-    // channel tid - 128; every thread one element of T and the beta of its column
-    TIn ra[kBC], rb[kBC];
-    float t_el = 0.f, b_col = 0.f;
-    const int s_col = tid & 15;
+    // the next chunk's inputs, loaded a chunk ahead as raw bits (lane l: channels 4l..4l+3):
+    // warp 0 g, warp 1 k, warp 2 v (16 rows each); warp 3 the tile T (two float4 a lane) and beta
+    float* s_G = smf + FwdSmem::GG;
+    float* s_K = smf + FwdSmem::KRAW;
+    float* s_T = smf + FwdSmem::T;
+    float* s_beta = smf + FwdSmem::BETA;
+    using V4 = typename Vec4<TIn>::T;
+    V4 rin[kBC];
+    float4 rt[2];
+    float rbeta = 0.f;
     auto issue_inputs = [&](int c) {
         const int64_t t0 = tb + (int64_t)c * kBC;
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
-        t_el = p.tiles[((c0 + c) * H + h) * (3 * kBC * kBC) + tid];
-        b_col = s_col < nt ? io<TIn>::to_f(p.beta[(t0 + s_col) * H + h]) : 0.f;
-        if (tid < kDim) {
-            load_raw(p.g, t0, nt, H, h, tid, ra);
-            load_raw(p.k, t0, nt, H, h, tid, rb);
-        } else {
-            load_raw(p.v, t0, nt, H, h, tid - kDim, ra);
+        if (warp < 3) {
+            load_rows4(warp == 0 ? p.g : warp == 1 ? p.k : p.v, t0, nt, H, h, lane, rin);
+        } else if (warp == 3) {
+            const float* tl = p.tiles + ((c0 + c) * H + h) * (3 * kBC * kBC);
+            rt[0] = *reinterpret_cast<const float4*>(tl + 4 * lane);
+            rt[1] = *reinterpret_cast<const float4*>(tl + 4 * lane + 128);
+            rbeta = lane < nt && lane < kBC ? io<TIn>::to_f(p.beta[(t0 + lane) * H + h]) : 0.f;
         }
     };
     if (nch > 0) issue_inputs(0);
@@ -376,28 +425,29 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(co
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
         if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncthreads();
-        if (tid < kDim) {
-            const int ch = tid;
-            float G[kBC], kk[kBC];
-            convert(ra, nt, G);
-            convert(rb, nt, kk);
-#pragma unroll
-            for (int i = 1; i < kBC; ++i) G[i] += G[i - 1];
-            const float GC = G[kBC - 1];
-            s_a[ch] = expf(GC);
+        if (warp == 0) {
+            float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < kBC; ++i) {
-                s_kf[swz(i, ch)] = tf32r(kk[i] * expf(G[i]));
-                s_kbar[swz(i, ch)] = tf32r(kk[i] * expf(GC - G[i]));
+                const float4 x = zero_if(i >= nt, Vec4<TIn>::unpack(rin[i]));
+                G.x += x.x; G.y += x.y; G.z += x.z; G.w += x.w;
+                st4(s_G, i, 4 * lane, G);
             }
-        } else {
-            const int ch = tid - kDim;
-            float vv[kBC];
-            convert(ra, nt, vv);
+            *reinterpret_cast<float4*>(s_a + 4 * lane) =
+                make_float4(expf(G.x), expf(G.y), expf(G.z), expf(G.w));
+        } else if (warp < 3) {
+            float* dst = warp == 1 ? s_K : s_v;
 #pragma unroll
-            for (int i = 0; i < kBC; ++i) s_v[swz(i, ch)] = vv[i];
+            for (int i = 0; i < kBC; ++i)
+                st4(dst, i, 4 * lane, zero_if(i >= nt, Vec4<TIn>::unpack(rin[i])));
+        } else if (warp == 3) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int e = 4 * lane + 128 * m;
+                *reinterpret_cast<float4*>(s_T + (e >> 4) * kSmallLd + (e & 15)) = rt[m];
+            }
+            if (lane < kBC) s_beta[lane] = rbeta;
         }
-        s_tb[(tid >> 4) * kSmallLd + s_col] = tf32r(t_el * b_col);
         // the chunk's start state S^T [value][key] into the store tile
 #pragma unroll
         for (int j = 0; j < kDim / 8; ++j) {
@@ -413,6 +463,23 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(co
                 "r"(smem_u32(s_st)), "n"(kState * 4)
                 : "memory");
         }
+        {
+            // K_f = k e^G, K_bar = k e^(G_C - G): row tid >> 4, channels 4 (tid & 15) + 64 m
+            const int i = tid >> 4;
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int cb = 4 * (tid & 15) + 64 * m;
+                const float4 G = ld4(s_G, i, cb), k4 = ld4(s_K, i, cb);
+                const float4 GC = ld4(s_G, kBC - 1, cb);
+                st4(s_kf, i, cb, tf32r4(make_float4(k4.x * expf(G.x), k4.y * expf(G.y),
+                                                    k4.z * expf(G.z), k4.w * expf(G.w))));
+                st4(s_kbar, i, cb, tf32r4(make_float4(k4.x * expf(GC.x - G.x), k4.y * expf(GC.y - G.y),
+                                                      k4.z * expf(GC.z - G.z), k4.w * expf(GC.w - G.w))));
+            }
+            const int sc = tid & 15;
+            s_tb[i * kSmallLd + sc] = tf32r(s_T[i * kSmallLd + sc] * s_beta[sc]);
+        }
+        __syncthreads();
         if (c + 1 < nch) issue_inputs(c + 1);
         // R^T = V^T - S^T K_f^T   (value rows, token columns)
         float R[2][4];
@@ -567,27 +634,35 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
                 : "memory");
         }
     };
-    // the next chunk's inputs, loaded a chunk ahead and converted when staged: warps 0-3 hold
-    // g, k, q of key channel tid; warps 4-7 hold v and dO of value channel tid - 128
-    TIn ra[kBC], rb[kBC], rc[kBC];
-    float rd[kBC];
-    float t_el = 0.f, p_el = 0.f, at_el = 0.f, b_el = 0.f;
+    // the next chunk's inputs, loaded a chunk ahead as raw bits (lane l: channels 4l..4l+3):
+    // warps 0-3 g, k, q, v (16 rows each); warps 4, 5 dO rows 0-7, 8-15; warp 6 the tiles T, P,
+    // At (six float4 a lane); warp 7 beta
+    using V4 = typename Vec4<TIn>::T;
+    V4 rin[kBC];
+    float4 rf[8];
+    float rbeta = 0.f;
     auto issue_inputs = [&](int c) {
-        const int64_t slot = (c0 + c) * H + h;
         const int64_t t0 = tb + (int64_t)c * kBC;
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
-        const float* tl = p.tiles + slot * (3 * kBC * kBC);
-        t_el = tl[tid];
-        p_el = tl[kBC * kBC + tid];
-        at_el = tl[2 * kBC * kBC + tid];
-        if (tid < kBC) b_el = tid < nt ? io<TIn>::to_f(p.beta[(t0 + tid) * H + h]) : 0.f;
-        if (tid < kDim) {
-            load_raw(p.g, t0, nt, H, h, tid, ra);
-            load_raw(p.k, t0, nt, H, h, tid, rb);
-            load_raw(p.q, t0, nt, H, h, tid, rc);
+        if (warp < 4) {
+            load_rows4(warp == 0 ? p.g : warp == 1 ? p.k : warp == 2 ? p.q : p.v, t0, nt, H, h,
+                       lane, rin);
+        } else if (warp < 6) {
+            const float* base = p.d_out + (t0 * H + h) * kDim + 4 * lane;
+            const int64_t stride = (int64_t)H * kDim;
+            const int r0 = (warp - 4) * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int row = r0 + i;
+                rf[i] = *reinterpret_cast<const float4*>(base + (row < nt ? row : nt - 1) * stride);
+            }
+        } else if (warp == 6) {
+            const float* tl = p.tiles + ((c0 + c) * H + h) * (3 * kBC * kBC);
+#pragma unroll
+            for (int m = 0; m < 6; ++m)
+                rf[m] = *reinterpret_cast<const float4*>(tl + 4 * (lane + 32 * m));
         } else {
-            load_raw(p.v, t0, nt, H, h, tid - kDim, ra);
-            load_raw(p.d_out, t0, nt, H, h, tid - kDim, rd);
+            rbeta = lane < nt && lane < kBC ? io<TIn>::to_f(p.beta[(t0 + lane) * H + h]) : 0.f;
         }
     };
     if (nch > 0) {
@@ -600,45 +675,56 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
         __syncthreads();
         // ---- phase 1: stage the chunk ----
-        {
-            const int i = tid >> 4, s = tid & 15;
-            sT[i * kSmallLd + s] = tf32r(t_el);
-            sP[i * kSmallLd + s] = tf32r(p_el);
-            sAt[i * kSmallLd + s] = at_el;
-            if (tid < kBC) sBeta[tid] = b_el;
+        if (warp == 0) {
+            float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < kBC; ++i) {
+                const float4 x = zero_if(i >= nt, Vec4<TIn>::unpack(rin[i]));
+                G.x += x.x; G.y += x.y; G.z += x.z; G.w += x.w;
+                st4(sG, i, 4 * lane, G);
+            }
+            *reinterpret_cast<float4*>(sA + 4 * lane) =
+                make_float4(expf(G.x), expf(G.y), expf(G.z), expf(G.w));
+            *reinterpret_cast<float4*>(sR + 4 * lane) =
+                make_float4(0.5f * G.x, 0.5f * G.y, 0.5f * G.z, 0.5f * G.w);
+        } else if (warp < 4) {
+            float* dst = warp == 1 ? sK : warp == 2 ? sQ : sRY;
+#pragma unroll
+            for (int i = 0; i < kBC; ++i)
+                st4(dst, i, 4 * lane, zero_if(i >= nt, Vec4<TIn>::unpack(rin[i])));
+        } else if (warp < 6) {
+            const int r0 = (warp - 4) * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                st4(sDO, r0 + i, 4 * lane, zero_if(r0 + i >= nt, tf32r4(rf[i])));
+        } else if (warp == 6) {
+#pragma unroll
+            for (int m = 0; m < 6; ++m) {
+                const int e = 4 * (lane + 32 * m), tile = e >> 8, r = (e & 255) >> 4, cc = e & 15;
+                float* dst = (tile == 0 ? sT : tile == 1 ? sP : sAt) + r * kSmallLd + cc;
+                *reinterpret_cast<float4*>(dst) = tile == 2 ? rf[m] : tf32r4(rf[m]);
+            }
+        } else if (lane < kBC) {
+            sBeta[lane] = rbeta;
         }
-        if (tid < kDim) {
-            const int ch = tid;
-            float G[kBC], kk[kBC], qq[kBC];
-            convert(ra, nt, G);
-            convert(rb, nt, kk);
-            convert(rc, nt, qq);
+        __syncthreads();
+        {
+            // K_f = k e^G, Q_f = q e^G, K_bar = k e^(G_C - G): row tid >> 4, channels
+            // 4 (tid & 15) + 64 m; and T diag(beta)
+            const int i = tid >> 4;
 #pragma unroll
-            for (int i = 1; i < kBC; ++i) G[i] += G[i - 1];
-            const float GC = G[kBC - 1];
-            sA[ch] = expf(GC);
-            sR[ch] = 0.5f * GC;
-#pragma unroll
-            for (int i = 0; i < kBC; ++i) {
-                const int o = swz(i, ch);
-                const float eg = expf(G[i]);
-                sG[o] = G[i];
-                sK[o] = kk[i];
-                sQ[o] = qq[i];
-                sKf[o] = tf32r(kk[i] * eg);
-                sQf[o] = tf32r(qq[i] * eg);
-                sKbar[o] = tf32r(kk[i] * expf(GC - G[i]));
+            for (int m = 0; m < 2; ++m) {
+                const int cb = 4 * (tid & 15) + 64 * m;
+                const float4 G = ld4(sG, i, cb), k4 = ld4(sK, i, cb), q4 = ld4(sQ, i, cb);
+                const float4 GC = ld4(sG, kBC - 1, cb);
+                const float4 eg = make_float4(expf(G.x), expf(G.y), expf(G.z), expf(G.w));
+                st4(sKf, i, cb, tf32r4(make_float4(k4.x * eg.x, k4.y * eg.y, k4.z * eg.z, k4.w * eg.w)));
+                st4(sQf, i, cb, tf32r4(make_float4(q4.x * eg.x, q4.y * eg.y, q4.z * eg.z, q4.w * eg.w)));
+                st4(sKbar, i, cb, tf32r4(make_float4(k4.x * expf(GC.x - G.x), k4.y * expf(GC.y - G.y),
+                                                     k4.z * expf(GC.z - G.z), k4.w * expf(GC.w - G.w))));
             }
-        } else {
-            const int ch = tid - kDim;
-            float vv[kBC];
-            convert(ra, nt, vv);
-#pragma unroll
-            for (int i = 0; i < kBC; ++i) {
-                const int o = swz(i, ch);
-                sRY[o] = vv[i];
-                sDO[o] = i < nt ? tf32r(rd[i]) : 0.f;
-            }
+            const int sc = tid & 15;
+            sTB[i * kSmallLd + sc] = tf32r(sT[i * kSmallLd + sc] * sBeta[sc]);
         }
         // the state's copy; a wait that gives up stops the unit (status KDA_ERR_TIMEOUT)
         const bool arrived = sm100::mbar_wait(bar, phase, kBwdWaitLimit);
@@ -649,10 +735,6 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
                 sm100::mbar_wait(bar, phase ^ 1u, kBwdWaitLimit);
             }
             return;
-        }
-        {
-            const int i = tid >> 4, s = tid & 15;
-            sTB[i * kSmallLd + s] = tf32r(sT[i * kSmallLd + s] * sBeta[s]);
         }
         // ---- phase 2 (value channels w16.. of this warp) ----
         // R = V - K_f S   (token rows, value columns)
@@ -1002,13 +1084,23 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
                 st_c(sRY, 0, w16 + 8 * jj, g, t, YS[jj]);   // dG; dY is no longer read
             }
             __syncwarp();
-            if (lane < kBC) {
-                // dg = suffix sum of dG over the chunk (the chunk end also carries the G_C terms)
-                const int col = w16 + lane;
-                float acc = sCX[col] + sA[col] * sES[col];
-                for (int i = kBC - 1; i >= 0; --i) {
-                    acc += sRY[swz(i, col)];
-                    if (i < nt) p.dg[((t0 + i) * H + h) * kDim + col] = acc;
+            {
+                // dg = suffix sum of dG over the chunk (the chunk end also carries the G_C terms):
+                // lanes 16-31 sum rows 15..8 of column w16 + (lane & 15), lanes 0-15 rows 7..0 and
+                // then add the upper half's total
+                const int col = w16 + (lane & 15), hi = lane >> 4;
+                float part[8];
+                float acc = hi ? sCX[col] + sA[col] * sES[col] : 0.f;
+#pragma unroll
+                for (int j = 7; j >= 0; --j) {
+                    acc += sRY[swz(8 * hi + j, col)];
+                    part[j] = acc;
+                }
+                const float upper = __shfl_sync(0xffffffffu, acc, lane | 16);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int i = 8 * hi + j;
+                    if (i < nt) p.dg[((t0 + i) * H + h) * kDim + col] = hi ? part[j] : part[j] + upper;
                 }
             }
         }

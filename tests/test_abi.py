@@ -311,6 +311,8 @@ def test_backward_host_checks(lib):
     assert call(outs=[outs[0], outs[0]] + outs[2:]) == -1     # two outputs alias
     assert call(d_out=None) == -1                             # no output gradient
     assert call(outs=[P(0x3004)] + outs[1:]) == -1            # output not 16-byte aligned
+    assert lib.kda_bwd(ctypes.byref(desc), P(0x1008), *ins[1:], None, cu, d_out, None, *outs, ws,
+                       need, None) == -1                      # q not 16-byte aligned
     assert call(ws_bytes=need - 1) == -3                      # workspace too small
     assert call(ws=None) == -3                                # no workspace
     assert call(ws=P(0x10008)) == -3                          # workspace not 16-byte aligned
