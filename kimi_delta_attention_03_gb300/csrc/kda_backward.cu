@@ -35,7 +35,11 @@
 // that accumulator fragments feed the next product's A operand directly and operand pairs load as
 // 64-bit words.  Shared tiles of 128 fp32 columns use an XOR swizzle that keeps both fragment
 // access patterns (rows g, columns 2t..2t+1 and rows 2t, 2t+1, columns g) free of bank conflicts.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <cstring>
+#include <mutex>
 
 #include "kda_common.cuh"
 #include "kda_sm100.cuh"
@@ -252,6 +256,12 @@ __global__ void __launch_bounds__(1024) kda_bwd_index_kernel(const int32_t* __re
     }
 }
 
+// TMA maps over the inputs, [T][H][128] (innermost first), box 128 channels x 1 head x 16 tokens:
+// g, k, q, v of the input dtype and the fp32 output gradient.
+struct BwdMaps {
+    CUtensorMap g, k, q, v, d;
+};
+
 template <typename TIn>
 struct BwdArgs {
     const TIn *q, *k, *v, *g, *beta;
@@ -347,17 +357,21 @@ __global__ void __launch_bounds__(kPrepThreads) kda_bwd_prep_kernel(const BwdArg
 
 // Shared memory of the forward kernel, in floats.
 struct FwdSmem {
-    static constexpr int KF = 0;                   // K_f   [token][key]
+    static constexpr int RAW = 0;                  // next chunk's g, k, v TMA boxes as loaded
+    static constexpr int kRawTile = kTile;         // floats per box (fp32 inputs; bf16 use half)
+    static constexpr int RAWT = RAW + 3 * kRawTile;  // next chunk's T tile
+    static constexpr int KF = RAWT + kBC * kBC;    // K_f   [token][key]
     static constexpr int KBAR = KF + kTile;        // K_bar [token][key]
     static constexpr int V = KBAR + kTile;         // V     [token][value]
     static constexpr int GG = V + kTile;           // G     [token][key]
     static constexpr int KRAW = GG + kTile;        // k     [token][key]
-    static constexpr int TB = KRAW + kTile;        // T diag(beta)
+    static constexpr int ST = KRAW + kTile;        // S^T being stored (swizzled tile)
+    static constexpr int TB = ST + kState;         // T diag(beta)
     static constexpr int T = TB + kSmall;          // T
     static constexpr int A = T + kSmall;           // exp(G_C) per key
     static constexpr int BETA = A + kDim;
-    static constexpr int ST = BETA + kBC;          // S^T being stored (swizzled tile)
-    static constexpr int TOTAL = ST + kState;
+    static constexpr int BAR = BETA + kBC;         // mbarrier of the input copies
+    static constexpr int TOTAL = BAR + 2;
 };
 constexpr size_t kFwdSmemBytes = FwdSmem::TOTAL * sizeof(float);
 
@@ -367,8 +381,9 @@ constexpr size_t kFwdSmemBytes = FwdSmem::TOTAL * sizeof(float);
 // one 64 KiB bulk asynchronous copy: the workspace holds that tile's image, which the reverse
 // kernel copies back unchanged.
 template <typename TIn>
-__global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(const BwdArgs<TIn> p) {
-    extern __shared__ __align__(16) float smf[];
+__global__ void __launch_bounds__(kBwdChainThreads, 1)
+kda_bwd_forward_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> p) {
+    extern __shared__ __align__(128) float smf[];
     float* s_kf = smf + FwdSmem::KF;
     float* s_kbar = smf + FwdSmem::KBAR;
     float* s_v = smf + FwdSmem::V;
@@ -396,27 +411,41 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(co
                 S[j][e] = s0 ? s0[col * kDim + row] : 0.f;
             }
     }
-    // the next chunk's inputs, loaded a chunk ahead as raw bits (lane l: channels 4l..4l+3):
-    // warp 0 g, warp 1 k, warp 2 v (16 rows each); warp 3 the tile T (two float4 a lane) and beta
+    // the next chunk's inputs, copied a chunk ahead: one TMA box each of g, k and v and a bulk
+    // copy of the tile T, issued by thread 0 and completing on an mbarrier; beta by warp 3 into
+    // registers
     float* s_G = smf + FwdSmem::GG;
     float* s_K = smf + FwdSmem::KRAW;
     float* s_T = smf + FwdSmem::T;
     float* s_beta = smf + FwdSmem::BETA;
-    using V4 = typename Vec4<TIn>::T;
-    V4 rin[kBC];
-    float4 rt[2];
+    const TIn* raw = reinterpret_cast<const TIn*>(smf + FwdSmem::RAW);
+    constexpr int kBoxElems = FwdSmem::kRawTile * 4 / (int)sizeof(TIn);   // box stride, elements
+    const float* rawT = smf + FwdSmem::RAWT;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smf + FwdSmem::BAR);
+    uint32_t phase = 0;
+    if (tid == 0) {
+        sm100::mbar_init(bar, 1);
+        sm100::mbar_init_fence();
+    }
+    __syncthreads();
     float rbeta = 0.f;
     auto issue_inputs = [&](int c) {
         const int64_t t0 = tb + (int64_t)c * kBC;
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
-        if (warp < 3) {
-            load_rows4(warp == 0 ? p.g : warp == 1 ? p.k : p.v, t0, nt, H, h, lane, rin);
-        } else if (warp == 3) {
-            const float* tl = p.tiles + ((c0 + c) * H + h) * (3 * kBC * kBC);
-            rt[0] = *reinterpret_cast<const float4*>(tl + 4 * lane);
-            rt[1] = *reinterpret_cast<const float4*>(tl + 4 * lane + 128);
-            rbeta = lane < nt && lane < kBC ? io<TIn>::to_f(p.beta[(t0 + lane) * H + h]) : 0.f;
+        if (tid == 0) {
+            sm100::mbar_arrive_expect_tx(bar, 3 * kBC * kDim * (int)sizeof(TIn) + kBC * kBC * 4);
+            const CUtensorMap* m3[3] = {&maps.g, &maps.k, &maps.v};
+#pragma unroll
+            for (int m = 0; m < 3; ++m)
+                sm100::tma_load_3d(const_cast<TIn*>(raw) + m * kBoxElems, m3[m], bar, 0, h, (int)t0);
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                "%2, [%3];" ::"r"(smem_u32(rawT)),
+                "l"(p.tiles + ((c0 + c) * H + h) * (3 * kBC * kBC)), "n"(kBC * kBC * 4),
+                "r"(smem_u32(bar))
+                : "memory");
         }
+        if (warp == 3) rbeta = lane < nt && lane < kBC ? io<TIn>::to_f(p.beta[(t0 + lane) * H + h]) : 0.f;
     };
     if (nch > 0) issue_inputs(0);
     for (int c = 0; c < nch; ++c) {
@@ -424,27 +453,41 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_forward_kernel(co
         const int64_t t0 = tb + (int64_t)c * kBC;
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
         if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-        __syncthreads();
-        if (warp == 0) {
+        // the chunk's inputs; a wait that gives up stops the unit (status KDA_ERR_TIMEOUT)
+        const bool arrived = sm100::mbar_wait(bar, phase, kBwdWaitLimit);
+        phase ^= 1u;
+        if (__syncthreads_or(!arrived)) {
+            if (tid == 0) {
+                report_status(p.status, kStatusTimeout);
+                sm100::mbar_wait(bar, phase ^ 1u, kBwdWaitLimit);
+                asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            }
+            return;
+        }
+        if (warp < 3) {
+            // channels 4 lane .. 4 lane + 3 of the chunk's rows of g (warp 0), k (1) or v (2)
+            const TIn* src = raw + warp * kBoxElems + 4 * lane;
             float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < kBC; ++i) {
-                const float4 x = zero_if(i >= nt, Vec4<TIn>::unpack(rin[i]));
-                G.x += x.x; G.y += x.y; G.z += x.z; G.w += x.w;
-                st4(s_G, i, 4 * lane, G);
+                const float4 x = zero_if(i >= nt, Vec4<TIn>::unpack(
+                    *reinterpret_cast<const typename Vec4<TIn>::T*>(src + i * kDim)));
+                if (warp == 0) {
+                    G.x += x.x; G.y += x.y; G.z += x.z; G.w += x.w;
+                    st4(s_G, i, 4 * lane, G);
+                } else {
+                    st4(warp == 1 ? s_K : s_v, i, 4 * lane, x);
+                }
             }
-            *reinterpret_cast<float4*>(s_a + 4 * lane) =
-                make_float4(expf(G.x), expf(G.y), expf(G.z), expf(G.w));
-        } else if (warp < 3) {
-            float* dst = warp == 1 ? s_K : s_v;
-#pragma unroll
-            for (int i = 0; i < kBC; ++i)
-                st4(dst, i, 4 * lane, zero_if(i >= nt, Vec4<TIn>::unpack(rin[i])));
+            if (warp == 0)
+                *reinterpret_cast<float4*>(s_a + 4 * lane) =
+                    make_float4(expf(G.x), expf(G.y), expf(G.z), expf(G.w));
         } else if (warp == 3) {
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 const int e = 4 * lane + 128 * m;
-                *reinterpret_cast<float4*>(s_T + (e >> 4) * kSmallLd + (e & 15)) = rt[m];
+                *reinterpret_cast<float4*>(s_T + (e >> 4) * kSmallLd + (e & 15)) =
+                    *reinterpret_cast<const float4*>(rawT + e);
             }
             if (lane < kBC) s_beta[lane] = rbeta;
         }
@@ -540,15 +583,17 @@ struct RevSmem {
     static constexpr int E = 0;                       // dE^T [value][key]
     static constexpr int KF = E + kState;             // K_f      [token][key]
     static constexpr int KBAR = KF + kTile;           // K_bar    [token][key]
-    static constexpr int QF = KBAR + kTile;           // Q_f      [token][key]
+    static constexpr int UU = KBAR + kTile;           // U        [token][value]
+    static constexpr int RAW = KF;                    // bf16 inputs: K_f, K_bar, U hold the next
+                                                      // chunk's boxes of g, k, q, v, dO as loaded
+    static constexpr int QF = UU + kTile;             // Q_f      [token][key]
     static constexpr int W = QF + kTile;              // W        [token][key]
     static constexpr int KRAW = W + kTile;            // k        [token][key]
     static constexpr int QRAW = KRAW + kTile;         // q        [token][key]
     static constexpr int GG = QRAW + kTile;           // G        [token][key]
     static constexpr int DO = GG + kTile;             // dO       [token][value]
     static constexpr int RY = DO + kTile;             // V, R, then dY, then dG [token][value|key]
-    static constexpr int UU = RY + kTile;             // U        [token][value]
-    static constexpr int DU = UU + kTile;             // dU       [token][value]
+    static constexpr int DU = RY + kTile;             // dU       [token][value]
     static constexpr int T = DU + kTile;              // 16 x 16 tiles
     static constexpr int P = T + kSmall;
     static constexpr int AT = P + kSmall;
@@ -563,15 +608,17 @@ struct RevSmem {
     static constexpr int DBP = BETA + kBC;            // per-warp partial rowsum(dY * R)
     static constexpr int SS = DBP + 8 * kBC;          // S^T [value][key] of the chunk (swizzled)
     static constexpr int BAR = SS + kState;           // mbarrier of the state's bulk copy
-    static constexpr int TOTAL = BAR + 2;
+    static constexpr int BAR_IN = BAR + 2;            // mbarrier of the inputs' copies
+    static constexpr int TOTAL = BAR_IN + 2;
 };
 constexpr size_t kRevSmemBytes = RevSmem::TOTAL * sizeof(float);
 
 // The reverse pass of one unit: chunks from last to first, with dE^T (the gradient of the state at
 // the end of the current chunk) in shared memory.
 template <typename TIn>
-__global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(const BwdArgs<TIn> p) {
-    extern __shared__ __align__(16) float sm[];
+__global__ void __launch_bounds__(kBwdChainThreads, 1)
+kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> p) {
+    extern __shared__ __align__(128) float sm[];
     float* sE = sm + RevSmem::E;
     float* sKf = sm + RevSmem::KF;
     float* sKbar = sm + RevSmem::KBAR;
@@ -634,36 +681,74 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
                 : "memory");
         }
     };
-    // the next chunk's inputs, loaded a chunk ahead as raw bits (lane l: channels 4l..4l+3):
-    // warps 0-3 g, k, q, v (16 rows each); warps 4, 5 dO rows 0-7, 8-15; warp 6 the tiles T, P,
-    // At (six float4 a lane); warp 7 beta
+    // The next chunk's inputs, fetched a chunk ahead.  bf16 inputs: one TMA box each of g, k, q, v
+    // and dO into the K_f / K_bar / U region (free from phase 3 to the next staging), issued by
+    // thread 0 on the mbarrier bar_in.  fp32 inputs (boxes twice as large): warps 0-3 load g, k,
+    // q, v and warps 4, 5 dO into registers (lane l: channels 4l..4l+3).  Warp 6 loads the tiles
+    // T, P, At (six float4 a lane) and warp 7 beta into registers.
+    constexpr bool kBulkIn = sizeof(TIn) == 2;
+    const TIn* rawIn = reinterpret_cast<const TIn*>(sm + RevSmem::RAW);   // [4][16][128]
+    const float* rawDO = sm + RevSmem::RAW + 4 * kTile * (int)sizeof(TIn) / 4;  // [16][128]
+    uint64_t* bar_in = reinterpret_cast<uint64_t*>(sm + RevSmem::BAR_IN);
+    uint32_t phase_in = 0;
+    if (tid == 0) {
+        sm100::mbar_init(bar_in, 1);
+        sm100::mbar_init_fence();
+    }
+    __syncthreads();
     using V4 = typename Vec4<TIn>::T;
-    V4 rin[kBC];
+    V4 rin[kBulkIn ? 1 : kBC];
     float4 rf[8];
     float rbeta = 0.f;
     auto issue_inputs = [&](int c) {
         const int64_t t0 = tb + (int64_t)c * kBC;
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
-        if (warp < 4) {
-            load_rows4(warp == 0 ? p.g : warp == 1 ? p.k : warp == 2 ? p.q : p.v, t0, nt, H, h,
-                       lane, rin);
-        } else if (warp < 6) {
-            const float* base = p.d_out + (t0 * H + h) * kDim + 4 * lane;
-            const int64_t stride = (int64_t)H * kDim;
-            const int r0 = (warp - 4) * 8;
+        if constexpr (kBulkIn) {
+            if (tid == 0) {
+                sm100::mbar_arrive_expect_tx(bar_in, 4 * kTile * (int)sizeof(TIn) + kTile * 4);
+                const CUtensorMap* m4[4] = {&maps.g, &maps.k, &maps.q, &maps.v};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int row = r0 + i;
-                rf[i] = *reinterpret_cast<const float4*>(base + (row < nt ? row : nt - 1) * stride);
+                for (int m = 0; m < 4; ++m)
+                    sm100::tma_load_3d(const_cast<TIn*>(rawIn) + m * kTile, m4[m], bar_in, 0, h,
+                                       (int)t0);
+                sm100::tma_load_3d(const_cast<float*>(rawDO), &maps.d, bar_in, 0, h, (int)t0);
             }
-        } else if (warp == 6) {
+        } else {
+            if (warp < 4) {
+                load_rows4(warp == 0 ? p.g : warp == 1 ? p.k : warp == 2 ? p.q : p.v, t0, nt, H, h,
+                           lane, rin);
+            } else if (warp < 6) {
+                const float* base = p.d_out + (t0 * H + h) * kDim + 4 * lane;
+                const int64_t stride = (int64_t)H * kDim;
+                const int r0 = (warp - 4) * 8;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = r0 + i;
+                    rf[i] = *reinterpret_cast<const float4*>(base + (row < nt ? row : nt - 1) * stride);
+                }
+            }
+        }
+        if (warp == 6) {
             const float* tl = p.tiles + ((c0 + c) * H + h) * (3 * kBC * kBC);
 #pragma unroll
             for (int m = 0; m < 6; ++m)
                 rf[m] = *reinterpret_cast<const float4*>(tl + 4 * (lane + 32 * m));
-        } else {
+        } else if (warp == 7) {
             rbeta = lane < nt && lane < kBC ? io<TIn>::to_f(p.beta[(t0 + lane) * H + h]) : 0.f;
         }
+    };
+    // row i, channels 4 lane .. 4 lane + 3 of input m (0 g, 1 k, 2 q, 3 v) and of dO
+    auto in_row = [&](int m, int i) -> float4 {
+        if constexpr (kBulkIn)
+            return Vec4<TIn>::unpack(*reinterpret_cast<const V4*>(rawIn + m * kTile + i * kDim + 4 * lane));
+        else
+            return Vec4<TIn>::unpack(rin[i]);
+    };
+    auto do_row = [&](int i) -> float4 {
+        if constexpr (kBulkIn)
+            return *reinterpret_cast<const float4*>(rawDO + i * kDim + 4 * lane);
+        else
+            return rf[i & 7];
     };
     if (nch > 0) {
         issue_state(nch - 1);
@@ -673,13 +758,25 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
     for (int c = nch - 1; c >= 0; --c) {
         const int64_t t0 = tb + (int64_t)c * kBC;
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
-        __syncthreads();
+        {
+            // the chunk's input copies; a wait that gives up stops the unit (KDA_ERR_TIMEOUT)
+            const bool arrived = !kBulkIn || sm100::mbar_wait(bar_in, phase_in, kBwdWaitLimit);
+            phase_in ^= 1u;
+            if (__syncthreads_or(!arrived)) {
+                if (tid == 0) {
+                    report_status(p.status, kStatusTimeout);
+                    sm100::mbar_wait(bar_in, phase_in ^ 1u, kBwdWaitLimit);
+                    sm100::mbar_wait(bar, phase, kBwdWaitLimit);
+                }
+                return;
+            }
+        }
         // ---- phase 1: stage the chunk ----
         if (warp == 0) {
             float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < kBC; ++i) {
-                const float4 x = zero_if(i >= nt, Vec4<TIn>::unpack(rin[i]));
+                const float4 x = zero_if(i >= nt, in_row(0, i));
                 G.x += x.x; G.y += x.y; G.z += x.z; G.w += x.w;
                 st4(sG, i, 4 * lane, G);
             }
@@ -690,13 +787,12 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
         } else if (warp < 4) {
             float* dst = warp == 1 ? sK : warp == 2 ? sQ : sRY;
 #pragma unroll
-            for (int i = 0; i < kBC; ++i)
-                st4(dst, i, 4 * lane, zero_if(i >= nt, Vec4<TIn>::unpack(rin[i])));
+            for (int i = 0; i < kBC; ++i) st4(dst, i, 4 * lane, zero_if(i >= nt, in_row(warp, i)));
         } else if (warp < 6) {
             const int r0 = (warp - 4) * 8;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                st4(sDO, r0 + i, 4 * lane, zero_if(r0 + i >= nt, tf32r4(rf[i])));
+                st4(sDO, r0 + i, 4 * lane, zero_if(r0 + i >= nt, tf32r4(do_row(r0 + i))));
         } else if (warp == 6) {
 #pragma unroll
             for (int m = 0; m < 6; ++m) {
@@ -1122,6 +1218,36 @@ __global__ void __launch_bounds__(kBwdChainThreads, 1) kda_bwd_reverse_kernel(co
     }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 bwd_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 3-D map over [T, H, 128] (innermost first) of `esize`-byte elements, box 128 x 1 x 16, no
+// swizzle (rows land dense in shared memory); rows past T read as zero.
+bool make_box_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, size_t esize,
+                  int64_t T, int H) {
+    auto enc = bwd_encode_fn();
+    if (!enc || !base) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)kDim * esize, (cuuint64_t)H * kDim * esize};
+    cuuint32_t box[3] = {(cuuint32_t)kDim, 1, (cuuint32_t)kBC};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(map, dt, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 }  // namespace
 
 size_t backward_workspace_floats(int num_seqs, int heads, int64_t chunks) {
@@ -1156,6 +1282,18 @@ cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, c
         const BwdArgs<T> a{(const T*)q, (const T*)k, (const T*)v, (const T*)g, (const T*)beta,
                            cu_seqlens, init_state, d_out, d_state, dq, dk, dv, dg, dbeta, d_init,
                            idx, tiles, states, status, num_seqs, heads};
+        BwdMaps maps;
+        memset(&maps, 0, sizeof(maps));
+        const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        if (total_tokens > 0 &&
+            !(make_box_map(&maps.g, g, dt, sizeof(T), total_tokens, heads) &&
+              make_box_map(&maps.k, k, dt, sizeof(T), total_tokens, heads) &&
+              make_box_map(&maps.q, q, dt, sizeof(T), total_tokens, heads) &&
+              make_box_map(&maps.v, v, dt, sizeof(T), total_tokens, heads) &&
+              make_box_map(&maps.d, d_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, total_tokens,
+                           heads)))
+            return cudaErrorInvalidValue;
         if (chunks > 0) {
             kda_bwd_prep_kernel<T><<<dim3((unsigned)chunks, (unsigned)heads), kPrepThreads, 0,
                                      stream>>>(a);
@@ -1166,7 +1304,7 @@ cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, c
                                        (int)kFwdSmemBytes);
             if (err != cudaSuccess) return err;
             kda_bwd_forward_kernel<T><<<(unsigned)(num_seqs * heads), kBwdChainThreads,
-                                        kFwdSmemBytes, stream>>>(a);
+                                        kFwdSmemBytes, stream>>>(maps, a);
             err = cudaGetLastError();
             if (err != cudaSuccess) return err;
         }
@@ -1175,7 +1313,7 @@ cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, c
                                                (int)kRevSmemBytes);
         if (err != cudaSuccess) return err;
         kda_bwd_reverse_kernel<T><<<(unsigned)(num_seqs * heads), kBwdChainThreads, kRevSmemBytes,
-                                    stream>>>(a);
+                                    stream>>>(maps, a);
         return cudaGetLastError();
     };
     if (dtype == KDA_BF16) return run(__nv_bfloat16{});
