@@ -548,13 +548,18 @@ def main():
                            x["seqlens"], d_out, init_state=x["init_state"], workspace=bws)
 
         bstep()
-        ms_b = max_over_ranks(time_device(bstep, 2, stream), world)
-        # the gradient outputs are fp32: 5 x 512 B + 4 B per token-head, plus the inputs and
-        # d_out read (1,026 + 512 B) and 2 x 64 KiB of states per unit
+        ms_b = max_over_ranks(time_device(bstep, 5, stream), world)
+        # dense tf32 products per 16-token chunk and head, in multiply-adds: prep 2 x 16*16*128;
+        # forward chain 2 x 16*128*128 + 16*16*128; reverse 7 x 16*128*128 + 10 x 16*16*128
+        chunks = sum((n + 15) // 16 for n in x["seqlens"])
+        flops_b = 2.0 * chunks * H * (9 * 16 * 128 * 128 + 13 * 16 * 16 * 128)
         extra["backward_4x8k" if not small else "backward_small"] = {
             "workload": w.name + ": gradients of q, k, v, log alpha, beta and the initial state",
-            "tokens": T, "ms_per_step": ms_b, "steps": 2,
+            "tokens": T, "ms_per_step": ms_b, "steps": 5,
             "value": T * world / (ms_b * 1e-3) / 1e6, "unit": "Mtokens/s",
+            "algorithmic_tflop_per_step": flops_b / 1e12,
+            "tensor_tflops": flops_b / (ms_b * 1e-3) / 1e12,
+            "kernels": "index, prep (chunk-parallel), forward chain, reverse chain (one CTA per unit)",
             "workspace_bytes": int(bws.numel())}
         del d_out, bws
 
