@@ -193,3 +193,16 @@ def test_backward_many_short_sequences():
         x["cu_seqlens"].cpu(), d_out.cpu(), state_in=x["init_state"].cpu())
     for name, g, r in zip(NAMES, got, ref):
         assert_close(name, g.cpu().numpy(), r)
+
+
+def test_backward_all_sequences_empty():
+    """No tokens at all: the initial-state gradient is the final-state gradient, bit for bit."""
+    lens, H = [0, 0, 0], 2
+    x = synth.make_inputs(lens, H, torch.bfloat16, seed=86, device=DEV)
+    d_state = torch.randn(3, H, 128, 128, device=DEV)
+    d_out = torch.zeros(0, H, 128, device=DEV)
+    got = kda().bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["cu_seqlens"],
+                    x["seqlens"], d_out, init_state=x["init_state"], d_state=d_state)
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    assert torch.equal(got[5], d_state)
