@@ -62,7 +62,8 @@ typedef enum kda_status {
     KDA_ERR_WORKSPACE = -3,    /* workspace missing or smaller than kda_fwd_workspace_bytes */
     KDA_ERR_CUDA = -4,         /* a CUDA launch or query failed                             */
     KDA_ERR_TIMEOUT = -5,      /* a bounded device-side wait gave up (device status word)   */
-    KDA_ERR_DECAY_RANGE = -6   /* log_alpha > 0, or below -20 (see kda_fwd_chunked)         */
+    KDA_ERR_DECAY_RANGE = -6   /* log_alpha > 0, or below -20 (see kda_fwd_chunked); in    */
+                               /* kda_bwd, a 16-token chunk decaying beyond 160           */
 } kda_status;
 
 typedef enum kda_dtype { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
