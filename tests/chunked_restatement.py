@@ -161,7 +161,7 @@ def _unit_lower_inverse16(A):
     return X
 
 
-def backward_prep(k, v, q, g, beta):
+def backward_prep(k, v, q, g, beta, mm=np.matmul):
     """Chunk-local factors of the chunked backward (one chunk of C tokens, zero-padded).
 
     G = cumsum g; r = G_C / 2; a = exp(G_C)
@@ -177,34 +177,34 @@ def backward_prep(k, v, q, g, beta):
     f = dict(G=G, GC=GC, a=np.exp(GC), K_f=k * np.exp(G), Q_f=q * np.exp(G),
              K_p=k * np.exp(G - r), K_m=k * np.exp(r - G), Q_r=q * np.exp(G - r),
              K_bar=k * np.exp(GC - G))
-    f["At"] = np.tril(f["K_p"] @ f["K_m"].T, -1)
-    f["P"] = np.tril(f["Q_r"] @ f["K_m"].T, 0)
+    f["At"] = np.tril(mm(f["K_p"], f["K_m"].T), -1)
+    f["P"] = np.tril(mm(f["Q_r"], f["K_m"].T), 0)
     f["T"] = _unit_lower_inverse16(beta[:, None] * f["At"])
-    f["W"] = f["T"] @ (beta[:, None] * f["K_f"])
-    f["U_bar"] = f["T"] @ (beta[:, None] * v)
-    f["Qp"] = f["Q_f"] - f["P"] @ f["W"]
+    f["W"] = mm(f["T"], beta[:, None] * f["K_f"])
+    f["U_bar"] = mm(f["T"], beta[:, None] * v)
+    f["Qp"] = f["Q_f"] - mm(f["P"], f["W"])
     return f
 
 
-def backward_chunk_grads(f, q, k, v, beta, dO, S, dE, U):
+def backward_chunk_grads(f, q, k, v, beta, dO, S, dE, U, mm=np.matmul):
     """Gradients of one chunk given its start state S, the gradient dE of its end state and
     its U = U_bar - W S.  Returns (dq, dk, dv, dG, dbeta) with dG the gradient with respect to
     the in-chunk cumulative decay G (the caller turns it into dg by a suffix sum)."""
-    dU = f["P"].T @ dO + f["K_bar"] @ dE
-    dY = f["T"].T @ dU
-    R = v - f["K_f"] @ S
+    dU = mm(f["P"].T, dO) + mm(f["K_bar"], dE)
+    dY = mm(f["T"].T, dU)
+    R = v - mm(f["K_f"], S)
     dbeta = np.sum(dY * R, axis=1)
     dR = beta[:, None] * dY
-    dA = -np.tril(dY @ U.T, -1)
+    dA = -np.tril(mm(dY, U.T), -1)
     dbeta = dbeta + np.sum(dA * f["At"], axis=1)
     dAt = beta[:, None] * dA
-    dP = np.tril(dO @ U.T, 0)
-    dK_f = -dR @ S.T
-    dQ_f = dO @ S.T
-    dK_bar = U @ dE.T
-    dK_p = dAt @ f["K_m"]
-    dK_m = dAt.T @ f["K_p"] + dP.T @ f["Q_r"]
-    dQ_r = dP @ f["K_m"]
+    dP = np.tril(mm(dO, U.T), 0)
+    dK_f = -mm(dR, S.T)
+    dQ_f = mm(dO, S.T)
+    dK_bar = mm(U, dE.T)
+    dK_p = mm(dAt, f["K_m"])
+    dK_m = mm(dAt.T, f["K_p"]) + mm(dP.T, f["Q_r"])
+    dQ_r = mm(dP, f["K_m"])
     G, GC = f["G"], f["GC"]
     r = GC / 2.0
     dk = dK_f * np.exp(G) + dK_p * np.exp(G - r) + dK_m * np.exp(r - G) + dK_bar * np.exp(GC - G)
@@ -215,31 +215,33 @@ def backward_chunk_grads(f, q, k, v, beta, dO, S, dE, U):
     return dq, dk, dR, dG, dbeta
 
 
-def unit_backward(q, k, v, g, beta, S0, dO, dSN, C=16):
+def unit_backward(q, k, v, g, beta, S0, dO, dSN, C=16, operand=None):
     """Chunked backward of one unit in three steps: chunk-local factors; the forward chain
     S_{c+1} = diag(a) S_c + K_bar^T (U_bar - W S_c) and the reverse chain
     dE_{c-1} = diag(a) dE_c + Q'^T dO - W^T (K_bar dE_c); then per-chunk gradients.
-    Returns (dq, dk, dv, dg, dbeta, dS0)."""
+    Returns (dq, dk, dv, dg, dbeta, dS0).  `operand`, if given, rounds both operands of every
+    matrix product (fp64 accumulation), to model a tensor-core input format."""
+    mm = np.matmul if operand is None else (lambda a, b: operand(a) @ operand(b))
     L = q.shape[0]
     chunks = _chunks(L, C)
     pads = [[_padded(x, c0, c1, C) for x in (q, k, v, g, beta, dO)] for c0, c1 in chunks]
-    facs = [backward_prep(kk, vv, qq, gg, bb) for qq, kk, vv, gg, bb, _ in pads]
+    facs = [backward_prep(kk, vv, qq, gg, bb, mm) for qq, kk, vv, gg, bb, _ in pads]
     S, starts, Us = S0.copy(), [], []
     for f in facs:
         starts.append(S)
-        U = f["U_bar"] - f["W"] @ S
+        U = f["U_bar"] - mm(f["W"], S)
         Us.append(U)
-        S = f["a"][:, None] * S + f["K_bar"].T @ U
+        S = f["a"][:, None] * S + mm(f["K_bar"].T, U)
     dE, ends = dSN.copy(), [None] * len(facs)
     for c in range(len(facs) - 1, -1, -1):
         f, dOc = facs[c], pads[c][5]
         ends[c] = dE
-        dE = f["a"][:, None] * dE + f["Qp"].T @ dOc - f["W"].T @ (f["K_bar"] @ dE)
+        dE = f["a"][:, None] * dE + mm(f["Qp"].T, dOc) - mm(f["W"].T, mm(f["K_bar"], dE))
     out = [np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), np.zeros_like(g), np.zeros(L)]
     for c, (c0, c1) in enumerate(chunks):
         qq, kk, vv, _, bb, dOc = pads[c]
         dq, dk, dv, dG, db = backward_chunk_grads(facs[c], qq, kk, vv, bb, dOc, starts[c],
-                                                  ends[c], Us[c])
+                                                  ends[c], Us[c], mm)
         dg = np.cumsum(dG[::-1], axis=0)[::-1]
         n = c1 - c0
         for o, x in zip(out, (dq, dk, dv, dg, db)):

@@ -109,3 +109,47 @@ def test_chunked_backward_equals_autograd_of_the_token_loop(L, gate):
     ref = _oracle_unit_backward(q, k, v, g, beta, S0, dO, dSN)
     for a, b in zip(got, ref):
         _close(a, b, 1e-9)
+
+
+def _round_tf32(x):
+    """Round to tf32 (10 explicit mantissa bits), to nearest with ties away from zero, as the
+    tensor-core input conversion of fp32 operands does."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    b = a.view(np.uint32).astype(np.uint64)
+    b = ((b + 0x1000) & 0xFFFFE000).astype(np.uint32)
+    return b.view(np.float32).astype(np.float64)
+
+
+def _round_bf16(x):
+    """Round to bf16 (7 explicit mantissa bits), to nearest even."""
+    import torch
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def test_backward_operand_precision_choice():
+    """Why the backward's products take tf32 operands: on the GPU test's bounded-gate input
+    (log alpha = -5 sigmoid(2z), 300 tokens), the chunked backward with every product's operands
+    rounded to tf32 meets the parity gate against the token-loop oracle, while bf16 operands miss
+    its max-abs term on dg.  Accumulation stays fp64 here (fp32 in the kernels)."""
+    import torch
+    from kimi_delta_attention_03_gb300 import synth
+    from tests.chunked_restatement import unit_backward
+    from tests.parity import errors, MAX_ABS_TOL, REL_L2_TOL
+    x = synth.make_inputs([300], 1, torch.bfloat16, seed=77, bounded_gate=-5.0)
+    gen = torch.Generator().manual_seed(78)
+    d_out = torch.randn(300, 1, 128, generator=gen)
+    d_state = torch.randn(1, 1, 128, 128, generator=gen) * 0.1
+    ref = oracle.recurrence_backward(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"],
+                                     x["cu_seqlens"], d_out, state_in=x["init_state"],
+                                     d_state=d_state)
+    f64 = lambda t: t[:, 0].double().numpy()
+    args = [f64(x[key]) for key in ("q", "k", "v", "log_alpha", "beta")]
+    args += [x["init_state"][0, 0].double().numpy(), f64(d_out), d_state[0, 0].double().numpy()]
+    worst = {}
+    for name, rnd in (("tf32", _round_tf32), ("bf16", _round_bf16)):
+        got = unit_backward(*args, C=16, operand=rnd)
+        errs = [errors(g, r[:, 0] if r.ndim == 3 else (r[:, 0] if r.ndim == 2 else r[0, 0]))
+                for g, r in zip(got, ref)]
+        worst[name] = (max(e[0] for e in errs), max(e[1] for e in errs))
+    assert worst["tf32"][0] <= REL_L2_TOL and worst["tf32"][1] <= MAX_ABS_TOL, worst
+    assert worst["bf16"][1] > MAX_ABS_TOL, worst
