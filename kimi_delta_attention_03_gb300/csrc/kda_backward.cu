@@ -139,21 +139,6 @@ __device__ __forceinline__ void load_col(const TIn* x, int64_t t0, int nt, int H
     for (int i = 0; i < kBC; ++i) out[i] = i < nt ? io<TIn>::to_f(raw[i]) : 0.f;
 }
 
-// Raw loads of one channel of a chunk, kept unconverted so that they stay in flight until used.
-template <typename TIn>
-__device__ __forceinline__ void load_raw(const TIn* x, int64_t t0, int nt, int H, int h, int ch,
-                                         TIn (&raw)[kBC]) {
-    const TIn* base = x + (t0 * H + h) * kDim + ch;
-    const int64_t stride = (int64_t)H * kDim;
-#pragma unroll
-    for (int i = 0; i < kBC; ++i) raw[i] = base[(i < nt ? i : nt - 1) * stride];
-}
-template <typename TIn>
-__device__ __forceinline__ void convert(const TIn (&raw)[kBC], int nt, float (&out)[kBC]) {
-#pragma unroll
-    for (int i = 0; i < kBC; ++i) out[i] = i < nt ? io<TIn>::to_f(raw[i]) : 0.f;
-}
-
 // Four consecutive channels of one row: their raw bits (8 bytes of bf16, 16 of fp32) and fp32.
 template <typename TIn> struct Vec4;
 template <> struct Vec4<__nv_bfloat16> {
@@ -604,7 +589,7 @@ struct RevSmem {
     static constexpr int DP = DA + kSmall;
     static constexpr int A = DP + kSmall;             // exp(G_C) per key
     static constexpr int R = A + kDim;                // G_C / 2 per key
-    static constexpr int ES = R + kDim;               // a * rowsum(dE * S) per key
+    static constexpr int ES = R + kDim;               // rowsum(dE * S) per key
     static constexpr int CX = ES + kDim;              // sum_t dK_bar K_bar per key
     static constexpr int BETA = CX + kDim;
     static constexpr int DBP = BETA + kBC;            // per-warp partial rowsum(dY * R)
