@@ -450,8 +450,8 @@ kda_status kda_decode_window_prologue(const kda_desc* desc, const kda_prologue_p
  *   dinit_state   device fp32 [N, H, 128, 128]
  *   workspace     device, at least kda_bwd_workspace_bytes(desc) bytes, 16-byte aligned: the
  *                 sequences' chunk offsets, then per 16-token chunk and head three 16 x 16 fp32
- *                 tiles and the chunk's start state (128 x 128 fp32); contents on return are
- *                 unspecified
+ *                 tiles, the chunk's start state (128 x 128 fp32) and a 16 x 128 fp32 tile;
+ *                 contents on return are unspecified
  * The gradients are deterministic (no atomics; every sum runs in a fixed order).  If the device
  * cu_seqlens disagree with the host lengths in their chunk total or run past T, the first launch
  * sets KDA_ERR_INVALID_ARG in the device status word, nothing else is computed and every output

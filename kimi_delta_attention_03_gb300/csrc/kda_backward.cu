@@ -54,6 +54,7 @@ constexpr int kBwdChainThreads = 256;
 constexpr int kPrepThreads = 128;
 constexpr int kTile = kBC * kDim;      // floats in a [16][128] tile
 constexpr int kState = kDim * kDim;    // floats in a state
+constexpr int kSlot = kState + kTile;  // per chunk and head: S^T at the chunk's start, then R
 constexpr int kSmallLd = 20;           // leading dimension of the 16 x 16 tiles in shared memory
 constexpr int kSmall = kBC * kSmallLd;
 constexpr float kMaxExponent = 80.f;   // |G - r| bound of the factors
@@ -259,7 +260,7 @@ struct BwdArgs {
     float *dq, *dk, *dv, *dg, *dbeta, *d_init;
     const int32_t* idx;       // [N + 2]
     float* tiles;             // [chunks][H][3][16][16]: T, P, At
-    float* states;            // [chunks][H][128][128]: S^T at each chunk's start
+    float* states;            // [chunks][H][kSlot]: S^T at each chunk's start, then R = V - K_f S
     int* status;
     int N, H;
 };
@@ -358,7 +359,8 @@ struct FwdSmem {
     static constexpr int A = T + kSmall;           // exp(G_C) per key
     static constexpr int BETA = A + kDim;
     static constexpr int BAR = BETA + kBC;         // mbarrier of the input copies
-    static constexpr int TOTAL = BAR + 2;
+    static constexpr int RT = (BAR + 2 + 31) / 32 * 32;  // R of the last two chunks (swizzled)
+    static constexpr int TOTAL = RT + 2 * kTile;
 };
 constexpr size_t kFwdSmemBytes = FwdSmem::TOTAL * sizeof(float);
 
@@ -366,7 +368,8 @@ constexpr size_t kFwdSmemBytes = FwdSmem::TOTAL * sizeof(float);
 // Each chunk's inputs are loaded during the previous chunk.  The state, rounded to tf32 (it is
 // only an MMA operand and a factor of one row sum later), leaves through a swizzled shared tile by
 // one 64 KiB bulk asynchronous copy: the workspace holds that tile's image, which the reverse
-// kernel copies back unchanged.
+// kernel copies back unchanged.  R = V - K_f S, which the reverse pass needs as it is, leaves the
+// same way one chunk later (two tiles alternate).
 template <typename TIn>
 __global__ void __launch_bounds__(kBwdChainThreads, 1)
 kda_bwd_forward_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> p) {
@@ -377,6 +380,7 @@ kda_bwd_forward_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
     float* s_tb = smf + FwdSmem::TB;
     float* s_a = smf + FwdSmem::A;
     float* s_st = smf + FwdSmem::ST;
+    float* s_rt = smf + FwdSmem::RT;
     if (p.idx[p.N + 1]) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -488,10 +492,17 @@ kda_bwd_forward_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
         __syncthreads();
         if (tid == 0) {
             asm volatile(
-                "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
-                "cp.async.bulk.commit_group;" ::"l"(p.states + slot * kState),
+                "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                    p.states + slot * kSlot),
                 "r"(smem_u32(s_st)), "n"(kState * 4)
                 : "memory");
+            if (c > 0)   // the previous chunk's R
+                asm volatile(
+                    "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                        p.states + (slot - H) * kSlot + kState),
+                    "r"(smem_u32(s_rt + ((c - 1) & 1) * kTile)), "n"(kTile * 4)
+                    : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
         {
             // K_f = k e^G, K_bar = k e^(G_C - G): row tid >> 4, channels 4 (tid & 15) + 64 m
@@ -529,6 +540,15 @@ kda_bwd_forward_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
                 mma8(R[jj], a, b);
             }
         }
+        // R [token][value] into this chunk's R tile, for the reverse pass
+        {
+            float* rt = s_rt + (c & 1) * kTile;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    rt[swz(8 * jj + 2 * t + (e & 1), dv0 + g + (e >> 1) * 8)] = R[jj][e];
+        }
         // U^T = R^T (T diag(beta))^T
         float U[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -561,7 +581,18 @@ kda_bwd_forward_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
             }
         }
     }
-    // the store must have completed before the CTA's shared memory is released
+    // the last chunk's R, then every store must have completed before the CTA's shared memory is
+    // released
+    if (nch > 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncthreads();
+        if (tid == 0)
+            asm volatile(
+                "cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
+                "cp.async.bulk.commit_group;" ::"l"(p.states + ((c0 + nch - 1) * H + h) * kSlot + kState),
+                "r"(smem_u32(s_rt + ((nch - 1) & 1) * kTile)), "n"(kTile * 4)
+                : "memory");
+    }
     if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
@@ -648,8 +679,9 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
         sE[swz(dv, dk)] = p.d_state ? p.d_state[ubase + e] : 0.f;
     }
 
-    // the chunk's start state S^T (the forward kernel's swizzled tile image) into shared memory,
-    // one 64 KiB bulk copy completing on an mbarrier
+    // the chunk's start state S^T and its R = V - K_f S (the forward kernel's swizzled tile
+    // images) into shared memory, two bulk copies completing on an mbarrier; R lands in sRY, free
+    // from phase 3 on (the chunk's dG goes to sDU)
     float* sS = sm + RevSmem::SS;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + RevSmem::BAR);
     uint32_t phase = 0;
@@ -660,22 +692,28 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
     __syncthreads();
     auto issue_state = [&](int c) {
         if (tid == 0) {
-            sm100::mbar_arrive_expect_tx(bar, kState * 4);
+            const float* src = p.states + ((c0 + c) * H + h) * kSlot;
+            sm100::mbar_arrive_expect_tx(bar, kSlot * 4);
             asm volatile(
                 "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
                 "[%3];" ::"r"(smem_u32(sS)),
-                "l"(p.states + ((c0 + c) * H + h) * kState), "n"(kState * 4), "r"(smem_u32(bar))
+                "l"(src), "n"(kState * 4), "r"(smem_u32(bar))
+                : "memory");
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+                "[%3];" ::"r"(smem_u32(sRY)),
+                "l"(src + kState), "n"(kTile * 4), "r"(smem_u32(bar))
                 : "memory");
         }
     };
-    // The next chunk's inputs, fetched a chunk ahead.  bf16 inputs: one TMA box each of g, k, q, v
-    // and dO into the K_f / K_bar / U region (free from phase 3 to the next staging), issued by
-    // thread 0 on the mbarrier bar_in.  fp32 inputs (boxes twice as large): warps 0-3 load g, k,
-    // q, v and warps 4, 5 dO into registers (lane l: channels 4l..4l+3).  Warp 6 loads the tiles
-    // T, P, At (six float4 a lane) and warp 7 beta into registers.
+    // The next chunk's inputs, fetched a chunk ahead (v is not needed: R comes with the state).
+    // bf16 inputs: one TMA box each of g, k, q and dO into the K_f / K_bar / U region (free from
+    // phase 3 to the next staging), issued by thread 0 on the mbarrier bar_in.  fp32 inputs
+    // (boxes twice as large): warps 0-2 load g, k, q and warps 4, 5 dO into registers (lane l:
+    // channels 4l..4l+3).  Warp 6 loads the tiles T, P, At (six float4 a lane) and warp 7 beta.
     constexpr bool kBulkIn = sizeof(TIn) == 2;
-    const TIn* rawIn = reinterpret_cast<const TIn*>(sm + RevSmem::RAW);   // [4][16][128]
-    const float* rawDO = sm + RevSmem::RAW + 4 * kTile * (int)sizeof(TIn) / 4;  // [16][128]
+    const TIn* rawIn = reinterpret_cast<const TIn*>(sm + RevSmem::RAW);   // [3][16][128]
+    const float* rawDO = sm + RevSmem::RAW + 3 * kTile * (int)sizeof(TIn) / 4;  // [16][128]
     uint64_t* bar_in = reinterpret_cast<uint64_t*>(sm + RevSmem::BAR_IN);
     uint32_t phase_in = 0;
     if (tid == 0) {
@@ -692,19 +730,18 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
         const int nt = (int)(te - t0 < kBC ? te - t0 : kBC);
         if constexpr (kBulkIn) {
             if (tid == 0) {
-                sm100::mbar_arrive_expect_tx(bar_in, 4 * kTile * (int)sizeof(TIn) + kTile * 4);
-                const CUtensorMap* m4[4] = {&maps.g, &maps.k, &maps.q, &maps.v};
+                sm100::mbar_arrive_expect_tx(bar_in, 3 * kTile * (int)sizeof(TIn) + kTile * 4);
+                const CUtensorMap* m4[3] = {&maps.g, &maps.k, &maps.q};
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
+                for (int m = 0; m < 3; ++m)
                     sm100::tma_load_3d(const_cast<TIn*>(rawIn) + m * kTile, m4[m], bar_in, 0, h,
                                        (int)t0);
                 sm100::tma_load_3d(const_cast<float*>(rawDO), &maps.d, bar_in, 0, h, (int)t0);
             }
         } else {
-            if (warp < 4) {
-                load_rows4(warp == 0 ? p.g : warp == 1 ? p.k : warp == 2 ? p.q : p.v, t0, nt, H, h,
-                           lane, rin);
-            } else if (warp < 6) {
+            if (warp < 3) {
+                load_rows4(warp == 0 ? p.g : warp == 1 ? p.k : p.q, t0, nt, H, h, lane, rin);
+            } else if (warp == 4 || warp == 5) {
                 const float* base = p.d_out + (t0 * H + h) * kDim + 4 * lane;
                 const int64_t stride = (int64_t)H * kDim;
                 const int r0 = (warp - 4) * 8;
@@ -724,7 +761,7 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
             rbeta = lane < nt && lane < kBC ? io<TIn>::to_f(p.beta[(t0 + lane) * H + h]) : 0.f;
         }
     };
-    // row i, channels 4 lane .. 4 lane + 3 of input m (0 g, 1 k, 2 q, 3 v) and of dO
+    // row i, channels 4 lane .. 4 lane + 3 of input m (0 g, 1 k, 2 q) and of dO
     auto in_row = [&](int m, int i) -> float4 {
         if constexpr (kBulkIn)
             return Vec4<TIn>::unpack(*reinterpret_cast<const V4*>(rawIn + m * kTile + i * kDim + 4 * lane));
@@ -758,7 +795,8 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
                 return;
             }
         }
-        // ---- phase 1: stage the chunk ----
+        // ---- phase 1: stage the chunk: warp 0 the prefix sums of g, warps 1, 2 k and q, warps
+        // 4, 5 dO rows 0-7 and 8-15, warp 6 the tiles T, P, At, warp 7 beta ----
         if (warp == 0) {
             float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -771,11 +809,11 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
                 make_float4(__expf(G.x), __expf(G.y), __expf(G.z), __expf(G.w));
             *reinterpret_cast<float4*>(sR + 4 * lane) =
                 make_float4(0.5f * G.x, 0.5f * G.y, 0.5f * G.z, 0.5f * G.w);
-        } else if (warp < 4) {
-            float* dst = warp == 1 ? sK : warp == 2 ? sQ : sRY;
+        } else if (warp < 3) {
+            float* dst = warp == 1 ? sK : sQ;
 #pragma unroll
             for (int i = 0; i < kBC; ++i) st4(dst, i, 4 * lane, zero_if(i >= nt, in_row(warp, i)));
-        } else if (warp < 6) {
+        } else if (warp == 4 || warp == 5) {
             const int r0 = (warp - 4) * 8;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -787,7 +825,7 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
                 float* dst = (tile == 0 ? sT : tile == 1 ? sP : sAt) + r * kSmallLd + cc;
                 *reinterpret_cast<float4*>(dst) = tile == 2 ? rf[m] : tf32r4(rf[m]);
             }
-        } else if (lane < kBC) {
+        } else if (warp == 7 && lane < kBC) {
             sBeta[lane] = rbeta;
         }
         __syncthreads();
@@ -820,31 +858,15 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
             return;
         }
         // ---- phase 2 (value channels w16.. of this warp) ----
-        // R = V - K_f S   (token rows, value columns)
+        // R = V - K_f S (token rows, value columns) arrived from the forward pass in sRY
         float R[2][4];
-        {
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                const float2 lo = *reinterpret_cast<const float2*>(sRY + swz(g, w16 + 8 * jj + 2 * t));
-                const float2 hi = *reinterpret_cast<const float2*>(sRY + swz(g + 8, w16 + 8 * jj + 2 * t));
-                R[jj][0] = lo.x; R[jj][1] = lo.y; R[jj][2] = hi.x; R[jj][3] = hi.y;
-            }
-#pragma unroll
-            for (int kk = 0; kk < kDim / 8; ++kk) {
-                uint32_t a[4];
-                lda_mk(sKf, 0, 8 * kk, g, t, a);
-                a[0] = neg(a[0]); a[1] = neg(a[1]); a[2] = neg(a[2]); a[3] = neg(a[3]);
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    uint32_t b[2];
-                    ldb_nk(sS, w16 + 8 * jj, 8 * kk, g, t, b);
-                    mma8(R[jj], a, b);
-                }
-            }
+        for (int jj = 0; jj < 2; ++jj) {
+            const float2 lo = *reinterpret_cast<const float2*>(sRY + swz(g, w16 + 8 * jj + 2 * t));
+            const float2 hi = *reinterpret_cast<const float2*>(sRY + swz(g + 8, w16 + 8 * jj + 2 * t));
+            R[jj][0] = lo.x; R[jj][1] = lo.y; R[jj][2] = hi.x; R[jj][3] = hi.y;
         }
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) st_c(sRY, 0, w16 + 8 * jj, g, t, R[jj]);
-        __syncthreads();  // sTB complete; R of every warp in sRY (only own columns are read)
+        __syncthreads();  // sTB complete
         // U = T diag(beta) R
         {
             float U[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -1164,7 +1186,7 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
                     *reinterpret_cast<float2*>(p.dk + o) = make_float2(KP[jj][2], KP[jj][3]);
                     *reinterpret_cast<float2*>(p.dq + o) = make_float2(QS[jj][2], QS[jj][3]);
                 }
-                st_c(sRY, 0, w16 + 8 * jj, g, t, YS[jj]);   // dG; dY is no longer read
+                st_c(sDU, 0, w16 + 8 * jj, g, t, YS[jj]);   // dG, in this warp's own columns
             }
             __syncwarp();
             {
@@ -1176,7 +1198,7 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
                 float acc = hi ? sCX[col] + sA[col] * sES[col] : 0.f;
 #pragma unroll
                 for (int j = 7; j >= 0; --j) {
-                    acc += sRY[swz(8 * hi + j, col)];
+                    acc += sDU[swz(8 * hi + j, col)];
                     part[j] = acc;
                 }
                 const float upper = __shfl_sync(0xffffffffu, acc, lane | 16);
@@ -1239,7 +1261,7 @@ bool make_box_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, si
 
 size_t backward_workspace_floats(int num_seqs, int heads, int64_t chunks) {
     const size_t idx_floats = ((size_t)num_seqs + 2 + 63) / 64 * 64;
-    return idx_floats + (size_t)chunks * heads * (3 * kBC * kBC + kState);
+    return idx_floats + (size_t)chunks * heads * (3 * kBC * kBC + kSlot);
 }
 
 int64_t backward_chunks(const int32_t* host_seqlens, int num_seqs) {

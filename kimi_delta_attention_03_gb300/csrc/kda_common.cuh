@@ -193,7 +193,7 @@ cudaError_t launch_prologue(int64_t rows, int heads, const void* q_raw, const vo
 // Gradients of the recurrence, chunked by 16 tokens.  `chunks` is the host's chunk total (sum over
 // the sequences of ceil(len / 16)); work holds backward_workspace_floats(num_seqs, heads, chunks)
 // floats: the chunk offsets of the sequences and a stop flag, then per (chunk, head) the 16 x 16
-// tiles T, P and At, then per (chunk, head) the state at the chunk's start.
+// tiles T, P and At, then per (chunk, head) the state at the chunk's start and R = V - K_f S.
 size_t backward_workspace_floats(int num_seqs, int heads, int64_t chunks);
 int64_t backward_chunks(const int32_t* host_seqlens, int num_seqs);
 cudaError_t launch_backward(int dtype, int num_seqs, int heads, const void* q, const void* k,

@@ -291,12 +291,12 @@ def test_backward_host_checks(lib):
     lens, H = [0, 5, 33, 2048], 3
     desc = binding.make_desc(lens, H, torch.bfloat16)
     # the sequences' chunk offsets and a stop flag (rounded up to 64 entries), then per 16-token
-    # chunk and head the tiles T, P, At (16 x 16 each) and the chunk's start state (128 x 128),
-    # all 4-byte words
+    # chunk and head the tiles T, P, At (16 x 16 each), the chunk's start state (128 x 128) and
+    # its R = V - K_f S (16 x 128), all 4-byte words
     chunks = sum((n + 15) // 16 for n in lens)
     index = ((len(lens) + 2 + 63) // 64) * 64
     need = lib.kda_bwd_workspace_bytes(ctypes.byref(desc))
-    assert need == (index + chunks * H * (3 * 16 * 16 + 128 * 128)) * 4
+    assert need == (index + chunks * H * (3 * 16 * 16 + 128 * 128 + 16 * 128)) * 4
     assert lib.kda_bwd_workspace_bytes(None) == 0
     ins = [P(0x1000 + 0x100 * i) for i in range(5)]          # q, k, v, log_alpha, beta
     cu, d_out = P(0x2000), P(0x2100)
