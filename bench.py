@@ -550,9 +550,9 @@ def main():
         bstep()
         ms_b = max_over_ranks(time_device(bstep, 5, stream), world)
         # dense tf32 products per 16-token chunk and head, in multiply-adds: prep 2 x 16*16*128;
-        # forward chain 2 x 16*128*128 + 16*16*128; reverse 7 x 16*128*128 + 10 x 16*16*128
+        # forward chain 2 x 16*128*128 + 16*16*128; reverse 6 x 16*128*128 + 10 x 16*16*128
         chunks = sum((n + 15) // 16 for n in x["seqlens"])
-        flops_b = 2.0 * chunks * H * (9 * 16 * 128 * 128 + 13 * 16 * 16 * 128)
+        flops_b = 2.0 * chunks * H * (8 * 16 * 128 * 128 + 13 * 16 * 16 * 128)
         extra["backward_4x8k" if not small else "backward_small"] = {
             "workload": w.name + ": gradients of q, k, v, log alpha, beta and the initial state",
             "tokens": T, "ms_per_step": ms_b, "steps": 5,
