@@ -66,12 +66,13 @@ def test_backward_long_sequence():
         assert_close(name, g.cpu().numpy(), r)
 
 
-def test_backward_bounded_gate_range():
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_backward_bounded_gate_range(dtype):
     """log alpha = -5 sigmoid(2z): the lower-bound gate of "How KDA updates its state" over its
     whole range (down to -5 per token), ragged lengths, with an initial state and a final-state
-    gradient."""
+    gradient; bf16 and fp32 inputs."""
     lens, H = [300, 7, 129], 2
-    x = synth.make_inputs(lens, H, torch.bfloat16, seed=77, device=DEV, bounded_gate=-5.0)
+    x = synth.make_inputs(lens, H, dtype, seed=77, device=DEV, bounded_gate=-5.0)
     gen = torch.Generator(device=DEV).manual_seed(78)
     d_out = torch.randn(sum(lens), H, 128, generator=gen, device=DEV)
     d_state = torch.randn(len(lens), H, 128, 128, generator=gen, device=DEV) * 0.1
