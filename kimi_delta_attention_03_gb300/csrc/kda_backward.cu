@@ -866,7 +866,6 @@ kda_bwd_reverse_kernel(const __grid_constant__ BwdMaps maps, const BwdArgs<TIn> 
             const float2 hi = *reinterpret_cast<const float2*>(sRY + swz(g + 8, w16 + 8 * jj + 2 * t));
             R[jj][0] = lo.x; R[jj][1] = lo.y; R[jj][2] = hi.x; R[jj][3] = hi.y;
         }
-        __syncthreads();  // sTB complete
         // U = T diag(beta) R
         {
             float U[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
