@@ -87,6 +87,30 @@ def test_backward_bounded_gate_range(dtype):
         assert_close(name, g.cpu().numpy(), r)
 
 
+def test_backward_decay_near_the_chunk_range_limit():
+    """log alpha = -9.5 in a few channels: each 16-token chunk decays by 152 there, just inside
+    the factors' limit of 160 (mean -10 per token), so the mid-chunk reference puts factors near
+    e^(+-76) in fp32; compared with the oracle."""
+    lens, H = [200, 45], 1
+    x = synth.make_inputs(lens, H, torch.bfloat16, seed=91, device=DEV)
+    la = x["log_alpha"].clone()
+    la[:, :, 3] = -9.5
+    la[:, :, 77] = -9.5
+    la[:, :, 100] = -9.5
+    gen = torch.Generator(device=DEV).manual_seed(92)
+    d_out = torch.randn(sum(lens), H, 128, generator=gen, device=DEV)
+    d_state = torch.randn(len(lens), H, 128, 128, generator=gen, device=DEV) * 0.1
+    got = kda().bwd(x["q"], x["k"], x["v"], la, x["beta"], x["cu_seqlens"], x["seqlens"], d_out,
+                    init_state=x["init_state"], d_state=d_state)
+    torch.cuda.synchronize()
+    assert kda().read_device_status() == 0
+    ref = oracle.recurrence_backward(
+        x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), la.cpu(), x["beta"].cpu(),
+        x["cu_seqlens"].cpu(), d_out.cpu(), state_in=x["init_state"].cpu(), d_state=d_state.cpu())
+    for name, g, r in zip(NAMES, got, ref):
+        assert_close(name, g.cpu().numpy(), r)
+
+
 def test_backward_decay_beyond_the_chunk_range_is_reported():
     """A 16-token chunk whose decay passes 160 in a channel (here -12 per token) leaves the
     factors' exponent range: KDA_ERR_DECAY_RANGE, and the next call is still correct."""
